@@ -1,0 +1,291 @@
+"""Plain, slow, float64 CPU statement of the single-GPU MoE layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+module; only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` use it.  It shares no code with the CUDA path.
+
+Sources.  Page "DeepSeek V4 MegaMoE Kernel 深度解析" (beaiera.top), section
+"经典 MoE 的计算过程" (steps 第一步 routing, 第三步 expert SwiGLU FFN,
+第四步 combine, and the 完整形状链 shape chain) and its MegaMoE sections
+二 (fused stages: FP8 x FP4 block-scaled GEMMs, SwiGLU + amax -> UE8M0 ->
+FP8 requant, BF16 L2 output, float32 combine).  Page "INT8 高吞吐/低延迟 EP
+代码梳理" (hncyxsy.com) sections 9.2-9.6 and 10 (topk_ids, inv_perm, the
+expert-contiguous permute with per-expert alignment, M_sum, the weighted
+gather, M_sum_upper).  The CUDA tag page's teaser table names
+"Fused TopK Bias Routing: sqrt(softplus), e_score_correction_bias".
+
+Readings where the pages are silent (each also listed in the design doc):
+* sqrt(softplus)(x) = sqrt(ln(1 + e^x)).
+* e_score_correction_bias is added to the scores for the top-K *selection*
+  only; the weights use the unbiased scores.
+* top-K ties go to the lower expert id; topk_ids[t, :] is ordered by
+  descending key (ties by lower id).
+* weights are renormalised to sum to 1 when ``renormalize`` is set (all
+  workloads); no routed scaling factor, no group-limited routing.
+* activation FP8 groups are 128 wide along H (the page's MegaMoE input
+  quantiser uses 32); the same rule requantises the SwiGLU output per 128
+  along I.  The UE8M0 exponent is the smallest e with amax <= 448 * 2**e.
+* topk_weight is applied in the final gather (classic path), not in the L1
+  epilogue.
+* within one expert, rows are ordered by ascending token index (the printed
+  permute example); ``sorted_token_ids`` holds the flat index t*K + k
+  (recovered by ``// top_k`` on the page) and T*K on padding rows;
+  ``expert_ids`` holds -1 on padding rows and on rows [M_sum, U).
+* the L2 result is rounded to bfloat16 per (token, expert) row before the
+  weighted sum, which is accumulated exactly (float64 here) and rounded
+  once to bfloat16.
+"""
+import math
+from typing import Callable, Dict, Optional
+
+import numpy as np
+
+from .formats import (bf16_to_f64, decode_e2m1_packed, decode_e4m3, decode_ue8m0,
+                      encode_e4m3_rne, round_bf16_rne, ue8m0_exponent_for_amax)
+
+ACT_GROUP = 128        # activation scale group along the reduction dimension
+MX_GROUP = 32          # MXFP4 weight scale group
+NV_GROUP = 16          # NVFP4 weight scale group
+
+
+# ----------------------------------------------------------------------------
+# Routing (MegaMoE page, 第一步：路由; CUDA tag page teaser: Fused TopK Bias Routing)
+
+def gate_logits(hidden_bits: np.ndarray, w_gate: np.ndarray,
+                gate_bias: Optional[np.ndarray] = None) -> np.ndarray:
+    """gate = hidden_states @ W_gate^T (+ per-expert bias), in float64.  [T,H] x [E,H] -> [T,E]."""
+    x = bf16_to_f64(hidden_bits)
+    w = np.asarray(w_gate, dtype=np.float32).astype(np.float64)
+    logits = x @ w.T
+    if gate_bias is not None:
+        logits = logits + np.asarray(gate_bias, dtype=np.float32).astype(np.float64)[None, :]
+    return logits
+
+
+def softmax(logits: np.ndarray) -> np.ndarray:
+    m = logits.max(axis=1, keepdims=True)
+    p = np.exp(logits - m)
+    return p / p.sum(axis=1, keepdims=True)
+
+
+def sqrt_softplus(logits: np.ndarray) -> np.ndarray:
+    """sqrt(ln(1 + e^x)), with softplus written in its overflow-free form max(x,0) + ln(1 + e^-|x|)."""
+    sp = np.maximum(logits, 0.0) + np.log1p(np.exp(-np.abs(logits)))
+    return np.sqrt(sp)
+
+
+def select_topk(keys: np.ndarray, K: int) -> np.ndarray:
+    """Per row, the K largest keys; ties to the lower index; ordered by (key desc, id asc)."""
+    T, E = keys.shape
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    # lexsort: last key is primary.  Primary: -key ascending; secondary: id ascending.
+    order = np.lexsort((ids, -keys), axis=1)
+    return order[:, :K].astype(np.int32)
+
+
+def route(hidden_bits, w_gate, gate_bias, e_score_bias, K: int, score_fn: str,
+          renormalize: bool = True) -> Dict[str, np.ndarray]:
+    """Gate GEMM -> scoring -> biased top-K selection -> weights.
+
+    Returns logits [T,E] f64, scores [T,E] f64, keys [T,E] f64,
+    topk_ids [T,K] int32, topk_w [T,K] float64.
+    """
+    logits = gate_logits(hidden_bits, w_gate, gate_bias)
+    if score_fn == "softmax":
+        scores = softmax(logits)
+    elif score_fn == "sqrt_softplus":
+        scores = sqrt_softplus(logits)
+    else:
+        raise ValueError(score_fn)
+    keys = scores
+    if e_score_bias is not None:
+        keys = scores + np.asarray(e_score_bias, dtype=np.float32).astype(np.float64)[None, :]
+    ids = select_topk(keys, K)
+    sel = np.take_along_axis(scores, ids.astype(np.int64), axis=1)
+    w = sel / sel.sum(axis=1, keepdims=True) if renormalize else sel
+    return dict(logits=logits, scores=scores, keys=keys, topk_ids=ids, topk_w=w)
+
+
+# ----------------------------------------------------------------------------
+# FP8 quantisation with power-of-two (UE8M0) scales, one scale per 128 along
+# the reduction dimension (MegaMoE page, 二、阶段 3 "amax -> UE8M0 scale ->
+# FP8 E4M3"; 三、数据流图 prepare_megamoe_inputs).
+
+def quantize_fp8_groups(x: np.ndarray, group: int = ACT_GROUP):
+    """x [R, C] float64 (C multiple of group) -> (codes [R, C] uint8, sf [R, C/group] uint8)."""
+    R, C = x.shape
+    assert C % group == 0
+    G = C // group
+    xg = x.reshape(R, G, group)
+    amax = np.abs(xg).max(axis=2)
+    e = np.vectorize(ue8m0_exponent_for_amax, otypes=[np.int64])(amax) if amax.size else np.zeros((R, G), np.int64)
+    scaled = xg * np.ldexp(1.0, -e)[:, :, None]          # exact power-of-two scaling
+    codes = encode_e4m3_rne(scaled).reshape(R, C)
+    sf = (e + 127).astype(np.uint8)
+    return codes, sf
+
+
+def act_quant(hidden_bits: np.ndarray):
+    """hidden bf16 [T,H] -> x_q [T,H] E4M3 codes, x_sf [T,H/128] UE8M0."""
+    return quantize_fp8_groups(bf16_to_f64(hidden_bits), ACT_GROUP)
+
+
+def dequant_fp8_groups(codes: np.ndarray, sf: np.ndarray, group: int = ACT_GROUP) -> np.ndarray:
+    R, C = codes.shape
+    v = decode_e4m3(codes).reshape(R, C // group, group)
+    return (v * decode_ue8m0(sf)[:, :, None]).reshape(R, C)
+
+
+# ----------------------------------------------------------------------------
+# Weight formats (CUDA tag page teaser: MXFP4 vs NVFP4; MegaMoE page 五 item 5)
+
+def dequant_mxfp4(q: np.ndarray, sf: np.ndarray) -> np.ndarray:
+    """q [N, Kd/2] packed E2M1, sf [N, Kd/32] UE8M0 -> [N, Kd] float64."""
+    w = decode_e2m1_packed(q)
+    N, Kd = w.shape
+    return (w.reshape(N, Kd // MX_GROUP, MX_GROUP) * decode_ue8m0(sf)[:, :, None]).reshape(N, Kd)
+
+
+def dequant_nvfp4(q: np.ndarray, sf: np.ndarray, tscale: float) -> np.ndarray:
+    """q [N, Kd/2] packed E2M1, sf [N, Kd/16] E4M3, per-matrix fp32 tscale -> [N, Kd] float64."""
+    w = decode_e2m1_packed(q)
+    N, Kd = w.shape
+    s = decode_e4m3(sf) * float(np.float32(tscale))
+    return (w.reshape(N, Kd // NV_GROUP, NV_GROUP) * s[:, :, None]).reshape(N, Kd)
+
+
+def dequant_weight(q, sf, tscale, fmt: str) -> np.ndarray:
+    if fmt == "mxfp4":
+        return dequant_mxfp4(q, sf)
+    if fmt == "nvfp4":
+        return dequant_nvfp4(q, sf, tscale)
+    raise ValueError(fmt)
+
+
+# ----------------------------------------------------------------------------
+# Permute (hncyxsy.com note, §9.3-9.4 and §10; MegaMoE page 路径 A/B/C)
+
+def msum_upper(T: int, K: int, E: int, align: int) -> int:
+    """M_sum_upper = M * topk + num_experts * (alignment - 1) (note §10)."""
+    return T * K + E * (align - 1)
+
+
+def permute(topk_ids: np.ndarray, E: int, align: int) -> Dict[str, np.ndarray]:
+    """Expert-contiguous layout with each expert's segment padded to a multiple of ``align``.
+
+    Each (token t, slot k) occupies one row; the rows of expert e start at
+    seg_e = sum_{e'<e} ceil(cnt_e'/align)*align and are ordered by ascending
+    flat index t*K + k (= ascending t, since a token's K ids are distinct).
+    """
+    T, K = topk_ids.shape
+    flat = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    if flat.size and (flat.min() < 0 or flat.max() >= E):
+        raise ValueError("expert id out of range")
+    cnt = np.bincount(flat, minlength=E).astype(np.int64)
+    aligned = (cnt + align - 1) // align * align
+    seg = np.concatenate([[0], np.cumsum(aligned)[:-1]]).astype(np.int64)
+    m_sum = int(aligned.sum())
+    U = msum_upper(T, K, E, align)
+    order = np.argsort(flat, kind="stable")                 # grouped by expert, ascending flat index
+    first = np.concatenate([[0], np.cumsum(cnt)[:-1]])      # position of each expert's first pair in ``order``
+    rank = np.empty(flat.size, dtype=np.int64)
+    rank[order] = np.arange(flat.size) - first[flat[order]]
+    inv = seg[flat] + rank
+    sorted_ids = np.full(U, T * K, dtype=np.int32)
+    expert_ids = np.full(U, -1, dtype=np.int32)
+    sorted_ids[inv] = np.arange(flat.size, dtype=np.int32)
+    expert_ids[inv] = flat.astype(np.int32)
+    return dict(sorted_token_ids=sorted_ids, expert_ids=expert_ids,
+                inv_perm=inv.reshape(T, K).astype(np.int32), m_sum=m_sum,
+                expert_counts=cnt.astype(np.int32), seg_start=seg.astype(np.int64), U=U)
+
+
+# ----------------------------------------------------------------------------
+# Expert SwiGLU FFN (MegaMoE page, 第三步 and 二、阶段 2-4)
+
+def silu(x: np.ndarray) -> np.ndarray:
+    return x / (1.0 + np.exp(-x))
+
+
+def expert_l1_swiglu(x_deq: np.ndarray, w13_deq: np.ndarray, I: int):
+    """gate_up = x @ W13^T; gate = first I, up = last I; h = silu(gate) * up; FP8 requant per 128.
+
+    Returns (h float64 [R, I], h_q uint8 [R, I], h_sf uint8 [R, I/128]).
+    """
+    gu = x_deq @ w13_deq.T
+    g, u = gu[:, :I], gu[:, I:]
+    h = silu(g) * u
+    h_q, h_sf = quantize_fp8_groups(h, ACT_GROUP)
+    return h, h_q, h_sf
+
+
+def expert_l2(h_q: np.ndarray, h_sf: np.ndarray, w2_deq: np.ndarray) -> np.ndarray:
+    """y = h @ W2^T from the requantised h, rounded to bfloat16 bits (L2 output is BF16)."""
+    h = dequant_fp8_groups(h_q, h_sf, ACT_GROUP)
+    return round_bf16_rne(h @ w2_deq.T)
+
+
+def unpermute_reduce(y_rows_bits: np.ndarray, inv_perm: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
+    """out[t] = bf16( sum_k topk_w[t,k] * y[inv_perm[t,k]] ), summed exactly in float64 (note §9.6)."""
+    y = bf16_to_f64(y_rows_bits)
+    T, K = inv_perm.shape
+    acc = np.zeros((T, y.shape[1]), dtype=np.float64)
+    for k in range(K):
+        acc += np.asarray(topk_w[:, k], dtype=np.float64)[:, None] * y[inv_perm[:, k]]
+    return round_bf16_rne(acc)
+
+
+# ----------------------------------------------------------------------------
+# Whole layer
+
+WeightProvider = Callable[[int], dict]
+"""expert e -> dict(w13_q, w13_sf, w13_ts, w2_q, w2_sf, w2_ts) in the logical layouts."""
+
+
+def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
+            score_fn: str, renormalize: bool = True, tokens=None,
+            topk_w_dtype=np.float64) -> Dict[str, object]:
+    """Route -> act quant -> permute -> per-expert L1+SwiGLU+requant -> L2 -> weighted reduce.
+
+    ``tokens``: optional subset of token indices; only the (token, expert)
+    rows those tokens need are computed and ``out`` holds only their rows
+    (in the order given).  Routing, quantisation and the permute always run
+    on all tokens, since the permute layout depends on every token.
+    ``topk_w_dtype``: precision in which the routing weights enter the final
+    sum (float64 by default; float32 mimics a kernel that stores them as fp32).
+    """
+    hidden = inp["hidden"]
+    T, H = hidden.shape
+    E = inp["w_gate"].shape[0]
+    r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
+    x_q, x_sf = act_quant(hidden)
+    p = permute(r["topk_ids"], E, align)
+    tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    need = {}
+    for t in tok:
+        for k in range(K):
+            need.setdefault(int(r["topk_ids"][t, k]), []).append((int(t), k))
+    I = None
+    y_rows = {}
+    h_rows = {}
+    for e, pairs in sorted(need.items()):
+        w = weights(e)
+        w13 = dequant_weight(w["w13_q"], w["w13_sf"], w.get("w13_ts"), fmt)
+        w2 = dequant_weight(w["w2_q"], w["w2_sf"], w.get("w2_ts"), fmt)
+        I = w13.shape[0] // 2
+        ts = sorted(set(t for t, _ in pairs))
+        xd = dequant_fp8_groups(x_q[ts], x_sf[ts])
+        _, hq, hsf = expert_l1_swiglu(xd, w13, I)
+        y = expert_l2(hq, hsf, w2)
+        for j, t in enumerate(ts):
+            y_rows[(t, e)] = y[j]
+            h_rows[(t, e)] = (hq[j], hsf[j])
+    out = np.zeros((len(tok), H), dtype=np.uint16)
+    wts = r["topk_w"].astype(topk_w_dtype).astype(np.float64)
+    for i, t in enumerate(tok):
+        acc = np.zeros(H, dtype=np.float64)
+        for k in range(K):
+            acc += wts[t, k] * bf16_to_f64(y_rows[(int(t), int(r["topk_ids"][t, k]))])
+        out[i] = round_bf16_rne(acc)
+    return dict(route=r, x_q=x_q, x_sf=x_sf, perm=p, out=out, tokens=tok,
+                y_rows=y_rows, h_rows=h_rows)
