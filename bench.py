@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE layer forward: tokens/s and fraction of the binding roofline.
+
+One step = one whole forward of the layer (route -> permute -> L1+SwiGLU -> L2 -> reduce) on
+one batch of synthetic, seeded inputs already resident in HBM.  Default workload: the pages'
+decode shape (T=8, H=7168, I=2048, E=256, K=6, MXFP4 weights), which is weight-bandwidth bound.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent replica (the
+layer is replicated per GPU, no collective on the data path); value = tokens of all ranks /
+max over ranks of the step time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+LAUNCHES_PER_STEP = 7          # gate GEMM, top-K/act-quant, permute, row copy, L1, L2, reduce
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="decode", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    return p.parse_args()
+
+
+def world():
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} K={w.K} align={w.align} "
+                        f"{w.score_fn} {w.fmt.upper()} weights, FP8 E4M3 activations (UE8M0/128)",
+            "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K, "align": w.align, "weights": w.fmt}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def traffic_record(kernel_file, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+        with open(kernel_file, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        r = recs.get(workload)
+        if r and r.get("source_sha") == sha:
+            return r["bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------ CPU oracle
+
+def oracle_tokens_per_s(w, inp, stack, budget_s, max_tokens=None):
+    """Times the float64 oracle on whole tokens of the workload until the budget is spent."""
+    from oracle import moe as O
+    prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
+    done, t0 = 0, time.perf_counter()
+    order = list(range(w.T))
+    while done < len(order) and (max_tokens is None or done < max_tokens):
+        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[order[done]])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def run_reference(args, w):
+    """The oracle as the reference arm: each step is one token of the workload on the host cores."""
+    W, rank, _ = world()
+    if rank != 0:
+        return
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    from oracle import moe as O
+    prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
+    for i in range(args.warmup):
+        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
+    times = []
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = 1e3 / ms
+    cores = os.cpu_count()
+    sample = f"1 token of the {w.name} workload per step (routing of all {w.T} tokens + that token's {w.K} experts)"
+    line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------ GPU arm
+
+def algorithmic_bytes(w, n_touched):
+    """Bytes the method must move per launch of each stage (padding and untouched experts excluded)."""
+    TK = w.T * w.K
+    if w.fmt == "mxfp4":
+        w13 = n_touched * (2 * w.I * w.H // 2 + 2 * w.I * w.H // 32)
+        w2 = n_touched * (w.H * w.I // 2 + w.H * w.I // 32)
+    else:
+        w13 = n_touched * (2 * w.I * w.H // 2 + 2 * w.I * w.H // 16 + 4)
+        w2 = n_touched * (w.H * w.I // 2 + w.H * w.I // 16 + 4)
+    l1 = w13 + TK * (w.H + w.H // 128) + TK * (w.I + w.I // 128)
+    l2 = w2 + TK * (w.I + w.I // 128) + TK * w.H * 2
+    return {"l1": l1, "l2": l2,
+            "layer": w13 + w2 + 4 * w.E * w.H + 2 * w.T * w.H * 2}
+
+
+def run_ours(args, w):
+    import torch
+    import moe_expert_ffn_sqrt_gb300 as M
+
+    W, rank, local = world()
+    if W > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M.lib()
+
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]), w.fmt)
+    w2 = M.Weight(d(stack["w2_q"]), d(stack["w2_sf"]), None if stack["w2_ts"] is None else d(stack["w2_ts"]), w.fmt)
+    T = w.T
+    hidden_host = torch.from_numpy(inp["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hidden = hidden_host.to(dev)
+    w_gate = d(inp["w_gate"])
+    gate_bias = None if inp["gate_bias"] is None else d(inp["gate_bias"])
+    e_bias = None if inp["e_score_bias"] is None else d(inp["e_score_bias"])
+    ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align, device=dev)
+    out = torch.empty(T, w.H, dtype=torch.bfloat16, device=dev)
+    out_host = torch.empty(T, w.H, dtype=torch.bfloat16).pin_memory()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)     # > L2 (126 MB)
+
+    def step():
+        M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out, ws)
+
+    def barrier():
+        if W > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    st = M.get_error(ws)
+    if st != M.OK:
+        raise RuntimeError(f"device status after warm-up: {M.status_str(st)}")
+
+    # ---- timed region: one forward per step, L2 flushed between steps (outside the events)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    barrier()
+    clk = clocks.stop()
+    times = [a.elapsed_time(b) for a, b in ev]
+    ms = statistics.mean(times)
+    if W > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    st = M.get_error(ws)
+    if st != M.OK:
+        raise RuntimeError(f"device status after timed steps: {M.status_str(st)}")
+    value = W * T / (ms / 1e3)
+
+    # ---- per-kernel durations: the same path called stage by stage with events in between
+    U = M.msum_upper(T, w.K, w.E, w.align)
+    ids = torch.empty(T, w.K, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, w.K, dtype=torch.float32, device=dev)
+    xq = torch.empty(T, w.H, dtype=torch.uint8, device=dev)
+    xsf = torch.empty(T, w.H // 128, dtype=torch.uint8, device=dev)
+    srt = torch.empty(U, dtype=torch.int32, device=dev)
+    eids = torch.empty(U, dtype=torch.int32, device=dev)
+    inv = torch.empty(T, w.K, dtype=torch.int32, device=dev)
+    msum = torch.empty(1, dtype=torch.int32, device=dev)
+    cnt = torch.empty(w.E, dtype=torch.int32, device=dev)
+    xp = torch.empty(U, w.H, dtype=torch.uint8, device=dev)
+    xpsf = torch.empty(M.act_sf_tiled_bytes(U, w.H // 128, w.align), dtype=torch.uint8, device=dev)
+    hq = torch.empty(U, w.I, dtype=torch.uint8, device=dev)
+    hsf = torch.empty(M.act_sf_tiled_bytes(U, w.I // 128, w.align), dtype=torch.uint8, device=dev)
+    y = torch.empty(U, w.H, dtype=torch.bfloat16, device=dev)
+    stages = ["route", "permute", "l1", "l2", "reduce"]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e = sev[i]
+        e[0].record()
+        M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
+        e[1].record()
+        M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
+                  x_perm_sf=xpsf)
+        e[2].record()
+        M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
+        e[3].record()
+        M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w2, y, ws)
+        e[4].record()
+        M.unpermute_reduce(y, inv, tw, out)
+        e[5].record()
+    barrier()
+    stage_ms = {s: statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(K)) for j, s in enumerate(stages)}
+    n_touched = int((cnt.cpu() > 0).sum().item())
+    ab = algorithmic_bytes(w, n_touched)
+    hbm, bf16, peak_src = peaks()
+    top = max(("l1", "l2"), key=lambda s: stage_ms[s])
+    achieved = ab[top] / (stage_ms[top] / 1e3) / 1e9
+    kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc", "gemm.cu")
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": f"{top} grouped GEMM",
+                "algorithmic_bytes": ab[top], "peak_source": f"{peak_src} HBM copy bandwidth",
+                "stage_ms": stage_ms, "experts_touched": n_touched,
+                "layer_frac": ab["layer"] / (ms / 1e3) / 1e9 / hbm}
+
+    # ---- end to end through the public API with host buffers: H2D input, forward, D2H output
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record()
+        hidden.copy_(hidden_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record()
+    barrier()
+    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
+    if W > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": W * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": T * w.H * 2,
+           "d2h_bytes_per_step": T * w.H * 2}
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if W == 1:
+            v, n, dt = oracle_tokens_per_s(w, inp, stack, args.cpu_seconds)
+            cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                   "sample": f"{n} token(s) of the {w.name} workload (routing of all {w.T} tokens each time), "
+                             f"{dt:.1f} s, numpy float64"}
+        cfg = workload_config(w)
+        cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
+        cfg["parallelism"] = f"replicas x{W}"
+        line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "fp8xfp4 (fp32 accumulate)", "data": "synthetic (seeded)",
+                "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clk}
+        print(json.dumps(line), flush=True)
+    if W > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def main():
+    args = parse_args()
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,209 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) single-GPU Mixture-of-Experts layer forward.
+ *
+ * The layer (page "DeepSeek V4 MegaMoE Kernel 深度解析", section 经典 MoE 的计算过程):
+ *   gate GEMM -> score (softmax | sqrt(softplus)) -> top-K with e_score_correction_bias
+ *   -> expert-contiguous permute padded per expert to `align` rows
+ *   -> L1 grouped GEMM against W13 [2I,H] + SwiGLU + FP8 requant
+ *   -> L2 grouped GEMM against W2 [H,I] (bf16 out)
+ *   -> topk-weighted unpermute-reduce back to [T,H] (bf16).
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are DEVICE pointers owned by the caller, contiguous, row-major,
+ *     unless a comment says "host".  Nothing here allocates, frees or synchronises the
+ *     device, except moe_get_error (which synchronises the given stream).
+ *   - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream) and runs asynchronously.  No call reads a device value back to the host:
+ *     M_sum stays in device memory and buffers are sized by moe_msum_upper().
+ *   - bf16 values are passed as their uint16 bit patterns.  E4M3 / E2M1 / UE8M0 values are
+ *     passed as their codes (uint8; E2M1 two per byte, element 2j in the low nibble).
+ *   - Host-side argument errors are returned at once and nothing is launched.  Errors the
+ *     device detects (an expert id outside [0,E) in topk_ids, a bounded wait that expired)
+ *     are recorded in a status word inside the workspace; moe_get_error reads and clears it.
+ *   - Calls are stateless and reentrant; calls that share a workspace must not overlap.
+ *   - H and I must be multiples of 128 (the pages state this limit for the fused kernel);
+ *     K <= E; align is a power of two in [1, 256]; all pointers 16-byte aligned
+ *     (W q pointers 32-byte aligned).
+ *
+ * Scale layouts used between the calls (documented so callers can interpret them):
+ *   - Activation scales "tiled" (x_perm_sf, h_sf): one UE8M0 byte per (row r, 128-column
+ *     slab s) of a permuted activation matrix with `rows` rows and `slabs` slabs.  With
+ *     Bt = moe_act_sf_block_rows(align) (the grouped GEMMs' row-block size: the largest power
+ *     of two <= align, clamped to [16, 128]), nb = ceil(rows/Bt) + 1 and CB = 256 for Bt = 16,
+ *     else 512, the byte of (r, s) is at
+ *       ((s/4)*nb + r/Bt)*CB + ((r%Bt)%32)*16 + ((r%Bt)/32)*4 + (s%4)
+ *     so each (row block, 4 slabs) is one contiguous chunk that the GEMM copies into tensor
+ *     memory as is.  Total moe_act_sf_tiled_bytes(rows, slabs, align); the _host helpers
+ *     convert to and from the plain [rows, slabs] layout.
+ *   - Weight scales "packed": produced once per weight tensor by moe_pack_weight_scales().
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or enum */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but not supported (e.g. E too large for the permute kernel) */
+  MOE_ERR_WORKSPACE = 3,     /* ws NULL or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE_INDEX = 5,  /* device saw an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 6,       /* a device-side bounded wait expired */
+  MOE_ERR_DEVICE_CHECK = 7   /* a kernel's own bounds / alignment check failed; the access was skipped */
+} moe_status;
+
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score_fn;
+
+/* Weight formats (CUDA tag page teaser: MXFP4 vs NVFP4, chosen by moe_quant_algo).
+ *   MXFP4: E2M1 codes + one UE8M0 scale per 32 along the reduction dim.
+ *   NVFP4: E2M1 codes + one E4M3 scale per 16 along the reduction dim + one fp32 scale per
+ *          expert matrix. */
+typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+
+/* One stacked expert weight tensor with logical shape [E, N, Kd] (N output rows, Kd the
+ * reduction dim).  W13: N = 2I, Kd = H, rows 0..I-1 are the gate projection W1 and rows
+ * I..2I-1 the up projection W3 (MegaMoE page, 第三步).  W2: N = H, Kd = I. */
+typedef struct {
+  const uint8_t* q;      /* [E, N, Kd/2] packed E2M1 codes (32-byte aligned)                 */
+  const uint8_t* sf;     /* scales in the packed layout written by moe_pack_weight_scales   */
+  const float* tscale;   /* NVFP4: [E] fp32 per-matrix scale; MXFP4: NULL                    */
+  moe_wfmt fmt;
+} moe_weight;
+
+/* --------------------------------------------------------------------------------------
+ * Sizes and host-side helpers (no device work).
+ * ------------------------------------------------------------------------------------ */
+
+/* M_sum_upper = T*K + E*(align-1): the most rows the aligned expert-contiguous layout can
+ * need (note "INT8 高吞吐/低延迟 EP 代码梳理", §10).  Every [U, ...] buffer below has U rows. */
+size_t moe_msum_upper(int T, int K, int E, int align);
+
+/* Rows per block of the tiled activation-scale layout for a permute alignment `align`. */
+int moe_act_sf_block_rows(int align);
+
+/* Bytes of a "tiled" activation-scale buffer for an activation with `rows` rows and
+ * `slabs` = columns/128 slabs, for permute alignment `align` (layout in the file header). */
+size_t moe_act_sf_tiled_bytes(int rows, int slabs, int align);
+
+/* Host memory: tiled [moe_act_sf_tiled_bytes(rows,slabs,align)] -> plain [rows, slabs]. */
+moe_status moe_act_sf_untile_host(const uint8_t* tiled, int rows, int slabs, int align, uint8_t* out);
+
+/* Host memory: plain [rows, slabs] -> tiled [moe_act_sf_tiled_bytes(rows,slabs,align)]; bytes of
+ * the tiled buffer that no (row, slab) maps to are set to 127 (scale 1.0). */
+moe_status moe_act_sf_tile_host(const uint8_t* plain, int rows, int slabs, int align, uint8_t* tiled);
+
+/* Bytes of the packed scale buffer of a weight tensor [E, N, Kd] in format fmt. */
+size_t moe_weight_sf_packed_bytes(moe_wfmt fmt, int E, int N, int Kd);
+
+/* Rearranges a weight tensor's scales from the logical layout ([E, N, Kd/32] UE8M0 for
+ * MXFP4, [E, N, Kd/16] E4M3 for NVFP4) into the layout the grouped GEMMs stream, so that
+ * each 128-row x 128-deep weight tile's scales are one contiguous block.  Done once per
+ * weight tensor (weights are static).  N and Kd must be multiples of 128. */
+moe_status moe_pack_weight_scales(moe_wfmt fmt, const uint8_t* sf, int E, int N, int Kd,
+                                  uint8_t* sf_packed, void* stream);
+
+/* Bytes of workspace needed by moe_route, moe_permute, the grouped GEMMs and moe_forward
+ * for this problem.  The first 256 bytes hold the device status word.  A workspace must
+ * be zero-filled once before first use (it is then kept consistent by the calls). */
+moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size_t* bytes);
+
+/* --------------------------------------------------------------------------------------
+ * Hot-path calls.
+ * ------------------------------------------------------------------------------------ */
+
+/* Routing and activation quantisation (MegaMoE page 第一步：路由; CUDA tag page teaser
+ * "Fused TopK Bias Routing": sqrt(softplus), e_score_correction_bias).
+ *   hidden       [T, H] bf16
+ *   w_gate       [E, H] fp32;  logits = hidden @ w_gate^T (+ gate_bias[E] if non-NULL)
+ *   e_score_bias [E] fp32 or NULL: added to the scores for top-K selection only
+ *   fn           softmax over E, or sqrt(ln(1 + e^logit)) per expert
+ *   topk_ids     [T, K] int32 out: the K largest (score + e_score_bias), ties to the lower
+ *                expert id, ordered by descending key
+ *   topk_w       [T, K] fp32 out: the selected unbiased scores, divided by their sum when
+ *                renormalize != 0
+ *   logits_out   [T, E] fp32 out or NULL
+ *   x_q, x_sf    [T, H] E4M3 and [T, H/128] UE8M0 out, or both NULL: per 128 columns the
+ *                scale is the smallest power of two 2^e with amax <= 448 * 2^e (e in
+ *                [-127,127], e = 0 when amax = 0) and x_q = RNE_e4m3(x / 2^e).
+ *   ws           workspace (split-K partial sums, status word). */
+moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                     const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
+                     int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
+                     uint8_t* x_q, uint8_t* x_sf, void* ws, size_t ws_bytes, void* stream);
+
+/* Expert-contiguous permute (note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4, §10 and the
+ * m_indices paragraph; MegaMoE page 路径 A moe_align_block_size).
+ * With cnt_e = #(t,k) routed to e and seg_e = sum_{e'<e} round_up(cnt_e', align):
+ *   inv_perm[t,k]          [T, K] out: seg_e + (rank of (t,k) among expert e's pairs in
+ *                          ascending t*K+k order)
+ *   sorted_token_ids[row]  [U] out: t*K + k of the pair on that row, T*K on padding rows
+ *   expert_ids[row]        [U] out: expert of the row, -1 on padding rows and rows >= M_sum
+ *   m_sum                  [1] out (device): sum_e round_up(cnt_e, align)
+ *   expert_counts          [E] out or NULL: cnt_e
+ *   x_q, x_sf, x_perm, x_perm_sf: optional (all NULL or all set): x_perm [U, H] gets row
+ *   x_q[t] on row inv_perm[t,k]; x_perm_sf (tiled for `align`, rows = U, slabs = H/128) its scales.
+ *   Rows of x_perm at padding positions are left unwritten.
+ * An id outside [0, E) records MOE_ERR_DEVICE_INDEX and the outputs are unspecified. */
+moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align,
+                       int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                       int32_t* m_sum, int32_t* expert_counts, const uint8_t* x_q,
+                       const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* L1 grouped GEMM + SwiGLU + FP8 requant (MegaMoE page 二、阶段 2 and 阶段 3).
+ * For every row r < M_sum with e = expert_ids[r] >= 0:
+ *   gu = dequant(x_perm[r]) @ dequant(W13[e])^T   ([2I], fp32 accumulate)
+ *   h  = silu(gu[0:I]) * gu[I:2I]
+ *   h_q[r] / h_sf: h requantised per 128 along I by the rule of moe_route.
+ *   x_perm [U, H] E4M3, x_perm_sf tiled (rows U, slabs H/128); h_q [U, I] E4M3 out,
+ *   h_sf tiled (rows U, slabs I/128) out.  Rows with expert_ids = -1 are unspecified. */
+moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                      const int32_t* expert_ids, const int32_t* m_sum, int T,
+                                      int K, int H, int I, int E, int align, moe_weight w13,
+                                      uint8_t* h_q, uint8_t* h_sf, void* ws, size_t ws_bytes,
+                                      void* stream);
+
+/* L2 grouped GEMM (MegaMoE page 二、阶段 4; L2 results are bf16, 阶段 5).
+ * For every row r < M_sum with e = expert_ids[r] >= 0:
+ *   y_perm[r] = bf16_rne( dequant(h_q[r]) @ dequant(W2[e])^T )   ([H], fp32 accumulate)
+ *   h_q [U, I] E4M3, h_sf tiled (rows U, slabs I/128); y_perm [U, H] bf16 out. */
+moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const int32_t* expert_ids,
+                               const int32_t* m_sum, int T, int K, int H, int I, int E,
+                               int align, moe_weight w2, uint16_t* y_perm, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* Weighted unpermute-reduce (note §9.6 "gather 再讲一遍"; MegaMoE page 阶段 5):
+ *   out[t] = bf16_rne( sum_{k=0}^{K-1} topk_w[t,k] * y_perm[inv_perm[t,k]] ), summed in fp32
+ *   in k order.  y_perm [>= max(inv_perm)+1, H] bf16, inv_perm [T,K], topk_w [T,K] fp32,
+ *   out [T, H] bf16. */
+moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
+                                const float* topk_w, int T, int K, int H, uint16_t* out,
+                                void* stream);
+
+/* The whole layer in one call: route -> permute -> L1 -> L2 -> reduce on `stream`, with all
+ * intermediates in the workspace.  The optional index outputs (any may be NULL) receive the
+ * same values as the individual calls would produce; out [T, H] bf16. */
+moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                       const float* e_score_bias, int T, int H, int I, int E, int K, int align,
+                       moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2,
+                       uint16_t* out, int32_t* topk_ids, float* topk_w,
+                       int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                       int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device status word recorded in `ws` through
+ * *device_status (MOE_OK if none) and clears it.  The return value reports host errors. */
+moe_status moe_get_error(void* ws, void* stream, moe_status* device_status);
+
+/* Static string for a status code. */
+const char* moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,254 @@
+"""Python binding of the GB300 MoE layer library (libmoe.so, C ABI in include/moe.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, checks them, and calls
+the C entry point of the same name on the current CUDA stream.  There is no fallback: if
+libmoe.so is missing or fails to load, importing the compute functions raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_INDEX, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(8)
+SCORE_SOFTMAX, SCORE_SQRT_SOFTPLUS = 0, 1
+W_MXFP4, W_NVFP4 = 0, 1
+SCORE_FNS = {"softmax": SCORE_SOFTMAX, "sqrt_softplus": SCORE_SQRT_SOFTPLUS}
+WFMTS = {"mxfp4": W_MXFP4, "nvfp4": W_NVFP4}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} ({status})")
+
+
+class _Weight(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("tscale", ctypes.c_void_p), ("fmt", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libmoe.so (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} not found: build it with `python -m moe_expert_ffn_sqrt_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, Z, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
+        L.moe_msum_upper.restype = Z
+        L.moe_msum_upper.argtypes = [I, I, I, I]
+        L.moe_act_sf_block_rows.restype = I
+        L.moe_act_sf_block_rows.argtypes = [I]
+        L.moe_act_sf_tiled_bytes.restype = Z
+        L.moe_act_sf_tiled_bytes.argtypes = [I, I, I]
+        L.moe_act_sf_untile_host.restype = S
+        L.moe_act_sf_untile_host.argtypes = [P, I, I, I, P]
+        L.moe_act_sf_tile_host.restype = S
+        L.moe_act_sf_tile_host.argtypes = [P, I, I, I, P]
+        L.moe_weight_sf_packed_bytes.restype = Z
+        L.moe_weight_sf_packed_bytes.argtypes = [I, I, I, I]
+        L.moe_pack_weight_scales.restype = S
+        L.moe_pack_weight_scales.argtypes = [I, P, I, I, I, P, P]
+        L.moe_workspace_size.restype = S
+        L.moe_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
+        L.moe_route.restype = S
+        L.moe_route.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, Z, P]
+        L.moe_permute.restype = S
+        L.moe_permute.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, Z, P]
+        L.moe_grouped_gemm_l1_swiglu.restype = S
+        L.moe_grouped_gemm_l1_swiglu.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
+        L.moe_grouped_gemm_l2.restype = S
+        L.moe_grouped_gemm_l2.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, Z, P]
+        L.moe_unpermute_reduce.restype = S
+        L.moe_unpermute_reduce.argtypes = [P, P, P, I, I, I, P, P]
+        L.moe_forward.restype = S
+        L.moe_forward.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P, Z, P]
+        L.moe_get_error.restype = S
+        L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
+        L.moe_status_str.restype = ctypes.c_char_p
+        L.moe_status_str.argtypes = [I]
+        _lib = L
+    return _lib
+
+
+def status_str(s: int) -> str:
+    return lib().moe_status_str(int(s)).decode()
+
+
+def _check(status, where):
+    if status != OK:
+        raise MoeError(status, where)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+# ---------------------------------------------------------------------------------- sizes
+
+def msum_upper(T, K, E, align):
+    return int(lib().moe_msum_upper(T, K, E, align))
+
+
+def act_sf_block_rows(align):
+    return int(lib().moe_act_sf_block_rows(align))
+
+
+def act_sf_tiled_bytes(rows, slabs, align):
+    return int(lib().moe_act_sf_tiled_bytes(rows, slabs, align))
+
+
+def act_sf_untile(tiled, rows, slabs, align):
+    """Host helper: tiled activation scales (numpy uint8) -> numpy [rows, slabs]."""
+    import numpy as np
+    src = np.ascontiguousarray(np.asarray(tiled, dtype=np.uint8).reshape(-1))
+    if src.size < act_sf_tiled_bytes(rows, slabs, align):
+        raise ValueError("tiled buffer too small")
+    out = np.empty((rows, slabs), dtype=np.uint8)
+    _check(lib().moe_act_sf_untile_host(src.ctypes.data, rows, slabs, align, out.ctypes.data),
+           "moe_act_sf_untile_host")
+    return out
+
+
+def act_sf_tile(plain, align):
+    """Host helper: numpy [rows, slabs] activation scales -> numpy tiled layout (1-D uint8)."""
+    import numpy as np
+    src = np.ascontiguousarray(np.asarray(plain, dtype=np.uint8))
+    rows, slabs = src.shape
+    out = np.empty(act_sf_tiled_bytes(rows, slabs, align), dtype=np.uint8)
+    _check(lib().moe_act_sf_tile_host(src.ctypes.data, rows, slabs, align, out.ctypes.data), "moe_act_sf_tile_host")
+    return out
+
+
+def weight_sf_packed_bytes(fmt, E, N, Kd):
+    return int(lib().moe_weight_sf_packed_bytes(WFMTS.get(fmt, fmt), E, N, Kd))
+
+
+def workspace_size(T, H, I, E, K, align):
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(T, H, I, E, K, align, ctypes.byref(n)), "moe_workspace_size")
+    return int(n.value)
+
+
+def new_workspace(T, H, I, E, K, align, device="cuda"):
+    """A zero-filled workspace tensor of the size moe_workspace_size() asks for."""
+    return torch.zeros(workspace_size(T, H, I, E, K, align), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------------------------- weights
+
+def pack_weight_scales(fmt, sf, E, N, Kd, out=None):
+    if out is None:
+        out = torch.empty(weight_sf_packed_bytes(fmt, E, N, Kd), dtype=torch.uint8, device=sf.device)
+    _check(lib().moe_pack_weight_scales(WFMTS.get(fmt, fmt), _ptr(sf, torch.uint8, "sf"), E, N, Kd,
+                                        _ptr(out, torch.uint8, "out"), _stream()), "moe_pack_weight_scales")
+    return out
+
+
+class Weight:
+    """One stacked expert weight tensor [E, N, Kd] on the device, with its scales packed."""
+
+    def __init__(self, q, sf, tscale=None, fmt="mxfp4"):
+        self.fmt = fmt
+        self.E, self.N, half = q.shape
+        self.Kd = 2 * half
+        self.q = q
+        self.sf_logical = sf
+        self.tscale = tscale
+        self.sf = pack_weight_scales(fmt, sf, self.E, self.N, self.Kd)
+
+    def c(self):
+        return _Weight(_ptr(self.q, torch.uint8, "w.q"), _ptr(self.sf, torch.uint8, "w.sf"),
+                       _ptr(self.tscale, torch.float32, "w.tscale"), WFMTS.get(self.fmt, self.fmt))
+
+
+# ---------------------------------------------------------------------------------- hot path
+
+def route(hidden, w_gate, gate_bias, e_score_bias, K, score_fn, renormalize, topk_ids, topk_w, ws,
+          logits_out=None, x_q=None, x_sf=None):
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_route(_ptr(hidden, torch.bfloat16, "hidden"),
+                           _ptr(w_gate, torch.float32, "w_gate"), _ptr(gate_bias, torch.float32, "gate_bias"),
+                           _ptr(e_score_bias, torch.float32, "e_score_bias"), T, H, E, K,
+                           SCORE_FNS.get(score_fn, score_fn), int(renormalize),
+                           _ptr(logits_out, torch.float32, "logits_out"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                           _ptr(topk_w, torch.float32, "topk_w"), _ptr(x_q, torch.uint8, "x_q"),
+                           _ptr(x_sf, torch.uint8, "x_sf"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
+           "moe_route")
+
+
+def permute(topk_ids, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, ws, expert_counts=None,
+            x_q=None, x_sf=None, x_perm=None, x_perm_sf=None):
+    T, K = topk_ids.shape
+    H = x_q.shape[1] if x_q is not None else 0
+    _check(lib().moe_permute(_ptr(topk_ids, torch.int32, "topk_ids"), T, K, E, align,
+                             _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                             _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
+                             _ptr(m_sum, torch.int32, "m_sum"), _ptr(expert_counts, torch.int32, "expert_counts"),
+                             _ptr(x_q, torch.uint8, "x_q"), _ptr(x_sf, torch.uint8, "x_sf"), H,
+                             _ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+                             _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_permute")
+
+
+def grouped_gemm_l1_swiglu(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, ws):
+    _check(lib().moe_grouped_gemm_l1_swiglu(_ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+                                            _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
+                                            T, K, H, I, E, align, w13.c(), _ptr(h_q, torch.uint8, "h_q"),
+                                            _ptr(h_sf, torch.uint8, "h_sf"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                            _stream()), "moe_grouped_gemm_l1_swiglu")
+
+
+def grouped_gemm_l2(h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, y_perm, ws):
+    _check(lib().moe_grouped_gemm_l2(_ptr(h_q, torch.uint8, "h_q"), _ptr(h_sf, torch.uint8, "h_sf"),
+                                     _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
+                                     T, K, H, I, E, align, w2.c(), _ptr(y_perm, torch.bfloat16, "y_perm"),
+                                     _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_gemm_l2")
+
+
+def unpermute_reduce(y_perm, inv_perm, topk_w, out):
+    T, K = inv_perm.shape
+    H = out.shape[1]
+    _check(lib().moe_unpermute_reduce(_ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(inv_perm, torch.int32, "inv_perm"),
+                                      _ptr(topk_w, torch.float32, "topk_w"), T, K, H, _ptr(out, torch.bfloat16, "out"),
+                                      _stream()), "moe_unpermute_reduce")
+
+
+def forward(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, renormalize, w13, w2, out, ws,
+            topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None):
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_forward(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+                             _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"),
+                             T, H, I, E, K, align, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
+                             _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                             _ptr(topk_w, torch.float32, "topk_w"), _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                             _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
+                             _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
+           "moe_forward")
+
+
+def get_error(ws):
+    """Synchronises the current stream, returns and clears the device status recorded in ws."""
+    v = ctypes.c_int(0)
+    _check(lib().moe_get_error(_ptr(ws, torch.uint8, "ws"), _stream(), ctypes.byref(v)), "moe_get_error")
+    return int(v.value)

@@ -1,0 +1,278 @@
+// C ABI of the MoE layer (declarations and contracts in include/moe.h).
+// Host-side validation, workspace layout, and launches on the caller's stream.
+#include <cstring>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+
+bool dims_ok(int T, int H, int I, int E, int K, int align) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || K <= 0 || K > E || K > 32) return false;
+  if (H % 128 || I % 128) return false;
+  if (align < 1 || align > 256 || (align & (align - 1))) return false;
+  return true;
+}
+
+// Workspace layout for one problem size.  Offsets are relative to the workspace base.
+struct WsLayout {
+  size_t status = 0;
+  size_t partial = 0, partial_bytes = 0;
+  size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
+  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0;
+  size_t total = 0;
+};
+
+WsLayout layout(int T, int H, int I, int E, int K, int align) {
+  WsLayout L;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  size_t off = kAlign;                             // [0, 256): status word
+  const int ns = route_nsplit(T > 0 ? T : 1, H, E);
+  L.partial = off;
+  L.partial_bytes = static_cast<size_t>(ns) * T * E * sizeof(float);
+  off = up(off + L.partial_bytes);
+  L.topk_ids = off;   off = up(off + static_cast<size_t>(T) * K * 4);
+  L.topk_w = off;     off = up(off + static_cast<size_t>(T) * K * 4);
+  L.x_q = off;        off = up(off + static_cast<size_t>(T) * H);
+  L.x_sf = off;       off = up(off + static_cast<size_t>(T) * (H / 128));
+  L.sorted = off;     off = up(off + U * 4);
+  L.expert_ids = off; off = up(off + U * 4);
+  L.inv_perm = off;   off = up(off + static_cast<size_t>(T) * K * 4);
+  L.m_sum = off;      off = up(off + 4);
+  L.x_perm = off;     off = up(off + U * H);
+  L.x_perm_sf = off;  off = up(off + moe_act_sf_tiled_bytes(static_cast<int>(U), H / 128, align));
+  L.h_q = off;        off = up(off + U * I);
+  L.h_sf = off;       off = up(off + moe_act_sf_tiled_bytes(static_cast<int>(U), I / 128, align));
+  L.y = off;          off = up(off + U * H * 2);
+  L.total = off;
+  return L;
+}
+
+inline uint32_t* status_of(void* ws) { return static_cast<uint32_t*>(ws); }
+inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool weight_ok(const moe_weight& w) {
+  if (!w.q || !w.sf) return false;
+  if (!aligned(w.q, 32) || !aligned(w.sf, 16)) return false;
+  if (w.fmt == MOE_W_NVFP4) return w.tscale != nullptr;
+  return w.fmt == MOE_W_MXFP4;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_msum_upper(int T, int K, int E, int align) {
+  if (T < 0 || K < 0 || E < 0 || align < 1) return 0;
+  return static_cast<size_t>(T) * K + static_cast<size_t>(E) * (align - 1);
+}
+
+int moe_act_sf_block_rows(int align) { return align >= 1 ? act_sf_block_rows(align) : 0; }
+
+size_t moe_act_sf_tiled_bytes(int rows, int slabs, int align) {
+  if (rows < 0 || slabs <= 0 || align < 1) return 0;
+  return act_sf_bytes(rows, slabs, act_sf_block_rows(align));
+}
+
+moe_status moe_act_sf_untile_host(const uint8_t* tiled, int rows, int slabs, int align, uint8_t* out) {
+  if (!tiled || !out || rows < 0 || slabs <= 0 || align < 1) return MOE_ERR_INVALID_ARG;
+  const int bt = act_sf_block_rows(align), nb = act_sf_blocks(rows, bt);
+  for (int r = 0; r < rows; ++r)
+    for (int s = 0; s < slabs; ++s) out[static_cast<size_t>(r) * slabs + s] = tiled[act_sf_offset(bt, nb, r, s)];
+  return MOE_OK;
+}
+
+moe_status moe_act_sf_tile_host(const uint8_t* plain, int rows, int slabs, int align, uint8_t* tiled) {
+  if (!tiled || !plain || rows < 0 || slabs <= 0 || align < 1) return MOE_ERR_INVALID_ARG;
+  const int bt = act_sf_block_rows(align), nb = act_sf_blocks(rows, bt);
+  memset(tiled, 127, act_sf_bytes(rows, slabs, bt));
+  for (int r = 0; r < rows; ++r)
+    for (int s = 0; s < slabs; ++s) tiled[act_sf_offset(bt, nb, r, s)] = plain[static_cast<size_t>(r) * slabs + s];
+  return MOE_OK;
+}
+
+size_t moe_weight_sf_packed_bytes(moe_wfmt fmt, int E, int N, int Kd) {
+  if (E <= 0 || N <= 0 || Kd <= 0) return 0;
+  if (fmt == MOE_W_MXFP4) return static_cast<size_t>(E) * N * (Kd / 32);
+  return 0;
+}
+
+moe_status moe_pack_weight_scales(moe_wfmt fmt, const uint8_t* sf, int E, int N, int Kd, uint8_t* sf_packed,
+                                  void* stream) {
+  if (!sf || !sf_packed || E <= 0 || N <= 0 || Kd <= 0 || N % 128 || Kd % 128) return MOE_ERR_INVALID_ARG;
+  if (fmt != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_pack_mx(sf, E * N, Kd, sf_packed, S(stream)));
+}
+
+moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size_t* bytes) {
+  if (!bytes || !dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  *bytes = layout(T, H, I, E, K, align).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_score_bias,
+                     int T, int H, int E, int K, moe_score_fn fn, int renormalize, float* logits_out,
+                     int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, void* ws, size_t ws_bytes,
+                     void* stream) {
+  if (!dims_ok(T, H, 128, E, K, 1) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
+  if ((x_q == nullptr) != (x_sf == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (x_q && (!aligned(hidden, 8) || !aligned(x_q, 4))) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const int ns = route_nsplit(T > 0 ? T : 1, H, E);
+  const size_t need = kAlign + static_cast<size_t>(ns) * T * E * sizeof(float);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
+  return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
+                                  renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, S(stream)));
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
+                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                       void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || K <= 0 || E <= 0 || K > E || align < 1 || align > 256 || (align & (align - 1)))
+    return MOE_ERR_INVALID_ARG;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (!topk_ids || !sorted_token_ids || !expert_ids || !inv_perm || !m_sum) return MOE_ERR_INVALID_ARG;
+  const bool copy = x_perm != nullptr;
+  if (copy != (x_q != nullptr) || copy != (x_sf != nullptr) || copy != (x_perm_sf != nullptr))
+    return MOE_ERR_INVALID_ARG;
+  if (copy && (H <= 0 || H % 128 || !aligned(x_q, 16) || !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  return cuda_status(launch_permute(topk_ids, T, K, E, align, static_cast<int>(U), sorted_token_ids, expert_ids,
+                                    inv_perm, m_sum, expert_counts, x_q, x_sf, H, x_perm, x_perm_sf,
+                                    status_of(ws), S(stream)));
+}
+
+static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
+                              const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
+                              const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  if (!x || !x_sf || !expert_ids || !m_sum || !weight_ok(w)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_sf, 16)) return MOE_ERR_INVALID_ARG;
+  if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
+  if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
+  if (w.fmt != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  if (U == 0) return MOE_OK;
+  GemmLaunch L;
+  L.w_q = w.q;
+  L.w_sf = w.sf;
+  L.x = x;
+  L.x_sf = x_sf;
+  L.expert_ids = expert_ids;
+  L.m_sum = m_sum;
+  L.h_q = h_q;
+  L.h_sf = h_sf;
+  L.y = y;
+  L.status = status_of(ws);
+  L.E = E;
+  L.w_rows = l1 ? 2 * I : H;
+  L.Kd = l1 ? H : I;
+  L.I = I;
+  L.U = static_cast<int>(U);
+  L.align = align;
+  return cuda_status(launch_gemm(L, l1, S(stream)));
+}
+
+moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+                                      const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
+                                      moe_weight w13, uint8_t* h_q, uint8_t* h_sf, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  return gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, nullptr, ws,
+                     ws_bytes, stream);
+}
+
+moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const int32_t* expert_ids,
+                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align, moe_weight w2,
+                               uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y_perm, ws,
+                     ws_bytes, stream);
+}
+
+moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int K,
+                                int H, uint16_t* out, void* stream) {
+  if (T < 0 || K <= 0 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
+  if (!y_perm || !inv_perm || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_perm, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_unpermute_reduce(y_perm, inv_perm, topk_w, T, K, H, out, S(stream)));
+}
+
+moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                       const float* e_score_bias, int T, int H, int I, int E, int K, int align, moe_score_fn fn,
+                       int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
+                       float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                       int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !out || !weight_ok(w13) || !weight_ok(w2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const WsLayout L = layout(T, H, I, E, K, align);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  char* b = static_cast<char*>(ws);
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(b + L.topk_ids);
+  float* tw = topk_w ? topk_w : reinterpret_cast<float*>(b + L.topk_w);
+  int32_t* sorted = sorted_token_ids ? sorted_token_ids : reinterpret_cast<int32_t*>(b + L.sorted);
+  int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.expert_ids);
+  int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.inv_perm);
+  int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.m_sum);
+  uint8_t* xq = reinterpret_cast<uint8_t*>(b + L.x_q);
+  uint8_t* xsf = reinterpret_cast<uint8_t*>(b + L.x_sf);
+  uint8_t* xp = reinterpret_cast<uint8_t*>(b + L.x_perm);
+  uint8_t* xpsf = reinterpret_cast<uint8_t*>(b + L.x_perm_sf);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(b + L.h_q);
+  uint8_t* hsf = reinterpret_cast<uint8_t*>(b + L.h_sf);
+  uint16_t* y = reinterpret_cast<uint16_t*>(b + L.y);
+  moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
+                            xq, xsf, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_permute(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_grouped_gemm_l1_swiglu(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, hq, hsf, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  st = moe_grouped_gemm_l2(hq, hsf, eids, ms, T, K, H, I, E, align, w2, y, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  return moe_unpermute_reduce(y, inv, tw, T, K, H, out, stream);
+}
+
+moe_status moe_get_error(void* ws, void* stream, moe_status* device_status) {
+  if (!ws || !device_status) return MOE_ERR_INVALID_ARG;
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0 && cudaMemset(ws, 0, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  *device_status = static_cast<moe_status>(v);
+  return MOE_OK;
+}
+
+const char* moe_status_str(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_INDEX: return "expert id out of range (device)";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "kernel self-check failed (bounds or alignment)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

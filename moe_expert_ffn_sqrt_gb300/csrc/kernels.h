@@ -1,0 +1,46 @@
+// Internal launchers shared between the kernel files and the C ABI layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// route.cu
+int route_nsplit(int T, int H, int E);
+cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
+                         int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
+                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
+                         cudaStream_t stream);
+
+// permute.cu
+size_t permute_smem_bytes(int E);
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
+                           int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
+                           const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                           uint32_t* status, cudaStream_t stream);
+
+// gemm.cu
+struct GemmLaunch {
+  const uint8_t* w_q;          // [E, w_rows, Kd/2]
+  const uint8_t* w_sf;         // packed scales
+  const uint8_t* x;            // [U, Kd] E4M3
+  const uint8_t* x_sf;         // tiled (rows U, slabs Kd/128)
+  const int32_t* expert_ids;
+  const int32_t* m_sum;
+  uint8_t* h_q;
+  uint8_t* h_sf;
+  uint16_t* y;
+  uint32_t* status;
+  int E, w_rows, Kd, I, U, align;
+};
+int num_sms();
+int gemm_block_n(int align);
+cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
+cudaError_t launch_pack_mx(const uint8_t* sf, int rows, int Kd, uint8_t* out, cudaStream_t stream);
+
+// reduce.cu
+cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int T, int K,
+                                    int H, uint16_t* out, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,171 @@
+// Expert-contiguous permute with per-expert alignment.
+// Note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4 (scatter, inv_perm, M_sum), §10 (M_sum_upper) and the
+// m_indices paragraph (expert_ids, -1 on padding); MegaMoE page 路径 A (moe_align_block_size).
+//
+// One CTA of 1024 threads does the whole index computation, deterministically:
+//   1. each warp counts its contiguous chunk of the flat (t,k) list into a private histogram;
+//   2. per expert: count, aligned size, exclusive scan -> segment starts, M_sum; per (warp,
+//      expert) base row = segment start + pairs of that expert in earlier chunks;
+//   3. each warp walks its chunk in order, 32 pairs at a time; __match_any_sync groups equal
+//      experts so that each pair's rank among earlier pairs of its expert is exact.
+// Padding rows get expert_ids = -1 and sorted_token_ids = T*K.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+struct PermuteArgs {
+  const int32_t* topk_ids;
+  int T, K, E, align, U;
+  int32_t* sorted_ids;
+  int32_t* expert_ids;
+  int32_t* inv_perm;
+  int32_t* m_sum;
+  int32_t* counts;       // optional
+  uint32_t* status;
+};
+
+__global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteArgs a) {
+  extern __shared__ int32_t sh[];
+  int32_t* hist = sh;                              // [kPermWarps][E]
+  int32_t* seg = sh + kPermWarps * a.E;            // [E] segment start
+  int32_t* cnt = seg + a.E;                        // [E]
+  __shared__ int32_t s_total;
+  __shared__ int32_t s_scan[kPermThreads];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int N = a.T * a.K;
+  const int chunk = (N + kPermWarps - 1) / kPermWarps;
+  const int cbeg = min(N, warp * chunk), cend = min(N, cbeg + chunk);
+  for (int i = tid; i < kPermWarps * a.E; i += kPermThreads) hist[i] = 0;
+  __syncthreads();
+  // 1. histograms
+  for (int i = cbeg + lane; i < cend; i += 32) {
+    const int e = a.topk_ids[i];
+    if (e < 0 || e >= a.E) {
+      record_error(a.status, kDevErrIndex);
+      continue;
+    }
+    atomicAdd(&hist[warp * a.E + e], 1);
+  }
+  __syncthreads();
+  // 2. counts, aligned sizes, exclusive scan over experts (blocked: each thread owns a run)
+  const int per = (a.E + kPermThreads - 1) / kPermThreads;
+  int local = 0;
+  for (int j = 0; j < per; ++j) {
+    const int e = tid * per + j;
+    if (e < a.E) {
+      int c = 0;
+      for (int w = 0; w < kPermWarps; ++w) c += hist[w * a.E + e];
+      cnt[e] = c;
+      local += (c + a.align - 1) / a.align * a.align;
+    }
+  }
+  s_scan[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < kPermThreads; off <<= 1) {   // inclusive Hillis-Steele scan
+    const int v = (tid >= off) ? s_scan[tid - off] : 0;
+    __syncthreads();
+    s_scan[tid] += v;
+    __syncthreads();
+  }
+  int run = s_scan[tid] - local;
+  for (int j = 0; j < per; ++j) {
+    const int e = tid * per + j;
+    if (e < a.E) {
+      seg[e] = run;
+      int base = run;
+      for (int w = 0; w < kPermWarps; ++w) {
+        const int h = hist[w * a.E + e];
+        hist[w * a.E + e] = base;
+        base += h;
+      }
+      run += (cnt[e] + a.align - 1) / a.align * a.align;
+    }
+  }
+  if (tid == kPermThreads - 1) s_total = s_scan[tid];
+  __syncthreads();
+  const int msum = s_total;
+  // 3. ranks in (t,k) order within each warp's chunk
+  for (int i0 = cbeg; i0 < cend; i0 += 32) {
+    const int i = i0 + lane;
+    const bool live = i < cend;
+    int e = live ? a.topk_ids[i] : -1;
+    const bool ok = live && e >= 0 && e < a.E;
+    if (!ok) e = -1 - lane;                            // unique dummy key for dead lanes
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int pos = 0;
+    if (ok) pos = hist[warp * a.E + e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) hist[warp * a.E + e] += __popc(peers);
+    __syncwarp();
+    if (ok) {
+      a.inv_perm[i] = pos;
+      a.sorted_ids[pos] = i;
+      a.expert_ids[pos] = e;
+    }
+  }
+  // padding rows inside each segment, then the tail [M_sum, U)
+  for (int e = warp; e < a.E; e += kPermWarps) {
+    const int c = cnt[e];
+    const int padded = (c + a.align - 1) / a.align * a.align;
+    for (int r = c + lane; r < padded; r += 32) {
+      a.sorted_ids[seg[e] + r] = N;
+      a.expert_ids[seg[e] + r] = -1;
+    }
+  }
+  for (int r = msum + tid; r < a.U; r += kPermThreads) {
+    a.sorted_ids[r] = N;
+    a.expert_ids[r] = -1;
+  }
+  if (a.counts)
+    for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
+  if (tid == 0) *a.m_sum = msum;
+}
+
+// Row copy: x_perm[inv_perm[t,k]] = x_q[t], scales into the tiled layout.  One warp per pair.
+__global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __restrict__ inv_perm,
+                                                           const int32_t* __restrict__ topk_ids, int T, int K, int E,
+                                                           int H, const uint8_t* __restrict__ x_q,
+                                                           const uint8_t* __restrict__ x_sf, uint8_t* __restrict__ x_perm,
+                                                           uint8_t* __restrict__ x_perm_sf, int bt, int nb) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const long long pair = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (pair >= static_cast<long long>(T) * K) return;
+  const int e = topk_ids[pair];
+  if (e < 0 || e >= E) return;
+  const int t = static_cast<int>(pair / K);
+  const int dst = inv_perm[pair];
+  const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
+  uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
+  for (int j = lane; j < H / 16; j += 32) out[j] = src[j];
+  const int slabs = H / 128;
+  for (int s = lane; s < slabs; s += 32) x_perm_sf[act_sf_offset(bt, nb, dst, s)] = x_sf[static_cast<size_t>(t) * slabs + s];
+}
+
+size_t permute_smem_bytes(int E) { return static_cast<size_t>(kPermWarps + 2) * E * sizeof(int32_t); }
+
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
+                           int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
+                           const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                           uint32_t* status, cudaStream_t stream) {
+  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status};
+  const size_t smem = permute_smem_bytes(E);
+  cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  permute_kernel<<<1, kPermThreads, smem, stream>>>(a);
+  err = cudaGetLastError();
+  if (err != cudaSuccess || x_perm == nullptr) return err;
+  const long long pairs = static_cast<long long>(T) * K;
+  if (pairs == 0) return cudaSuccess;
+  permute_rows_kernel<<<static_cast<int>((pairs + 7) / 8), 256, 0, stream>>>(inv_perm, topk_ids, T, K, E, H, x_q, x_sf,
+                                                                              x_perm, x_perm_sf, act_sf_block_rows(align),
+                                                                              act_sf_blocks(U, act_sf_block_rows(align)));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

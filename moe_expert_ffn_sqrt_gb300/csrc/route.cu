@@ -1,0 +1,245 @@
+// Routing: gate GEMM (split over H, deterministic), scoring + biased top-K, FP8 activation
+// quantisation.  Page "DeepSeek V4 MegaMoE Kernel 深度解析", 经典 MoE 的计算过程 / 第一步：路由,
+// and the CUDA tag page teaser row "Fused TopK Bias Routing" (sqrt(softplus), e_score_correction_bias).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------------------------------
+// Gate GEMM: partial[split][t][e] = sum_{h in split} hidden[t,h] * w_gate[e,h].
+// CTA tile 32 tokens x 64 experts, H walked in chunks of 32; 256 threads, 2x4 outputs each.
+constexpr int GT = 32, GE = 64, GH = 32;
+
+__global__ void __launch_bounds__(256) gate_gemm_kernel(const uint16_t* __restrict__ hidden,
+                                                        const float* __restrict__ wg, int T, int H, int E,
+                                                        int h_per_split, float* __restrict__ partial) {
+  __shared__ float xs[GH][GT + 1];
+  __shared__ float ws[GH][GE + 1];
+  const int t0 = blockIdx.x * GT, e0 = blockIdx.y * GE, split = blockIdx.z;
+  const int hbeg = split * h_per_split, hend = min(H, hbeg + h_per_split);
+  const int tid = threadIdx.x;
+  const int tr = (tid / 16) * 2;   // token rows tr, tr+1
+  const int ec = (tid % 16) * 4;   // expert cols ec..ec+3
+  float acc[2][4] = {};
+  for (int h0 = hbeg; h0 < hend; h0 += GH) {
+    // hidden tile: 32 tokens x 32 h  (1024 values, 4 per thread)
+    for (int i = tid; i < GT * GH; i += 256) {
+      const int tt = i / GH, hh = i % GH;
+      const int t = t0 + tt, h = h0 + hh;
+      float v = 0.f;
+      if (t < T && h < hend) v = __uint_as_float(static_cast<uint32_t>(hidden[static_cast<size_t>(t) * H + h]) << 16);
+      xs[hh][tt] = v;
+    }
+    for (int i = tid; i < GE * GH; i += 256) {
+      const int ee = i / GH, hh = i % GH;
+      const int e = e0 + ee, h = h0 + hh;
+      ws[hh][ee] = (e < E && h < hend) ? wg[static_cast<size_t>(e) * H + h] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int hh = 0; hh < GH; ++hh) {
+      const float x0 = xs[hh][tr], x1 = xs[hh][tr + 1];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float w = ws[hh][ec + j];
+        acc[0][j] = fmaf(x0, w, acc[0][j]);
+        acc[1][j] = fmaf(x1, w, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+  for (int i = 0; i < 2; ++i) {
+    const int t = t0 + tr + i;
+    if (t >= T) continue;
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + ec + j;
+      if (e < E) partial[(static_cast<size_t>(split) * T + t) * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-K (one warp per token; lane holds experts lane, lane+32, ...) and FP8 activation
+// quantisation (one warp per 128-column group), in one launch.
+constexpr int kMaxEPerLane = 32;   // E <= 1024
+
+struct RouteFinishArgs {
+  const float* partial;
+  int nsplit;
+  const float* gate_bias;
+  const float* e_bias;
+  int T, H, E, K;
+  int score_fn;      // 0 softmax, 1 sqrt(softplus)
+  int renormalize;
+  float* logits_out;
+  int32_t* topk_ids;
+  float* topk_w;
+  const uint16_t* hidden;
+  uint8_t* x_q;
+  uint8_t* x_sf;
+  int topk_blocks;   // blocks [0, topk_blocks) do top-K
+};
+
+__device__ __forceinline__ void warp_argmax(float& key, int& id) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float k2 = __shfl_xor_sync(0xffffffffu, key, off);
+    const int i2 = __shfl_xor_sync(0xffffffffu, id, off);
+    if (k2 > key || (k2 == key && i2 < id)) {
+      key = k2;
+      id = i2;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs a) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (static_cast<int>(blockIdx.x) < a.topk_blocks) {
+    const int t = blockIdx.x * 8 + warp;
+    if (t >= a.T) return;
+    const int per = (a.E + 31) / 32;
+    float s[kMaxEPerLane], key[kMaxEPerLane];
+    float lmax = -INFINITY;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane + 32 * j;
+      float l = -INFINITY;
+      if (e < a.E) {
+        l = 0.f;
+        for (int sp = 0; sp < a.nsplit; ++sp) l += a.partial[(static_cast<size_t>(sp) * a.T + t) * a.E + e];
+        if (a.gate_bias) l += a.gate_bias[e];
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * a.E + e] = l;
+      }
+      s[j] = l;
+      lmax = fmaxf(lmax, l);
+    }
+    if (a.score_fn == 0) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+      float sum = 0.f;
+      for (int j = 0; j < per; ++j) {
+        const int e = lane + 32 * j;
+        s[j] = (e < a.E) ? expf(s[j] - lmax) : 0.f;
+        sum += s[j];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      for (int j = 0; j < per; ++j) s[j] = s[j] / sum;
+    } else {
+      for (int j = 0; j < per; ++j) {
+        const float l = s[j];
+        s[j] = (lane + 32 * j < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
+      }
+    }
+    for (int j = 0; j < per; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (e < a.E) ? s[j] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
+    }
+    float wsel[32];
+    float wsum = 0.f;
+    for (int k = 0; k < a.K; ++k) {
+      // best candidate of this lane (ties: lower id, i.e. lower j)
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int j = 0; j < per; ++j) {
+        const int e = lane + 32 * j;
+        if (e < a.E && (key[j] > bk || (key[j] == bk && e < bi))) {
+          bk = key[j];
+          bi = e;
+        }
+      }
+      warp_argmax(bk, bi);
+      // owner lane removes the winner and publishes its unbiased score
+      float sw = 0.f;
+      if ((bi & 31) == lane) {
+        const int j = bi >> 5;
+        for (int jj = 0; jj < per; ++jj)
+          if (jj == j) {
+            sw = s[jj];
+            key[jj] = -INFINITY;
+          }
+      }
+      sw = __shfl_sync(0xffffffffu, sw, bi & 31);
+      if (k < 32) wsel[k] = sw;
+      wsum += sw;
+      if (lane == 0) a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
+    }
+    if (lane == 0) {
+      for (int k = 0; k < a.K; ++k) {
+        const float w = a.renormalize ? wsel[k] / wsum : wsel[k];
+        a.topk_w[static_cast<size_t>(t) * a.K + k] = w;
+      }
+    }
+    return;
+  }
+  // FP8 activation quantisation: group g of token t = 128 columns, 4 per lane.
+  const int gpt = a.H / 128;
+  const long long gidx = static_cast<long long>(blockIdx.x - a.topk_blocks) * 8 + warp;
+  if (gidx >= static_cast<long long>(a.T) * gpt) return;
+  const int t = static_cast<int>(gidx / gpt), g = static_cast<int>(gidx % gpt);
+  const size_t base = static_cast<size_t>(t) * a.H + g * 128 + lane * 4;
+  const uint2 raw = *reinterpret_cast<const uint2*>(a.hidden + base);
+  float v[4];
+  v[0] = __uint_as_float(raw.x << 16);
+  v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+  v[2] = __uint_as_float(raw.y << 16);
+  v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+  float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const int e = ue8m0_exponent(amax);
+  const float sc = pow2_neg(e);
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v[0] * sc, v[1] * sc), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v[2] * sc, v[3] * sc), __NV_SATFINITE, __NV_E4M3);
+  *reinterpret_cast<uint32_t*>(a.x_q + base) = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  if (lane == 0) a.x_sf[static_cast<size_t>(t) * gpt + g] = static_cast<uint8_t>(e + 127);
+}
+
+int route_nsplit(int T, int H, int E) {
+  const int tiles = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
+  int ns = (2 * 152 + tiles - 1) / tiles;
+  const int maxs = (H + 127) / 128;
+  if (ns > maxs) ns = maxs;
+  if (ns < 1) ns = 1;
+  return ns;
+}
+
+cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
+                         int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
+                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
+                         cudaStream_t stream) {
+  const int ns = route_nsplit(T, H, E);
+  int hps = (H + ns - 1) / ns;
+  hps = (hps + GH - 1) / GH * GH;
+  dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
+  gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  RouteFinishArgs a;
+  a.partial = partial;
+  a.nsplit = ns;
+  a.gate_bias = gate_bias;
+  a.e_bias = e_bias;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.K = K;
+  a.score_fn = score_fn;
+  a.renormalize = renormalize;
+  a.logits_out = logits_out;
+  a.topk_ids = topk_ids;
+  a.topk_w = topk_w;
+  a.hidden = hidden;
+  a.x_q = x_q;
+  a.x_sf = x_sf;
+  a.topk_blocks = (T + 7) / 8;
+  const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;
+  const int qblocks = static_cast<int>((qgroups + 7) / 8);
+  route_finish_kernel<<<a.topk_blocks + qblocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,124 @@
+"""CPU checks of the C ABI: the library builds and loads, exports every symbol include/moe.h declares,
+its host-side helpers are consistent, and bad arguments are rejected before any device work."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def M():
+    import moe_expert_ffn_sqrt_gb300 as M
+    if not os.path.exists(M.LIB_PATH):
+        from moe_expert_ffn_sqrt_gb300 import build
+        build.build()
+    M.lib()
+    return M
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(M):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(M.lib(), n), n
+
+
+def test_sizes(M):
+    assert M.msum_upper(8, 6, 256, 16) == 3888
+    assert M.msum_upper(3, 2, 3, 1) == 6
+    assert M.act_sf_block_rows(1) == 16 and M.act_sf_block_rows(64) == 64 and M.act_sf_block_rows(256) == 128
+    assert M.weight_sf_packed_bytes("mxfp4", 2, 256, 512) == 2 * 256 * 16
+    n = M.workspace_size(8, 7168, 2048, 256, 6, 16)
+    assert n > 3888 * 7168  # holds the permuted activations
+
+
+@pytest.mark.parametrize("rows,slabs,align", [(3888, 56, 16), (100, 2, 1), (257, 16, 64), (1000, 5, 256), (0, 4, 16)])
+def test_act_sf_tile_roundtrip(M, rows, slabs, align):
+    rng = np.random.default_rng(rows + slabs)
+    plain = rng.integers(0, 256, size=(rows, slabs), dtype=np.uint8)
+    tiled = M.act_sf_tile(plain, align)
+    assert tiled.size == M.act_sf_tiled_bytes(rows, slabs, align)
+    assert np.array_equal(M.act_sf_untile(tiled, rows, slabs, align), plain)
+    # distinct (row, slab) pairs land on distinct bytes
+    if rows:
+        marks = np.arange(rows * slabs, dtype=np.int64).reshape(rows, slabs)
+        for v in (marks % 251, marks // 251 % 251):
+            back = M.act_sf_untile(M.act_sf_tile(v.astype(np.uint8), align), rows, slabs, align)
+            assert np.array_equal(back, v.astype(np.uint8))
+
+
+def test_act_sf_layout_formula(M):
+    # the byte of (r, s) sits where the header's formula says (spot checks, block rows 16 and 128)
+    for align, rows, slabs in ((16, 70, 9), (256, 300, 6)):
+        bt = M.act_sf_block_rows(align)
+        nb = (rows + bt - 1) // bt + 1
+        cb = 256 if bt == 16 else 512
+        plain = np.zeros((rows, slabs), np.uint8)
+        for r, s in ((0, 0), (rows - 1, slabs - 1), (17, 5), (rows // 2, 3)):
+            plain[:] = 0
+            plain[r, s] = 200
+            tiled = M.act_sf_tile(plain, align)
+            off = ((s // 4) * nb + r // bt) * cb + ((r % bt) % 32) * 16 + ((r % bt) // 32) * 4 + s % 4
+            assert tiled[off] == 200
+
+
+def test_invalid_arguments_are_rejected(M):
+    L = M.lib()
+    fake = ctypes.c_void_p(0x10000)     # never dereferenced: validation fails first
+    ws = ctypes.c_void_p(0x20000)
+    # H not a multiple of 128
+    assert L.moe_route(fake, fake, None, None, 8, 100, 16, 2, 0, 1, None, fake, fake, None, None, ws, 1 << 20,
+                       None) == M.ERR_INVALID_ARG
+    # K > E
+    assert L.moe_route(fake, fake, None, None, 8, 128, 4, 5, 0, 1, None, fake, fake, None, None, ws, 1 << 20,
+                       None) == M.ERR_INVALID_ARG
+    # bad score function
+    assert L.moe_route(fake, fake, None, None, 8, 128, 16, 2, 9, 1, None, fake, fake, None, None, ws, 1 << 20,
+                       None) == M.ERR_INVALID_ARG
+    # workspace too small
+    assert L.moe_route(fake, fake, None, None, 8, 128, 16, 2, 0, 1, None, fake, fake, None, None, ws, 16,
+                       None) == M.ERR_WORKSPACE
+    # align not a power of two
+    assert L.moe_permute(fake, 8, 2, 16, 3, fake, fake, fake, fake, None, None, None, 0, None, None, ws, 4096,
+                         None) == M.ERR_INVALID_ARG
+    # only some of the optional row-copy buffers
+    assert L.moe_permute(fake, 8, 2, 16, 16, fake, fake, fake, fake, None, fake, None, 128, None, None, ws, 4096,
+                         None) == M.ERR_INVALID_ARG
+    # unsupported number of experts for the permute kernel
+    assert L.moe_permute(fake, 8, 2, 4096, 16, fake, fake, fake, fake, None, None, None, 0, None, None, ws, 4096,
+                         None) == M.ERR_UNSUPPORTED
+    w = M._Weight(0x10000, 0x20000, None, M.W_MXFP4)
+    # misaligned weight pointer
+    wbad = M._Weight(0x10010, 0x20000, None, M.W_MXFP4)
+    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wbad, fake, fake, ws, 4096,
+                                        None) == M.ERR_INVALID_ARG
+    # NVFP4 needs a tensor scale pointer
+    wnv = M._Weight(0x10000, 0x20000, None, M.W_NVFP4)
+    assert L.moe_grouped_gemm_l2(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wnv, fake, ws, 4096,
+                                 None) == M.ERR_INVALID_ARG
+    # forward with a workspace smaller than moe_workspace_size
+    assert L.moe_forward(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, w, w, fake, None, None, None, None,
+                         None, None, ws, 1024, None) == M.ERR_WORKSPACE
+    # unpermute-reduce with H not a multiple of 8
+    assert L.moe_unpermute_reduce(fake, fake, fake, 2, 2, 12, fake, None) == M.ERR_INVALID_ARG
+    assert M.status_str(M.ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_product_path_does_not_touch_the_oracle():
+    # the library and its binding never import, load or call the oracle
+    pkg = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"(import|from)\s+oracle|oracle/", src), f
