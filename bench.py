@@ -39,7 +39,12 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default="decode", choices=sorted(synth.WORKLOADS))
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="budget of the oracle CPU baseline (0 skips it, e.g. under a profiler)")
+    p.add_argument("--ref-seconds", type=float, default=150.0,
+                   help="time budget of the reference (oracle) arm's timed steps")
+    p.add_argument("--experts", type=int, default=None,
+                   help="override E (smaller cases of the same kernels for profiler captures)")
     return p.parse_args()
 
 
@@ -155,10 +160,15 @@ def run_reference(args, w):
     stack = synth.all_expert_weights(w)
     from oracle import moe as O
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
-    for i in range(args.warmup):
+    # warm-up (at most one step: each oracle step is seconds long), then as many timed steps as fit
+    # the time budget, at most --steps; the line reports the number actually run
+    t0 = time.perf_counter()
+    for i in range(min(args.warmup, 1)):
         O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
+    est = max(time.perf_counter() - t0, 1e-3)
+    steps = max(1, min(args.steps, int(args.ref_seconds / est)))
     times = []
-    for i in range(args.steps):
+    for i in range(steps):
         t0 = time.perf_counter()
         O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
         times.append(time.perf_counter() - t0)
@@ -167,7 +177,7 @@ def run_reference(args, w):
     cores = os.cpu_count()
     sample = f"1 token of the {w.name} workload per step (routing of all {w.T} tokens + that token's {w.K} experts)"
     line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
@@ -212,8 +222,10 @@ def run_ours(args, w):
     def d(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]), w.fmt)
-    w2 = M.Weight(d(stack["w2_q"]), d(stack["w2_sf"]), None if stack["w2_ts"] is None else d(stack["w2_ts"]), w.fmt)
+    w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]), w.fmt,
+                   pair=2)
+    w2 = M.Weight(d(stack["w2_q"]), d(stack["w2_sf"]), None if stack["w2_ts"] is None else d(stack["w2_ts"]), w.fmt,
+                  pair=1)
     T = w.T
     hidden_host = torch.from_numpy(inp["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hidden = hidden_host.to(dev)
@@ -334,7 +346,7 @@ def run_ours(args, w):
     line = None
     if rank == 0:
         cpu = None
-        if W == 1:
+        if W == 1 and args.cpu_seconds > 0:
             v, n, dt = oracle_tokens_per_s(w, inp, stack, args.cpu_seconds)
             cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                    "sample": f"{n} token(s) of the {w.name} workload (routing of all {w.T} tokens each time), "
@@ -356,6 +368,9 @@ def run_ours(args, w):
 def main():
     args = parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        w = dataclasses.replace(w, E=args.experts, name=f"{w.name}-E{args.experts}")
     if args.impl == "reference":
         run_reference(args, w)
     else:

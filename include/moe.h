@@ -35,7 +35,7 @@
  *     so each (row block, 4 slabs) is one contiguous chunk that the GEMM copies into tensor
  *     memory as is.  Total moe_act_sf_tiled_bytes(rows, slabs, align); the _host helpers
  *     convert to and from the plain [rows, slabs] layout.
- *   - Weight scales "packed": produced once per weight tensor by moe_pack_weight_scales().
+ *   - Weights: read from the packed stream produced once per tensor by moe_pack_weights().
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -67,13 +67,15 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score_fn
 typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
 
 /* One stacked expert weight tensor with logical shape [E, N, Kd] (N output rows, Kd the
- * reduction dim).  W13: N = 2I, Kd = H, rows 0..I-1 are the gate projection W1 and rows
- * I..2I-1 the up projection W3 (MegaMoE page, 第三步).  W2: N = H, Kd = I. */
+ * reduction dim), in the packed stream written by moe_pack_weights.  W13: N = 2I, Kd = H,
+ * rows 0..I-1 are the gate projection W1 and rows I..2I-1 the up projection W3 (MegaMoE page,
+ * 第三步), packed with pair = 2.  W2: N = H, Kd = I, packed with pair = 1. */
 typedef struct {
-  const uint8_t* q;      /* [E, N, Kd/2] packed E2M1 codes (32-byte aligned)                 */
-  const uint8_t* sf;     /* scales in the packed layout written by moe_pack_weight_scales   */
-  const float* tscale;   /* NVFP4: [E] fp32 per-matrix scale; MXFP4: NULL                    */
+  const uint8_t* packed;  /* moe_pack_weights output (32-byte aligned)                        */
+  const float* tscale;    /* NVFP4: [E] fp32 per-matrix scale; MXFP4: NULL                    */
   moe_wfmt fmt;
+  int E, N, Kd;           /* logical shape                                                    */
+  int pair;               /* 2 for W13 (gate/up row tiles interleaved), 1 for W2              */
 } moe_weight;
 
 /* --------------------------------------------------------------------------------------
@@ -98,15 +100,19 @@ moe_status moe_act_sf_untile_host(const uint8_t* tiled, int rows, int slabs, int
  * the tiled buffer that no (row, slab) maps to are set to 127 (scale 1.0). */
 moe_status moe_act_sf_tile_host(const uint8_t* plain, int rows, int slabs, int align, uint8_t* tiled);
 
-/* Bytes of the packed scale buffer of a weight tensor [E, N, Kd] in format fmt. */
-size_t moe_weight_sf_packed_bytes(moe_wfmt fmt, int E, int N, int Kd);
+/* Bytes of the packed stream of a weight tensor [E, N, Kd] in format fmt with the given pairing
+ * (0 if the shape is not supported). */
+size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair);
 
-/* Rearranges a weight tensor's scales from the logical layout ([E, N, Kd/32] UE8M0 for
- * MXFP4, [E, N, Kd/16] E4M3 for NVFP4) into the layout the grouped GEMMs stream, so that
- * each 128-row x 128-deep weight tile's scales are one contiguous block.  Done once per
- * weight tensor (weights are static).  N and Kd must be multiples of 128. */
-moe_status moe_pack_weight_scales(moe_wfmt fmt, const uint8_t* sf, int E, int N, int Kd,
-                                  uint8_t* sf_packed, void* stream);
+/* Rearranges a weight tensor (codes [E, N, Kd/2] packed E2M1; scales [E, N, Kd/32] UE8M0 for
+ * MXFP4) into the stream the grouped GEMMs read: one contiguous chunk per (expert, weight tile,
+ * 128-deep slab) in reading order, so that weights stream from HBM in long sequential runs.
+ * A weight tile is 256 rows: pair = 2 joins rows 128t.. with rows N/2 + 128t.. (W13: gate with
+ * up); pair = 1 takes rows 256t.. (W2; rows past N read as zero).  Each chunk holds the tile's
+ * codes, then its scales arranged for tensor memory.  Done once per weight tensor (weights are
+ * static).  Kd must be a multiple of 128; N of 256 (pair = 2) or 128 (pair = 1). */
+moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair,
+                            uint8_t* packed, void* stream);
 
 /* Bytes of workspace needed by moe_route, moe_permute, the grouped GEMMs and moe_forward
  * for this problem.  The first 256 bytes hold the device status word.  A workspace must

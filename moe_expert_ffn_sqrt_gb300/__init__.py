@@ -26,7 +26,8 @@ class MoeError(RuntimeError):
 
 
 class _Weight(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("tscale", ctypes.c_void_p), ("fmt", ctypes.c_int)]
+    _fields_ = [("packed", ctypes.c_void_p), ("tscale", ctypes.c_void_p), ("fmt", ctypes.c_int),
+                ("E", ctypes.c_int), ("N", ctypes.c_int), ("Kd", ctypes.c_int), ("pair", ctypes.c_int)]
 
 
 _lib = None
@@ -50,10 +51,10 @@ def lib():
         L.moe_act_sf_untile_host.argtypes = [P, I, I, I, P]
         L.moe_act_sf_tile_host.restype = S
         L.moe_act_sf_tile_host.argtypes = [P, I, I, I, P]
-        L.moe_weight_sf_packed_bytes.restype = Z
-        L.moe_weight_sf_packed_bytes.argtypes = [I, I, I, I]
-        L.moe_pack_weight_scales.restype = S
-        L.moe_pack_weight_scales.argtypes = [I, P, I, I, I, P, P]
+        L.moe_weight_packed_bytes.restype = Z
+        L.moe_weight_packed_bytes.argtypes = [I, I, I, I, I]
+        L.moe_pack_weights.restype = S
+        L.moe_pack_weights.argtypes = [I, P, P, I, I, I, I, P, P]
         L.moe_workspace_size.restype = S
         L.moe_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
         L.moe_route.restype = S
@@ -139,8 +140,8 @@ def act_sf_tile(plain, align):
     return out
 
 
-def weight_sf_packed_bytes(fmt, E, N, Kd):
-    return int(lib().moe_weight_sf_packed_bytes(WFMTS.get(fmt, fmt), E, N, Kd))
+def weight_packed_bytes(fmt, E, N, Kd, pair):
+    return int(lib().moe_weight_packed_bytes(WFMTS.get(fmt, fmt), E, N, Kd, pair))
 
 
 def workspace_size(T, H, I, E, K, align):
@@ -156,29 +157,35 @@ def new_workspace(T, H, I, E, K, align, device="cuda"):
 
 # ---------------------------------------------------------------------------------- weights
 
-def pack_weight_scales(fmt, sf, E, N, Kd, out=None):
+def pack_weights(fmt, q, sf, pair, out=None):
+    """Packs codes q [E, N, Kd/2] and scales sf into the GEMMs' weight stream (moe_pack_weights)."""
+    E, N, half = q.shape
+    Kd = 2 * half
     if out is None:
-        out = torch.empty(weight_sf_packed_bytes(fmt, E, N, Kd), dtype=torch.uint8, device=sf.device)
-    _check(lib().moe_pack_weight_scales(WFMTS.get(fmt, fmt), _ptr(sf, torch.uint8, "sf"), E, N, Kd,
-                                        _ptr(out, torch.uint8, "out"), _stream()), "moe_pack_weight_scales")
+        out = torch.empty(weight_packed_bytes(fmt, E, N, Kd, pair), dtype=torch.uint8, device=q.device)
+    _check(lib().moe_pack_weights(WFMTS.get(fmt, fmt), _ptr(q, torch.uint8, "q"), _ptr(sf, torch.uint8, "sf"), E, N,
+                                  Kd, pair, _ptr(out, torch.uint8, "out"), _stream()), "moe_pack_weights")
     return out
 
 
 class Weight:
-    """One stacked expert weight tensor [E, N, Kd] on the device, with its scales packed."""
+    """One stacked expert weight tensor [E, N, Kd] on the device, packed for the grouped GEMMs.
 
-    def __init__(self, q, sf, tscale=None, fmt="mxfp4"):
+    pair = 2 for W13 (gate rows 0..I-1 and up rows I..2I-1), 1 for W2.  The logical tensors are
+    only read while packing.
+    """
+
+    def __init__(self, q, sf, tscale=None, fmt="mxfp4", pair=1):
         self.fmt = fmt
         self.E, self.N, half = q.shape
         self.Kd = 2 * half
-        self.q = q
-        self.sf_logical = sf
+        self.pair = pair
         self.tscale = tscale
-        self.sf = pack_weight_scales(fmt, sf, self.E, self.N, self.Kd)
+        self.packed = pack_weights(fmt, q, sf, pair)
 
     def c(self):
-        return _Weight(_ptr(self.q, torch.uint8, "w.q"), _ptr(self.sf, torch.uint8, "w.sf"),
-                       _ptr(self.tscale, torch.float32, "w.tscale"), WFMTS.get(self.fmt, self.fmt))
+        return _Weight(_ptr(self.packed, torch.uint8, "w.packed"), _ptr(self.tscale, torch.float32, "w.tscale"),
+                       WFMTS.get(self.fmt, self.fmt), self.E, self.N, self.Kd, self.pair)
 
 
 # ---------------------------------------------------------------------------------- hot path

@@ -60,9 +60,10 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
 inline uint32_t* status_of(void* ws) { return static_cast<uint32_t*>(ws); }
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
-bool weight_ok(const moe_weight& w) {
-  if (!w.q || !w.sf) return false;
-  if (!aligned(w.q, 32) || !aligned(w.sf, 16)) return false;
+// A packed weight of logical shape [E, N, Kd] with the given pairing.
+bool weight_ok(const moe_weight& w, int E, int N, int Kd, int pair) {
+  if (!w.packed || !aligned(w.packed, 32)) return false;
+  if (w.E != E || w.N != N || w.Kd != Kd || w.pair != pair) return false;
   if (w.fmt == MOE_W_NVFP4) return w.tscale != nullptr;
   return w.fmt == MOE_W_MXFP4;
 }
@@ -100,17 +101,19 @@ moe_status moe_act_sf_tile_host(const uint8_t* plain, int rows, int slabs, int a
   return MOE_OK;
 }
 
-size_t moe_weight_sf_packed_bytes(moe_wfmt fmt, int E, int N, int Kd) {
-  if (E <= 0 || N <= 0 || Kd <= 0) return 0;
-  if (fmt == MOE_W_MXFP4) return static_cast<size_t>(E) * N * (Kd / 32);
+size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair) {
+  if (E <= 0 || N <= 0 || Kd <= 0 || Kd % 128 || (pair != 1 && pair != 2)) return 0;
+  if (pair == 2 ? N % 256 : N % 128) return 0;
+  if (fmt == MOE_W_MXFP4) return packed_weight_bytes(E, N, Kd, pair);
   return 0;
 }
 
-moe_status moe_pack_weight_scales(moe_wfmt fmt, const uint8_t* sf, int E, int N, int Kd, uint8_t* sf_packed,
-                                  void* stream) {
-  if (!sf || !sf_packed || E <= 0 || N <= 0 || Kd <= 0 || N % 128 || Kd % 128) return MOE_ERR_INVALID_ARG;
+moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair,
+                            uint8_t* packed, void* stream) {
+  if (!q || !sf || !packed || E <= 0 || N <= 0 || Kd <= 0 || Kd % 128) return MOE_ERR_INVALID_ARG;
+  if ((pair != 1 && pair != 2) || (pair == 2 ? N % 256 : N % 128)) return MOE_ERR_INVALID_ARG;
   if (fmt != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_pack_mx(sf, E * N, Kd, sf_packed, S(stream)));
+  return cuda_status(launch_pack_mx(q, sf, E, N, Kd, pair, packed, S(stream)));
 }
 
 moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size_t* bytes) {
@@ -127,7 +130,8 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
   if (!hidden || !w_gate || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
   if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
   if ((x_q == nullptr) != (x_sf == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (x_q && (!aligned(hidden, 8) || !aligned(x_q, 4))) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_gate, 16)) return MOE_ERR_INVALID_ARG;
+  if (x_q && !aligned(x_q, 4)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const int ns = route_nsplit(T > 0 ? T : 1, H, E);
   const size_t need = kAlign + static_cast<size_t>(ns) * T * E * sizeof(float);
@@ -162,7 +166,8 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
                               size_t ws_bytes, void* stream) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
-  if (!x || !x_sf || !expert_ids || !m_sum || !weight_ok(w)) return MOE_ERR_INVALID_ARG;
+  if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
+  if (!(l1 ? weight_ok(w, E, 2 * I, H, 2) : weight_ok(w, E, H, I, 1))) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(x_sf, 16)) return MOE_ERR_INVALID_ARG;
   if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
   if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
@@ -171,8 +176,7 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
   const size_t U = moe_msum_upper(T, K, E, align);
   if (U == 0) return MOE_OK;
   GemmLaunch L;
-  L.w_q = w.q;
-  L.w_sf = w.sf;
+  L.w = w.packed;
   L.x = x;
   L.x_sf = x_sf;
   L.expert_ids = expert_ids;
@@ -219,7 +223,8 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
                        float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                        int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
   if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
-  if (!hidden || !w_gate || !out || !weight_ok(w13) || !weight_ok(w2)) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !out || !weight_ok(w13, E, 2 * I, H, 2) || !weight_ok(w2, E, H, I, 1))
+    return MOE_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const WsLayout L = layout(T, H, I, E, K, align);

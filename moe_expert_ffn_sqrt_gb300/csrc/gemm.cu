@@ -6,22 +6,26 @@
 // TMEM accumulators, full/empty barrier pipeline, SwiGLU + amax -> UE8M0 -> E4M3 epilogue).
 //
 // Design (this file's own, for one GPU):
-//  * Weights are the MMA's M side (128 rows per tile) and tokens the N side (BN rows), so a
-//    3-row expert at decode costs an N=16 MMA, not a 128-row one.  L1 tiles hold the gate rows
-//    i0..i0+127 and the up rows I+i0..I+i0+127 in two accumulators, so one CTA sees both halves
-//    of SwiGLU and the full 128-wide requant group.
-//  * A work item is (row block of BN permuted rows, weight tile, expert).  BN divides the
-//    permute alignment in the common case, so a block holds one expert; otherwise each expert
-//    present in the block is a separate pass whose stores are masked by expert_ids.
-//  * Persistent CTAs (one per SM) walk the items in a fixed order; producer warp (TMA),
-//    MMA warp (one thread issues tcgen05.cp + tcgen05.mma) and four epilogue warps run
-//    decoupled through mbarriers; accumulators are double-buffered in TMEM when they fit.
-//  * FP4 weights are loaded with the padded 4-bit TMA type (each 16 codes -> 16 bytes of shared
-//    memory), 128-byte swizzle, which is the operand layout kind::mxf8f6f4 reads.
-//  * Scale factors: weight scales arrive pre-arranged (moe_pack_weight_scales) as one 512-byte
-//    32x(4x4 bytes) image per (128-row tile, 128-deep slab); token scales as the tiled layout.
-//    Both are copied into TMEM with tcgen05.cp .32x128b.warpx4.  Row m of the weight tile reads
-//    its scale from column (m/32), byte (k-step); token n from column (n/32), byte (slab % 4).
+//  * One MMA is M = 128 token rows x N = 256 weight rows x K = 32.  On this part a block-scaled
+//    M=128 MMA occupies the tensor pipe for about the same time at N = 16 as at N = 128, and an
+//    N = 256 one for ~1.3x that, so the weights go on the N side, 256 rows at a time: at decode
+//    (a handful of tokens per expert) the tensor pipe then moves weights at ~2x HBM speed.
+//    L1 tiles are 128 gate rows + the matching 128 up rows, so one thread (= one token, one TMEM
+//    lane) holds both SwiGLU halves and the whole 128-wide requant group of its row.
+//  * A work item is (row block of BN permuted rows, weight tile, expert).  Only the block's BN
+//    token rows are loaded; the MMA's other rows read unrelated shared memory and their results
+//    are never stored.  BN divides the permute alignment in the common case, so a block holds
+//    one expert; otherwise each expert in the block is a separate pass with masked stores.
+//  * Persistent CTAs (one per SM) walk the items in a fixed order; a producer warp (TMA), an MMA
+//    warp (one thread issues tcgen05.cp + tcgen05.mma) and four epilogue warps run decoupled
+//    through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
+//    the shared-memory ring keeps the weights streaming while the epilogue drains it.
+//  * Weights come pre-packed (moe_pack_weights): per (expert, tile, 128-deep slab) one chunk of
+//    256 rows of FP4 codes followed by two 512-byte scale images.  The codes are loaded with the
+//    padded 4-bit TMA type (16 codes -> 16 bytes of shared memory, 128-byte swizzle), the operand
+//    layout kind::mxf8f6f4 reads; the scale images go to TMEM with tcgen05.cp .32x128b.warpx4,
+//    where weight row n is read from column n/32 (byte = k-step) and token row m from column m/32
+//    (byte = slab % 4).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -33,52 +37,46 @@ namespace moe {
 constexpr int kGemmThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: accumulators in [0, 384); scale factors in [384, 512), every region starting
-// on a 16-column boundary (weight scales of the gate / up tiles and token scales, 2 slots each).
-constexpr uint32_t kAccCols = 384;
-constexpr uint32_t kSfaGate = 384;
-constexpr uint32_t kSfaUp = 416;
-constexpr uint32_t kSfbCol = 448;
+// TMEM columns: accumulator [0, 256); token scales 2 slots x 16 at 256; weight scales 2 x 16 at 288.
+constexpr uint32_t kSfaCol = 256;
+constexpr uint32_t kSfbCol = 288;
+constexpr int kTileRows = 256;           // weight rows per tile (MMA N)
 
 template <int BN, bool L1>
 struct GemmCfg {
-  static constexpr int NW = L1 ? 2 : 1;                          // weight tiles per stage
-  static constexpr int W_BYTES = 16384;                          // 128 x 128 codes, padded
-  static constexpr int X_BYTES = BN * 128;
-  static constexpr int SFA_OFF = NW * W_BYTES + X_BYTES;
-  static constexpr int SFB_OFF = SFA_OFF + NW * 512;
-  static constexpr int STAGE_RAW = SFB_OFF + 512;
-  static constexpr int STAGE = (STAGE_RAW + 1023) / 1024 * 1024;
-  static constexpr int EXTRA = 4096;                             // barriers, reductions, flags
+  static constexpr int X_BYTES = BN * 128;                       // token rows loaded per slab
+  static constexpr int X_SLOT = (X_BYTES + 1023) / 1024 * 1024;  // MMA reads 16 KB from here
+  static constexpr int W_OFF = X_SLOT;
+  static constexpr int W_BYTES = kTileRows * 128;                // 256 rows of padded FP4 codes
+  static constexpr int SFB_OFF = W_OFF + W_BYTES;                // weight scale images (2 x 512 B)
+  static constexpr int SFA_OFF = SFB_OFF + 1024;                 // token scale chunk (every 4th slab)
+  static constexpr int SFA_BYTES = 512;
+  static constexpr int STAGE = (SFA_OFF + SFA_BYTES + 1023) / 1024 * 1024;
+  static constexpr int EXTRA = 1024;                             // barriers and flags
   static constexpr int S_FIT = (kSmemBudget - EXTRA - 1024) / STAGE;
   static constexpr int STAGES = S_FIT > 8 ? 8 : S_FIT;
-  static constexpr int UP_OFF = (BN + 31) / 32 * 32;            // column offset of the up accumulator
-  static constexpr int ACC_COLS = NW * UP_OFF;                   // columns per accumulator buffer
-  static constexpr int NBUF = (2 * ACC_COLS <= (int)kAccCols) ? 2 : 1;
-  static constexpr int SFB_BYTES = 512;                          // one token-scale chunk
   static constexpr int SMEM = 1024 + STAGES * STAGE + EXTRA;
-  static constexpr uint32_t TX_W = 8192;                         // global bytes of one FP4 tile
-  static_assert(STAGES >= 2, "shared memory too small for two stages");
-  static_assert(ACC_COLS * NBUF <= (int)kAccCols, "accumulators overlap the scale columns");
+  static constexpr uint32_t TX_W = kTileRows * 64;               // global bytes of the FP4 box
+  static constexpr size_t W_CHUNK = 2 * (8192 + 512);            // packed bytes per (tile, slab)
+  static_assert(STAGES >= 3, "shared memory too small");
+  static_assert(X_SLOT + 16384 <= STAGE, "MMA A reads must stay inside the stage");
 };
 
 struct GemmArgs {
-  const uint8_t* w_sf;          // packed weight scale images
-  const uint8_t* x_sf;          // tiled token scales (rows U)
+  const uint8_t* w;             // packed weight stream
+  const uint8_t* x_sf;          // tiled token scales (rows U, block rows BN)
   const int32_t* expert_ids;    // [U]
   const int32_t* m_sum;         // [1]
   uint8_t* h_q;                 // L1 out [U, I]
   uint8_t* h_sf;                // L1 out, tiled (rows U, slabs I/128)
   uint16_t* y;                  // L2 out [U, H] bf16
   uint32_t* status;
-  size_t w_sf_bytes;            // sizes, for the kernel's own bounds checks
+  size_t w_bytes;               // sizes, for the kernel's own bounds checks
   size_t x_sf_bytes;
   int n_slabs;                  // reduction depth / 128
-  int w_rows;                   // rows per expert in the weight tensor (2I or H)
-  int n_wt;                     // weight tiles per item row (I/128 or H/128)
-  int up_off;                   // L1: I (row offset of the up half)
+  int n_wt;                     // weight tiles per expert
   int out_cols;                 // L1: I, L2: H
-  int sf_nb;                    // blocks of the tiled token-scale layouts (rows U, block rows BN)
+  int sf_nb;                    // blocks of the tiled token-scale layouts
   int n_tiles;                  // ceil(U/BN) * n_wt
 };
 
@@ -103,6 +101,11 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, i
   return false;
 }
 
+// silu(g) * u with the fast exponential and division intrinsics: the result is requantised to
+// E4M3 (3 mantissa bits), far coarser than their few-ulp error, and unlike the IEEE division they
+// have no slow path for the infinities that unused accumulator rows may hold.
+__device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
 template <int BN, bool L1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
@@ -115,11 +118,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(extra);
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(extra + 256);              // [4][BN] warp partial maxima
-  uint8_t* row_ok = extra + 256 + 4 * BN * 4;                      // [BN]
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -127,10 +128,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(acc_full + b), 1);
-      mbar_init(smem_u32(acc_empty + b), 128);
-    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 128);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_w);
@@ -155,8 +154,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int t = blockIdx.x, e = -1;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
       const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
-      const int wrow = e * a.w_rows + wt * 128;
-      const size_t sfa_chunk = static_cast<size_t>(wrow / 128) * a.n_slabs;
+      const size_t chunk0 = (static_cast<size_t>(e) * a.n_wt + wt) * a.n_slabs;
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
@@ -164,29 +162,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) {
           uint8_t* st = stages + stage * C::STAGE;
           const uint32_t fb = smem_u32(full + stage);
-          const int urow = wrow + a.up_off;
-          const size_t sfa_g = (sfa_chunk + s) * 512;
-          const size_t sfa_u = (static_cast<size_t>(urow / 128) * a.n_slabs + s) * 512;
-          const size_t sfb = (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
-          // self-check: every bulk copy inside its buffer and 16-byte aligned
-          const bool good = sfa_g + 512 <= a.w_sf_bytes && (!L1 || sfa_u + 512 <= a.w_sf_bytes) &&
-                            ((s & 3) != 0 || sfb + C::SFB_BYTES <= a.x_sf_bytes) &&
-                            ((reinterpret_cast<uintptr_t>(a.w_sf) | reinterpret_cast<uintptr_t>(a.x_sf)) & 15) == 0;
+          const size_t wbase = (chunk0 + s) * C::W_CHUNK;
+          const size_t sfa = (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
+          // self-check: every copy inside its buffer and 16-byte aligned
+          const bool good = wbase + C::W_CHUNK <= a.w_bytes &&
+                            ((s & 3) != 0 || sfa + C::SFA_BYTES <= a.x_sf_bytes) &&
+                            ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x_sf)) & 15) == 0;
           if (!good) {
             record_error(a.status, kDevErrCheck);
             *abort_flag = 1;
           } else {
-            uint32_t bytes = C::NW * (C::TX_W + 512) + C::X_BYTES;
-            if ((s & 3) == 0) bytes += C::SFB_BYTES;
+            uint32_t bytes = C::TX_W + 1024 + C::X_BYTES;
+            if ((s & 3) == 0) bytes += C::SFA_BYTES;
             mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(smem_u32(st), &tmap_w, s * 128, wrow, fb, pol_w);
-            bulk_load(smem_u32(st + C::SFA_OFF), a.w_sf + sfa_g, 512, fb);
-            if (L1) {
-              tma_load_2d(smem_u32(st + C::W_BYTES), &tmap_w, s * 128, urow, fb, pol_w);
-              bulk_load(smem_u32(st + C::SFA_OFF + 512), a.w_sf + sfa_u, 512, fb);
-            }
-            tma_load_2d(smem_u32(st + C::NW * C::W_BYTES), &tmap_x, s * 128, r0, fb, pol_x);
-            if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFB_OFF), a.x_sf + sfb, C::SFB_BYTES, fb);
+            tma_load_2d(smem_u32(st + C::W_OFF), &tmap_w, 0, static_cast<int>(wbase / 64), fb, pol_w);
+            bulk_load(smem_u32(st + C::SFB_OFF), a.w + wbase + C::TX_W, 1024, fb);
+            tma_load_2d(smem_u32(st), &tmap_x, s * 128, r0, fb, pol_x);
+            if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFA_OFF), a.x_sf + sfa, C::SFA_BYTES, fb);
           }
         }
         __syncwarp();
@@ -208,35 +200,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // ---------------- MMA issuer (whole warp iterates, lane 0 issues) ----------------
     int stage = 0;
     uint32_t phase = 0;
-    int buf = 0;
     uint32_t acc_phase = 0;
     int t = blockIdx.x, e = -1;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty + buf), acc_phase ^ 1, a.status));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
-        const uint32_t acc = tmem + buf * C::ACC_COLS;
         for (int s = 0; s < a.n_slabs; ++s) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + stage), phase, a.status));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
             const uint32_t st = smem_u32(stages + stage * C::STAGE);
-            const uint32_t sfa = tmem + kSfaGate + (s & 1) * 16;
-            const uint32_t sfu = tmem + kSfaUp + (s & 1) * 16;
-            const uint32_t sfb = tmem + kSfbCol + ((s >> 2) & 1) * 16;
-            tc_cp_32x128b_x4(sfa, smem_desc(st + C::SFA_OFF, 0, 128, 0));
-            if (L1) tc_cp_32x128b_x4(sfu, smem_desc(st + C::SFA_OFF + 512, 0, 128, 0));
-            if ((s & 3) == 0) tc_cp_32x128b_x4(sfb, smem_desc(st + C::SFB_OFF, 0, 128, 0));
-            const uint32_t xs = st + C::NW * C::W_BYTES;
+            const uint32_t sfa = tmem + kSfaCol + ((s >> 2) & 1) * 16;
+            const uint32_t sfb = tmem + kSfbCol + (s & 1) * 16;
+            if ((s & 3) == 0) tc_cp_32x128b_x4(sfa, smem_desc(st + C::SFA_OFF, 0, 128, 0));
+            tc_cp_32x128b_x4(sfb, smem_desc(st + C::SFB_OFF, 0, 128, 0));
+            tc_cp_32x128b_x4(sfb + 4, smem_desc(st + C::SFB_OFF + 512, 0, 128, 0));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint32_t id = idesc_mxf8f6f4(5, 0, 128, BN, k, s & 3);
-              const uint32_t accum = (s > 0 || k > 0) ? 1u : 0u;
-              mma_mxf8f6f4(acc, desc_sw128(st + k * 32), desc_sw128(xs + k * 32), id, sfa, sfb, accum);
-              if (L1)
-                mma_mxf8f6f4(acc + C::UP_OFF, desc_sw128(st + C::W_BYTES + k * 32), desc_sw128(xs + k * 32), id, sfu,
-                             sfb, accum);
+              const uint32_t id = idesc_mxf8f6f4(0, 5, 128, kTileRows, s & 3, k);
+              mma_mxf8f6f4(tmem, desc_sw128(st + k * 32), desc_sw128(st + C::W_OFF + k * 32), id, sfa, sfb,
+                           (s > 0 || k > 0) ? 1u : 0u);
             }
             tc_commit(smem_u32(empty + stage));
           }
@@ -251,93 +236,97 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         break;
       }
-      if (lane == 0) tc_commit(smem_u32(acc_full + buf));
+      if (lane == 0) tc_commit(smem_u32(acc_full));
       __syncwarp();
-      if (++buf == C::NBUF) {
-        buf = 0;
-        acc_phase ^= 1;
-      }
+      acc_phase ^= 1;
     }
   } else {
-    // ---------------- epilogue (warps 2..5, 128 threads) ----------------
+    // ---------------- epilogue (warps 2..5): thread = token row m of the block ----------------
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;           // weight row within the tile (L1: i, L2: output col)
-    const int et = threadIdx.x - 64;         // 0..127
-    int buf = 0;
+    const int m = q * 32 + lane;
+    const bool warp_has_rows = q * 32 < BN;  // warp-uniform
+    const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0;
     int t = blockIdx.x, e = -1;
     while (next_item<BN>(a, msum, t, e)) {
       const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
-      if (et < BN) row_ok[et] = (r0 + et < msum && __ldg(a.expert_ids + r0 + et) == e) ? 1 : 0;
-      bool ok = mbar_wait(smem_u32(acc_full + buf), acc_phase, a.status) && *abort_flag == 0;
-      // one vote over the four epilogue warps (also orders the row_ok writes before their reads)
-      ok = named_barrier_and(1, 128, ok);
+      const int row = r0 + m;
+      const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == e;
+      bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+      ok = named_barrier_and(1, 128, ok);    // one vote over the four epilogue warps
       if (!ok) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t acc = tmem + buf * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       if (L1) {
-        // pass 1: per-token amax of h over the 128 rows of this tile
-        for (int n0 = 0; n0 < BN; n0 += 16) {
-          uint32_t g[16], u[16];
-          tc_ld_x16(acc + n0, g);
-          tc_ld_x16(acc + C::UP_OFF + n0, u);
-          tc_wait_ld();
+        // h = silu(gate) * up for the 128 columns of this tile, kept in registers so that the
+        // accumulator is released before the quantise-and-store part
+        float h[128];
+        float amax = 0.f;
+        if (warp_has_rows) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float gv = __uint_as_float(g[j]);
-            float m = fabsf(gv / (1.0f + expf(-gv)) * __uint_as_float(u[j]));
+          for (int c0 = 0; c0 < 128; c0 += 16) {
+            uint32_t g[16], u[16];
+            tc_ld_x16(acc + c0, g);
+            tc_ld_x16(acc + 128 + c0, u);
+            tc_wait_ld();
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) red[q * BN + n0 + j] = m;
+            for (int j = 0; j < 16; ++j) {
+              h[c0 + j] = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
+              amax = fmaxf(amax, fabsf(h[c0 + j]));
+            }
           }
         }
-        named_barrier(1, 128);
-        if (et < BN && row_ok[et]) {
-          const float am = fmaxf(fmaxf(red[et], red[BN + et]), fmaxf(red[2 * BN + et], red[3 * BN + et]));
-          a.h_sf[act_sf_offset(BN, a.sf_nb, r0 + et, wt)] = static_cast<uint8_t>(ue8m0_exponent(am) + 127);
-        }
-        // pass 2: quantise and store
-        for (int n0 = 0; n0 < BN; n0 += 16) {
-          uint32_t g[16], u[16];
-          tc_ld_x16(acc + n0, g);
-          tc_ld_x16(acc + C::UP_OFF + n0, u);
-          tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc_empty));
+        if (mine) {
+          const int ex = ue8m0_exponent(amax);
+          const float sc = pow2_neg(ex);
+          a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+          uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = n0 + j;
-            if (!row_ok[n]) continue;
-            const float am = fmaxf(fmaxf(red[n], red[BN + n]), fmaxf(red[2 * BN + n], red[3 * BN + n]));
-            const float sc = pow2_neg(ue8m0_exponent(am));
-            const float gv = __uint_as_float(g[j]);
-            const float h = gv / (1.0f + expf(-gv)) * __uint_as_float(u[j]);
-            const __nv_fp8x2_storage_t p = __nv_cvt_float2_to_fp8x2(make_float2(h * sc, 0.f), __NV_SATFINITE, __NV_E4M3);
-            a.h_q[static_cast<size_t>(r0 + n) * a.out_cols + wt * 128 + row] = static_cast<uint8_t>(p & 0xFF);
+          for (int c0 = 0; c0 < 128; c0 += 16) {
+            uint32_t packed[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int c = c0 + 4 * j;
+              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi =
+                  __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
+              packed[j] = lo | (hi << 16);
+            }
+            dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
         }
       } else {
-        for (int n0 = 0; n0 < BN; n0 += 16) {
-          uint32_t v[16];
-          tc_ld_x16(acc + n0, v);
-          tc_wait_ld();
+        // 256 outputs as bf16 pairs in registers, accumulator released, then stored
+        uint32_t packed[128];
+        const int ncols = min(kTileRows, a.out_cols - wt * kTileRows);
+        if (warp_has_rows) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int n = n0 + j;
-            if (!row_ok[n]) continue;
-            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(v[j]));
-            a.y[static_cast<size_t>(r0 + n) * a.out_cols + wt * 128 + row] = __bfloat16_as_ushort(b);
+          for (int c0 = 0; c0 < kTileRows; c0 += 16) {
+            uint32_t v[16];
+            tc_ld_x16(acc + c0, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j])));
+              const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j + 1])));
+              packed[c0 / 2 + j] = lo | (hi << 16);
+            }
           }
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc_empty));
+        if (mine) {
+          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kTileRows);
+#pragma unroll
+          for (int c = 0; c < kTileRows / 8; ++c)
+            if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        }
       }
-      tc_fence_before();
-      named_barrier(1, 128);               // row_ok / red reuse on the next item
-      mbar_arrive(smem_u32(acc_empty + buf));
-      if (++buf == C::NBUF) {
-        buf = 0;
-        acc_phase ^= 1;
-      }
+      acc_phase ^= 1;
     }
   }
   tc_fence_before();
@@ -392,16 +381,25 @@ int num_sms() {
   return n;
 }
 
+int weight_tiles(int N, int pair) { return pair == 2 ? N / kTileRows : (N + kTileRows - 1) / kTileRows; }
+
+size_t packed_weight_bytes(int E, int N, int Kd, int pair) {
+  return static_cast<size_t>(E) * weight_tiles(N, pair) * (Kd / 128) * (2 * (8192 + 512));
+}
+
 template <int BN, bool L1>
 static cudaError_t launch_gemm_t(const GemmLaunch& L, cudaStream_t stream) {
   using C = GemmCfg<BN, L1>;
   CUtensorMap mw, mx;
-  const int E_rows = L.E * L.w_rows;
-  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L.w_q, L.Kd, E_rows, L.Kd / 2, 128, 128))
+  const int n_slabs = L.Kd / 128;
+  const int n_wt = weight_tiles(L.w_rows, L1 ? 2 : 1);
+  const size_t w_bytes = packed_weight_bytes(L.E, L.w_rows, L.Kd, L1 ? 2 : 1);
+  // the packed stream viewed as rows of 128 FP4 codes (64 bytes); a box is 256 rows
+  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L.w, 128, w_bytes / 64, 64, 128, kTileRows))
     return cudaErrorInvalidValue;
   if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN)) return cudaErrorInvalidValue;
   GemmArgs a;
-  a.w_sf = L.w_sf;
+  a.w = L.w;
   a.x_sf = L.x_sf;
   a.expert_ids = L.expert_ids;
   a.m_sum = L.m_sum;
@@ -409,12 +407,10 @@ static cudaError_t launch_gemm_t(const GemmLaunch& L, cudaStream_t stream) {
   a.h_sf = L.h_sf;
   a.y = L.y;
   a.status = L.status;
-  a.w_sf_bytes = static_cast<size_t>(L.E) * L.w_rows * (L.Kd / 32);
+  a.w_bytes = w_bytes;
   a.x_sf_bytes = act_sf_bytes(L.U, L.Kd / 128, BN);
-  a.n_slabs = L.Kd / 128;
-  a.w_rows = L.w_rows;
-  a.n_wt = L1 ? L.I / 128 : L.w_rows / 128;
-  a.up_off = L1 ? L.I : 0;
+  a.n_slabs = n_slabs;
+  a.n_wt = n_wt;
   a.out_cols = L1 ? L.I : L.w_rows;
   a.sf_nb = act_sf_blocks(L.U, BN);
   const int nrb = (L.U + BN - 1) / BN;
@@ -449,27 +445,43 @@ cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream) {
 }
 
 // ------------------------------------------------------------------------------------------
-// Weight scale packing: logical [E*N, Kd/32] UE8M0 -> per (128-row tile, 128-deep slab) a
-// 512-byte image whose byte l*16 + w*4 + b holds row (32w + l), k-block (4*slab + b).
-__global__ void pack_mx_scales_kernel(const uint8_t* __restrict__ sf, int rows, int kblocks,
-                                      uint8_t* __restrict__ out) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(rows) * kblocks;
-  if (i >= total) return;
-  const int nslab = kblocks / 4;
-  const long long chunk = i / 512;
-  const int within = static_cast<int>(i % 512);
-  const int rt = static_cast<int>(chunk / nslab), s = static_cast<int>(chunk % nslab);
-  const int l = within / 16, w = (within / 4) & 3, b = within & 3;
-  const int r = rt * 128 + w * 32 + l;
-  out[i] = sf[static_cast<size_t>(r) * kblocks + s * 4 + b];
+// Weight packing (once per weight tensor): logical codes [E, N, Kd/2] and UE8M0 scales
+// [E, N, Kd/32] -> a stream of chunks, one per (expert, 256-row tile, 128-deep slab), in the order
+// the GEMM reads them.  A tile is two halves of 128 rows: pair = 2 (W13) joins the gate rows
+// 128t.. with the up rows N/2 + 128t..; pair = 1 (W2) takes rows 256t .. 256t+255 (rows past N
+// are zero codes with scale 1).  Chunk = 2 x [128 rows x 64 B codes], then 2 x 512-byte scale
+// images whose byte l*16 + w*4 + b holds the scale of half-row (32w + l), k-block (4*slab + b):
+// the layout tcgen05.cp .32x128b.warpx4 turns into "row n at TMEM column n/32, byte = k-step".
+__global__ void pack_mx_weights_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int E, int N,
+                                       int Kd, int pair, uint8_t* __restrict__ out) {
+  const size_t chunk_bytes = 2 * (8192 + 512);
+  const int n_slabs = Kd / 128, n_wt = pair == 2 ? N / kTileRows : (N + kTileRows - 1) / kTileRows;
+  const size_t total = static_cast<size_t>(E) * n_wt * n_slabs * chunk_bytes;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const size_t c = i / chunk_bytes;
+    const int o = static_cast<int>(i % chunk_bytes);
+    const int s = static_cast<int>(c % n_slabs);
+    const size_t ew = c / n_slabs;
+    const int wt = static_cast<int>(ew % n_wt), e = static_cast<int>(ew / n_wt);
+    if (o < 2 * 8192) {
+      const int h = o / 8192, m = (o % 8192) / 64, j = o % 64;
+      const int r = pair == 2 ? h * (N / 2) + wt * 128 + m : wt * 256 + h * 128 + m;
+      out[i] = r < N ? q[(static_cast<size_t>(e) * N + r) * (Kd / 2) + s * 64 + j] : 0;
+    } else {
+      const int o2 = o - 2 * 8192;
+      const int h = o2 / 512, within = o2 % 512;
+      const int l = within / 16, w = (within / 4) & 3, b = within & 3;
+      const int mm = 32 * w + l;
+      const int r = pair == 2 ? h * (N / 2) + wt * 128 + mm : wt * 256 + h * 128 + mm;
+      out[i] = r < N ? sf[(static_cast<size_t>(e) * N + r) * (Kd / 32) + s * 4 + b] : 127;
+    }
+  }
 }
 
-cudaError_t launch_pack_mx(const uint8_t* sf, int rows, int Kd, uint8_t* out, cudaStream_t stream) {
-  const int kblocks = Kd / 32;
-  const long long total = static_cast<long long>(rows) * kblocks;
-  if (total == 0) return cudaSuccess;
-  pack_mx_scales_kernel<<<static_cast<int>((total + 255) / 256), 256, 0, stream>>>(sf, rows, kblocks, out);
+cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
+                           cudaStream_t stream) {
+  pack_mx_weights_kernel<<<4 * num_sms(), 256, 0, stream>>>(q, sf, E, N, Kd, pair, out);
   return cudaGetLastError();
 }
 

@@ -22,8 +22,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
 
 // gemm.cu
 struct GemmLaunch {
-  const uint8_t* w_q;          // [E, w_rows, Kd/2]
-  const uint8_t* w_sf;         // packed scales
+  const uint8_t* w;            // packed weight stream
   const uint8_t* x;            // [U, Kd] E4M3
   const uint8_t* x_sf;         // tiled (rows U, slabs Kd/128)
   const int32_t* expert_ids;
@@ -35,9 +34,12 @@ struct GemmLaunch {
   int E, w_rows, Kd, I, U, align;
 };
 int num_sms();
+int weight_tiles(int N, int pair);
+size_t packed_weight_bytes(int E, int N, int Kd, int pair);
 int gemm_block_n(int align);
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
-cudaError_t launch_pack_mx(const uint8_t* sf, int rows, int Kd, uint8_t* out, cudaStream_t stream);
+cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
+                           cudaStream_t stream);
 
 // reduce.cu
 cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int T, int K,

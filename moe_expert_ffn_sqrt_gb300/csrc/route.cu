@@ -63,10 +63,87 @@ __global__ void __launch_bounds__(256) gate_gemm_kernel(const uint16_t* __restri
 }
 
 // ------------------------------------------------------------------------------------------
-// Top-K (one warp per token; lane holds experts lane, lane+32, ...) and FP8 activation
-// quantisation (one warp per 128-column group), in one launch.
-constexpr int kMaxEPerLane = 32;   // E <= 1024
+// Gate GEMV for small batches (T <= kGemvT): CTA = 4 experts x one quarter of H; each thread
+// walks 8-column groups of its quarter, all T tokens at once; block reduction at the end.
+// partial[split][t][e] as for the tiled kernel (4 splits).
+constexpr int kGemvT = 16;
+constexpr int kGemvE = 4;
+constexpr int kGemvSplit = 4;
 
+template <int TT>
+__global__ void __launch_bounds__(256) gate_gemv_kernel(const uint16_t* __restrict__ hidden,
+                                                        const float* __restrict__ wg, int T, int H, int E,
+                                                        float* __restrict__ partial) {
+  __shared__ float red[8][kGemvE * TT];
+  const int e0 = blockIdx.x * kGemvE, split = blockIdx.y;
+  const int hq = H / kGemvSplit;                     // multiple of 32 (H multiple of 128)
+  const int hbeg = split * hq;
+  float acc[kGemvE][TT];
+#pragma unroll
+  for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[i][t] = 0.f;
+  for (int h = hbeg + threadIdx.x * 8; h < hbeg + hq; h += 256 * 8) {
+    float w[kGemvE][8];
+#pragma unroll
+    for (int i = 0; i < kGemvE; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h));
+        const float4 b = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h + 4));
+        w[i][0] = a.x; w[i][1] = a.y; w[i][2] = a.z; w[i][3] = a.w;
+        w[i][4] = b.x; w[i][5] = b.y; w[i][6] = b.z; w[i][7] = b.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[i][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      if (t < T) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H + h));
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        float xv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xv[2 * j] = __uint_as_float(xw[j] << 16);
+          xv[2 * j + 1] = __uint_as_float(xw[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][t] = fmaf(xv[j], w[i][j], acc[i][t]);
+      }
+    }
+  }
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+  for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      float v = acc[i][t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) red[warp][i * TT + t] = v;
+    }
+  __syncthreads();
+  for (int j = threadIdx.x; j < kGemvE * TT; j += 256) {
+    const int i = j / TT, t = j % TT, e = e0 + i;
+    if (t < T && e < E) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += red[w][j];
+      partial[(static_cast<size_t>(split) * T + t) * E + e] = v;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Top-K: one CTA (256 threads) per token.  Threads sum the split partials of one expert each
+// (independent loads, fixed split order), score, and stage scores/keys in shared memory; warp 0
+// then holds PER = E/32 keys per lane in registers and runs K rounds of warp arg-max (ties to
+// the lower expert id).  FP8 activation quantisation (one warp per 128-column group) runs in
+// the blocks after the top-K blocks of the same launch.
 struct RouteFinishArgs {
   const float* partial;
   int nsplit;
@@ -96,83 +173,94 @@ __device__ __forceinline__ void warp_argmax(float& key, int& id) {
   }
 }
 
+__device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float r = sh[0];
+  for (int w = 1; w < 8; ++w) r = is_max ? fmaxf(r, sh[w]) : r + sh[w];
+  return r;
+}
+
+template <int PER>
 __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs a) {
+  __shared__ float s_score[32 * PER];
+  __shared__ float s_key[32 * PER];
+  __shared__ float s_red[8];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (static_cast<int>(blockIdx.x) < a.topk_blocks) {
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= a.T) return;
-    const int per = (a.E + 31) / 32;
-    float s[kMaxEPerLane], key[kMaxEPerLane];
+    const int t = blockIdx.x;
+    // logits: one expert per thread per pass, splits summed in a fixed order
     float lmax = -INFINITY;
-    for (int j = 0; j < per; ++j) {
-      const int e = lane + 32 * j;
+    for (int e = threadIdx.x; e < 32 * PER; e += 256) {
       float l = -INFINITY;
       if (e < a.E) {
-        l = 0.f;
-        for (int sp = 0; sp < a.nsplit; ++sp) l += a.partial[(static_cast<size_t>(sp) * a.T + t) * a.E + e];
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        int sp = 0;
+        for (; sp + 4 <= a.nsplit; sp += 4)
+#pragma unroll
+          for (int u = 0; u < 4; ++u) v[u] += a.partial[(static_cast<size_t>(sp + u) * a.T + t) * a.E + e];
+        l = (v[0] + v[1]) + (v[2] + v[3]);
+        for (; sp < a.nsplit; ++sp) l += a.partial[(static_cast<size_t>(sp) * a.T + t) * a.E + e];
         if (a.gate_bias) l += a.gate_bias[e];
         if (a.logits_out) a.logits_out[static_cast<size_t>(t) * a.E + e] = l;
       }
-      s[j] = l;
+      s_score[e] = l;
       lmax = fmaxf(lmax, l);
     }
     if (a.score_fn == 0) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+      lmax = block_reduce(lmax, s_red, true);
       float sum = 0.f;
-      for (int j = 0; j < per; ++j) {
-        const int e = lane + 32 * j;
-        s[j] = (e < a.E) ? expf(s[j] - lmax) : 0.f;
-        sum += s[j];
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
+        const float p = (e < a.E) ? expf(s_score[e] - lmax) : 0.f;
+        s_score[e] = p;
+        sum += p;
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-      for (int j = 0; j < per; ++j) s[j] = s[j] / sum;
+      sum = block_reduce(sum, s_red, false);
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) s_score[e] = s_score[e] / sum;
     } else {
-      for (int j = 0; j < per; ++j) {
-        const float l = s[j];
-        s[j] = (lane + 32 * j < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
+        const float l = s_score[e];
+        s_score[e] = (e < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
       }
     }
-    for (int j = 0; j < per; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (e < a.E) ? s[j] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
-    }
-    float wsel[32];
-    float wsum = 0.f;
+    for (int e = threadIdx.x; e < 32 * PER; e += 256)
+      s_key[e] = (e < a.E) ? s_score[e] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
+    __syncthreads();
+    if (warp != 0) return;
+    float key[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) key[j] = s_key[lane + 32 * j];
+    float wsum = 0.f, wmine = 0.f;
     for (int k = 0; k < a.K; ++k) {
-      // best candidate of this lane (ties: lower id, i.e. lower j)
       float bk = -INFINITY;
       int bi = 0x7fffffff;
-      for (int j = 0; j < per; ++j) {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
         const int e = lane + 32 * j;
-        if (e < a.E && (key[j] > bk || (key[j] == bk && e < bi))) {
+        if (key[j] > bk || (key[j] == bk && e < bi)) {
           bk = key[j];
           bi = e;
         }
       }
       warp_argmax(bk, bi);
-      // owner lane removes the winner and publishes its unbiased score
-      float sw = 0.f;
       if ((bi & 31) == lane) {
-        const int j = bi >> 5;
-        for (int jj = 0; jj < per; ++jj)
-          if (jj == j) {
-            sw = s[jj];
-            key[jj] = -INFINITY;
-          }
+#pragma unroll
+        for (int j = 0; j < PER; ++j)
+          if (j == (bi >> 5)) key[j] = -INFINITY;
       }
-      sw = __shfl_sync(0xffffffffu, sw, bi & 31);
-      if (k < 32) wsel[k] = sw;
+      const float sw = s_score[bi];
       wsum += sw;
+      if (lane == k) wmine = sw;
       if (lane == 0) a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
     }
-    if (lane == 0) {
-      for (int k = 0; k < a.K; ++k) {
-        const float w = a.renormalize ? wsel[k] / wsum : wsel[k];
-        a.topk_w[static_cast<size_t>(t) * a.K + k] = w;
-      }
-    }
+    if (lane < a.K) a.topk_w[static_cast<size_t>(t) * a.K + lane] = a.renormalize ? wmine / wsum : wmine;
     return;
   }
   // FP8 activation quantisation: group g of token t = 128 columns, 4 per lane.
@@ -199,6 +287,7 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
 }
 
 int route_nsplit(int T, int H, int E) {
+  if (T <= kGemvT) return kGemvSplit;
   const int tiles = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
   int ns = (2 * 152 + tiles - 1) / tiles;
   const int maxs = (H + 127) / 128;
@@ -212,10 +301,18 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
                          cudaStream_t stream) {
   const int ns = route_nsplit(T, H, E);
-  int hps = (H + ns - 1) / ns;
-  hps = (hps + GH - 1) / GH * GH;
-  dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
-  gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
+  if (T <= kGemvT) {
+    dim3 g0((E + kGemvE - 1) / kGemvE, kGemvSplit);
+    if (T <= 8)
+      gate_gemv_kernel<8><<<g0, 256, 0, stream>>>(hidden, w_gate, T, H, E, partial);
+    else
+      gate_gemv_kernel<16><<<g0, 256, 0, stream>>>(hidden, w_gate, T, H, E, partial);
+  } else {
+    int hps = (H + ns - 1) / ns;
+    hps = (hps + GH - 1) / GH * GH;
+    dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
+    gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
+  }
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   RouteFinishArgs a;
@@ -235,10 +332,16 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
   a.hidden = hidden;
   a.x_q = x_q;
   a.x_sf = x_sf;
-  a.topk_blocks = (T + 7) / 8;
+  a.topk_blocks = T;
   const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;
-  const int qblocks = static_cast<int>((qgroups + 7) / 8);
-  route_finish_kernel<<<a.topk_blocks + qblocks, 256, 0, stream>>>(a);
+  const int blocks = T + static_cast<int>((qgroups + 7) / 8);
+  const int per = (E + 31) / 32;
+  if (per <= 1) route_finish_kernel<1><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 2) route_finish_kernel<2><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 4) route_finish_kernel<4><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 8) route_finish_kernel<8><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 16) route_finish_kernel<16><<<blocks, 256, 0, stream>>>(a);
+  else route_finish_kernel<32><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -40,9 +40,9 @@ def host_bits(t):
 
 def device_weights(M, stack, fmt):
     w13 = M.Weight(dev(stack["w13_q"]), dev(stack["w13_sf"]),
-                   None if stack["w13_ts"] is None else dev(stack["w13_ts"]), fmt)
+                   None if stack["w13_ts"] is None else dev(stack["w13_ts"]), fmt, pair=2)
     w2 = M.Weight(dev(stack["w2_q"]), dev(stack["w2_sf"]),
-                  None if stack["w2_ts"] is None else dev(stack["w2_ts"]), fmt)
+                  None if stack["w2_ts"] is None else dev(stack["w2_ts"]), fmt, pair=1)
     return w13, w2
 
 

@@ -37,7 +37,10 @@ def test_sizes(M):
     assert M.msum_upper(8, 6, 256, 16) == 3888
     assert M.msum_upper(3, 2, 3, 1) == 6
     assert M.act_sf_block_rows(1) == 16 and M.act_sf_block_rows(64) == 64 and M.act_sf_block_rows(256) == 128
-    assert M.weight_sf_packed_bytes("mxfp4", 2, 256, 512) == 2 * 256 * 16
+    # 256-row tiles: W13 [2, 512, 512] pairs rows (gate, up); W2 [2, 384, 256] has a half-empty last tile
+    assert M.weight_packed_bytes("mxfp4", 2, 512, 512, 2) == 2 * 512 * (256 + 16)
+    assert M.weight_packed_bytes("mxfp4", 2, 384, 256, 1) == 2 * 2 * 2 * 2 * (8192 + 512)
+    assert M.weight_packed_bytes("mxfp4", 2, 384, 256, 2) == 0
     n = M.workspace_size(8, 7168, 2048, 256, 6, 16)
     assert n > 3888 * 7168  # holds the permuted activations
 
@@ -97,17 +100,22 @@ def test_invalid_arguments_are_rejected(M):
     # unsupported number of experts for the permute kernel
     assert L.moe_permute(fake, 8, 2, 4096, 16, fake, fake, fake, fake, None, None, None, 0, None, None, ws, 4096,
                          None) == M.ERR_UNSUPPORTED
-    w = M._Weight(0x10000, 0x20000, None, M.W_MXFP4)
+    w = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 2)
     # misaligned weight pointer
-    wbad = M._Weight(0x10010, 0x20000, None, M.W_MXFP4)
+    wbad = M._Weight(0x10010, None, M.W_MXFP4, 16, 512, 512, 2)
     assert L.moe_grouped_gemm_l1_swiglu(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wbad, fake, fake, ws, 4096,
                                         None) == M.ERR_INVALID_ARG
+    # W13 must be packed with pair = 2 and the matching shape
+    wpair = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 1)
+    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wpair, fake, fake, ws, 4096,
+                                        None) == M.ERR_INVALID_ARG
     # NVFP4 needs a tensor scale pointer
-    wnv = M._Weight(0x10000, 0x20000, None, M.W_NVFP4)
+    wnv = M._Weight(0x10000, None, M.W_NVFP4, 16, 512, 256, 1)
     assert L.moe_grouped_gemm_l2(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wnv, fake, ws, 4096,
                                  None) == M.ERR_INVALID_ARG
     # forward with a workspace smaller than moe_workspace_size
-    assert L.moe_forward(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, w, w, fake, None, None, None, None,
+    w2 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 256, 1)
+    assert L.moe_forward(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, w, w2, fake, None, None, None, None,
                          None, None, ws, 1024, None) == M.ERR_WORKSPACE
     # unpermute-reduce with H not a multiple of 8
     assert L.moe_unpermute_reduce(fake, fake, fake, 2, 2, 12, fake, None) == M.ERR_INVALID_ARG
