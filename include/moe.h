@@ -143,6 +143,21 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
                      int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
                      uint8_t* x_q, uint8_t* x_sf, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route without a workspace and without allocating anything.  This call has no counterpart in
+ * the method's description; it exists for callers that can neither pass a workspace nor allocate
+ * device memory (an engine that plans all device buffers up front and forbids cudaMalloc later,
+ * a plugin interface that supplies only inputs and outputs).  Same arguments and results as
+ * moe_route minus ws/ws_bytes.  Its scratch is a fixed 4 MiB array in device memory inside the
+ * library (held on every GPU that loads the library until exit): the call needs nsplit*T*E*4
+ * bytes of it (nsplit = 4 for T <= 16) and returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
+ * All calls on a device share the array, so calls that may overlap on the GPU race.  The first
+ * call on each device looks up the array's device address (cudaGetSymbolAddress): make it before
+ * any stream capture starts. */
+moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                             const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
+                             int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
+                             uint8_t* x_q, uint8_t* x_sf, void* stream);
+
 /* Expert-contiguous permute (note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4, §10 and the
  * m_indices paragraph; MegaMoE page 路径 A moe_align_block_size).
  * With cnt_e = #(t,k) routed to e and seg_e = sum_{e'<e} round_up(cnt_e', align):

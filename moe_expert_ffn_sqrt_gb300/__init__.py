@@ -59,6 +59,8 @@ def lib():
         L.moe_workspace_size.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
         L.moe_route.restype = S
         L.moe_route.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, Z, P]
+        L.moe_route_noalloc.restype = S
+        L.moe_route_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]
         L.moe_permute.restype = S
         L.moe_permute.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, Z, P]
         L.moe_grouped_gemm_l1_swiglu.restype = S
@@ -202,6 +204,20 @@ def route(hidden, w_gate, gate_bias, e_score_bias, K, score_fn, renormalize, top
                            _ptr(topk_w, torch.float32, "topk_w"), _ptr(x_q, torch.uint8, "x_q"),
                            _ptr(x_sf, torch.uint8, "x_sf"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
            "moe_route")
+
+
+def route_noalloc(hidden, w_gate, gate_bias, e_score_bias, K, score_fn, renormalize, topk_ids, topk_w,
+                  logits_out=None, x_q=None, x_sf=None):
+    """moe_route without a workspace (scratch lives in a fixed device array inside the library)."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_route_noalloc(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+                                   _ptr(gate_bias, torch.float32, "gate_bias"),
+                                   _ptr(e_score_bias, torch.float32, "e_score_bias"), T, H, E, K,
+                                   SCORE_FNS.get(score_fn, score_fn), int(renormalize),
+                                   _ptr(logits_out, torch.float32, "logits_out"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                   _ptr(topk_w, torch.float32, "topk_w"), _ptr(x_q, torch.uint8, "x_q"),
+                                   _ptr(x_sf, torch.uint8, "x_sf"), _stream()), "moe_route_noalloc")
 
 
 def permute(topk_ids, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, ws, expert_counts=None,

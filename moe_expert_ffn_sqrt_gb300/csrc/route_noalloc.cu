@@ -1,0 +1,75 @@
+// moe_route_noalloc: the routing call without a workspace and without any allocation.
+//
+// Some callers cannot hand this library a workspace and cannot allocate one either: for
+// example an inference engine that plans every device buffer before it starts and forbids
+// cudaMalloc afterwards, a plugin interface that passes in only its inputs and outputs, or code
+// running where an allocation would stall or fail.  For them this entry point keeps the
+// routing scratch (the split-over-H partial gate sums) in a fixed array in device memory that
+// is part of the library image, so the call needs nothing beyond its inputs and outputs.
+//
+// Properties of the array:
+//   * 4 MiB (kNoAllocScratchBytes), held on every GPU that loads the library until the process
+//     exits.  The partial sums take nsplit * T * E * 4 bytes (nsplit = 4 for T <= 16); larger
+//     problems are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+//   * Shared by every call on a device and left holding the last call's partial sums.  Every
+//     entry a call reads is written earlier in the same call, so nothing needs clearing, but
+//     calls that can overlap on the GPU (different streams without ordering) race on it.
+//   * Host code cannot pass the array's name to a kernel (on the host it is only a stand-in for
+//     the device symbol), so the first call on each device looks up its device address with
+//     cudaGetSymbolAddress while that device is current and caches it.  That first call is a
+//     host-side query: make it before any stream capture begins.
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) float g_route_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+float* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_route_scratch on the current device (looked up once per device).
+moe_status scratch_on_current_device(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                        const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
+                                        int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
+                                        uint8_t* x_q, uint8_t* x_sf, void* stream) {
+  if (T < 0 || H <= 0 || H % 128 || E <= 0 || E > 1024 || K <= 0 || K > E || K > 32) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
+  if ((x_q == nullptr) != (x_sf == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(w_gate)) return MOE_ERR_INVALID_ARG;
+  if (x_q && (reinterpret_cast<uintptr_t>(x_q) & 3)) return MOE_ERR_INVALID_ARG;
+  const int ns = moe::route_nsplit(T > 0 ? T : 1, H, E);
+  if (static_cast<size_t>(ns) * T * E * sizeof(float) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  float* scratch = nullptr;
+  const moe_status st = scratch_on_current_device(&scratch);
+  if (st != MOE_OK) return st;
+  const cudaError_t err = moe::launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
+                                            renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, scratch,
+                                            static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
