@@ -28,7 +28,7 @@ struct WsLayout {
   size_t status = 0;
   size_t partial = 0, partial_bytes = 0;
   size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
-  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0;
+  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0;
   size_t total = 0;
 };
 
@@ -53,6 +53,7 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   L.h_q = off;        off = up(off + U * I);
   L.h_sf = off;       off = up(off + moe_act_sf_tiled_bytes(static_cast<int>(U), I / 128, align));
   L.y = off;          off = up(off + U * H * 2);
+  L.xb = off;         off = up(off + U * (H > I ? H : I) * 2);   // bf16 activation rows (NVFP4 GEMMs)
   L.total = off;
   return L;
 }
@@ -105,6 +106,7 @@ size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair) {
   if (E <= 0 || N <= 0 || Kd <= 0 || Kd % 128 || (pair != 1 && pair != 2)) return 0;
   if (pair == 2 ? N % 256 : N % 128) return 0;
   if (fmt == MOE_W_MXFP4) return packed_weight_bytes(E, N, Kd, pair);
+  if (fmt == MOE_W_NVFP4) return packed_nv_weight_bytes(E, N, Kd, pair);
   return 0;
 }
 
@@ -112,8 +114,9 @@ moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, i
                             uint8_t* packed, void* stream) {
   if (!q || !sf || !packed || E <= 0 || N <= 0 || Kd <= 0 || Kd % 128) return MOE_ERR_INVALID_ARG;
   if ((pair != 1 && pair != 2) || (pair == 2 ? N % 256 : N % 128)) return MOE_ERR_INVALID_ARG;
-  if (fmt != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
-  return cuda_status(launch_pack_mx(q, sf, E, N, Kd, pair, packed, S(stream)));
+  if (fmt == MOE_W_MXFP4) return cuda_status(launch_pack_mx(q, sf, E, N, Kd, pair, packed, S(stream)));
+  if (fmt == MOE_W_NVFP4) return cuda_status(launch_pack_nv(q, sf, E, N, Kd, pair, packed, S(stream)));
+  return MOE_ERR_INVALID_ARG;
 }
 
 moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size_t* bytes) {
@@ -171,10 +174,35 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
   if (!aligned(x, 16) || !aligned(x_sf, 16)) return MOE_ERR_INVALID_ARG;
   if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
   if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
-  if (w.fmt != MOE_W_MXFP4) return MOE_ERR_UNSUPPORTED;
   if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
   const size_t U = moe_msum_upper(T, K, E, align);
   if (U == 0) return MOE_OK;
+  if (w.fmt == MOE_W_NVFP4) {
+    // bf16 copy of the activation rows in the workspace, then the bf16 MMA path
+    const WsLayout Lw = layout(T, H, I, E, K, align);
+    if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
+    uint16_t* xb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + Lw.xb);
+    const int Kd = l1 ? H : I;
+    cudaError_t err = launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream));
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    NvLaunch N;
+    N.w = w.packed;
+    N.tscale = w.tscale;
+    N.xb = xb;
+    N.expert_ids = expert_ids;
+    N.m_sum = m_sum;
+    N.h_q = h_q;
+    N.h_sf = h_sf;
+    N.y = y;
+    N.status = status_of(ws);
+    N.E = E;
+    N.w_rows = l1 ? 2 * I : H;
+    N.Kd = Kd;
+    N.I = I;
+    N.U = static_cast<int>(U);
+    N.align = align;
+    return cuda_status(launch_gemm_nv(N, l1, S(stream)));
+  }
   GemmLaunch L;
   L.w = w.packed;
   L.x = x;

@@ -41,6 +41,26 @@ cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
                            cudaStream_t stream);
 
+// gemm_nv.cu (NVFP4 weights, bf16 MMA)
+struct NvLaunch {
+  const uint8_t* w;            // packed NVFP4 weight stream
+  const float* tscale;         // [E]
+  const uint16_t* xb;          // [U, Kd] bf16 activation rows
+  const int32_t* expert_ids;
+  const int32_t* m_sum;
+  uint8_t* h_q;
+  uint8_t* h_sf;
+  uint16_t* y;
+  uint32_t* status;
+  int E, w_rows, Kd, I, U, align;
+};
+size_t packed_nv_weight_bytes(int E, int N, int Kd, int pair);
+cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
+                           cudaStream_t stream);
+cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_t* expert_ids, const int32_t* m_sum,
+                               int U, int Kd, int align, uint16_t* xb, cudaStream_t stream);
+cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
+
 // reduce.cu
 cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int T, int K,
                                     int H, uint16_t* out, cudaStream_t stream);

@@ -248,8 +248,8 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
     """Route -> act quant -> permute -> per-expert L1+SwiGLU+requant -> L2 -> weighted reduce.
 
     ``tokens``: optional subset of token indices; only the (token, expert)
-    rows those tokens need are computed and ``out`` holds only their rows
-    (in the order given).  Routing, quantisation and the permute always run
+    rows those tokens need are computed and ``out``, ``x_q``, ``x_sf`` hold
+    only their rows (in the order given).  Routing and the permute always run
     on all tokens, since the permute layout depends on every token.
     ``topk_w_dtype``: precision in which the routing weights enter the final
     sum (float64 by default; float32 mimics a kernel that stores them as fp32).
@@ -258,9 +258,12 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
     T, H = hidden.shape
     E = inp["w_gate"].shape[0]
     r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
-    x_q, x_sf = act_quant(hidden)
     p = permute(r["topk_ids"], E, align)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    # activations are quantised per token, so only the checked tokens' rows are needed
+    q_rows, sf_rows = act_quant(hidden[tok])
+    x_q = {int(t): q_rows[i] for i, t in enumerate(tok)}
+    x_sf = {int(t): sf_rows[i] for i, t in enumerate(tok)}
     need = {}
     for t in tok:
         for k in range(K):
@@ -274,7 +277,7 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
         w2 = dequant_weight(w["w2_q"], w["w2_sf"], w.get("w2_ts"), fmt)
         I = w13.shape[0] // 2
         ts = sorted(set(t for t, _ in pairs))
-        xd = dequant_fp8_groups(x_q[ts], x_sf[ts])
+        xd = dequant_fp8_groups(np.stack([x_q[t] for t in ts]), np.stack([x_sf[t] for t in ts]))
         _, hq, hsf = expert_l1_swiglu(xd, w13, I)
         y = expert_l2(hq, hsf, w2)
         for j, t in enumerate(ts):
@@ -287,5 +290,5 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
         for k in range(K):
             acc += wts[t, k] * bf16_to_f64(y_rows[(int(t), int(r["topk_ids"][t, k]))])
         out[i] = round_bf16_rne(acc)
-    return dict(route=r, x_q=x_q, x_sf=x_sf, perm=p, out=out, tokens=tok,
+    return dict(route=r, x_q=q_rows, x_sf=sf_rows, perm=p, out=out, tokens=tok,
                 y_rows=y_rows, h_rows=h_rows)
