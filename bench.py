@@ -29,7 +29,18 @@ import synth  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-LAUNCHES_PER_STEP = 7          # gate GEMM, top-K/act-quant, permute, row copy, L1, L2, reduce
+
+
+def launches_per_forward(w):
+    """Kernel launches of one moe_forward, mirroring the library's dispatch."""
+    route = 1 if w.T <= 16 else 2                 # fused small-batch route, else gate GEMM + top-K
+    permute = 1 if w.T * w.K <= 128 else 2        # permute with the row copy in the same launch, else + copy
+    if w.fmt == "mxfp4":
+        ffn = 1                                   # L1 and L2 in one cooperative launch
+    else:
+        ffn = 4                                   # bf16 activation rows + GEMM, for L1 and for L2
+    reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue
+    return route + permute + ffn + reduce
 
 
 def parse_args():
@@ -374,7 +385,7 @@ def run_ours(args, w):
                 "dtype": "fp8xfp4 (fp32 accumulate)" if w.fmt == "mxfp4" else "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
                 "data": "synthetic (seeded)",
                 "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": LAUNCHES_PER_STEP * K, "clocks": clk}
+                "gpu_launches": launches_per_forward(w) * K, "clocks": clk}
         print(json.dumps(line), flush=True)
     if W > 1:
         torch.distributed.destroy_process_group()

@@ -137,7 +137,8 @@ moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size
  *   x_q, x_sf    [T, H] E4M3 and [T, H/128] UE8M0 out, or both NULL: per 128 columns the
  *                scale is the smallest power of two 2^e with amax <= 448 * 2^e (e in
  *                [-127,127], e = 0 when amax = 0) and x_q = RNE_e4m3(x / 2^e).
- *   ws           workspace (split-K partial sums, status word). */
+ *   ws           workspace (split-K partial sums, a counter for the small-batch kernel that the
+ *                call leaves at zero, status word). */
 moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                      const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
                      int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
@@ -149,7 +150,8 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
  * a plugin interface that supplies only inputs and outputs).  Same arguments and results as
  * moe_route minus ws/ws_bytes.  Its scratch is a fixed 4 MiB array in device memory inside the
  * library (held on every GPU that loads the library until exit): the call needs nsplit*T*E*4
- * bytes of it (nsplit = 4 for T <= 16) and returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
+ * bytes of it (nsplit = 4 for T <= 16) rounded up to 256, plus a 256-byte counter slot that each
+ * call leaves at zero, and returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
  * All calls on a device share the array, so calls that may overlap on the GPU race.  The first
  * call on each device looks up the array's device address (cudaGetSymbolAddress): make it before
  * any stream capture starts. */

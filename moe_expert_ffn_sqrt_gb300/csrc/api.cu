@@ -28,7 +28,7 @@ struct WsLayout {
   size_t status = 0;
   size_t partial = 0, partial_bytes = 0;
   size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
-  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0;
+  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, ready = 0;
   size_t total = 0;
 };
 
@@ -36,9 +36,8 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   WsLayout L;
   const size_t U = moe_msum_upper(T, K, E, align);
   size_t off = kAlign;                             // [0, 256): status word
-  const int ns = route_nsplit(T > 0 ? T : 1, H, E);
   L.partial = off;
-  L.partial_bytes = static_cast<size_t>(ns) * T * E * sizeof(float);
+  L.partial_bytes = route_scratch_bytes(T, H, E);
   off = up(off + L.partial_bytes);
   L.topk_ids = off;   off = up(off + static_cast<size_t>(T) * K * 4);
   L.topk_w = off;     off = up(off + static_cast<size_t>(T) * K * 4);
@@ -54,9 +53,16 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   L.h_sf = off;       off = up(off + moe_act_sf_tiled_bytes(static_cast<int>(U), I / 128, align));
   L.y = off;          off = up(off + U * H * 2);
   L.xb = off;         off = up(off + U * (H > I ? H : I) * 2);   // bf16 activation rows (NVFP4 GEMMs)
+  L.tickets = off;    off = up(off + static_cast<size_t>(T) * ((H + 255) / 256) * 4);   // fused reduce
+  L.ready = off;      off = up(off + ffn_ready_words(static_cast<int>(U), align) * 4);   // L1 -> L2 order
   L.total = off;
   return L;
 }
+
+// moe_forward folds the unpermute-reduce into the L2 epilogue up to this many tokens.  With many
+// tokens per row block one epilogue warp would reduce tokens one after another; the separate
+// reduce kernel is faster there.
+constexpr int kFusedReduceMaxTokens = 32;
 
 inline uint32_t* status_of(void* ws) { return static_cast<uint32_t*>(ws); }
 inline moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -136,8 +142,7 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
   if (!aligned(hidden, 16) || !aligned(w_gate, 16)) return MOE_ERR_INVALID_ARG;
   if (x_q && !aligned(x_q, 4)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
-  const int ns = route_nsplit(T > 0 ? T : 1, H, E);
-  const size_t need = kAlign + static_cast<size_t>(ns) * T * E * sizeof(float);
+  const size_t need = kAlign + route_scratch_bytes(T, H, E);
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
@@ -145,10 +150,10 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
                                   renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, S(stream)));
 }
 
-moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
-                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
-                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                       void* ws, size_t ws_bytes, void* stream) {
+static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
+                                 int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                                 const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                                 void* ws, size_t ws_bytes, void* stream, uint32_t* clear, int n_clear) {
   if (T < 0 || K <= 0 || E <= 0 || K > E || align < 1 || align > 256 || (align & (align - 1)))
     return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
@@ -161,13 +166,44 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, 
   const size_t U = moe_msum_upper(T, K, E, align);
   return cuda_status(launch_permute(topk_ids, T, K, E, align, static_cast<int>(U), sorted_token_ids, expert_ids,
                                     inv_perm, m_sum, expert_counts, x_q, x_sf, H, x_perm, x_perm_sf,
-                                    status_of(ws), S(stream)));
+                                    status_of(ws), S(stream), clear, n_clear));
+}
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
+                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                       void* ws, size_t ws_bytes, void* stream) {
+  return permute_common(topk_ids, T, K, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, expert_counts, x_q,
+                        x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream, nullptr, 0);
+}
+
+// Launch description of one MXFP4 GEMM (L1: x = x_perm [U, H] against W13; L2: x = h [U, I] against W2).
+static GemmLaunch mx_launch(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
+                            const int32_t* m_sum, int H, int I, int E, int align, size_t U, const moe_weight& w,
+                            uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws) {
+  GemmLaunch L;
+  L.w = w.packed;
+  L.x = x;
+  L.x_sf = x_sf;
+  L.expert_ids = expert_ids;
+  L.m_sum = m_sum;
+  L.h_q = h_q;
+  L.h_sf = h_sf;
+  L.y = y;
+  L.status = status_of(ws);
+  L.E = E;
+  L.w_rows = l1 ? 2 * I : H;
+  L.Kd = l1 ? H : I;
+  L.I = I;
+  L.U = static_cast<int>(U);
+  L.align = align;
+  return L;
 }
 
 static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
-                              size_t ws_bytes, void* stream) {
+                              size_t ws_bytes, void* stream, const FusedReduce* red = nullptr) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
   if (!(l1 ? weight_ok(w, E, 2 * I, H, 2) : weight_ok(w, E, H, I, 1))) return MOE_ERR_INVALID_ARG;
@@ -201,24 +237,11 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     N.I = I;
     N.U = static_cast<int>(U);
     N.align = align;
+    if (red) N.red = *red;
     return cuda_status(launch_gemm_nv(N, l1, S(stream)));
   }
-  GemmLaunch L;
-  L.w = w.packed;
-  L.x = x;
-  L.x_sf = x_sf;
-  L.expert_ids = expert_ids;
-  L.m_sum = m_sum;
-  L.h_q = h_q;
-  L.h_sf = h_sf;
-  L.y = y;
-  L.status = status_of(ws);
-  L.E = E;
-  L.w_rows = l1 ? 2 * I : H;
-  L.Kd = l1 ? H : I;
-  L.I = I;
-  L.U = static_cast<int>(U);
-  L.align = align;
+  GemmLaunch L = mx_launch(l1, x, x_sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
+  if (red) L.red = *red;
   return cuda_status(launch_gemm(L, l1, S(stream)));
 }
 
@@ -275,13 +298,37 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
   moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
                             xq, xsf, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  st = moe_permute(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream);
+  const size_t U = moe_msum_upper(T, K, E, align);
+  const bool mx = w13.fmt == MOE_W_MXFP4 && w2.fmt == MOE_W_MXFP4;
+  uint32_t* ready = reinterpret_cast<uint32_t*>(b + L.ready);
+  st = permute_common(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream,
+                      mx ? ready : nullptr, mx ? static_cast<int>(ffn_ready_words(static_cast<int>(U), align)) : 0);
   if (st != MOE_OK) return st;
-  st = moe_grouped_gemm_l1_swiglu(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, hq, hsf, ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  st = moe_grouped_gemm_l2(hq, hsf, eids, ms, T, K, H, I, E, align, w2, y, ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  return moe_unpermute_reduce(y, inv, tw, T, K, H, out, stream);
+  const bool fuse_reduce = T <= kFusedReduceMaxTokens;
+  FusedReduce red{};
+  if (fuse_reduce) {
+    red.out = out;
+    red.inv_perm = inv;
+    red.topk_w = tw;
+    red.sorted_ids = sorted;
+    red.tickets = reinterpret_cast<uint32_t*>(b + L.tickets);
+    red.K = K;
+  }
+  if (mx) {
+    // L1 and L2 in one persistent launch: L2 tiles fill the SMs as soon as their rows' h is ready
+    GemmLaunch l1 = mx_launch(true, xp, xpsf, eids, ms, H, I, E, align, U, w13, hq, hsf, nullptr, ws);
+    GemmLaunch l2 = mx_launch(false, hq, hsf, eids, ms, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
+    l2.red = red;
+    if (launch_ffn(l1, l2, ready, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    st = moe_grouped_gemm_l1_swiglu(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, hq, hsf, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    st = gemm_common(false, hq, hsf, eids, ms, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws, ws_bytes, stream,
+                     fuse_reduce ? &red : nullptr);
+    if (st != MOE_OK) return st;
+  }
+  if (fuse_reduce) return MOE_OK;
+  return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
 }
 
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status) {

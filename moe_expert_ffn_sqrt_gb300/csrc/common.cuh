@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 namespace moe {
 
@@ -64,6 +65,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 }
 
 // ------------------------------------------------------------------------------------------
+// Counters shared between CTAs of one launch
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy (TMA / bulk copy)
+// accesses: used on both sides when one CTA's plain stores are read by another CTA's TMA.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *p >= target (acquire).  Bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target, uint32_t* status) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(p) < target) {
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      record_error(status, kDevErrTimeout);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------------------
 // TMA and bulk copies (global -> shared, completion counted on an mbarrier)
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
@@ -80,6 +110,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// Starts pulling [src, src + bytes) into L2 (no completion tracking).  16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -198,6 +233,16 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t nthreads
   return r != 0;
 }
 
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.or.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 // ------------------------------------------------------------------------------------------
 // FP8 (E4M3) quantisation with a power-of-two scale: the smallest e with amax <= 448 * 2^e,
 // clamped to [-127, 127], 0 when amax == 0.  Exact integer arithmetic on the fp32 bits.
@@ -238,5 +283,79 @@ __host__ __device__ __forceinline__ size_t act_sf_bytes(int rows, int slabs, int
 }
 
 constexpr uint32_t kDevErrCheck = 7;    // a kernel self-check (bounds / alignment) failed
+
+// ------------------------------------------------------------------------------------------
+// Weighted unpermute-reduce folded into the L2 epilogue: out[t] = bf16(sum_k w[t,k] y[inv[t,k]]).
+// After an epilogue has stored the y values of column tile `tile` for its rows, each real row
+// takes a ticket for (token, tile); the row that brings the count to K completes the token.
+struct FusedReduce {
+  uint16_t* out;                 // [T, H] bf16; nullptr = not fused
+  const int32_t* inv_perm;       // [T, K]
+  const float* topk_w;           // [T, K]
+  const int32_t* sorted_ids;     // [U]
+  uint32_t* tickets;             // [T, n_col_tiles], zero between calls
+  int K;
+};
+
+// Called by a whole epilogue warp after its rows' y values for column tile `tile` are stored.
+// Each lane that holds a real row counts that row's (token, tile) ticket; a lane that completes
+// a token's K-th arrival marks the token, and the warp then reduces the marked tokens one at a
+// time, 8 columns per lane, in slot order k = 0..K-1 with fp32 fma (the order of the separate
+// unpermute-reduce kernel, so both give identical bits).  The completing warp resets the ticket.
+__device__ __forceinline__ void fused_reduce_tail(const FusedReduce& f, const uint16_t* y, int H, bool mine, int row,
+                                                  int tile, int n_tiles, int c0, int ncols) {
+  const int lane = threadIdx.x & 31;
+  int t = 0;
+  bool last = false;
+  if (mine) {
+    t = __ldg(f.sorted_ids + row) / f.K;
+    __threadfence();
+    last = atomicAdd(f.tickets + static_cast<size_t>(t) * n_tiles + tile, 1u) == static_cast<uint32_t>(f.K - 1);
+  }
+  unsigned todo = __ballot_sync(0xffffffffu, last);
+  if (todo == 0) return;
+  __threadfence();
+  while (todo) {
+    const int src = __ffs(todo) - 1;
+    todo &= todo - 1;
+    const int tt = __shfl_sync(0xffffffffu, t, src);
+    int rk = 0;
+    float wk = 0.f;
+    if (lane < f.K) {
+      rk = __ldg(f.inv_perm + static_cast<size_t>(tt) * f.K + lane);
+      wk = __ldg(f.topk_w + static_cast<size_t>(tt) * f.K + lane);
+    }
+    for (int cb = 0; cb < ncols; cb += 256) {
+      const int c = c0 + cb + lane * 8;
+      const bool active = cb + lane * 8 < ncols;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+      for (int k = 0; k < f.K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, rk, k);
+        const float w = __shfl_sync(0xffffffffu, wk, k);
+        if (active) {
+          const uint4 v = __ldcg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(r) * H + c));
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            acc[2 * j] = fmaf(w, __uint_as_float(u[j] << 16), acc[2 * j]);
+            acc[2 * j + 1] = fmaf(w, __uint_as_float(u[j] & 0xFFFF0000u), acc[2 * j + 1]);
+          }
+        }
+      }
+      if (active) {
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j]));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * j + 1]));
+          o[j] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(f.out + static_cast<size_t>(tt) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+    if (lane == 0) f.tickets[static_cast<size_t>(tt) * n_tiles + tile] = 0;
+  }
+}
 
 }  // namespace moe

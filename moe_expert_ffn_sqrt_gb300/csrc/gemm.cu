@@ -16,6 +16,8 @@
 //    token rows are loaded; the MMA's other rows read unrelated shared memory and their results
 //    are never stored.  BN divides the permute alignment in the common case, so a block holds
 //    one expert; otherwise each expert in the block is a separate pass with masked stores.
+//  * moe_forward runs L1 and L2 as one cooperative launch: L2 items wait (bounded) on per-row-block
+//    counters of finished L1 tiles, so the L1 tail wave and the launch gap are filled with L2 work.
 //  * Persistent CTAs (one per SM) walk the items in a fixed order; a producer warp (TMA), an MMA
 //    warp (one thread issues tcgen05.cp + tcgen05.mma) and four epilogue warps run decoupled
 //    through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
@@ -42,7 +44,7 @@ constexpr uint32_t kSfaCol = 256;
 constexpr uint32_t kSfbCol = 288;
 constexpr int kTileRows = 256;           // weight rows per tile (MMA N)
 
-template <int BN, bool L1>
+template <int BN>
 struct GemmCfg {
   static constexpr int X_BYTES = BN * 128;                       // token rows loaded per slab
   static constexpr int X_SLOT = (X_BYTES + 1023) / 1024 * 1024;  // MMA reads 16 KB from here
@@ -62,31 +64,62 @@ struct GemmCfg {
   static_assert(X_SLOT + 16384 <= STAGE, "MMA A reads must stay inside the stage");
 };
 
-struct GemmArgs {
+// One GEMM of the layer as the kernel sees it.
+struct GemmPhase {
   const uint8_t* w;             // packed weight stream
   const uint8_t* x_sf;          // tiled token scales (rows U, block rows BN)
+  size_t w_bytes;               // sizes, for the kernel's own bounds checks
+  size_t x_sf_bytes;
+  int n_slabs;                  // reduction depth / 128
+  int n_wt;                     // weight tiles per expert
+  int out_cols;                 // L1: I, L2: H
+  int n_tiles;                  // ceil(U/BN) * n_wt; 0 = phase not run by this launch
+};
+
+struct GemmArgs {
+  GemmPhase ph[2];              // [0] L1: W13, SwiGLU, FP8 requant; [1] L2: W2, bf16
   const int32_t* expert_ids;    // [U]
   const int32_t* m_sum;         // [1]
   uint8_t* h_q;                 // L1 out [U, I]
   uint8_t* h_sf;                // L1 out, tiled (rows U, slabs I/128)
   uint16_t* y;                  // L2 out [U, H] bf16
   uint32_t* status;
-  size_t w_bytes;               // sizes, for the kernel's own bounds checks
-  size_t x_sf_bytes;
-  int n_slabs;                  // reduction depth / 128
-  int n_wt;                     // weight tiles per expert
-  int out_cols;                 // L1: I, L2: H
   int sf_nb;                    // blocks of the tiled token-scale layouts
-  int n_tiles;                  // ceil(U/BN) * n_wt
+  uint32_t* ready;              // both phases in one launch: [ceil(U/BN)] finished L1 tiles per row
+                                // block, zero at launch; nullptr otherwise
+  FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
-// Next work item after (t, e): smallest expert id > e present in the row block of tile t,
-// else the first expert of the next tile of this CTA.  Rows are sorted by expert (ignoring -1).
+// Work items are numbered L1 tiles first, then L2 tiles, each phase row-block major
+// (t = row_block * n_wt + weight_tile).  CTA b takes items b, b + G, b + 2G, ... in order.
+struct Item {
+  int phase, rb, wt;
+};
+
+__device__ __forceinline__ Item decode_item(const GemmArgs& a, int t) {
+  Item it;
+  it.phase = t >= a.ph[0].n_tiles ? 1 : 0;
+  const int l = it.phase ? t - a.ph[0].n_tiles : t;
+  it.rb = l / a.ph[it.phase].n_wt;
+  it.wt = l - it.rb * a.ph[it.phase].n_wt;
+  return it;
+}
+
+// Next work item after (t, e): smallest expert id > e present in the row block of item t, else
+// the first expert of this CTA's next item.  Rows are sorted by expert (ignoring -1).  Row
+// blocks past m_sum hold no rows: the rest of that phase is skipped.
 template <int BN>
 __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, int& e) {
-  while (t < a.n_tiles) {
-    const int r0 = (t / a.n_wt) * BN;
-    if (r0 >= msum) return false;
+  const int G = gridDim.x, n0 = a.ph[0].n_tiles, total = n0 + a.ph[1].n_tiles;
+  while (t < total) {
+    const Item it = decode_item(a, t);
+    const int r0 = it.rb * BN;
+    if (r0 >= msum) {
+      if (it.phase == 1) return false;
+      t = n0 + ((static_cast<int>(blockIdx.x) - n0) % G + G) % G;   // this CTA's first L2 item
+      e = -1;
+      continue;
+    }
     const int rend = min(r0 + BN, msum);
     for (int r = r0; r < rend; ++r) {
       const int x = __ldg(a.expert_ids + r);
@@ -95,7 +128,7 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, i
         return true;
       }
     }
-    t += gridDim.x;
+    t += G;
     e = -1;
   }
   return false;
@@ -106,11 +139,17 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, i
 // have no slow path for the infinities that unused accumulator rows may hold.
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
-template <int BN, bool L1>
+// Runs the L1 items, the L2 items, or both.  With both, an L2 item of row block rb reads h rows
+// written by other CTAs: its producer first waits until ready[rb] counts all n_wt L1 tiles of the
+// block (each L1 item's epilogue adds one after its stores).  Every CTA finishes all of its L1
+// items before it takes an L2 item and the launch is cooperative (all CTAs resident), so every
+// awaited item is running or done; the wait is bounded all the same.
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_x,
+    moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
+                    const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_x2,
                     const GemmArgs a) {
-  using C = GemmCfg<BN, L1>;
+  using C = GemmCfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -132,8 +171,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(smem_u32(acc_empty), 128);
     *abort_flag = 0;
     fence_barrier_init();
-    prefetch_tmap(&tmap_w);
-    prefetch_tmap(&tmap_x);
+    if (a.ph[0].n_tiles) {
+      prefetch_tmap(&tmap_w1);
+      prefetch_tmap(&tmap_x1);
+    }
+    if (a.ph[1].n_tiles) {
+      prefetch_tmap(&tmap_w2);
+      prefetch_tmap(&tmap_x2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -153,10 +198,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     int t = blockIdx.x, e = -1;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
-      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
-      const size_t chunk0 = (static_cast<size_t>(e) * a.n_wt + wt) * a.n_slabs;
+      const Item it = decode_item(a, t);
+      const GemmPhase& P = a.ph[it.phase];
+      const CUtensorMap* mw = it.phase ? &tmap_w2 : &tmap_w1;
+      const CUtensorMap* mx = it.phase ? &tmap_x2 : &tmap_x1;
+      const int r0 = it.rb * BN;
+      const size_t chunk0 = (static_cast<size_t>(e) * P.n_wt + it.wt) * P.n_slabs;
       bool ok = true;
-      for (int s = 0; s < a.n_slabs; ++s) {
+      if (it.phase == 1 && a.ready != nullptr) {
+        // h rows of this block come from other CTAs' L1 epilogues
+        if (lane == 0) {
+          const uint32_t need = static_cast<uint32_t>(a.ph[0].n_wt);
+          if (ld_acquire_gpu(a.ready + it.rb) < need) {
+            // start the item's weights towards L2 while waiting
+            const size_t wb = chunk0 * C::W_CHUNK, nb = static_cast<size_t>(P.n_slabs) * C::W_CHUNK;
+            if (wb + nb <= P.w_bytes && nb < (size_t(1) << 31)) bulk_prefetch_l2(P.w + wb, static_cast<uint32_t>(nb));
+            ok = wait_counter(a.ready + it.rb, need, a.status);
+          }
+          fence_proxy_async_global();
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+      }
+      for (int s = 0; ok && s < P.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
         if (!ok) break;
         if (lane == 0) {
@@ -165,9 +228,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const size_t wbase = (chunk0 + s) * C::W_CHUNK;
           const size_t sfa = (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
           // self-check: every copy inside its buffer and 16-byte aligned
-          const bool good = wbase + C::W_CHUNK <= a.w_bytes &&
-                            ((s & 3) != 0 || sfa + C::SFA_BYTES <= a.x_sf_bytes) &&
-                            ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x_sf)) & 15) == 0;
+          const bool good = wbase + C::W_CHUNK <= P.w_bytes &&
+                            ((s & 3) != 0 || sfa + C::SFA_BYTES <= P.x_sf_bytes) &&
+                            ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0;
           if (!good) {
             record_error(a.status, kDevErrCheck);
             *abort_flag = 1;
@@ -175,10 +238,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t bytes = C::TX_W + 1024 + C::X_BYTES;
             if ((s & 3) == 0) bytes += C::SFA_BYTES;
             mbar_arrive_expect_tx(fb, bytes);
-            tma_load_2d(smem_u32(st + C::W_OFF), &tmap_w, 0, static_cast<int>(wbase / 64), fb, pol_w);
-            bulk_load(smem_u32(st + C::SFB_OFF), a.w + wbase + C::TX_W, 1024, fb);
-            tma_load_2d(smem_u32(st), &tmap_x, s * 128, r0, fb, pol_x);
-            if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFA_OFF), a.x_sf + sfa, C::SFA_BYTES, fb);
+            tma_load_2d(smem_u32(st + C::W_OFF), mw, 0, static_cast<int>(wbase / 64), fb, pol_w);
+            bulk_load(smem_u32(st + C::SFB_OFF), P.w + wbase + C::TX_W, 1024, fb);
+            tma_load_2d(smem_u32(st), mx, s * 128, r0, fb, pol_x);
+            if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFA_OFF), P.x_sf + sfa, C::SFA_BYTES, fb);
           }
         }
         __syncwarp();
@@ -203,10 +266,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     int t = blockIdx.x, e = -1;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
+      const int n_slabs = a.ph[decode_item(a, t).phase].n_slabs;
       bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
-        for (int s = 0; s < a.n_slabs; ++s) {
+        for (int s = 0; s < n_slabs; ++s) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + stage), phase, a.status));
           if (!ok) break;
           tc_fence_after();
@@ -249,9 +313,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     int t = blockIdx.x, e = -1;
     while (next_item<BN>(a, msum, t, e)) {
-      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
+      const Item it = decode_item(a, t);
+      const int r0 = it.rb * BN, wt = it.wt;
       const int row = r0 + m;
-      const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == e;
+      const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
+      const bool mine = row_e == e;
       bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, 128, ok);    // one vote over the four epilogue warps
       if (!ok) {
@@ -259,12 +325,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      if (L1) {
+      if (it.phase == 0) {
+        const int I = a.ph[0].out_cols;
         // h = silu(gate) * up for the 128 columns of this tile, kept in registers so that the
         // accumulator is released before the quantise-and-store part
-        float h[128];
-        float amax = 0.f;
         if (warp_has_rows) {
+          float h[128];
+          float amax = 0.f;
 #pragma unroll
           for (int c0 = 0; c0 < 128; c0 += 16) {
             uint32_t g[16], u[16];
@@ -277,33 +344,48 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               amax = fmaxf(amax, fabsf(h[c0 + j]));
             }
           }
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty));
-        if (mine) {
-          const int ex = ue8m0_exponent(amax);
-          const float sc = pow2_neg(ex);
-          a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
-          uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+          if (mine) {
+            const int ex = ue8m0_exponent(amax);
+            const float sc = pow2_neg(ex);
+            a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+            uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * I + wt * 128);
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t packed[4];
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+              uint32_t packed[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = c0 + 4 * j;
-              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
-              const uint32_t hi =
-                  __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
-              packed[j] = lo | (hi << 16);
+              for (int j = 0; j < 4; ++j) {
+                const int c = c0 + 4 * j;
+                const uint32_t lo =
+                    __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t hi =
+                    __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
+                packed[j] = lo | (hi << 16);
+              }
+              dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if (a.ready) fence_proxy_async_global();
+          }
+        } else {
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+        }
+        if (a.ready) {
+          // publish the tile once the block's last expert pass is stored: bar.red doubles as the
+          // barrier that orders all 128 threads' stores before the release below
+          const bool later = row_e > e;
+          if (!named_barrier_or(1, 128, later) && threadIdx.x == 64) {
+            __threadfence();
+            atomicAdd(a.ready + it.rb, 1u);
           }
         }
       } else {
+        const int H = a.ph[1].out_cols;
+        const int ncols = min(kTileRows, H - wt * kTileRows);
         // 256 outputs as bf16 pairs in registers, accumulator released, then stored
-        uint32_t packed[128];
-        const int ncols = min(kTileRows, a.out_cols - wt * kTileRows);
         if (warp_has_rows) {
+          uint32_t packed[128];
 #pragma unroll
           for (int c0 = 0; c0 < kTileRows; c0 += 16) {
             uint32_t v[16];
@@ -316,15 +398,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               packed[c0 / 2 + j] = lo | (hi << 16);
             }
           }
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty));
-        if (mine) {
-          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kTileRows);
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+          if (mine) {
+            uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * H + wt * kTileRows);
 #pragma unroll
-          for (int c = 0; c < kTileRows / 8; ++c)
-            if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            for (int c = 0; c < kTileRows / 8; ++c)
+              if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          }
+        } else {
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
         }
+        if (a.red.out) fused_reduce_tail(a.red, a.y, H, mine, row, wt, a.ph[1].n_wt, wt * kTileRows, ncols);
       }
       acc_phase ^= 1;
     }
@@ -387,61 +473,97 @@ size_t packed_weight_bytes(int E, int N, int Kd, int pair) {
   return static_cast<size_t>(E) * weight_tiles(N, pair) * (Kd / 128) * (2 * (8192 + 512));
 }
 
-template <int BN, bool L1>
-static cudaError_t launch_gemm_t(const GemmLaunch& L, cudaStream_t stream) {
-  using C = GemmCfg<BN, L1>;
-  CUtensorMap mw, mx;
-  const int n_slabs = L.Kd / 128;
-  const int n_wt = weight_tiles(L.w_rows, L1 ? 2 : 1);
-  const size_t w_bytes = packed_weight_bytes(L.E, L.w_rows, L.Kd, L1 ? 2 : 1);
+// Fills one phase's arguments and tensor maps.  L1 reads x_perm [U, H] against W13 (2I rows,
+// gate/up paired tiles), L2 reads h [U, I] against W2 (H rows).
+template <int BN>
+static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& mw, CUtensorMap& mx) {
+  const int pair = l1 ? 2 : 1;
+  P.w = L.w;
+  P.x_sf = L.x_sf;
+  P.w_bytes = packed_weight_bytes(L.E, L.w_rows, L.Kd, pair);
+  P.x_sf_bytes = act_sf_bytes(L.U, L.Kd / 128, BN);
+  P.n_slabs = L.Kd / 128;
+  P.n_wt = weight_tiles(L.w_rows, pair);
+  P.out_cols = l1 ? L.I : L.w_rows;
+  P.n_tiles = (L.U + BN - 1) / BN * P.n_wt;
   // the packed stream viewed as rows of 128 FP4 codes (64 bytes); a box is 256 rows
-  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L.w, 128, w_bytes / 64, 64, 128, kTileRows))
-    return cudaErrorInvalidValue;
-  if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN)) return cudaErrorInvalidValue;
-  GemmArgs a;
-  a.w = L.w;
-  a.x_sf = L.x_sf;
-  a.expert_ids = L.expert_ids;
-  a.m_sum = L.m_sum;
-  a.h_q = L.h_q;
-  a.h_sf = L.h_sf;
-  a.y = L.y;
-  a.status = L.status;
-  a.w_bytes = w_bytes;
-  a.x_sf_bytes = act_sf_bytes(L.U, L.Kd / 128, BN);
-  a.n_slabs = n_slabs;
-  a.n_wt = n_wt;
-  a.out_cols = L1 ? L.I : L.w_rows;
-  a.sf_nb = act_sf_blocks(L.U, BN);
-  const int nrb = (L.U + BN - 1) / BN;
-  a.n_tiles = nrb * a.n_wt;
+  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L.w, 128, P.w_bytes / 64, 64, 128, kTileRows))
+    return false;
+  return make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN);
+}
+
+// l1 and/or l2 (non-null ones run).  With both, `ready` ([ceil(U/BN)] words, zero) orders the
+// phases and the launch is cooperative so that all CTAs are resident together.
+template <int BN>
+static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* ready, cudaStream_t stream) {
+  using C = GemmCfg<BN>;
+  GemmArgs a{};
+  CUtensorMap m[4];
+  const GemmLaunch& any = l1 ? *l1 : *l2;
+  if (l1 && !make_phase<BN>(*l1, true, a.ph[0], m[0], m[1])) return cudaErrorInvalidValue;
+  if (l2 && !make_phase<BN>(*l2, false, a.ph[1], m[2], m[3])) return cudaErrorInvalidValue;
+  if (!l1) {
+    a.ph[0] = a.ph[1];
+    a.ph[0].n_tiles = 0;
+    m[0] = m[2];
+    m[1] = m[3];
+  }
+  if (!l2) {
+    a.ph[1] = a.ph[0];
+    a.ph[1].n_tiles = 0;
+    m[2] = m[0];
+    m[3] = m[1];
+  }
+  a.expert_ids = any.expert_ids;
+  a.m_sum = any.m_sum;
+  a.h_q = l1 ? l1->h_q : nullptr;
+  a.h_sf = l1 ? l1->h_sf : nullptr;
+  a.y = l2 ? l2->y : nullptr;
+  a.status = any.status;
+  a.sf_nb = act_sf_blocks(any.U, BN);
+  a.ready = (l1 && l2) ? ready : nullptr;
+  if (l2) a.red = l2->red;
+  const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
   int grid = num_sms();
-  if (grid > a.n_tiles) grid = a.n_tiles;
+  if (grid > total) grid = total;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
-  moe_gemm_kernel<BN, L1><<<grid, kGemmThreads, C::SMEM, stream>>>(mw, mx, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.ready ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
 }
 
 int gemm_block_n(int align) { return act_sf_block_rows(align); }
 
+static cudaError_t launch_bn(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* ready, cudaStream_t stream) {
+  switch (gemm_block_n((l1 ? l1 : l2)->align)) {
+    case 16: return launch_gemm_t<16>(l1, l2, ready, stream);
+    case 32: return launch_gemm_t<32>(l1, l2, ready, stream);
+    case 64: return launch_gemm_t<64>(l1, l2, ready, stream);
+    default: return launch_gemm_t<128>(l1, l2, ready, stream);
+  }
+}
+
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream) {
-  const int bn = gemm_block_n(L.align);
-  if (l1) {
-    switch (bn) {
-      case 16: return launch_gemm_t<16, true>(L, stream);
-      case 32: return launch_gemm_t<32, true>(L, stream);
-      case 64: return launch_gemm_t<64, true>(L, stream);
-      default: return launch_gemm_t<128, true>(L, stream);
-    }
-  }
-  switch (bn) {
-    case 16: return launch_gemm_t<16, false>(L, stream);
-    case 32: return launch_gemm_t<32, false>(L, stream);
-    case 64: return launch_gemm_t<64, false>(L, stream);
-    default: return launch_gemm_t<128, false>(L, stream);
-  }
+  return l1 ? launch_bn(&L, nullptr, nullptr, stream) : launch_bn(nullptr, &L, nullptr, stream);
+}
+
+cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* ready, cudaStream_t stream) {
+  return launch_bn(&l1, &l2, ready, stream);
+}
+
+size_t ffn_ready_words(int U, int align) {
+  const int bn = gemm_block_n(align);
+  return static_cast<size_t>((U + bn - 1) / bn);
 }
 
 // ------------------------------------------------------------------------------------------

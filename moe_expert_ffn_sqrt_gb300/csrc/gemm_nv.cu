@@ -59,6 +59,7 @@ struct NvArgs {
   int out_cols;
   int sf_nb;
   int n_tiles;
+  FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
 template <int BN>
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           for (int c = 0; c < kNvTile / 8; ++c)
             if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
         }
+        if (a.red.out) fused_reduce_tail(a.red, a.y, a.out_cols, mine, row, wt, a.n_wt, wt * kNvTile, ncols);
       }
       acc_phase ^= 1;
     }
@@ -462,6 +464,7 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.h_q = L.h_q;
   a.h_sf = L.h_sf;
   a.y = L.y;
+  a.red = L.red;
   a.status = L.status;
   const int pair = L1 ? 2 : 1;
   a.n_wt = pair == 2 ? L.w_rows / kNvTile : (L.w_rows + kNvTile - 1) / kNvTile;

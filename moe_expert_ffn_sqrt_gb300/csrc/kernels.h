@@ -4,10 +4,13 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "common.cuh"
+
 namespace moe {
 
 // route.cu
 int route_nsplit(int T, int H, int E);
+size_t route_scratch_bytes(int T, int H, int E);   // partial sums + ticket slot
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
@@ -18,7 +21,7 @@ size_t permute_smem_bytes(int E);
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, cudaStream_t stream);
+                           uint32_t* status, cudaStream_t stream, uint32_t* clear = nullptr, int n_clear = 0);
 
 // gemm.cu
 struct GemmLaunch {
@@ -32,12 +35,16 @@ struct GemmLaunch {
   uint16_t* y;
   uint32_t* status;
   int E, w_rows, Kd, I, U, align;
+  FusedReduce red{};           // L2: fold the unpermute-reduce into the epilogue when red.out is set
 };
 int num_sms();
 int weight_tiles(int N, int pair);
 size_t packed_weight_bytes(int E, int N, int Kd, int pair);
 int gemm_block_n(int align);
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
+// L1 and L2 in one cooperative launch; `ready` holds ffn_ready_words(U, align) zero words.
+cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* ready, cudaStream_t stream);
+size_t ffn_ready_words(int U, int align);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
                            cudaStream_t stream);
 
@@ -53,6 +60,7 @@ struct NvLaunch {
   uint16_t* y;
   uint32_t* status;
   int E, w_rows, Kd, I, U, align;
+  FusedReduce red{};
 };
 size_t packed_nv_weight_bytes(int E, int N, int Kd, int pair);
 cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,

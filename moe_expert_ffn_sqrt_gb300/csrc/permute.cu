@@ -2,7 +2,8 @@
 // Note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4 (scatter, inv_perm, M_sum), §10 (M_sum_upper) and the
 // m_indices paragraph (expert_ids, -1 on padding); MegaMoE page 路径 A (moe_align_block_size).
 //
-// One CTA of 1024 threads does the whole index computation, deterministically:
+// Up to 1024 (t,k) pairs a small single-pass kernel handles the index computation (and, up to 128
+// pairs, the row copy); above that one CTA of 1024 threads does it, deterministically:
 //   1. each warp counts its contiguous chunk of the flat (t,k) list into a private histogram;
 //   2. per expert: count, aligned size, exclusive scan -> segment starts, M_sum; per (warp,
 //      expert) base row = segment start + pairs of that expert in earlier chunks;
@@ -26,6 +27,8 @@ struct PermuteArgs {
   int32_t* m_sum;
   int32_t* counts;       // optional
   uint32_t* status;
+  uint32_t* clear;       // optional: n_clear words zeroed for the kernels that follow (GEMM counters)
+  int n_clear;
 };
 
 __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteArgs a) {
@@ -124,6 +127,122 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteA
   if (a.counts)
     for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
   if (tid == 0) *a.m_sum = msum;
+  for (int i = tid; i < a.n_clear; i += kPermThreads) a.clear[i] = 0;
+}
+
+// Small problems (T*K <= 1024): one thread per (t,k) pair.  A pair's rank within its expert is
+// the number of earlier pairs (smaller flat index) with the same expert, counted in shared
+// memory; one warp scans the expert counts.  CTA 0 writes the permutation.  When there are few
+// pairs the same launch also copies the activation rows: every CTA recomputes the (cheap)
+// permutation and its warps copy one pair's row each, so the copy is spread over ceil(N/32) SMs
+// with all of a lane's loads issued before its stores.
+constexpr int kSmallPairs = 1024;
+constexpr int kSmallCopyPairs = 128;
+
+__global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const PermuteArgs a, const uint8_t* x_q,
+                                                                        const uint8_t* x_sf, int H, uint8_t* x_perm,
+                                                                        uint8_t* x_perm_sf, int bt, int nb) {
+  extern __shared__ int32_t sh[];
+  int32_t* cnt = sh;                 // [E]
+  int32_t* seg = sh + a.E;           // [E]
+  __shared__ int32_t s_ids[kSmallPairs];
+  __shared__ int32_t s_rank[kSmallPairs];
+  __shared__ int32_t s_total;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int N = a.T * a.K;
+  for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
+  int e_mine = -1;
+  if (tid < N) {
+    e_mine = a.topk_ids[tid];
+    if (e_mine < 0 || e_mine >= a.E) {
+      if (blockIdx.x == 0) record_error(a.status, kDevErrIndex);
+      e_mine = -1;
+    }
+    s_ids[tid] = e_mine;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (e_mine >= 0) {
+    atomicAdd(&cnt[e_mine], 1);
+    for (int j = 0; j < tid; ++j) rank += (s_ids[j] == e_mine);
+  }
+  if (tid < N) s_rank[tid] = rank;
+  __syncthreads();
+  if (warp == 0) {                   // exclusive scan of the aligned segment sizes
+    const int per = (a.E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane * per + j;
+      if (e < a.E) local += (cnt[e] + a.align - 1) / a.align * a.align;
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane * per + j;
+      if (e < a.E) {
+        seg[e] = run;
+        run += (cnt[e] + a.align - 1) / a.align * a.align;
+      }
+    }
+    if (lane == 31) s_total = incl;
+  }
+  __syncthreads();
+  const int msum = s_total;
+  if (blockIdx.x == 0) {
+    if (e_mine >= 0) {
+      const int pos = seg[e_mine] + rank;
+      a.inv_perm[tid] = pos;
+      a.sorted_ids[pos] = tid;
+      a.expert_ids[pos] = e_mine;
+    }
+    for (int e = warp; e < a.E; e += kPermWarps) {
+      const int c = cnt[e];
+      const int padded = (c + a.align - 1) / a.align * a.align;
+      for (int r = c + lane; r < padded; r += 32) {
+        a.sorted_ids[seg[e] + r] = N;
+        a.expert_ids[seg[e] + r] = -1;
+      }
+    }
+    for (int r = msum + tid; r < a.U; r += kPermThreads) {
+      a.sorted_ids[r] = N;
+      a.expert_ids[r] = -1;
+    }
+    if (a.counts)
+      for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
+    if (tid == 0) *a.m_sum = msum;
+    for (int i = tid; i < a.n_clear; i += kPermThreads) a.clear[i] = 0;
+  }
+  if (x_perm != nullptr && N <= kSmallCopyPairs) {
+    const int chunks = H / 16, slabs = H / 128;
+    for (int p = blockIdx.x * kPermWarps + warp; p < N; p += gridDim.x * kPermWarps) {
+      const int e = s_ids[p];
+      if (e < 0) continue;
+      const int dst = seg[e] + s_rank[p];
+      const int t = p / a.K;
+      const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
+      uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
+      for (int j0 = 0; j0 < chunks; j0 += 32 * 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u * 32 + lane;
+          if (j < chunks) v[u] = __ldg(src + j);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u * 32 + lane;
+          if (j < chunks) out[j] = v[u];
+        }
+      }
+      for (int s2 = lane; s2 < slabs; s2 += 32)
+        x_perm_sf[act_sf_offset(bt, nb, dst, s2)] = x_sf[static_cast<size_t>(t) * slabs + s2];
+    }
+  }
 }
 
 // Row copy: x_perm[inv_perm[t,k]] = x_q[t], scales into the tiled layout.  One warp per pair.
@@ -151,20 +270,31 @@ size_t permute_smem_bytes(int E) { return static_cast<size_t>(kPermWarps + 2) * 
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, cudaStream_t stream) {
-  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status};
-  const size_t smem = permute_smem_bytes(E);
-  cudaError_t err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  permute_kernel<<<1, kPermThreads, smem, stream>>>(a);
-  err = cudaGetLastError();
-  if (err != cudaSuccess || x_perm == nullptr) return err;
-  const long long pairs = static_cast<long long>(T) * K;
-  if (pairs == 0) return cudaSuccess;
-  permute_rows_kernel<<<static_cast<int>((pairs + 7) / 8), 256, 0, stream>>>(inv_perm, topk_ids, T, K, E, H, x_q, x_sf,
-                                                                              x_perm, x_perm_sf, act_sf_block_rows(align),
-                                                                              act_sf_blocks(U, act_sf_block_rows(align)));
+                           uint32_t* status, cudaStream_t stream, uint32_t* clear, int n_clear) {
+  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status, clear, n_clear};
+  const int bt = act_sf_block_rows(align), nb = act_sf_blocks(U, bt);
+  const long long npairs = static_cast<long long>(T) * K;
+  cudaError_t err;
+  if (npairs <= kSmallPairs) {
+    const size_t smem = 2 * static_cast<size_t>(E) * sizeof(int32_t);
+    err = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    const bool copy = x_perm != nullptr && npairs <= kSmallCopyPairs;
+    const int grid = copy && npairs > 0 ? static_cast<int>((npairs + kPermWarps - 1) / kPermWarps) : 1;
+    permute_small_kernel<<<grid, kPermThreads, smem, stream>>>(a, x_q, x_sf, H, x_perm, x_perm_sf, bt, nb);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || x_perm == nullptr || copy) return err;
+  } else {
+    const size_t smem = permute_smem_bytes(E);
+    err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    permute_kernel<<<1, kPermThreads, smem, stream>>>(a);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || x_perm == nullptr) return err;
+  }
+  if (npairs == 0) return cudaSuccess;
+  permute_rows_kernel<<<static_cast<int>((npairs + 7) / 8), 256, 0, stream>>>(inv_perm, topk_ids, T, K, E, H, x_q, x_sf,
+                                                                               x_perm, x_perm_sf, bt, nb);
   return cudaGetLastError();
 }
 

@@ -63,80 +63,10 @@ __global__ void __launch_bounds__(256) gate_gemm_kernel(const uint16_t* __restri
 }
 
 // ------------------------------------------------------------------------------------------
-// Gate GEMV for small batches (T <= kGemvT): CTA = 4 experts x one quarter of H; each thread
-// walks 8-column groups of its quarter, all T tokens at once; block reduction at the end.
-// partial[split][t][e] as for the tiled kernel (4 splits).
+// Small batches (T <= kGemvT) use route_small_kernel below: CTA = 4 experts x one quarter of H.
 constexpr int kGemvT = 16;
 constexpr int kGemvE = 4;
 constexpr int kGemvSplit = 4;
-
-template <int TT>
-__global__ void __launch_bounds__(256) gate_gemv_kernel(const uint16_t* __restrict__ hidden,
-                                                        const float* __restrict__ wg, int T, int H, int E,
-                                                        float* __restrict__ partial) {
-  __shared__ float red[8][kGemvE * TT];
-  const int e0 = blockIdx.x * kGemvE, split = blockIdx.y;
-  const int hq = H / kGemvSplit;                     // multiple of 32 (H multiple of 128)
-  const int hbeg = split * hq;
-  float acc[kGemvE][TT];
-#pragma unroll
-  for (int i = 0; i < kGemvE; ++i)
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[i][t] = 0.f;
-  for (int h = hbeg + threadIdx.x * 8; h < hbeg + hq; h += 256 * 8) {
-    float w[kGemvE][8];
-#pragma unroll
-    for (int i = 0; i < kGemvE; ++i) {
-      const int e = e0 + i;
-      if (e < E) {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h + 4));
-        w[i][0] = a.x; w[i][1] = a.y; w[i][2] = a.z; w[i][3] = a.w;
-        w[i][4] = b.x; w[i][5] = b.y; w[i][6] = b.z; w[i][7] = b.w;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[i][j] = 0.f;
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      if (t < T) {
-        const uint4 x = __ldg(reinterpret_cast<const uint4*>(hidden + static_cast<size_t>(t) * H + h));
-        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
-        float xv[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xv[2 * j] = __uint_as_float(xw[j] << 16);
-          xv[2 * j + 1] = __uint_as_float(xw[j] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int i = 0; i < kGemvE; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][t] = fmaf(xv[j], w[i][j], acc[i][t]);
-      }
-    }
-  }
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-#pragma unroll
-  for (int i = 0; i < kGemvE; ++i)
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      float v = acc[i][t];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0) red[warp][i * TT + t] = v;
-    }
-  __syncthreads();
-  for (int j = threadIdx.x; j < kGemvE * TT; j += 256) {
-    const int i = j / TT, t = j % TT, e = e0 + i;
-    if (t < T && e < E) {
-      float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) v += red[w][j];
-      partial[(static_cast<size_t>(split) * T + t) * E + e] = v;
-    }
-  }
-}
 
 // ------------------------------------------------------------------------------------------
 // Top-K: one CTA (256 threads) per token.  Threads sum the split partials of one expert each
@@ -286,6 +216,187 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
   if (lane == 0) a.x_sf[static_cast<size_t>(t) * gpt + g] = static_cast<uint8_t>(e + 127);
 }
 
+// ------------------------------------------------------------------------------------------
+// Small batches (T <= kGemvT), one launch.  Each CTA (4 experts x one quarter of H) writes its
+// gate partial sums for all T tokens, then quantises its share of the FP8 activation groups.  The
+// last CTA to finish (ticket counter in the scratch buffer) sums the 4 partials per (t, e) in
+// split order and runs the top-K of every token, one warp per token, as route_finish_kernel does.
+// It resets the counter to zero for the next call.
+template <int TT, int PER>
+__global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs a, const float* __restrict__ wg,
+                                                          float* __restrict__ partial, uint32_t* __restrict__ ticket) {
+  __shared__ float red[8][kGemvE * TT];
+  __shared__ int s_last;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int nblocks = gridDim.x * gridDim.y;
+  const int bid = blockIdx.y * gridDim.x + blockIdx.x;
+  const int T = a.T, H = a.H, E = a.E;
+  // 1. gate GEMV partial: experts e0..e0+3 over one quarter of H
+  const int e0 = blockIdx.x * kGemvE, split = blockIdx.y;
+  const int hq = H / kGemvSplit, hbeg = split * hq;   // hq is a multiple of 32 (H multiple of 128)
+  float acc[kGemvE][TT];
+#pragma unroll
+  for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[i][t] = 0.f;
+  for (int h = hbeg + threadIdx.x * 8; h < hbeg + hq; h += 256 * 8) {
+    float w[kGemvE][8];
+#pragma unroll
+    for (int i = 0; i < kGemvE; ++i) {
+      const int e = e0 + i;
+      if (e < E) {
+        const float4 p = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h));
+        const float4 q = __ldg(reinterpret_cast<const float4*>(wg + static_cast<size_t>(e) * H + h + 4));
+        w[i][0] = p.x; w[i][1] = p.y; w[i][2] = p.z; w[i][3] = p.w;
+        w[i][4] = q.x; w[i][5] = q.y; w[i][6] = q.z; w[i][7] = q.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[i][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      if (t < T) {
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.hidden + static_cast<size_t>(t) * H + h));
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+        float xv[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xv[2 * j] = __uint_as_float(xw[j] << 16);
+          xv[2 * j + 1] = __uint_as_float(xw[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][t] = fmaf(xv[j], w[i][j], acc[i][t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kGemvE; ++i)
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      float v = acc[i][t];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      if (lane == 0) red[warp][i * TT + t] = v;
+    }
+  __syncthreads();
+  for (int j = threadIdx.x; j < kGemvE * TT; j += 256) {
+    const int i = j / TT, t = j % TT, e = e0 + i;
+    if (t < T && e < E) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += red[w][j];
+      partial[(static_cast<size_t>(split) * T + t) * E + e] = v;
+    }
+  }
+  // 2. FP8 activation quantisation of this CTA's share of the 128-column groups
+  if (a.x_q) {
+    const int gpt = H / 128;
+    for (long long gidx = static_cast<long long>(bid) * 8 + warp; gidx < static_cast<long long>(T) * gpt;
+         gidx += static_cast<long long>(nblocks) * 8) {
+      const int t = static_cast<int>(gidx / gpt), g = static_cast<int>(gidx % gpt);
+      const size_t base = static_cast<size_t>(t) * H + g * 128 + lane * 4;
+      const uint2 raw = *reinterpret_cast<const uint2*>(a.hidden + base);
+      float v[4];
+      v[0] = __uint_as_float(raw.x << 16);
+      v[1] = __uint_as_float(raw.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(raw.y << 16);
+      v[3] = __uint_as_float(raw.y & 0xFFFF0000u);
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      const int ex = ue8m0_exponent(amax);
+      const float sc = pow2_neg(ex);
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[0] * sc, v[1] * sc), __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[2] * sc, v[3] * sc), __NV_SATFINITE, __NV_E4M3);
+      *reinterpret_cast<uint32_t*>(a.x_q + base) = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      if (lane == 0) a.x_sf[static_cast<size_t>(t) * gpt + g] = static_cast<uint8_t>(ex + 127);
+    }
+  }
+  // 3. the last CTA to finish does the top-K
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == static_cast<uint32_t>(nblocks - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = warp; t < T; t += 8) {
+    float s[PER], key[PER];
+    float lmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane + 32 * j;
+      float l = -INFINITY;
+      if (e < E) {
+        float v[kGemvSplit];
+#pragma unroll
+        for (int sp = 0; sp < kGemvSplit; ++sp) v[sp] = __ldcg(partial + (static_cast<size_t>(sp) * T + t) * E + e);
+        l = (v[0] + v[1]) + (v[2] + v[3]);       // the order route_finish_kernel sums 4 splits in
+        if (a.gate_bias) l += a.gate_bias[e];
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+      }
+      s[j] = l;
+      lmax = fmaxf(lmax, l);
+    }
+    if (a.score_fn == 0) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        s[j] = (lane + 32 * j < E) ? expf(s[j] - lmax) : 0.f;
+        sum += s[j];
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+#pragma unroll
+      for (int j = 0; j < PER; ++j) s[j] = s[j] / sum;
+    } else {
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const float l = s[j];
+        s[j] = (lane + 32 * j < E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int e = lane + 32 * j;
+      key[j] = (e < E) ? s[j] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
+    }
+    float wsum = 0.f, wmine = 0.f;
+    for (int k = 0; k < a.K; ++k) {
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int e = lane + 32 * j;
+        if (key[j] > bk || (key[j] == bk && e < bi)) {
+          bk = key[j];
+          bi = e;
+        }
+      }
+      warp_argmax(bk, bi);
+      float sw = 0.f;
+#pragma unroll
+      for (int j = 0; j < PER; ++j)
+        if ((bi & 31) == lane && j == (bi >> 5)) {
+          sw = s[j];
+          key[j] = -INFINITY;
+        }
+      sw = __shfl_sync(0xffffffffu, sw, bi & 31);
+      wsum += sw;
+      if (lane == k) wmine = sw;
+      if (lane == 0) a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
+    }
+    if (lane < a.K) a.topk_w[static_cast<size_t>(t) * a.K + lane] = a.renormalize ? wmine / wsum : wmine;
+  }
+  if (threadIdx.x == 0) *ticket = 0;     // ready for the next call (the kernel boundary orders it)
+}
+
 int route_nsplit(int T, int H, int E) {
   if (T <= kGemvT) return kGemvSplit;
   const int tiles = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
@@ -296,25 +407,29 @@ int route_nsplit(int T, int H, int E) {
   return ns;
 }
 
+size_t route_scratch_bytes(int T, int H, int E) {
+  // partial sums, then one 256-byte slot for the small-batch kernel's ticket counter
+  return (static_cast<size_t>(route_nsplit(T > 0 ? T : 1, H, E)) * T * E * sizeof(float) + 255) / 256 * 256 + 256;
+}
+
+template <int TT>
+static void launch_route_small(const RouteFinishArgs& a, const float* w_gate, float* partial, uint32_t* ticket,
+                               cudaStream_t stream) {
+  dim3 g((a.E + kGemvE - 1) / kGemvE, kGemvSplit);
+  const int per = (a.E + 31) / 32;
+  if (per <= 1) route_small_kernel<TT, 1><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+  else if (per <= 2) route_small_kernel<TT, 2><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+  else if (per <= 4) route_small_kernel<TT, 4><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+  else if (per <= 8) route_small_kernel<TT, 8><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+  else if (per <= 16) route_small_kernel<TT, 16><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+  else route_small_kernel<TT, 32><<<g, 256, 0, stream>>>(a, w_gate, partial, ticket);
+}
+
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
                          cudaStream_t stream) {
   const int ns = route_nsplit(T, H, E);
-  if (T <= kGemvT) {
-    dim3 g0((E + kGemvE - 1) / kGemvE, kGemvSplit);
-    if (T <= 8)
-      gate_gemv_kernel<8><<<g0, 256, 0, stream>>>(hidden, w_gate, T, H, E, partial);
-    else
-      gate_gemv_kernel<16><<<g0, 256, 0, stream>>>(hidden, w_gate, T, H, E, partial);
-  } else {
-    int hps = (H + ns - 1) / ns;
-    hps = (hps + GH - 1) / GH * GH;
-    dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
-    gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
-  }
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
   RouteFinishArgs a;
   a.partial = partial;
   a.nsplit = ns;
@@ -333,6 +448,20 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
   a.x_q = x_q;
   a.x_sf = x_sf;
   a.topk_blocks = T;
+  if (T <= kGemvT) {
+    uint32_t* ticket = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(partial) + route_scratch_bytes(T, H, E) - 256);
+    if (T <= 8) launch_route_small<8>(a, w_gate, partial, ticket, stream);
+    else launch_route_small<16>(a, w_gate, partial, ticket, stream);
+    return cudaGetLastError();
+  }
+  {
+    int hps = (H + ns - 1) / ns;
+    hps = (hps + GH - 1) / GH * GH;
+    dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
+    gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
   const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;
   const int blocks = T + static_cast<int>((qgroups + 7) / 8);
   const int per = (E + 31) / 32;

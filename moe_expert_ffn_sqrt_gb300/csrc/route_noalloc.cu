@@ -9,11 +9,14 @@
 //
 // Properties of the array:
 //   * 4 MiB (kNoAllocScratchBytes), held on every GPU that loads the library until the process
-//     exits.  The partial sums take nsplit * T * E * 4 bytes (nsplit = 4 for T <= 16); larger
-//     problems are rejected with MOE_ERR_UNSUPPORTED before anything is launched.
+//     exits.  A call needs nsplit * T * E * 4 bytes of partial sums (nsplit = 4 for T <= 16),
+//     rounded up to 256, plus a 256-byte slot; larger problems are rejected with
+//     MOE_ERR_UNSUPPORTED before anything is launched.
 //   * Shared by every call on a device and left holding the last call's partial sums.  Every
-//     entry a call reads is written earlier in the same call, so nothing needs clearing, but
-//     calls that can overlap on the GPU (different streams without ordering) race on it.
+//     partial a call reads is written earlier in the same call; the slot holds a counter that must
+//     be zero when a call starts: it is zero when the library loads and each call that uses it
+//     sets it back to zero before finishing.  Calls that can overlap on the GPU (different streams
+//     without ordering) race on the array.
 //   * Host code cannot pass the array's name to a kernel (on the host it is only a stand-in for
 //     the device symbol), so the first call on each device looks up its device address with
 //     cudaGetSymbolAddress while that device is current and caches it.  That first call is a
@@ -62,8 +65,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_g
   if ((x_q == nullptr) != (x_sf == nullptr)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(hidden) || !aligned16(w_gate)) return MOE_ERR_INVALID_ARG;
   if (x_q && (reinterpret_cast<uintptr_t>(x_q) & 3)) return MOE_ERR_INVALID_ARG;
-  const int ns = moe::route_nsplit(T > 0 ? T : 1, H, E);
-  if (static_cast<size_t>(ns) * T * E * sizeof(float) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+  if (moe::route_scratch_bytes(T, H, E) > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   float* scratch = nullptr;
   const moe_status st = scratch_on_current_device(&scratch);

@@ -363,3 +363,57 @@ def test_forward_sampled(M, name):
     w = synth.WORKLOADS[name]
     toks = np.random.default_rng(3).choice(w.T, 4, replace=False)
     _check_forward(M, w, tokens=np.sort(toks))
+
+
+def test_forward_pad_only_row_blocks(M):
+    # align 256 gives 128-row GEMM blocks; experts with few rows leave blocks that hold only padding
+    w = synth.custom(T=12, H=256, I=256, E=8, K=2, align=256, score_fn="sqrt_softplus", e_bias=True, seed=11)
+    _check_forward(M, w)
+
+
+def _run_stages(M, w, inp, stack):
+    """The layer as five separate C-ABI calls (route, permute, L1, L2, reduce)."""
+    T = inp["hidden"].shape[0]
+    w13, w2 = device_weights(M, stack, w.fmt)
+    ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align)
+    U = M.msum_upper(T, w.K, w.E, w.align)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    ids, tw = torch.empty(T, w.K, **i32), torch.empty(T, w.K, dtype=torch.float32, device="cuda")
+    xq, xsf = torch.empty(T, w.H, **u8), torch.empty(T, w.H // 128, **u8)
+    M.route(dev_bf16(inp["hidden"]), dev(inp["w_gate"]), None if inp["gate_bias"] is None else dev(inp["gate_bias"]),
+            None if inp["e_score_bias"] is None else dev(inp["e_score_bias"]), w.K, w.score_fn, w.renormalize,
+            ids, tw, ws, x_q=xq, x_sf=xsf)
+    srt, eid, inv, ms = torch.empty(U, **i32), torch.empty(U, **i32), torch.empty(T, w.K, **i32), torch.empty(1, **i32)
+    xp = torch.zeros(U, w.H, **u8)
+    xpsf = torch.zeros(M.act_sf_tiled_bytes(U, w.H // 128, w.align), **u8)
+    M.permute(ids, w.E, w.align, srt, eid, inv, ms, ws, x_q=xq, x_sf=xsf, x_perm=xp, x_perm_sf=xpsf)
+    hq = torch.zeros(U, w.I, **u8)
+    hsf = torch.zeros(M.act_sf_tiled_bytes(U, w.I // 128, w.align), **u8)
+    M.grouped_gemm_l1_swiglu(xp, xpsf, eid, ms, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
+    y = torch.zeros(U, w.H, dtype=torch.bfloat16, device="cuda")
+    M.grouped_gemm_l2(hq, hsf, eid, ms, T, w.K, w.H, w.I, w.E, w.align, w2, y, ws)
+    out = torch.empty(T, w.H, dtype=torch.bfloat16, device="cuda")
+    M.unpermute_reduce(y, inv, tw, out)
+    assert M.get_error(ws) == M.OK
+    return out.cpu()
+
+
+@pytest.mark.parametrize("case", ["tiny", "tiny77", "align1", "decode", "tiny_nvfp4"])
+def test_forward_matches_stage_calls(M, case):
+    # moe_forward fuses launches (one L1+L2 launch, the reduce in the L2 epilogue for small T); the
+    # arithmetic is the same as the separate calls', so the outputs agree bit for bit
+    T = None
+    if case == "align1":
+        w = synth.custom(T=23, H=512, I=256, E=16, K=4, align=1, score_fn="sqrt_softplus", e_bias=True, seed=5)
+    elif case == "tiny_nvfp4":
+        w = synth.custom(T=40, H=512, I=256, E=16, K=4, align=16, score_fn="sqrt_softplus", e_bias=True,
+                         fmt="nvfp4", seed=9)
+    else:
+        w = synth.WORKLOADS["decode" if case == "decode" else "tiny"]
+        T = 77 if case == "tiny77" else None
+    inp = synth.layer_inputs(w, T)
+    stack = synth.all_expert_weights(w)
+    a = _run_forward(M, w, inp, stack)["out"]
+    b = _run_stages(M, w, inp, stack)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
