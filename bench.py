@@ -209,8 +209,12 @@ def algorithmic_bytes(w, n_touched):
         w2 = n_touched * (w.H * w.I // 2 + w.H * w.I // 16 + 4)
     l1 = w13 + TK * (w.H + w.H // 128) + TK * (w.I + w.I // 128)
     l2 = w2 + TK * (w.I + w.I // 128) + TK * w.H * 2
-    return {"l1": l1, "l2": l2,
+    return {"l1": l1, "l2": l2, "ffn": w13 + w2 + TK * (w.H + w.H // 128) + TK * w.H * 2,
             "layer": w13 + w2 + 4 * w.E * w.H + 2 * w.T * w.H * 2}
+
+
+def kernel_name(stage):
+    return "L1+L2 grouped GEMM (one launch)" if stage == "ffn" else f"{stage} grouped GEMM"
 
 
 def run_ours(args, w):
@@ -303,40 +307,52 @@ def run_ours(args, w):
     hq = torch.empty(U, w.I, dtype=torch.uint8, device=dev)
     hsf = torch.empty(M.act_sf_tiled_bytes(U, w.I // 128, w.align), dtype=torch.uint8, device=dev)
     y = torch.empty(U, w.H, dtype=torch.bfloat16, device=dev)
-    stages = ["route", "permute", "l1", "l2", "reduce"]
+    # MXFP4: the expert FFN is one launch (moe_grouped_ffn), timed as one stage; NVFP4: L1 and L2 apart
+    fused = w.fmt == "mxfp4"
+    stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     barrier()
     for i in range(K):
         flush.fill_(i & 0xFF)
         e = sev[i]
-        e[0].record()
+        j = 0
+        e[j].record()
         M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
-        e[1].record()
+        j += 1
+        e[j].record()
         M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
                   x_perm_sf=xpsf)
-        e[2].record()
-        M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
-        e[3].record()
-        M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w2, y, ws)
-        e[4].record()
+        j += 1
+        e[j].record()
+        if fused:
+            M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, w2, hq, hsf, y, ws)
+        else:
+            M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
+            j += 1
+            e[j].record()
+            M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w2, y, ws)
+        j += 1
+        e[j].record()
         M.unpermute_reduce(y, inv, tw, out)
-        e[5].record()
+        j += 1
+        e[j].record()
     barrier()
     stage_ms = {s: statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(K)) for j, s in enumerate(stages)}
     n_touched = int((cnt.cpu() > 0).sum().item())
     ab = algorithmic_bytes(w, n_touched)
     hbm, bf16, peak_src = peaks()
-    top = max(("l1", "l2"), key=lambda s: stage_ms[s])
+    top = "ffn" if fused else max(("l1", "l2"), key=lambda s: stage_ms[s])
     kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc", "gemm.cu" if w.fmt == "mxfp4" else "gemm_nv.cu")
     tk = w.T * w.K
     flops = {"l1": 2.0 * tk * 2 * w.I * w.H, "l2": 2.0 * tk * w.I * w.H}
+    flops["ffn"] = flops["l1"] + flops["l2"]
     if w.T * w.K >= 4096:
         # prefill: a dense contraction.  MXFP4 runs FP8 x FP4 block-scaled MMAs (FP8 rate: the measured
         # bf16 peak x the nominal 4.5/2.25 ratio); NVFP4 runs bf16 MMAs (the measured bf16 peak).
         peak = bf16 * (2.0 if w.fmt == "mxfp4" else 1.0)
         achieved = flops[top] / (stage_ms[top] / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                    "traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": f"{top} grouped GEMM",
+                    "traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": kernel_name(top),
                     "algorithmic_flops": flops[top],
                     "peak_source": f"{peak_src} bf16 GEMM" + (" x 2 (FP8 / bf16 nominal ratio)" if w.fmt == "mxfp4" else ""),
                     "stage_ms": stage_ms, "experts_touched": n_touched,
@@ -344,7 +360,7 @@ def run_ours(args, w):
     else:
         achieved = ab[top] / (stage_ms[top] / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": f"{top} grouped GEMM",
+                    "traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": kernel_name(top),
                     "algorithmic_bytes": ab[top], "peak_source": f"{peak_src} HBM copy bandwidth",
                     "stage_ms": stage_ms, "experts_touched": n_touched,
                     "layer_frac": ab["layer"] / (ms / 1e3) / 1e9 / hbm}

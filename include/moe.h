@@ -201,6 +201,17 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
                                int align, moe_weight w2, uint16_t* y_perm, void* ws,
                                size_t ws_bytes, void* stream);
 
+/* Both expert GEMMs in one call (MegaMoE page 二、阶段 2-5 as one persistent kernel): the results
+ * of moe_grouped_gemm_l1_swiglu (h_q, h_sf) and of moe_grouped_gemm_l2 (y_perm), bit for bit.
+ * With MXFP4 weights it is one cooperative launch in which an L2 tile starts once every L1 tile
+ * of its row block is stored; it needs the full moe_workspace_size() workspace (per-row-block
+ * counters that the launch leaves at zero).  With NVFP4 weights the two calls run in turn.
+ * Arguments as for the two calls; h_q/h_sf/y_perm 16-byte aligned. */
+moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+                           const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
+                           moe_weight w13, moe_weight w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* Weighted unpermute-reduce (note §9.6 "gather 再讲一遍"; MegaMoE page 阶段 5):
  *   out[t] = bf16_rne( sum_{k=0}^{K-1} topk_w[t,k] * y_perm[inv_perm[t,k]] ), summed in fp32
  *   in k order.  y_perm [>= max(inv_perm)+1, H] bf16, inv_perm [T,K], topk_w [T,K] fp32,
@@ -210,7 +221,8 @@ moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
                                 void* stream);
 
 /* The whole layer in one call: route -> permute -> L1 -> L2 -> reduce on `stream`, with all
- * intermediates in the workspace.  The optional index outputs (any may be NULL) receive the
+ * intermediates in the workspace (L1 and L2 as in moe_grouped_ffn; up to 32 tokens the reduce
+ * runs inside the L2 epilogue, with the same arithmetic as moe_unpermute_reduce).  The optional index outputs (any may be NULL) receive the
  * same values as the individual calls would produce; out [T, H] bf16. */
 moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                        const float* e_score_bias, int T, int H, int I, int E, int K, int align,

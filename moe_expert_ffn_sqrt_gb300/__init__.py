@@ -67,6 +67,8 @@ def lib():
         L.moe_grouped_gemm_l1_swiglu.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
         L.moe_grouped_gemm_l2.restype = S
         L.moe_grouped_gemm_l2.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, Z, P]
+        L.moe_grouped_ffn.restype = S
+        L.moe_grouped_ffn.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, Z, P]
         L.moe_unpermute_reduce.restype = S
         L.moe_unpermute_reduce.argtypes = [P, P, P, I, I, I, P, P]
         L.moe_forward.restype = S
@@ -246,6 +248,15 @@ def grouped_gemm_l2(h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, y_pe
                                      _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
                                      T, K, H, I, E, align, w2.c(), _ptr(y_perm, torch.bfloat16, "y_perm"),
                                      _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_gemm_l2")
+
+
+def grouped_ffn(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws):
+    """L1 + SwiGLU + requant and L2 in one call (one launch for MXFP4 weights)."""
+    _check(lib().moe_grouped_ffn(_ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+                                 _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
+                                 T, K, H, I, E, align, w13.c(), w2.c(), _ptr(h_q, torch.uint8, "h_q"),
+                                 _ptr(h_sf, torch.uint8, "h_sf"), _ptr(y_perm, torch.bfloat16, "y_perm"),
+                                 _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_ffn")
 
 
 def unpermute_reduce(y_perm, inv_perm, topk_w, out):

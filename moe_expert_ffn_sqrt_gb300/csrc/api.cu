@@ -150,10 +150,10 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
                                   renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, S(stream)));
 }
 
-static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
-                                 int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
-                                 const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                                 void* ws, size_t ws_bytes, void* stream, uint32_t* clear, int n_clear) {
+moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
+                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                       void* ws, size_t ws_bytes, void* stream) {
   if (T < 0 || K <= 0 || E <= 0 || K > E || align < 1 || align > 256 || (align & (align - 1)))
     return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
@@ -166,15 +166,7 @@ static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, i
   const size_t U = moe_msum_upper(T, K, E, align);
   return cuda_status(launch_permute(topk_ids, T, K, E, align, static_cast<int>(U), sorted_token_ids, expert_ids,
                                     inv_perm, m_sum, expert_counts, x_q, x_sf, H, x_perm, x_perm_sf,
-                                    status_of(ws), S(stream), clear, n_clear));
-}
-
-moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
-                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
-                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                       void* ws, size_t ws_bytes, void* stream) {
-  return permute_common(topk_ids, T, K, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, expert_counts, x_q,
-                        x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream, nullptr, 0);
+                                    status_of(ws), S(stream)));
 }
 
 // Launch description of one MXFP4 GEMM (L1: x = x_perm [U, H] against W13; L2: x = h [U, I] against W2).
@@ -260,6 +252,44 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
                      ws_bytes, stream);
 }
 
+// L1 + SwiGLU + requant and L2.  MXFP4: one cooperative launch (L2 tiles start as soon as the
+// h rows of their block are stored).  NVFP4: the two GEMM calls one after the other.
+static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+                             const int32_t* m_sum, int T, int K, int H, int I, int E, int align, const moe_weight& w13,
+                             const moe_weight& w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
+                             size_t ws_bytes, void* stream, const FusedReduce* red) {
+  if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
+    moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
+                                nullptr, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws,
+                       ws_bytes, stream, red);
+  }
+  if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  if (!x_perm || !x_perm_sf || !expert_ids || !m_sum || !h_q || !h_sf || !y) return MOE_ERR_INVALID_ARG;
+  if (!weight_ok(w13, E, 2 * I, H, 2) || !weight_ok(w2, E, H, I, 1)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_perm, 16) || !aligned(x_perm_sf, 16) || !aligned(h_q, 16) || !aligned(h_sf, 16) || !aligned(y, 16))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const WsLayout L = layout(T, H, I, E, K, align);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  if (U == 0) return MOE_OK;
+  GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
+  GemmLaunch l2 = mx_launch(false, h_q, h_sf, expert_ids, m_sum, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
+  if (red) l2.red = *red;
+  uint32_t* ready = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.ready);
+  return cuda_status(launch_ffn(l1, l2, ready, S(stream)));
+}
+
+moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+                           const int32_t* m_sum, int T, int K, int H, int I, int E, int align, moe_weight w13,
+                           moe_weight w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                           void* stream) {
+  return ffn_common(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws,
+                    ws_bytes, stream, nullptr);
+}
+
 moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int K,
                                 int H, uint16_t* out, void* stream) {
   if (T < 0 || K <= 0 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
@@ -298,11 +328,7 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
   moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
                             xq, xsf, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  const size_t U = moe_msum_upper(T, K, E, align);
-  const bool mx = w13.fmt == MOE_W_MXFP4 && w2.fmt == MOE_W_MXFP4;
-  uint32_t* ready = reinterpret_cast<uint32_t*>(b + L.ready);
-  st = permute_common(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream,
-                      mx ? ready : nullptr, mx ? static_cast<int>(ffn_ready_words(static_cast<int>(U), align)) : 0);
+  st = moe_permute(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
   const bool fuse_reduce = T <= kFusedReduceMaxTokens;
   FusedReduce red{};
@@ -314,20 +340,9 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
     red.tickets = reinterpret_cast<uint32_t*>(b + L.tickets);
     red.K = K;
   }
-  if (mx) {
-    // L1 and L2 in one persistent launch: L2 tiles fill the SMs as soon as their rows' h is ready
-    GemmLaunch l1 = mx_launch(true, xp, xpsf, eids, ms, H, I, E, align, U, w13, hq, hsf, nullptr, ws);
-    GemmLaunch l2 = mx_launch(false, hq, hsf, eids, ms, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
-    l2.red = red;
-    if (launch_ffn(l1, l2, ready, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
-  } else {
-    st = moe_grouped_gemm_l1_swiglu(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, hq, hsf, ws, ws_bytes, stream);
-    if (st != MOE_OK) return st;
-    st = gemm_common(false, hq, hsf, eids, ms, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws, ws_bytes, stream,
-                     fuse_reduce ? &red : nullptr);
-    if (st != MOE_OK) return st;
-  }
-  if (fuse_reduce) return MOE_OK;
+  st = ffn_common(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y, ws, ws_bytes, stream,
+                  fuse_reduce ? &red : nullptr);
+  if (st != MOE_OK || fuse_reduce) return st;
   return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
 }
 

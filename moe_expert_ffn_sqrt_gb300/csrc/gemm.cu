@@ -85,8 +85,10 @@ struct GemmArgs {
   uint16_t* y;                  // L2 out [U, H] bf16
   uint32_t* status;
   int sf_nb;                    // blocks of the tiled token-scale layouts
-  uint32_t* ready;              // both phases in one launch: [ceil(U/BN)] finished L1 tiles per row
-                                // block, zero at launch; nullptr otherwise
+  uint32_t* ready;              // both phases in one launch: [n_ready] finished L1 tiles per row
+                                // block, then one exit counter; zero at launch and left at zero by
+                                // the last CTA to exit; nullptr otherwise
+  int n_ready;                  // ceil(U/BN)
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
@@ -143,7 +145,8 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 // written by other CTAs: its producer first waits until ready[rb] counts all n_wt L1 tiles of the
 // block (each L1 item's epilogue adds one after its stores).  Every CTA finishes all of its L1
 // items before it takes an L2 item and the launch is cooperative (all CTAs resident), so every
-// awaited item is running or done; the wait is bounded all the same.
+// awaited item is running or done; the wait is bounded all the same.  The last CTA to exit
+// (counted in ready[n_ready]) sets all counters back to zero: no CTA can still be waiting then.
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
@@ -421,6 +424,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (a.ready != nullptr) {
+    __shared__ int s_last_cta;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_last_cta = atomicAdd(a.ready + a.n_ready, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (s_last_cta) {
+      __threadfence();
+      for (int i = threadIdx.x; i <= a.n_ready; i += blockDim.x) a.ready[i] = 0;
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------------
@@ -492,8 +507,9 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
   return make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN);
 }
 
-// l1 and/or l2 (non-null ones run).  With both, `ready` ([ceil(U/BN)] words, zero) orders the
-// phases and the launch is cooperative so that all CTAs are resident together.
+// l1 and/or l2 (non-null ones run).  With both, `ready` (ffn_ready_words words, zero; the kernel
+// leaves them at zero) orders the phases and the launch is cooperative so that all CTAs are
+// resident together.
 template <int BN>
 static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* ready, cudaStream_t stream) {
   using C = GemmCfg<BN>;
@@ -522,6 +538,7 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   a.status = any.status;
   a.sf_nb = act_sf_blocks(any.U, BN);
   a.ready = (l1 && l2) ? ready : nullptr;
+  a.n_ready = (any.U + BN - 1) / BN;
   if (l2) a.red = l2->red;
   const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
   int grid = num_sms();
@@ -563,7 +580,7 @@ cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* rea
 
 size_t ffn_ready_words(int U, int align) {
   const int bn = gemm_block_n(align);
-  return static_cast<size_t>((U + bn - 1) / bn);
+  return static_cast<size_t>((U + bn - 1) / bn) + 1;   // one counter per row block + exit counter
 }
 
 // ------------------------------------------------------------------------------------------

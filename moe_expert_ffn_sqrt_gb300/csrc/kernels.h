@@ -21,7 +21,7 @@ size_t permute_smem_bytes(int E);
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, cudaStream_t stream, uint32_t* clear = nullptr, int n_clear = 0);
+                           uint32_t* status, cudaStream_t stream);
 
 // gemm.cu
 struct GemmLaunch {
@@ -42,7 +42,8 @@ int weight_tiles(int N, int pair);
 size_t packed_weight_bytes(int E, int N, int Kd, int pair);
 int gemm_block_n(int align);
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
-// L1 and L2 in one cooperative launch; `ready` holds ffn_ready_words(U, align) zero words.
+// L1 and L2 in one cooperative launch; `ready` holds ffn_ready_words(U, align) words that are zero
+// before the launch and zero again after it.
 cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* ready, cudaStream_t stream);
 size_t ffn_ready_words(int U, int align);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,

@@ -27,8 +27,6 @@ struct PermuteArgs {
   int32_t* m_sum;
   int32_t* counts;       // optional
   uint32_t* status;
-  uint32_t* clear;       // optional: n_clear words zeroed for the kernels that follow (GEMM counters)
-  int n_clear;
 };
 
 __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteArgs a) {
@@ -127,7 +125,6 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteA
   if (a.counts)
     for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
   if (tid == 0) *a.m_sum = msum;
-  for (int i = tid; i < a.n_clear; i += kPermThreads) a.clear[i] = 0;
 }
 
 // Small problems (T*K <= 1024): one thread per (t,k) pair.  A pair's rank within its expert is
@@ -215,7 +212,6 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
     if (a.counts)
       for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
     if (tid == 0) *a.m_sum = msum;
-    for (int i = tid; i < a.n_clear; i += kPermThreads) a.clear[i] = 0;
   }
   if (x_perm != nullptr && N <= kSmallCopyPairs) {
     const int chunks = H / 16, slabs = H / 128;
@@ -270,8 +266,8 @@ size_t permute_smem_bytes(int E) { return static_cast<size_t>(kPermWarps + 2) * 
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, cudaStream_t stream, uint32_t* clear, int n_clear) {
-  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status, clear, n_clear};
+                           uint32_t* status, cudaStream_t stream) {
+  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status};
   const int bt = act_sf_block_rows(align), nb = act_sf_blocks(U, bt);
   const long long npairs = static_cast<long long>(T) * K;
   cudaError_t err;

@@ -417,3 +417,52 @@ def test_forward_matches_stage_calls(M, case):
     a = _run_forward(M, w, inp, stack)["out"]
     b = _run_stages(M, w, inp, stack)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("case", ["tiny", "align1", "pad_only", "nvfp4"])
+def test_grouped_ffn_matches_separate_gemms(M, case):
+    # moe_grouped_ffn = moe_grouped_gemm_l1_swiglu then moe_grouped_gemm_l2, bit for bit; called twice
+    # in a row, since its per-row-block counters must be back at zero after each call
+    if case == "align1":
+        w = synth.custom(T=23, H=512, I=256, E=16, K=4, align=1, score_fn="sqrt_softplus", e_bias=True, seed=5)
+    elif case == "pad_only":
+        w = synth.custom(T=12, H=256, I=256, E=8, K=2, align=256, score_fn="sqrt_softplus", e_bias=True, seed=11)
+    elif case == "nvfp4":
+        w = synth.custom(T=40, H=512, I=256, E=16, K=4, align=16, score_fn="sqrt_softplus", e_bias=True,
+                         fmt="nvfp4", seed=9)
+    else:
+        w = synth.WORKLOADS["tiny"]
+    inp = synth.layer_inputs(w)
+    T = inp["hidden"].shape[0]
+    stack = synth.all_expert_weights(w)
+    w13, w2 = device_weights(M, stack, w.fmt)
+    ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align)
+    U = M.msum_upper(T, w.K, w.E, w.align)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    ids, tw = torch.empty(T, w.K, **i32), torch.empty(T, w.K, dtype=torch.float32, device="cuda")
+    xq, xsf = torch.empty(T, w.H, **u8), torch.empty(T, w.H // 128, **u8)
+    M.route(dev_bf16(inp["hidden"]), dev(inp["w_gate"]), None if inp["gate_bias"] is None else dev(inp["gate_bias"]),
+            None if inp["e_score_bias"] is None else dev(inp["e_score_bias"]), w.K, w.score_fn, w.renormalize,
+            ids, tw, ws, x_q=xq, x_sf=xsf)
+    srt, eid, inv, ms = torch.empty(U, **i32), torch.empty(U, **i32), torch.empty(T, w.K, **i32), torch.empty(1, **i32)
+    xp = torch.zeros(U, w.H, **u8)
+    xpsf = torch.zeros(M.act_sf_tiled_bytes(U, w.H // 128, w.align), **u8)
+    M.permute(ids, w.E, w.align, srt, eid, inv, ms, ws, x_q=xq, x_sf=xsf, x_perm=xp, x_perm_sf=xpsf)
+    sfb = M.act_sf_tiled_bytes(U, w.I // 128, w.align)
+    hq0, hsf0 = torch.zeros(U, w.I, **u8), torch.zeros(sfb, **u8)
+    y0 = torch.zeros(U, w.H, dtype=torch.bfloat16, device="cuda")
+    M.grouped_gemm_l1_swiglu(xp, xpsf, eid, ms, T, w.K, w.H, w.I, w.E, w.align, w13, hq0, hsf0, ws)
+    M.grouped_gemm_l2(hq0, hsf0, eid, ms, T, w.K, w.H, w.I, w.E, w.align, w2, y0, ws)
+    ms_h = int(ms.item())
+    real = (eid[:ms_h] >= 0).nonzero().flatten()
+    for _ in range(2):
+        hq, hsf = torch.full((U, w.I), 0x7F, **u8), torch.zeros(sfb, **u8)
+        y = torch.zeros(U, w.H, dtype=torch.bfloat16, device="cuda")
+        M.grouped_ffn(xp, xpsf, eid, ms, T, w.K, w.H, w.I, w.E, w.align, w13, w2, hq, hsf, y, ws)
+        assert M.get_error(ws) == M.OK
+        assert torch.equal(hq[real], hq0[real])
+        assert torch.equal(y[real].view(torch.int16), y0[real].view(torch.int16))
+        h_rows = M.act_sf_untile(hsf.cpu().numpy(), U, w.I // 128, w.align)
+        h_rows0 = M.act_sf_untile(hsf0.cpu().numpy(), U, w.I // 128, w.align)
+        assert np.array_equal(h_rows[real.cpu().numpy()], h_rows0[real.cpu().numpy()])
