@@ -89,6 +89,7 @@ struct GemmArgs {
                                 // block, then one exit counter; zero at launch and left at zero by
                                 // the last CTA to exit; nullptr otherwise
   int n_ready;                  // ceil(U/BN)
+  int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
@@ -109,10 +110,14 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& a, int t) {
 
 // Next work item after (t, e): smallest expert id > e present in the row block of item t, else
 // the first expert of this CTA's next item.  Rows are sorted by expert (ignoring -1).  Row
-// blocks past m_sum hold no rows: the rest of that phase is skipped.
+// blocks past m_sum hold no rows: the rest of that phase is skipped.  Called by whole warps.
+// When the permute alignment is a multiple of BN every block lies inside one expert's segment
+// (real rows first, then padding), so the block's first entry names its only expert (-1: the
+// block is padding); otherwise the warp scans the block's entries in one round of loads.
 template <int BN>
 __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, int& e) {
   const int G = gridDim.x, n0 = a.ph[0].n_tiles, total = n0 + a.ph[1].n_tiles;
+  const int lane = threadIdx.x & 31;
   while (t < total) {
     const Item it = decode_item(a, t);
     const int r0 = it.rb * BN;
@@ -122,11 +127,28 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, i
       e = -1;
       continue;
     }
-    const int rend = min(r0 + BN, msum);
-    for (int r = r0; r < rend; ++r) {
-      const int x = __ldg(a.expert_ids + r);
-      if (x > e) {
-        e = x;
+    if (a.one_expert_blocks) {
+      if (e < 0) {
+        const int x = __ldg(a.expert_ids + r0);
+        if (x >= 0) {
+          e = x;
+          return true;
+        }
+      }
+    } else {
+      const int rend = min(r0 + BN, msum);
+      int best = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < (BN + 31) / 32; ++j) {
+        const int r = r0 + j * 32 + lane;
+        if (r < rend) {
+          const int x = __ldg(a.expert_ids + r);
+          if (x > e && x < best) best = x;
+        }
+      }
+      best = __reduce_min_sync(0xffffffffu, best);
+      if (best != 0x7fffffff) {
+        e = best;
         return true;
       }
     }
@@ -539,6 +561,7 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   a.sf_nb = act_sf_blocks(any.U, BN);
   a.ready = (l1 && l2) ? ready : nullptr;
   a.n_ready = (any.U + BN - 1) / BN;
+  a.one_expert_blocks = any.align % BN == 0;
   if (l2) a.red = l2->red;
   const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
   int grid = num_sms();

@@ -59,19 +59,39 @@ struct NvArgs {
   int out_cols;
   int sf_nb;
   int n_tiles;
+  int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
 template <int BN>
 __device__ __forceinline__ bool nv_next_item(const NvArgs& a, int msum, int& t, int& e) {
+  // as next_item in gemm.cu: called by whole warps; one load per block when blocks hold one expert
+  const int lane = threadIdx.x & 31;
   while (t < a.n_tiles) {
     const int r0 = (t / a.n_wt) * BN;
     if (r0 >= msum) return false;
-    const int rend = min(r0 + BN, msum);
-    for (int r = r0; r < rend; ++r) {
-      const int x = __ldg(a.expert_ids + r);
-      if (x > e) {
-        e = x;
+    if (a.one_expert_blocks) {
+      if (e < 0) {
+        const int x = __ldg(a.expert_ids + r0);
+        if (x >= 0) {
+          e = x;
+          return true;
+        }
+      }
+    } else {
+      const int rend = min(r0 + BN, msum);
+      int best = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < (BN + 31) / 32; ++j) {
+        const int r = r0 + j * 32 + lane;
+        if (r < rend) {
+          const int x = __ldg(a.expert_ids + r);
+          if (x > e && x < best) best = x;
+        }
+      }
+      best = __reduce_min_sync(0xffffffffu, best);
+      if (best != 0x7fffffff) {
+        e = best;
         return true;
       }
     }
@@ -473,6 +493,7 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.out_cols = L1 ? L.I : L.w_rows;
   a.sf_nb = act_sf_blocks(L.U, BN);
   a.n_tiles = ((L.U + BN - 1) / BN) * a.n_wt;
+  a.one_expert_blocks = L.align % BN == 0;
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
