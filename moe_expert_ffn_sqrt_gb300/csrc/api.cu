@@ -147,7 +147,8 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
   if (T == 0) return MOE_OK;
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
   return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
-                                  renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, S(stream)));
+                                  renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, status_of(ws),
+                                  S(stream)));
 }
 
 moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,

@@ -14,7 +14,7 @@ size_t route_scratch_bytes(int T, int H, int E);   // partial sums + ticket slot
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         cudaStream_t stream);
+                         uint32_t* status, cudaStream_t stream);
 
 // permute.cu
 size_t permute_smem_bytes(int E);
@@ -23,7 +23,16 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
                            uint32_t* status, cudaStream_t stream);
 
+// gate.cu (T > 16: gate GEMM on the tensor cores, three exact bf16 parts of the fp32 gate weight)
+int gate_nsplit(int T, int H, int E);
+size_t gate_parts_bytes(int T, int H, int E);
+cudaError_t launch_gate_mma(const uint16_t* hidden, const float* w_gate, int T, int H, int E, int nsplit,
+                            uint16_t* parts, float* partial, uint32_t* status, cudaStream_t stream);
+
 // gemm.cu
+// 2D tiled tensor map with 128-byte swizzle (inner extent `inner` elements, `outer` rows).
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 struct GemmLaunch {
   const uint8_t* w;            // packed weight stream
   const uint8_t* x;            // [U, Kd] E4M3

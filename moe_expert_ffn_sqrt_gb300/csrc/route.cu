@@ -1,5 +1,5 @@
-// Routing: gate GEMM (split over H, deterministic), scoring + biased top-K, FP8 activation
-// quantisation.  Page "DeepSeek V4 MegaMoE Kernel 深度解析", 经典 MoE 的计算过程 / 第一步：路由,
+// Routing: gate GEMM (split over H, deterministic; on the tensor cores above 16 tokens, see
+// gate.cu), scoring + biased top-K, FP8 activation quantisation.  Page "DeepSeek V4 MegaMoE Kernel 深度解析", 经典 MoE 的计算过程 / 第一步：路由,
 // and the CUDA tag page teaser row "Fused TopK Bias Routing" (sqrt(softplus), e_score_correction_bias).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -8,59 +8,6 @@
 #include "kernels.h"
 
 namespace moe {
-
-// ------------------------------------------------------------------------------------------
-// Gate GEMM: partial[split][t][e] = sum_{h in split} hidden[t,h] * w_gate[e,h].
-// CTA tile 32 tokens x 64 experts, H walked in chunks of 32; 256 threads, 2x4 outputs each.
-constexpr int GT = 32, GE = 64, GH = 32;
-
-__global__ void __launch_bounds__(256) gate_gemm_kernel(const uint16_t* __restrict__ hidden,
-                                                        const float* __restrict__ wg, int T, int H, int E,
-                                                        int h_per_split, float* __restrict__ partial) {
-  __shared__ float xs[GH][GT + 1];
-  __shared__ float ws[GH][GE + 1];
-  const int t0 = blockIdx.x * GT, e0 = blockIdx.y * GE, split = blockIdx.z;
-  const int hbeg = split * h_per_split, hend = min(H, hbeg + h_per_split);
-  const int tid = threadIdx.x;
-  const int tr = (tid / 16) * 2;   // token rows tr, tr+1
-  const int ec = (tid % 16) * 4;   // expert cols ec..ec+3
-  float acc[2][4] = {};
-  for (int h0 = hbeg; h0 < hend; h0 += GH) {
-    // hidden tile: 32 tokens x 32 h  (1024 values, 4 per thread)
-    for (int i = tid; i < GT * GH; i += 256) {
-      const int tt = i / GH, hh = i % GH;
-      const int t = t0 + tt, h = h0 + hh;
-      float v = 0.f;
-      if (t < T && h < hend) v = __uint_as_float(static_cast<uint32_t>(hidden[static_cast<size_t>(t) * H + h]) << 16);
-      xs[hh][tt] = v;
-    }
-    for (int i = tid; i < GE * GH; i += 256) {
-      const int ee = i / GH, hh = i % GH;
-      const int e = e0 + ee, h = h0 + hh;
-      ws[hh][ee] = (e < E && h < hend) ? wg[static_cast<size_t>(e) * H + h] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int hh = 0; hh < GH; ++hh) {
-      const float x0 = xs[hh][tr], x1 = xs[hh][tr + 1];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float w = ws[hh][ec + j];
-        acc[0][j] = fmaf(x0, w, acc[0][j]);
-        acc[1][j] = fmaf(x1, w, acc[1][j]);
-      }
-    }
-    __syncthreads();
-  }
-  for (int i = 0; i < 2; ++i) {
-    const int t = t0 + tr + i;
-    if (t >= T) continue;
-    for (int j = 0; j < 4; ++j) {
-      const int e = e0 + ec + j;
-      if (e < E) partial[(static_cast<size_t>(split) * T + t) * E + e] = acc[i][j];
-    }
-  }
-}
 
 // ------------------------------------------------------------------------------------------
 // Small batches (T <= kGemvT) use route_small_kernel below: CTA = 4 experts x one quarter of H.
@@ -397,19 +344,16 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
   if (threadIdx.x == 0) *ticket = 0;     // ready for the next call (the kernel boundary orders it)
 }
 
-int route_nsplit(int T, int H, int E) {
-  if (T <= kGemvT) return kGemvSplit;
-  const int tiles = ((T + GT - 1) / GT) * ((E + GE - 1) / GE);
-  int ns = (2 * 152 + tiles - 1) / tiles;
-  const int maxs = (H + 127) / 128;
-  if (ns > maxs) ns = maxs;
-  if (ns < 1) ns = 1;
-  return ns;
+int route_nsplit(int T, int H, int E) { return T <= kGemvT ? kGemvSplit : gate_nsplit(T, H, E); }
+
+static size_t partial_bytes(int T, int H, int E) {
+  return (static_cast<size_t>(route_nsplit(T > 0 ? T : 1, H, E)) * T * E * sizeof(float) + 255) / 256 * 256;
 }
 
 size_t route_scratch_bytes(int T, int H, int E) {
-  // partial sums, then one 256-byte slot for the small-batch kernel's ticket counter
-  return (static_cast<size_t>(route_nsplit(T > 0 ? T : 1, H, E)) * T * E * sizeof(float) + 255) / 256 * 256 + 256;
+  // partial sums; above 16 tokens the bf16 parts of the gate weight; one 256-byte slot for the
+  // small-batch kernel's ticket counter
+  return partial_bytes(T, H, E) + (T > kGemvT ? gate_parts_bytes(T, H, E) : 0) + 256;
 }
 
 template <int TT>
@@ -428,7 +372,7 @@ static void launch_route_small(const RouteFinishArgs& a, const float* w_gate, fl
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         cudaStream_t stream) {
+                         uint32_t* status, cudaStream_t stream) {
   const int ns = route_nsplit(T, H, E);
   RouteFinishArgs a;
   a.partial = partial;
@@ -455,11 +399,8 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
     return cudaGetLastError();
   }
   {
-    int hps = (H + ns - 1) / ns;
-    hps = (hps + GH - 1) / GH * GH;
-    dim3 g1((T + GT - 1) / GT, (E + GE - 1) / GE, ns);
-    gate_gemm_kernel<<<g1, 256, 0, stream>>>(hidden, w_gate, T, H, E, hps, partial);
-    cudaError_t err = cudaGetLastError();
+    uint16_t* parts = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(partial) + partial_bytes(T, H, E));
+    const cudaError_t err = launch_gate_mma(hidden, w_gate, T, H, E, ns, parts, partial, status, stream);
     if (err != cudaSuccess) return err;
   }
   const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;

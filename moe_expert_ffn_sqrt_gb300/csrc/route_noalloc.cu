@@ -71,7 +71,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_g
   const moe_status st = scratch_on_current_device(&scratch);
   if (st != MOE_OK) return st;
   const cudaError_t err = moe::launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
-                                            renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, scratch,
+                                            renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, scratch, nullptr,
                                             static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
