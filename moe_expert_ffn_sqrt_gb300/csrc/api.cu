@@ -28,7 +28,7 @@ struct WsLayout {
   size_t status = 0;
   size_t partial = 0, partial_bytes = 0;
   size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
-  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, ready = 0;
+  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, sched = 0;
   size_t total = 0;
 };
 
@@ -54,7 +54,7 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   L.y = off;          off = up(off + U * H * 2);
   L.xb = off;         off = up(off + U * (H > I ? H : I) * 2);   // bf16 activation rows (NVFP4 GEMMs)
   L.tickets = off;    off = up(off + static_cast<size_t>(T) * ((H + 255) / 256) * 4);   // fused reduce
-  L.ready = off;      off = up(off + ffn_ready_words(static_cast<int>(U), align) * 4);   // L1 -> L2 order
+  L.sched = off;      off = up(off + gemm_sched_words(static_cast<int>(U), align) * 4);   // GEMM work counters
   L.total = off;
   return L;
 }
@@ -233,9 +233,12 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     if (red) N.red = *red;
     return cuda_status(launch_gemm_nv(N, l1, S(stream)));
   }
+  const WsLayout Lw = layout(T, H, I, E, K, align);
+  if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
   GemmLaunch L = mx_launch(l1, x, x_sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
   if (red) L.red = *red;
-  return cuda_status(launch_gemm(L, l1, S(stream)));
+  uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + Lw.sched);
+  return cuda_status(launch_gemm(L, l1, sched, S(stream)));
 }
 
 moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
@@ -279,8 +282,8 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
   GemmLaunch l2 = mx_launch(false, h_q, h_sf, expert_ids, m_sum, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
   if (red) l2.red = *red;
-  uint32_t* ready = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.ready);
-  return cuda_status(launch_ffn(l1, l2, ready, S(stream)));
+  uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.sched);
+  return cuda_status(launch_ffn(l1, l2, sched, S(stream)));
 }
 
 moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,

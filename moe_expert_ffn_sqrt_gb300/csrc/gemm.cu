@@ -85,77 +85,62 @@ struct GemmArgs {
   uint16_t* y;                  // L2 out [U, H] bf16
   uint32_t* status;
   int sf_nb;                    // blocks of the tiled token-scale layouts
-  uint32_t* ready;              // both phases in one launch: [n_ready] finished L1 tiles per row
-                                // block, then one exit counter; zero at launch and left at zero by
-                                // the last CTA to exit; nullptr otherwise
+  uint32_t* sched;              // [n_ready + 2] words, zero at launch and left at zero by the last CTA
+                                // to exit: [0, n_ready) finished L1 tiles per row block (fused
+                                // launches), [n_ready] next work item, [n_ready + 1] exited CTAs
   int n_ready;                  // ceil(U/BN)
+  int fused;                    // both phases in one launch: L2 items wait for their block's L1 tiles
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
-// Work items are numbered L1 tiles first, then L2 tiles, each phase row-block major
-// (t = row_block * n_wt + weight_tile).  CTA b takes items b, b + G, b + 2G, ... in order.
+// Work items: the L1 tiles of the row blocks below m_sum, then their L2 tiles, each phase
+// row-block major (t = row_block * n_wt + weight_tile).  The producer warp of each CTA takes the
+// next index from a global counter, so items start in index order and a CTA that drew short
+// items draws more of them.  It hands (t, expert) to the MMA and epilogue warps through a small
+// ring in shared memory.
 struct Item {
   int phase, rb, wt;
 };
 
-__device__ __forceinline__ Item decode_item(const GemmArgs& a, int t) {
+__device__ __forceinline__ Item decode_item(const GemmArgs& a, int n0, int t) {
   Item it;
-  it.phase = t >= a.ph[0].n_tiles ? 1 : 0;
-  const int l = it.phase ? t - a.ph[0].n_tiles : t;
+  it.phase = t >= n0 ? 1 : 0;
+  const int l = it.phase ? t - n0 : t;
   it.rb = l / a.ph[it.phase].n_wt;
   it.wt = l - it.rb * a.ph[it.phase].n_wt;
   return it;
 }
 
-// Next work item after (t, e): smallest expert id > e present in the row block of item t, else
-// the first expert of this CTA's next item.  Rows are sorted by expert (ignoring -1).  Row
-// blocks past m_sum hold no rows: the rest of that phase is skipped.  Called by whole warps.
-// When the permute alignment is a multiple of BN every block lies inside one expert's segment
-// (real rows first, then padding), so the block's first entry names its only expert (-1: the
-// block is padding); otherwise the warp scans the block's entries in one round of loads.
+// Smallest expert id > e among the rows of item t's block (rows are sorted by expert, ignoring
+// -1).  Called by whole warps.  When the permute alignment is a multiple of BN every block lies
+// inside one expert's segment (real rows first, then padding), so the block's first entry names
+// its only expert (-1: the block is padding); otherwise the warp scans the block in one round.
 template <int BN>
-__device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, int& e) {
-  const int G = gridDim.x, n0 = a.ph[0].n_tiles, total = n0 + a.ph[1].n_tiles;
-  const int lane = threadIdx.x & 31;
-  while (t < total) {
-    const Item it = decode_item(a, t);
-    const int r0 = it.rb * BN;
-    if (r0 >= msum) {
-      if (it.phase == 1) return false;
-      t = n0 + ((static_cast<int>(blockIdx.x) - n0) % G + G) % G;   // this CTA's first L2 item
-      e = -1;
-      continue;
-    }
-    if (a.one_expert_blocks) {
-      if (e < 0) {
-        const int x = __ldg(a.expert_ids + r0);
-        if (x >= 0) {
-          e = x;
-          return true;
-        }
-      }
-    } else {
-      const int rend = min(r0 + BN, msum);
-      int best = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < (BN + 31) / 32; ++j) {
-        const int r = r0 + j * 32 + lane;
-        if (r < rend) {
-          const int x = __ldg(a.expert_ids + r);
-          if (x > e && x < best) best = x;
-        }
-      }
-      best = __reduce_min_sync(0xffffffffu, best);
-      if (best != 0x7fffffff) {
-        e = best;
-        return true;
-      }
-    }
-    t += G;
-    e = -1;
+__device__ __forceinline__ bool find_expert(const GemmArgs& a, int n0, int msum, int t, int& e) {
+  const int r0 = decode_item(a, n0, t).rb * BN;
+  if (a.one_expert_blocks) {
+    if (e >= 0) return false;
+    const int x = __ldg(a.expert_ids + r0);
+    if (x < 0) return false;
+    e = x;
+    return true;
   }
-  return false;
+  const int lane = threadIdx.x & 31;
+  const int rend = min(r0 + BN, msum);
+  int best = 0x7fffffff;
+#pragma unroll
+  for (int j = 0; j < (BN + 31) / 32; ++j) {
+    const int r = r0 + j * 32 + lane;
+    if (r < rend) {
+      const int x = __ldg(a.expert_ids + r);
+      if (x > e && x < best) best = x;
+    }
+  }
+  best = __reduce_min_sync(0xffffffffu, best);
+  if (best == 0x7fffffff) return false;
+  e = best;
+  return true;
 }
 
 // silu(g) * u with the fast exponential and division intrinsics: the result is requantised to
@@ -163,12 +148,15 @@ __device__ __forceinline__ bool next_item(const GemmArgs& a, int msum, int& t, i
 // have no slow path for the infinities that unused accumulator rows may hold.
 __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+constexpr int kItemSlots = 4;
+
 // Runs the L1 items, the L2 items, or both.  With both, an L2 item of row block rb reads h rows
-// written by other CTAs: its producer first waits until ready[rb] counts all n_wt L1 tiles of the
-// block (each L1 item's epilogue adds one after its stores).  Every CTA finishes all of its L1
-// items before it takes an L2 item and the launch is cooperative (all CTAs resident), so every
-// awaited item is running or done; the wait is bounded all the same.  The last CTA to exit
-// (counted in ready[n_ready]) sets all counters back to zero: no CTA can still be waiting then.
+// written by other CTAs: its producer first waits until sched[rb] counts all n_wt L1 tiles of the
+// block (each L1 item's epilogue adds one after its stores).  Items are drawn in index order, all
+// L1 items before any L2 item; a producer waits only while holding an L2 item, after issuing every
+// load of the items it drew before; and the launch is cooperative (all CTAs resident).  So every
+// awaited L1 item is running or done; the wait is bounded all the same.  The last CTA to exit sets
+// all counters back to zero: no CTA can still be waiting or drawing then.
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
@@ -183,7 +171,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* item_full = acc_empty + 1;             // [kItemSlots], producer arrives
+  uint64_t* item_empty = item_full + kItemSlots;   // [kItemSlots], MMA warp + epilogue arrive
+  int2* items = reinterpret_cast<int2*>(item_empty + kItemSlots);   // (t, e); t < 0 ends the work
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kItemSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -194,6 +185,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(smem_u32(acc_full), 1);
     mbar_init(smem_u32(acc_empty), 128);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(smem_u32(item_full + s), 1);
+      mbar_init(smem_u32(item_empty + s), 2);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     if (a.ph[0].n_tiles) {
@@ -214,6 +209,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int msum = *a.m_sum;
+  const int nrb = (msum + BN - 1) / BN;
+  const int n0 = a.ph[0].n_tiles ? nrb * a.ph[0].n_wt : 0;
+  const int n_items = n0 + (a.ph[1].n_tiles ? nrb * a.ph[1].n_wt : 0);
 
   if (warp == 0) {
     // ---------------- TMA producer (whole warp iterates, lane 0 issues) ----------------
@@ -221,24 +219,51 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t pol_x = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
-    int t = blockIdx.x, e = -1;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
-      const Item it = decode_item(a, t);
+    uint32_t islot = 0, iphase = 0;
+    int t = -1, e = -1;
+    bool ok = true;
+    while (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+      bool have = t >= 0 && find_expert<BN>(a, n0, msum, t, e);    // another expert of the same block
+      while (!have) {
+        int nt = 0;
+        if (lane == 0) nt = static_cast<int>(atomicAdd(a.sched + a.n_ready, 1u));
+        nt = __shfl_sync(0xffffffffu, nt, 0);
+        if (nt >= n_items) {
+          t = -1;
+          break;
+        }
+        t = nt;
+        e = -1;
+        have = find_expert<BN>(a, n0, msum, t, e);
+      }
+      if (!have) break;
+      // hand the item to the MMA and epilogue warps
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(item_empty + islot), iphase ^ 1, a.status));
+      if (!ok) break;
+      if (lane == 0) {
+        items[islot] = make_int2(t, e);
+        mbar_arrive(smem_u32(item_full + islot));
+      }
+      __syncwarp();
+      if (++islot == kItemSlots) {
+        islot = 0;
+        iphase ^= 1;
+      }
+      const Item it = decode_item(a, n0, t);
       const GemmPhase& P = a.ph[it.phase];
       const CUtensorMap* mw = it.phase ? &tmap_w2 : &tmap_w1;
       const CUtensorMap* mx = it.phase ? &tmap_x2 : &tmap_x1;
       const int r0 = it.rb * BN;
       const size_t chunk0 = (static_cast<size_t>(e) * P.n_wt + it.wt) * P.n_slabs;
-      bool ok = true;
-      if (it.phase == 1 && a.ready != nullptr) {
+      if (it.phase == 1 && a.fused) {
         // h rows of this block come from other CTAs' L1 epilogues
         if (lane == 0) {
           const uint32_t need = static_cast<uint32_t>(a.ph[0].n_wt);
-          if (ld_acquire_gpu(a.ready + it.rb) < need) {
+          if (ld_acquire_gpu(a.sched + it.rb) < need) {
             // start the item's weights towards L2 while waiting
             const size_t wb = chunk0 * C::W_CHUNK, nb = static_cast<size_t>(P.n_slabs) * C::W_CHUNK;
             if (wb + nb <= P.w_bytes && nb < (size_t(1) << 31)) bulk_prefetch_l2(P.w + wb, static_cast<uint32_t>(nb));
-            ok = wait_counter(a.ready + it.rb, need, a.status);
+            ok = wait_counter(a.sched + it.rb, need, a.status);
           }
           fence_proxy_async_global();
         }
@@ -275,10 +300,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           phase ^= 1;
         }
       }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
+    }
+    if (!ok) *abort_flag = 1;
+    // end of work for the other warps (if the ring does not free up they stop on their own waits)
+    if (__all_sync(0xffffffffu, mbar_wait(smem_u32(item_empty + islot), iphase ^ 1, a.status))) {
+      if (lane == 0) {
+        items[islot] = make_int2(-1, -1);
+        mbar_arrive(smem_u32(item_full + islot));
       }
+      __syncwarp();
     }
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       // let every copy issued into shared memory land before the CTA exits
@@ -289,10 +319,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t acc_phase = 0;
-    int t = blockIdx.x, e = -1;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_item<BN>(a, msum, t, e)) {
-      const int n_slabs = a.ph[decode_item(a, t).phase].n_slabs;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+    uint32_t islot = 0, iphase = 0;
+    while (true) {
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(item_full + islot), iphase, a.status));
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      const int2 item = items[islot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(item_empty + islot));
+      if (++islot == kItemSlots) {
+        islot = 0;
+        iphase ^= 1;
+      }
+      if (item.x < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int n_slabs = a.ph[decode_item(a, n0, item.x).phase].n_slabs;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
         for (int s = 0; s < n_slabs; ++s) {
@@ -336,14 +379,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const bool warp_has_rows = q * 32 < BN;  // warp-uniform
     const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0;
-    int t = blockIdx.x, e = -1;
-    while (next_item<BN>(a, msum, t, e)) {
-      const Item it = decode_item(a, t);
+    uint32_t islot = 0, iphase = 0;
+    while (true) {
+      bool ok = mbar_wait(smem_u32(item_full + islot), iphase, a.status);
+      const int2 item = items[islot];
+      ok = named_barrier_and(1, 128, ok);    // every epilogue thread has read the slot
+      if (ok && threadIdx.x == 64) mbar_arrive(smem_u32(item_empty + islot));
+      if (++islot == kItemSlots) {
+        islot = 0;
+        iphase ^= 1;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      if (item.x < 0) break;
+      const int e = item.y;
+      const Item it = decode_item(a, n0, item.x);
       const int r0 = it.rb * BN, wt = it.wt;
       const int row = r0 + m;
       const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
       const bool mine = row_e == e;
-      bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+      ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, 128, ok);    // one vote over the four epilogue warps
       if (!ok) {
         *abort_flag = 1;
@@ -358,14 +415,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           float h[128];
           float amax = 0.f;
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t g[16], u[16];
-            tc_ld_x16(acc + c0, g);
-            tc_ld_x16(acc + 128 + c0, u);
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t g[2][16], u[2][16];
+            tc_ld_x16(acc + c0, g[0]);
+            tc_ld_x16(acc + c0 + 16, g[1]);
+            tc_ld_x16(acc + 128 + c0, u[0]);
+            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
             tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              h[c0 + j] = silu_mul(__uint_as_float(g[j]), __uint_as_float(u[j]));
+            for (int j = 0; j < 32; ++j) {
+              h[c0 + j] = silu_mul(__uint_as_float(g[j >> 4][j & 15]), __uint_as_float(u[j >> 4][j & 15]));
               amax = fmaxf(amax, fabsf(h[c0 + j]));
             }
           }
@@ -390,19 +449,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               }
               dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            if (a.ready) fence_proxy_async_global();
+            if (a.fused) fence_proxy_async_global();
           }
         } else {
           tc_fence_before();
           mbar_arrive(smem_u32(acc_empty));
         }
-        if (a.ready) {
+        if (a.fused) {
           // publish the tile once the block's last expert pass is stored: bar.red doubles as the
           // barrier that orders all 128 threads' stores before the release below
           const bool later = row_e > e;
           if (!named_barrier_or(1, 128, later) && threadIdx.x == 64) {
             __threadfence();
-            atomicAdd(a.ready + it.rb, 1u);
+            atomicAdd(a.sched + it.rb, 1u);
           }
         }
       } else {
@@ -412,14 +471,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (warp_has_rows) {
           uint32_t packed[128];
 #pragma unroll
-          for (int c0 = 0; c0 < kTileRows; c0 += 16) {
-            uint32_t v[16];
-            tc_ld_x16(acc + c0, v);
+          for (int c0 = 0; c0 < kTileRows; c0 += 64) {
+            uint32_t v[4][16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tc_ld_x16(acc + c0 + 16 * j, v[j]);
             tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j])));
-              const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j + 1])));
+            for (int j = 0; j < 32; ++j) {
+              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j) & 15])));
+              const uint32_t hi =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j + 1) & 15])));
               packed[c0 / 2 + j] = lo | (hi << 16);
             }
           }
@@ -446,17 +507,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (a.ready != nullptr) {
-    __shared__ int s_last_cta;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      s_last_cta = atomicAdd(a.ready + a.n_ready, 1u) == gridDim.x - 1;
-    }
-    __syncthreads();
-    if (s_last_cta) {
-      __threadfence();
-      for (int i = threadIdx.x; i <= a.n_ready; i += blockDim.x) a.ready[i] = 0;
-    }
+  __shared__ int s_last_cta;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last_cta = atomicAdd(a.sched + a.n_ready + 1, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last_cta) {
+    __threadfence();
+    for (int i = threadIdx.x; i < a.n_ready + 2; i += blockDim.x) a.sched[i] = 0;
   }
 }
 
@@ -529,15 +588,16 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
   return make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN);
 }
 
-// l1 and/or l2 (non-null ones run).  With both, `ready` (ffn_ready_words words, zero; the kernel
-// leaves them at zero) orders the phases and the launch is cooperative so that all CTAs are
-// resident together.
+// l1 and/or l2 (non-null ones run).  `sched` holds gemm_sched_words(U, align) words that are zero
+// before the launch and zero again after it (work counter; with both phases also the per-row-block
+// counters that order them, and then the launch is cooperative so that all CTAs are resident).
 template <int BN>
-static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* ready, cudaStream_t stream) {
+static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   GemmArgs a{};
   CUtensorMap m[4];
   const GemmLaunch& any = l1 ? *l1 : *l2;
+  if (!sched) return cudaErrorInvalidValue;
   if (l1 && !make_phase<BN>(*l1, true, a.ph[0], m[0], m[1])) return cudaErrorInvalidValue;
   if (l2 && !make_phase<BN>(*l2, false, a.ph[1], m[2], m[3])) return cudaErrorInvalidValue;
   if (!l1) {
@@ -559,8 +619,9 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   a.y = l2 ? l2->y : nullptr;
   a.status = any.status;
   a.sf_nb = act_sf_blocks(any.U, BN);
-  a.ready = (l1 && l2) ? ready : nullptr;
+  a.sched = sched;
   a.n_ready = (any.U + BN - 1) / BN;
+  a.fused = (l1 && l2) ? 1 : 0;
   a.one_expert_blocks = any.align % BN == 0;
   if (l2) a.red = l2->red;
   const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
@@ -578,32 +639,32 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = a.ready ? 1 : 0;
+  cfg.numAttrs = a.fused ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
 }
 
 int gemm_block_n(int align) { return act_sf_block_rows(align); }
 
-static cudaError_t launch_bn(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* ready, cudaStream_t stream) {
+static cudaError_t launch_bn(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   switch (gemm_block_n((l1 ? l1 : l2)->align)) {
-    case 16: return launch_gemm_t<16>(l1, l2, ready, stream);
-    case 32: return launch_gemm_t<32>(l1, l2, ready, stream);
-    case 64: return launch_gemm_t<64>(l1, l2, ready, stream);
-    default: return launch_gemm_t<128>(l1, l2, ready, stream);
+    case 16: return launch_gemm_t<16>(l1, l2, sched, stream);
+    case 32: return launch_gemm_t<32>(l1, l2, sched, stream);
+    case 64: return launch_gemm_t<64>(l1, l2, sched, stream);
+    default: return launch_gemm_t<128>(l1, l2, sched, stream);
   }
 }
 
-cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream) {
-  return l1 ? launch_bn(&L, nullptr, nullptr, stream) : launch_bn(nullptr, &L, nullptr, stream);
+cudaError_t launch_gemm(const GemmLaunch& L, bool l1, uint32_t* sched, cudaStream_t stream) {
+  return l1 ? launch_bn(&L, nullptr, sched, stream) : launch_bn(nullptr, &L, sched, stream);
 }
 
-cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* ready, cudaStream_t stream) {
-  return launch_bn(&l1, &l2, ready, stream);
+cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* sched, cudaStream_t stream) {
+  return launch_bn(&l1, &l2, sched, stream);
 }
 
-size_t ffn_ready_words(int U, int align) {
+size_t gemm_sched_words(int U, int align) {
   const int bn = gemm_block_n(align);
-  return static_cast<size_t>((U + bn - 1) / bn) + 1;   // one counter per row block + exit counter
+  return static_cast<size_t>((U + bn - 1) / bn) + 2;   // row-block counters, work counter, exit counter
 }
 
 // ------------------------------------------------------------------------------------------

@@ -50,11 +50,11 @@ int num_sms();
 int weight_tiles(int N, int pair);
 size_t packed_weight_bytes(int E, int N, int Kd, int pair);
 int gemm_block_n(int align);
-cudaError_t launch_gemm(const GemmLaunch& L, bool l1, cudaStream_t stream);
-// L1 and L2 in one cooperative launch; `ready` holds ffn_ready_words(U, align) words that are zero
-// before the launch and zero again after it.
-cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* ready, cudaStream_t stream);
-size_t ffn_ready_words(int U, int align);
+// `sched`: gemm_sched_words(U, align) words of the workspace, zero before a launch and left at zero.
+cudaError_t launch_gemm(const GemmLaunch& L, bool l1, uint32_t* sched, cudaStream_t stream);
+// L1 and L2 in one cooperative launch.
+cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* sched, cudaStream_t stream);
+size_t gemm_sched_words(int U, int align);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
                            cudaStream_t stream);
 
