@@ -150,8 +150,9 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
  * a plugin interface that supplies only inputs and outputs).  Same arguments and results as
  * moe_route minus ws/ws_bytes.  Its scratch is a fixed 4 MiB array in device memory inside the
  * library (held on every GPU that loads the library until exit): the call needs nsplit*T*E*4
- * bytes of it (nsplit = 4 for T <= 16) rounded up to 256, plus a 256-byte counter slot that each
- * call leaves at zero, and returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
+ * bytes of it (nsplit = 4 for T <= 16) rounded up to 256, for T > 16 another 3*E*H*2 bytes (bf16
+ * parts of the gate weight), plus a 256-byte counter slot that each call leaves at zero, and
+ * returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
  * All calls on a device share the array, so calls that may overlap on the GPU race.  The first
  * call on each device looks up the array's device address (cudaGetSymbolAddress): make it before
  * any stream capture starts. */

@@ -10,8 +10,9 @@
 // Properties of the array:
 //   * 4 MiB (kNoAllocScratchBytes), held on every GPU that loads the library until the process
 //     exits.  A call needs nsplit * T * E * 4 bytes of partial sums (nsplit = 4 for T <= 16),
-//     rounded up to 256, plus a 256-byte slot; larger problems are rejected with
-//     MOE_ERR_UNSUPPORTED before anything is launched.
+//     rounded up to 256, for T > 16 the three bf16 parts of the gate weight (3 * E * H * 2 bytes),
+//     plus a 256-byte slot; larger problems are rejected with MOE_ERR_UNSUPPORTED before anything
+//     is launched.
 //   * Shared by every call on a device and left holding the last call's partial sums.  Every
 //     partial a call reads is written earlier in the same call; the slot holds a counter that must
 //     be zero when a call starts: it is zero when the library loads and each call that uses it
