@@ -7,12 +7,15 @@
 // though: an E2M1 value times an E4M3 scale has at most 6 significant bits, and an E4M3 activation
 // times its power-of-two scale at most 4.  So this path runs kind::f16 (bf16 x bf16 -> fp32):
 //  * activations are dequantised once per call into bf16 rows (act_to_bf16_kernel);
-//  * each pipeline stage brings 256 weight rows x 64 codes + their scales with one bulk copy, and
-//    the four epilogue warps turn them into a 128-byte-swizzled bf16 tile (byte-permute table for
+//  * a load ring (5 slots) receives each slab's bf16 token rows by TMA and its packed weights
+//    (256 rows x 64 codes + scales) by one bulk copy; six converter warps turn the packed weights
+//    into a 128-byte-swizzled bf16 tile in a second ring (3 slots; byte-permute table for
 //    E2M1 -> bf16, exact bf16 multiply by the scale) before the MMA warp consumes it;
+//  * two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM) let an item's
+//    MMAs run while four epilogue warps drain the previous item 32 columns at a time;
 //  * the per-expert fp32 tensor scale multiplies the accumulator in the epilogue.
 // Layout and scheduling otherwise follow gemm.cu: M = 128 token rows x N = 256 weight rows, one
-// persistent CTA per SM, TMA producer warp, single-thread MMA issue, 128x256 fp32 accumulator.
+// persistent CTA per SM, TMA producer warp, single-thread MMA issue.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -23,26 +26,25 @@ namespace moe {
 
 namespace {
 
-constexpr int kNvThreads = 192;          // warp 0 TMA, warp 1 MMA, warps 2..5 convert + epilogue
+constexpr int kNvThreads = 384;          // warp 0 TMA, 1 MMA, 2..7 convert, 8..11 epilogue
+constexpr int kNvConvThreads = 192;
 constexpr int kNvBudget = 227 * 1024;
-constexpr uint32_t kNvTmemCols = 512;
+constexpr uint32_t kNvTmemCols = 512;    // two 256-column accumulators
 constexpr int kNvTile = 256;             // weight rows per tile (MMA N)
 constexpr int kNvSlab = 64;              // K per pipeline stage (64 bf16 = one 128-byte row)
 constexpr int kNvChunk = kNvTile * 32 + kNvTile * 4;   // packed bytes per (tile, slab): codes + scales
-
-template <int BN>
-struct NvCfg {
-  static constexpr int A_OFF = 0;                               // bf16 tokens, MMA reads 128 rows
-  static constexpr int A_BYTES = BN * 128;
-  static constexpr int B_OFF = 16384;                           // bf16 weights 256 x 128 B
-  static constexpr int P_OFF = B_OFF + kNvTile * 128;           // packed codes + scales
-  static constexpr int STAGE = (P_OFF + kNvChunk + 1023) / 1024 * 1024;
-  static constexpr int EXTRA = 1024;
-  static constexpr int S_FIT = (kNvBudget - EXTRA - 1024) / STAGE;
-  static constexpr int STAGES = S_FIT > 4 ? 4 : S_FIT;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + EXTRA;
-  static_assert(STAGES >= 2, "shared memory too small");
-};
+// Load ring slot: bf16 token rows (the MMA reads 128 rows = 16 KB) + one packed weight chunk.
+constexpr int kNvAOff = 0;
+constexpr int kNvABytes = 16384;
+constexpr int kNvLoadStage = (kNvABytes + kNvChunk + 1023) / 1024 * 1024;   // 25 KB
+constexpr int kNvLoadStages = 5;
+// bf16 weight ring slot: 256 rows x 128 B, 128-byte swizzle.
+constexpr int kNvBStage = kNvTile * 128;                                     // 32 KB
+constexpr int kNvBStages = 3;
+constexpr int kNvExtra = 1024;
+constexpr int kNvSmem = 1024 + kNvLoadStages * kNvLoadStage + kNvBStages * kNvBStage + kNvExtra;
+static_assert(kNvSmem <= kNvBudget, "shared memory budget");
+static_assert(kNvConvThreads % 32 == 0 && 2 + kNvConvThreads / 32 + 4 == kNvThreads / 32, "warp roles");
 
 struct NvArgs {
   const uint8_t* w;             // packed NVFP4 weight stream
@@ -132,58 +134,58 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
-// Converts the packed (codes, scales) of one stage into the 128-byte-swizzled bf16 weight tile.
-// 128 threads, two weight rows each.
-__device__ __forceinline__ void convert_stage(const uint8_t* packed, uint8_t* btile, int tid) {
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    const int n = tid * 2 + rr;
-    const uint4 c0 = *reinterpret_cast<const uint4*>(packed + n * 32);
-    const uint4 c1 = *reinterpret_cast<const uint4*>(packed + n * 32 + 16);
-    const uint32_t scw = *reinterpret_cast<const uint32_t*>(packed + kNvTile * 32 + n * 4);
-    const uint32_t codes[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    uint8_t* rowp = btile + n * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {           // 16-byte chunk c = elements 8c .. 8c+7 (group c/2)
-      const uint32_t s = e4m3_to_bf16_bits((scw >> (8 * (c >> 1))) & 0xFF);
-      const uint32_t s2 = s | (s << 16);
-      uint32_t p[4];
-      e2m1x4_to_bf16(codes[c], p[0], p[1]);
-      e2m1x4_to_bf16(codes[c] >> 16, p[2], p[3]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) p[j] = bf16x2_mul(p[j], s2);
-      *reinterpret_cast<uint4*>(rowp + ((c ^ (n & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
-    }
-  }
-}
-
 __device__ __forceinline__ float silu_mul_nv(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+// One 16-byte chunk of the bf16 weight tile: codes 8c .. 8c+7 of weight row n (4 code bytes) times
+// their E4M3 scale, stored at the row's 128-byte-swizzled position.
+__device__ __forceinline__ void convert_chunk(const uint8_t* packed, uint8_t* btile, int task) {
+  const int n = task >> 3, c = task & 7;
+  const uint32_t codes = *reinterpret_cast<const uint32_t*>(packed + n * 32 + c * 4);
+  const uint32_t s = e4m3_to_bf16_bits(packed[kNvTile * 32 + n * 4 + (c >> 1)]);
+  const uint32_t s2 = s | (s << 16);
+  uint32_t p[4];
+  e2m1x4_to_bf16(codes, p[0], p[1]);
+  e2m1x4_to_bf16(codes >> 16, p[2], p[3]);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) p[j] = bf16x2_mul(p[j], s2);
+  *reinterpret_cast<uint4*>(btile + n * 128 + ((c ^ (n & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+}
+
+// Warp roles: 0 loads (TMA token rows + bulk copy of packed weights into the load ring), 1 issues
+// the MMAs, 2..7 convert packed weights into the bf16 ring, 8..11 drain the accumulators.
+// Two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM), so an item's MMAs
+// overlap the previous item's epilogue; the epilogue streams each accumulator in 32-column chunks.
 template <int BN, bool L1>
 __global__ void __launch_bounds__(kNvThreads, 1)
     moe_gemm_nv_kernel(const __grid_constant__ CUtensorMap tmap_x, const NvArgs a) {
-  using C = NvCfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* stages = smem;
-  uint8_t* extra = smem + C::STAGES * C::STAGE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(extra);
-  uint64_t* conv = full + C::STAGES;
-  uint64_t* empty = conv + C::STAGES;
-  uint64_t* acc_full = empty + C::STAGES;
-  uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint8_t* lring = smem;                                   // [kNvLoadStages] token tile + packed weights
+  uint8_t* bring = smem + kNvLoadStages * kNvLoadStage;    // [kNvBStages] bf16 weight tiles
+  uint8_t* extra = bring + kNvBStages * kNvBStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(extra);     // load slot filled (TMA)
+  uint64_t* lempty = full + kNvLoadStages;                 // load slot consumed (MMA commit)
+  uint64_t* bready = lempty + kNvLoadStages;               // bf16 tile written (converters)
+  uint64_t* bempty = bready + kNvBStages;                  // bf16 tile consumed (MMA commit)
+  uint64_t* acc_full = bempty + kNvBStages;                // [2]
+  uint64_t* acc_empty = acc_full + 2;                      // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < kNvLoadStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(conv + s), 128);
-      mbar_init(smem_u32(empty + s), 1);
+      mbar_init(smem_u32(lempty + s), 1);
     }
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), 128);
+    for (int s = 0; s < kNvBStages; ++s) {
+      mbar_init(smem_u32(bready + s), kNvConvThreads);
+      mbar_init(smem_u32(bempty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), 128);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_x);
@@ -201,33 +203,33 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   if (warp == 0) {
     // ---------------- producer: bf16 token rows by TMA, packed weights by one bulk copy ----------------
     const uint64_t pol_x = policy_evict_last();
-    int stage = 0;
-    uint32_t phase = 0;
+    int ls = 0;
+    uint32_t lph = 0;
     int t = blockIdx.x, e = -1;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
       const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
       const size_t chunk0 = (static_cast<size_t>(e) * a.n_wt + wt) * a.n_slabs;
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status));
         if (!ok) break;
         if (lane == 0) {
-          uint8_t* st = stages + stage * C::STAGE;
-          const uint32_t fb = smem_u32(full + stage);
+          uint8_t* st = lring + ls * kNvLoadStage;
+          const uint32_t fb = smem_u32(full + ls);
           const size_t wbase = (chunk0 + s) * kNvChunk;
           if (wbase + kNvChunk > a.w_bytes || (reinterpret_cast<uintptr_t>(a.w) & 15)) {
             record_error(a.status, kDevErrCheck);
             *abort_flag = 1;
           } else {
-            mbar_arrive_expect_tx(fb, C::A_BYTES + kNvChunk);
-            tma_load_2d(smem_u32(st + C::A_OFF), &tmap_x, s * kNvSlab, r0, fb, pol_x);
-            bulk_load(smem_u32(st + C::P_OFF), a.w + wbase, kNvChunk, fb);
+            mbar_arrive_expect_tx(fb, BN * 128 + kNvChunk);
+            tma_load_2d(smem_u32(st), &tmap_x, s * kNvSlab, r0, fb, pol_x);
+            bulk_load(smem_u32(st + kNvAOff + kNvABytes), a.w + wbase, kNvChunk, fb);
           }
         }
         __syncwarp();
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
+        if (++ls == kNvLoadStages) {
+          ls = 0;
+          lph ^= 1;
         }
       }
       if (!ok) {
@@ -236,35 +238,45 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       }
     }
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-      for (int s = 0; s < C::STAGES; ++s) mbar_wait(smem_u32(full + s), (s < stage) ? phase : (phase ^ 1), nullptr);
+      // let every copy issued into shared memory land before the CTA exits
+      for (int s = 0; s < kNvLoadStages; ++s) mbar_wait(smem_u32(full + s), (s < ls) ? lph : (lph ^ 1), nullptr);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: kind::f16, M=128, N=256, K=16 x 4 per stage ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t acc_phase = 0;
+    // ---------------- MMA issuer: kind::f16, M=128, N=256, K=16 x 4 per slab ----------------
+    int ls = 0, bs = 0;
+    uint32_t lph = 0, bph = 0;
+    int i = 0;
     int t = blockIdx.x, e = -1;
     const uint32_t id = idesc_bf16(128, kNvTile);
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+      const int b = i & 1;
+      const uint32_t use = static_cast<uint32_t>(i >> 1) & 1u;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty + b), use ^ 1u, a.status));
+      const uint32_t d = tmem + static_cast<uint32_t>(b * kNvTile);
       if (ok) {
         tc_fence_after();
         for (int s = 0; s < a.n_slabs; ++s) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(conv + stage), phase, a.status));
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
+                                           mbar_wait(smem_u32(bready + bs), bph, a.status));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t st = smem_u32(stages + stage * C::STAGE);
+            const uint32_t sa = smem_u32(lring + ls * kNvLoadStage + kNvAOff);
+            const uint32_t sb = smem_u32(bring + bs * kNvBStage);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_bf16(tmem, desc_sw128(st + C::A_OFF + k * 32), desc_sw128(st + C::B_OFF + k * 32), id,
-                       (s > 0 || k > 0) ? 1u : 0u);
-            tc_commit(smem_u32(empty + stage));
+              mma_bf16(d, desc_sw128(sa + k * 32), desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
+            tc_commit(smem_u32(lempty + ls));
+            tc_commit(smem_u32(bempty + bs));
           }
           __syncwarp();
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
+          if (++ls == kNvLoadStages) {
+            ls = 0;
+            lph ^= 1;
+          }
+          if (++bs == kNvBStages) {
+            bs = 0;
+            bph ^= 1;
           }
         }
       }
@@ -272,115 +284,144 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         *abort_flag = 1;
         break;
       }
-      if (lane == 0) tc_commit(smem_u32(acc_full));
+      if (lane == 0) tc_commit(smem_u32(acc_full + b));
       __syncwarp();
-      acc_phase ^= 1;
+      ++i;
     }
-  } else {
-    // ---------------- warps 2..5: convert each stage's weights, then the epilogue per item ----------------
-    const int tid = threadIdx.x - 64;
-    const int q = warp & 3;
-    const int m = q * 32 + lane;
-    const bool warp_has_rows = q * 32 < BN;
-    const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t acc_phase = 0;
+  } else if (warp < 2 + kNvConvThreads / 32) {
+    // ---------------- converters: packed NVFP4 slab -> 128-byte-swizzled bf16 tile ----------------
+    const int ctid = threadIdx.x - 64;
+    int ls = 0, bs = 0;
+    uint32_t lph = 0, bph = 0;
     int t = blockIdx.x, e = -1;
-    while (nv_next_item<BN>(a, msum, t, e)) {
-      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
-        ok = mbar_wait(smem_u32(full + stage), phase, a.status) && *abort_flag == 0;
-        ok = named_barrier_and(1, 128, ok);
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
+                                         mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
         if (!ok) break;
-        uint8_t* st = stages + stage * C::STAGE;
-        convert_stage(st + C::P_OFF, st + C::B_OFF, tid);
+        const uint8_t* packed = lring + ls * kNvLoadStage + kNvAOff + kNvABytes;
+        uint8_t* btile = bring + bs * kNvBStage;
+#pragma unroll 4
+        for (int task = ctid; task < kNvTile * 8; task += kNvConvThreads) convert_chunk(packed, btile, task);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(smem_u32(conv + stage));
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1;
+        mbar_arrive(smem_u32(bready + bs));
+        if (++ls == kNvLoadStages) {
+          ls = 0;
+          lph ^= 1;
+        }
+        if (++bs == kNvBStages) {
+          bs = 0;
+          bph ^= 1;
         }
       }
-      if (ok) {
-        ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
-        ok = named_barrier_and(1, 128, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
       }
+    }
+  } else {
+    // ---------------- epilogue (warps 8..11): thread = token row m of the block ----------------
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const bool warp_has_rows = q * 32 < BN;   // warp-uniform
+    int i = 0;
+    int t = blockIdx.x, e = -1;
+    while (nv_next_item<BN>(a, msum, t, e)) {
+      const int b = i & 1;
+      const uint32_t use = static_cast<uint32_t>(i >> 1) & 1u;
+      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
+      bool ok = mbar_wait(smem_u32(acc_full + b), use, a.status) && *abort_flag == 0;
+      ok = named_barrier_and(1, 128, ok);
       if (!ok) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
+      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kNvTile);
       const int row = r0 + m;
       const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == e;
       const float ts = __ldg(a.tscale + e);
       if (L1) {
-        float h[128];
+        // pass 1: amax of h over the 128 columns; pass 2: recompute h, quantise, store
         float amax = 0.f;
         if (warp_has_rows) {
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t g[16], u[16];
-            tc_ld_x16(acc + c0, g);
-            tc_ld_x16(acc + 128 + c0, u);
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t g[2][16], u[2][16];
+            tc_ld_x16(acc + c0, g[0]);
+            tc_ld_x16(acc + c0 + 16, g[1]);
+            tc_ld_x16(acc + 128 + c0, u[0]);
+            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
             tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              h[c0 + j] = silu_mul_nv(__uint_as_float(g[j]) * ts, __uint_as_float(u[j]) * ts);
-              amax = fmaxf(amax, fabsf(h[c0 + j]));
-            }
+            for (int j = 0; j < 32; ++j)
+              amax = fmaxf(amax, fabsf(silu_mul_nv(__uint_as_float(g[j >> 4][j & 15]) * ts,
+                                                   __uint_as_float(u[j >> 4][j & 15]) * ts)));
           }
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty));
-        if (mine) {
           const int ex = ue8m0_exponent(amax);
           const float sc = pow2_neg(ex);
-          a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
           uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 16) {
-            uint32_t packed[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int c = c0 + 4 * j;
-              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
-              const uint32_t hi =
-                  __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
-              packed[j] = lo | (hi << 16);
-            }
-            dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          }
-        }
-      } else {
-        uint32_t packed[128];
-        const int ncols = min(kNvTile, a.out_cols - wt * kNvTile);
-        if (warp_has_rows) {
-#pragma unroll
-          for (int c0 = 0; c0 < kNvTile; c0 += 16) {
-            uint32_t v[16];
-            tc_ld_x16(acc + c0, v);
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t g[2][16], u[2][16];
+            tc_ld_x16(acc + c0, g[0]);
+            tc_ld_x16(acc + c0 + 16, g[1]);
+            tc_ld_x16(acc + 128 + c0, u[0]);
+            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
             tc_wait_ld();
+            uint32_t packed[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j]) * ts));
-              const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[2 * j + 1]) * ts));
-              packed[c0 / 2 + j] = lo | (hi << 16);
+              float h[4];
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int c = 4 * j + v;
+                h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts);
+              }
+              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
+              packed[j] = lo | (hi << 16);
+            }
+            if (mine) {
+              dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+              dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+            }
+          }
+          if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc_empty + b));
+      } else {
+        const int ncols = min(kNvTile, a.out_cols - wt * kNvTile);
+        if (warp_has_rows) {
+          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kNvTile);
+#pragma unroll 1
+          for (int c0 = 0; c0 < kNvTile; c0 += 32) {
+            uint32_t v[2][16];
+            tc_ld_x16(acc + c0, v[0]);
+            tc_ld_x16(acc + c0 + 16, v[1]);
+            tc_wait_ld();
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j) & 15]) * ts));
+              const uint32_t hi =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j + 1) & 15]) * ts));
+              packed[j] = lo | (hi << 16);
+            }
+            if (mine && c0 < ncols) {
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
             }
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty));
-        if (mine) {
-          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kNvTile);
-#pragma unroll
-          for (int c = 0; c < kNvTile / 8; ++c)
-            if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-        }
+        mbar_arrive(smem_u32(acc_empty + b));
         if (a.red.out) fused_reduce_tail(a.red, a.y, a.out_cols, mine, row, wt, a.n_wt, wt * kNvTile, ncols);
       }
-      acc_phase ^= 1;
+      ++i;
     }
   }
   tc_fence_before();
@@ -464,7 +505,6 @@ EncodeTiledFnNv get_encode_nv() {
 
 template <int BN, bool L1>
 cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
-  using C = NvCfg<BN>;
   EncodeTiledFnNv enc = get_encode_nv();
   if (!enc) return cudaErrorInvalidValue;
   CUtensorMap mx;
@@ -497,9 +537,9 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(moe_gemm_nv_kernel<BN, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t err = cudaFuncSetAttribute(moe_gemm_nv_kernel<BN, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
   if (err != cudaSuccess) return err;
-  moe_gemm_nv_kernel<BN, L1><<<grid, kNvThreads, C::SMEM, stream>>>(mx, a);
+  moe_gemm_nv_kernel<BN, L1><<<grid, kNvThreads, kNvSmem, stream>>>(mx, a);
   return cudaGetLastError();
 }
 
