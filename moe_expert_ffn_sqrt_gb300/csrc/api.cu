@@ -26,7 +26,7 @@ bool dims_ok(int T, int H, int I, int E, int K, int align) {
 // Workspace layout for one problem size.  Offsets are relative to the workspace base.
 struct WsLayout {
   size_t status = 0;
-  size_t partial = 0, partial_bytes = 0;
+  size_t perm = 0, partial = 0, partial_bytes = 0;
   size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
   size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, sched = 0;
   size_t total = 0;
@@ -36,6 +36,7 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   WsLayout L;
   const size_t U = moe_msum_upper(T, K, E, align);
   size_t off = kAlign;                             // [0, 256): status word
+  L.perm = off;       off = up(off + permute_scratch_bytes(T, K, E));   // permute chunk counts
   L.partial = off;
   L.partial_bytes = route_scratch_bytes(T, H, E);
   off = up(off + L.partial_bytes);
@@ -142,10 +143,11 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
   if (!aligned(hidden, 16) || !aligned(w_gate, 16)) return MOE_ERR_INVALID_ARG;
   if (x_q && !aligned(x_q, 4)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
-  const size_t need = kAlign + route_scratch_bytes(T, H, E);
+  const size_t poff = up(kAlign + permute_scratch_bytes(T, K, E));   // as in layout()
+  const size_t need = poff + route_scratch_bytes(T, H, E);
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + kAlign);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + poff);
   return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
                                   renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, status_of(ws),
                                   S(stream)));
@@ -163,11 +165,12 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, 
   if (copy != (x_q != nullptr) || copy != (x_sf != nullptr) || copy != (x_perm_sf != nullptr))
     return MOE_ERR_INVALID_ARG;
   if (copy && (H <= 0 || H % 128 || !aligned(x_q, 16) || !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
+  if (!ws || ws_bytes < kAlign + permute_scratch_bytes(T, K, E)) return MOE_ERR_WORKSPACE;
   const size_t U = moe_msum_upper(T, K, E, align);
+  int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kAlign);   // layout().perm
   return cuda_status(launch_permute(topk_ids, T, K, E, align, static_cast<int>(U), sorted_token_ids, expert_ids,
                                     inv_perm, m_sum, expert_counts, x_q, x_sf, H, x_perm, x_perm_sf,
-                                    status_of(ws), S(stream)));
+                                    status_of(ws), scratch, S(stream)));
 }
 
 // Launch description of one MXFP4 GEMM (L1: x = x_perm [U, H] against W13; L2: x = h [U, I] against W2).

@@ -2,12 +2,13 @@
 // Note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4 (scatter, inv_perm, M_sum), §10 (M_sum_upper) and the
 // m_indices paragraph (expert_ids, -1 on padding); MegaMoE page 路径 A (moe_align_block_size).
 //
-// Up to 1024 (t,k) pairs a small single-pass kernel handles the index computation (and, up to 128
-// pairs, the row copy); above that one CTA of 1024 threads does it, deterministically:
-//   1. each warp counts its contiguous chunk of the flat (t,k) list into a private histogram;
-//   2. per expert: count, aligned size, exclusive scan -> segment starts, M_sum; per (warp,
-//      expert) base row = segment start + pairs of that expert in earlier chunks;
-//   3. each warp walks its chunk in order, 32 pairs at a time; __match_any_sync groups equal
+// Up to 1024 (t,k) pairs one small kernel does the index computation (and, up to 128 pairs, the
+// row copy); above that two launches over up to 128 CTAs of 1024 threads do it, deterministically:
+//   1. each CTA counts its contiguous chunk of the flat (t,k) list per expert;
+//   2. each CTA sums the chunk counts per expert (total, and the CTAs before it), scans the aligned
+//      segment sizes -> segment starts, M_sum; per (warp, expert) base row = segment start +
+//      pairs of that expert in earlier CTAs and earlier warps of this CTA;
+//   3. each warp walks its sub-range in order, 32 pairs at a time; __match_any_sync groups equal
 //      experts so that each pair's rank among earlier pairs of its expert is exact.
 // Padding rows get expert_ids = -1 and sorted_token_ids = T*K.
 #include "common.cuh"
@@ -29,39 +30,86 @@ struct PermuteArgs {
   uint32_t* status;
 };
 
-__global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteArgs a) {
-  extern __shared__ int32_t sh[];
-  int32_t* hist = sh;                              // [kPermWarps][E]
-  int32_t* seg = sh + kPermWarps * a.E;            // [E] segment start
-  int32_t* cnt = seg + a.E;                        // [E]
-  __shared__ int32_t s_total;
-  __shared__ int32_t s_scan[kPermThreads];
+// Larger problems: G CTAs, CTA c owning the contiguous pairs [c*CH, (c+1)*CH) and each of its 32
+// warps a contiguous sub-range, so that "earlier pair" order is (CTA, warp, lane).
+// permute_count_kernel: per-CTA expert counts, stored expert-major as ccount[e*G + c].
+// permute_place_kernel: each CTA sums its expert rows of ccount (total, and the part of earlier
+// CTAs), scans the aligned segment sizes over experts, adds its per-warp histograms and places
+// its pairs with __match_any_sync ranks; padding rows and the tail [M_sum, U) are split over CTAs.
+constexpr int kPermMaxCtas = 128;
+
+int permute_ctas(long long N) {
+  long long g = (N + kPermThreads - 1) / kPermThreads;
+  if (g > kPermMaxCtas) g = kPermMaxCtas;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+static int permute_warp_chunk(long long N, int G) {
+  const long long ch = (N + G - 1) / G;
+  return static_cast<int>((ch + kPermWarps - 1) / kPermWarps);
+}
+
+size_t permute_scratch_bytes(int T, int K, int E) {
+  const long long N = static_cast<long long>(T) * K;
+  if (N <= 1024) return 0;
+  return (static_cast<size_t>(permute_ctas(N)) * E * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+__global__ void __launch_bounds__(kPermThreads, 1) permute_count_kernel(const PermuteArgs a, int W, int32_t* ccount) {
+  extern __shared__ int32_t cnt[];                 // [E]
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-  const int N = a.T * a.K;
-  const int chunk = (N + kPermWarps - 1) / kPermWarps;
-  const int cbeg = min(N, warp * chunk), cend = min(N, cbeg + chunk);
-  for (int i = tid; i < kPermWarps * a.E; i += kPermThreads) hist[i] = 0;
+  const int N = a.T * a.K, G = gridDim.x, c = blockIdx.x;
+  for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
   __syncthreads();
-  // 1. histograms
-  for (int i = cbeg + lane; i < cend; i += 32) {
+  const int beg = min(N, (c * kPermWarps + warp) * W), end = min(N, beg + W);
+  for (int i = beg + lane; i < end; i += 32) {
     const int e = a.topk_ids[i];
     if (e < 0 || e >= a.E) {
       record_error(a.status, kDevErrIndex);
       continue;
     }
-    atomicAdd(&hist[warp * a.E + e], 1);
+    atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
-  // 2. counts, aligned sizes, exclusive scan over experts (blocked: each thread owns a run)
+  for (int e = tid; e < a.E; e += kPermThreads) ccount[static_cast<size_t>(e) * G + c] = cnt[e];
+}
+
+__global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const PermuteArgs a, int W,
+                                                                        const int32_t* __restrict__ ccount) {
+  extern __shared__ int32_t sh[];
+  int32_t* hist = sh;                              // [kPermWarps][E] -> per-warp base rows
+  int32_t* seg = sh + kPermWarps * a.E;            // [E] segment start
+  int32_t* tot = seg + a.E;                        // [E] pairs per expert
+  __shared__ int32_t s_total;
+  __shared__ int32_t s_scan[kPermThreads];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int N = a.T * a.K, G = gridDim.x, c = blockIdx.x;
+  const int beg = min(N, (c * kPermWarps + warp) * W), end = min(N, beg + W);
+  for (int i = tid; i < kPermWarps * a.E; i += kPermThreads) hist[i] = 0;
+  __syncthreads();
+  // 1. per-warp histograms of this CTA's pairs
+  for (int i = beg + lane; i < end; i += 32) {
+    const int e = a.topk_ids[i];
+    if (e >= 0 && e < a.E) atomicAdd(&hist[warp * a.E + e], 1);
+  }
+  // 2. totals and the earlier CTAs' share per expert; exclusive scan of aligned sizes
   const int per = (a.E + kPermThreads - 1) / kPermThreads;
   int local = 0;
+  int pre_mine[4] = {0, 0, 0, 0};                  // per <= 4 (E <= 4096; E <= 1024 here)
   for (int j = 0; j < per; ++j) {
     const int e = tid * per + j;
     if (e < a.E) {
-      int c = 0;
-      for (int w = 0; w < kPermWarps; ++w) c += hist[w * a.E + e];
-      cnt[e] = c;
-      local += (c + a.align - 1) / a.align * a.align;
+      const int32_t* row = ccount + static_cast<size_t>(e) * G;
+      int t_all = 0, t_pre = 0;
+#pragma unroll 8
+      for (int cc = 0; cc < G; ++cc) {
+        const int v = __ldg(row + cc);
+        t_all += v;
+        if (cc < c) t_pre += v;
+      }
+      tot[e] = t_all;
+      pre_mine[j] = t_pre;
+      local += (t_all + a.align - 1) / a.align * a.align;
     }
   }
   s_scan[tid] = local;
@@ -77,22 +125,22 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteA
     const int e = tid * per + j;
     if (e < a.E) {
       seg[e] = run;
-      int base = run;
+      int base = run + pre_mine[j];
       for (int w = 0; w < kPermWarps; ++w) {
         const int h = hist[w * a.E + e];
         hist[w * a.E + e] = base;
         base += h;
       }
-      run += (cnt[e] + a.align - 1) / a.align * a.align;
+      run += (tot[e] + a.align - 1) / a.align * a.align;
     }
   }
   if (tid == kPermThreads - 1) s_total = s_scan[tid];
   __syncthreads();
   const int msum = s_total;
-  // 3. ranks in (t,k) order within each warp's chunk
-  for (int i0 = cbeg; i0 < cend; i0 += 32) {
+  // 3. ranks in (t,k) order within each warp's sub-range
+  for (int i0 = beg; i0 < end; i0 += 32) {
     const int i = i0 + lane;
-    const bool live = i < cend;
+    const bool live = i < end;
     int e = live ? a.topk_ids[i] : -1;
     const bool ok = live && e >= 0 && e < a.E;
     if (!ok) e = -1 - lane;                            // unique dummy key for dead lanes
@@ -109,22 +157,24 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_kernel(const PermuteA
       a.expert_ids[pos] = e;
     }
   }
-  // padding rows inside each segment, then the tail [M_sum, U)
-  for (int e = warp; e < a.E; e += kPermWarps) {
-    const int c = cnt[e];
-    const int padded = (c + a.align - 1) / a.align * a.align;
-    for (int r = c + lane; r < padded; r += 32) {
+  // 4. padding rows inside each segment (experts split over CTAs), then the tail [M_sum, U)
+  for (int e = c * kPermWarps + warp; e < a.E; e += G * kPermWarps) {
+    const int n = tot[e];
+    const int padded = (n + a.align - 1) / a.align * a.align;
+    for (int r = n + lane; r < padded; r += 32) {
       a.sorted_ids[seg[e] + r] = N;
       a.expert_ids[seg[e] + r] = -1;
     }
   }
-  for (int r = msum + tid; r < a.U; r += kPermThreads) {
+  for (int r = msum + c * kPermThreads + tid; r < a.U; r += G * kPermThreads) {
     a.sorted_ids[r] = N;
     a.expert_ids[r] = -1;
   }
-  if (a.counts)
-    for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
-  if (tid == 0) *a.m_sum = msum;
+  if (c == 0) {
+    if (a.counts)
+      for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = tot[e];
+    if (tid == 0) *a.m_sum = msum;
+  }
 }
 
 // Small problems (T*K <= 1024): one thread per (t,k) pair.  A pair's rank within its expert is
@@ -263,10 +313,11 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
 
 size_t permute_smem_bytes(int E) { return static_cast<size_t>(kPermWarps + 2) * E * sizeof(int32_t); }
 
+
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, cudaStream_t stream) {
+                           uint32_t* status, int32_t* scratch, cudaStream_t stream) {
   PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status};
   const int bt = act_sf_block_rows(align), nb = act_sf_blocks(U, bt);
   const long long npairs = static_cast<long long>(T) * K;
@@ -281,10 +332,18 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     err = cudaGetLastError();
     if (err != cudaSuccess || x_perm == nullptr || copy) return err;
   } else {
-    const size_t smem = permute_smem_bytes(E);
-    err = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (scratch == nullptr) return cudaErrorInvalidValue;
+    const int G = permute_ctas(npairs), W = permute_warp_chunk(npairs, G);
+    err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(E * sizeof(int32_t)));
     if (err != cudaSuccess) return err;
-    permute_kernel<<<1, kPermThreads, smem, stream>>>(a);
+    permute_count_kernel<<<G, kPermThreads, E * sizeof(int32_t), stream>>>(a, W, scratch);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    const size_t smem = permute_smem_bytes(E);
+    err = cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    permute_place_kernel<<<G, kPermThreads, smem, stream>>>(a, W, scratch);
     err = cudaGetLastError();
     if (err != cudaSuccess || x_perm == nullptr) return err;
   }

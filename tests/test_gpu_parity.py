@@ -93,7 +93,8 @@ def test_act_quant_edge_values(M):
 
 @pytest.mark.parametrize("T,K,E,align,skew", [(8, 6, 256, 16, 0.0), (128, 6, 256, 64, 1.0), (3, 2, 3, 1, 0.0),
                                               (37, 4, 16, 16, 0.5), (500, 8, 64, 2, 1.5), (4096, 6, 256, 256, 0.0),
-                                              (3000, 6, 256, 128, 1.2), (1, 1, 1, 1, 0.0)])
+                                              (3000, 6, 256, 128, 1.2), (1, 1, 1, 1, 0.0), (171, 6, 32, 4, 0.7),
+                                              (2000, 8, 1024, 16, 1.0)])
 def test_permute_parity(M, T, K, E, align, skew):
     rng = np.random.default_rng(T * 31 + E)
     ids = synth.topk_ids_random(rng, T, E, K, skew)
@@ -110,7 +111,7 @@ def test_permute_parity(M, T, K, E, align, skew):
     d_cnt = torch.empty(E, dtype=torch.int32, device="cuda")
     d_xp = torch.full((U, H), 0xAA, dtype=torch.uint8, device="cuda")
     d_xpsf = torch.zeros(M.act_sf_tiled_bytes(U, H // 128, align), dtype=torch.uint8, device="cuda")
-    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    ws = M.new_workspace(T, H, 256, E, K, align)
     M.permute(dev(ids), E, align, d_sorted, d_eids, d_inv, d_ms, ws, expert_counts=d_cnt, x_q=dev(xq),
               x_sf=dev(xsf), x_perm=d_xp, x_perm_sf=d_xpsf)
     assert M.get_error(ws) == M.OK
