@@ -8,7 +8,7 @@
 // times its power-of-two scale at most 4.  So this path runs kind::f16 (bf16 x bf16 -> fp32):
 //  * activations are dequantised once per call into bf16 rows (act_to_bf16_kernel);
 //  * a load ring (5 slots) receives each slab's bf16 token rows by TMA and its packed weights
-//    (256 rows x 64 codes + scales) by one bulk copy; six converter warps turn the packed weights
+//    (256 rows x 64 codes + scales) by one bulk copy; ten converter warps turn the packed weights
 //    into a 128-byte-swizzled bf16 tile in a second ring (3 slots; byte-permute table for
 //    E2M1 -> bf16, exact bf16 multiply by the scale) before the MMA warp consumes it;
 //  * two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM) let an item's
@@ -26,8 +26,9 @@ namespace moe {
 
 namespace {
 
-constexpr int kNvThreads = 384;          // warp 0 TMA, 1 MMA, 2..7 convert, 8..11 epilogue
-constexpr int kNvConvThreads = 192;
+constexpr int kNvThreads = 512;          // warp 0 TMA, 1 MMA, 2..11 convert, 12..15 epilogue
+constexpr int kNvConvThreads = 320;
+constexpr int kNvConvBatch = 4;          // conversion tasks per thread with loads issued together
 constexpr int kNvBudget = 227 * 1024;
 constexpr uint32_t kNvTmemCols = 512;    // two 256-column accumulators
 constexpr int kNvTile = 256;             // weight rows per tile (MMA N)
@@ -136,23 +137,52 @@ __device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
 
 __device__ __forceinline__ float silu_mul_nv(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
-// One 16-byte chunk of the bf16 weight tile: codes 8c .. 8c+7 of weight row n (4 code bytes) times
-// their E4M3 scale, stored at the row's 128-byte-swizzled position.
-__device__ __forceinline__ void convert_chunk(const uint8_t* packed, uint8_t* btile, int task) {
-  const int n = task >> 3, c = task & 7;
-  const uint32_t codes = *reinterpret_cast<const uint32_t*>(packed + n * 32 + c * 4);
-  const uint32_t s = e4m3_to_bf16_bits(packed[kNvTile * 32 + n * 4 + (c >> 1)]);
+// Sixteen weights of the bf16 tile: codes 16p .. 16p+15 of weight row n (8 code bytes, one E4M3
+// scale) -> two 16-byte chunks at the row's 128-byte-swizzled positions.  Inputs come in already
+// loaded so that a thread can issue the loads of several pairs before it computes any.
+__device__ __forceinline__ void convert_pair(uint2 codes, uint32_t scale_code, uint8_t* btile, int n, int p) {
+  const uint32_t s = e4m3_to_bf16_bits(scale_code);
   const uint32_t s2 = s | (s << 16);
-  uint32_t p[4];
-  e2m1x4_to_bf16(codes, p[0], p[1]);
-  e2m1x4_to_bf16(codes >> 16, p[2], p[3]);
+  const uint32_t cw[2] = {codes.x, codes.y};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) p[j] = bf16x2_mul(p[j], s2);
-  *reinterpret_cast<uint4*>(btile + n * 128 + ((c ^ (n & 7)) << 4)) = make_uint4(p[0], p[1], p[2], p[3]);
+  for (int h = 0; h < 2; ++h) {
+    uint32_t q[4];
+    e2m1x4_to_bf16(cw[h], q[0], q[1]);
+    e2m1x4_to_bf16(cw[h] >> 16, q[2], q[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) q[j] = bf16x2_mul(q[j], s2);
+    const int c = 2 * p + h;
+    *reinterpret_cast<uint4*>(btile + n * 128 + ((c ^ (n & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+// Converts one slab: 256 rows x 4 pairs of 16 weights = 1024 tasks over the converter threads,
+// kNvConvBatch tasks at a time with all their shared-memory loads issued first.
+__device__ __forceinline__ void convert_slab(const uint8_t* __restrict__ packed, uint8_t* __restrict__ btile,
+                                             int ctid) {
+  constexpr int kTasks = kNvTile * 4;
+  for (int t0 = ctid; t0 < kTasks; t0 += kNvConvThreads * kNvConvBatch) {
+    uint2 codes[kNvConvBatch];
+    uint32_t sc[kNvConvBatch];
+#pragma unroll
+    for (int j = 0; j < kNvConvBatch; ++j) {
+      const int task = t0 + j * kNvConvThreads;
+      if (task < kTasks) {
+        const int n = task >> 2, p = task & 3;
+        codes[j] = *reinterpret_cast<const uint2*>(packed + n * 32 + p * 8);
+        sc[j] = packed[kNvTile * 32 + n * 4 + p];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kNvConvBatch; ++j) {
+      const int task = t0 + j * kNvConvThreads;
+      if (task < kTasks) convert_pair(codes[j], sc[j], btile, task >> 2, task & 3);
+    }
+  }
 }
 
 // Warp roles: 0 loads (TMA token rows + bulk copy of packed weights into the load ring), 1 issues
-// the MMAs, 2..7 convert packed weights into the bf16 ring, 8..11 drain the accumulators.
+// the MMAs, 2..11 convert packed weights into the bf16 ring, 12..15 drain the accumulators.
 // Two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM), so an item's MMAs
 // overlap the previous item's epilogue; the epilogue streams each accumulator in 32-column chunks.
 template <int BN, bool L1>
@@ -302,8 +332,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         if (!ok) break;
         const uint8_t* packed = lring + ls * kNvLoadStage + kNvAOff + kNvABytes;
         uint8_t* btile = bring + bs * kNvBStage;
-#pragma unroll 4
-        for (int task = ctid; task < kNvTile * 8; task += kNvConvThreads) convert_chunk(packed, btile, task);
+        convert_slab(packed, btile, ctid);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(smem_u32(bready + bs));
         if (++ls == kNvLoadStages) {
@@ -321,7 +350,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 8..11): thread = token row m of the block ----------------
+    // ---------------- epilogue (warps 12..15): thread = token row m of the block ----------------
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const bool warp_has_rows = q * 32 < BN;   // warp-uniform
