@@ -34,11 +34,12 @@ constexpr uint32_t kNvTmemCols = 512;    // two 256-column accumulators
 constexpr int kNvTile = 256;             // weight rows per tile (MMA N)
 constexpr int kNvSlab = 64;              // K per pipeline stage (64 bf16 = one 128-byte row)
 constexpr int kNvChunk = kNvTile * 32 + kNvTile * 4;   // packed bytes per (tile, slab): codes + scales
-// Load ring slot: bf16 token rows (the MMA reads 128 rows = 16 KB) + one packed weight chunk.
-constexpr int kNvAOff = 0;
+// Load ring slot: bf16 token rows of up to two row blocks (the MMA reads 128 rows = 16 KB each) +
+// one packed weight chunk.
 constexpr int kNvABytes = 16384;
-constexpr int kNvLoadStage = (kNvABytes + kNvChunk + 1023) / 1024 * 1024;   // 25 KB
-constexpr int kNvLoadStages = 5;
+constexpr int kNvPOff = 2 * kNvABytes;
+constexpr int kNvLoadStage = (kNvPOff + kNvChunk + 1023) / 1024 * 1024;   // 41 KB
+constexpr int kNvLoadStages = 3;
 // bf16 weight ring slot: 256 rows x 128 B, 128-byte swizzle.
 constexpr int kNvBStage = kNvTile * 128;                                     // 32 KB
 constexpr int kNvBStages = 3;
@@ -66,22 +67,51 @@ struct NvArgs {
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
+// One pass of the pipeline: expert e against rows [rb*BN, (rb+nb)*BN), nb = 1 or 2 row blocks
+// (two blocks share each converted weight tile, halving the conversion work per MMA).
+struct NvPass {
+  int e, rb, nb;
+};
+
+// Walks this CTA's items and their passes.  With one expert per row block (alignment a multiple of
+// BN) item t covers blocks 2k and 2k+1 (k = t / n_wt): one pass if both hold the same expert, else
+// a pass per block that holds rows.  Otherwise item t is one block and each expert present in it
+// is a pass (smallest expert id first).  Called by whole warps; every role walks the same sequence.
 template <int BN>
-__device__ __forceinline__ bool nv_next_item(const NvArgs& a, int msum, int& t, int& e) {
-  // as next_item in gemm.cu: called by whole warps; one load per block when blocks hold one expert
+__device__ __forceinline__ bool nv_next_pass(const NvArgs& a, int msum, int& t, int& p, int& e_prev, NvPass& P) {
   const int lane = threadIdx.x & 31;
   while (t < a.n_tiles) {
-    const int r0 = (t / a.n_wt) * BN;
-    if (r0 >= msum) return false;
+    const int k = t / a.n_wt;
     if (a.one_expert_blocks) {
-      if (e < 0) {
-        const int x = __ldg(a.expert_ids + r0);
-        if (x >= 0) {
-          e = x;
+      const int rb0 = 2 * k, rb1 = 2 * k + 1;
+      if (rb0 * BN >= msum) return false;
+      const int e0 = __ldg(a.expert_ids + rb0 * BN);
+      const int e1 = rb1 * BN < msum ? __ldg(a.expert_ids + rb1 * BN) : -1;
+      if (e0 >= 0 && e1 == e0) {
+        if (p == 0) {
+          P = NvPass{e0, rb0, 2};
+          p = 2;
           return true;
+        }
+      } else {
+        if (p == 0) {
+          p = 1;
+          if (e0 >= 0) {
+            P = NvPass{e0, rb0, 1};
+            return true;
+          }
+        }
+        if (p == 1) {
+          p = 2;
+          if (e1 >= 0) {
+            P = NvPass{e1, rb1, 1};
+            return true;
+          }
         }
       }
     } else {
+      const int r0 = k * BN;
+      if (r0 >= msum) return false;
       const int rend = min(r0 + BN, msum);
       int best = 0x7fffffff;
 #pragma unroll
@@ -89,17 +119,19 @@ __device__ __forceinline__ bool nv_next_item(const NvArgs& a, int msum, int& t, 
         const int r = r0 + j * 32 + lane;
         if (r < rend) {
           const int x = __ldg(a.expert_ids + r);
-          if (x > e && x < best) best = x;
+          if (x > e_prev && x < best) best = x;
         }
       }
       best = __reduce_min_sync(0xffffffffu, best);
       if (best != 0x7fffffff) {
-        e = best;
+        e_prev = best;
+        P = NvPass{best, k, 1};
         return true;
       }
     }
     t += gridDim.x;
-    e = -1;
+    p = 0;
+    e_prev = -1;
   }
   return false;
 }
@@ -183,23 +215,23 @@ __device__ __forceinline__ void convert_slab(const uint8_t* __restrict__ packed,
 
 // Warp roles: 0 loads (TMA token rows + bulk copy of packed weights into the load ring), 1 issues
 // the MMAs, 2..11 convert packed weights into the bf16 ring, 12..15 drain the accumulators.
-// Two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM), so an item's MMAs
-// overlap the previous item's epilogue; the epilogue streams each accumulator in 32-column chunks.
+// A pass with two row blocks accumulates block j into TMEM columns [256j, 256j+256); the
+// epilogue releases the accumulators after the pass.
 template <int BN, bool L1>
 __global__ void __launch_bounds__(kNvThreads, 1)
     moe_gemm_nv_kernel(const __grid_constant__ CUtensorMap tmap_x, const NvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* lring = smem;                                   // [kNvLoadStages] token tile + packed weights
+  uint8_t* lring = smem;                                   // [kNvLoadStages] token tiles + packed weights
   uint8_t* bring = smem + kNvLoadStages * kNvLoadStage;    // [kNvBStages] bf16 weight tiles
   uint8_t* extra = bring + kNvBStages * kNvBStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(extra);     // load slot filled (TMA)
   uint64_t* lempty = full + kNvLoadStages;                 // load slot consumed (MMA commit)
   uint64_t* bready = lempty + kNvLoadStages;               // bf16 tile written (converters)
   uint64_t* bempty = bready + kNvBStages;                  // bf16 tile consumed (MMA commit)
-  uint64_t* acc_full = bempty + kNvBStages;                // [2]
-  uint64_t* acc_empty = acc_full + 2;                      // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* acc_full = bempty + kNvBStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -212,10 +244,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       mbar_init(smem_u32(bready + s), kNvConvThreads);
       mbar_init(smem_u32(bempty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(acc_full + b), 1);
-      mbar_init(smem_u32(acc_empty + b), 128);
-    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 128);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_x);
@@ -235,10 +265,11 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const uint64_t pol_x = policy_evict_last();
     int ls = 0;
     uint32_t lph = 0;
-    int t = blockIdx.x, e = -1;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
-      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
-      const size_t chunk0 = (static_cast<size_t>(e) * a.n_wt + wt) * a.n_slabs;
+    int t = blockIdx.x, p = 0, ep = -1;
+    NvPass P;
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+      const int wt = t % a.n_wt;
+      const size_t chunk0 = (static_cast<size_t>(P.e) * a.n_wt + wt) * a.n_slabs;
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status));
@@ -251,9 +282,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             record_error(a.status, kDevErrCheck);
             *abort_flag = 1;
           } else {
-            mbar_arrive_expect_tx(fb, BN * 128 + kNvChunk);
-            tma_load_2d(smem_u32(st), &tmap_x, s * kNvSlab, r0, fb, pol_x);
-            bulk_load(smem_u32(st + kNvAOff + kNvABytes), a.w + wbase, kNvChunk, fb);
+            mbar_arrive_expect_tx(fb, P.nb * BN * 128 + kNvChunk);
+            for (int j = 0; j < P.nb; ++j)
+              tma_load_2d(smem_u32(st + j * kNvABytes), &tmap_x, s * kNvSlab, (P.rb + j) * BN, fb, pol_x);
+            bulk_load(smem_u32(st + kNvPOff), a.w + wbase, kNvChunk, fb);
           }
         }
         __syncwarp();
@@ -272,17 +304,14 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       for (int s = 0; s < kNvLoadStages; ++s) mbar_wait(smem_u32(full + s), (s < ls) ? lph : (lph ^ 1), nullptr);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer: kind::f16, M=128, N=256, K=16 x 4 per slab ----------------
+    // ---------------- MMA issuer: kind::f16, M=128, N=256, K=16 x 4 per slab and block ----------------
     int ls = 0, bs = 0;
-    uint32_t lph = 0, bph = 0;
-    int i = 0;
-    int t = blockIdx.x, e = -1;
+    uint32_t lph = 0, bph = 0, acc_phase = 0;
+    int t = blockIdx.x, p = 0, ep = -1;
+    NvPass P;
     const uint32_t id = idesc_bf16(128, kNvTile);
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
-      const int b = i & 1;
-      const uint32_t use = static_cast<uint32_t>(i >> 1) & 1u;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty + b), use ^ 1u, a.status));
-      const uint32_t d = tmem + static_cast<uint32_t>(b * kNvTile);
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
         for (int s = 0; s < a.n_slabs; ++s) {
@@ -291,11 +320,13 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t sa = smem_u32(lring + ls * kNvLoadStage + kNvAOff);
+            const uint32_t sa = smem_u32(lring + ls * kNvLoadStage);
             const uint32_t sb = smem_u32(bring + bs * kNvBStage);
+            for (int j = 0; j < P.nb; ++j)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16(d, desc_sw128(sa + k * 32), desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16(tmem + static_cast<uint32_t>(j * kNvTile), desc_sw128(sa + j * kNvABytes + k * 32),
+                         desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
             tc_commit(smem_u32(lempty + ls));
             tc_commit(smem_u32(bempty + bs));
           }
@@ -314,25 +345,24 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         *abort_flag = 1;
         break;
       }
-      if (lane == 0) tc_commit(smem_u32(acc_full + b));
+      if (lane == 0) tc_commit(smem_u32(acc_full));
       __syncwarp();
-      ++i;
+      acc_phase ^= 1;
     }
   } else if (warp < 2 + kNvConvThreads / 32) {
     // ---------------- converters: packed NVFP4 slab -> 128-byte-swizzled bf16 tile ----------------
     const int ctid = threadIdx.x - 64;
     int ls = 0, bs = 0;
     uint32_t lph = 0, bph = 0;
-    int t = blockIdx.x, e = -1;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_item<BN>(a, msum, t, e)) {
+    int t = blockIdx.x, p = 0, ep = -1;
+    NvPass P;
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
                                          mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
         if (!ok) break;
-        const uint8_t* packed = lring + ls * kNvLoadStage + kNvAOff + kNvABytes;
-        uint8_t* btile = bring + bs * kNvBStage;
-        convert_slab(packed, btile, ctid);
+        convert_slab(lring + ls * kNvLoadStage + kNvPOff, bring + bs * kNvBStage, ctid);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(smem_u32(bready + bs));
         if (++ls == kNvLoadStages) {
@@ -350,107 +380,106 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue (warps 12..15): thread = token row m of the block ----------------
+    // ---------------- epilogue (warps 12..15): thread = token row m of each block ----------------
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const bool warp_has_rows = q * 32 < BN;   // warp-uniform
-    int i = 0;
-    int t = blockIdx.x, e = -1;
-    while (nv_next_item<BN>(a, msum, t, e)) {
-      const int b = i & 1;
-      const uint32_t use = static_cast<uint32_t>(i >> 1) & 1u;
-      const int r0 = (t / a.n_wt) * BN, wt = t % a.n_wt;
-      bool ok = mbar_wait(smem_u32(acc_full + b), use, a.status) && *abort_flag == 0;
+    uint32_t acc_phase = 0;
+    int t = blockIdx.x, p = 0, ep = -1;
+    NvPass P;
+    while (nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+      const int wt = t % a.n_wt;
+      bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, 128, ok);
       if (!ok) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kNvTile);
-      const int row = r0 + m;
-      const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == e;
-      const float ts = __ldg(a.tscale + e);
-      if (L1) {
-        // pass 1: amax of h over the 128 columns; pass 2: recompute h, quantise, store
-        float amax = 0.f;
-        if (warp_has_rows) {
+      const float ts = __ldg(a.tscale + P.e);
+      for (int j = 0; j < P.nb; ++j) {
+        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNvTile);
+        const int row = (P.rb + j) * BN + m;
+        const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == P.e;
+        if (L1) {
+          // pass 1: amax of h over the 128 columns; pass 2: recompute h, quantise, store
+          if (warp_has_rows) {
+            float amax = 0.f;
 #pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t g[2][16], u[2][16];
-            tc_ld_x16(acc + c0, g[0]);
-            tc_ld_x16(acc + c0 + 16, g[1]);
-            tc_ld_x16(acc + 128 + c0, u[0]);
-            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
-            tc_wait_ld();
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              uint32_t g[2][16], u[2][16];
+              tc_ld_x16(acc + c0, g[0]);
+              tc_ld_x16(acc + c0 + 16, g[1]);
+              tc_ld_x16(acc + 128 + c0, u[0]);
+              tc_ld_x16(acc + 128 + c0 + 16, u[1]);
+              tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              amax = fmaxf(amax, fabsf(silu_mul_nv(__uint_as_float(g[j >> 4][j & 15]) * ts,
-                                                   __uint_as_float(u[j >> 4][j & 15]) * ts)));
-          }
-          const int ex = ue8m0_exponent(amax);
-          const float sc = pow2_neg(ex);
-          uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
+              for (int i = 0; i < 32; ++i)
+                amax = fmaxf(amax, fabsf(silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
+                                                     __uint_as_float(u[i >> 4][i & 15]) * ts)));
+            }
+            const int ex = ue8m0_exponent(amax);
+            const float sc = pow2_neg(ex);
+            uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
 #pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t g[2][16], u[2][16];
-            tc_ld_x16(acc + c0, g[0]);
-            tc_ld_x16(acc + c0 + 16, g[1]);
-            tc_ld_x16(acc + 128 + c0, u[0]);
-            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
-            tc_wait_ld();
-            uint32_t packed[8];
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              uint32_t g[2][16], u[2][16];
+              tc_ld_x16(acc + c0, g[0]);
+              tc_ld_x16(acc + c0 + 16, g[1]);
+              tc_ld_x16(acc + 128 + c0, u[0]);
+              tc_ld_x16(acc + 128 + c0 + 16, u[1]);
+              tc_wait_ld();
+              uint32_t packed[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float h[4];
+              for (int i = 0; i < 8; ++i) {
+                float h[4];
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const int c = 4 * j + v;
-                h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts);
+                for (int v = 0; v < 4; ++v) {
+                  const int c = 4 * i + v;
+                  h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts);
+                }
+                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
+                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
+                packed[i] = lo | (hi << 16);
               }
-              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
-              const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
-              packed[j] = lo | (hi << 16);
+              if (mine) {
+                dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
             }
-            if (mine) {
-              dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            }
+            if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
           }
-          if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
-        }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty + b));
-      } else {
-        const int ncols = min(kNvTile, a.out_cols - wt * kNvTile);
-        if (warp_has_rows) {
-          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kNvTile);
+        } else {
+          const int ncols = min(kNvTile, a.out_cols - wt * kNvTile);
+          if (warp_has_rows) {
+            uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kNvTile);
 #pragma unroll 1
-          for (int c0 = 0; c0 < kNvTile; c0 += 32) {
-            uint32_t v[2][16];
-            tc_ld_x16(acc + c0, v[0]);
-            tc_ld_x16(acc + c0 + 16, v[1]);
-            tc_wait_ld();
-            uint32_t packed[16];
+            for (int c0 = 0; c0 < kNvTile; c0 += 32) {
+              uint32_t v[2][16];
+              tc_ld_x16(acc + c0, v[0]);
+              tc_ld_x16(acc + c0 + 16, v[1]);
+              tc_wait_ld();
+              uint32_t packed[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j) & 15]) * ts));
-              const uint32_t hi =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j + 1) & 15]) * ts));
-              packed[j] = lo | (hi << 16);
-            }
-            if (mine && c0 < ncols) {
+              for (int i = 0; i < 16; ++i) {
+                const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
+                const uint32_t hi =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
+                packed[i] = lo | (hi << 16);
+              }
+              if (mine && c0 < ncols) {
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
-                dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                for (int c = 0; c < 4; ++c)
+                  dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+              }
             }
           }
+          if (a.red.out) fused_reduce_tail(a.red, a.y, a.out_cols, mine, row, wt, a.n_wt, wt * kNvTile, ncols);
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty + b));
-        if (a.red.out) fused_reduce_tail(a.red, a.y, a.out_cols, mine, row, wt, a.n_wt, wt * kNvTile, ncols);
       }
-      ++i;
+      tc_fence_before();
+      mbar_arrive(smem_u32(acc_empty));
+      acc_phase ^= 1;
     }
   }
   tc_fence_before();
@@ -561,8 +590,9 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.w_bytes = static_cast<size_t>(L.E) * a.n_wt * a.n_slabs * kNvChunk;
   a.out_cols = L1 ? L.I : L.w_rows;
   a.sf_nb = act_sf_blocks(L.U, BN);
-  a.n_tiles = ((L.U + BN - 1) / BN) * a.n_wt;
   a.one_expert_blocks = L.align % BN == 0;
+  const int nrb = (L.U + BN - 1) / BN;
+  a.n_tiles = (a.one_expert_blocks ? (nrb + 1) / 2 : nrb) * a.n_wt;   // items: row-block pairs or blocks
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
