@@ -54,7 +54,7 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   L.h_sf = off;       off = up(off + moe_act_sf_tiled_bytes(static_cast<int>(U), I / 128, align));
   L.y = off;          off = up(off + U * H * 2);
   L.xb = off;         off = up(off + U * (H > I ? H : I) * 2);   // bf16 activation rows (NVFP4 GEMMs)
-  L.tickets = off;    off = up(off + static_cast<size_t>(T) * ((H + 255) / 256) * 4);   // fused reduce
+  L.tickets = off;    off = up(off + static_cast<size_t>(T) * ((H + 255) / 256) * 2 * 4);   // fused reduce
   L.sched = off;      off = up(off + gemm_sched_words(static_cast<int>(U), align) * 4);   // GEMM work counters
   L.total = off;
   return L;

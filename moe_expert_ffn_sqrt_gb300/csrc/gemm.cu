@@ -36,7 +36,9 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 192;        // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kGemmThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kEpiThreads = 256;         // two warps per TMEM lane quarter, one per column half
+constexpr int kEpiThread0 = 64;          // first epilogue thread
 constexpr int kSmemBudget = 227 * 1024;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulator [0, 256); token scales 2 slots x 16 at 256; weight scales 2 x 16 at 288.
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(empty + s), 1);
     }
     mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), 128);
+    mbar_init(smem_u32(acc_empty), kEpiThreads);
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(smem_u32(item_full + s), 1);
       mbar_init(smem_u32(item_empty + s), 2);
@@ -373,8 +375,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc_phase ^= 1;
     }
   } else {
-    // ---------------- epilogue (warps 2..5): thread = token row m of the block ----------------
+    // ---------------- epilogue (warps 2..9): thread = token row m of the block, one column half --------
+    // Warps 2..5 take the first half of the accumulator's columns and warps 6..9 the second, so each
+    // thread drains half a row: two TMEM load rounds before the accumulator is released.
+    __shared__ float s_amax[2][128];
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;
     const int m = q * 32 + lane;
     const bool warp_has_rows = q * 32 < BN;  // warp-uniform
     const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -383,8 +389,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     while (true) {
       bool ok = mbar_wait(smem_u32(item_full + islot), iphase, a.status);
       const int2 item = items[islot];
-      ok = named_barrier_and(1, 128, ok);    // every epilogue thread has read the slot
-      if (ok && threadIdx.x == 64) mbar_arrive(smem_u32(item_empty + islot));
+      ok = named_barrier_and(1, kEpiThreads, ok);    // every epilogue thread has read the slot
+      if (ok && threadIdx.x == kEpiThread0) mbar_arrive(smem_u32(item_empty + islot));
       if (++islot == kItemSlots) {
         islot = 0;
         iphase ^= 1;
@@ -401,7 +407,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
       const bool mine = row_e == e;
       ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
-      ok = named_barrier_and(1, 128, ok);    // one vote over the four epilogue warps
+      ok = named_barrier_and(1, kEpiThreads, ok);    // one vote over the eight epilogue warps
       if (!ok) {
         *abort_flag = 1;
         break;
@@ -409,18 +415,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       if (it.phase == 0) {
         const int I = a.ph[0].out_cols;
-        // h = silu(gate) * up for the 128 columns of this tile, kept in registers so that the
-        // accumulator is released before the quantise-and-store part
+        // h = silu(gate) * up for this thread's 64 of the tile's 128 columns, kept in registers so
+        // that the accumulator is released before the quantise-and-store part; the 128-wide amax
+        // combines both halves through shared memory
+        float h[64];
+        float amax = 0.f;
         if (warp_has_rows) {
-          float h[128];
-          float amax = 0.f;
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+          for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t g[2][16], u[2][16];
-            tc_ld_x16(acc + c0, g[0]);
-            tc_ld_x16(acc + c0 + 16, g[1]);
-            tc_ld_x16(acc + 128 + c0, u[0]);
-            tc_ld_x16(acc + 128 + c0 + 16, u[1]);
+            const uint32_t col = static_cast<uint32_t>(half * 64 + c0);
+            tc_ld_x16(acc + col, g[0]);
+            tc_ld_x16(acc + col + 16, g[1]);
+            tc_ld_x16(acc + 128 + col, u[0]);
+            tc_ld_x16(acc + 128 + col + 16, u[1]);
             tc_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -428,75 +436,83 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               amax = fmaxf(amax, fabsf(h[c0 + j]));
             }
           }
-          tc_fence_before();
-          mbar_arrive(smem_u32(acc_empty));
-          if (mine) {
-            const int ex = ue8m0_exponent(amax);
-            const float sc = pow2_neg(ex);
-            a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
-            uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * I + wt * 128);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc_empty));
+        s_amax[half][m] = amax;
+        named_barrier(1, kEpiThreads);
+        if (warp_has_rows && mine) {
+          amax = fmaxf(amax, s_amax[half ^ 1][m]);
+          const int ex = ue8m0_exponent(amax);
+          const float sc = pow2_neg(ex);
+          if (half == 0) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+          uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * I + wt * 128 + half * 64);
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 16) {
-              uint32_t packed[4];
+          for (int c0 = 0; c0 < 64; c0 += 16) {
+            uint32_t packed[4];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int c = c0 + 4 * j;
-                const uint32_t lo =
-                    __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t hi =
-                    __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
-                packed[j] = lo | (hi << 16);
-              }
-              dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            for (int j = 0; j < 4; ++j) {
+              const int c = c0 + 4 * j;
+              const uint32_t lo =
+                  __nv_cvt_float2_to_fp8x2(make_float2(h[c] * sc, h[c + 1] * sc), __NV_SATFINITE, __NV_E4M3);
+              const uint32_t hi =
+                  __nv_cvt_float2_to_fp8x2(make_float2(h[c + 2] * sc, h[c + 3] * sc), __NV_SATFINITE, __NV_E4M3);
+              packed[j] = lo | (hi << 16);
             }
-            if (a.fused) fence_proxy_async_global();
+            dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           }
-        } else {
-          tc_fence_before();
-          mbar_arrive(smem_u32(acc_empty));
+          if (a.fused) fence_proxy_async_global();
         }
         if (a.fused) {
           // publish the tile once the block's last expert pass is stored: bar.red doubles as the
-          // barrier that orders all 128 threads' stores before the release below
+          // barrier that orders all epilogue threads' stores before the release below
           const bool later = row_e > e;
-          if (!named_barrier_or(1, 128, later) && threadIdx.x == 64) {
+          if (!named_barrier_or(1, kEpiThreads, later) && threadIdx.x == kEpiThread0) {
             __threadfence();
             atomicAdd(a.sched + it.rb, 1u);
           }
         }
       } else {
         const int H = a.ph[1].out_cols;
-        const int ncols = min(kTileRows, H - wt * kTileRows);
-        // 256 outputs as bf16 pairs in registers, accumulator released, then stored
+        const int ncols = min(kTileRows, H - wt * kTileRows) - half * (kTileRows / 2);   // this half's columns
+        // 128 outputs in two rounds of 64: each round is converted to bf16 and stored right away;
+        // the accumulator is released after the last round's loads
         if (warp_has_rows) {
-          uint32_t packed[128];
+          uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * H + wt * kTileRows +
+                                                half * (kTileRows / 2));
 #pragma unroll
-          for (int c0 = 0; c0 < kTileRows; c0 += 64) {
+          for (int c0 = 0; c0 < kTileRows / 2; c0 += 64) {
             uint32_t v[4][16];
+            const uint32_t col = static_cast<uint32_t>(half * (kTileRows / 2) + c0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tc_ld_x16(acc + c0 + 16 * j, v[j]);
+            for (int j = 0; j < 4; ++j) tc_ld_x16(acc + col + 16 * j, v[j]);
             tc_wait_ld();
+            if (c0 + 64 >= kTileRows / 2) {
+              tc_fence_before();
+              mbar_arrive(smem_u32(acc_empty));
+            }
+            uint32_t packed[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j) & 15])));
               const uint32_t hi =
                   __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j + 1) & 15])));
-              packed[c0 / 2 + j] = lo | (hi << 16);
+              packed[j] = lo | (hi << 16);
             }
-          }
-          tc_fence_before();
-          mbar_arrive(smem_u32(acc_empty));
-          if (mine) {
-            uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * H + wt * kTileRows);
+            if (mine) {
 #pragma unroll
-            for (int c = 0; c < kTileRows / 8; ++c)
-              if (c * 8 < ncols) dst[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+              for (int c = 0; c < 8; ++c)
+                if (c0 + c * 8 < ncols)
+                  dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            }
           }
         } else {
           tc_fence_before();
           mbar_arrive(smem_u32(acc_empty));
         }
-        if (a.red.out) fused_reduce_tail(a.red, a.y, H, mine, row, wt, a.ph[1].n_wt, wt * kTileRows, ncols);
+        if (a.red.out && ncols > 0)
+          fused_reduce_tail(a.red, a.y, H, mine, row, wt * 2 + half, a.ph[1].n_wt * 2,
+                            wt * kTileRows + half * (kTileRows / 2), min(ncols, kTileRows / 2));
       }
       acc_phase ^= 1;
     }
