@@ -200,6 +200,39 @@ def permute(topk_ids: np.ndarray, E: int, align: int) -> Dict[str, np.ndarray]:
                 expert_counts=cnt.astype(np.int32), seg_start=seg.astype(np.int64), U=U)
 
 
+def permute_batched(topk_ids: np.ndarray, E: int, max_tokens: int) -> Dict[str, np.ndarray]:
+    """BatchedExperts layout [E, max_tokens, H] (MegaMoE page, vLLM 的两种 Activation Format and
+    路径 B: "for each expert: boolean mask -> copy -> b_a1[expert, :rows, :]"; EP note section 11.2,
+    the low-latency (E, T, H) layout with expert_num_tokens).
+
+    Expert e's rows are e*max_tokens + [0, n_e): the tokens whose top-K holds e, in token order
+    (the boolean mask over tokens); rows [n_e, max_tokens) of its slot are padding.
+    """
+    T, K = topk_ids.shape
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    if ids.size and (ids.min() < 0 or ids.max() >= E):
+        raise ValueError("expert id out of range")
+    rows = E * max_tokens
+    sorted_ids = np.full(rows, T * K, dtype=np.int32)
+    expert_ids = np.full(rows, -1, dtype=np.int32)
+    inv = np.zeros((T, K), dtype=np.int32)
+    counts = np.zeros(E, dtype=np.int32)
+    for e in range(E):
+        mask = ids == e                                   # [T, K]; at most one True per token
+        toks = np.nonzero(mask.any(axis=1))[0]            # ascending token order
+        if len(toks) > max_tokens:
+            raise ValueError("expert receives more tokens than its slot holds")
+        for i, t in enumerate(toks):
+            k = int(np.nonzero(mask[t])[0][0])
+            r = e * max_tokens + i
+            sorted_ids[r] = t * K + k
+            expert_ids[r] = e
+            inv[t, k] = r
+        counts[e] = len(toks)
+    return dict(sorted_token_ids=sorted_ids, expert_ids=expert_ids, inv_perm=inv, m_sum=rows,
+                expert_num_tokens=counts)
+
+
 # ----------------------------------------------------------------------------
 # Expert SwiGLU FFN (MegaMoE page, 第三步 and 二、阶段 2-4)
 

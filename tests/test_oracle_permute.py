@@ -98,3 +98,42 @@ def test_msum_upper_decode_shape():
 def test_bad_expert_id_rejected():
     with pytest.raises(ValueError):
         moe.permute(np.array([[0, 5]], dtype=np.int32), 4, 1)
+
+
+# ------------------------------------------------------------------------------------------ BatchedExperts layout
+
+def test_batched_printed_example():
+    g = load_golden("permute_batched_example.txt")
+    ids = np.array(g["topk_ids"], dtype=np.int32).reshape(g["T"], g["K"])
+    p = moe.permute_batched(ids, g["E"], g["max_tokens"])
+    assert p["sorted_token_ids"].tolist() == g["sorted_token_ids"]
+    assert p["expert_ids"].tolist() == g["expert_ids"]
+    assert p["inv_perm"].reshape(-1).tolist() == g["inv_perm"]
+    assert p["expert_num_tokens"].tolist() == g["expert_num_tokens"]
+    assert p["m_sum"] == g["E"] * g["max_tokens"]
+
+
+@pytest.mark.parametrize("T,K,E,S,seed", [(8, 6, 256, 16, 0), (37, 4, 16, 64, 1), (5, 2, 3, 8, 2), (128, 6, 64, 128, 3)])
+def test_batched_slots_hold_the_contiguous_segments(T, K, E, S, seed):
+    # each expert's slot holds exactly the pairs of that expert's contiguous segment, in the same
+    # order (two independent constructions: per-expert boolean masks vs one stable sort)
+    rng = np.random.default_rng(seed)
+    ids = np.array([rng.choice(E, K, replace=False) for _ in range(T)], dtype=np.int32)
+    b = moe.permute_batched(ids, E, S)
+    c = moe.permute(ids, E, 1)
+    for e in range(E):
+        n = int(c["expert_counts"][e])
+        seg = int(c["seg_start"][e])
+        assert b["expert_num_tokens"][e] == n
+        assert b["sorted_token_ids"][e * S: e * S + n].tolist() == c["sorted_token_ids"][seg: seg + n].tolist()
+        assert (b["expert_ids"][e * S: e * S + n] == e).all() and (b["expert_ids"][e * S + n: (e + 1) * S] == -1).all()
+        assert (b["sorted_token_ids"][e * S + n: (e + 1) * S] == T * K).all()
+    flat = b["inv_perm"].reshape(-1)
+    assert np.array_equal(b["sorted_token_ids"][flat], np.arange(T * K))
+    assert np.array_equal(b["expert_ids"][flat], ids.reshape(-1))
+
+
+def test_batched_rejects_an_overfull_slot():
+    ids = np.array([[0, 1], [0, 2], [0, 1]], dtype=np.int32)     # expert 0 receives 3 tokens
+    with pytest.raises(ValueError):
+        moe.permute_batched(ids, 3, 2)
