@@ -232,6 +232,62 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
                        int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                        int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* --------------------------------------------------------------------------------------
+ * BatchedExperts layout (MegaMoE page, vLLM 的两种 Activation Format and 路径 B: each expert
+ * owns a fixed slot of max_tokens rows filled through a boolean mask over the tokens; note
+ * "INT8 高吞吐/低延迟 EP 代码梳理" §11.2: the low-latency (E, max_tokens, H) buffer with
+ * expert_num_tokens).  Rows of the permuted buffers: U = E * max_tokens, expert e's slot is rows
+ * [e * max_tokens, (e + 1) * max_tokens), its first expert_num_tokens[e] rows live, the rest
+ * padding.  max_tokens is a power of two in [1, 4096].  Scale tensors are tiled as for the
+ * contiguous calls with align = min(max_tokens, 256).
+ * ------------------------------------------------------------------------------------ */
+
+/* Workspace bytes of the BatchedExperts calls (zero-filled once before first use). */
+moe_status moe_workspace_size_batched(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes);
+
+/* BatchedExperts permute.  With n_e = #(t,k) routed to e:
+ *   inv_perm[t,k]          [T, K] out: e * max_tokens + (rank of (t,k) among expert e's pairs
+ *                          in ascending t*K+k order)
+ *   sorted_token_ids[row]  [U] out: t*K + k of the pair on that row, T*K on padding rows
+ *   expert_ids[row]        [U] out: expert of the row, -1 on padding rows
+ *   m_sum                  [1] out (device): U
+ *   expert_num_tokens      [E] out or NULL: n_e
+ *   x_q, x_sf, x_perm, x_perm_sf: as for moe_permute (x_perm [U, H]).
+ * A pair that would land past its expert's slot (n_e > max_tokens, possible only when a token
+ * names one expert twice or T > max_tokens) is dropped: inv_perm = -1, nothing else written
+ * for it, and MOE_ERR_DEVICE_INDEX is recorded.  An id outside [0, E) as for moe_permute. */
+moe_status moe_permute_batched(const int32_t* topk_ids, int T, int K, int E, int max_tokens,
+                               int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                               int32_t* m_sum, int32_t* expert_num_tokens, const uint8_t* x_q,
+                               const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* Both expert GEMMs over a BatchedExperts buffer: moe_grouped_ffn's arithmetic on every live row
+ * (row i of slot e with i < expert_num_tokens[e], expert e); padding rows of h_q and y_perm are
+ * unspecified.  x_perm [U, H] E4M3, x_perm_sf tiled (rows U, slabs H/128); h_q [U, I], h_sf,
+ * y_perm [U, H] bf16 out.  expert_num_tokens [E] int32 on the device (a count above max_tokens
+ * records MOE_ERR_DEVICE_INDEX).  The row map (expert of each row) is written into the
+ * workspace by a small kernel before the GEMMs.  ws: moe_workspace_size_batched(T, H, I, E, K,
+ * max_tokens) bytes; T and K only size that workspace (T = max_tokens, K = 1 when the buffer
+ * comes from elsewhere). */
+moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                   const int32_t* expert_num_tokens, int T, int K, int H, int I, int E,
+                                   int max_tokens, moe_weight w13, moe_weight w2, uint8_t* h_q,
+                                   uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                                   void* stream);
+
+/* moe_forward over the BatchedExperts layout: route -> moe_permute_batched -> L1 -> L2 ->
+ * reduce.  `out` equals moe_forward's bit for bit (each row's arithmetic does not depend on the
+ * row it sits on).  Requires T <= max_tokens (an expert receives at most T tokens).  The index
+ * outputs (any may be NULL) are those of moe_permute_batched. */
+moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                               const float* e_score_bias, int T, int H, int I, int E, int K,
+                               int max_tokens, moe_score_fn fn, int renormalize, moe_weight w13,
+                               moe_weight w2, uint16_t* out, int32_t* topk_ids, float* topk_w,
+                               int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                               int32_t* m_sum, int32_t* expert_num_tokens, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* Synchronises `stream`, returns the device status word recorded in `ws` through
  * *device_status (MOE_OK if none) and clears it.  The return value reports host errors. */
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status);

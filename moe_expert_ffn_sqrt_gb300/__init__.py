@@ -73,6 +73,15 @@ def lib():
         L.moe_unpermute_reduce.argtypes = [P, P, P, I, I, I, P, P]
         L.moe_forward.restype = S
         L.moe_forward.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P, Z, P]
+        L.moe_workspace_size_batched.restype = S
+        L.moe_workspace_size_batched.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
+        L.moe_permute_batched.restype = S
+        L.moe_permute_batched.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, Z, P]
+        L.moe_grouped_ffn_batched.restype = S
+        L.moe_grouped_ffn_batched.argtypes = [P, P, P, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, Z, P]
+        L.moe_forward_batched.restype = S
+        L.moe_forward_batched.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P,
+                                          P, P, Z, P]
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.moe_status_str.restype = ctypes.c_char_p
@@ -279,6 +288,64 @@ def forward(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, reno
                              _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
                              _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
            "moe_forward")
+
+
+# ------------------------------------------------------------------ BatchedExperts layout
+
+def workspace_size_batched(T, H, I, E, K, max_tokens):
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_batched(T, H, I, E, K, max_tokens, ctypes.byref(n)), "moe_workspace_size_batched")
+    return int(n.value)
+
+
+def new_workspace_batched(T, H, I, E, K, max_tokens, device="cuda"):
+    """A zero-filled workspace tensor of the size moe_workspace_size_batched() asks for."""
+    return torch.zeros(workspace_size_batched(T, H, I, E, K, max_tokens), dtype=torch.uint8, device=device)
+
+
+def batched_align(max_tokens):
+    """Alignment the scale tiling of the BatchedExperts buffers uses."""
+    return min(max_tokens, 256)
+
+
+def permute_batched(topk_ids, E, max_tokens, sorted_token_ids, expert_ids, inv_perm, m_sum, ws,
+                    expert_num_tokens=None, x_q=None, x_sf=None, x_perm=None, x_perm_sf=None):
+    T, K = topk_ids.shape
+    H = x_q.shape[1] if x_q is not None else 0
+    _check(lib().moe_permute_batched(_ptr(topk_ids, torch.int32, "topk_ids"), T, K, E, max_tokens,
+                                     _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                                     _ptr(expert_ids, torch.int32, "expert_ids"),
+                                     _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"),
+                                     _ptr(expert_num_tokens, torch.int32, "expert_num_tokens"),
+                                     _ptr(x_q, torch.uint8, "x_q"), _ptr(x_sf, torch.uint8, "x_sf"), H,
+                                     _ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+                                     _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_permute_batched")
+
+
+def grouped_ffn_batched(x_perm, x_perm_sf, expert_num_tokens, T, K, H, I, E, max_tokens, w13, w2, h_q, h_sf, y_perm,
+                        ws):
+    """L1 + SwiGLU + requant and L2 over a BatchedExperts buffer [E * max_tokens, H]."""
+    _check(lib().moe_grouped_ffn_batched(_ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+                                         _ptr(expert_num_tokens, torch.int32, "expert_num_tokens"), T, K, H, I, E,
+                                         max_tokens, w13.c(), w2.c(), _ptr(h_q, torch.uint8, "h_q"),
+                                         _ptr(h_sf, torch.uint8, "h_sf"), _ptr(y_perm, torch.bfloat16, "y_perm"),
+                                         _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_ffn_batched")
+
+
+def forward_batched(hidden, w_gate, gate_bias, e_score_bias, I, K, max_tokens, score_fn, renormalize, w13, w2, out,
+                    ws, topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None,
+                    m_sum=None, expert_num_tokens=None):
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_forward_batched(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"),
+        T, H, I, E, K, max_tokens, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
+        _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"),
+        _ptr(expert_num_tokens, torch.int32, "expert_num_tokens"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream()), "moe_forward_batched")
 
 
 def get_error(ws):

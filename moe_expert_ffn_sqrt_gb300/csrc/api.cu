@@ -32,9 +32,10 @@ struct WsLayout {
   size_t total = 0;
 };
 
-WsLayout layout(int T, int H, int I, int E, int K, int align) {
+// U: rows of the permuted buffers (moe_msum_upper for the contiguous layout, E * max_tokens for
+// the BatchedExperts layout).
+WsLayout layout_rows(int T, int H, int I, int E, int K, int align, size_t U) {
   WsLayout L;
-  const size_t U = moe_msum_upper(T, K, E, align);
   size_t off = kAlign;                             // [0, 256): status word
   L.perm = off;       off = up(off + permute_scratch_bytes(T, K, E));   // permute chunk counts
   L.partial = off;
@@ -59,6 +60,20 @@ WsLayout layout(int T, int H, int I, int E, int K, int align) {
   L.total = off;
   return L;
 }
+
+WsLayout layout(int T, int H, int I, int E, int K, int align) {
+  return layout_rows(T, H, I, E, K, align, moe_msum_upper(T, K, E, align));
+}
+
+// BatchedExperts slot size: a power of two, at most kMaxSlot rows.
+constexpr int kMaxSlot = 4096;
+bool slot_ok(int max_tokens) {
+  return max_tokens >= 1 && max_tokens <= kMaxSlot && (max_tokens & (max_tokens - 1)) == 0;
+}
+// Alignment the GEMMs and the scale tiling see for a slot size: slots of 256 rows or more keep
+// whole 128-row blocks inside one expert exactly as the 256 alignment does.
+int slot_align(int max_tokens) { return max_tokens < 256 ? max_tokens : 256; }
+size_t slot_rows(int E, int max_tokens) { return static_cast<size_t>(E) * max_tokens; }
 
 // moe_forward folds the unpermute-reduce into the L2 epilogue up to this many tokens.  With many
 // tokens per row block one epilogue warp would reduce tokens one after another; the separate
@@ -153,10 +168,13 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
                                   S(stream)));
 }
 
-moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
-                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
-                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                       void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+// slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
+static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, int align, int slot,
+                                 int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum,
+                                 int32_t* expert_counts, const uint8_t* x_q, const uint8_t* x_sf, int H,
+                                 uint8_t* x_perm, uint8_t* x_perm_sf, void* ws, size_t ws_bytes, void* stream) {
   if (T < 0 || K <= 0 || E <= 0 || K > E || align < 1 || align > 256 || (align & (align - 1)))
     return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
@@ -166,11 +184,36 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, 
     return MOE_ERR_INVALID_ARG;
   if (copy && (H <= 0 || H % 128 || !aligned(x_q, 16) || !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kAlign + permute_scratch_bytes(T, K, E)) return MOE_ERR_WORKSPACE;
-  const size_t U = moe_msum_upper(T, K, E, align);
+  const size_t U = slot ? slot_rows(E, slot) : moe_msum_upper(T, K, E, align);
   int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kAlign);   // layout().perm
   return cuda_status(launch_permute(topk_ids, T, K, E, align, static_cast<int>(U), sorted_token_ids, expert_ids,
                                     inv_perm, m_sum, expert_counts, x_q, x_sf, H, x_perm, x_perm_sf,
-                                    status_of(ws), scratch, S(stream)));
+                                    status_of(ws), scratch, S(stream), slot));
+}
+
+extern "C" {
+
+moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, int32_t* sorted_token_ids,
+                       int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                       const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
+                       void* ws, size_t ws_bytes, void* stream) {
+  return permute_common(topk_ids, T, K, E, align, 0, sorted_token_ids, expert_ids, inv_perm, m_sum, expert_counts,
+                        x_q, x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream);
+}
+
+moe_status moe_workspace_size_batched(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes) {
+  if (!bytes || !slot_ok(max_tokens) || !dims_ok(T, H, I, E, K, slot_align(max_tokens))) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_rows(T, H, I, E, K, slot_align(max_tokens), slot_rows(E, max_tokens)).total;
+  return MOE_OK;
+}
+
+moe_status moe_permute_batched(const int32_t* topk_ids, int T, int K, int E, int max_tokens,
+                               int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum,
+                               int32_t* expert_num_tokens, const uint8_t* x_q, const uint8_t* x_sf, int H,
+                               uint8_t* x_perm, uint8_t* x_perm_sf, void* ws, size_t ws_bytes, void* stream) {
+  if (!slot_ok(max_tokens)) return MOE_ERR_INVALID_ARG;
+  return permute_common(topk_ids, T, K, E, slot_align(max_tokens), max_tokens, sorted_token_ids, expert_ids,
+                        inv_perm, m_sum, expert_num_tokens, x_q, x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream);
 }
 
 // Launch description of one MXFP4 GEMM (L1: x = x_perm [U, H] against W13; L2: x = h [U, I] against W2).
@@ -199,7 +242,7 @@ static GemmLaunch mx_launch(bool l1, const uint8_t* x, const uint8_t* x_sf, cons
 static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
-                              size_t ws_bytes, void* stream, const FusedReduce* red = nullptr) {
+                              size_t ws_bytes, void* stream, const FusedReduce* red = nullptr, size_t rows = 0) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
   if (!(l1 ? weight_ok(w, E, 2 * I, H, 2) : weight_ok(w, E, H, I, 1))) return MOE_ERR_INVALID_ARG;
@@ -207,11 +250,11 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
   if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
   if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
-  const size_t U = moe_msum_upper(T, K, E, align);
+  const size_t U = rows ? rows : moe_msum_upper(T, K, E, align);
   if (U == 0) return MOE_OK;
   if (w.fmt == MOE_W_NVFP4) {
     // bf16 copy of the activation rows in the workspace, then the bf16 MMA path
-    const WsLayout Lw = layout(T, H, I, E, K, align);
+    const WsLayout Lw = layout_rows(T, H, I, E, K, align, U);
     if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
     uint16_t* xb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + Lw.xb);
     const int Kd = l1 ? H : I;
@@ -236,7 +279,7 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     if (red) N.red = *red;
     return cuda_status(launch_gemm_nv(N, l1, S(stream)));
   }
-  const WsLayout Lw = layout(T, H, I, E, K, align);
+  const WsLayout Lw = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
   GemmLaunch L = mx_launch(l1, x, x_sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
   if (red) L.red = *red;
@@ -264,13 +307,13 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
 static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
                              const int32_t* m_sum, int T, int K, int H, int I, int E, int align, const moe_weight& w13,
                              const moe_weight& w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
-                             size_t ws_bytes, void* stream, const FusedReduce* red) {
+                             size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
-                                nullptr, ws, ws_bytes, stream);
+                                nullptr, ws, ws_bytes, stream, nullptr, rows);
     if (st != MOE_OK) return st;
     return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws,
-                       ws_bytes, stream, red);
+                       ws_bytes, stream, red, rows);
   }
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x_perm || !x_perm_sf || !expert_ids || !m_sum || !h_q || !h_sf || !y) return MOE_ERR_INVALID_ARG;
@@ -278,9 +321,9 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   if (!aligned(x_perm, 16) || !aligned(x_perm_sf, 16) || !aligned(h_q, 16) || !aligned(h_sf, 16) || !aligned(y, 16))
     return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
-  const WsLayout L = layout(T, H, I, E, K, align);
+  const size_t U = rows ? rows : moe_msum_upper(T, K, E, align);
+  const WsLayout L = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  const size_t U = moe_msum_upper(T, K, E, align);
   if (U == 0) return MOE_OK;
   GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
   GemmLaunch l2 = mx_launch(false, h_q, h_sf, expert_ids, m_sum, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
@@ -297,6 +340,27 @@ moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, cons
                     ws_bytes, stream, nullptr);
 }
 
+moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_num_tokens,
+                                   int T, int K, int H, int I, int E, int max_tokens, moe_weight w13, moe_weight w2,
+                                   uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!slot_ok(max_tokens) || !expert_num_tokens) return MOE_ERR_INVALID_ARG;
+  const int align = slot_align(max_tokens);
+  if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  const size_t U = slot_rows(E, max_tokens);
+  if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = layout_rows(T, H, I, E, K, align, U);
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  char* b = static_cast<char*>(ws);
+  int32_t* eids = reinterpret_cast<int32_t*>(b + L.expert_ids);
+  int32_t* ms = reinterpret_cast<int32_t*>(b + L.m_sum);
+  if (launch_batched_rows(expert_num_tokens, E, max_tokens, eids, ms, status_of(ws), S(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return ffn_common(x_perm, x_perm_sf, eids, ms, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws, ws_bytes,
+                    stream, nullptr, U);
+}
+
 moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int K,
                                 int H, uint16_t* out, void* stream) {
   if (T < 0 || K <= 0 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
@@ -305,17 +369,23 @@ moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
   return cuda_status(launch_unpermute_reduce(y_perm, inv_perm, topk_w, T, K, H, out, S(stream)));
 }
 
-moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
-                       const float* e_score_bias, int T, int H, int I, int E, int K, int align, moe_score_fn fn,
-                       int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
-                       float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
-                       int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+// slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
+static moe_status forward_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                 const float* e_score_bias, int T, int H, int I, int E, int K, int align, int slot,
+                                 moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
+                                 uint16_t* out, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
+                                 int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                                 void* ws, size_t ws_bytes, void* stream) {
   if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
   if (!hidden || !w_gate || !out || !weight_ok(w13, E, 2 * I, H, 2) || !weight_ok(w2, E, H, I, 1))
     return MOE_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
-  const WsLayout L = layout(T, H, I, E, K, align);
+  const size_t U = slot ? slot_rows(E, slot) : moe_msum_upper(T, K, E, align);
+  if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  const WsLayout L = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
   char* b = static_cast<char*>(ws);
@@ -335,7 +405,8 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
   moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
                             xq, xsf, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  st = moe_permute(ids, T, K, E, align, sorted, eids, inv, ms, nullptr, xq, xsf, H, xp, xpsf, ws, ws_bytes, stream);
+  st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, expert_counts, xq, xsf, H, xp, xpsf, ws,
+                      ws_bytes, stream);
   if (st != MOE_OK) return st;
   const bool fuse_reduce = T <= kFusedReduceMaxTokens;
   FusedReduce red{};
@@ -348,9 +419,34 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
     red.K = K;
   }
   st = ffn_common(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y, ws, ws_bytes, stream,
-                  fuse_reduce ? &red : nullptr);
+                  fuse_reduce ? &red : nullptr, U);
   if (st != MOE_OK || fuse_reduce) return st;
   return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
+}
+
+extern "C" {
+
+moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                       const float* e_score_bias, int T, int H, int I, int E, int K, int align, moe_score_fn fn,
+                       int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
+                       float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                       int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, fn, renormalize, w13, w2,
+                        out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws, ws_bytes,
+                        stream);
+}
+
+moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                               const float* e_score_bias, int T, int H, int I, int E, int K, int max_tokens,
+                               moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
+                               int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                               int32_t* inv_perm, int32_t* m_sum, int32_t* expert_num_tokens, void* ws,
+                               size_t ws_bytes, void* stream) {
+  // a token's K experts are distinct, so no expert receives more than T tokens
+  if (!slot_ok(max_tokens) || max_tokens < T) return MOE_ERR_INVALID_ARG;
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(max_tokens), max_tokens,
+                        fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        expert_num_tokens, ws, ws_bytes, stream);
 }
 
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status) {

@@ -19,10 +19,12 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
 // permute.cu
 size_t permute_smem_bytes(int E);
 size_t permute_scratch_bytes(int T, int K, int E);   // per-CTA expert counts of the multi-CTA path
+cudaError_t launch_batched_rows(const int32_t* counts, int E, int slot, int32_t* expert_ids, int32_t* m_sum,
+                                uint32_t* status, cudaStream_t stream);   // BatchedExperts row map from counts
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, int32_t* scratch, cudaStream_t stream);
+                           uint32_t* status, int32_t* scratch, cudaStream_t stream, int slot = 0);
 
 // gate.cu (T > 16: gate GEMM on the tensor cores, three exact bf16 parts of the fp32 gate weight)
 int gate_nsplit(int T, int H, int E);

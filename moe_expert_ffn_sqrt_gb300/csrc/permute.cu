@@ -11,6 +11,8 @@
 //   3. each warp walks its sub-range in order, 32 pairs at a time; __match_any_sync groups equal
 //      experts so that each pair's rank among earlier pairs of its expert is exact.
 // Padding rows get expert_ids = -1 and sorted_token_ids = T*K.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -28,6 +30,9 @@ struct PermuteArgs {
   int32_t* m_sum;
   int32_t* counts;       // optional
   uint32_t* status;
+  int slot;              // 0: contiguous segments padded to align; > 0: BatchedExperts, expert e's rows
+                         // start at e * slot and its segment is slot rows.  A pair that would land past
+                         // its expert's slot is dropped (inv_perm -1) and recorded as an index error.
 };
 
 // Larger problems: G CTAs, CTA c owning the contiguous pairs [c*CH, (c+1)*CH) and each of its 32
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
       }
       tot[e] = t_all;
       pre_mine[j] = t_pre;
-      local += (t_all + a.align - 1) / a.align * a.align;
+      local += a.slot > 0 ? a.slot : (t_all + a.align - 1) / a.align * a.align;
     }
   }
   s_scan[tid] = local;
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
         hist[w * a.E + e] = base;
         base += h;
       }
-      run += (tot[e] + a.align - 1) / a.align * a.align;
+      run += a.slot > 0 ? a.slot : (tot[e] + a.align - 1) / a.align * a.align;
     }
   }
   if (tid == kPermThreads - 1) s_total = s_scan[tid];
@@ -152,15 +157,20 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
     if (ok && rank == 0) hist[warp * a.E + e] += __popc(peers);
     __syncwarp();
     if (ok) {
-      a.inv_perm[i] = pos;
-      a.sorted_ids[pos] = i;
-      a.expert_ids[pos] = e;
+      if (a.slot > 0 && pos - seg[e] >= a.slot) {
+        record_error(a.status, kDevErrIndex);
+        a.inv_perm[i] = -1;
+      } else {
+        a.inv_perm[i] = pos;
+        a.sorted_ids[pos] = i;
+        a.expert_ids[pos] = e;
+      }
     }
   }
   // 4. padding rows inside each segment (experts split over CTAs), then the tail [M_sum, U)
   for (int e = c * kPermWarps + warp; e < a.E; e += G * kPermWarps) {
     const int n = tot[e];
-    const int padded = (n + a.align - 1) / a.align * a.align;
+    const int padded = a.slot > 0 ? a.slot : (n + a.align - 1) / a.align * a.align;
     for (int r = n + lane; r < padded; r += 32) {
       a.sorted_ids[seg[e] + r] = N;
       a.expert_ids[seg[e] + r] = -1;
@@ -215,7 +225,10 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
   }
   if (tid < N) s_rank[tid] = rank;
   __syncthreads();
-  if (warp == 0) {                   // exclusive scan of the aligned segment sizes
+  if (a.slot > 0) {                  // BatchedExperts: fixed slots
+    for (int e = tid; e < a.E; e += kPermThreads) seg[e] = e * a.slot;
+    if (tid == 0) s_total = a.E * a.slot;
+  } else if (warp == 0) {            // exclusive scan of the aligned segment sizes
     const int per = (a.E + 31) / 32;
     int local = 0;
     for (int j = 0; j < per; ++j) {
@@ -242,14 +255,19 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
   const int msum = s_total;
   if (blockIdx.x == 0) {
     if (e_mine >= 0) {
-      const int pos = seg[e_mine] + rank;
-      a.inv_perm[tid] = pos;
-      a.sorted_ids[pos] = tid;
-      a.expert_ids[pos] = e_mine;
+      if (a.slot > 0 && rank >= a.slot) {
+        record_error(a.status, kDevErrIndex);
+        a.inv_perm[tid] = -1;
+      } else {
+        const int pos = seg[e_mine] + rank;
+        a.inv_perm[tid] = pos;
+        a.sorted_ids[pos] = tid;
+        a.expert_ids[pos] = e_mine;
+      }
     }
     for (int e = warp; e < a.E; e += kPermWarps) {
       const int c = cnt[e];
-      const int padded = (c + a.align - 1) / a.align * a.align;
+      const int padded = a.slot > 0 ? a.slot : (c + a.align - 1) / a.align * a.align;
       for (int r = c + lane; r < padded; r += 32) {
         a.sorted_ids[seg[e] + r] = N;
         a.expert_ids[seg[e] + r] = -1;
@@ -267,7 +285,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
     const int chunks = H / 16, slabs = H / 128;
     for (int p = blockIdx.x * kPermWarps + warp; p < N; p += gridDim.x * kPermWarps) {
       const int e = s_ids[p];
-      if (e < 0) continue;
+      if (e < 0 || (a.slot > 0 && s_rank[p] >= a.slot)) continue;
       const int dst = seg[e] + s_rank[p];
       const int t = p / a.K;
       const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
@@ -304,6 +322,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
   if (e < 0 || e >= E) return;
   const int t = static_cast<int>(pair / K);
   const int dst = inv_perm[pair];
+  if (dst < 0) return;                         // dropped by a full BatchedExperts slot
   const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
   uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
   for (int j = lane; j < H / 16; j += 32) out[j] = src[j];
@@ -314,11 +333,36 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
 size_t permute_smem_bytes(int E) { return static_cast<size_t>(kPermWarps + 2) * E * sizeof(int32_t); }
 
 
+// BatchedExperts row map from per-expert live-row counts: row r of slot e = r / slot is live
+// (expert_ids[r] = e) when r % slot < count[e], else padding (-1).  A count above the slot size
+// is an index error (the slot's rows are then all taken as live).  m_sum = E * slot.
+__global__ void __launch_bounds__(256) batched_rows_kernel(const int32_t* __restrict__ counts, int E, int slot,
+                                                           int32_t* __restrict__ expert_ids, int32_t* m_sum,
+                                                           uint32_t* status) {
+  const long long U = static_cast<long long>(E) * slot;
+  for (long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; r < U;
+       r += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int e = static_cast<int>(r / slot), i = static_cast<int>(r - static_cast<long long>(e) * slot);
+    const int n = __ldg(counts + e);
+    if (i == 0 && (n < 0 || n > slot)) record_error(status, kDevErrIndex);
+    expert_ids[r] = i < n ? e : -1;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *m_sum = static_cast<int>(U);
+}
+
+cudaError_t launch_batched_rows(const int32_t* counts, int E, int slot, int32_t* expert_ids, int32_t* m_sum,
+                                uint32_t* status, cudaStream_t stream) {
+  const long long U = static_cast<long long>(E) * slot;
+  const int grid = static_cast<int>(std::min<long long>((U + 255) / 256, 4 * 152));
+  batched_rows_kernel<<<grid < 1 ? 1 : grid, 256, 0, stream>>>(counts, E, slot, expert_ids, m_sum, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int align, int U, int32_t* sorted_ids,
                            int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* counts,
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
-                           uint32_t* status, int32_t* scratch, cudaStream_t stream) {
-  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status};
+                           uint32_t* status, int32_t* scratch, cudaStream_t stream, int slot) {
+  PermuteArgs a{topk_ids, T, K, E, align, U, sorted_ids, expert_ids, inv_perm, m_sum, counts, status, slot};
   const int bt = act_sf_block_rows(align), nb = act_sf_blocks(U, bt);
   const long long npairs = static_cast<long long>(T) * K;
   cudaError_t err;
