@@ -61,6 +61,9 @@ def parse_args():
                    help="override E (smaller cases of the same kernels for profiler captures)")
     p.add_argument("--tokens", type=int, default=None,
                    help="override T (smaller cases of the same kernels for profiler captures)")
+    p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched"],
+                   help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
+                        "BatchedExperts slots of max_tokens = the smallest power of two >= T (moe_forward_batched)")
     return p.parse_args()
 
 
@@ -218,8 +221,10 @@ def algorithmic_bytes(w, n_touched):
             "layer": w13 + w2 + 4 * w.E * w.H + 2 * w.T * w.H * 2}
 
 
-def kernel_name(stage):
-    return "L1+L2 grouped GEMM (one launch)" if stage == "ffn" else f"{stage} grouped GEMM"
+def kernel_name(stage, fmt):
+    if stage == "ffn":
+        return "L1+L2 grouped GEMM (one launch)" if fmt == "mxfp4" else "L1 then L2 grouped GEMM"
+    return f"{stage} grouped GEMM"
 
 
 def run_ours(args, w):
@@ -252,13 +257,23 @@ def run_ours(args, w):
     w_gate = d(inp["w_gate"])
     gate_bias = None if inp["gate_bias"] is None else d(inp["gate_bias"])
     e_bias = None if inp["e_score_bias"] is None else d(inp["e_score_bias"])
-    ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align, device=dev)
+    batched = args.layout == "batched"
+    S = 1 << max(0, (T - 1).bit_length())         # BatchedExperts slot: smallest power of two >= T
+    if batched:
+        ws = M.new_workspace_batched(T, w.H, w.I, w.E, w.K, S, device=dev)
+    else:
+        ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align, device=dev)
     out = torch.empty(T, w.H, dtype=torch.bfloat16, device=dev)
     out_host = torch.empty(T, w.H, dtype=torch.bfloat16).pin_memory()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)     # > L2 (126 MB)
 
     def step():
-        M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out, ws)
+        if batched:
+            M.forward_batched(hidden, w_gate, gate_bias, e_bias, w.I, w.K, S, w.score_fn, w.renormalize, w13, w2, out,
+                              ws)
+        else:
+            M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out,
+                      ws)
 
     def barrier():
         if W > 1:
@@ -297,7 +312,8 @@ def run_ours(args, w):
     value = W * T / (ms / 1e3)
 
     # ---- per-kernel durations: the same path called stage by stage with events in between
-    U = M.msum_upper(T, w.K, w.E, w.align)
+    align = M.batched_align(S) if batched else w.align
+    U = w.E * S if batched else M.msum_upper(T, w.K, w.E, w.align)
     ids = torch.empty(T, w.K, dtype=torch.int32, device=dev)
     tw = torch.empty(T, w.K, dtype=torch.float32, device=dev)
     xq = torch.empty(T, w.H, dtype=torch.uint8, device=dev)
@@ -308,12 +324,14 @@ def run_ours(args, w):
     msum = torch.empty(1, dtype=torch.int32, device=dev)
     cnt = torch.empty(w.E, dtype=torch.int32, device=dev)
     xp = torch.empty(U, w.H, dtype=torch.uint8, device=dev)
-    xpsf = torch.empty(M.act_sf_tiled_bytes(U, w.H // 128, w.align), dtype=torch.uint8, device=dev)
+    xpsf = torch.empty(M.act_sf_tiled_bytes(U, w.H // 128, align), dtype=torch.uint8, device=dev)
     hq = torch.empty(U, w.I, dtype=torch.uint8, device=dev)
-    hsf = torch.empty(M.act_sf_tiled_bytes(U, w.I // 128, w.align), dtype=torch.uint8, device=dev)
+    hsf = torch.empty(M.act_sf_tiled_bytes(U, w.I // 128, align), dtype=torch.uint8, device=dev)
     y = torch.empty(U, w.H, dtype=torch.bfloat16, device=dev)
     # MXFP4: the expert FFN is one launch (moe_grouped_ffn), timed as one stage; NVFP4: L1 and L2 apart
-    fused = w.fmt == "mxfp4"
+    # (BatchedExperts: the whole FFN through moe_grouped_ffn_batched, whose row-map kernel from the
+    # per-expert counts is counted in the stage; moe_forward_batched takes the row map from the permute)
+    fused = w.fmt == "mxfp4" or batched
     stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     barrier()
@@ -328,11 +346,17 @@ def run_ours(args, w):
         M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
         j += 1
         e[j].record()
-        M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
-                  x_perm_sf=xpsf)
+        if batched:
+            M.permute_batched(ids, w.E, S, srt, eids, inv, msum, ws, expert_num_tokens=cnt, x_q=xq, x_sf=xsf,
+                              x_perm=xp, x_perm_sf=xpsf)
+        else:
+            M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
+                      x_perm_sf=xpsf)
         j += 1
         e[j].record()
-        if fused:
+        if batched:
+            M.grouped_ffn_batched(xp, xpsf, cnt, T, w.K, w.H, w.I, w.E, S, w13, w2, hq, hsf, y, ws)
+        elif fused:
             M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, w2, hq, hsf, y, ws)
         else:
             M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
@@ -350,6 +374,7 @@ def run_ours(args, w):
     ab = algorithmic_bytes(w, n_touched)
     hbm, bf16, peak_src = peaks()
     top = "ffn" if fused else max(("l1", "l2"), key=lambda s: stage_ms[s])
+    top_key = f"{w.name}:{top}" + (":batched" if batched else "")
     kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc", "gemm.cu" if w.fmt == "mxfp4" else "gemm_nv.cu")
     tk = w.T * w.K
     flops = {"l1": 2.0 * tk * 2 * w.I * w.H, "l2": 2.0 * tk * w.I * w.H}
@@ -362,7 +387,7 @@ def run_ours(args, w):
     sec = stage_ms[top] / 1e3
     hbm_frac = ab[top] / sec / 1e9 / hbm
     tensor_frac = flops[top] / sec / 1e12 / peak_t
-    common = {"traffic": traffic_record(kernel_file, f"{w.name}:{top}"), "kernel": kernel_name(top),
+    common = {"traffic": traffic_record(kernel_file, top_key), "kernel": kernel_name(top, w.fmt),
               "algorithmic_bytes": ab[top], "algorithmic_flops": flops[top], "stage_ms": stage_ms,
               "experts_touched": n_touched, "hbm_frac": hbm_frac, "tensor_frac": tensor_frac,
               "layer_hbm_frac": ab["layer"] / (ms / 1e3) / 1e9 / hbm}
@@ -405,6 +430,7 @@ def run_ours(args, w):
         cfg = workload_config(w)
         cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
         cfg["parallelism"] = f"replicas x{W}"
+        cfg["layout"] = f"BatchedExperts, max_tokens={S}" if batched else "expert-contiguous, padded to align"
         line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None,

@@ -191,10 +191,11 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
 // the number of earlier pairs (smaller flat index) with the same expert, counted in shared
 // memory; one warp scans the expert counts.  CTA 0 writes the permutation.  When there are few
 // pairs the same launch also copies the activation rows: every CTA recomputes the (cheap)
-// permutation and its warps copy one pair's row each, so the copy is spread over ceil(N/32) SMs
-// with all of a lane's loads issued before its stores.
+// permutation and each warp copies a 1 KB piece of one pair's row (two 16-byte loads per lane,
+// issued before the stores), so the copy is spread over N * H / 1024 warps.
 constexpr int kSmallPairs = 1024;
 constexpr int kSmallCopyPairs = 128;
+constexpr int kCopyPiece = 64;       // 16-byte chunks of a row one warp copies (1 KB)
 
 __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const PermuteArgs a, const uint8_t* x_q,
                                                                         const uint8_t* x_sf, int H, uint8_t* x_perm,
@@ -282,29 +283,30 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
     if (tid == 0) *a.m_sum = msum;
   }
   if (x_perm != nullptr && N <= kSmallCopyPairs) {
-    const int chunks = H / 16, slabs = H / 128;
-    for (int p = blockIdx.x * kPermWarps + warp; p < N; p += gridDim.x * kPermWarps) {
+    // one warp per (pair, 1 KB piece of its row); the piece-0 warp also copies the row's scales
+    const int chunks = H / 16, slabs = H / 128, pieces = (chunks + kCopyPiece - 1) / kCopyPiece;
+    for (int u = blockIdx.x * kPermWarps + warp; u < N * pieces; u += gridDim.x * kPermWarps) {
+      const int p = u / pieces, piece = u - p * pieces;
       const int e = s_ids[p];
       if (e < 0 || (a.slot > 0 && s_rank[p] >= a.slot)) continue;
       const int dst = seg[e] + s_rank[p];
       const int t = p / a.K;
       const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
       uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
-      for (int j0 = 0; j0 < chunks; j0 += 32 * 8) {
-        uint4 v[8];
+      uint4 v[kCopyPiece / 32];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = j0 + u * 32 + lane;
-          if (j < chunks) v[u] = __ldg(src + j);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = j0 + u * 32 + lane;
-          if (j < chunks) out[j] = v[u];
-        }
+      for (int i = 0; i < kCopyPiece / 32; ++i) {
+        const int j = piece * kCopyPiece + i * 32 + lane;
+        if (j < chunks) v[i] = __ldg(src + j);
       }
-      for (int s2 = lane; s2 < slabs; s2 += 32)
-        x_perm_sf[act_sf_offset(bt, nb, dst, s2)] = x_sf[static_cast<size_t>(t) * slabs + s2];
+#pragma unroll
+      for (int i = 0; i < kCopyPiece / 32; ++i) {
+        const int j = piece * kCopyPiece + i * 32 + lane;
+        if (j < chunks) out[j] = v[i];
+      }
+      if (piece == 0)
+        for (int s2 = lane; s2 < slabs; s2 += 32)
+          x_perm_sf[act_sf_offset(bt, nb, dst, s2)] = x_sf[static_cast<size_t>(t) * slabs + s2];
     }
   }
 }
@@ -371,7 +373,8 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     err = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const bool copy = x_perm != nullptr && npairs <= kSmallCopyPairs;
-    const int grid = copy && npairs > 0 ? static_cast<int>((npairs + kPermWarps - 1) / kPermWarps) : 1;
+    const long long units = npairs * ((H / 16 + kCopyPiece - 1) / kCopyPiece);
+    const int grid = copy && npairs > 0 ? static_cast<int>((units + kPermWarps - 1) / kPermWarps) : 1;
     permute_small_kernel<<<grid, kPermThreads, smem, stream>>>(a, x_q, x_sf, H, x_perm, x_perm_sf, bt, nb);
     err = cudaGetLastError();
     if (err != cudaSuccess || x_perm == nullptr || copy) return err;

@@ -271,6 +271,15 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  // the biases first, in registers: their loads then overlap the partial-sum loads instead of
+  // waiting behind the optional logits stores
+  float gbias[PER], ebias[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = lane + 32 * j;
+    gbias[j] = (a.gate_bias && e < E) ? __ldg(a.gate_bias + e) : 0.f;
+    ebias[j] = (a.e_bias && e < E) ? __ldg(a.e_bias + e) : 0.f;
+  }
   for (int t = warp; t < T; t += 8) {
     float s[PER], key[PER];
     float lmax = -INFINITY;
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
 #pragma unroll
         for (int sp = 0; sp < kGemvSplit; ++sp) v[sp] = __ldcg(partial + (static_cast<size_t>(sp) * T + t) * E + e);
         l = (v[0] + v[1]) + (v[2] + v[3]);       // the order route_finish_kernel sums 4 splits in
-        if (a.gate_bias) l += a.gate_bias[e];
+        if (a.gate_bias) l += gbias[j];
         if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
       }
       s[j] = l;
@@ -312,7 +321,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
 #pragma unroll
     for (int j = 0; j < PER; ++j) {
       const int e = lane + 32 * j;
-      key[j] = (e < E) ? s[j] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
+      key[j] = (e < E) ? s[j] + (a.e_bias ? ebias[j] : 0.f) : -INFINITY;
     }
     float wsum = 0.f, wmine = 0.f;
     for (int k = 0; k < a.K; ++k) {
