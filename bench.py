@@ -61,6 +61,9 @@ def parse_args():
                    help="override E (smaller cases of the same kernels for profiler captures)")
     p.add_argument("--tokens", type=int, default=None,
                    help="override T (smaller cases of the same kernels for profiler captures)")
+    p.add_argument("--weights-in-l1", action="store_true",
+                   help="apply the routing weights in the L1 epilogue and sum without weights "
+                        "(moe_forward_l1_weighted) instead of weighting in the reduce")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
                         "BatchedExperts slots of max_tokens = the smallest power of two >= T (moe_forward_batched)")
@@ -273,7 +276,7 @@ def run_ours(args, w):
                               ws)
         else:
             M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out,
-                      ws)
+                      ws, weights_in_l1=args.weights_in_l1)
 
     def barrier():
         if W > 1:
@@ -431,6 +434,8 @@ def run_ours(args, w):
         cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
         cfg["parallelism"] = f"replicas x{W}"
         cfg["layout"] = f"BatchedExperts, max_tokens={S}" if batched else "expert-contiguous, padded to align"
+        cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
+                                  "stage calls)" if args.weights_in_l1 else "applied in the reduce")
         line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None,
@@ -446,6 +451,8 @@ def run_ours(args, w):
 
 def main():
     args = parse_args()
+    if args.weights_in_l1 and args.layout == "batched":
+        raise SystemExit("--weights-in-l1 applies to the expert-contiguous layout")
     w = synth.WORKLOADS[args.workload]
     if args.experts or args.tokens:
         import dataclasses

@@ -193,6 +193,18 @@ moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_pe
                                       uint8_t* h_q, uint8_t* h_sf, void* ws, size_t ws_bytes,
                                       void* stream);
 
+/* moe_grouped_gemm_l1_swiglu with the routing weight applied in the L1 epilogue (MegaMoE page
+ * 二、阶段 3: the SwiGLU output is silu(gate) * up * topk_weight, then amax -> UE8M0 -> E4M3):
+ *   h = (silu(gu[0:I]) * gu[I:2I]) * topk_w[sorted_token_ids[r]]   before the requant.
+ * sorted_token_ids [U] and topk_w [T*K] fp32 as produced by moe_permute / moe_route.  The reduce
+ * that follows then sums without weights (moe_unpermute_reduce with topk_w = NULL). */
+moe_status moe_grouped_gemm_l1_swiglu_weighted(const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                               const int32_t* expert_ids, const int32_t* m_sum,
+                                               const int32_t* sorted_token_ids, const float* topk_w,
+                                               int T, int K, int H, int I, int E, int align,
+                                               moe_weight w13, uint8_t* h_q, uint8_t* h_sf, void* ws,
+                                               size_t ws_bytes, void* stream);
+
 /* L2 grouped GEMM (MegaMoE page 二、阶段 4; L2 results are bf16, 阶段 5).
  * For every row r < M_sum with e = expert_ids[r] >= 0:
  *   y_perm[r] = bf16_rne( dequant(h_q[r]) @ dequant(W2[e])^T )   ([H], fp32 accumulate)
@@ -215,8 +227,9 @@ moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, cons
 
 /* Weighted unpermute-reduce (note §9.6 "gather 再讲一遍"; MegaMoE page 阶段 5):
  *   out[t] = bf16_rne( sum_{k=0}^{K-1} topk_w[t,k] * y_perm[inv_perm[t,k]] ), summed in fp32
- *   in k order.  y_perm [>= max(inv_perm)+1, H] bf16, inv_perm [T,K], topk_w [T,K] fp32,
- *   out [T, H] bf16. */
+ *   in k order.  y_perm [>= max(inv_perm)+1, H] bf16, inv_perm [T,K], topk_w [T,K] fp32 or NULL
+ *   (plain sum, for weights already applied in L1: MegaMoE page 阶段 5 accumulates the
+ *   contributions in float32 without weights), out [T, H] bf16. */
 moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
                                 const float* topk_w, int T, int K, int H, uint16_t* out,
                                 void* stream);
@@ -287,6 +300,18 @@ moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, cons
                                int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                                int32_t* m_sum, int32_t* expert_num_tokens, void* ws, size_t ws_bytes,
                                void* stream);
+
+/* moe_forward with the routing weights applied in the L1 epilogue instead of the reduce (MegaMoE
+ * page 二、阶段 3 and 阶段 5): L1 as moe_grouped_gemm_l1_swiglu_weighted, L2 as usual, and the
+ * reduce an unweighted fp32 sum.  Same arguments, workspace and index outputs as moe_forward; the
+ * output differs from moe_forward's only through the FP8 requant and bf16 roundings of the
+ * weighted intermediate values (identical when every routing weight is a power of two). */
+moe_status moe_forward_l1_weighted(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                   const float* e_score_bias, int T, int H, int I, int E, int K,
+                                   int align, moe_score_fn fn, int renormalize, moe_weight w13,
+                                   moe_weight w2, uint16_t* out, int32_t* topk_ids, float* topk_w,
+                                   int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                                   int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the device status word recorded in `ws` through
  * *device_status (MOE_OK if none) and clears it.  The return value reports host errors. */

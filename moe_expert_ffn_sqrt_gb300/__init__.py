@@ -82,6 +82,10 @@ def lib():
         L.moe_forward_batched.restype = S
         L.moe_forward_batched.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P,
                                           P, P, Z, P]
+        L.moe_grouped_gemm_l1_swiglu_weighted.restype = S
+        L.moe_grouped_gemm_l1_swiglu_weighted.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
+        L.moe_forward_l1_weighted.restype = S
+        L.moe_forward_l1_weighted.argtypes = L.moe_forward.argtypes
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.moe_status_str.restype = ctypes.c_char_p
@@ -252,6 +256,17 @@ def grouped_gemm_l1_swiglu(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, 
                                             _stream()), "moe_grouped_gemm_l1_swiglu")
 
 
+def grouped_gemm_l1_swiglu_weighted(x_perm, x_perm_sf, expert_ids, m_sum, sorted_token_ids, topk_w, T, K, H, I, E,
+                                    align, w13, h_q, h_sf, ws):
+    """L1 with the routing weight of each row's pair applied before the requant."""
+    _check(lib().moe_grouped_gemm_l1_swiglu_weighted(
+        _ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+        _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(topk_w, torch.float32, "topk_w"),
+        T, K, H, I, E, align, w13.c(), _ptr(h_q, torch.uint8, "h_q"), _ptr(h_sf, torch.uint8, "h_sf"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_gemm_l1_swiglu_weighted")
+
+
 def grouped_gemm_l2(h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, y_perm, ws):
     _check(lib().moe_grouped_gemm_l2(_ptr(h_q, torch.uint8, "h_q"), _ptr(h_sf, torch.uint8, "h_sf"),
                                      _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
@@ -269,6 +284,7 @@ def grouped_ffn(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13,
 
 
 def unpermute_reduce(y_perm, inv_perm, topk_w, out):
+    """topk_w None: plain sum (weights applied in L1)."""
     T, K = inv_perm.shape
     H = out.shape[1]
     _check(lib().moe_unpermute_reduce(_ptr(y_perm, torch.bfloat16, "y_perm"), _ptr(inv_perm, torch.int32, "inv_perm"),
@@ -277,10 +293,13 @@ def unpermute_reduce(y_perm, inv_perm, topk_w, out):
 
 
 def forward(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, renormalize, w13, w2, out, ws,
-            topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None):
+            topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None,
+            weights_in_l1=False):
+    """moe_forward, or moe_forward_l1_weighted when weights_in_l1 (routing weights applied in L1)."""
     T, H = hidden.shape
     E = w_gate.shape[0]
-    _check(lib().moe_forward(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+    fn = lib().moe_forward_l1_weighted if weights_in_l1 else lib().moe_forward
+    _check(fn(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
                              _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"),
                              T, H, I, E, K, align, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
                              _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"),

@@ -242,13 +242,15 @@ static GemmLaunch mx_launch(bool l1, const uint8_t* x, const uint8_t* x_sf, cons
 static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
-                              size_t ws_bytes, void* stream, const FusedReduce* red = nullptr, size_t rows = 0) {
+                              size_t ws_bytes, void* stream, const FusedReduce* red = nullptr, size_t rows = 0,
+                              const int32_t* row_ids = nullptr, const float* row_w = nullptr) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
   if (!(l1 ? weight_ok(w, E, 2 * I, H, 2) : weight_ok(w, E, H, I, 1))) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(x_sf, 16)) return MOE_ERR_INVALID_ARG;
   if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
   if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
+  if ((row_ids == nullptr) != (row_w == nullptr) || (!l1 && row_w)) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kAlign) return MOE_ERR_WORKSPACE;
   const size_t U = rows ? rows : moe_msum_upper(T, K, E, align);
   if (U == 0) return MOE_OK;
@@ -277,12 +279,16 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     N.U = static_cast<int>(U);
     N.align = align;
     if (red) N.red = *red;
+    N.row_ids = row_ids;
+    N.row_w = row_w;
     return cuda_status(launch_gemm_nv(N, l1, S(stream)));
   }
   const WsLayout Lw = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
   GemmLaunch L = mx_launch(l1, x, x_sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
   if (red) L.red = *red;
+  L.row_ids = row_ids;
+  L.row_w = row_w;
   uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + Lw.sched);
   return cuda_status(launch_gemm(L, l1, sched, S(stream)));
 }
@@ -293,6 +299,16 @@ moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_pe
                                       void* stream) {
   return gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, nullptr, ws,
                      ws_bytes, stream);
+}
+
+moe_status moe_grouped_gemm_l1_swiglu_weighted(const uint8_t* x_perm, const uint8_t* x_perm_sf,
+                                               const int32_t* expert_ids, const int32_t* m_sum,
+                                               const int32_t* sorted_token_ids, const float* topk_w, int T, int K,
+                                               int H, int I, int E, int align, moe_weight w13, uint8_t* h_q,
+                                               uint8_t* h_sf, void* ws, size_t ws_bytes, void* stream) {
+  if (!sorted_token_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  return gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, nullptr, ws,
+                     ws_bytes, stream, nullptr, 0, sorted_token_ids, topk_w);
 }
 
 moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const int32_t* expert_ids,
@@ -307,10 +323,11 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
 static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
                              const int32_t* m_sum, int T, int K, int H, int I, int E, int align, const moe_weight& w13,
                              const moe_weight& w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
-                             size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0) {
+                             size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0,
+                             const int32_t* row_ids = nullptr, const float* row_w = nullptr) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
-                                nullptr, ws, ws_bytes, stream, nullptr, rows);
+                                nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w);
     if (st != MOE_OK) return st;
     return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws,
                        ws_bytes, stream, red, rows);
@@ -325,7 +342,10 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   const WsLayout L = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (U == 0) return MOE_OK;
+  if ((row_ids == nullptr) != (row_w == nullptr)) return MOE_ERR_INVALID_ARG;
   GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
+  l1.row_ids = row_ids;
+  l1.row_w = row_w;
   GemmLaunch l2 = mx_launch(false, h_q, h_sf, expert_ids, m_sum, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
   if (red) l2.red = *red;
   uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.sched);
@@ -364,7 +384,7 @@ moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_
 moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int K,
                                 int H, uint16_t* out, void* stream) {
   if (T < 0 || K <= 0 || H <= 0 || H % 8) return MOE_ERR_INVALID_ARG;
-  if (!y_perm || !inv_perm || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+  if (!y_perm || !inv_perm || !out) return MOE_ERR_INVALID_ARG;   // topk_w NULL: plain sum
   if (!aligned(y_perm, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   return cuda_status(launch_unpermute_reduce(y_perm, inv_perm, topk_w, T, K, H, out, S(stream)));
 }
@@ -374,7 +394,7 @@ moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
 // slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
 static moe_status forward_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                                  const float* e_score_bias, int T, int H, int I, int E, int K, int align, int slot,
-                                 moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
+                                 bool l1w, moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
                                  uint16_t* out, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
                                  int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
                                  void* ws, size_t ws_bytes, void* stream) {
@@ -413,15 +433,15 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   if (fuse_reduce) {
     red.out = out;
     red.inv_perm = inv;
-    red.topk_w = tw;
+    red.topk_w = l1w ? nullptr : tw;
     red.sorted_ids = sorted;
     red.tickets = reinterpret_cast<uint32_t*>(b + L.tickets);
     red.K = K;
   }
   st = ffn_common(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y, ws, ws_bytes, stream,
-                  fuse_reduce ? &red : nullptr, U);
+                  fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr);
   if (st != MOE_OK || fuse_reduce) return st;
-  return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
+  return cuda_status(launch_unpermute_reduce(y, inv, l1w ? nullptr : tw, T, K, H, out, S(stream)));
 }
 
 extern "C" {
@@ -431,9 +451,19 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
                        int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
                        float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                        int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
-  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, fn, renormalize, w13, w2,
-                        out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws, ws_bytes,
-                        stream);
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, false, fn, renormalize, w13,
+                        w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws,
+                        ws_bytes, stream);
+}
+
+moe_status moe_forward_l1_weighted(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                   const float* e_score_bias, int T, int H, int I, int E, int K, int align,
+                                   moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
+                                   int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                                   int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, true, fn, renormalize, w13,
+                        w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws,
+                        ws_bytes, stream);
 }
 
 moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
@@ -445,7 +475,7 @@ moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, cons
   // a token's K experts are distinct, so no expert receives more than T tokens
   if (!slot_ok(max_tokens) || max_tokens < T) return MOE_ERR_INVALID_ARG;
   return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(max_tokens), max_tokens,
-                        fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        false, fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
                         expert_num_tokens, ws, ws_bytes, stream);
 }
 

@@ -291,7 +291,7 @@ constexpr uint32_t kDevErrCheck = 7;    // a kernel self-check (bounds / alignme
 struct FusedReduce {
   uint16_t* out;                 // [T, H] bf16; nullptr = not fused
   const int32_t* inv_perm;       // [T, K]
-  const float* topk_w;           // [T, K]
+  const float* topk_w;           // [T, K]; nullptr: plain sum (the weights were applied in L1)
   const int32_t* sorted_ids;     // [U]
   uint32_t* tickets;             // [T, n_col_tiles], zero between calls
   int K;
@@ -323,7 +323,7 @@ __device__ __forceinline__ void fused_reduce_tail(const FusedReduce& f, const ui
     float wk = 0.f;
     if (lane < f.K) {
       rk = __ldg(f.inv_perm + static_cast<size_t>(tt) * f.K + lane);
-      wk = __ldg(f.topk_w + static_cast<size_t>(tt) * f.K + lane);
+      wk = f.topk_w ? __ldg(f.topk_w + static_cast<size_t>(tt) * f.K + lane) : 1.f;
     }
     for (int cb = 0; cb < ncols; cb += 256) {
       const int c = c0 + cb + lane * 8;

@@ -94,6 +94,8 @@ struct GemmArgs {
   int fused;                    // both phases in one launch: L2 items wait for their block's L1 tiles
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
+  const int32_t* row_ids;       // L1: h of row r scaled by row_w[row_ids[r]] when row_w != nullptr
+  const float* row_w;
 };
 
 // Work items: the L1 tiles of the row blocks below m_sum, then their L2 tiles, each phase
@@ -406,6 +408,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row = r0 + m;
       const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
       const bool mine = row_e == e;
+      // the routing weight of this row's (token, slot) pair when it is applied in L1 (else 1)
+      const float wr = (it.phase == 0 && a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
       ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, kEpiThreads, ok);    // one vote over the eight epilogue warps
       if (!ok) {
@@ -415,30 +419,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       if (it.phase == 0) {
         const int I = a.ph[0].out_cols;
-        // h = silu(gate) * up for this thread's 64 of the tile's 128 columns, kept in registers so
-        // that the accumulator is released before the quantise-and-store part; the 128-wide amax
-        // combines both halves through shared memory
+        // This thread's 64 gate and 64 up values (of the tile's 128 columns) are read from TMEM in
+        // one round and the accumulator is released before h = silu(gate) * up is formed; the
+        // 128-wide amax combines both halves through shared memory
         float h[64];
         float amax = 0.f;
         if (warp_has_rows) {
+          uint32_t g[4][16], u[4][16];
+          const uint32_t col = static_cast<uint32_t>(half * 64);
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            uint32_t g[2][16], u[2][16];
-            const uint32_t col = static_cast<uint32_t>(half * 64 + c0);
-            tc_ld_x16(acc + col, g[0]);
-            tc_ld_x16(acc + col + 16, g[1]);
-            tc_ld_x16(acc + 128 + col, u[0]);
-            tc_ld_x16(acc + 128 + col + 16, u[1]);
-            tc_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              h[c0 + j] = silu_mul(__uint_as_float(g[j >> 4][j & 15]), __uint_as_float(u[j >> 4][j & 15]));
-              amax = fmaxf(amax, fabsf(h[c0 + j]));
-            }
+          for (int j = 0; j < 4; ++j) {
+            tc_ld_x16(acc + col + 16 * j, g[j]);
+            tc_ld_x16(acc + 128 + col + 16 * j, u[j]);
           }
+          tc_wait_ld();
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            h[j] = silu_mul(__uint_as_float(g[j >> 4][j & 15]), __uint_as_float(u[j >> 4][j & 15])) * wr;
+            amax = fmaxf(amax, fabsf(h[j]));
+          }
+        } else {
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(acc_empty));
         s_amax[half][m] = amax;
         named_barrier(1, kEpiThreads);
         if (warp_has_rows && mine) {
@@ -640,6 +645,10 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   a.fused = (l1 && l2) ? 1 : 0;
   a.one_expert_blocks = any.align % BN == 0;
   if (l2) a.red = l2->red;
+  if (l1) {
+    a.row_ids = l1->row_ids;
+    a.row_w = l1->row_w;
+  }
   const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
   int grid = num_sms();
   if (grid > total) grid = total;

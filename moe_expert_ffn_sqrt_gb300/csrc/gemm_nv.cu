@@ -65,6 +65,8 @@ struct NvArgs {
   int n_tiles;
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
+  const int32_t* row_ids;       // L1: h of row r scaled by row_w[row_ids[r]] when row_w != nullptr
+  const float* row_w;
 };
 
 // One pass of the pipeline: expert e against rows [rb*BN, (rb+nb)*BN), nb = 1 or 2 row blocks
@@ -402,6 +404,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
         const int row = (P.rb + j) * BN + m;
         const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == P.e;
         if (L1) {
+          const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
           // pass 1: amax of h over the 128 columns; pass 2: recompute h, quantise, store
           if (warp_has_rows) {
             float amax = 0.f;
@@ -416,7 +419,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i)
                 amax = fmaxf(amax, fabsf(silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
-                                                     __uint_as_float(u[i >> 4][i & 15]) * ts)));
+                                                     __uint_as_float(u[i >> 4][i & 15]) * ts) * wr));
             }
             const int ex = ue8m0_exponent(amax);
             const float sc = pow2_neg(ex);
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 4; ++v) {
                   const int c = 4 * i + v;
-                  h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts);
+                  h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts) * wr;
                 }
                 const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
                 const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
@@ -583,6 +586,8 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.h_sf = L.h_sf;
   a.y = L.y;
   a.red = L.red;
+  a.row_ids = L.row_ids;
+  a.row_w = L.row_w;
   a.status = L.status;
   const int pair = L1 ? 2 : 1;
   a.n_wt = pair == 2 ? L.w_rows / kNvTile : (L.w_rows + kNvTile - 1) / kNvTile;

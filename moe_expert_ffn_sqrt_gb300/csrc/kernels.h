@@ -48,6 +48,8 @@ struct GemmLaunch {
   uint32_t* status;
   int E, w_rows, Kd, I, U, align;
   FusedReduce red{};           // L2: fold the unpermute-reduce into the epilogue when red.out is set
+  const int32_t* row_ids = nullptr;   // L1 with row weights: h of row r is scaled by
+  const float* row_w = nullptr;       // row_w[row_ids[r]] (the routing weight of the row's pair)
 };
 int num_sms();
 int weight_tiles(int N, int pair);
@@ -74,6 +76,8 @@ struct NvLaunch {
   uint32_t* status;
   int E, w_rows, Kd, I, U, align;
   FusedReduce red{};
+  const int32_t* row_ids = nullptr;   // L1 row weights, as in GemmLaunch
+  const float* row_w = nullptr;
 };
 size_t packed_nv_weight_bytes(int E, int N, int Kd, int pair);
 cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,

@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(128) unpermute_reduce_kernel(const uint16_t* _
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int k = 0; k < K; ++k) {
     const int row = __ldg(inv_perm + static_cast<size_t>(t) * K + k);
-    const float w = __ldg(topk_w + static_cast<size_t>(t) * K + k);
+    const float w = topk_w ? __ldg(topk_w + static_cast<size_t>(t) * K + k) : 1.f;   // nullptr: plain sum
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(row) * H + c));
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

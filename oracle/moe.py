@@ -240,14 +240,18 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (1.0 + np.exp(-x))
 
 
-def expert_l1_swiglu(x_deq: np.ndarray, w13_deq: np.ndarray, I: int):
+def expert_l1_swiglu(x_deq: np.ndarray, w13_deq: np.ndarray, I: int, row_weight=None):
     """gate_up = x @ W13^T; gate = first I, up = last I; h = silu(gate) * up; FP8 requant per 128.
 
-    Returns (h float64 [R, I], h_q uint8 [R, I], h_sf uint8 [R, I/128]).
+    ``row_weight`` [R] (optional): each row's routing weight applied before the requant, the
+    placement of the MegaMoE page (二、阶段 3: silu(gate) * up * topk_weight, then amax -> UE8M0
+    -> E4M3).  Returns (h float64 [R, I], h_q uint8 [R, I], h_sf uint8 [R, I/128]).
     """
     gu = x_deq @ w13_deq.T
     g, u = gu[:, :I], gu[:, I:]
     h = silu(g) * u
+    if row_weight is not None:
+        h = h * np.asarray(row_weight, dtype=np.float64)[:, None]
     h_q, h_sf = quantize_fp8_groups(h, ACT_GROUP)
     return h, h_q, h_sf
 
@@ -258,13 +262,18 @@ def expert_l2(h_q: np.ndarray, h_sf: np.ndarray, w2_deq: np.ndarray) -> np.ndarr
     return round_bf16_rne(h @ w2_deq.T)
 
 
-def unpermute_reduce(y_rows_bits: np.ndarray, inv_perm: np.ndarray, topk_w: np.ndarray) -> np.ndarray:
-    """out[t] = bf16( sum_k topk_w[t,k] * y[inv_perm[t,k]] ), summed exactly in float64 (note §9.6)."""
+def unpermute_reduce(y_rows_bits: np.ndarray, inv_perm: np.ndarray, topk_w) -> np.ndarray:
+    """out[t] = bf16( sum_k topk_w[t,k] * y[inv_perm[t,k]] ), summed exactly in float64 (note §9.6).
+
+    ``topk_w`` None: the plain sum of the K rows (weights already applied in L1; MegaMoE page
+    阶段 5 accumulates the contributions without weights).
+    """
     y = bf16_to_f64(y_rows_bits)
     T, K = inv_perm.shape
     acc = np.zeros((T, y.shape[1]), dtype=np.float64)
     for k in range(K):
-        acc += np.asarray(topk_w[:, k], dtype=np.float64)[:, None] * y[inv_perm[:, k]]
+        wk = 1.0 if topk_w is None else np.asarray(topk_w[:, k], dtype=np.float64)[:, None]
+        acc += wk * y[inv_perm[:, k]]
     return round_bf16_rne(acc)
 
 
@@ -277,9 +286,11 @@ WeightProvider = Callable[[int], dict]
 
 def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
             score_fn: str, renormalize: bool = True, tokens=None,
-            topk_w_dtype=np.float64) -> Dict[str, object]:
+            topk_w_dtype=np.float64, weights_in_l1: bool = False) -> Dict[str, object]:
     """Route -> act quant -> permute -> per-expert L1+SwiGLU+requant -> L2 -> weighted reduce.
 
+    ``weights_in_l1``: apply each pair's routing weight to h before the requant (MegaMoE page
+    二、阶段 3) and sum the L2 rows without weights (阶段 5), instead of weighting in the reduce.
     ``tokens``: optional subset of token indices; only the (token, expert)
     rows those tokens need are computed and ``out``, ``x_q``, ``x_sf`` hold
     only their rows (in the order given).  Routing and the permute always run
@@ -311,7 +322,11 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
         I = w13.shape[0] // 2
         ts = sorted(set(t for t, _ in pairs))
         xd = dequant_fp8_groups(np.stack([x_q[t] for t in ts]), np.stack([x_sf[t] for t in ts]))
-        _, hq, hsf = expert_l1_swiglu(xd, w13, I)
+        rw = None
+        if weights_in_l1:                       # a token holds expert e in exactly one slot k
+            slot = {t: k for t, k in pairs}
+            rw = np.array([r["topk_w"][t, slot[t]] for t in ts]).astype(topk_w_dtype).astype(np.float64)
+        _, hq, hsf = expert_l1_swiglu(xd, w13, I, rw)
         y = expert_l2(hq, hsf, w2)
         for j, t in enumerate(ts):
             y_rows[(t, e)] = y[j]
@@ -321,7 +336,8 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
     for i, t in enumerate(tok):
         acc = np.zeros(H, dtype=np.float64)
         for k in range(K):
-            acc += wts[t, k] * bf16_to_f64(y_rows[(int(t), int(r["topk_ids"][t, k]))])
+            wk = 1.0 if weights_in_l1 else wts[t, k]
+            acc += wk * bf16_to_f64(y_rows[(int(t), int(r["topk_ids"][t, k]))])
         out[i] = round_bf16_rne(acc)
     return dict(route=r, x_q=q_rows, x_sf=sf_rows, perm=p, out=out, tokens=tok,
                 y_rows=y_rows, h_rows=h_rows)

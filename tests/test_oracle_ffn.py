@@ -163,3 +163,51 @@ def test_tiny_layer_output_is_sane():
     out = F.bf16_to_f64(res["out"])
     assert np.isfinite(out).all() and out.std() > 0
     assert res["perm"]["m_sum"] % w.align == 0
+
+
+def test_l1_weight_power_of_two_commutes_with_requant_and_l2():
+    # A power-of-two routing weight applied to h before the requant (MegaMoE page, 二、阶段 3) only
+    # shifts the UE8M0 exponent: the E4M3 codes stay, the L2 row is scaled exactly, and the plain sum
+    # of such rows equals the weighted sum of the unscaled ones, bit for bit.
+    rng = np.random.default_rng(21)
+    R, H, I = 5, 256, 256
+    x = F.bf16_to_f64(synth.bf16_rows(rng, R, H))
+    xq, xsf = moe.quantize_fp8_groups(x, 128)
+    xd = moe.dequant_fp8_groups(xq, xsf)
+    W13 = rng.normal(0, 0.05, (2 * I, H))
+    W2 = rng.normal(0, 0.05, (H, I))
+    w = np.array([1.0, 0.5, 0.25, 2.0, 0.125])
+    _, hq0, hsf0 = moe.expert_l1_swiglu(xd, W13, I)
+    _, hq1, hsf1 = moe.expert_l1_swiglu(xd, W13, I, w)
+    assert np.array_equal(hq1, hq0)
+    assert np.array_equal(hsf1.astype(int) - hsf0.astype(int), np.repeat(np.log2(w).astype(int)[:, None], I // 128, 1))
+    y0 = moe.expert_l2(hq0, hsf0, W2)
+    y1 = moe.expert_l2(hq1, hsf1, W2)
+    assert np.array_equal(F.bf16_to_f64(y1), w[:, None] * F.bf16_to_f64(y0))
+    inv = np.array([[0, 1], [2, 3], [4, 0]], dtype=np.int32)
+    tw = w[inv]
+    assert np.array_equal(moe.unpermute_reduce(y1, inv, None), moe.unpermute_reduce(y0, inv, tw))
+
+
+def test_l1_weight_general_differs_only_by_requant_rounding():
+    # general routing weights: the two placements agree to the FP8 requant error and no better
+    w = synth.WORKLOADS["tiny"]
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    a = moe.forward(inp, _weights_from_stack(stack), w.fmt, w.K, w.align, w.score_fn)
+    b = moe.forward(inp, _weights_from_stack(stack), w.fmt, w.K, w.align, w.score_fn, weights_in_l1=True)
+    assert np.array_equal(a["route"]["topk_ids"], b["route"]["topk_ids"])
+    oa, ob = F.bf16_to_f64(a["out"]), F.bf16_to_f64(b["out"])
+    rms = np.sqrt(np.mean(oa * oa))
+    # two independent E4M3 roundings of h (up to 2^-4 relative each) leave noise of a few percent of
+    # the output's RMS; a weight dropped or applied twice moves it by tens of percent or more
+    assert np.sqrt(np.mean((oa - ob) ** 2)) <= 0.08 * rms
+    assert np.abs(oa - ob).max() <= 0.4 * rms
+    assert not np.array_equal(a["out"], b["out"])       # the weights did move into L1
+    # every y row of the L1 placement is its pair's weight times the reduce placement's row, up to
+    # the same requant noise
+    for (t, e), y_b in b["y_rows"].items():
+        k = int(np.nonzero(a["route"]["topk_ids"][t] == e)[0][0])
+        ya = a["route"]["topk_w"][t, k] * F.bf16_to_f64(a["y_rows"][(t, e)])
+        yb = F.bf16_to_f64(y_b)
+        assert np.sqrt(np.mean((yb - ya) ** 2)) <= 0.1 * np.sqrt(np.mean(ya * ya))
