@@ -34,10 +34,12 @@ FALLBACK_BF16_TFLOPS = 1900.0
 SPIN_CYCLES = 1_000_000      # ~0.5 ms at 2 GHz, outside the timed events
 
 
-def launches_per_forward(w):
+def launches_per_forward(w, naive=False):
     """Kernel launches of one moe_forward, mirroring the library's dispatch."""
     route = 1 if w.T <= 16 else 2                 # fused small-batch route, else gate GEMM + top-K
     permute = 1 if w.T * w.K <= 128 else 2        # permute with the row copy in the same launch, else + copy
+    if naive:
+        permute = 0                               # the routing launch writes the tiny-batch layout
     if w.fmt == "mxfp4":
         ffn = 1                                   # L1 and L2 in one cooperative launch
     else:
@@ -64,9 +66,10 @@ def parse_args():
     p.add_argument("--weights-in-l1", action="store_true",
                    help="apply the routing weights in the L1 epilogue and sum without weights "
                         "(moe_forward_l1_weighted) instead of weighting in the reduce")
-    p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched"],
+    p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
-                        "BatchedExperts slots of max_tokens = the smallest power of two >= T (moe_forward_batched)")
+                        "BatchedExperts slots of max_tokens = the smallest power of two >= T (moe_forward_batched) or "
+                        "the tiny-batch layout, one 16-row block per (token, expert) pair, no sort (moe_forward_naive)")
     return p.parse_args()
 
 
@@ -261,17 +264,20 @@ def run_ours(args, w):
     gate_bias = None if inp["gate_bias"] is None else d(inp["gate_bias"])
     e_bias = None if inp["e_score_bias"] is None else d(inp["e_score_bias"])
     batched = args.layout == "batched"
+    naive = args.layout == "naive"
     S = 1 << max(0, (T - 1).bit_length())         # BatchedExperts slot: smallest power of two >= T
     if batched:
         ws = M.new_workspace_batched(T, w.H, w.I, w.E, w.K, S, device=dev)
     else:
-        ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align, device=dev)
+        ws = M.new_workspace(T, w.H, w.I, w.E, w.K, M.NAIVE_ROWS if naive else w.align, device=dev)
     out = torch.empty(T, w.H, dtype=torch.bfloat16, device=dev)
     out_host = torch.empty(T, w.H, dtype=torch.bfloat16).pin_memory()
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)     # > L2 (126 MB)
 
     def step():
-        if batched:
+        if naive:
+            M.forward_naive(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.score_fn, w.renormalize, w13, w2, out, ws)
+        elif batched:
             M.forward_batched(hidden, w_gate, gate_bias, e_bias, w.I, w.K, S, w.score_fn, w.renormalize, w13, w2, out,
                               ws)
         else:
@@ -315,8 +321,8 @@ def run_ours(args, w):
     value = W * T / (ms / 1e3)
 
     # ---- per-kernel durations: the same path called stage by stage with events in between
-    align = M.batched_align(S) if batched else w.align
-    U = w.E * S if batched else M.msum_upper(T, w.K, w.E, w.align)
+    align = M.batched_align(S) if batched else (M.NAIVE_ROWS if naive else w.align)
+    U = w.E * S if batched else M.msum_upper(T, w.K, w.E, align)
     ids = torch.empty(T, w.K, dtype=torch.int32, device=dev)
     tw = torch.empty(T, w.K, dtype=torch.float32, device=dev)
     xq = torch.empty(T, w.H, dtype=torch.uint8, device=dev)
@@ -334,8 +340,11 @@ def run_ours(args, w):
     # MXFP4: the expert FFN is one launch (moe_grouped_ffn), timed as one stage; NVFP4: L1 and L2 apart
     # (BatchedExperts: the whole FFN through moe_grouped_ffn_batched, whose row-map kernel from the
     # per-expert counts is counted in the stage; moe_forward_batched takes the row map from the permute)
+    # (tiny-batch layout: routing and layout are one stage, moe_route_naive)
     fused = w.fmt == "mxfp4" or batched
     stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
+    if naive:
+        stages.remove("permute")
     sev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
     barrier()
     for i in range(K):
@@ -346,26 +355,33 @@ def run_ours(args, w):
         e = sev[i]
         j = 0
         e[j].record()
-        M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
+        if naive:
+            M.route_naive(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, srt, eids, inv,
+                          msum, xp, xpsf, ws)
+        else:
+            M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
         j += 1
         e[j].record()
-        if batched:
+        if naive:
+            pass
+        elif batched:
             M.permute_batched(ids, w.E, S, srt, eids, inv, msum, ws, expert_num_tokens=cnt, x_q=xq, x_sf=xsf,
                               x_perm=xp, x_perm_sf=xpsf)
         else:
             M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
                       x_perm_sf=xpsf)
-        j += 1
-        e[j].record()
+        if not naive:
+            j += 1
+            e[j].record()
         if batched:
             M.grouped_ffn_batched(xp, xpsf, cnt, T, w.K, w.H, w.I, w.E, S, w13, w2, hq, hsf, y, ws)
         elif fused:
-            M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, w2, hq, hsf, y, ws)
+            M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, w2, hq, hsf, y, ws)
         else:
-            M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w13, hq, hsf, ws)
+            M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws)
             j += 1
             e[j].record()
-            M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, w.align, w2, y, ws)
+            M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w2, y, ws)
         j += 1
         e[j].record()
         M.unpermute_reduce(y, inv, tw, out)
@@ -373,7 +389,10 @@ def run_ours(args, w):
         e[j].record()
     barrier()
     stage_ms = {s: statistics.mean(sev[i][j].elapsed_time(sev[i][j + 1]) for i in range(K)) for j, s in enumerate(stages)}
-    n_touched = int((cnt.cpu() > 0).sum().item())
+    if naive:     # no per-expert counts in this layout: count the distinct experts of the routing
+        n_touched = int(torch.unique(ids).numel())
+    else:
+        n_touched = int((cnt.cpu() > 0).sum().item())
     ab = algorithmic_bytes(w, n_touched)
     hbm, bf16, peak_src = peaks()
     top = "ffn" if fused else max(("l1", "l2"), key=lambda s: stage_ms[s])
@@ -433,7 +452,9 @@ def run_ours(args, w):
         cfg = workload_config(w)
         cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
         cfg["parallelism"] = f"replicas x{W}"
-        cfg["layout"] = f"BatchedExperts, max_tokens={S}" if batched else "expert-contiguous, padded to align"
+        cfg["layout"] = (f"BatchedExperts, max_tokens={S}" if batched else
+                         "tiny-batch, one 16-row block per (token, expert) pair" if naive else
+                         "expert-contiguous, padded to align")
         cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
                                   "stage calls)" if args.weights_in_l1 else "applied in the reduce")
         line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
@@ -442,7 +463,7 @@ def run_ours(args, w):
                 "dtype": "fp8xfp4 (fp32 accumulate)" if w.fmt == "mxfp4" else "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
                 "data": "synthetic (seeded)",
                 "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_forward(w) * K, "clocks": clk}
+                "gpu_launches": launches_per_forward(w, naive) * K, "clocks": clk}
         print(json.dumps(line), flush=True)
     if W > 1:
         torch.distributed.destroy_process_group()
@@ -451,7 +472,7 @@ def run_ours(args, w):
 
 def main():
     args = parse_args()
-    if args.weights_in_l1 and args.layout == "batched":
+    if args.weights_in_l1 and args.layout != "contiguous":
         raise SystemExit("--weights-in-l1 applies to the expert-contiguous layout")
     w = synth.WORKLOADS[args.workload]
     if args.experts or args.tokens:

@@ -313,6 +313,43 @@ moe_status moe_forward_l1_weighted(const uint16_t* hidden, const float* w_gate, 
                                    int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                                    int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* --------------------------------------------------------------------------------------
+ * Tiny-batch path (MegaMoE page, the permute-path table 何时选择什么: with very few tokens,
+ * T * topk * 4 <= E, even sorted_token_ids is skipped and each (token, expert) pair is given its
+ * own block).  Pair p = t*K + k owns row 16 * p of the permuted buffers; the other 15 rows of its
+ * block, and the rows [16 * T * K, U) with U = moe_msum_upper(T, K, E, 16), are padding.  No
+ * counting or sorting: the routing launch itself writes the activation rows (each token's FP8
+ * row K times) and the index arrays, and the expert GEMMs then run with align = 16, one pair
+ * per row block.  Requires T <= 16 and T * K <= E (else MOE_ERR_UNSUPPORTED); meant for
+ * T * K * 4 <= E, where two pairs rarely share an expert (a shared expert's weights are read once
+ * per pair).
+ * ------------------------------------------------------------------------------------ */
+
+/* Routing (as moe_route) plus the tiny-batch layout:
+ *   sorted_token_ids [U] out: p on row 16p, T*K elsewhere
+ *   expert_ids [U] out: topk_ids[p] on row 16p, -1 elsewhere
+ *   inv_perm [T, K] out: 16 * (t*K + k);  m_sum [1] out: 16 * T * K
+ *   x_perm [U, H] E4M3 out (row 16p = x_q[t], other rows unwritten), x_perm_sf out, tiled for
+ *   align 16 (rows U, slabs H/128).
+ * ws as for moe_route.  The index arrays and buffers feed moe_grouped_ffn / the grouped GEMMs
+ * with align = 16 and the same T, K, E. */
+moe_status moe_route_naive(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                           const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
+                           int renormalize, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
+                           int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, uint8_t* x_perm,
+                           uint8_t* x_perm_sf, void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward over the tiny-batch layout: two launches (routing with the layout, then L1 + L2
+ * with the weighted reduce in the L2 epilogue).  ws: moe_workspace_size(T, H, I, E, K, 16)
+ * bytes.  `out` equals moe_forward's (align 16) bit for bit; the optional index outputs are
+ * those of moe_route_naive. */
+moe_status moe_forward_naive(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                             const float* e_score_bias, int T, int H, int I, int E, int K,
+                             moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2,
+                             uint16_t* out, int32_t* topk_ids, float* topk_w,
+                             int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                             int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, returns the device status word recorded in `ws` through
  * *device_status (MOE_OK if none) and clears it.  The return value reports host errors. */
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status);

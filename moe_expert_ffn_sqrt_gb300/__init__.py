@@ -86,6 +86,11 @@ def lib():
         L.moe_grouped_gemm_l1_swiglu_weighted.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
         L.moe_forward_l1_weighted.restype = S
         L.moe_forward_l1_weighted.argtypes = L.moe_forward.argtypes
+        L.moe_route_naive.restype = S
+        L.moe_route_naive.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, Z, P]
+        L.moe_forward_naive.restype = S
+        L.moe_forward_naive.argtypes = [P, P, P, P, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P,
+                                        Z, P]
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.moe_status_str.restype = ctypes.c_char_p
@@ -365,6 +370,41 @@ def forward_batched(hidden, w_gate, gate_bias, e_score_bias, I, K, max_tokens, s
         _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"),
         _ptr(expert_num_tokens, torch.int32, "expert_num_tokens"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
         _stream()), "moe_forward_batched")
+
+
+# ------------------------------------------------------------------ tiny-batch layout
+
+NAIVE_ROWS = 16      # rows per (token, expert) pair; the GEMMs run with align = NAIVE_ROWS
+
+
+def route_naive(hidden, w_gate, gate_bias, e_score_bias, K, score_fn, renormalize, topk_ids, topk_w,
+                sorted_token_ids, expert_ids, inv_perm, m_sum, x_perm, x_perm_sf, ws):
+    """Routing plus the tiny-batch layout (pair p on row 16p of the permuted buffers)."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_route_naive(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"), T, H, E, K,
+        SCORE_FNS.get(score_fn, score_fn), int(renormalize), _ptr(topk_ids, torch.int32, "topk_ids"),
+        _ptr(topk_w, torch.float32, "topk_w"), _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+        _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
+        _ptr(m_sum, torch.int32, "m_sum"), _ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_route_naive")
+
+
+def forward_naive(hidden, w_gate, gate_bias, e_score_bias, I, K, score_fn, renormalize, w13, w2, out, ws,
+                  topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None):
+    """moe_forward over the tiny-batch layout (T <= 16, T*K <= E); ws sized for align 16."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_forward_naive(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"),
+        T, H, I, E, K, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
+        _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"),
+        ws.numel(), _stream()), "moe_forward_naive")
 
 
 def get_error(ws):

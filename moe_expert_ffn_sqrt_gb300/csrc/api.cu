@@ -170,6 +170,52 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
 
 }  // extern "C"
 
+// Routing plus the tiny-batch layout in one launch: pair p = t*K + k owns row kNaiveRows * p of
+// [U, H] buffers with U = moe_msum_upper(T, K, E, kNaiveRows) (T*K <= E makes T*K*kNaiveRows fit).
+static moe_status route_naive_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                     const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
+                                     int renormalize, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
+                                     int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, uint8_t* x_perm,
+                                     uint8_t* x_perm_sf, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, 128, E, K, kNaiveRows) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (T > 16 || T * K > E) return MOE_ERR_UNSUPPORTED;
+  if (!hidden || !w_gate || !topk_ids || !topk_w || !sorted_token_ids || !expert_ids || !inv_perm || !m_sum ||
+      !x_perm || !x_perm_sf)
+    return MOE_ERR_INVALID_ARG;
+  if (fn != MOE_SCORE_SOFTMAX && fn != MOE_SCORE_SQRT_SOFTPLUS) return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_gate, 16) || !aligned(x_perm, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const size_t poff = up(kAlign + permute_scratch_bytes(T, K, E));   // as in layout()
+  if (ws_bytes < poff + route_scratch_bytes(T, H, E)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  NaiveLayout nv;
+  nv.sorted = sorted_token_ids;
+  nv.eids = expert_ids;
+  nv.inv = inv_perm;
+  nv.m_sum = m_sum;
+  nv.xp = x_perm;
+  nv.xp_sf = x_perm_sf;
+  nv.U = static_cast<int>(moe_msum_upper(T, K, E, kNaiveRows));
+  nv.sf_nb = act_sf_blocks(nv.U, kNaiveRows);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + poff);
+  return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
+                                  renormalize, nullptr, topk_ids, topk_w, nullptr, nullptr, partial, status_of(ws),
+                                  S(stream), &nv));
+}
+
+extern "C" {
+
+moe_status moe_route_naive(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                           const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn, int renormalize,
+                           int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                           int32_t* inv_perm, int32_t* m_sum, uint8_t* x_perm, uint8_t* x_perm_sf, void* ws,
+                           size_t ws_bytes, void* stream) {
+  return route_naive_common(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, topk_ids, topk_w,
+                            sorted_token_ids, expert_ids, inv_perm, m_sum, x_perm, x_perm_sf, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
 // slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
 static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, int align, int slot,
                                  int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum,
@@ -394,7 +440,7 @@ moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
 // slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
 static moe_status forward_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                                  const float* e_score_bias, int T, int H, int I, int E, int K, int align, int slot,
-                                 bool l1w, moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
+                                 bool l1w, bool naive, moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
                                  uint16_t* out, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
                                  int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
                                  void* ws, size_t ws_bytes, void* stream) {
@@ -422,12 +468,19 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   uint8_t* hq = reinterpret_cast<uint8_t*>(b + L.h_q);
   uint8_t* hsf = reinterpret_cast<uint8_t*>(b + L.h_sf);
   uint16_t* y = reinterpret_cast<uint16_t*>(b + L.y);
-  moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
-                            xq, xsf, ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, expert_counts, xq, xsf, H, xp, xpsf, ws,
-                      ws_bytes, stream);
-  if (st != MOE_OK) return st;
+  moe_status st;
+  if (naive) {
+    st = route_naive_common(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, ids, tw, sorted,
+                            eids, inv, ms, xp, xpsf, ws, ws_bytes, stream);
+    if (st != MOE_OK) return st;
+  } else {
+    st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw, xq, xsf, ws,
+                   ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, expert_counts, xq, xsf, H, xp, xpsf, ws,
+                        ws_bytes, stream);
+    if (st != MOE_OK) return st;
+  }
   const bool fuse_reduce = T <= kFusedReduceMaxTokens;
   FusedReduce red{};
   if (fuse_reduce) {
@@ -451,9 +504,20 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
                        int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
                        float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                        int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
-  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, false, fn, renormalize, w13,
-                        w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws,
-                        ws_bytes, stream);
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, false, false, fn,
+                        renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        nullptr, ws, ws_bytes, stream);
+}
+
+moe_status moe_forward_naive(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                             const float* e_score_bias, int T, int H, int I, int E, int K, moe_score_fn fn,
+                             int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
+                             float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                             int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  if (T > 16 || T * K > E) return MOE_ERR_UNSUPPORTED;
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, kNaiveRows, 0, false, true, fn,
+                        renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        nullptr, ws, ws_bytes, stream);
 }
 
 moe_status moe_forward_l1_weighted(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
@@ -461,9 +525,9 @@ moe_status moe_forward_l1_weighted(const uint16_t* hidden, const float* w_gate, 
                                    moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
                                    int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
                                    int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
-  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, true, fn, renormalize, w13,
-                        w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws,
-                        ws_bytes, stream);
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, true, false, fn,
+                        renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        nullptr, ws, ws_bytes, stream);
 }
 
 moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
@@ -475,7 +539,7 @@ moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, cons
   // a token's K experts are distinct, so no expert receives more than T tokens
   if (!slot_ok(max_tokens) || max_tokens < T) return MOE_ERR_INVALID_ARG;
   return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(max_tokens), max_tokens,
-                        false, fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
+                        false, false, fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
                         expert_num_tokens, ws, ws_bytes, stream);
 }
 

@@ -147,6 +147,12 @@ __device__ __forceinline__ bool find_expert(const GemmArgs& a, int n0, int msum,
   return true;
 }
 
+// Two floats -> bf16 (round to nearest even) packed low | high << 16, one conversion instruction.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // silu(g) * u with the fast exponential and division intrinsics: the result is requantised to
 // E4M3 (3 mantissa bits), far coarser than their few-ulp error, and unlike the IEEE division they
 // have no slow path for the infinities that unused accumulator rows may hold.
@@ -480,35 +486,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       } else {
         const int H = a.ph[1].out_cols;
         const int ncols = min(kTileRows, H - wt * kTileRows) - half * (kTileRows / 2);   // this half's columns
-        // 128 outputs in two rounds of 64: each round is converted to bf16 and stored right away;
-        // the accumulator is released after the last round's loads
+        // 128 outputs in two rounds of 64 columns: round 0 is packed to bf16 pairs while round 1's
+        // TMEM loads are issued; the accumulator is released once round 1 has landed, and both
+        // rounds are stored after that
         if (warp_has_rows) {
           uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * H + wt * kTileRows +
                                                 half * (kTileRows / 2));
+          const uint32_t col = static_cast<uint32_t>(half * (kTileRows / 2));
+          uint32_t v[4][16];
+          uint32_t p0[32];
 #pragma unroll
-          for (int c0 = 0; c0 < kTileRows / 2; c0 += 64) {
-            uint32_t v[4][16];
-            const uint32_t col = static_cast<uint32_t>(half * (kTileRows / 2) + c0);
+          for (int j = 0; j < 4; ++j) tc_ld_x16(acc + col + 16 * j, v[j]);
+          tc_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tc_ld_x16(acc + col + 16 * j, v[j]);
-            tc_wait_ld();
-            if (c0 + 64 >= kTileRows / 2) {
-              tc_fence_before();
-              mbar_arrive(smem_u32(acc_empty));
-            }
-            uint32_t packed[32];
+          for (int j = 0; j < 32; ++j) p0[j] = pack_bf16x2(__uint_as_float(v[j >> 3][(2 * j) & 15]),
+                                                            __uint_as_float(v[j >> 3][(2 * j + 1) & 15]));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j) & 15])));
-              const uint32_t hi =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j >> 3][(2 * j + 1) & 15])));
-              packed[j] = lo | (hi << 16);
-            }
-            if (mine) {
+          for (int j = 0; j < 4; ++j) tc_ld_x16(acc + col + 64 + 16 * j, v[j]);
+          tc_wait_ld();
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+          if (mine) {
 #pragma unroll
-              for (int c = 0; c < 8; ++c)
-                if (c0 + c * 8 < ncols)
-                  dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            for (int c = 0; c < 8; ++c)
+              if (c * 8 < ncols) dst[c] = make_uint4(p0[4 * c], p0[4 * c + 1], p0[4 * c + 2], p0[4 * c + 3]);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              if (64 + c * 8 < ncols) {
+                uint32_t q4[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int j = 4 * c + i;
+                  q4[i] = pack_bf16x2(__uint_as_float(v[j >> 3][(2 * j) & 15]),
+                                      __uint_as_float(v[j >> 3][(2 * j + 1) & 15]));
+                }
+                dst[8 + c] = make_uint4(q4[0], q4[1], q4[2], q4[3]);
+              }
             }
           }
         } else {

@@ -11,10 +11,23 @@ namespace moe {
 // route.cu
 int route_nsplit(int T, int H, int E);
 size_t route_scratch_bytes(int T, int H, int E);   // partial sums + ticket slot
+// Tiny-batch layout (no sort): pair p = t*K + k owns row kNaiveRows * p of the permuted buffers,
+// the other rows of its block and the rows [kNaiveRows * T * K, U) are padding.  Written by the
+// small-batch routing launch (T <= 16).
+constexpr int kNaiveRows = 16;
+struct NaiveLayout {
+  int32_t* sorted = nullptr;   // [U]
+  int32_t* eids = nullptr;     // [U]
+  int32_t* inv = nullptr;      // [T*K]
+  int32_t* m_sum = nullptr;    // [1]
+  uint8_t* xp = nullptr;       // [U, H] E4M3
+  uint8_t* xp_sf = nullptr;    // tiled (block rows kNaiveRows, rows U, slabs H/128)
+  int U = 0, sf_nb = 0;
+};
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         uint32_t* status, cudaStream_t stream);
+                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv = nullptr);
 
 // permute.cu
 size_t permute_smem_bytes(int E);

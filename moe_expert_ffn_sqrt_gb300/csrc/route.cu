@@ -36,6 +36,7 @@ struct RouteFinishArgs {
   uint8_t* x_q;
   uint8_t* x_sf;
   int topk_blocks;   // blocks [0, topk_blocks) do top-K
+  NaiveLayout nv;    // small batches: the tiny-batch layout written by the same launch (nv.eids null: off)
 };
 
 __device__ __forceinline__ void warp_argmax(float& key, int& id) {
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
     }
   }
   // 2. FP8 activation quantisation of this CTA's share of the 128-column groups
-  if (a.x_q) {
+  if (a.x_q || a.nv.xp) {
     const int gpt = H / 128;
     for (long long gidx = static_cast<long long>(bid) * 8 + warp; gidx < static_cast<long long>(T) * gpt;
          gidx += static_cast<long long>(nblocks) * 8) {
@@ -260,11 +261,33 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
           __nv_cvt_float2_to_fp8x2(make_float2(v[0] * sc, v[1] * sc), __NV_SATFINITE, __NV_E4M3);
       const __nv_fp8x2_storage_t hi =
           __nv_cvt_float2_to_fp8x2(make_float2(v[2] * sc, v[3] * sc), __NV_SATFINITE, __NV_E4M3);
-      *reinterpret_cast<uint32_t*>(a.x_q + base) = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-      if (lane == 0) a.x_sf[static_cast<size_t>(t) * gpt + g] = static_cast<uint8_t>(ex + 127);
+      const uint32_t packed = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      if (a.x_q) {
+        *reinterpret_cast<uint32_t*>(a.x_q + base) = packed;
+        if (lane == 0) a.x_sf[static_cast<size_t>(t) * gpt + g] = static_cast<uint8_t>(ex + 127);
+      }
+      if (a.nv.xp) {                               // the token's row of each of its K pairs
+        for (int k = 0; k < a.K; ++k) {
+          const int r = (t * a.K + k) * kNaiveRows;
+          *reinterpret_cast<uint32_t*>(a.nv.xp + static_cast<size_t>(r) * H + g * 128 + lane * 4) = packed;
+          if (lane == 0) a.nv.xp_sf[act_sf_offset(kNaiveRows, a.nv.sf_nb, r, g)] = static_cast<uint8_t>(ex + 127);
+        }
+      }
     }
   }
-  // 3. the last CTA to finish does the top-K
+  // 3. tiny-batch layout: every entry that does not depend on the routing (pair p owns row
+  //    kNaiveRows * p; the other rows of its block and the rows up to U are padding)
+  if (a.nv.eids) {
+    const int npairs = T * a.K;
+    for (int r = bid * 256 + threadIdx.x; r < a.nv.U; r += nblocks * 256) {
+      const bool real = r % kNaiveRows == 0 && r / kNaiveRows < npairs;
+      a.nv.sorted[r] = real ? r / kNaiveRows : npairs;
+      if (!real) a.nv.eids[r] = -1;                // real rows: the top-K below
+      if (r < npairs) a.nv.inv[r] = r * kNaiveRows;
+    }
+    if (bid == 0 && threadIdx.x == 0) *a.nv.m_sum = npairs * kNaiveRows;
+  }
+  // 4. the last CTA to finish does the top-K
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == static_cast<uint32_t>(nblocks - 1));
@@ -346,7 +369,10 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
       sw = __shfl_sync(0xffffffffu, sw, bi & 31);
       wsum += sw;
       if (lane == k) wmine = sw;
-      if (lane == 0) a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
+      if (lane == 0) {
+        a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
+        if (a.nv.eids) a.nv.eids[(t * a.K + k) * kNaiveRows] = bi;
+      }
     }
     if (lane < a.K) a.topk_w[static_cast<size_t>(t) * a.K + lane] = a.renormalize ? wmine / wsum : wmine;
   }
@@ -381,7 +407,7 @@ static void launch_route_small(const RouteFinishArgs& a, const float* w_gate, fl
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         uint32_t* status, cudaStream_t stream) {
+                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv) {
   const int ns = route_nsplit(T, H, E);
   RouteFinishArgs a;
   a.partial = partial;
@@ -401,6 +427,11 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
   a.x_q = x_q;
   a.x_sf = x_sf;
   a.topk_blocks = T;
+  a.nv = NaiveLayout{};
+  if (nv) {
+    if (T > kGemvT) return cudaErrorInvalidValue;
+    a.nv = *nv;
+  }
   if (T <= kGemvT) {
     uint32_t* ticket = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(partial) + route_scratch_bytes(T, H, E) - 256);
     if (T <= 8) launch_route_small<8>(a, w_gate, partial, ticket, stream);

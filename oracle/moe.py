@@ -233,6 +233,31 @@ def permute_batched(topk_ids: np.ndarray, E: int, max_tokens: int) -> Dict[str, 
                 expert_num_tokens=counts)
 
 
+def permute_naive(topk_ids: np.ndarray, E: int, rows_per_pair: int = 16) -> Dict[str, np.ndarray]:
+    """Tiny-batch layout without sorting (MegaMoE page, the permute-path table 何时选择什么: when
+    T * topk * 4 <= E even sorted_token_ids is skipped and each pair is assigned its own block).
+
+    Pair p = t*K + k owns row rows_per_pair * p; every other row up to U = T*K + E*(rows_per_pair-1)
+    (the contiguous layout's bound for align = rows_per_pair) is padding.
+    """
+    T, K = topk_ids.shape
+    ids = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    n = T * K
+    U = n + E * (rows_per_pair - 1)
+    if n * rows_per_pair > U:
+        raise ValueError("the tiny-batch layout needs T*K <= E")
+    sorted_ids = np.full(U, n, dtype=np.int32)
+    expert_ids = np.full(U, -1, dtype=np.int32)
+    inv = np.zeros(n, dtype=np.int32)
+    for p in range(n):
+        r = rows_per_pair * p
+        sorted_ids[r] = p
+        expert_ids[r] = ids[p]
+        inv[p] = r
+    return dict(sorted_token_ids=sorted_ids, expert_ids=expert_ids, inv_perm=inv.reshape(T, K),
+                m_sum=rows_per_pair * n, U=U)
+
+
 # ----------------------------------------------------------------------------
 # Expert SwiGLU FFN (MegaMoE page, 第三步 and 二、阶段 2-4)
 

@@ -2,6 +2,7 @@
 import numpy as np
 import pytest
 
+import synth
 from oracle import moe
 from conftest import load_golden
 
@@ -137,3 +138,39 @@ def test_batched_rejects_an_overfull_slot():
     ids = np.array([[0, 1], [0, 2], [0, 1]], dtype=np.int32)     # expert 0 receives 3 tokens
     with pytest.raises(ValueError):
         moe.permute_batched(ids, 3, 2)
+
+
+def test_naive_layout_by_hand():
+    # token 0 picks experts 5 then 2 (K = 2, E = 8): pair 0 on row 0, pair 1 on row 16
+    p = moe.permute_naive(np.array([[5, 2]]), 8)
+    assert p["U"] == 2 + 8 * 15 and p["m_sum"] == 32
+    assert p["inv_perm"].tolist() == [[0, 16]]
+    assert p["expert_ids"][0] == 5 and p["expert_ids"][16] == 2
+    assert (np.delete(p["expert_ids"], [0, 16]) == -1).all()
+    assert p["sorted_token_ids"][0] == 0 and p["sorted_token_ids"][16] == 1
+    assert (np.delete(p["sorted_token_ids"], [0, 16]) == 2).all()
+
+
+@pytest.mark.parametrize("T,K,E", [(1, 6, 256), (4, 4, 16), (8, 6, 256), (3, 1, 3)])
+def test_naive_layout_holds_the_same_pairs_as_the_contiguous_one(T, K, E):
+    rng = np.random.default_rng(T * 7 + E)
+    ids = synth.topk_ids_random(rng, T, E, K, 0.5)
+    a = moe.permute_naive(ids, E)
+    c = moe.permute(ids, E, 16)
+    assert a["U"] == c["U"]                       # fits the contiguous layout's buffers (align 16)
+    inv = a["inv_perm"].reshape(-1)
+    assert np.array_equal(a["sorted_token_ids"][inv], np.arange(T * K))
+    assert np.array_equal(a["expert_ids"][inv], ids.reshape(-1))
+    assert (inv % 16 == 0).all() and len(set((inv // 16).tolist())) == T * K    # one pair per 16-row block
+    real = a["expert_ids"] >= 0
+    assert real.sum() == T * K and (a["sorted_token_ids"][~real] == T * K).all()
+    # the same (token, expert) rows as the sorted layout, in another order
+    pairs_a = sorted(zip(a["sorted_token_ids"][real] // K, a["expert_ids"][real]))
+    rc = c["expert_ids"] >= 0
+    pairs_c = sorted(zip(c["sorted_token_ids"][rc] // K, c["expert_ids"][rc]))
+    assert pairs_a == pairs_c
+
+
+def test_naive_layout_rejects_too_many_pairs():
+    with pytest.raises(ValueError):
+        moe.permute_naive(np.zeros((5, 4), dtype=np.int32) + np.arange(4), 16)
