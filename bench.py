@@ -68,7 +68,7 @@ def parse_args():
                         "(moe_forward_l1_weighted) instead of weighting in the reduce")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
-                        "BatchedExperts slots of max_tokens = the smallest power of two >= T (moe_forward_batched) or "
+                        "BatchedExperts slots of max_tokens = max(16, the smallest power of two >= T) (moe_forward_batched) or "
                         "the tiny-batch layout, one 16-row block per (token, expert) pair, no sort (moe_forward_naive)")
     return p.parse_args()
 
@@ -265,7 +265,8 @@ def run_ours(args, w):
     e_bias = None if inp["e_score_bias"] is None else d(inp["e_score_bias"])
     batched = args.layout == "batched"
     naive = args.layout == "naive"
-    S = 1 << max(0, (T - 1).bit_length())         # BatchedExperts slot: smallest power of two >= T
+    # BatchedExperts slot: the smallest power of two >= T, at least 16 (one expert per GEMM row block)
+    S = max(16, 1 << max(0, (T - 1).bit_length()))
     if batched:
         ws = M.new_workspace_batched(T, w.H, w.I, w.E, w.K, S, device=dev)
     else:
@@ -321,7 +322,7 @@ def run_ours(args, w):
     value = W * T / (ms / 1e3)
 
     # ---- per-kernel durations: the same path called stage by stage with events in between
-    align = M.batched_align(S) if batched else (M.NAIVE_ROWS if naive else w.align)
+    align = M.batched_align(T, w.K, w.E, S) if batched else (M.NAIVE_ROWS if naive else w.align)
     U = w.E * S if batched else M.msum_upper(T, w.K, w.E, align)
     ids = torch.empty(T, w.K, dtype=torch.int32, device=dev)
     tw = torch.empty(T, w.K, dtype=torch.float32, device=dev)

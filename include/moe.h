@@ -252,8 +252,10 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
  * expert_num_tokens).  Rows of the permuted buffers: U = E * max_tokens, expert e's slot is rows
  * [e * max_tokens, (e + 1) * max_tokens), its first expert_num_tokens[e] rows live, the rest
  * padding.  max_tokens is a power of two in [1, 4096].  Scale tensors are tiled as for the
- * contiguous calls with align = min(max_tokens, 256).
- * ------------------------------------------------------------------------------------ */
+ * contiguous calls with align = moe_batched_align(T, K, E, max_tokens) (the GEMM row-block height:
+ * max_tokens below 16, else min(max_tokens, 64), or min(max_tokens, 128) when T*K > 64*E).
+ * max_tokens >= 16 keeps every GEMM row block inside one expert's slot. */
+int moe_batched_align(int T, int K, int E, int max_tokens);
 
 /* Workspace bytes of the BatchedExperts calls (zero-filled once before first use). */
 moe_status moe_workspace_size_batched(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes);

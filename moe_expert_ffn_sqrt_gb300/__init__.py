@@ -73,6 +73,8 @@ def lib():
         L.moe_unpermute_reduce.argtypes = [P, P, P, I, I, I, P, P]
         L.moe_forward.restype = S
         L.moe_forward.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P, Z, P]
+        L.moe_batched_align.restype = I
+        L.moe_batched_align.argtypes = [I, I, I, I]
         L.moe_workspace_size_batched.restype = S
         L.moe_workspace_size_batched.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
         L.moe_permute_batched.restype = S
@@ -327,9 +329,12 @@ def new_workspace_batched(T, H, I, E, K, max_tokens, device="cuda"):
     return torch.zeros(workspace_size_batched(T, H, I, E, K, max_tokens), dtype=torch.uint8, device=device)
 
 
-def batched_align(max_tokens):
-    """Alignment the scale tiling of the BatchedExperts buffers uses."""
-    return min(max_tokens, 256)
+def batched_align(T, K, E, max_tokens):
+    """Row-block height (the `align`) of the BatchedExperts buffers' scale tiling and GEMMs."""
+    a = int(lib().moe_batched_align(T, K, E, max_tokens))
+    if a <= 0:
+        raise MoeError(ERR_INVALID_ARG, "moe_batched_align")
+    return a
 
 
 def permute_batched(topk_ids, E, max_tokens, sorted_token_ids, expert_ids, inv_perm, m_sum, ws,

@@ -70,9 +70,16 @@ constexpr int kMaxSlot = 4096;
 bool slot_ok(int max_tokens) {
   return max_tokens >= 1 && max_tokens <= kMaxSlot && (max_tokens & (max_tokens - 1)) == 0;
 }
-// Alignment the GEMMs and the scale tiling see for a slot size: slots of 256 rows or more keep
-// whole 128-row blocks inside one expert exactly as the 256 alignment does.
-int slot_align(int max_tokens) { return max_tokens < 256 ? max_tokens : 256; }
+// Alignment the GEMMs and the scale tiling see for a slot size, i.e. their row-block height.
+// Below 16 rows a 16-row block spans several slots (the GEMM walks each block's experts).  From 16
+// rows on the block stays inside one slot: 64 rows when an expert receives at most 64 tokens on
+// average (deeper TMA ring per SM for the weight stream; a slot's blocks past its tokens are
+// skipped), else 128 (one block per expert's rows, weights read once).
+int slot_align(int T, int K, int E, int max_tokens) {
+  if (max_tokens < 16) return max_tokens;
+  const int cap = static_cast<long long>(T) * K > 64LL * E ? 128 : 64;
+  return max_tokens < cap ? max_tokens : cap;
+}
 size_t slot_rows(int E, int max_tokens) { return static_cast<size_t>(E) * max_tokens; }
 
 // moe_forward folds the unpermute-reduce into the L2 epilogue up to this many tokens.  With many
@@ -247,9 +254,14 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align, 
                         x_q, x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream);
 }
 
+int moe_batched_align(int T, int K, int E, int max_tokens) {
+  if (T < 0 || K <= 0 || E <= 0 || !slot_ok(max_tokens)) return 0;
+  return slot_align(T, K, E, max_tokens);
+}
+
 moe_status moe_workspace_size_batched(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes) {
-  if (!bytes || !slot_ok(max_tokens) || !dims_ok(T, H, I, E, K, slot_align(max_tokens))) return MOE_ERR_INVALID_ARG;
-  *bytes = layout_rows(T, H, I, E, K, slot_align(max_tokens), slot_rows(E, max_tokens)).total;
+  if (!bytes || !slot_ok(max_tokens) || !dims_ok(T, H, I, E, K, slot_align(T, K, E, max_tokens))) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_rows(T, H, I, E, K, slot_align(T, K, E, max_tokens), slot_rows(E, max_tokens)).total;
   return MOE_OK;
 }
 
@@ -258,7 +270,7 @@ moe_status moe_permute_batched(const int32_t* topk_ids, int T, int K, int E, int
                                int32_t* expert_num_tokens, const uint8_t* x_q, const uint8_t* x_sf, int H,
                                uint8_t* x_perm, uint8_t* x_perm_sf, void* ws, size_t ws_bytes, void* stream) {
   if (!slot_ok(max_tokens)) return MOE_ERR_INVALID_ARG;
-  return permute_common(topk_ids, T, K, E, slot_align(max_tokens), max_tokens, sorted_token_ids, expert_ids,
+  return permute_common(topk_ids, T, K, E, slot_align(T, K, E, max_tokens), max_tokens, sorted_token_ids, expert_ids,
                         inv_perm, m_sum, expert_num_tokens, x_q, x_sf, H, x_perm, x_perm_sf, ws, ws_bytes, stream);
 }
 
@@ -411,7 +423,7 @@ moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_
                                    uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes,
                                    void* stream) {
   if (!slot_ok(max_tokens) || !expert_num_tokens) return MOE_ERR_INVALID_ARG;
-  const int align = slot_align(max_tokens);
+  const int align = slot_align(T, K, E, max_tokens);
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   const size_t U = slot_rows(E, max_tokens);
   if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
@@ -538,7 +550,7 @@ moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, cons
                                size_t ws_bytes, void* stream) {
   // a token's K experts are distinct, so no expert receives more than T tokens
   if (!slot_ok(max_tokens) || max_tokens < T) return MOE_ERR_INVALID_ARG;
-  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(max_tokens), max_tokens,
+  return forward_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(T, K, E, max_tokens), max_tokens,
                         false, false, fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum,
                         expert_num_tokens, ws, ws_bytes, stream);
 }

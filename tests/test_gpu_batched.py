@@ -36,7 +36,7 @@ def _permute_batched(M, ids, E, S, xq=None, xsf=None):
     T, K = ids.shape
     H = 0 if xq is None else xq.shape[1]
     U = E * S
-    align = M.batched_align(S)
+    align = M.batched_align(T, K, E, S)
     o = dict(sorted_token_ids=torch.empty(U, **I32), expert_ids=torch.empty(U, **I32),
              inv_perm=torch.empty(T, K, **I32), m_sum=torch.empty(1, **I32), expert_num_tokens=torch.empty(E, **I32))
     ws = M.new_workspace_batched(T, max(H, 128), 128, E, K, S)
@@ -52,9 +52,10 @@ def _permute_batched(M, ids, E, S, xq=None, xsf=None):
 
 @pytest.mark.parametrize("T,K,E,S,skew", [(3, 2, 3, 4, 0.0), (8, 6, 256, 8, 0.0), (1, 1, 1, 1, 0.0),
                                           (37, 4, 16, 64, 0.5), (171, 6, 32, 256, 0.7), (500, 8, 64, 512, 1.5),
-                                          (2000, 8, 1024, 2048, 1.0), (100, 1, 2, 128, 0.0)])
+                                          (2000, 8, 1024, 2048, 1.0), (100, 1, 2, 128, 0.0), (300, 6, 16, 512, 0.3)])
 def test_permute_batched_parity(M, T, K, E, S, skew):
-    # covers the single-CTA (T*K <= 1024) and multi-CTA kernels, slots below and above 256 rows
+    # covers the single-CTA (T*K <= 1024) and multi-CTA kernels, slots below 16 rows (several per
+    # GEMM block) and above (64- and 128-row blocks)
     rng = np.random.default_rng(T * 17 + E)
     ids = synth.topk_ids_random(rng, T, E, K, skew)
     H = 256
@@ -68,7 +69,7 @@ def test_permute_batched_parity(M, T, K, E, S, skew):
         assert np.array_equal(g[k].cpu().numpy(), p[k]), k
     inv = p["inv_perm"].reshape(-1)
     assert np.array_equal(g["x_perm"].cpu().numpy()[inv], np.repeat(xq, K, axis=0))
-    psf = M.act_sf_untile(g["x_perm_sf"].cpu().numpy(), E * S, H // 128, M.batched_align(S))
+    psf = M.act_sf_untile(g["x_perm_sf"].cpu().numpy(), E * S, H // 128, M.batched_align(T, K, E, S))
     assert np.array_equal(psf[inv], np.repeat(xsf, K, axis=0))
 
 
@@ -192,7 +193,7 @@ def test_grouped_ffn_batched_equals_grouped_ffn(M, case):
     assert M.get_error(ws) == M.OK
     # BatchedExperts
     S = _pow2_at_least(T)
-    Ub, align_b = w.E * S, M.batched_align(S)
+    Ub, align_b = w.E * S, M.batched_align(T, w.K, w.E, S)
     wsb = M.new_workspace_batched(T, w.H, w.I, w.E, w.K, S)
     bs, be, bi, bm, bn = (torch.empty(Ub, **I32), torch.empty(Ub, **I32), torch.empty(T, w.K, **I32),
                           torch.empty(1, **I32), torch.empty(w.E, **I32))
@@ -225,9 +226,10 @@ def test_grouped_ffn_batched_reports_overfull_count(M):
     counts = torch.zeros(w.E, **I32)
     counts[3] = S + 1
     xp = torch.zeros(Ub, w.H, **U8)
-    xpsf = torch.full((M.act_sf_tiled_bytes(Ub, w.H // 128, S),), 127, **U8)
+    align = M.batched_align(S, 1, w.E, S)
+    xpsf = torch.full((M.act_sf_tiled_bytes(Ub, w.H // 128, align),), 127, **U8)
     hq = torch.zeros(Ub, w.I, **U8)
-    hsf = torch.zeros(M.act_sf_tiled_bytes(Ub, w.I // 128, S), **U8)
+    hsf = torch.zeros(M.act_sf_tiled_bytes(Ub, w.I // 128, align), **U8)
     y = torch.full((Ub, w.H), 1.0, dtype=torch.bfloat16, device="cuda")
     M.grouped_ffn_batched(xp, xpsf, counts, S, 1, w.H, w.I, w.E, S, w13, w2, hq, hsf, y, ws)
     assert M.get_error(ws) == M.ERR_DEVICE_INDEX
