@@ -28,7 +28,7 @@ struct WsLayout {
   size_t status = 0;
   size_t perm = 0, partial = 0, partial_bytes = 0;
   size_t topk_ids = 0, topk_w = 0, x_q = 0, x_sf = 0, sorted = 0, expert_ids = 0, inv_perm = 0, m_sum = 0;
-  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, sched = 0;
+  size_t x_perm = 0, x_perm_sf = 0, h_q = 0, h_sf = 0, y = 0, xb = 0, tickets = 0, sched = 0, counts = 0;
   size_t total = 0;
 };
 
@@ -57,6 +57,7 @@ WsLayout layout_rows(int T, int H, int I, int E, int K, int align, size_t U) {
   L.xb = off;         off = up(off + U * (H > I ? H : I) * 2);   // bf16 activation rows (NVFP4 GEMMs)
   L.tickets = off;    off = up(off + static_cast<size_t>(T) * ((H + 255) / 256) * 2 * 4);   // fused reduce
   L.sched = off;      off = up(off + gemm_sched_words(static_cast<int>(U), align) * 4);   // GEMM work counters
+  L.counts = off;     off = up(off + static_cast<size_t>(E) * 4);                     // tokens per expert
   L.total = off;
   return L;
 }
@@ -382,7 +383,8 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
                              const int32_t* m_sum, int T, int K, int H, int I, int E, int align, const moe_weight& w13,
                              const moe_weight& w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
                              size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0,
-                             const int32_t* row_ids = nullptr, const float* row_w = nullptr) {
+                             const int32_t* row_ids = nullptr, const float* row_w = nullptr,
+                             const int32_t* slot_counts = nullptr, int slot = 0) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
                                 nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w);
@@ -404,6 +406,11 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
   l1.row_ids = row_ids;
   l1.row_w = row_w;
+  if (slot_counts && slot % gemm_block_n(align) == 0 && align % gemm_block_n(align) == 0) {
+    // BatchedExperts with one expert per row block: only the blocks holding tokens are work
+    l1.counts = slot_counts;
+    l1.slot = slot;
+  }
   GemmLaunch l2 = mx_launch(false, h_q, h_sf, expert_ids, m_sum, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
   if (red) l2.red = *red;
   uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + L.sched);
@@ -436,7 +443,7 @@ moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_
   if (launch_batched_rows(expert_num_tokens, E, max_tokens, eids, ms, status_of(ws), S(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return ffn_common(x_perm, x_perm_sf, eids, ms, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws, ws_bytes,
-                    stream, nullptr, U);
+                    stream, nullptr, U, nullptr, nullptr, E <= 1024 ? expert_num_tokens : nullptr, max_tokens);
 }
 
 moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm, const float* topk_w, int T, int K,
@@ -473,6 +480,7 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.expert_ids);
   int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.inv_perm);
   int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.m_sum);
+  int32_t* cnt = expert_counts ? expert_counts : reinterpret_cast<int32_t*>(b + L.counts);
   uint8_t* xq = reinterpret_cast<uint8_t*>(b + L.x_q);
   uint8_t* xsf = reinterpret_cast<uint8_t*>(b + L.x_sf);
   uint8_t* xp = reinterpret_cast<uint8_t*>(b + L.x_perm);
@@ -489,8 +497,8 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
     st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw, xq, xsf, ws,
                    ws_bytes, stream);
     if (st != MOE_OK) return st;
-    st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, expert_counts, xq, xsf, H, xp, xpsf, ws,
-                        ws_bytes, stream);
+    st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, slot ? cnt : expert_counts, xq, xsf, H, xp,
+                        xpsf, ws, ws_bytes, stream);
     if (st != MOE_OK) return st;
   }
   const bool fuse_reduce = T <= kFusedReduceMaxTokens;
@@ -504,7 +512,8 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
     red.K = K;
   }
   st = ffn_common(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y, ws, ws_bytes, stream,
-                  fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr);
+                  fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr, slot ? cnt : nullptr,
+                  slot);
   if (st != MOE_OK || fuse_reduce) return st;
   return cuda_status(launch_unpermute_reduce(y, inv, l1w ? nullptr : tw, T, K, H, out, S(stream)));
 }

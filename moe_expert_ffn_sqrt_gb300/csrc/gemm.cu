@@ -96,7 +96,14 @@ struct GemmArgs {
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
   const int32_t* row_ids;       // L1: h of row r scaled by row_w[row_ids[r]] when row_w != nullptr
   const float* row_w;
+  // BatchedExperts (masked) mode: expert e owns slot_blocks row blocks from row block
+  // e * slot_blocks, of which ceil(counts[e] / BN) hold tokens; only those are work items
+  const int32_t* counts;        // nullptr: every row block below m_sum is an item
+  int slot_blocks;
+  int E;
 };
+
+constexpr int kMaxMaskedExperts = 1024;   // masked mode: experts in the shared prefix table
 
 // Work items: the L1 tiles of the row blocks below m_sum, then their L2 tiles, each phase
 // row-block major (t = row_block * n_wt + weight_tile).  The producer warp of each CTA takes the
@@ -107,12 +114,24 @@ struct Item {
   int phase, rb, wt;
 };
 
-__device__ __forceinline__ Item decode_item(const GemmArgs& a, int n0, int t) {
+// bpre (masked mode, shared memory): bpre[e] = active row blocks of experts < e, bpre[E] = all.
+__device__ __forceinline__ Item decode_item(const GemmArgs& a, int n0, int t, const int* bpre) {
   Item it;
   it.phase = t >= n0 ? 1 : 0;
   const int l = it.phase ? t - n0 : t;
-  it.rb = l / a.ph[it.phase].n_wt;
-  it.wt = l - it.rb * a.ph[it.phase].n_wt;
+  const int ab = l / a.ph[it.phase].n_wt;
+  it.wt = l - ab * a.ph[it.phase].n_wt;
+  if (bpre == nullptr) {
+    it.rb = ab;
+  } else {                                 // expert e with bpre[e] <= ab < bpre[e + 1]
+    int lo = 0, hi = a.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (bpre[mid] <= ab) lo = mid;
+      else hi = mid;
+    }
+    it.rb = lo * a.slot_blocks + (ab - bpre[lo]);
+  }
   return it;
 }
 
@@ -121,8 +140,8 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& a, int n0, int t) {
 // inside one expert's segment (real rows first, then padding), so the block's first entry names
 // its only expert (-1: the block is padding); otherwise the warp scans the block in one round.
 template <int BN>
-__device__ __forceinline__ bool find_expert(const GemmArgs& a, int n0, int msum, int t, int& e) {
-  const int r0 = decode_item(a, n0, t).rb * BN;
+__device__ __forceinline__ bool find_expert(const GemmArgs& a, int n0, int msum, int t, int& e, const int* bpre) {
+  const int r0 = decode_item(a, n0, t, bpre).rb * BN;
   if (a.one_expert_blocks) {
     if (e >= 0) return false;
     const int x = __ldg(a.expert_ids + r0);
@@ -219,7 +238,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int msum = *a.m_sum;
-  const int nrb = (msum + BN - 1) / BN;
+  // masked mode: prefix of the experts' active row blocks (an epilogue warp, idle at this point)
+  __shared__ int s_bpre[kMaxMaskedExperts + 1];
+  const int* bpre = nullptr;
+  if (a.counts) {
+    if (warp == 2) {
+      int run = 0;
+      for (int e0 = 0; e0 < a.E; e0 += 32) {
+        const int e = e0 + lane;
+        int nb = 0;
+        if (e < a.E) nb = min((max(__ldg(a.counts + e), 0) + BN - 1) / BN, a.slot_blocks);
+        int incl = nb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += v;
+        }
+        if (e < a.E) s_bpre[e] = run + incl - nb;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) s_bpre[a.E] = run;
+    }
+    __syncthreads();
+    bpre = s_bpre;
+  }
+  const int nrb = bpre ? bpre[a.E] : (msum + BN - 1) / BN;
   const int n0 = a.ph[0].n_tiles ? nrb * a.ph[0].n_wt : 0;
   const int n_items = n0 + (a.ph[1].n_tiles ? nrb * a.ph[1].n_wt : 0);
 
@@ -233,7 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int t = -1, e = -1;
     bool ok = true;
     while (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      bool have = t >= 0 && find_expert<BN>(a, n0, msum, t, e);    // another expert of the same block
+      bool have = t >= 0 && find_expert<BN>(a, n0, msum, t, e, bpre);    // another expert of the same block
       while (!have) {
         int nt = 0;
         if (lane == 0) nt = static_cast<int>(atomicAdd(a.sched + a.n_ready, 1u));
@@ -244,7 +287,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         t = nt;
         e = -1;
-        have = find_expert<BN>(a, n0, msum, t, e);
+        have = find_expert<BN>(a, n0, msum, t, e, bpre);
       }
       if (!have) break;
       // hand the item to the MMA and epilogue warps
@@ -259,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         islot = 0;
         iphase ^= 1;
       }
-      const Item it = decode_item(a, n0, t);
+      const Item it = decode_item(a, n0, t, bpre);
       const GemmPhase& P = a.ph[it.phase];
       const CUtensorMap* mw = it.phase ? &tmap_w2 : &tmap_w1;
       const CUtensorMap* mx = it.phase ? &tmap_x2 : &tmap_x1;
@@ -344,7 +387,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         iphase ^= 1;
       }
       if (item.x < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int n_slabs = a.ph[decode_item(a, n0, item.x).phase].n_slabs;
+      const int n_slabs = a.ph[decode_item(a, n0, item.x, bpre).phase].n_slabs;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
@@ -409,7 +452,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (item.x < 0) break;
       const int e = item.y;
-      const Item it = decode_item(a, n0, item.x);
+      const Item it = decode_item(a, n0, item.x, bpre);
       const int r0 = it.rb * BN, wt = it.wt;
       const int row = r0 + m;
       const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
@@ -661,6 +704,13 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   if (l1) {
     a.row_ids = l1->row_ids;
     a.row_w = l1->row_w;
+  }
+  a.E = any.E;
+  if (any.counts) {
+    // masked mode needs one expert per row block and whole blocks per slot
+    if (any.slot % BN != 0 || any.align % BN != 0 || any.E > kMaxMaskedExperts) return cudaErrorInvalidValue;
+    a.counts = any.counts;
+    a.slot_blocks = any.slot / BN;
   }
   const int total = a.ph[0].n_tiles + a.ph[1].n_tiles;
   int grid = num_sms();

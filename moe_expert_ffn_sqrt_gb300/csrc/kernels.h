@@ -63,6 +63,8 @@ struct GemmLaunch {
   FusedReduce red{};           // L2: fold the unpermute-reduce into the epilogue when red.out is set
   const int32_t* row_ids = nullptr;   // L1 with row weights: h of row r is scaled by
   const float* row_w = nullptr;       // row_w[row_ids[r]] (the routing weight of the row's pair)
+  const int32_t* counts = nullptr;    // BatchedExperts: tokens per expert slot (masked work list)
+  int slot = 0;                       // BatchedExperts slot rows (a multiple of the block height)
 };
 int num_sms();
 int weight_tiles(int N, int pair);
