@@ -233,21 +233,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // masked mode: each expert's row blocks that hold tokens, loaded by all threads at once; the
+  // prefix over experts is formed after the barrier below
+  __shared__ int s_bpre[kMaxMaskedExperts + 1];
+  if (a.counts)
+    for (int e = threadIdx.x; e < a.E; e += kGemmThreads)
+      s_bpre[e] = min((max(__ldg(a.counts + e), 0) + BN - 1) / BN, a.slot_blocks);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int msum = *a.m_sum;
-  // masked mode: prefix of the experts' active row blocks (an epilogue warp, idle at this point)
-  __shared__ int s_bpre[kMaxMaskedExperts + 1];
+  // masked mode: exclusive prefix of the experts' active row blocks, in place (an epilogue warp,
+  // idle at this point)
   const int* bpre = nullptr;
   if (a.counts) {
     if (warp == 2) {
       int run = 0;
       for (int e0 = 0; e0 < a.E; e0 += 32) {
         const int e = e0 + lane;
-        int nb = 0;
-        if (e < a.E) nb = min((max(__ldg(a.counts + e), 0) + BN - 1) / BN, a.slot_blocks);
+        const int nb = e < a.E ? s_bpre[e] : 0;
         int incl = nb;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
