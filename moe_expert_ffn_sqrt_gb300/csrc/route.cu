@@ -128,11 +128,10 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
         }
       }
       warp_argmax(bk, bi);
-      if ((bi & 31) == lane) {
+      const bool won = (bi & 31) == lane;   // selects with compile-time indices keep key[] in registers
+      const int jw = bi >> 5;
 #pragma unroll
-        for (int j = 0; j < PER; ++j)
-          if (j == (bi >> 5)) key[j] = -INFINITY;
-      }
+      for (int j = 0; j < PER; ++j) key[j] = (won && j == jw) ? -INFINITY : key[j];
       const float sw = s_score[bi];
       wsum += sw;
       if (lane == k) wmine = sw;
@@ -359,13 +358,17 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
         }
       }
       warp_argmax(bk, bi);
+      // the winner's lane takes its score and retires its key; selects with compile-time indices
+      // keep s[] and key[] in registers
       float sw = 0.f;
+      const bool won = (bi & 31) == lane;
+      const int jw = bi >> 5;
 #pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if ((bi & 31) == lane && j == (bi >> 5)) {
-          sw = s[j];
-          key[j] = -INFINITY;
-        }
+      for (int j = 0; j < PER; ++j) {
+        const bool hit = won && j == jw;
+        sw = hit ? s[j] : sw;
+        key[j] = hit ? -INFINITY : key[j];
+      }
       sw = __shfl_sync(0xffffffffu, sw, bi & 31);
       wsum += sw;
       if (lane == k) wmine = sw;
