@@ -19,7 +19,7 @@
 //  * moe_forward runs L1 and L2 as one cooperative launch: L2 items wait (bounded) on per-row-block
 //    counters of finished L1 tiles, so the L1 tail wave and the launch gap are filled with L2 work.
 //  * Persistent CTAs (one per SM) walk the items in a fixed order; a producer warp (TMA), an MMA
-//    warp (one thread issues tcgen05.cp + tcgen05.mma) and four epilogue warps run decoupled
+//    warp (one thread issues tcgen05.cp + tcgen05.mma) and eight epilogue warps run decoupled
 //    through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
 //    the shared-memory ring keeps the weights streaming while the epilogue drains it.
 //  * Weights come pre-packed (moe_pack_weights): per (expert, tile, 128-deep slab) one chunk of
@@ -135,13 +135,12 @@ __device__ __forceinline__ Item decode_item(const GemmArgs& a, int n0, int t, co
   return it;
 }
 
-// Smallest expert id > e among the rows of item t's block (rows are sorted by expert, ignoring
-// -1).  Called by whole warps.  When the permute alignment is a multiple of BN every block lies
+// Smallest expert id > e among the rows of the block starting at row r0 (rows are sorted by
+// expert, ignoring -1).  Called by whole warps.  When the permute alignment is a multiple of BN every block lies
 // inside one expert's segment (real rows first, then padding), so the block's first entry names
 // its only expert (-1: the block is padding); otherwise the warp scans the block in one round.
 template <int BN>
-__device__ __forceinline__ bool find_expert(const GemmArgs& a, int n0, int msum, int t, int& e, const int* bpre) {
-  const int r0 = decode_item(a, n0, t, bpre).rb * BN;
+__device__ __forceinline__ bool find_expert(const GemmArgs& a, int msum, int r0, int& e) {
   if (a.one_expert_blocks) {
     if (e >= 0) return false;
     const int x = __ldg(a.expert_ids + r0);
@@ -202,7 +201,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* item_full = acc_empty + 1;             // [kItemSlots], producer arrives
   uint64_t* item_empty = item_full + kItemSlots;   // [kItemSlots], MMA warp + epilogue arrive
-  int2* items = reinterpret_cast<int2*>(item_empty + kItemSlots);   // (t, e); t < 0 ends the work
+  // (t, e, row block, weight tile | phase << 16), decoded once by the producer; t < 0 ends the work
+  int4* items = reinterpret_cast<int4*>(item_empty + kItemSlots);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kItemSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -279,9 +279,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     uint32_t islot = 0, iphase = 0;
     int t = -1, e = -1;
+    Item it{0, 0, 0};
     bool ok = true;
     while (ok && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      bool have = t >= 0 && find_expert<BN>(a, n0, msum, t, e, bpre);    // another expert of the same block
+      bool have = t >= 0 && find_expert<BN>(a, msum, it.rb * BN, e);    // another expert of the same block
       while (!have) {
         int nt = 0;
         if (lane == 0) nt = static_cast<int>(atomicAdd(a.sched + a.n_ready, 1u));
@@ -292,14 +293,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         t = nt;
         e = -1;
-        have = find_expert<BN>(a, n0, msum, t, e, bpre);
+        it = decode_item(a, n0, t, bpre);
+        have = find_expert<BN>(a, msum, it.rb * BN, e);
       }
       if (!have) break;
       // hand the item to the MMA and epilogue warps
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(item_empty + islot), iphase ^ 1, a.status));
       if (!ok) break;
       if (lane == 0) {
-        items[islot] = make_int2(t, e);
+        items[islot] = make_int4(t, e, it.rb, it.wt | (it.phase << 16));
         mbar_arrive(smem_u32(item_full + islot));
       }
       __syncwarp();
@@ -307,7 +309,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         islot = 0;
         iphase ^= 1;
       }
-      const Item it = decode_item(a, n0, t, bpre);
       const GemmPhase& P = a.ph[it.phase];
       const CUtensorMap* mw = it.phase ? &tmap_w2 : &tmap_w1;
       const CUtensorMap* mx = it.phase ? &tmap_x2 : &tmap_x1;
@@ -363,7 +364,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // end of work for the other warps (if the ring does not free up they stop on their own waits)
     if (__all_sync(0xffffffffu, mbar_wait(smem_u32(item_empty + islot), iphase ^ 1, a.status))) {
       if (lane == 0) {
-        items[islot] = make_int2(-1, -1);
+        items[islot] = make_int4(-1, -1, 0, 0);
         mbar_arrive(smem_u32(item_full + islot));
       }
       __syncwarp();
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *abort_flag = 1;
         break;
       }
-      const int2 item = items[islot];
+      const int4 item = items[islot];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(item_empty + islot));
       if (++islot == kItemSlots) {
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         iphase ^= 1;
       }
       if (item.x < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int n_slabs = a.ph[decode_item(a, n0, item.x, bpre).phase].n_slabs;
+      const int n_slabs = a.ph[item.w >> 16].n_slabs;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
@@ -444,7 +445,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t islot = 0, iphase = 0;
     while (true) {
       bool ok = mbar_wait(smem_u32(item_full + islot), iphase, a.status);
-      const int2 item = items[islot];
+      const int4 item = items[islot];
       ok = named_barrier_and(1, kEpiThreads, ok);    // every epilogue thread has read the slot
       if (ok && threadIdx.x == kEpiThread0) mbar_arrive(smem_u32(item_empty + islot));
       if (++islot == kItemSlots) {
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       if (item.x < 0) break;
       const int e = item.y;
-      const Item it = decode_item(a, n0, item.x, bpre);
+      const Item it{item.w >> 16, item.z, item.w & 0xFFFF};
       const int r0 = it.rb * BN, wt = it.wt;
       const int row = r0 + m;
       const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
