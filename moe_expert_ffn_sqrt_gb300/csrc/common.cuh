@@ -75,6 +75,11 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 
 // Orders this thread's generic-proxy global accesses with its async-proxy (TMA / bulk copy)
 // accesses: used on both sides when one CTA's plain stores are read by another CTA's TMA.
+// Programmatic dependent launch: a kernel launched with programmatic stream serialization may start
+// while the previous kernel of the stream still runs; this waits until that kernel has completed
+// and its memory operations are visible (returns at once for an ordinary launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }

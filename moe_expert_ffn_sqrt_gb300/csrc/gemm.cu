@@ -236,6 +236,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // masked mode: each expert's row blocks that hold tokens, loaded by all threads at once; the
   // prefix over experts is formed after the barrier below
   __shared__ int s_bpre[kMaxMaskedExperts + 1];
+  grid_dependency_wait();          // everything below reads the previous launch's results
   if (a.counts)
     for (int e = threadIdx.x; e < a.E; e += kGemmThreads)
       s_bpre[e] = min((max(__ldg(a.counts + e), 0) + BN - 1) / BN, a.slot_blocks);
@@ -729,12 +730,32 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   cfg.blockDim = dim3(kGemmThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  // Programmatic stream serialization lets the CTAs start their prologue (barriers, TMEM, tensor
+  // maps) while the permute finishes; they wait for it before reading its results.  Should the
+  // runtime refuse it next to the cooperative attribute, the launch is repeated without it.
+  static bool pdl_ok = true;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (a.fused) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  }
+  if (pdl_ok) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = a.fused ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
+  cfg.numAttrs = n;
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
+  if (err != cudaSuccess && pdl_ok) {
+    (void)cudaGetLastError();
+    pdl_ok = false;
+    cfg.numAttrs = n - 1;
+    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
+  }
+  return err;
 }
 
 int gemm_block_n(int align) { return act_sf_block_rows(align); }

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_count_kernel(const Pe
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int N = a.T * a.K, G = gridDim.x, c = blockIdx.x;
   for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
+  grid_dependency_wait();                          // topk_ids come from the previous launch
   __syncthreads();
   const int beg = min(N, (c * kPermWarps + warp) * W), end = min(N, beg + W);
   for (int i = beg + lane; i < end; i += 32) {
@@ -209,6 +210,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int N = a.T * a.K;
   for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
+  grid_dependency_wait();                          // topk_ids come from the previous launch
   int e_mine = -1;
   if (tid < N) {
     e_mine = a.topk_ids[tid];
@@ -375,8 +377,8 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     const bool copy = x_perm != nullptr && npairs <= kSmallCopyPairs;
     const long long units = npairs * ((H / 16 + kCopyPiece - 1) / kCopyPiece);
     const int grid = copy && npairs > 0 ? static_cast<int>((units + kPermWarps - 1) / kPermWarps) : 1;
-    permute_small_kernel<<<grid, kPermThreads, smem, stream>>>(a, x_q, x_sf, H, x_perm, x_perm_sf, bt, nb);
-    err = cudaGetLastError();
+    err = launch_pdl(permute_small_kernel, dim3(grid), dim3(kPermThreads), smem, stream, a, x_q, x_sf, H, x_perm,
+                     x_perm_sf, bt, nb);
     if (err != cudaSuccess || x_perm == nullptr || copy) return err;
   } else {
     if (scratch == nullptr) return cudaErrorInvalidValue;
@@ -384,8 +386,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     err = cudaFuncSetAttribute(permute_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(E * sizeof(int32_t)));
     if (err != cudaSuccess) return err;
-    permute_count_kernel<<<G, kPermThreads, E * sizeof(int32_t), stream>>>(a, W, scratch);
-    err = cudaGetLastError();
+    err = launch_pdl(permute_count_kernel, dim3(G), dim3(kPermThreads), E * sizeof(int32_t), stream, a, W, scratch);
     if (err != cudaSuccess) return err;
     const size_t smem = permute_smem_bytes(E);
     err = cudaFuncSetAttribute(permute_place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
