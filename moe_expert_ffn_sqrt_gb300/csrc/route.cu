@@ -178,6 +178,12 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
   const int nblocks = gridDim.x * gridDim.y;
   const int bid = blockIdx.y * gridDim.x + blockIdx.x;
   const int T = a.T, H = a.H, E = a.E;
+  // the biases are read only by the last CTA, after every other CTA's work: start them towards L2
+  if (bid == 0 && warp == 0)
+    for (int off = lane * 32; off < E; off += 32 * 32) {     // one 128-byte line per lane and round
+      if (a.gate_bias) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.gate_bias + off));
+      if (a.e_bias) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.e_bias + off));
+    }
   // 1. gate GEMV partial: experts e0..e0+3 over one quarter of H
   const int e0 = blockIdx.x * kGemvE, split = blockIdx.y;
   const int hq = H / kGemvSplit, hbeg = split * hq;   // hq is a multiple of 32 (H multiple of 128)
