@@ -198,8 +198,7 @@ constexpr int kSmallPairs = 1024;
 constexpr int kSmallCopyPairs = 128;
 constexpr int kCopyPiece = 64;       // 16-byte chunks of a row one warp copies (1 KB)
 
-template <int NT>
-__global__ void __launch_bounds__(NT, 1) permute_small_kernel(const PermuteArgs a, const uint8_t* x_q,
+__global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const PermuteArgs a, const uint8_t* x_q,
                                                                         const uint8_t* x_sf, int H, uint8_t* x_perm,
                                                                         uint8_t* x_perm_sf, int bt, int nb) {
   extern __shared__ int32_t sh[];
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(NT, 1) permute_small_kernel(const PermuteArgs 
   __shared__ int32_t s_total;
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
   const int N = a.T * a.K;
-  for (int e = tid; e < a.E; e += NT) cnt[e] = 0;
+  for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
   grid_dependency_wait();                          // topk_ids come from the previous launch
   int e_mine = -1;
   if (tid < N) {
@@ -230,7 +229,7 @@ __global__ void __launch_bounds__(NT, 1) permute_small_kernel(const PermuteArgs 
   if (tid < N) s_rank[tid] = rank;
   __syncthreads();
   if (a.slot > 0) {                  // BatchedExperts: fixed slots
-    for (int e = tid; e < a.E; e += NT) seg[e] = e * a.slot;
+    for (int e = tid; e < a.E; e += kPermThreads) seg[e] = e * a.slot;
     if (tid == 0) s_total = a.E * a.slot;
   } else if (warp == 0) {            // exclusive scan of the aligned segment sizes
     const int per = (a.E + 31) / 32;
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(NT, 1) permute_small_kernel(const PermuteArgs 
         a.expert_ids[pos] = e_mine;
       }
     }
-    for (int e = warp; e < a.E; e += (NT / 32)) {
+    for (int e = warp; e < a.E; e += kPermWarps) {
       const int c = cnt[e];
       const int padded = a.slot > 0 ? a.slot : (c + a.align - 1) / a.align * a.align;
       for (int r = c + lane; r < padded; r += 32) {
@@ -277,18 +276,18 @@ __global__ void __launch_bounds__(NT, 1) permute_small_kernel(const PermuteArgs 
         a.expert_ids[seg[e] + r] = -1;
       }
     }
-    for (int r = msum + tid; r < a.U; r += NT) {
+    for (int r = msum + tid; r < a.U; r += kPermThreads) {
       a.sorted_ids[r] = N;
       a.expert_ids[r] = -1;
     }
     if (a.counts)
-      for (int e = tid; e < a.E; e += NT) a.counts[e] = cnt[e];
+      for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
     if (tid == 0) *a.m_sum = msum;
   }
   if (x_perm != nullptr && N <= kSmallCopyPairs) {
     // one warp per (pair, 1 KB piece of its row); the piece-0 warp also copies the row's scales
     const int chunks = H / 16, slabs = H / 128, pieces = (chunks + kCopyPiece - 1) / kCopyPiece;
-    for (int u = blockIdx.x * (NT / 32) + warp; u < N * pieces; u += gridDim.x * (NT / 32)) {
+    for (int u = blockIdx.x * kPermWarps + warp; u < N * pieces; u += gridDim.x * kPermWarps) {
       const int p = u / pieces, piece = u - p * pieces;
       const int e = s_ids[p];
       if (e < 0 || (a.slot > 0 && s_rank[p] >= a.slot)) continue;
@@ -372,22 +371,14 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
   const long long npairs = static_cast<long long>(T) * K;
   cudaError_t err;
   if (npairs <= kSmallPairs) {
-    // one thread per pair: 256-thread CTAs up to 256 pairs (shorter barriers, more copy CTAs), else 1024
     const size_t smem = 2 * static_cast<size_t>(E) * sizeof(int32_t);
-    const bool small = npairs <= 256;
-    const int nt = small ? 256 : kPermThreads;
-    err = small ? cudaFuncSetAttribute(permute_small_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem))
-                : cudaFuncSetAttribute(permute_small_kernel<kPermThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+    err = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     const bool copy = x_perm != nullptr && npairs <= kSmallCopyPairs;
     const long long units = npairs * ((H / 16 + kCopyPiece - 1) / kCopyPiece);
-    const int grid = copy && npairs > 0 ? static_cast<int>((units + nt / 32 - 1) / (nt / 32)) : 1;
-    err = small ? launch_pdl(permute_small_kernel<256>, dim3(grid), dim3(nt), smem, stream, a, x_q, x_sf, H, x_perm,
-                             x_perm_sf, bt, nb)
-                : launch_pdl(permute_small_kernel<kPermThreads>, dim3(grid), dim3(nt), smem, stream, a, x_q, x_sf, H,
-                             x_perm, x_perm_sf, bt, nb);
+    const int grid = copy && npairs > 0 ? static_cast<int>((units + kPermWarps - 1) / kPermWarps) : 1;
+    err = launch_pdl(permute_small_kernel, dim3(grid), dim3(kPermThreads), smem, stream, a, x_q, x_sf, H, x_perm,
+                     x_perm_sf, bt, nb);
     if (err != cudaSuccess || x_perm == nullptr || copy) return err;
   } else {
     if (scratch == nullptr) return cudaErrorInvalidValue;
