@@ -311,20 +311,31 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
   for (int t = warp; t < T; t += 8) {
     float s[PER], key[PER];
     float lmax = -INFINITY;
+    // partial sums of 8 experts per lane at a time: every load of a group is issued before the
+    // optional logits stores (which the compiler may not move loads across)
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane + 32 * j;
-      float l = -INFINITY;
-      if (e < E) {
-        float v[kGemvSplit];
+    for (int j0 = 0; j0 < PER; j0 += 8) {
+      constexpr int G = PER < 8 ? PER : 8;
+      float v[G][kGemvSplit];
 #pragma unroll
-        for (int sp = 0; sp < kGemvSplit; ++sp) v[sp] = __ldcg(partial + (static_cast<size_t>(sp) * T + t) * E + e);
-        l = (v[0] + v[1]) + (v[2] + v[3]);       // the order route_finish_kernel sums 4 splits in
-        if (a.gate_bias) l += gbias[j];
-        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+      for (int jj = 0; jj < G; ++jj) {
+        const int e = lane + 32 * (j0 + jj);
+#pragma unroll
+        for (int sp = 0; sp < kGemvSplit; ++sp)
+          v[jj][sp] = e < E ? __ldcg(partial + (static_cast<size_t>(sp) * T + t) * E + e) : 0.f;
       }
-      s[j] = l;
-      lmax = fmaxf(lmax, l);
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        const int j = j0 + jj, e = lane + 32 * j;
+        float l = -INFINITY;
+        if (e < E) {
+          l = (v[jj][0] + v[jj][1]) + (v[jj][2] + v[jj][3]);   // the order route_finish_kernel sums 4 splits in
+          if (a.gate_bias) l += gbias[j];
+          if (a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+        }
+        s[j] = l;
+        lmax = fmaxf(lmax, l);
+      }
     }
     if (a.score_fn == 0) {
 #pragma unroll
