@@ -39,16 +39,14 @@ struct RouteFinishArgs {
   NaiveLayout nv;    // small batches: the tiny-batch layout written by the same launch (nv.eids null: off)
 };
 
-__device__ __forceinline__ void warp_argmax(float& key, int& id) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float k2 = __shfl_xor_sync(0xffffffffu, key, off);
-    const int i2 = __shfl_xor_sync(0xffffffffu, id, off);
-    if (k2 > key || (k2 == key && i2 < id)) {
-      key = k2;
-      id = i2;
-    }
-  }
+// Warp arg-max of (key, id), ties to the lower id, with the warp reduction instructions: the keys
+// as order-preserving unsigned integers (-0 folded into +0, so that equal floats stay equal), the
+// maximum, then the smallest id among the lanes that hold it.  Keys are finite or -inf.
+__device__ __forceinline__ int warp_argmax_id(float key, int id) {
+  const uint32_t u = __float_as_uint(key + 0.0f);
+  const uint32_t ok = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t best = __reduce_max_sync(0xffffffffu, ok);
+  return static_cast<int>(__reduce_min_sync(0xffffffffu, ok == best ? static_cast<uint32_t>(id) : 0xffffffffu));
 }
 
 __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
@@ -127,7 +125,7 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
           bi = e;
         }
       }
-      warp_argmax(bk, bi);
+      bi = warp_argmax_id(bk, bi);
       const bool won = (bi & 31) == lane;   // selects with compile-time indices keep key[] in registers
       const int jw = bi >> 5;
 #pragma unroll
@@ -374,7 +372,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
           bi = e;
         }
       }
-      warp_argmax(bk, bi);
+      bi = warp_argmax_id(bk, bi);
       // the winner's lane takes its score and retires its key; selects with compile-time indices
       // keep s[] and key[] in registers
       float sw = 0.f;
