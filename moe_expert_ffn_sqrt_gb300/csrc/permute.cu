@@ -21,6 +21,9 @@ namespace moe {
 constexpr int kPermThreads = 1024;
 constexpr int kPermWarps = kPermThreads / 32;
 
+// The alignment is a power of two (checked by the host), so rounding up is a mask, not a division.
+__device__ __forceinline__ int round_up_pow2(int n, int align) { return (n + align - 1) & ~(align - 1); }
+
 struct PermuteArgs {
   const int32_t* topk_ids;
   int T, K, E, align, U;
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
       }
       tot[e] = t_all;
       pre_mine[j] = t_pre;
-      local += a.slot > 0 ? a.slot : (t_all + a.align - 1) / a.align * a.align;
+      local += a.slot > 0 ? a.slot : round_up_pow2(t_all, a.align);
     }
   }
   s_scan[tid] = local;
@@ -137,7 +140,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
         hist[w * a.E + e] = base;
         base += h;
       }
-      run += a.slot > 0 ? a.slot : (tot[e] + a.align - 1) / a.align * a.align;
+      run += a.slot > 0 ? a.slot : round_up_pow2(tot[e], a.align);
     }
   }
   if (tid == kPermThreads - 1) s_total = s_scan[tid];
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
   // 4. padding rows inside each segment (experts split over CTAs), then the tail [M_sum, U)
   for (int e = c * kPermWarps + warp; e < a.E; e += G * kPermWarps) {
     const int n = tot[e];
-    const int padded = a.slot > 0 ? a.slot : (n + a.align - 1) / a.align * a.align;
+    const int padded = a.slot > 0 ? a.slot : round_up_pow2(n, a.align);
     for (int r = n + lane; r < padded; r += 32) {
       a.sorted_ids[seg[e] + r] = N;
       a.expert_ids[seg[e] + r] = -1;
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
     int local = 0;
     for (int j = 0; j < per; ++j) {
       const int e = lane * per + j;
-      if (e < a.E) local += (cnt[e] + a.align - 1) / a.align * a.align;
+      if (e < a.E) local += round_up_pow2(cnt[e], a.align);
     }
     int incl = local;
 #pragma unroll
@@ -249,7 +252,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
       const int e = lane * per + j;
       if (e < a.E) {
         seg[e] = run;
-        run += (cnt[e] + a.align - 1) / a.align * a.align;
+        run += round_up_pow2(cnt[e], a.align);
       }
     }
     if (lane == 31) s_total = incl;
@@ -268,21 +271,23 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
         a.expert_ids[pos] = e_mine;
       }
     }
-    for (int e = warp; e < a.E; e += kPermWarps) {
-      const int c = cnt[e];
-      const int padded = a.slot > 0 ? a.slot : (c + a.align - 1) / a.align * a.align;
-      for (int r = c + lane; r < padded; r += 32) {
-        a.sorted_ids[seg[e] + r] = N;
-        a.expert_ids[seg[e] + r] = -1;
-      }
-    }
-    for (int r = msum + tid; r < a.U; r += kPermThreads) {
-      a.sorted_ids[r] = N;
-      a.expert_ids[r] = -1;
-    }
     if (a.counts)
       for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
     if (tid == 0) *a.m_sum = msum;
+  }
+  // padding rows of each segment and the tail [M_sum, U), split over every CTA of the launch (each
+  // holds the same counts and segment starts)
+  for (int e = blockIdx.x * kPermWarps + warp; e < a.E; e += gridDim.x * kPermWarps) {
+    const int c = cnt[e];
+    const int padded = a.slot > 0 ? a.slot : round_up_pow2(c, a.align);
+    for (int r = c + lane; r < padded; r += 32) {
+      a.sorted_ids[seg[e] + r] = N;
+      a.expert_ids[seg[e] + r] = -1;
+    }
+  }
+  for (int r = msum + blockIdx.x * kPermThreads + tid; r < a.U; r += gridDim.x * kPermThreads) {
+    a.sorted_ids[r] = N;
+    a.expert_ids[r] = -1;
   }
   if (x_perm != nullptr && N <= kSmallCopyPairs) {
     // one warp per (pair, 1 KB piece of its row); the piece-0 warp also copies the row's scales
