@@ -41,7 +41,7 @@ def launches_per_forward(w, naive=False):
     if naive:
         permute = 0                               # the routing launch writes the tiny-batch layout
     if w.fmt == "mxfp4":
-        ffn = 1                                   # L1 and L2 in one cooperative launch
+        ffn = 1                                   # L1 and L2 in one launch
     else:
         ffn = 4                                   # bf16 activation rows + GEMM, for L1 and for L2
     reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue

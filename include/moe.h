@@ -216,7 +216,7 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
 
 /* Both expert GEMMs in one call (MegaMoE page 二、阶段 2-5 as one persistent kernel): the results
  * of moe_grouped_gemm_l1_swiglu (h_q, h_sf) and of moe_grouped_gemm_l2 (y_perm), bit for bit.
- * With MXFP4 weights it is one cooperative launch in which an L2 tile starts once every L1 tile
+ * With MXFP4 weights it is one launch in which an L2 tile starts once every L1 tile
  * of its row block is stored; it needs the full moe_workspace_size() workspace (per-row-block
  * counters that the launch leaves at zero).  With NVFP4 weights the two calls run in turn.
  * Arguments as for the two calls; h_q/h_sf/y_perm 16-byte aligned. */

@@ -377,7 +377,7 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
                      ws_bytes, stream);
 }
 
-// L1 + SwiGLU + requant and L2.  MXFP4: one cooperative launch (L2 tiles start as soon as the
+// L1 + SwiGLU + requant and L2.  MXFP4: one launch (L2 tiles start as soon as the
 // h rows of their block are stored).  NVFP4: the two GEMM calls one after the other.
 static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
                              const int32_t* m_sum, int T, int K, int H, int I, int E, int align, const moe_weight& w13,

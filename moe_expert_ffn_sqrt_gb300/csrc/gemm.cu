@@ -16,8 +16,8 @@
 //    token rows are loaded; the MMA's other rows read unrelated shared memory and their results
 //    are never stored.  BN divides the permute alignment in the common case, so a block holds
 //    one expert; otherwise each expert in the block is a separate pass with masked stores.
-//  * moe_forward runs L1 and L2 as one cooperative launch: L2 items wait (bounded) on per-row-block
-//    counters of finished L1 tiles, so the L1 tail wave and the launch gap are filled with L2 work.
+//  * moe_forward runs L1 and L2 as one launch: L2 items wait (bounded) on per-row-block counters of
+//    finished L1 tiles, so the L1 tail wave and the launch gap are filled with L2 work.
 //  * Persistent CTAs (one per SM) walk the items in a fixed order; a producer warp (TMA), an MMA
 //    warp (one thread issues tcgen05.cp + tcgen05.mma) and eight epilogue warps run decoupled
 //    through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
@@ -182,9 +182,10 @@ constexpr int kItemSlots = 4;
 // written by other CTAs: its producer first waits until sched[rb] counts all n_wt L1 tiles of the
 // block (each L1 item's epilogue adds one after its stores).  Items are drawn in index order, all
 // L1 items before any L2 item; a producer waits only while holding an L2 item, after issuing every
-// load of the items it drew before; and the launch is cooperative (all CTAs resident).  So every
-// awaited L1 item is running or done; the wait is bounded all the same.  The last CTA to exit sets
-// all counters back to zero: no CTA can still be waiting or drawing then.
+// load of the items it drew before.  So every awaited L1 item was drawn by a CTA that is running
+// (or has finished it), and that CTA's MMA and epilogue warps complete it whatever its producer
+// waits for: progress needs no co-residency of the CTAs, and the wait is bounded all the same.
+// The last CTA to exit sets all counters back to zero: no CTA can still be waiting or drawing then.
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
@@ -674,7 +675,7 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
 
 // l1 and/or l2 (non-null ones run).  `sched` holds gemm_sched_words(U, align) words that are zero
 // before the launch and zero again after it (work counter; with both phases also the per-row-block
-// counters that order them, and then the launch is cooperative so that all CTAs are resident).
+// counters that order them).
 template <int BN>
 static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   using C = GemmCfg<BN>;
@@ -732,15 +733,10 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   cfg.stream = stream;
   // Programmatic stream serialization lets the CTAs start their prologue (barriers, TMEM, tensor
   // maps) while the permute finishes; they wait for it before reading its results.  Should the
-  // runtime refuse it next to the cooperative attribute, the launch is repeated without it.
+  // runtime refuse it, the launch is repeated without it.
   static bool pdl_ok = true;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   int n = 0;
-  if (a.fused) {
-    attr[n].id = cudaLaunchAttributeCooperative;
-    attr[n].val.cooperative = 1;
-    ++n;
-  }
   if (pdl_ok) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;

@@ -72,7 +72,7 @@ size_t packed_weight_bytes(int E, int N, int Kd, int pair);
 int gemm_block_n(int align);
 // `sched`: gemm_sched_words(U, align) words of the workspace, zero before a launch and left at zero.
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, uint32_t* sched, cudaStream_t stream);
-// L1 and L2 in one cooperative launch.
+// L1 and L2 in one launch (L2 tiles wait for their row block's L1 tiles).
 cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* sched, cudaStream_t stream);
 size_t gemm_sched_words(int U, int align);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
