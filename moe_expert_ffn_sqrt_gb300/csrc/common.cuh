@@ -79,6 +79,9 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 // while the previous kernel of the stream still runs; this waits until that kernel has completed
 // and its memory operations are visible (returns at once for an ordinary launch).
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the stream's next kernel, if launched with programmatic stream serialization, start its
+// CTAs now (they still wait for this kernel's completion before reading its results).
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");

@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
   const int N = a.T * a.K;
   for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
   grid_dependency_wait();                          // topk_ids come from the previous launch
+  grid_launch_dependents();                        // the expert FFN may start its prologue
   int e_mine = -1;
   if (tid < N) {
     e_mine = a.topk_ids[tid];
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
                                                            const uint8_t* __restrict__ x_sf, uint8_t* __restrict__ x_perm,
                                                            uint8_t* __restrict__ x_perm_sf, int bt, int nb) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  grid_launch_dependents();                        // the expert FFN may start its prologue
   const long long pair = static_cast<long long>(blockIdx.x) * 8 + warp;
   if (pair >= static_cast<long long>(T) * K) return;
   const int e = topk_ids[pair];

@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(256) route_small_kernel(const RouteFinishArgs 
   const int nblocks = gridDim.x * gridDim.y;
   const int bid = blockIdx.y * gridDim.x + blockIdx.x;
   const int T = a.T, H = a.H, E = a.E;
+  grid_launch_dependents();        // the permute may start (it waits for this launch's results)
   // the biases are read only by the last CTA, after every other CTA's work: start them towards L2
   if (bid == 0 && warp == 0)
     for (int off = lane * 32; off < E; off += 32 * 32) {     // one 128-byte line per lane and round
