@@ -336,7 +336,20 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
   if (dst < 0) return;                         // dropped by a full BatchedExperts slot
   const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
   uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
-  for (int j = lane; j < H / 16; j += 32) out[j] = src[j];
+  const int chunks = H / 16;
+  for (int j0 = 0; j0 < chunks; j0 += 8 * 32) {      // eight 16-byte loads per lane in flight, then stores
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      if (j < chunks) v[u] = __ldg(src + j);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int j = j0 + u * 32 + lane;
+      if (j < chunks) out[j] = v[u];
+    }
+  }
   const int slabs = H / 128;
   for (int s = lane; s < slabs; s += 32) x_perm_sf[act_sf_offset(bt, nb, dst, s)] = x_sf[static_cast<size_t>(t) * slabs + s];
 }
