@@ -352,6 +352,15 @@ moe_status moe_forward_naive(const uint16_t* hidden, const float* w_gate, const 
                              int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                              int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* Self-test of the device failure path (no counterpart in the method's description): launches one
+ * bounded wait that nothing can satisfy, through the primitives the hot path uses.  mode 0: a
+ * counter that is never incremented (word 32 of the workspace's reserved first 256 bytes, which
+ * stays zero), as the L2-after-L1 waits of the expert FFN; mode 1: an mbarrier phase that never
+ * completes, as the pipeline waits.  After its cycle budget (~2 s) the wait gives up, records
+ * MOE_ERR_TIMEOUT in the status word and the kernel returns: moe_get_error then reports it, and
+ * the context stays usable.  No fault and no unbounded wait is involved. */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int mode, void* stream);
+
 /* Synchronises `stream`, returns the device status word recorded in `ws` through
  * *device_status (MOE_OK if none) and clears it.  The return value reports host errors. */
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status);

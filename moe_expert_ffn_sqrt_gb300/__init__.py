@@ -93,6 +93,8 @@ def lib():
         L.moe_forward_naive.restype = S
         L.moe_forward_naive.argtypes = [P, P, P, P, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P,
                                         Z, P]
+        L.moe_selftest_wait_timeout.restype = S
+        L.moe_selftest_wait_timeout.argtypes = [P, Z, I, P]
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
         L.moe_status_str.restype = ctypes.c_char_p
@@ -410,6 +412,12 @@ def forward_naive(hidden, w_gate, gate_bias, e_score_bias, I, K, score_fn, renor
         _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
         _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"),
         ws.numel(), _stream()), "moe_forward_naive")
+
+
+def selftest_wait_timeout(ws, mode):
+    """One bounded wait that nothing satisfies (0: counter, 1: mbarrier); it records ERR_TIMEOUT."""
+    _check(lib().moe_selftest_wait_timeout(_ptr(ws, torch.uint8, "ws"), ws.numel(), int(mode), _stream()),
+           "moe_selftest_wait_timeout")
 
 
 def get_error(ws):

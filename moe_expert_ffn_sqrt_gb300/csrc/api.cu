@@ -564,6 +564,13 @@ moe_status moe_forward_batched(const uint16_t* hidden, const float* w_gate, cons
                         expert_num_tokens, ws, ws_bytes, stream);
 }
 
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int mode, void* stream) {
+  if (!ws || ws_bytes < kAlign || (mode != 0 && mode != 1)) return MOE_ERR_INVALID_ARG;
+  // word 32 of the reserved first 256 bytes: zero in a zero-filled workspace, never written
+  const uint32_t* never_set = static_cast<const uint32_t*>(ws) + 32;
+  return cuda_status(launch_wait_selftest(never_set, status_of(ws), mode, S(stream)));
+}
+
 moe_status moe_get_error(void* ws, void* stream, moe_status* device_status) {
   if (!ws || !device_status) return MOE_ERR_INVALID_ARG;
   uint32_t v = 0;

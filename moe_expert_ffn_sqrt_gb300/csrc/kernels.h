@@ -102,6 +102,7 @@ cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_
 cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
 
 // reduce.cu
+cudaError_t launch_wait_selftest(const uint32_t* never_set, uint32_t* status, int mode, cudaStream_t stream);
 cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int T, int K,
                                     int H, uint16_t* out, cudaStream_t stream);
 

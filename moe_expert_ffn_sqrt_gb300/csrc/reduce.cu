@@ -45,4 +45,27 @@ cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, 
   return cudaGetLastError();
 }
 
+// Failure-path self-test: one bounded wait that nothing can satisfy, through the same primitives
+// the hot-path kernels use.  Mode 0: a counter that is never incremented (the L2-after-L1 waits);
+// mode 1: an mbarrier phase that never completes (the pipeline waits).  The wait gives up after
+// its cycle budget, records a timeout in the status word and the kernel returns.
+__global__ void wait_selftest_kernel(const uint32_t* never_set, uint32_t* status, int mode) {
+  __shared__ uint64_t bar;
+  if (mode == 0) {
+    if (threadIdx.x == 0) wait_counter(never_set, 1u, status);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, status);
+}
+
+cudaError_t launch_wait_selftest(const uint32_t* never_set, uint32_t* status, int mode, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(never_set, status, mode);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
