@@ -7,12 +7,13 @@
 // though: an E2M1 value times an E4M3 scale has at most 6 significant bits, and an E4M3 activation
 // times its power-of-two scale at most 4.  So this path runs kind::f16 (bf16 x bf16 -> fp32):
 //  * activations are dequantised once per call into bf16 rows (act_to_bf16_kernel);
-//  * a load ring (5 slots) receives each slab's bf16 token rows by TMA and its packed weights
-//    (256 rows x 64 codes + scales) by one bulk copy; ten converter warps turn the packed weights
-//    into a 128-byte-swizzled bf16 tile in a second ring (3 slots; byte-permute table for
-//    E2M1 -> bf16, exact bf16 multiply by the scale) before the MMA warp consumes it;
-//  * two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM) let an item's
-//    MMAs run while four epilogue warps drain the previous item 32 columns at a time;
+//  * a load ring (3 slots) receives each slab's bf16 token rows (one or two row blocks) by TMA and
+//    its packed weights (256 rows x 64 codes + scales) by one bulk copy; ten converter warps turn
+//    the packed weights into a 128-byte-swizzled bf16 tile in a second ring (3 slots; byte-permute
+//    table for E2M1 -> bf16, exact bf16 multiply by the scale) before the MMA warp consumes it;
+//  * two 256-column TMEM accumulators (kind::f16 keeps no scale factors in TMEM) hold two row
+//    blocks of one expert that share each converted tile; four epilogue warps drain them 32
+//    columns at a time;
 //  * the per-expert fp32 tensor scale multiplies the accumulator in the epilogue.
 // Layout and scheduling otherwise follow gemm.cu: M = 128 token rows x N = 256 weight rows, one
 // persistent CTA per SM, TMA producer warp, single-thread MMA issue.
