@@ -16,10 +16,11 @@ constexpr int kGemvE = 4;
 constexpr int kGemvSplit = 4;
 
 // ------------------------------------------------------------------------------------------
-// Top-K above 16 tokens: one warp per token, eight tokens per CTA.  Each lane holds PER = E/32
-// experts in registers: it sums their split partials (fixed split order), scores them and runs K
-// rounds of warp arg-max (ties to the lower expert id).  FP8 activation quantisation (one warp per
-// 128-column group) runs in the blocks after the top-K blocks of the same launch.
+// Top-K: one CTA (256 threads) per token.  Threads sum the split partials of one expert each
+// (independent loads, fixed split order), score, and stage scores/keys in shared memory; warp 0
+// then holds PER = E/32 keys per lane in registers and runs K rounds of warp arg-max (ties to
+// the lower expert id).  FP8 activation quantisation (one warp per 128-column group) runs in
+// the blocks after the top-K blocks of the same launch.
 struct RouteFinishArgs {
   const float* partial;
   int nsplit;
@@ -48,64 +49,70 @@ __device__ __forceinline__ int warp_argmax_id(float key, int id) {
   return static_cast<int>(__reduce_min_sync(0xffffffffu, ok == best ? static_cast<uint32_t>(id) : 0xffffffffu));
 }
 
+__device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  float r = sh[0];
+  for (int w = 1; w < 8; ++w) r = is_max ? fmaxf(r, sh[w]) : r + sh[w];
+  return r;
+}
+
 template <int PER>
 __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs a) {
+  __shared__ float s_score[32 * PER];
+  __shared__ float s_key[32 * PER];
+  __shared__ float s_red[8];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (static_cast<int>(blockIdx.x) < a.topk_blocks) {
-    // one warp per token, PER experts per lane (e = lane + 32 j) in registers
-    const int t = blockIdx.x * 8 + warp;
-    if (t >= a.T) return;
-    float s[PER], key[PER];
+    const int t = blockIdx.x;
+    // logits: one expert per thread per pass, splits summed in a fixed order
     float lmax = -INFINITY;
-    // logits: the split partial sums in a fixed order (groups of four, then the rest); every load
-    // of the pass is issued before any store
-#pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane + 32 * j;
+    for (int e = threadIdx.x; e < 32 * PER; e += 256) {
       float l = -INFINITY;
       if (e < a.E) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         int sp = 0;
         for (; sp + 4 <= a.nsplit; sp += 4)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] += __ldcg(a.partial + (static_cast<size_t>(sp + u) * a.T + t) * a.E + e);
+          for (int u = 0; u < 4; ++u) v[u] += a.partial[(static_cast<size_t>(sp + u) * a.T + t) * a.E + e];
         l = (v[0] + v[1]) + (v[2] + v[3]);
-        for (; sp < a.nsplit; ++sp) l += __ldcg(a.partial + (static_cast<size_t>(sp) * a.T + t) * a.E + e);
-        if (a.gate_bias) l += __ldg(a.gate_bias + e);
+        for (; sp < a.nsplit; ++sp) l += a.partial[(static_cast<size_t>(sp) * a.T + t) * a.E + e];
+        if (a.gate_bias) l += a.gate_bias[e];
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * a.E + e] = l;
       }
-      s[j] = l;
+      s_score[e] = l;
       lmax = fmaxf(lmax, l);
     }
-    if (a.logits_out) {
-#pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if (lane + 32 * j < a.E) a.logits_out[static_cast<size_t>(t) * a.E + lane + 32 * j] = s[j];
-    }
     if (a.score_fn == 0) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, off));
+      lmax = block_reduce(lmax, s_red, true);
       float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        s[j] = (lane + 32 * j < a.E) ? expf(s[j] - lmax) : 0.f;
-        sum += s[j];
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
+        const float p = (e < a.E) ? expf(s_score[e] - lmax) : 0.f;
+        s_score[e] = p;
+        sum += p;
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-#pragma unroll
-      for (int j = 0; j < PER; ++j) s[j] = s[j] / sum;
+      sum = block_reduce(sum, s_red, false);
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) s_score[e] = s_score[e] / sum;
     } else {
-#pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const float l = s[j];
-        s[j] = (lane + 32 * j < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
+        const float l = s_score[e];
+        s_score[e] = (e < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
       }
     }
+    for (int e = threadIdx.x; e < 32 * PER; e += 256)
+      s_key[e] = (e < a.E) ? s_score[e] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
+    __syncthreads();
+    if (warp != 0) return;
+    float key[PER];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = (e < a.E) ? s[j] + (a.e_bias ? __ldg(a.e_bias + e) : 0.f) : -INFINITY;
-    }
+    for (int j = 0; j < PER; ++j) key[j] = s_key[lane + 32 * j];
     float wsum = 0.f, wmine = 0.f;
     for (int k = 0; k < a.K; ++k) {
       float bk = -INFINITY;
@@ -119,16 +126,11 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
         }
       }
       bi = warp_argmax_id(bk, bi);
-      float sw = 0.f;
-      const bool won = (bi & 31) == lane;   // selects with compile-time indices keep s[], key[] in registers
+      const bool won = (bi & 31) == lane;   // selects with compile-time indices keep key[] in registers
       const int jw = bi >> 5;
 #pragma unroll
-      for (int j = 0; j < PER; ++j) {
-        const bool hit = won && j == jw;
-        sw = hit ? s[j] : sw;
-        key[j] = hit ? -INFINITY : key[j];
-      }
-      sw = __shfl_sync(0xffffffffu, sw, bi & 31);
+      for (int j = 0; j < PER; ++j) key[j] = (won && j == jw) ? -INFINITY : key[j];
+      const float sw = s_score[bi];
       wsum += sw;
       if (lane == k) wmine = sw;
       if (lane == 0) a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
@@ -443,7 +445,7 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
   a.hidden = hidden;
   a.x_q = x_q;
   a.x_sf = x_sf;
-  a.topk_blocks = (T + 7) / 8;      // route_finish_kernel: one warp per token
+  a.topk_blocks = T;
   a.nv = NaiveLayout{};
   if (nv) {
     if (T > kGemvT) return cudaErrorInvalidValue;
@@ -461,7 +463,7 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
     if (err != cudaSuccess) return err;
   }
   const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;
-  const int blocks = a.topk_blocks + static_cast<int>((qgroups + 7) / 8);
+  const int blocks = T + static_cast<int>((qgroups + 7) / 8);
   const int per = (E + 31) / 32;
   if (per <= 1) route_finish_kernel<1><<<blocks, 256, 0, stream>>>(a);
   else if (per <= 2) route_finish_kernel<2><<<blocks, 256, 0, stream>>>(a);
