@@ -130,3 +130,39 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"(import|from)\s+oracle|oracle/", src), f
+
+
+def test_variant_entry_points_reject_invalid_arguments(M):
+    L = M.lib()
+    fake = ctypes.c_void_p(0x10000)     # never dereferenced: validation fails first
+    ws = ctypes.c_void_p(0x20000)
+    n = ctypes.c_size_t(0)
+    # BatchedExperts slot sizes: powers of two in [1, 4096]
+    for bad in (0, 3, 8192):
+        assert L.moe_workspace_size_batched(8, 512, 256, 16, 4, bad, ctypes.byref(n)) == M.ERR_INVALID_ARG
+        assert L.moe_batched_align(8, 4, 16, bad) == 0
+    assert L.moe_workspace_size_batched(8, 512, 256, 16, 4, 16, ctypes.byref(n)) == M.OK and n.value > 0
+    # the row-block height: the slot below 16 rows, else 64 (128 once experts average > 64 tokens)
+    assert [L.moe_batched_align(8, 4, 16, s) for s in (1, 8, 16, 32, 64, 128, 4096)] == [1, 8, 16, 32, 64, 64, 64]
+    assert L.moe_batched_align(4096, 6, 256, 4096) == 128
+    assert L.moe_permute_batched(fake, 8, 2, 16, 12, fake, fake, fake, fake, None, None, None, 0, None, None, ws,
+                                 1 << 20, None) == M.ERR_INVALID_ARG
+    w13 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 2)
+    w2 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 256, 1)
+    # a slot smaller than the batch
+    assert L.moe_forward_batched(fake, fake, None, None, 9, 512, 256, 16, 4, 8, 0, 1, w13, w2, fake, None, None, None,
+                                 None, None, None, None, ws, 1 << 30, None) == M.ERR_INVALID_ARG
+    # the tiny-batch path: at most 16 tokens and T*K <= E
+    assert L.moe_forward_naive(fake, fake, None, None, 17, 512, 256, 1024, 4, 0, 1, w13, w2, fake, None, None, None,
+                               None, None, None, ws, 1 << 30, None) == M.ERR_UNSUPPORTED
+    assert L.moe_forward_naive(fake, fake, None, None, 5, 512, 256, 16, 4, 0, 1, w13, w2, fake, None, None, None,
+                               None, None, None, ws, 1 << 30, None) == M.ERR_UNSUPPORTED
+    assert L.moe_route_naive(fake, fake, None, None, 5, 512, 16, 4, 0, 1, fake, fake, fake, fake, fake, fake, fake,
+                             fake, ws, 1 << 20, None) == M.ERR_UNSUPPORTED
+    # weighted L1 needs both the row ids and the weights
+    assert L.moe_grouped_gemm_l1_swiglu_weighted(fake, fake, fake, fake, None, fake, 8, 2, 512, 256, 16, 16, w13,
+                                                 fake, fake, ws, 1 << 20, None) == M.ERR_INVALID_ARG
+    # failure-path self-test: workspace and mode checked on the host
+    assert L.moe_selftest_wait_timeout(None, 256, 0, None) == M.ERR_INVALID_ARG
+    assert L.moe_selftest_wait_timeout(ws, 128, 0, None) == M.ERR_INVALID_ARG
+    assert L.moe_selftest_wait_timeout(ws, 256, 2, None) == M.ERR_INVALID_ARG
