@@ -16,14 +16,11 @@ constexpr int kGemvE = 4;
 constexpr int kGemvSplit = 4;
 
 // ------------------------------------------------------------------------------------------
-// Top-K above 16 tokens: one CTA of kFinishThreads per token.  Each thread sums the split partials
-// of its E / kFinishThreads experts (every load issued before any store, fixed split order),
-// scores them and stages scores/keys in shared memory; warp 0 then holds PER = E/32 keys per lane
-// in registers and runs K rounds of warp arg-max (ties to the lower expert id).  FP8 activation
-// quantisation (one warp per 128-column group) runs in the blocks after the top-K blocks of the
-// same launch.  Small CTAs keep many tokens resident per SM.
-constexpr int kFinishThreads = 64;
-constexpr int kFinishWarps = kFinishThreads / 32;
+// Top-K: one CTA (256 threads) per token.  Threads sum the split partials of one expert each
+// (independent loads, fixed split order), score, and stage scores/keys in shared memory; warp 0
+// then holds PER = E/32 keys per lane in registers and runs K rounds of warp arg-max (ties to
+// the lower expert id).  FP8 activation quantisation (one warp per 128-column group) runs in
+// the blocks after the top-K blocks of the same launch.
 struct RouteFinishArgs {
   const float* partial;
   int nsplit;
@@ -63,64 +60,54 @@ __device__ __forceinline__ float block_reduce(float v, float* sh, bool is_max) {
   if (lane == 0) sh[warp] = v;
   __syncthreads();
   float r = sh[0];
-  for (int w = 1; w < kFinishWarps; ++w) r = is_max ? fmaxf(r, sh[w]) : r + sh[w];
+  for (int w = 1; w < 8; ++w) r = is_max ? fmaxf(r, sh[w]) : r + sh[w];
   return r;
 }
 
 template <int PER>
-__global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(const RouteFinishArgs a) {
-  constexpr int kPerThread = (32 * PER + kFinishThreads - 1) / kFinishThreads;   // experts per thread
+__global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs a) {
   __shared__ float s_score[32 * PER];
   __shared__ float s_key[32 * PER];
-  __shared__ float s_red[kFinishWarps];
+  __shared__ float s_red[8];
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (static_cast<int>(blockIdx.x) < a.topk_blocks) {
     const int t = blockIdx.x;
-    // logits: experts e = threadIdx.x + kFinishThreads i, splits summed in a fixed order; all of a
-    // thread's loads come before its stores (which the compiler may not move loads across)
-    float lv[kPerThread];
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const int e = threadIdx.x + kFinishThreads * i;
+    // logits: one expert per thread per pass, splits summed in a fixed order
+    float lmax = -INFINITY;
+    for (int e = threadIdx.x; e < 32 * PER; e += 256) {
       float l = -INFINITY;
       if (e < a.E) {
         float v[4] = {0.f, 0.f, 0.f, 0.f};
         int sp = 0;
         for (; sp + 4 <= a.nsplit; sp += 4)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] += __ldcg(a.partial + (static_cast<size_t>(sp + u) * a.T + t) * a.E + e);
+          for (int u = 0; u < 4; ++u) v[u] += a.partial[(static_cast<size_t>(sp + u) * a.T + t) * a.E + e];
         l = (v[0] + v[1]) + (v[2] + v[3]);
-        for (; sp < a.nsplit; ++sp) l += __ldcg(a.partial + (static_cast<size_t>(sp) * a.T + t) * a.E + e);
-        if (a.gate_bias) l += __ldg(a.gate_bias + e);
+        for (; sp < a.nsplit; ++sp) l += a.partial[(static_cast<size_t>(sp) * a.T + t) * a.E + e];
+        if (a.gate_bias) l += a.gate_bias[e];
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * a.E + e] = l;
       }
-      lv[i] = l;
-    }
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-      const int e = threadIdx.x + kFinishThreads * i;
-      if (e < 32 * PER) s_score[e] = lv[i];
-      if (a.logits_out && e < a.E) a.logits_out[static_cast<size_t>(t) * a.E + e] = lv[i];
-      lmax = fmaxf(lmax, lv[i]);
+      s_score[e] = l;
+      lmax = fmaxf(lmax, l);
     }
     if (a.score_fn == 0) {
       lmax = block_reduce(lmax, s_red, true);
       float sum = 0.f;
-      for (int e = threadIdx.x; e < 32 * PER; e += kFinishThreads) {
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
         const float p = (e < a.E) ? expf(s_score[e] - lmax) : 0.f;
         s_score[e] = p;
         sum += p;
       }
       sum = block_reduce(sum, s_red, false);
-      for (int e = threadIdx.x; e < 32 * PER; e += kFinishThreads) s_score[e] = s_score[e] / sum;
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) s_score[e] = s_score[e] / sum;
     } else {
-      for (int e = threadIdx.x; e < 32 * PER; e += kFinishThreads) {
+      for (int e = threadIdx.x; e < 32 * PER; e += 256) {
         const float l = s_score[e];
         s_score[e] = (e < a.E) ? sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l)))) : 0.f;
       }
     }
-    for (int e = threadIdx.x; e < 32 * PER; e += kFinishThreads)
-      s_key[e] = (e < a.E) ? s_score[e] + (a.e_bias ? __ldg(a.e_bias + e) : 0.f) : -INFINITY;
+    for (int e = threadIdx.x; e < 32 * PER; e += 256)
+      s_key[e] = (e < a.E) ? s_score[e] + (a.e_bias ? a.e_bias[e] : 0.f) : -INFINITY;
     __syncthreads();
     if (warp != 0) return;
     float key[PER];
@@ -153,7 +140,7 @@ __global__ void __launch_bounds__(kFinishThreads) route_finish_kernel(const Rout
   }
   // FP8 activation quantisation: group g of token t = 128 columns, 4 per lane.
   const int gpt = a.H / 128;
-  const long long gidx = static_cast<long long>(blockIdx.x - a.topk_blocks) * kFinishWarps + warp;
+  const long long gidx = static_cast<long long>(blockIdx.x - a.topk_blocks) * 8 + warp;
   if (gidx >= static_cast<long long>(a.T) * gpt) return;
   const int t = static_cast<int>(gidx / gpt), g = static_cast<int>(gidx % gpt);
   const size_t base = static_cast<size_t>(t) * a.H + g * 128 + lane * 4;
@@ -476,14 +463,14 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
     if (err != cudaSuccess) return err;
   }
   const long long qgroups = (x_q != nullptr) ? static_cast<long long>(T) * (H / 128) : 0;
-  const int blocks = T + static_cast<int>((qgroups + kFinishWarps - 1) / kFinishWarps);
+  const int blocks = T + static_cast<int>((qgroups + 7) / 8);
   const int per = (E + 31) / 32;
-  if (per <= 1) route_finish_kernel<1><<<blocks, kFinishThreads, 0, stream>>>(a);
-  else if (per <= 2) route_finish_kernel<2><<<blocks, kFinishThreads, 0, stream>>>(a);
-  else if (per <= 4) route_finish_kernel<4><<<blocks, kFinishThreads, 0, stream>>>(a);
-  else if (per <= 8) route_finish_kernel<8><<<blocks, kFinishThreads, 0, stream>>>(a);
-  else if (per <= 16) route_finish_kernel<16><<<blocks, kFinishThreads, 0, stream>>>(a);
-  else route_finish_kernel<32><<<blocks, kFinishThreads, 0, stream>>>(a);
+  if (per <= 1) route_finish_kernel<1><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 2) route_finish_kernel<2><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 4) route_finish_kernel<4><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 8) route_finish_kernel<8><<<blocks, 256, 0, stream>>>(a);
+  else if (per <= 16) route_finish_kernel<16><<<blocks, 256, 0, stream>>>(a);
+  else route_finish_kernel<32><<<blocks, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
