@@ -18,9 +18,10 @@
 //    one expert; otherwise each expert in the block is a separate pass with masked stores.
 //  * moe_forward runs L1 and L2 as one launch: L2 items wait (bounded) on per-row-block counters of
 //    finished L1 tiles, so the L1 tail wave and the launch gap are filled with L2 work.
-//  * Persistent CTAs (one per SM) walk the items in a fixed order; a producer warp (TMA), an MMA
-//    warp (one thread issues tcgen05.cp + tcgen05.mma) and eight epilogue warps run decoupled
-//    through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
+//  * Persistent CTAs (one per SM) draw the items in index order from a counter in the workspace
+//    (BatchedExperts: only the row blocks that hold tokens, from expert_num_tokens); a producer
+//    warp (TMA), an MMA warp (one thread issues tcgen05.cp + tcgen05.mma) and eight epilogue
+//    warps run decoupled through mbarriers.  The 128x256 fp32 accumulator takes half of TMEM and is single-buffered;
 //    the shared-memory ring keeps the weights streaming while the epilogue drains it.
 //  * Weights come pre-packed (moe_pack_weights): per (expert, tile, 128-deep slab) one chunk of
 //    256 rows of FP4 codes followed by two 512-byte scale images.  The codes are loaded with the
@@ -680,9 +681,9 @@ template <int BN>
 static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   GemmArgs a{};
-  CUtensorMap m[4];
+  CUtensorMap m[4] = {};
+  if (!sched || (!l1 && !l2)) return cudaErrorInvalidValue;
   const GemmLaunch& any = l1 ? *l1 : *l2;
-  if (!sched) return cudaErrorInvalidValue;
   if (l1 && !make_phase<BN>(*l1, true, a.ph[0], m[0], m[1])) return cudaErrorInvalidValue;
   if (l2 && !make_phase<BN>(*l2, false, a.ph[1], m[2], m[3])) return cudaErrorInvalidValue;
   if (!l1) {
