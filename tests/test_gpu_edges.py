@@ -8,6 +8,7 @@ permute's index outputs bit for bit where the routing agrees, and every token's 
   * E = 3 (not a multiple of 32) with K = 2 and align 1;
   * K = 1, and H = 384 (the last W2 tile is a half tile of 128 rows), I = 128 (one W13 tile);
   * NVFP4 at H = 384;
+  * T = 32 and 33, either side of the reduce moving out of the L2 epilogue;
 plus the three variants (BatchedExperts, tiny batch, weights in L1) on the E = 1024 case.
 """
 import numpy as np
@@ -29,6 +30,9 @@ CASES = {
     "K1_H384_I128": dict(T=5, H=384, I=128, E=64, K=1, align=4, score_fn="sqrt_softplus", e_bias=True, seed=24),
     "nvfp4_H384": dict(T=9, H=384, I=256, E=32, K=4, align=8, score_fn="sqrt_softplus", e_bias=True, fmt="nvfp4",
                        seed=25),
+    # the reduce runs in the L2 epilogue up to 32 tokens, as a separate kernel above
+    "T32_fused_reduce": dict(T=32, H=512, I=256, E=16, K=4, align=16, score_fn="softmax", seed=26),
+    "T33_separate_reduce": dict(T=33, H=512, I=256, E=16, K=4, align=16, score_fn="softmax", seed=27),
 }
 
 

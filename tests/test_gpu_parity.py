@@ -94,7 +94,11 @@ def test_act_quant_edge_values(M):
 @pytest.mark.parametrize("T,K,E,align,skew", [(8, 6, 256, 16, 0.0), (128, 6, 256, 64, 1.0), (3, 2, 3, 1, 0.0),
                                               (37, 4, 16, 16, 0.5), (500, 8, 64, 2, 1.5), (4096, 6, 256, 256, 0.0),
                                               (3000, 6, 256, 128, 1.2), (1, 1, 1, 1, 0.0), (171, 6, 32, 4, 0.7),
-                                              (2000, 8, 1024, 16, 1.0)])
+                                              (2000, 8, 1024, 16, 1.0),
+                                              # kernel boundaries: row copy inside the small kernel up to
+                                              # 128 pairs, the small kernel up to 1024 pairs
+                                              (32, 4, 16, 16, 0.3), (43, 3, 16, 16, 0.3), (256, 4, 64, 8, 0.5),
+                                              (205, 5, 64, 8, 0.5)])
 def test_permute_parity(M, T, K, E, align, skew):
     rng = np.random.default_rng(T * 31 + E)
     ids = synth.topk_ids_random(rng, T, E, K, skew)
