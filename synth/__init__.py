@@ -26,6 +26,11 @@ Distributions:
 * NVFP4 weights: same E2M1 codes; each per-16 E4M3 scale code is uniform in
   [0x30, 0x48) (0.5 .. 3.75); one float32 tensor scale per expert matrix,
   uniform in [0.0058, 0.0068), for the same RMS.
+* INT8 weights (any workload with ``fmt="int8"``): int8 codes in [-127, 127]
+  with probabilities proportional to exp(-c**2 / (2 * 40**2)) (a discretised
+  normal of spread 40, drawn through a 16-bit lookup table), and one float32
+  scale per output channel uniform in [4.5e-4, 5.5e-4), again an RMS of
+  about 0.02.
 Each expert's weights come from their own generator, seeded by
 (seed, matrix, expert), so any expert can be regenerated alone.
 """
@@ -48,7 +53,7 @@ class Workload:
     K: int
     align: int
     score_fn: str            # "softmax" or "sqrt_softplus"
-    fmt: str                 # "mxfp4" or "nvfp4"
+    fmt: str                 # "mxfp4", "nvfp4" or "int8"
     e_bias: bool             # e_score_correction_bias present
     gate_offset: str         # "none", "normal" (N(0,1) per expert), "zipf"
     gate_uniform: bool = False
@@ -102,6 +107,29 @@ def fp4_codes(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     return _BYTE[r].reshape(rows, cols // 2)
 
 
+def _i8_lut() -> np.ndarray:
+    """uint16 draw -> int8 code with probabilities proportional to exp(-c^2 / (2 * 40^2)), |c| <= 127."""
+    c = np.arange(-127, 128)
+    cum = np.cumsum(np.exp(-(c / 40.0) ** 2 / 2.0))
+    cum *= 65536.0 / cum[-1]
+    idx = np.searchsorted(cum, np.arange(65536) + 0.5, side="right")
+    return c[np.minimum(idx, c.size - 1)].astype(np.int8)
+
+
+_I8 = _i8_lut()
+
+
+def i8_codes(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
+    """[rows, cols] int8 weight codes (discretised normal, spread 40)."""
+    r = np.frombuffer(rng.bytes(2 * rows * cols), dtype=np.uint16)
+    return _I8[r].reshape(rows, cols)
+
+
+def i8_channel_scales(rng: np.random.Generator, rows: int) -> np.ndarray:
+    """[rows] float32 per-output-channel scales uniform in [4.5e-4, 5.5e-4)."""
+    return rng.uniform(4.5e-4, 5.5e-4, size=rows).astype(np.float32)
+
+
 def mx_scales(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
     """[rows, cols/32] UE8M0 bytes, 120 or 121 (2**-7 or 2**-6)."""
     return (120 + rng.integers(0, 2, size=(rows, cols // 32), dtype=np.uint8)).astype(np.uint8)
@@ -113,10 +141,19 @@ def nv_scales(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
 
 
 def expert_weights(w: Workload, e: int) -> dict:
-    """Weights of expert e in the logical layouts: W13 [2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [H, I]."""
+    """Weights of expert e in the logical layouts: W13 [2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [H, I].
+
+    FP4 formats: ``*_q`` packed E2M1 [N, Kd/2], ``*_sf`` block scales, ``*_ts`` NVFP4 tensor scale.
+    INT8: ``*_q`` int8 [N, Kd], ``*_sf`` float32 channel scales [N], ``*_ts`` None.
+    """
     out = {}
     for mat, (rows, cols) in (("w13", (2 * w.I, w.H)), ("w2", (w.H, w.I))):
         rng = _rng(w.seed, 1 if mat == "w13" else 2, e)
+        if w.fmt == "int8":
+            out[mat + "_q"] = i8_codes(rng, rows, cols)
+            out[mat + "_sf"] = i8_channel_scales(rng, rows)
+            out[mat + "_ts"] = None
+            continue
         out[mat + "_q"] = fp4_codes(rng, rows, cols)
         if w.fmt == "mxfp4":
             out[mat + "_sf"] = mx_scales(rng, rows, cols)
