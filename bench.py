@@ -35,16 +35,23 @@ SPIN_CYCLES = 1_000_000      # ~0.5 ms at 2 GHz, outside the timed events
 
 
 def launches_per_forward(w, naive=False):
-    """Kernel launches of one moe_forward, mirroring the library's dispatch."""
-    route = 1 if w.T <= 16 else 2                 # fused small-batch route, else gate GEMM + top-K
-    permute = 1 if w.T * w.K <= 128 else 2        # permute with the row copy in the same launch, else + copy
+    """Kernel launches of one forward call, mirroring the library's dispatch."""
+    tk = w.T * w.K
+    route = 1 if w.T <= 16 else 3                 # fused small-batch route, else gate split + gate GEMM + top-K
+    reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue
+    if w.fmt == "int8":
+        # route, per-token act quant, permute indices (one kernel up to 1024 pairs, else count + place),
+        # then the row gather to fp16, L1, the per-row h requant and L2
+        return route + 1 + (1 if tk <= 1024 else 2) + 4 + reduce
+    # permute: the row copy inside the small kernel up to 128 pairs, else a copy kernel after the
+    # small kernel (up to 1024 pairs) or after count + place
+    permute = 1 if tk <= 128 else (2 if tk <= 1024 else 3)
     if naive:
         permute = 0                               # the routing launch writes the tiny-batch layout
     if w.fmt == "mxfp4":
         ffn = 1                                   # L1 and L2 in one launch
     else:
         ffn = 4                                   # bf16 activation rows + GEMM, for L1 and for L2
-    reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue
     return route + permute + ffn + reduce
 
 
@@ -66,6 +73,9 @@ def parse_args():
     p.add_argument("--weights-in-l1", action="store_true",
                    help="apply the routing weights in the L1 epilogue and sum without weights "
                         "(moe_forward_l1_weighted) instead of weighting in the reduce")
+    p.add_argument("--weights", default="workload", choices=["workload", "int8"],
+                   help="the workload's FP4 weight format, or the INT8 variant (int8 weights with per-channel "
+                        "scales, int8 activations with per-token scales: moe_forward_i8) on the same shapes")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
                         "BatchedExperts slots of max_tokens = max(16, the smallest power of two >= T) (moe_forward_batched) or "
@@ -78,8 +88,10 @@ def world():
 
 
 def workload_config(w):
+    acts = ("INT8 activations (fp32 scale per token)" if w.fmt == "int8" else "FP8 E4M3 activations (UE8M0/128)")
+    wts = "INT8 weights (fp32 scale per channel)" if w.fmt == "int8" else f"{w.fmt.upper()} weights"
     return {"workload": f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} K={w.K} align={w.align} "
-                        f"{w.score_fn} {w.fmt.upper()} weights, FP8 E4M3 activations (UE8M0/128)",
+                        f"{w.score_fn} {wts}, {acts}",
             "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K, "align": w.align, "weights": w.fmt}
 
 
@@ -161,14 +173,25 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------------ CPU oracle
 
+def oracle_forward(w):
+    """The oracle's whole-layer function for the workload's weight format, as f(inp, prov, tokens)."""
+    if w.fmt == "int8":
+        from oracle import int8 as QI
+        return lambda inp, prov, tokens: QI.forward_i8(inp, prov, w.K, w.align, w.score_fn, w.renormalize,
+                                                       tokens=tokens)
+    from oracle import moe as O
+    return lambda inp, prov, tokens: O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize,
+                                               tokens=tokens)
+
+
 def oracle_tokens_per_s(w, inp, stack, budget_s, max_tokens=None):
     """Times the float64 oracle on whole tokens of the workload until the budget is spent."""
-    from oracle import moe as O
+    fwd = oracle_forward(w)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
     done, t0 = 0, time.perf_counter()
     order = list(range(w.T))
     while done < len(order) and (max_tokens is None or done < max_tokens):
-        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[order[done]])
+        fwd(inp, prov, [order[done]])
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -183,19 +206,19 @@ def run_reference(args, w):
         return
     inp = synth.layer_inputs(w)
     stack = synth.all_expert_weights(w)
-    from oracle import moe as O
+    fwd = oracle_forward(w)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
     # warm-up (at most one step: each oracle step is seconds long), then as many timed steps as fit
     # the time budget, at most --steps; the line reports the number actually run
     t0 = time.perf_counter()
     for i in range(min(args.warmup, 1)):
-        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
+        fwd(inp, prov, [i % w.T])
     est = max(time.perf_counter() - t0, 1e-3)
     steps = max(1, min(args.steps, int(args.ref_seconds / est)))
     times = []
     for i in range(steps):
         t0 = time.perf_counter()
-        O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=[i % w.T])
+        fwd(inp, prov, [i % w.T])
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     value = 1e3 / ms
@@ -215,6 +238,14 @@ def run_reference(args, w):
 def algorithmic_bytes(w, n_touched):
     """Bytes the method must move per launch of each stage (padding and untouched experts excluded)."""
     TK = w.T * w.K
+    if w.fmt == "int8":
+        # int8 codes + fp32 channel scales; activations int8 + one fp32 scale per row
+        w13 = n_touched * (2 * w.I * w.H + 2 * w.I * 4)
+        w2 = n_touched * (w.H * w.I + w.H * 4)
+        l1 = w13 + TK * (w.H + 4) + TK * (w.I + 4)
+        l2 = w2 + TK * (w.I + 4) + TK * w.H * 2
+        return {"l1": l1, "l2": l2, "ffn": w13 + w2 + TK * (w.H + 4) + TK * w.H * 2,
+                "layer": w13 + w2 + 4 * w.E * w.H + 2 * w.T * w.H * 2}
     if w.fmt == "mxfp4":
         w13 = n_touched * (2 * w.I * w.H // 2 + 2 * w.I * w.H // 32)
         w2 = n_touched * (w.H * w.I // 2 + w.H * w.I // 32)
@@ -228,6 +259,9 @@ def algorithmic_bytes(w, n_touched):
 
 
 def kernel_name(stage, fmt):
+    if fmt == "int8":
+        return {"ffn": "INT8 L1 (row gather, GEMM, h requant) then L2 (h to fp16, GEMM)",
+                "l1": "INT8 L1 (row gather, GEMM, h requant)", "l2": "INT8 L2 (h to fp16, GEMM)"}[stage]
     if stage == "ffn":
         return "L1+L2 grouped GEMM (one launch)" if fmt == "mxfp4" else "L1 then L2 grouped GEMM"
     return f"{stage} grouped GEMM"
@@ -253,10 +287,15 @@ def run_ours(args, w):
     def d(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]), w.fmt,
-                   pair=2)
-    w2 = M.Weight(d(stack["w2_q"]), d(stack["w2_sf"]), None if stack["w2_ts"] is None else d(stack["w2_ts"]), w.fmt,
-                  pair=1)
+    i8 = w.fmt == "int8"
+    if i8:      # int8 codes; the per-channel scales travel as the weight's tscale
+        w13 = M.Weight(d(stack["w13_q"]), None, d(stack["w13_sf"]), "int8", pair=2)
+        w2 = M.Weight(d(stack["w2_q"]), None, d(stack["w2_sf"]), "int8", pair=1)
+    else:
+        w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]),
+                       w.fmt, pair=2)
+        w2 = M.Weight(d(stack["w2_q"]), d(stack["w2_sf"]), None if stack["w2_ts"] is None else d(stack["w2_ts"]), w.fmt,
+                      pair=1)
     T = w.T
     hidden_host = torch.from_numpy(inp["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hidden = hidden_host.to(dev)
@@ -269,6 +308,8 @@ def run_ours(args, w):
     S = max(16, 1 << max(0, (T - 1).bit_length()))
     if batched:
         ws = M.new_workspace_batched(T, w.H, w.I, w.E, w.K, S, device=dev)
+    elif i8:
+        ws = M.new_workspace_i8(T, w.H, w.I, w.E, w.K, w.align, device=dev)
     else:
         ws = M.new_workspace(T, w.H, w.I, w.E, w.K, M.NAIVE_ROWS if naive else w.align, device=dev)
     out = torch.empty(T, w.H, dtype=torch.bfloat16, device=dev)
@@ -276,7 +317,10 @@ def run_ours(args, w):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)     # > L2 (126 MB)
 
     def step():
-        if naive:
+        if i8:
+            M.forward_i8(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out,
+                         ws)
+        elif naive:
             M.forward_naive(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.score_fn, w.renormalize, w13, w2, out, ws)
         elif batched:
             M.forward_batched(hidden, w_gate, gate_bias, e_bias, w.I, w.K, S, w.score_fn, w.renormalize, w13, w2, out,
@@ -338,10 +382,17 @@ def run_ours(args, w):
     hq = torch.empty(U, w.I, dtype=torch.uint8, device=dev)
     hsf = torch.empty(M.act_sf_tiled_bytes(U, w.I // 128, align), dtype=torch.uint8, device=dev)
     y = torch.empty(U, w.H, dtype=torch.bfloat16, device=dev)
+    if i8:
+        xq8 = torch.empty(T, w.H, dtype=torch.int8, device=dev)
+        xs8 = torch.empty(T, dtype=torch.float32, device=dev)
+        hq8 = torch.empty(U, w.I, dtype=torch.int8, device=dev)
+        hs8 = torch.empty(U, dtype=torch.float32, device=dev)
     # MXFP4: the expert FFN is one launch (moe_grouped_ffn), timed as one stage; NVFP4: L1 and L2 apart
     # (BatchedExperts: the whole FFN through moe_grouped_ffn_batched, whose row-map kernel from the
     # per-expert counts is counted in the stage; moe_forward_batched takes the row map from the permute)
     # (tiny-batch layout: routing and layout are one stage, moe_route_naive)
+    # (INT8: the routing stage includes the per-token quantisation, L1 the row gather and the h requant,
+    # L2 the conversion of h to fp16 rows)
     fused = w.fmt == "mxfp4" or batched
     stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
     if naive:
@@ -359,12 +410,17 @@ def run_ours(args, w):
         if naive:
             M.route_naive(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, srt, eids, inv,
                           msum, xp, xpsf, ws)
+        elif i8:
+            M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws)
+            M.act_quant_i8(hidden, xq8, xs8)
         else:
             M.route(hidden, w_gate, gate_bias, e_bias, w.K, w.score_fn, w.renormalize, ids, tw, ws, x_q=xq, x_sf=xsf)
         j += 1
         e[j].record()
         if naive:
             pass
+        elif i8:
+            M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt)
         elif batched:
             M.permute_batched(ids, w.E, S, srt, eids, inv, msum, ws, expert_num_tokens=cnt, x_q=xq, x_sf=xsf,
                               x_perm=xp, x_perm_sf=xpsf)
@@ -374,7 +430,12 @@ def run_ours(args, w):
         if not naive:
             j += 1
             e[j].record()
-        if batched:
+        if i8:
+            M.grouped_gemm_l1_swiglu_i8(xq8, xs8, srt, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq8, hs8, ws)
+            j += 1
+            e[j].record()
+            M.grouped_gemm_l2_i8(hq8, hs8, eids, msum, T, w.K, w.H, w.I, w.E, align, w2, y, ws)
+        elif batched:
             M.grouped_ffn_batched(xp, xpsf, cnt, T, w.K, w.H, w.I, w.E, S, w13, w2, hq, hsf, y, ws)
         elif fused:
             M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, w2, hq, hsf, y, ws)
@@ -398,14 +459,15 @@ def run_ours(args, w):
     hbm, bf16, peak_src = peaks()
     top = "ffn" if fused else max(("l1", "l2"), key=lambda s: stage_ms[s])
     top_key = f"{w.name}:{top}" + (":batched" if batched else "")
-    kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc", "gemm.cu" if w.fmt == "mxfp4" else "gemm_nv.cu")
+    kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc",
+                               {"mxfp4": "gemm.cu", "nvfp4": "gemm_nv.cu", "int8": "gemm_i8.cu"}[w.fmt])
     tk = w.T * w.K
     flops = {"l1": 2.0 * tk * 2 * w.I * w.H, "l2": 2.0 * tk * w.I * w.H}
     flops["ffn"] = flops["l1"] + flops["l2"]
     # The binding roofline is the one whose minimum time is longer: the kernel's algorithmic bytes at
     # the measured HBM copy bandwidth, or its useful FLOPs at the tensor peak.  MXFP4 runs FP8 x FP4
     # block-scaled MMAs (FP8 rate: the measured bf16 peak x the nominal 4.5/2.25 ratio); NVFP4 runs
-    # bf16 MMAs (the measured bf16 peak).
+    # bf16 MMAs and INT8 fp16 MMAs (the measured bf16 peak; fp16 runs at the bf16 rate).
     peak_t = bf16 * (2.0 if w.fmt == "mxfp4" else 1.0)
     sec = stage_ms[top] / 1e3
     hbm_frac = ab[top] / sec / 1e9 / hbm
@@ -461,7 +523,9 @@ def run_ours(args, w):
         line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None,
-                "dtype": "fp8xfp4 (fp32 accumulate)" if w.fmt == "mxfp4" else "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
+                "dtype": {"mxfp4": "fp8xfp4 (fp32 accumulate)",
+                          "nvfp4": "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
+                          "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)"}[w.fmt],
                 "data": "synthetic (seeded)",
                 "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": launches_per_forward(w, naive) * K, "clocks": clk}
@@ -475,7 +539,12 @@ def main():
     args = parse_args()
     if args.weights_in_l1 and args.layout != "contiguous":
         raise SystemExit("--weights-in-l1 applies to the expert-contiguous layout")
+    if args.weights == "int8" and (args.weights_in_l1 or args.layout != "contiguous"):
+        raise SystemExit("--weights int8 runs the expert-contiguous layout with the weights applied in the reduce")
     w = synth.WORKLOADS[args.workload]
+    if args.weights == "int8":
+        import dataclasses
+        w = dataclasses.replace(w, fmt="int8", name=f"{w.name}-int8")
     if args.experts or args.tokens:
         import dataclasses
         E = args.experts or w.E

@@ -60,11 +60,13 @@ typedef enum {
 
 typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score_fn;
 
-/* Weight formats (CUDA tag page teaser: MXFP4 vs NVFP4, chosen by moe_quant_algo).
+/* Weight formats (CUDA tag page teaser: MXFP4 vs NVFP4, chosen by moe_quant_algo; note
+ * "INT8 高吞吐/低延迟 EP 代码梳理" §2, §3.1: INT8 with channel-wise weights).
  *   MXFP4: E2M1 codes + one UE8M0 scale per 32 along the reduction dim.
  *   NVFP4: E2M1 codes + one E4M3 scale per 16 along the reduction dim + one fp32 scale per
- *          expert matrix. */
-typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+ *          expert matrix.
+ *   INT8:  int8 codes + one fp32 scale per output channel (row); only the *_i8 calls take it. */
+typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1, MOE_W_INT8 = 2 } moe_wfmt;
 
 /* One stacked expert weight tensor with logical shape [E, N, Kd] (N output rows, Kd the
  * reduction dim), in the packed stream written by moe_pack_weights.  W13: N = 2I, Kd = H,
@@ -72,7 +74,8 @@ typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
  * 第三步), packed with pair = 2.  W2: N = H, Kd = I, packed with pair = 1. */
 typedef struct {
   const uint8_t* packed;  /* moe_pack_weights output (32-byte aligned)                        */
-  const float* tscale;    /* NVFP4: [E] fp32 per-matrix scale; MXFP4: NULL                    */
+  const float* tscale;    /* NVFP4: [E] fp32 per-matrix scale; INT8: [E, N] fp32 per-output-  *
+                           * channel scales (logical row order, 16-byte aligned); MXFP4: NULL */
   moe_wfmt fmt;
   int E, N, Kd;           /* logical shape                                                    */
   int pair;               /* 2 for W13 (gate/up row tiles interleaved), 1 for W2              */
@@ -110,7 +113,9 @@ size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair);
  * A weight tile is 256 rows: pair = 2 joins rows 128t.. with rows N/2 + 128t.. (W13: gate with
  * up); pair = 1 takes rows 256t.. (W2; rows past N read as zero).  Each chunk holds the tile's
  * codes, then its scales arranged for tensor memory.  Done once per weight tensor (weights are
- * static).  Kd must be a multiple of 128; N of 256 (pair = 2) or 128 (pair = 1). */
+ * static).  Kd must be a multiple of 128; N of 256 (pair = 2) or 128 (pair = 1).
+ * INT8: q is the int8 codes [E, N, Kd] (16-byte aligned), sf is ignored (may be NULL); each
+ * chunk is a tile's 256 rows x 64 codes (the channel scales stay in the caller's [E, N] array). */
 moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair,
                             uint8_t* packed, void* stream);
 
@@ -351,6 +356,59 @@ moe_status moe_forward_naive(const uint16_t* hidden, const float* w_gate, const 
                              uint16_t* out, int32_t* topk_ids, float* topk_w,
                              int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                              int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------------------------------
+ * INT8 (W8A8) variant (note "INT8 高吞吐/低延迟 EP 代码梳理": §2 INT8 dispatch with quant_dtype
+ * int8, §3.1 INT8 with channel-wise weights, §11.6.2 the high-throughput INT8 path quantises the
+ * activations per token).  Weights: MOE_W_INT8 (int8 codes, fp32 scale per output channel).
+ * Activations, both the layer input and the SwiGLU output: int8 codes with one fp32 scale per row,
+ *   amax = max |x| over the row, inv = fp32(127 / amax), s = fp32(amax / 127),
+ *   q = clamp(rint(fp32(x * inv)), -127, 127)   (rint: to nearest, ties to even),
+ * every division correctly rounded; a zero row gives q = 0, s = 0 (rows with 0 < amax <
+ * 127 / FLT_MAX are not supported).  The expert GEMMs are integer dot products of the codes (run on
+ * the 16-bit tensor cores with fp16 operands, summed in fp32) times the row scale times the channel
+ * scale; L1 rounds silu(gate) * up to bf16 and then quantises each row of h.  Routing, the permute
+ * and the reduce are those of the FP4 path; the index arrays have the same meaning.
+ * ------------------------------------------------------------------------------------ */
+
+/* Workspace bytes of the INT8 calls (moe_workspace_size's layout plus the INT8 row scales and a
+ * bf16 [U, I] h); zero-filled once before first use, as moe_workspace_size's. */
+moe_status moe_workspace_size_i8(int T, int H, int I, int E, int K, int align, size_t* bytes);
+
+/* Per-row int8 quantisation by the rule above: x [rows, cols] bf16 -> x_q [rows, cols] int8,
+ * x_s [rows] fp32.  cols a multiple of 128; x and x_q 16-byte aligned.  No workspace. */
+moe_status moe_act_quant_i8(const uint16_t* x, int rows, int cols, int8_t* x_q, float* x_s, void* stream);
+
+/* L1 + SwiGLU + per-row int8 requant.  The activation rows are read in token order and gathered
+ * through sorted_token_ids (row r of the permuted layout is token sorted_token_ids[r] / K):
+ *   x_q [T, H] int8, x_s [T] fp32 (moe_act_quant_i8 of the layer input)
+ *   sorted_token_ids, expert_ids [U], m_sum [1]: moe_permute's outputs for (T, K, E, align)
+ *   w13: MOE_W_INT8, N = 2I, Kd = H, pair = 2 (tscale = [E, 2I] channel scales)
+ *   h_q [U, I] int8 out, h_s [U] fp32 out: for rows r < M_sum with expert_ids[r] >= 0,
+ *     h = bf16(silu(g) * u), g / u = (integer dot of x_q row and W13 row) * x_s * channel scale,
+ *     then the per-row rule; other rows unspecified.
+ * ws: moe_workspace_size_i8 bytes (fp16 operand rows, row scales, bf16 h). */
+moe_status moe_grouped_gemm_l1_swiglu_i8(const int8_t* x_q, const float* x_s, const int32_t* sorted_token_ids,
+                                         const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H,
+                                         int I, int E, int align, moe_weight w13, int8_t* h_q, float* h_s,
+                                         void* ws, size_t ws_bytes, void* stream);
+
+/* L2: y_perm[r] = bf16((integer dot of h_q row r and W2 row j) * h_s[r] * channel scale j) for rows
+ * r < M_sum with expert_ids[r] >= 0 (others unspecified).  h_q [U, I] int8, h_s [U] fp32; w2:
+ * MOE_W_INT8, N = H, Kd = I, pair = 1; y_perm [U, H] bf16; ws: moe_workspace_size_i8 bytes. */
+moe_status moe_grouped_gemm_l2_i8(const int8_t* h_q, const float* h_s, const int32_t* expert_ids,
+                                  const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
+                                  moe_weight w2, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* The INT8 layer: moe_route (without the FP8 activation output) -> moe_act_quant_i8 -> moe_permute
+ * (indices only) -> INT8 L1 (h requantised per row) -> INT8 L2 -> the topk-weighted reduce, inside
+ * the L2 epilogue up to 32 tokens.  Arguments and optional index outputs as moe_forward's; w13, w2
+ * MOE_W_INT8; ws: moe_workspace_size_i8 bytes. */
+moe_status moe_forward_i8(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                          const float* e_score_bias, int T, int H, int I, int E, int K, int align,
+                          moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
+                          int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                          int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
 /* Self-test of the device failure path (no counterpart in the method's description): launches one
  * bounded wait that nothing can satisfy, through the primitives the hot path uses.  mode 0: a

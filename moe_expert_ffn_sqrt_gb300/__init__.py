@@ -14,9 +14,9 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_INDEX, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(8)
 SCORE_SOFTMAX, SCORE_SQRT_SOFTPLUS = 0, 1
-W_MXFP4, W_NVFP4 = 0, 1
+W_MXFP4, W_NVFP4, W_INT8 = 0, 1, 2
 SCORE_FNS = {"softmax": SCORE_SOFTMAX, "sqrt_softplus": SCORE_SQRT_SOFTPLUS}
-WFMTS = {"mxfp4": W_MXFP4, "nvfp4": W_NVFP4}
+WFMTS = {"mxfp4": W_MXFP4, "nvfp4": W_NVFP4, "int8": W_INT8}
 
 
 class MoeError(RuntimeError):
@@ -94,6 +94,16 @@ def lib():
         L.moe_forward_naive.argtypes = [P, P, P, P, I, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, P, P, P, P,
                                         Z, P]
         L.moe_selftest_wait_timeout.restype = S
+        L.moe_workspace_size_i8.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
+        L.moe_workspace_size_i8.restype = S
+        L.moe_act_quant_i8.argtypes = [P, I, I, P, P, P]
+        L.moe_act_quant_i8.restype = S
+        L.moe_grouped_gemm_l1_swiglu_i8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
+        L.moe_grouped_gemm_l1_swiglu_i8.restype = S
+        L.moe_grouped_gemm_l2_i8.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, Z, P]
+        L.moe_grouped_gemm_l2_i8.restype = S
+        L.moe_forward_i8.argtypes = L.moe_forward.argtypes
+        L.moe_forward_i8.restype = S
         L.moe_selftest_wait_timeout.argtypes = [P, Z, I, P]
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
@@ -184,13 +194,22 @@ def new_workspace(T, H, I, E, K, align, device="cuda"):
 # ---------------------------------------------------------------------------------- weights
 
 def pack_weights(fmt, q, sf, pair, out=None):
-    """Packs codes q [E, N, Kd/2] and scales sf into the GEMMs' weight stream (moe_pack_weights)."""
-    E, N, half = q.shape
-    Kd = 2 * half
+    """Packs codes q and scales sf into the GEMMs' weight stream (moe_pack_weights).
+
+    FP4 formats: q [E, N, Kd/2] packed E2M1 (uint8), sf the block scales.  INT8: q [E, N, Kd] int8,
+    sf unused (the channel scales are passed to Weight as tscale).
+    """
+    if WFMTS.get(fmt, fmt) == W_INT8:
+        E, N, Kd = q.shape
+        qp, sfp = _ptr(q, torch.int8, "q"), None
+    else:
+        E, N, half = q.shape
+        Kd = 2 * half
+        qp, sfp = _ptr(q, torch.uint8, "q"), _ptr(sf, torch.uint8, "sf")
     if out is None:
         out = torch.empty(weight_packed_bytes(fmt, E, N, Kd, pair), dtype=torch.uint8, device=q.device)
-    _check(lib().moe_pack_weights(WFMTS.get(fmt, fmt), _ptr(q, torch.uint8, "q"), _ptr(sf, torch.uint8, "sf"), E, N,
-                                  Kd, pair, _ptr(out, torch.uint8, "out"), _stream()), "moe_pack_weights")
+    _check(lib().moe_pack_weights(WFMTS.get(fmt, fmt), qp, sfp, E, N, Kd, pair, _ptr(out, torch.uint8, "out"),
+                                  _stream()), "moe_pack_weights")
     return out
 
 
@@ -203,8 +222,8 @@ class Weight:
 
     def __init__(self, q, sf, tscale=None, fmt="mxfp4", pair=1):
         self.fmt = fmt
-        self.E, self.N, half = q.shape
-        self.Kd = 2 * half
+        self.E, self.N, kq = q.shape
+        self.Kd = kq if WFMTS.get(fmt, fmt) == W_INT8 else 2 * kq     # INT8: tscale = [E, N] channel scales
         self.pair = pair
         self.tscale = tscale
         self.packed = pack_weights(fmt, q, sf, pair)
@@ -412,6 +431,60 @@ def forward_naive(hidden, w_gate, gate_bias, e_score_bias, I, K, score_fn, renor
         _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
         _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"),
         ws.numel(), _stream()), "moe_forward_naive")
+
+
+# ------------------------------------------------------------------ INT8 (W8A8) variant
+
+def workspace_size_i8(T, H, I, E, K, align):
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_i8(T, H, I, E, K, align, ctypes.byref(n)), "moe_workspace_size_i8")
+    return int(n.value)
+
+
+def new_workspace_i8(T, H, I, E, K, align, device="cuda"):
+    """A zero-filled workspace tensor of the size moe_workspace_size_i8() asks for."""
+    return torch.zeros(workspace_size_i8(T, H, I, E, K, align), dtype=torch.uint8, device=device)
+
+
+def act_quant_i8(x, x_q, x_s):
+    """Per-row int8 quantisation: x [R, C] bf16 -> x_q [R, C] int8, x_s [R] fp32."""
+    R, C = x.shape
+    _check(lib().moe_act_quant_i8(_ptr(x, torch.bfloat16, "x"), R, C, _ptr(x_q, torch.int8, "x_q"),
+                                  _ptr(x_s, torch.float32, "x_s"), _stream()), "moe_act_quant_i8")
+
+
+def grouped_gemm_l1_swiglu_i8(x_q, x_s, sorted_token_ids, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_s, ws):
+    """INT8 L1 + SwiGLU + per-row requant; x_q [T, H] in token order, gathered by sorted_token_ids."""
+    _check(lib().moe_grouped_gemm_l1_swiglu_i8(
+        _ptr(x_q, torch.int8, "x_q"), _ptr(x_s, torch.float32, "x_s"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(m_sum, torch.int32, "m_sum"), T, K, H, I, E, align, w13.c(), _ptr(h_q, torch.int8, "h_q"),
+        _ptr(h_s, torch.float32, "h_s"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
+        "moe_grouped_gemm_l1_swiglu_i8")
+
+
+def grouped_gemm_l2_i8(h_q, h_s, expert_ids, m_sum, T, K, H, I, E, align, w2, y_perm, ws):
+    _check(lib().moe_grouped_gemm_l2_i8(_ptr(h_q, torch.int8, "h_q"), _ptr(h_s, torch.float32, "h_s"),
+                                        _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
+                                        T, K, H, I, E, align, w2.c(), _ptr(y_perm, torch.bfloat16, "y_perm"),
+                                        _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_gemm_l2_i8")
+
+
+def forward_i8(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, renormalize, w13, w2, out, ws,
+               topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None):
+    """moe_forward_i8: the layer with INT8 weights and per-token INT8 activations."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_forward_i8(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+                                _ptr(gate_bias, torch.float32, "gate_bias"),
+                                _ptr(e_score_bias, torch.float32, "e_score_bias"), T, H, I, E, K, align,
+                                SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
+                                _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                _ptr(topk_w, torch.float32, "topk_w"),
+                                _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
+                                _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
+                                _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                _stream()), "moe_forward_i8")
 
 
 def selftest_wait_timeout(ws, mode):

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "route.cu", "route_noalloc.cu", "permute.cu", "gate.cu", "gemm.cu", "gemm_nv.cu", "reduce.cu"]
+SOURCES = ["api.cu", "route.cu", "route_noalloc.cu", "permute.cu", "gate.cu", "gemm.cu", "gemm_nv.cu", "gemm_i8.cu", "reduce.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

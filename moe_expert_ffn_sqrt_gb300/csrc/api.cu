@@ -99,6 +99,32 @@ bool weight_ok(const moe_weight& w, int E, int N, int Kd, int pair) {
   return w.fmt == MOE_W_MXFP4;
 }
 
+// An INT8 weight (the INT8 calls take no other format, and the FP4 calls no INT8 weight).
+bool weight_ok_i8(const moe_weight& w, int E, int N, int Kd, int pair) {
+  if (!w.packed || !aligned(w.packed, 32) || !w.tscale || !aligned(w.tscale, 16)) return false;
+  return w.fmt == MOE_W_INT8 && w.E == E && w.N == N && w.Kd == Kd && w.pair == pair;
+}
+
+// INT8 variant: the common layout (its x_q, h_q and xb regions hold the int8 token rows, the int8 h
+// and the fp16 operand rows) plus the per-row scales and the bf16 h between L1 and its quantisation.
+struct I8Layout {
+  WsLayout L;
+  size_t x_s = 0, a_s = 0, h_s = 0, hb = 0, total = 0;
+};
+
+I8Layout layout_i8(int T, int H, int I, int E, int K, int align) {
+  const size_t U = moe_msum_upper(T, K, E, align);
+  I8Layout r;
+  r.L = layout_rows(T, H, I, E, K, align, U);
+  size_t off = r.L.total;
+  r.x_s = off;  off = up(off + static_cast<size_t>(T) * 4);   // token scales
+  r.a_s = off;  off = up(off + U * 4);                         // per-row scales of the GEMM operand rows
+  r.h_s = off;  off = up(off + U * 4);                         // h scales (forward)
+  r.hb = off;   off = up(off + U * I * 2);                     // bf16 h
+  r.total = off;
+  return r;
+}
+
 }  // namespace
 
 extern "C" {
@@ -137,13 +163,19 @@ size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair) {
   if (pair == 2 ? N % 256 : N % 128) return 0;
   if (fmt == MOE_W_MXFP4) return packed_weight_bytes(E, N, Kd, pair);
   if (fmt == MOE_W_NVFP4) return packed_nv_weight_bytes(E, N, Kd, pair);
+  if (fmt == MOE_W_INT8) return packed_i8_weight_bytes(E, N, Kd, pair);
   return 0;
 }
 
 moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair,
                             uint8_t* packed, void* stream) {
-  if (!q || !sf || !packed || E <= 0 || N <= 0 || Kd <= 0 || Kd % 128) return MOE_ERR_INVALID_ARG;
+  if (!q || !packed || E <= 0 || N <= 0 || Kd <= 0 || Kd % 128) return MOE_ERR_INVALID_ARG;
   if ((pair != 1 && pair != 2) || (pair == 2 ? N % 256 : N % 128)) return MOE_ERR_INVALID_ARG;
+  if (fmt == MOE_W_INT8) {
+    if (!aligned(q, 16) || !aligned(packed, 16)) return MOE_ERR_INVALID_ARG;
+    return cuda_status(launch_pack_i8(reinterpret_cast<const int8_t*>(q), E, N, Kd, pair, packed, S(stream)));
+  }
+  if (!sf) return MOE_ERR_INVALID_ARG;
   if (fmt == MOE_W_MXFP4) return cuda_status(launch_pack_mx(q, sf, E, N, Kd, pair, packed, S(stream)));
   if (fmt == MOE_W_NVFP4) return cuda_status(launch_pack_nv(q, sf, E, N, Kd, pair, packed, S(stream)));
   return MOE_ERR_INVALID_ARG;
@@ -593,6 +625,173 @@ const char* moe_status_str(moe_status s) {
     case MOE_ERR_DEVICE_CHECK: return "kernel self-check failed (bounds or alignment)";
   }
   return "unknown status";
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------------------------
+// INT8 (W8A8) variant
+
+// L1 of the INT8 variant into bf16 h (workspace), then h quantised per row into h_q / h_s; with
+// h_f16 the codes are also written as fp16 rows for the L2 GEMM.
+static moe_status l1_i8_common(const int8_t* x_q, const float* x_s, int x_rows, const int32_t* sorted_token_ids,
+                               const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H, int I, int E,
+                               int align, const moe_weight& w13, int8_t* h_q, float* h_s, uint16_t* h_f16, void* ws,
+                               size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  if (!x_q || !x_s || !sorted_token_ids || !expert_ids || !m_sum || !h_q || !h_s) return MOE_ERR_INVALID_ARG;
+  if (!weight_ok_i8(w13, E, 2 * I, H, 2)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_q, 16) || !aligned(h_q, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const I8Layout L = layout_i8(T, H, I, E, K, align);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  if (U == 0 || T == 0) return MOE_OK;
+  char* b = static_cast<char*>(ws);
+  uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
+  float* as = reinterpret_cast<float*>(b + L.a_s);
+  uint16_t* hb = reinterpret_cast<uint16_t*>(b + L.hb);
+  if (launch_i8_rows_to_f16(x_q, x_s, x_rows, sorted_token_ids, K, expert_ids, m_sum, static_cast<int>(U), H, xf, as,
+                            status_of(ws), S(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  I8Launch G;
+  G.w = w13.packed;
+  G.col_scale = w13.tscale;
+  G.xf = xf;
+  G.row_scale = as;
+  G.expert_ids = expert_ids;
+  G.m_sum = m_sum;
+  G.out = hb;
+  G.status = status_of(ws);
+  G.E = E;
+  G.w_rows = 2 * I;
+  G.Kd = H;
+  G.I = I;
+  G.U = static_cast<int>(U);
+  G.align = align;
+  if (launch_gemm_i8(G, true, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_quant_rows_i8(hb, static_cast<int>(U), I, expert_ids, m_sum, h_q, h_s, h_f16, S(stream)));
+}
+
+// L2 of the INT8 variant from fp16 h codes already in the workspace's operand rows.
+static moe_status l2_i8_launch(const float* h_s, const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H,
+                               int I, int E, int align, const moe_weight& w2, uint16_t* y, const FusedReduce* red,
+                               void* ws, const I8Layout& L, void* stream) {
+  I8Launch G;
+  G.w = w2.packed;
+  G.col_scale = w2.tscale;
+  G.xf = reinterpret_cast<const uint16_t*>(static_cast<char*>(ws) + L.L.xb);
+  G.row_scale = h_s;
+  G.expert_ids = expert_ids;
+  G.m_sum = m_sum;
+  G.out = y;
+  G.status = status_of(ws);
+  G.E = E;
+  G.w_rows = H;
+  G.Kd = I;
+  G.I = I;
+  G.U = static_cast<int>(moe_msum_upper(T, K, E, align));
+  G.align = align;
+  if (red) G.red = *red;
+  return cuda_status(launch_gemm_i8(G, false, S(stream)));
+}
+
+extern "C" {
+
+moe_status moe_workspace_size_i8(int T, int H, int I, int E, int K, int align, size_t* bytes) {
+  if (!bytes || !dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  *bytes = layout_i8(T, H, I, E, K, align).total;
+  return MOE_OK;
+}
+
+moe_status moe_act_quant_i8(const uint16_t* x, int rows, int cols, int8_t* x_q, float* x_s, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 128 || !x || !x_q || !x_s) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_q, 16)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  return cuda_status(launch_quant_rows_i8(x, rows, cols, nullptr, nullptr, x_q, x_s, nullptr, S(stream)));
+}
+
+moe_status moe_grouped_gemm_l1_swiglu_i8(const int8_t* x_q, const float* x_s, const int32_t* sorted_token_ids,
+                                         const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H, int I,
+                                         int E, int align, moe_weight w13, int8_t* h_q, float* h_s, void* ws,
+                                         size_t ws_bytes, void* stream) {
+  return l1_i8_common(x_q, x_s, T, sorted_token_ids, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_s, nullptr,
+                      ws, ws_bytes, stream);
+}
+
+moe_status moe_grouped_gemm_l2_i8(const int8_t* h_q, const float* h_s, const int32_t* expert_ids,
+                                  const int32_t* m_sum, int T, int K, int H, int I, int E, int align, moe_weight w2,
+                                  uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
+  if (!h_q || !h_s || !expert_ids || !m_sum || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!weight_ok_i8(w2, E, H, I, 1)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(h_q, 16) || !aligned(y_perm, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const I8Layout L = layout_i8(T, H, I, E, K, align);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  if (U == 0 || T == 0) return MOE_OK;
+  char* b = static_cast<char*>(ws);
+  uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
+  float* as = reinterpret_cast<float*>(b + L.a_s);
+  if (launch_i8_rows_to_f16(h_q, h_s, static_cast<int>(U), nullptr, 1, expert_ids, m_sum, static_cast<int>(U), I, xf,
+                            as, status_of(ws), S(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return l2_i8_launch(as, expert_ids, m_sum, T, K, H, I, E, align, w2, y_perm, nullptr, ws, L, stream);
+}
+
+moe_status moe_forward_i8(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                          const float* e_score_bias, int T, int H, int I, int E, int K, int align, moe_score_fn fn,
+                          int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
+                          float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                          int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !out || !weight_ok_i8(w13, E, 2 * I, H, 2) || !weight_ok_i8(w2, E, H, I, 1))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  const I8Layout L = layout_i8(T, H, I, E, K, align);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  char* b = static_cast<char*>(ws);
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(b + L.L.topk_ids);
+  float* tw = topk_w ? topk_w : reinterpret_cast<float*>(b + L.L.topk_w);
+  int32_t* sorted = sorted_token_ids ? sorted_token_ids : reinterpret_cast<int32_t*>(b + L.L.sorted);
+  int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.L.expert_ids);
+  int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.L.inv_perm);
+  int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.L.m_sum);
+  int8_t* xq = reinterpret_cast<int8_t*>(b + L.L.x_q);
+  float* xs = reinterpret_cast<float*>(b + L.x_s);
+  int8_t* hq = reinterpret_cast<int8_t*>(b + L.L.h_q);
+  float* hs = reinterpret_cast<float*>(b + L.h_s);
+  uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
+  uint16_t* y = reinterpret_cast<uint16_t*>(b + L.L.y);
+  moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
+                            nullptr, nullptr, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  if (launch_quant_rows_i8(hidden, T, H, nullptr, nullptr, xq, xs, nullptr, S(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = permute_common(ids, T, K, E, align, 0, sorted, eids, inv, ms, nullptr, nullptr, nullptr, H, nullptr, nullptr,
+                      ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  // L1, then h quantised per row with its codes also written as the L2 operand rows
+  st = l1_i8_common(xq, xs, T, sorted, eids, ms, T, K, H, I, E, align, w13, hq, hs, xf, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  const bool fuse_reduce = T <= kFusedReduceMaxTokens;
+  FusedReduce red{};
+  if (fuse_reduce) {
+    red.out = out;
+    red.inv_perm = inv;
+    red.topk_w = tw;
+    red.sorted_ids = sorted;
+    red.tickets = reinterpret_cast<uint32_t*>(b + L.L.tickets);
+    red.K = K;
+  }
+  st = l2_i8_launch(hs, eids, ms, T, K, H, I, E, align, w2, y, fuse_reduce ? &red : nullptr, ws, L, stream);
+  if (st != MOE_OK || fuse_reduce) return st;
+  return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
 }
 
 }  // extern "C"

@@ -22,6 +22,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "passes.cuh"
 
 namespace moe {
 
@@ -69,75 +70,6 @@ struct NvArgs {
   const int32_t* row_ids;       // L1: h of row r scaled by row_w[row_ids[r]] when row_w != nullptr
   const float* row_w;
 };
-
-// One pass of the pipeline: expert e against rows [rb*BN, (rb+nb)*BN), nb = 1 or 2 row blocks
-// (two blocks share each converted weight tile, halving the conversion work per MMA).
-struct NvPass {
-  int e, rb, nb;
-};
-
-// Walks this CTA's items and their passes.  With one expert per row block (alignment a multiple of
-// BN) item t covers blocks 2k and 2k+1 (k = t / n_wt): one pass if both hold the same expert, else
-// a pass per block that holds rows.  Otherwise item t is one block and each expert present in it
-// is a pass (smallest expert id first).  Called by whole warps; every role walks the same sequence.
-template <int BN>
-__device__ __forceinline__ bool nv_next_pass(const NvArgs& a, int msum, int& t, int& p, int& e_prev, NvPass& P) {
-  const int lane = threadIdx.x & 31;
-  while (t < a.n_tiles) {
-    const int k = t / a.n_wt;
-    if (a.one_expert_blocks) {
-      const int rb0 = 2 * k, rb1 = 2 * k + 1;
-      if (rb0 * BN >= msum) return false;
-      const int e0 = __ldg(a.expert_ids + rb0 * BN);
-      const int e1 = rb1 * BN < msum ? __ldg(a.expert_ids + rb1 * BN) : -1;
-      if (e0 >= 0 && e1 == e0) {
-        if (p == 0) {
-          P = NvPass{e0, rb0, 2};
-          p = 2;
-          return true;
-        }
-      } else {
-        if (p == 0) {
-          p = 1;
-          if (e0 >= 0) {
-            P = NvPass{e0, rb0, 1};
-            return true;
-          }
-        }
-        if (p == 1) {
-          p = 2;
-          if (e1 >= 0) {
-            P = NvPass{e1, rb1, 1};
-            return true;
-          }
-        }
-      }
-    } else {
-      const int r0 = k * BN;
-      if (r0 >= msum) return false;
-      const int rend = min(r0 + BN, msum);
-      int best = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < (BN + 31) / 32; ++j) {
-        const int r = r0 + j * 32 + lane;
-        if (r < rend) {
-          const int x = __ldg(a.expert_ids + r);
-          if (x > e_prev && x < best) best = x;
-        }
-      }
-      best = __reduce_min_sync(0xffffffffu, best);
-      if (best != 0x7fffffff) {
-        e_prev = best;
-        P = NvPass{best, k, 1};
-        return true;
-      }
-    }
-    t += gridDim.x;
-    p = 0;
-    e_prev = -1;
-  }
-  return false;
-}
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -269,8 +201,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     int ls = 0;
     uint32_t lph = 0;
     int t = blockIdx.x, p = 0, ep = -1;
-    NvPass P;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+    RowPass P;
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
       const int wt = t % a.n_wt;
       const size_t chunk0 = (static_cast<size_t>(P.e) * a.n_wt + wt) * a.n_slabs;
       bool ok = true;
@@ -311,9 +243,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     int ls = 0, bs = 0;
     uint32_t lph = 0, bph = 0, acc_phase = 0;
     int t = blockIdx.x, p = 0, ep = -1;
-    NvPass P;
+    RowPass P;
     const uint32_t id = idesc_bf16(128, kNvTile);
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
       bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
       if (ok) {
         tc_fence_after();
@@ -358,8 +290,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     int ls = 0, bs = 0;
     uint32_t lph = 0, bph = 0;
     int t = blockIdx.x, p = 0, ep = -1;
-    NvPass P;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+    RowPass P;
+    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
       bool ok = true;
       for (int s = 0; s < a.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
@@ -389,8 +321,8 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const bool warp_has_rows = q * 32 < BN;   // warp-uniform
     uint32_t acc_phase = 0;
     int t = blockIdx.x, p = 0, ep = -1;
-    NvPass P;
-    while (nv_next_pass<BN>(a, msum, t, p, ep, P)) {
+    RowPass P;
+    while (next_row_pass<BN>(a, msum, t, p, ep, P)) {
       const int wt = t % a.n_wt;
       bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, 128, ok);

@@ -101,6 +101,33 @@ cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_
                                int U, int Kd, int align, uint16_t* xb, cudaStream_t stream);
 cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
 
+// gemm_i8.cu (INT8 W8A8 variant: int8 codes as fp16 on the 16-bit MMA, row and channel scales in the
+// epilogue)
+struct I8Launch {
+  const uint8_t* w;            // packed int8 weight stream
+  const float* col_scale;      // [E, w_rows] per-output-channel scales
+  const uint16_t* xf;          // [U, Kd] fp16 activation codes
+  const float* row_scale;      // [U] per-row activation scales
+  const int32_t* expert_ids;
+  const int32_t* m_sum;
+  uint16_t* out;               // L1: h [U, I] bf16; L2: y [U, H] bf16
+  uint32_t* status;
+  int E, w_rows, Kd, I, U, align;
+  FusedReduce red{};
+};
+size_t packed_i8_weight_bytes(int E, int N, int Kd, int pair);
+cudaError_t launch_pack_i8(const int8_t* q, int E, int N, int Kd, int pair, uint8_t* out, cudaStream_t stream);
+// fp16 rows of int8 codes (+ row scales) for rows r < m_sum with expert_ids[r] >= 0; source row
+// src_map[r] / K when src_map is given, else r.
+cudaError_t launch_i8_rows_to_f16(const int8_t* src, const float* src_scale, int src_rows, const int32_t* src_map,
+                                  int K, const int32_t* expert_ids, const int32_t* m_sum, int U, int C, uint16_t* dst,
+                                  float* dst_scale, uint32_t* status, cudaStream_t stream);
+// Per-row int8 quantisation of bf16 rows (all R rows, or with expert_ids the pair rows below m_sum);
+// f16 (nullable) receives the codes as fp16.
+cudaError_t launch_quant_rows_i8(const uint16_t* x, int R, int C, const int32_t* expert_ids, const int32_t* m_sum,
+                                 int8_t* q, float* s, uint16_t* f16, cudaStream_t stream);
+cudaError_t launch_gemm_i8(const I8Launch& L, bool l1, cudaStream_t stream);
+
 // reduce.cu
 cudaError_t launch_wait_selftest(const uint32_t* never_set, uint32_t* status, int mode, cudaStream_t stream);
 cudaError_t launch_unpermute_reduce(const uint16_t* y, const int32_t* inv_perm, const float* topk_w, int T, int K,

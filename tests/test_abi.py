@@ -166,3 +166,40 @@ def test_variant_entry_points_reject_invalid_arguments(M):
     assert L.moe_selftest_wait_timeout(None, 256, 0, None) == M.ERR_INVALID_ARG
     assert L.moe_selftest_wait_timeout(ws, 128, 0, None) == M.ERR_INVALID_ARG
     assert L.moe_selftest_wait_timeout(ws, 256, 2, None) == M.ERR_INVALID_ARG
+
+
+def test_int8_entry_points_reject_invalid_arguments(M):
+    L = M.lib()
+    fake = ctypes.c_void_p(0x10000)     # never dereferenced: validation fails first
+    ws = ctypes.c_void_p(0x20000)
+    n = ctypes.c_size_t(0)
+    # the packed INT8 stream: 256-row tiles x 64-deep slabs of one byte per code (W2 [2, 384, 256] pads a half tile)
+    assert M.weight_packed_bytes("int8", 2, 512, 512, 2) == 2 * 512 * 512
+    assert M.weight_packed_bytes("int8", 2, 384, 256, 1) == 2 * 2 * 4 * 256 * 64
+    assert L.moe_workspace_size_i8(8, 512, 256, 16, 4, 16, ctypes.byref(n)) == M.OK
+    assert n.value > M.workspace_size(8, 512, 256, 16, 4, 16)
+    i13 = M._Weight(0x10000, 0x30000, M.W_INT8, 16, 512, 512, 2)
+    i2 = M._Weight(0x10000, 0x30000, M.W_INT8, 16, 512, 256, 1)
+    f13 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 2)
+    f2 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 256, 1)
+    big = 1 << 30
+    # INT8 weights only through the INT8 calls, FP4 weights never through them
+    assert L.moe_forward(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, i13, i2, fake, None, None, None, None,
+                         None, None, ws, big, None) == M.ERR_INVALID_ARG
+    assert L.moe_forward_i8(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, f13, f2, fake, None, None, None,
+                            None, None, None, ws, big, None) == M.ERR_INVALID_ARG
+    # channel scales are required (and 16-byte aligned)
+    for bad in (M._Weight(0x10000, None, M.W_INT8, 16, 512, 512, 2), M._Weight(0x10000, 0x30004, M.W_INT8, 16, 512, 512, 2)):
+        assert L.moe_grouped_gemm_l1_swiglu_i8(fake, fake, fake, fake, fake, 8, 4, 512, 256, 16, 16, bad, fake, fake,
+                                               ws, big, None) == M.ERR_INVALID_ARG
+    # L2 needs W2's shape ([E, H, I], pair 1)
+    assert L.moe_grouped_gemm_l2_i8(fake, fake, fake, fake, 8, 4, 512, 256, 16, 16, i13, fake, ws, big,
+                                    None) == M.ERR_INVALID_ARG
+    # workspace smaller than moe_workspace_size_i8
+    assert L.moe_forward_i8(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, i13, i2, fake, None, None, None,
+                            None, None, None, ws, n.value - 1, None) == M.ERR_WORKSPACE
+    # per-row quantisation: columns a multiple of 128, 16-byte aligned buffers
+    assert L.moe_act_quant_i8(fake, 4, 100, fake, fake, None) == M.ERR_INVALID_ARG
+    assert L.moe_act_quant_i8(ctypes.c_void_p(0x10008), 4, 128, fake, fake, None) == M.ERR_INVALID_ARG
+    # packing INT8 codes wants a 16-byte aligned source
+    assert L.moe_pack_weights(M.W_INT8, ctypes.c_void_p(0x10004), None, 2, 512, 512, 2, fake, None) == M.ERR_INVALID_ARG
