@@ -530,7 +530,7 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.sf_nb = act_sf_blocks(L.U, BN);
   a.one_expert_blocks = L.align % BN == 0;
   const int nrb = (L.U + BN - 1) / BN;
-  a.n_tiles = (a.one_expert_blocks ? (nrb + 1) / 2 : nrb) * a.n_wt;   // items: row-block pairs or blocks
+  a.n_tiles = (a.one_expert_blocks ? (nrb + 1) / 2 * 2 : nrb) * a.n_wt;   // items: halves of row-block pairs, or blocks
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
