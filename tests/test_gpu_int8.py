@@ -144,6 +144,8 @@ CASES = {
     "K1_H384": dict(T=5, H=384, I=128, E=64, K=1, align=4, score_fn="sqrt_softplus", e_bias=True, seed=44),
     "decode_dims_E32": dict(T=8, H=7168, I=2048, E=32, K=6, align=16, score_fn="sqrt_softplus", e_bias=True, seed=45),
     "T40_align64": dict(T=40, H=1024, I=512, E=32, K=6, align=64, score_fn="sqrt_softplus", e_bias=True, seed=46),
+    "E1024_T16": dict(T=16, H=256, I=256, E=1024, K=8, align=16, score_fn="sqrt_softplus", e_bias=True, seed=47),
+    "T300_align256": dict(T=300, H=512, I=256, E=8, K=2, align=256, score_fn="softmax", seed=48),
 }
 
 
