@@ -87,6 +87,23 @@ def world():
     return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(x, device=None):
+    """The largest value of x over the ranks of the default process group (x itself without one):
+    the whole job takes as long as its slowest replica."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world_size, tokens_per_rank, ms):
+    """Whole-job throughput: every rank processes its own tokens_per_rank in the slowest rank's ms."""
+    return world_size * tokens_per_rank / (ms / 1e3)
+
+
 def workload_config(w):
     acts = ("INT8 activations (fp32 scale per token)" if w.fmt == "int8" else "FP8 E4M3 activations (UE8M0/128)")
     wts = "INT8 weights (fp32 scale per channel)" if w.fmt == "int8" else f"{w.fmt.upper()} weights"
@@ -355,15 +372,11 @@ def run_ours(args, w):
     barrier()
     clk = clocks.stop()
     times = [a.elapsed_time(b) for a, b in ev]
-    ms = statistics.mean(times)
-    if W > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(times), dev)
     st = M.get_error(ws)
     if st != M.OK:
         raise RuntimeError(f"device status after timed steps: {M.status_str(st)}")
-    value = W * T / (ms / 1e3)
+    value = job_tokens_per_s(W, T, ms)
 
     # ---- per-kernel durations: the same path called stage by stage with events in between
     align = M.batched_align(T, w.K, w.E, S) if batched else (M.NAIVE_ROWS if naive else w.align)
@@ -496,12 +509,8 @@ def run_ours(args, w):
         out_host.copy_(out, non_blocking=True)
         e2e_ev[i][1].record()
     barrier()
-    e2e_ms = statistics.mean(a.elapsed_time(b) for a, b in e2e_ev)
-    if W > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": W * T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": T * w.H * 2,
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dev)
+    e2e = {"value": job_tokens_per_s(W, T, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": T * w.H * 2,
            "d2h_bytes_per_step": T * w.H * 2}
 
     line = None
