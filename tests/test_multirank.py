@@ -66,3 +66,20 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_launch_counts_match_the_measured_launch_lists():
+    # kernels per forward as counted in the committed ncu launch lists (decode: 3; batched: 7;
+    # prefill: 8; INT8 decode: 7) and the tiny-batch path's two launches
+    import dataclasses
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    W = synth.WORKLOADS
+    assert bench.launches_per_forward(W["decode"]) == 3
+    assert bench.launches_per_forward(W["batched"]) == 7
+    assert bench.launches_per_forward(W["prefill"]) == 8
+    assert bench.launches_per_forward(dataclasses.replace(W["decode"], fmt="int8")) == 7
+    assert bench.launches_per_forward(W["decode"], naive=True) == 2
+    # NVFP4: two launches (bf16 rows, GEMM) for each of L1 and L2
+    assert bench.launches_per_forward(W["skewed"]) == 3 + 3 + 4 + 1
