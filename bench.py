@@ -18,6 +18,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -148,7 +149,10 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw samples go to a scratch file (MOE_BENCH_CLOCKS_DIR, else the system temp
+        # directory); the JSON line carries their summary
+        base = os.environ.get("MOE_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(base, f"moe_bench_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
