@@ -47,9 +47,9 @@ struct I8Cfg {
   static constexpr int kABytes = BN * 128;
   static constexpr int kPOff = 2 * kABytes;
   static constexpr int kStage = (kPOff + kI8Chunk + 1023) / 1024 * 1024;
-  static constexpr int kBStages = BN >= 128 ? 2 : 3;
+  static constexpr int kBStages = 2;
   static constexpr int kFit = (kI8Budget - 1024 - kBStages * kI8BStage - kI8Extra) / kStage;
-  static constexpr int kStages = kFit > 6 ? 6 : kFit;
+  static constexpr int kStages = kFit > 8 ? 8 : kFit;
   static constexpr int kSmem = 1024 + kStages * kStage + kBStages * kI8BStage + kI8Extra;
   static_assert(kStages >= 2 && kSmem <= kI8Budget, "shared memory budget");
   static_assert(kABytes + 128 * 128 <= kStage, "the MMA's 128-row window of block 1 stays in its slot");
