@@ -410,6 +410,22 @@ moe_status moe_forward_i8(const uint16_t* hidden, const float* w_gate, const flo
                           int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
                           int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* The INT8 layer over the BatchedExperts layout (note "INT8 高吞吐/低延迟 EP 代码梳理" §2: the INT8
+ * dispatch flag is passed to the low-latency path, whose experts receive fixed [max_tokens] slots,
+ * §11.2): moe_forward_i8 with moe_permute_batched's layout (expert e's rows at e * max_tokens, in
+ * token order, unused rows padding).  `out` equals moe_forward_i8's bit for bit (each row's
+ * arithmetic does not depend on the row it sits on).  Requires T <= max_tokens; max_tokens a power
+ * of two in [1, 4096]; ws: moe_workspace_size_batched_i8 bytes; the optional index outputs are
+ * those of moe_permute_batched (expert_num_tokens [E]). */
+moe_status moe_workspace_size_batched_i8(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes);
+moe_status moe_forward_batched_i8(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                  const float* e_score_bias, int T, int H, int I, int E, int K,
+                                  int max_tokens, moe_score_fn fn, int renormalize, moe_weight w13,
+                                  moe_weight w2, uint16_t* out, int32_t* topk_ids, float* topk_w,
+                                  int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
+                                  int32_t* m_sum, int32_t* expert_num_tokens, void* ws, size_t ws_bytes,
+                                  void* stream);
+
 /* Self-test of the device failure path (no counterpart in the method's description): launches one
  * bounded wait that nothing can satisfy, through the primitives the hot path uses.  mode 0: a
  * counter that is never incremented (word 32 of the workspace's reserved first 256 bytes, which

@@ -104,6 +104,10 @@ def lib():
         L.moe_grouped_gemm_l2_i8.restype = S
         L.moe_forward_i8.argtypes = L.moe_forward.argtypes
         L.moe_forward_i8.restype = S
+        L.moe_workspace_size_batched_i8.argtypes = [I, I, I, I, I, I, ctypes.POINTER(Z)]
+        L.moe_workspace_size_batched_i8.restype = S
+        L.moe_forward_batched_i8.argtypes = L.moe_forward_batched.argtypes
+        L.moe_forward_batched_i8.restype = S
         L.moe_selftest_wait_timeout.argtypes = [P, Z, I, P]
         L.moe_get_error.restype = S
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_int)]
@@ -485,6 +489,35 @@ def forward_i8(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, r
                                 _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
                                 _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
                                 _stream()), "moe_forward_i8")
+
+
+def workspace_size_batched_i8(T, H, I, E, K, max_tokens):
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size_batched_i8(T, H, I, E, K, max_tokens, ctypes.byref(n)),
+           "moe_workspace_size_batched_i8")
+    return int(n.value)
+
+
+def new_workspace_batched_i8(T, H, I, E, K, max_tokens, device="cuda"):
+    """A zero-filled workspace tensor of the size moe_workspace_size_batched_i8() asks for."""
+    return torch.zeros(workspace_size_batched_i8(T, H, I, E, K, max_tokens), dtype=torch.uint8, device=device)
+
+
+def forward_batched_i8(hidden, w_gate, gate_bias, e_score_bias, I, K, max_tokens, score_fn, renormalize, w13, w2, out,
+                       ws, topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None,
+                       m_sum=None, expert_num_tokens=None):
+    """moe_forward_batched_i8: the INT8 layer over the BatchedExperts layout."""
+    T, H = hidden.shape
+    E = w_gate.shape[0]
+    _check(lib().moe_forward_batched_i8(
+        _ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
+        _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"), T, H, I, E, K,
+        max_tokens, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
+        _ptr(out, torch.bfloat16, "out"), _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(topk_w, torch.float32, "topk_w"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(inv_perm, torch.int32, "inv_perm"), _ptr(m_sum, torch.int32, "m_sum"),
+        _ptr(expert_num_tokens, torch.int32, "expert_num_tokens"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+        _stream()), "moe_forward_batched_i8")
 
 
 def selftest_wait_timeout(ws, mode):

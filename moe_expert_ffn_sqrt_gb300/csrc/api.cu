@@ -112,8 +112,9 @@ struct I8Layout {
   size_t x_s = 0, a_s = 0, h_s = 0, hb = 0, total = 0;
 };
 
-I8Layout layout_i8(int T, int H, int I, int E, int K, int align) {
-  const size_t U = moe_msum_upper(T, K, E, align);
+// U: rows of the permuted buffers (0: moe_msum_upper for the contiguous layout).
+I8Layout layout_i8(int T, int H, int I, int E, int K, int align, size_t U = 0) {
+  if (U == 0) U = moe_msum_upper(T, K, E, align);
   I8Layout r;
   r.L = layout_rows(T, H, I, E, K, align, U);
   size_t off = r.L.total;
@@ -637,15 +638,15 @@ const char* moe_status_str(moe_status s) {
 static moe_status l1_i8_common(const int8_t* x_q, const float* x_s, int x_rows, const int32_t* sorted_token_ids,
                                const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H, int I, int E,
                                int align, const moe_weight& w13, int8_t* h_q, float* h_s, uint16_t* h_f16, void* ws,
-                               size_t ws_bytes, void* stream) {
+                               size_t ws_bytes, void* stream, size_t rows = 0) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x_q || !x_s || !sorted_token_ids || !expert_ids || !m_sum || !h_q || !h_s) return MOE_ERR_INVALID_ARG;
   if (!weight_ok_i8(w13, E, 2 * I, H, 2)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_q, 16) || !aligned(h_q, 16)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
-  const I8Layout L = layout_i8(T, H, I, E, K, align);
+  const size_t U = rows ? rows : moe_msum_upper(T, K, E, align);
+  const I8Layout L = layout_i8(T, H, I, E, K, align, U);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  const size_t U = moe_msum_upper(T, K, E, align);
   if (U == 0 || T == 0) return MOE_OK;
   char* b = static_cast<char*>(ws);
   uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
@@ -674,8 +675,8 @@ static moe_status l1_i8_common(const int8_t* x_q, const float* x_s, int x_rows, 
 }
 
 // L2 of the INT8 variant from fp16 h codes already in the workspace's operand rows.
-static moe_status l2_i8_launch(const float* h_s, const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H,
-                               int I, int E, int align, const moe_weight& w2, uint16_t* y, const FusedReduce* red,
+static moe_status l2_i8_launch(const float* h_s, const int32_t* expert_ids, const int32_t* m_sum, int H, int I, int E,
+                               int align, size_t U, const moe_weight& w2, uint16_t* y, const FusedReduce* red,
                                void* ws, const I8Layout& L, void* stream) {
   I8Launch G;
   G.w = w2.packed;
@@ -690,10 +691,68 @@ static moe_status l2_i8_launch(const float* h_s, const int32_t* expert_ids, cons
   G.w_rows = H;
   G.Kd = I;
   G.I = I;
-  G.U = static_cast<int>(moe_msum_upper(T, K, E, align));
+  G.U = static_cast<int>(U);
   G.align = align;
   if (red) G.red = *red;
   return cuda_status(launch_gemm_i8(G, false, S(stream)));
+}
+
+// The INT8 layer.  slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align =
+// slot_align(slot)), the slot mode of the permute, U = E * slot rows.
+static moe_status forward_i8_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                    const float* e_score_bias, int T, int H, int I, int E, int K, int align, int slot,
+                                    moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
+                                    uint16_t* out, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
+                                    int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, int32_t* expert_counts,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !out || !weight_ok_i8(w13, E, 2 * I, H, 2) || !weight_ok_i8(w2, E, H, I, 1))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const size_t U = slot ? slot_rows(E, slot) : moe_msum_upper(T, K, E, align);
+  if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
+  const I8Layout L = layout_i8(T, H, I, E, K, align, U);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  char* b = static_cast<char*>(ws);
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(b + L.L.topk_ids);
+  float* tw = topk_w ? topk_w : reinterpret_cast<float*>(b + L.L.topk_w);
+  int32_t* sorted = sorted_token_ids ? sorted_token_ids : reinterpret_cast<int32_t*>(b + L.L.sorted);
+  int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.L.expert_ids);
+  int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.L.inv_perm);
+  int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.L.m_sum);
+  int32_t* cnt = expert_counts ? expert_counts : reinterpret_cast<int32_t*>(b + L.L.counts);
+  int8_t* xq = reinterpret_cast<int8_t*>(b + L.L.x_q);
+  float* xs = reinterpret_cast<float*>(b + L.x_s);
+  int8_t* hq = reinterpret_cast<int8_t*>(b + L.L.h_q);
+  float* hs = reinterpret_cast<float*>(b + L.h_s);
+  uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
+  uint16_t* y = reinterpret_cast<uint16_t*>(b + L.L.y);
+  moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
+                            nullptr, nullptr, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  if (launch_quant_rows_i8(hidden, T, H, nullptr, nullptr, xq, xs, nullptr, S(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, slot ? cnt : nullptr, nullptr, nullptr, H,
+                      nullptr, nullptr, ws, ws_bytes, stream);
+  if (st != MOE_OK) return st;
+  // L1, then h quantised per row with its codes also written as the L2 operand rows
+  st = l1_i8_common(xq, xs, T, sorted, eids, ms, T, K, H, I, E, align, w13, hq, hs, xf, ws, ws_bytes, stream, U);
+  if (st != MOE_OK) return st;
+  const bool fuse_reduce = T <= kFusedReduceMaxTokens;
+  FusedReduce red{};
+  if (fuse_reduce) {
+    red.out = out;
+    red.inv_perm = inv;
+    red.topk_w = tw;
+    red.sorted_ids = sorted;
+    red.tickets = reinterpret_cast<uint32_t*>(b + L.L.tickets);
+    red.K = K;
+  }
+  st = l2_i8_launch(hs, eids, ms, H, I, E, align, U, w2, y, fuse_reduce ? &red : nullptr, ws, L, stream);
+  if (st != MOE_OK || fuse_reduce) return st;
+  return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
 }
 
 extern "C" {
@@ -737,7 +796,7 @@ moe_status moe_grouped_gemm_l2_i8(const int8_t* h_q, const float* h_s, const int
   if (launch_i8_rows_to_f16(h_q, h_s, static_cast<int>(U), nullptr, 1, expert_ids, m_sum, static_cast<int>(U), I, xf,
                             as, status_of(ws), S(stream)) != cudaSuccess)
     return MOE_ERR_CUDA;
-  return l2_i8_launch(as, expert_ids, m_sum, T, K, H, I, E, align, w2, y_perm, nullptr, ws, L, stream);
+  return l2_i8_launch(as, expert_ids, m_sum, H, I, E, align, U, w2, y_perm, nullptr, ws, L, stream);
 }
 
 moe_status moe_forward_i8(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
@@ -745,53 +804,28 @@ moe_status moe_forward_i8(const uint16_t* hidden, const float* w_gate, const flo
                           int renormalize, moe_weight w13, moe_weight w2, uint16_t* out, int32_t* topk_ids,
                           float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                           int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
-  if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
-  if (!hidden || !w_gate || !out || !weight_ok_i8(w13, E, 2 * I, H, 2) || !weight_ok_i8(w2, E, H, I, 1))
+  return forward_i8_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, 0, fn, renormalize, w13, w2,
+                           out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, nullptr, ws, ws_bytes,
+                           stream);
+}
+
+moe_status moe_workspace_size_batched_i8(int T, int H, int I, int E, int K, int max_tokens, size_t* bytes) {
+  if (!bytes || !slot_ok(max_tokens) || !dims_ok(T, H, I, E, K, slot_align(T, K, E, max_tokens)))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
-  if (!ws) return MOE_ERR_WORKSPACE;
-  const size_t U = moe_msum_upper(T, K, E, align);
-  if (U > static_cast<size_t>(INT32_MAX)) return MOE_ERR_UNSUPPORTED;
-  const I8Layout L = layout_i8(T, H, I, E, K, align);
-  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-  if (T == 0) return MOE_OK;
-  char* b = static_cast<char*>(ws);
-  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(b + L.L.topk_ids);
-  float* tw = topk_w ? topk_w : reinterpret_cast<float*>(b + L.L.topk_w);
-  int32_t* sorted = sorted_token_ids ? sorted_token_ids : reinterpret_cast<int32_t*>(b + L.L.sorted);
-  int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.L.expert_ids);
-  int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.L.inv_perm);
-  int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.L.m_sum);
-  int8_t* xq = reinterpret_cast<int8_t*>(b + L.L.x_q);
-  float* xs = reinterpret_cast<float*>(b + L.x_s);
-  int8_t* hq = reinterpret_cast<int8_t*>(b + L.L.h_q);
-  float* hs = reinterpret_cast<float*>(b + L.h_s);
-  uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
-  uint16_t* y = reinterpret_cast<uint16_t*>(b + L.L.y);
-  moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
-                            nullptr, nullptr, ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  if (launch_quant_rows_i8(hidden, T, H, nullptr, nullptr, xq, xs, nullptr, S(stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  st = permute_common(ids, T, K, E, align, 0, sorted, eids, inv, ms, nullptr, nullptr, nullptr, H, nullptr, nullptr,
-                      ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  // L1, then h quantised per row with its codes also written as the L2 operand rows
-  st = l1_i8_common(xq, xs, T, sorted, eids, ms, T, K, H, I, E, align, w13, hq, hs, xf, ws, ws_bytes, stream);
-  if (st != MOE_OK) return st;
-  const bool fuse_reduce = T <= kFusedReduceMaxTokens;
-  FusedReduce red{};
-  if (fuse_reduce) {
-    red.out = out;
-    red.inv_perm = inv;
-    red.topk_w = tw;
-    red.sorted_ids = sorted;
-    red.tickets = reinterpret_cast<uint32_t*>(b + L.L.tickets);
-    red.K = K;
-  }
-  st = l2_i8_launch(hs, eids, ms, T, K, H, I, E, align, w2, y, fuse_reduce ? &red : nullptr, ws, L, stream);
-  if (st != MOE_OK || fuse_reduce) return st;
-  return cuda_status(launch_unpermute_reduce(y, inv, tw, T, K, H, out, S(stream)));
+  *bytes = layout_i8(T, H, I, E, K, slot_align(T, K, E, max_tokens), slot_rows(E, max_tokens)).total;
+  return MOE_OK;
+}
+
+moe_status moe_forward_batched_i8(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                  const float* e_score_bias, int T, int H, int I, int E, int K, int max_tokens,
+                                  moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
+                                  int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                                  int32_t* inv_perm, int32_t* m_sum, int32_t* expert_num_tokens, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (!slot_ok(max_tokens) || max_tokens < T) return MOE_ERR_INVALID_ARG;
+  return forward_i8_common(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, slot_align(T, K, E, max_tokens),
+                           max_tokens, fn, renormalize, w13, w2, out, topk_ids, topk_w, sorted_token_ids, expert_ids,
+                           inv_perm, m_sum, expert_num_tokens, ws, ws_bytes, stream);
 }
 
 }  // extern "C"

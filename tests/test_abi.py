@@ -203,3 +203,11 @@ def test_int8_entry_points_reject_invalid_arguments(M):
     assert L.moe_act_quant_i8(ctypes.c_void_p(0x10008), 4, 128, fake, fake, None) == M.ERR_INVALID_ARG
     # packing INT8 codes wants a 16-byte aligned source
     assert L.moe_pack_weights(M.W_INT8, ctypes.c_void_p(0x10004), None, 2, 512, 512, 2, fake, None) == M.ERR_INVALID_ARG
+    # the INT8 BatchedExperts layout: power-of-two slots, no smaller than the batch
+    for bad in (0, 3, 8192):
+        assert L.moe_workspace_size_batched_i8(8, 512, 256, 16, 4, bad, ctypes.byref(n)) == M.ERR_INVALID_ARG
+    assert L.moe_workspace_size_batched_i8(8, 512, 256, 16, 4, 16, ctypes.byref(n)) == M.OK and n.value > 0
+    assert L.moe_forward_batched_i8(fake, fake, None, None, 9, 512, 256, 16, 4, 8, 0, 1, i13, i2, fake, None, None,
+                                    None, None, None, None, None, ws, big, None) == M.ERR_INVALID_ARG
+    assert L.moe_forward_batched_i8(fake, fake, None, None, 8, 512, 256, 16, 4, 16, 0, 1, f13, f2, fake, None, None,
+                                    None, None, None, None, None, ws, big, None) == M.ERR_INVALID_ARG

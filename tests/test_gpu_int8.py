@@ -246,3 +246,30 @@ def test_forward_i8_graph_replay(M):
         torch.cuda.synchronize()
         assert torch.equal(out.view(torch.int16), eager[i].view(torch.int16)), f"input {i}"
     assert M.get_error(ws) == M.OK
+
+
+@pytest.mark.parametrize("case,S", [("tiny", 16), ("decode_dims_E32", 16), ("T40_align64", 64), ("K1_H384", 8),
+                                    ("T77_tensor_gate", 128)])
+def test_forward_batched_i8_equals_forward_i8(M, case, S):
+    # the BatchedExperts layout changes where a row sits, not its arithmetic: the same bits
+    w = synth.custom(name=case, fmt="int8", **CASES[case])
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    T = w.T
+    a = _forward(M, w, inp, stack)
+    w13, w2 = device_weights(M, stack, "int8")
+    ws = M.new_workspace_batched_i8(T, w.H, w.I, w.E, w.K, S)
+    U = w.E * S
+    o = dict(topk_ids=torch.empty(T, w.K, **I32), topk_w=torch.empty(T, w.K, **F32),
+             sorted_token_ids=torch.empty(U, **I32), expert_ids=torch.empty(U, **I32),
+             inv_perm=torch.empty(T, w.K, **I32), m_sum=torch.empty(1, **I32), expert_num_tokens=torch.empty(w.E, **I32))
+    out = torch.empty(T, w.H, dtype=torch.bfloat16, device="cuda")
+    M.forward_batched_i8(*_args(inp), w.I, w.K, S, w.score_fn, w.renormalize, w13, w2, out, ws, **o)
+    assert M.get_error(ws) == M.OK
+    assert np.array_equal(host_bits(out), a["out"])
+    ids = o["topk_ids"].cpu().numpy()
+    assert np.array_equal(ids, a["topk_ids"])
+    p = O.permute_batched(ids, w.E, S)
+    for k in ("sorted_token_ids", "expert_ids", "inv_perm"):
+        assert np.array_equal(o[k].cpu().numpy(), p[k]), k
+    assert np.array_equal(o["expert_num_tokens"].cpu().numpy(), p["expert_num_tokens"])
