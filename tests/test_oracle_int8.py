@@ -139,3 +139,36 @@ def test_forward_wiring_against_per_token_loop():
     # a token subset gives the same rows
     sub = Q.forward_i8(inp, wp, w.K, w.align, w.score_fn, w.renormalize, tokens=[7, 2])
     assert np.array_equal(sub["out"], res["out"][[7, 2]])
+
+
+def test_quantize_rows_power_of_two_and_sign_symmetry():
+    # scaling a row by 2^k leaves its codes unchanged and scales its scale by exactly 2^k (both
+    # float32 divisions are exact under power-of-two scaling); negating a row negates its codes
+    rng = np.random.default_rng(7)
+    x = F.bf16_to_f64(synth.bf16_rows(rng, 20, 384))
+    q, s = Q.quantize_i8_rows(x)
+    for k in (-20, -3, 5, 30):
+        qk, sk = Q.quantize_i8_rows(x * 2.0 ** k)
+        assert np.array_equal(qk, q)
+        assert np.array_equal(sk, (s * np.float32(2.0 ** k)).astype(np.float32))
+    qn, sn = Q.quantize_i8_rows(-x)
+    assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+
+
+def test_l2_linear_in_row_and_channel_scales():
+    # doubling a row scale or a channel scale doubles those outputs exactly (bf16 rounding commutes
+    # with a power of two); a dropped or misplaced scale fails this
+    rng = np.random.default_rng(8)
+    hq = synth.i8_codes(rng, 6, 256)
+    hs = rng.uniform(1e-3, 1e-1, size=6).astype(np.float32)
+    w2 = synth.i8_codes(rng, 128, 256)
+    ws = synth.i8_channel_scales(rng, 128)
+    y = F.bf16_to_f64(Q.expert_l2_i8(hq, hs, w2, ws))
+    hs2 = hs.copy()
+    hs2[2] *= 2
+    y2 = F.bf16_to_f64(Q.expert_l2_i8(hq, hs2, w2, ws))
+    assert np.array_equal(y2[2], 2 * y[2]) and np.array_equal(np.delete(y2, 2, 0), np.delete(y, 2, 0))
+    ws2 = ws.copy()
+    ws2[5] *= 2
+    y3 = F.bf16_to_f64(Q.expert_l2_i8(hq, hs, w2, ws2))
+    assert np.array_equal(y3[:, 5], 2 * y[:, 5]) and np.array_equal(np.delete(y3, 5, 1), np.delete(y, 5, 1))
