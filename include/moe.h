@@ -142,8 +142,9 @@ moe_status moe_workspace_size(int T, int H, int I, int E, int K, int align, size
  *   x_q, x_sf    [T, H] E4M3 and [T, H/128] UE8M0 out, or both NULL: per 128 columns the
  *                scale is the smallest power of two 2^e with amax <= 448 * 2^e (e in
  *                [-127,127], e = 0 when amax = 0) and x_q = RNE_e4m3(x / 2^e).
- *   ws           workspace (split-K partial sums, a counter for the small-batch kernel that the
- *                call leaves at zero, status word). */
+ *   ws           workspace (status word; routing scratch: a counter slot at a fixed offset that
+ *                every call leaves at zero, then split-K partial sums that each call writes
+ *                before it reads them). */
 moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                      const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
                      int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,
@@ -154,13 +155,16 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
  * device memory (an engine that plans all device buffers up front and forbids cudaMalloc later,
  * a plugin interface that supplies only inputs and outputs).  Same arguments and results as
  * moe_route minus ws/ws_bytes.  Its scratch is a fixed 4 MiB array in device memory inside the
- * library (held on every GPU that loads the library until exit): the call needs nsplit*T*E*4
- * bytes of it (nsplit = 4 for T <= 16) rounded up to 256, for T > 16 another 3*E*H*2 bytes (bf16
- * parts of the gate weight), plus a 256-byte counter slot that each call leaves at zero, and
- * returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
- * All calls on a device share the array, so calls that may overlap on the GPU race.  The first
- * call on each device looks up the array's device address (cudaGetSymbolAddress): make it before
- * any stream capture starts. */
+ * library (held on every GPU that loads the library until exit): 256 bytes for a failure word,
+ * a 256-byte counter slot at a fixed place (every call leaves it at zero), nsplit*T*E*4 bytes of
+ * partial sums (nsplit = 4 for T <= 16) rounded up to 256, and for T > 16 another 3*E*H*2 bytes
+ * (bf16 parts of the gate weight); the call returns MOE_ERR_UNSUPPORTED when that exceeds 4 MiB.
+ * The partial sums and parts a call reads are the ones it wrote; the array keeps the last call's.
+ * Without a workspace there is no status word: if the tensor-core gate GEMM (T > 16) gives up on
+ * a bounded wait, the call still returns MOE_OK but writes -1 to every topk_ids entry and NaN to
+ * every weight (and logit).  All calls on a device share the array, so calls that may overlap on
+ * the GPU race.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress): make it before any stream capture starts. */
 moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                              const float* e_score_bias, int T, int H, int E, int K, moe_score_fn fn,
                              int renormalize, float* logits_out, int32_t* topk_ids, float* topk_w,

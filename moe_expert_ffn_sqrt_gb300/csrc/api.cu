@@ -203,9 +203,9 @@ moe_status moe_route(const uint16_t* hidden, const float* w_gate, const float* g
   const size_t need = poff + route_scratch_bytes(T, H, E);
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + poff);
+  void* scratch = static_cast<char*>(ws) + poff;
   return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
-                                  renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, partial, status_of(ws),
+                                  renormalize, logits_out, topk_ids, topk_w, x_q, x_sf, scratch, status_of(ws),
                                   S(stream)));
 }
 
@@ -238,9 +238,9 @@ static moe_status route_naive_common(const uint16_t* hidden, const float* w_gate
   nv.xp_sf = x_perm_sf;
   nv.U = static_cast<int>(moe_msum_upper(T, K, E, kNaiveRows));
   nv.sf_nb = act_sf_blocks(nv.U, kNaiveRows);
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + poff);
+  void* scratch = static_cast<char*>(ws) + poff;
   return cuda_status(launch_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, static_cast<int>(fn),
-                                  renormalize, nullptr, topk_ids, topk_w, nullptr, nullptr, partial, status_of(ws),
+                                  renormalize, nullptr, topk_ids, topk_w, nullptr, nullptr, scratch, status_of(ws),
                                   S(stream), &nv));
 }
 

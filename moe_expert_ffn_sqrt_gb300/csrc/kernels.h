@@ -10,7 +10,7 @@ namespace moe {
 
 // route.cu
 int route_nsplit(int T, int H, int E);
-size_t route_scratch_bytes(int T, int H, int E);   // partial sums + ticket slot
+size_t route_scratch_bytes(int T, int H, int E);   // ticket slot (first 256 bytes) + partial sums + gate parts
 // Tiny-batch layout (no sort): pair p = t*K + k owns row kNaiveRows * p of the permuted buffers,
 // the other rows of its block and the rows [kNaiveRows * T * K, U) are padding.  Written by the
 // small-batch routing launch (T <= 16).
@@ -26,8 +26,9 @@ struct NaiveLayout {
 };
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
-                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv = nullptr);
+                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, void* scratch,
+                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv = nullptr,
+                         const uint32_t* gate_failed = nullptr);
 
 // permute.cu
 size_t permute_smem_bytes(int E);

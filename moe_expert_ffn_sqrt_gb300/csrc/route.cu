@@ -37,6 +37,9 @@ struct RouteFinishArgs {
   uint8_t* x_sf;
   int topk_blocks;   // blocks [0, topk_blocks) do top-K
   NaiveLayout nv;    // small batches: the tiny-batch layout written by the same launch (nv.eids null: off)
+  // Optional: a word that is zero unless this call's gate GEMM gave up on a wait (and so left its
+  // partial sums unwritten); when set, the top-K writes id -1 and NaN weights and logits instead.
+  const uint32_t* gate_failed;
 };
 
 // Warp arg-max of (key, id), ties to the lower id, with the warp reduction instructions: the keys
@@ -72,6 +75,16 @@ __global__ void __launch_bounds__(256) route_finish_kernel(const RouteFinishArgs
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (static_cast<int>(blockIdx.x) < a.topk_blocks) {
     const int t = blockIdx.x;
+    if (a.gate_failed != nullptr && *a.gate_failed != 0) {
+      // the partial sums of this call were never written: mark the token's routing invalid
+      for (int e = threadIdx.x; e < a.E; e += 256)
+        if (a.logits_out) a.logits_out[static_cast<size_t>(t) * a.E + e] = __int_as_float(0x7fc00000);
+      if (threadIdx.x < a.K) {
+        a.topk_ids[static_cast<size_t>(t) * a.K + threadIdx.x] = -1;
+        a.topk_w[static_cast<size_t>(t) * a.K + threadIdx.x] = __int_as_float(0x7fc00000);
+      }
+      return;
+    }
     // logits: one expert per thread per pass, splits summed in a fixed order
     float lmax = -INFINITY;
     for (int e = threadIdx.x; e < 32 * PER; e += 256) {
@@ -404,10 +417,15 @@ static size_t partial_bytes(int T, int H, int E) {
   return (static_cast<size_t>(route_nsplit(T > 0 ? T : 1, H, E)) * T * E * sizeof(float) + 255) / 256 * 256;
 }
 
+// Routing scratch: [0, 256) the small-batch kernel's ticket counter, at the same place for every T,
+// H and E, so that a buffer reused for another problem size still finds it at zero (each launch
+// that takes tickets sets it back to zero at its end); then the split partial sums; then, above 16
+// tokens, the three bf16 parts of the gate weight.  Partial sums and parts are written by a call
+// before the same call reads them.
+constexpr size_t kTicketSlot = 256;
+
 size_t route_scratch_bytes(int T, int H, int E) {
-  // partial sums; above 16 tokens the bf16 parts of the gate weight; one 256-byte slot for the
-  // small-batch kernel's ticket counter
-  return partial_bytes(T, H, E) + (T > kGemvT ? gate_parts_bytes(T, H, E) : 0) + 256;
+  return kTicketSlot + partial_bytes(T, H, E) + (T > kGemvT ? gate_parts_bytes(T, H, E) : 0);
 }
 
 template <int TT>
@@ -425,9 +443,11 @@ static void launch_route_small(const RouteFinishArgs& a, const float* w_gate, fl
 
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
-                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, float* partial,
-                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv) {
+                         int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, void* scratch,
+                         uint32_t* status, cudaStream_t stream, const NaiveLayout* nv, const uint32_t* gate_failed) {
   const int ns = route_nsplit(T, H, E);
+  uint32_t* ticket = static_cast<uint32_t*>(scratch);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(scratch) + kTicketSlot);
   RouteFinishArgs a;
   a.partial = partial;
   a.nsplit = ns;
@@ -447,12 +467,12 @@ cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const floa
   a.x_sf = x_sf;
   a.topk_blocks = T;
   a.nv = NaiveLayout{};
+  a.gate_failed = gate_failed;
   if (nv) {
     if (T > kGemvT) return cudaErrorInvalidValue;
     a.nv = *nv;
   }
   if (T <= kGemvT) {
-    uint32_t* ticket = reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(partial) + route_scratch_bytes(T, H, E) - 256);
     if (T <= 8) launch_route_small<8>(a, w_gate, partial, ticket, stream);
     else launch_route_small<16>(a, w_gate, partial, ticket, stream);
     return cudaGetLastError();
