@@ -11,7 +11,7 @@ channel-wise weights), §11.6.2 (the high-throughput INT8 path quantises the
 activations per token before the dispatch).  The routing, the permute, M_sum
 and the weighted gather are those of ``oracle.moe`` (same page, §9-§10).
 
-Readings where the page is silent (each also listed in the design doc):
+Readings where the page is silent:
 * weights: int8 codes, one float32 scale per output channel (row of W13 and
   of W2): w[n, k] = q[n, k] * s[n].  The page's ``[256, 256]`` is the
   alignment shape (§11.6.1: the 256 passed in was meant for the per-expert
@@ -97,18 +97,23 @@ WeightProvider = Callable[[int], dict]
 
 
 def forward_i8(inp: dict, weights: WeightProvider, K: int, align: int, score_fn: str,
-               renormalize: bool = True, tokens=None, topk_w_dtype=np.float64) -> Dict[str, object]:
+               renormalize: bool = True, tokens=None, topk_w_dtype=np.float64, routing=None) -> Dict[str, object]:
     """Route -> per-token int8 quantisation -> permute -> per expert: integer L1, SwiGLU, bf16,
     per-row int8 requant, integer L2 -> bf16 rows -> weighted reduce (bf16).
 
     ``tokens``: optional subset of token indices (routing and the permute still use every token);
     ``out`` and ``x_q``/``x_s`` then hold only those tokens' rows, in the order given.
     ``topk_w_dtype``: precision of the routing weights in the final sum.
+    ``routing``: optional dict with topk_ids [T,K] and topk_w [T,K] used in place of the computed routing.
     """
     hidden = inp["hidden"]
     T, H = hidden.shape
     E = inp["w_gate"].shape[0]
-    r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
+    if routing is None:
+        r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
+    else:
+        r = dict(topk_ids=np.asarray(routing["topk_ids"], dtype=np.int32),
+                 topk_w=np.asarray(routing["topk_w"], dtype=np.float64))
     p = permute(r["topk_ids"], E, align)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     q_rows, s_rows = act_quant_i8(hidden[tok])

@@ -14,7 +14,7 @@ expert-contiguous permute with per-expert alignment, M_sum, the weighted
 gather, M_sum_upper).  The CUDA tag page's teaser table names
 "Fused TopK Bias Routing: sqrt(softplus), e_score_correction_bias".
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
 * sqrt(softplus)(x) = sqrt(ln(1 + e^x)).
 * e_score_correction_bias is added to the scores for the top-K *selection*
   only; the weights use the unbiased scores.
@@ -90,7 +90,12 @@ def route(hidden_bits, w_gate, gate_bias, e_score_bias, K: int, score_fn: str,
     Returns logits [T,E] f64, scores [T,E] f64, keys [T,E] f64,
     topk_ids [T,K] int32, topk_w [T,K] float64.
     """
-    logits = gate_logits(hidden_bits, w_gate, gate_bias)
+    return route_from_logits(gate_logits(hidden_bits, w_gate, gate_bias), e_score_bias, K, score_fn, renormalize)
+
+
+def route_from_logits(logits, e_score_bias, K: int, score_fn: str, renormalize: bool = True) -> Dict[str, np.ndarray]:
+    """Scoring -> biased top-K selection -> weights, from given gate logits [T,E] (taken as float64)."""
+    logits = np.asarray(logits, dtype=np.float64)
     if score_fn == "softmax":
         scores = softmax(logits)
     elif score_fn == "sqrt_softplus":
@@ -311,7 +316,8 @@ WeightProvider = Callable[[int], dict]
 
 def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
             score_fn: str, renormalize: bool = True, tokens=None,
-            topk_w_dtype=np.float64, weights_in_l1: bool = False) -> Dict[str, object]:
+            topk_w_dtype=np.float64, weights_in_l1: bool = False, routing=None,
+            workers: int = 1) -> Dict[str, object]:
     """Route -> act quant -> permute -> per-expert L1+SwiGLU+requant -> L2 -> weighted reduce.
 
     ``weights_in_l1``: apply each pair's routing weight to h before the requant (MegaMoE page
@@ -322,11 +328,19 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
     on all tokens, since the permute layout depends on every token.
     ``topk_w_dtype``: precision in which the routing weights enter the final
     sum (float64 by default; float32 mimics a kernel that stores them as fp32).
+    ``routing``: optional dict with topk_ids [T,K] and topk_w [T,K] used in place of the routing
+    this function would compute (every later step is a function of the routing).
+    ``workers``: experts computed by that many threads at once (each expert's arithmetic is the
+    same whichever thread runs it; only the wall time changes).
     """
     hidden = inp["hidden"]
     T, H = hidden.shape
     E = inp["w_gate"].shape[0]
-    r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
+    if routing is None:
+        r = route(hidden, inp["w_gate"], inp.get("gate_bias"), inp.get("e_score_bias"), K, score_fn, renormalize)
+    else:
+        r = dict(topk_ids=np.asarray(routing["topk_ids"], dtype=np.int32),
+                 topk_w=np.asarray(routing["topk_w"], dtype=np.float64))
     p = permute(r["topk_ids"], E, align)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     # activations are quantised per token, so only the checked tokens' rows are needed
@@ -337,10 +351,11 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
     for t in tok:
         for k in range(K):
             need.setdefault(int(r["topk_ids"][t, k]), []).append((int(t), k))
-    I = None
     y_rows = {}
     h_rows = {}
-    for e, pairs in sorted(need.items()):
+
+    def one_expert(item):
+        e, pairs = item
         w = weights(e)
         w13 = dequant_weight(w["w13_q"], w["w13_sf"], w.get("w13_ts"), fmt)
         w2 = dequant_weight(w["w2_q"], w["w2_sf"], w.get("w2_ts"), fmt)
@@ -356,6 +371,15 @@ def forward(inp: dict, weights: WeightProvider, fmt: str, K: int, align: int,
         for j, t in enumerate(ts):
             y_rows[(t, e)] = y[j]
             h_rows[(t, e)] = (hq[j], hsf[j])
+
+    items = sorted(need.items())
+    if workers > 1:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one_expert, items))
+    else:
+        for item in items:
+            one_expert(item)
     out = np.zeros((len(tok), H), dtype=np.uint16)
     wts = r["topk_w"].astype(topk_w_dtype).astype(np.float64)
     for i, t in enumerate(tok):

@@ -59,6 +59,7 @@ class Workload:
     gate_uniform: bool = False
     renormalize: bool = True
     seed: int = 0
+    wide_scales: bool = False  # per-stage tests: weight block scales over a wide code range
 
 
 WORKLOADS = {
@@ -130,13 +131,19 @@ def i8_channel_scales(rng: np.random.Generator, rows: int) -> np.ndarray:
     return rng.uniform(4.5e-4, 5.5e-4, size=rows).astype(np.float32)
 
 
-def mx_scales(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
-    """[rows, cols/32] UE8M0 bytes, 120 or 121 (2**-7 or 2**-6)."""
+def mx_scales(rng: np.random.Generator, rows: int, cols: int, wide: bool = False) -> np.ndarray:
+    """[rows, cols/32] UE8M0 bytes, 120 or 121 (2**-7 or 2**-6); ``wide``: uniform over 97..131
+    (2**-30 .. 2**4)."""
+    if wide:
+        return rng.integers(97, 132, size=(rows, cols // 32), dtype=np.uint8).astype(np.uint8)
     return (120 + rng.integers(0, 2, size=(rows, cols // 32), dtype=np.uint8)).astype(np.uint8)
 
 
-def nv_scales(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
-    """[rows, cols/16] E4M3 bytes uniform in [0x30, 0x48)."""
+def nv_scales(rng: np.random.Generator, rows: int, cols: int, wide: bool = False) -> np.ndarray:
+    """[rows, cols/16] E4M3 bytes uniform in [0x30, 0x48); ``wide``: uniform over every positive
+    finite non-zero code 0x01 .. 0x7E (subnormal 2**-9 up to 448)."""
+    if wide:
+        return rng.integers(0x01, 0x7F, size=(rows, cols // 16), dtype=np.uint8).astype(np.uint8)
     return (0x30 + rng.integers(0, 0x18, size=(rows, cols // 16), dtype=np.uint8)).astype(np.uint8)
 
 
@@ -156,10 +163,10 @@ def expert_weights(w: Workload, e: int) -> dict:
             continue
         out[mat + "_q"] = fp4_codes(rng, rows, cols)
         if w.fmt == "mxfp4":
-            out[mat + "_sf"] = mx_scales(rng, rows, cols)
+            out[mat + "_sf"] = mx_scales(rng, rows, cols, w.wide_scales)
             out[mat + "_ts"] = None
         else:
-            out[mat + "_sf"] = nv_scales(rng, rows, cols)
+            out[mat + "_sf"] = nv_scales(rng, rows, cols, w.wide_scales)
             out[mat + "_ts"] = np.float32(rng.uniform(0.0058, 0.0068))
     return out
 
@@ -223,16 +230,24 @@ def layer_inputs(w: Workload, T: Optional[int] = None) -> dict:
 # --- stage inputs drawn directly (for per-stage tests that must not feed one stage's
 # --- GPU output into the next stage's oracle)
 
-def e4m3_codes(rng: np.random.Generator, shape) -> np.ndarray:
-    """E4M3 codes with uniform sign, exponent field uniform in 3..14, uniform mantissa (no NaN)."""
+def e4m3_codes(rng: np.random.Generator, shape, wide: bool = False) -> np.ndarray:
+    """E4M3 codes with uniform sign, exponent field uniform in 3..14, uniform mantissa (no NaN).
+
+    ``wide``: every non-NaN code with equal odds (zeros, subnormals and the top binade up to 448)."""
+    if wide:
+        c = rng.integers(0, 254, size=shape, dtype=np.int32)      # 254 non-NaN codes
+        c = c + (c >= 0x7F) + (c >= 0xFE)                         # skip 0x7F and 0xFF
+        return c.astype(np.uint8)
     s = rng.integers(0, 2, size=shape, dtype=np.uint8)
     e = rng.integers(3, 15, size=shape, dtype=np.uint8)
     m = rng.integers(0, 8, size=shape, dtype=np.uint8)
     return ((s << 7) | (e << 3) | m).astype(np.uint8)
 
 
-def act_scale_codes(rng: np.random.Generator, shape) -> np.ndarray:
-    """UE8M0 activation scales in 2**-10 .. 2**-6."""
+def act_scale_codes(rng: np.random.Generator, shape, wide: bool = False) -> np.ndarray:
+    """UE8M0 activation scales in 2**-10 .. 2**-6; ``wide``: uniform over 2**-120 .. 2**10."""
+    if wide:
+        return rng.integers(7, 138, size=shape, dtype=np.uint8).astype(np.uint8)
     return (117 + rng.integers(0, 5, size=shape, dtype=np.uint8)).astype(np.uint8)
 
 

@@ -12,8 +12,8 @@ import pytest
 import torch
 
 import synth
-from gpu_util import (OUT_TOL, bf16_ulp_diff, check_out, check_topk, dev, dev_bf16, device_weights, ensure_lib,
-                      host_bits)
+from gpu_util import (OUT_TOL, bf16_ulp_diff, check_layer, check_out, check_topk, dev, dev_bf16, device_weights,
+                      ensure_lib, host_bits, oracle_route_on)
 from oracle import formats as F
 from oracle import moe as O
 
@@ -52,8 +52,9 @@ def test_route_parity(M, name, T):
     assert M.get_error(ws) == M.OK
     lg = logits.cpu().numpy()
     assert np.allclose(lg, r["logits"], rtol=1e-4, atol=2e-5)
-    nties = check_topk(ids.cpu().numpy(), tw.cpu().numpy(), r, w.K)
-    assert nties <= max(2, T // 100)
+    counts = check_topk(ids.cpu().numpy(), tw.cpu().numpy(), r, w.K, oracle_route_on(lg, w, inp))
+    print(f"routing parity {name} T={T}: {counts}")
+    assert counts["unresolved"] <= max(2, T // 100)
     rows = np.arange(T) if T <= 512 else np.random.default_rng(0).choice(T, 256, replace=False)
     xq_ref, xsf_ref = O.act_quant(inp["hidden"][rows])
     assert np.array_equal(xq.cpu().numpy()[rows], xq_ref)
@@ -161,9 +162,9 @@ def test_permute_reports_bad_expert_id(M):
 
 # ------------------------------------------------------------------------------------------ grouped GEMMs
 
-def _gemm_case(T, K, E, H, I, align, seed, skew=0.5, fmt="mxfp4"):
+def _gemm_case(T, K, E, H, I, align, seed, skew=0.5, fmt="mxfp4", wide=False):
     rng = np.random.default_rng(seed)
-    wl = synth.custom(T=T, H=H, I=I, E=E, K=K, align=align, seed=seed, fmt=fmt)
+    wl = synth.custom(T=T, H=H, I=I, E=E, K=K, align=align, seed=seed, fmt=fmt, wide_scales=wide)
     ids = synth.topk_ids_random(rng, T, E, K, skew)
     stack = synth.all_expert_weights(wl)
     return wl, rng, ids, stack
@@ -171,14 +172,17 @@ def _gemm_case(T, K, E, H, I, align, seed, skew=0.5, fmt="mxfp4"):
 
 L1_CASES = [(8, 4, 16, 512, 256, 16), (37, 4, 16, 512, 256, 16), (200, 6, 32, 1024, 512, 64), (64, 4, 8, 512, 384, 1),
             (300, 2, 4, 256, 256, 128), (41, 3, 8, 640, 256, 32)]
-L1_PARAMS = [c + ("mxfp4",) for c in L1_CASES] + [c + ("nvfp4",) for c in L1_CASES[:5]]
+# "wide": every E4M3 activation code (zeros, subnormals, the top binade), activation scales 2^-120 .. 2^10,
+# MXFP4 block scales 2^-30 .. 2^4, NVFP4 scale codes 0x01 .. 0x7E
+L1_PARAMS = ([c + ("mxfp4", False) for c in L1_CASES] + [c + ("nvfp4", False) for c in L1_CASES[:5]] +
+             [L1_CASES[i] + (f, True) for i in (1, 2, 4) for f in ("mxfp4", "nvfp4")])
 
 
-@pytest.mark.parametrize("T,K,E,H,I,align,fmt", L1_PARAMS)
-def test_l1_swiglu_parity(M, T, K, E, H, I, align, fmt):
-    wl, rng, ids, stack = _gemm_case(T, K, E, H, I, align, seed=T + H, fmt=fmt)
-    xq = synth.e4m3_codes(rng, (T, H))
-    xsf = synth.act_scale_codes(rng, (T, H // 128))
+@pytest.mark.parametrize("T,K,E,H,I,align,fmt,wide", L1_PARAMS)
+def test_l1_swiglu_parity(M, T, K, E, H, I, align, fmt, wide):
+    wl, rng, ids, stack = _gemm_case(T, K, E, H, I, align, seed=T + H, fmt=fmt, wide=wide)
+    xq = synth.e4m3_codes(rng, (T, H), wide)
+    xsf = synth.act_scale_codes(rng, (T, H // 128), wide)
     w13, _ = device_weights(M, stack, fmt)
     U = M.msum_upper(T, K, E, align)
     d_sorted = torch.empty(U, dtype=torch.int32, device="cuda")
@@ -211,23 +215,27 @@ def test_l1_swiglu_parity(M, T, K, E, H, I, align, fmt):
         bound = np.abs(h) * 2.0 ** -4 + gmax * 2.0 ** -12 + 1e-30
         bad = np.abs(got - h) > bound
         assert not bad.any(), f"expert {e}: {bad.sum()} values off; worst {np.abs(got - h).max():.3e}"
-        n_codes += hq_ref.size
-        n_same += int((hq[rows] == hq_ref).sum())
+        # code identity over groups whose h is in fp32's normal range (below it the kernel's fp32 h
+        # carries fewer bits than the codes; the absolute bound above covers those groups)
+        normal = gmax >= 2.0 ** -90
+        n_codes += int(normal.sum())
+        n_same += int(((hq[rows] == hq_ref) & normal).sum())
     assert n_same >= 0.97 * n_codes, f"only {n_same}/{n_codes} E4M3 codes identical"
 
 
 L2_CASES = [(8, 4, 16, 512, 256, 16), (37, 4, 16, 512, 256, 16), (200, 6, 32, 1024, 512, 64), (64, 4, 8, 384, 512, 1),
             (300, 2, 4, 256, 256, 128)]
-L2_PARAMS = [c + ("mxfp4",) for c in L2_CASES] + [c + ("nvfp4",) for c in L2_CASES]
+L2_PARAMS = ([c + ("mxfp4", False) for c in L2_CASES] + [c + ("nvfp4", False) for c in L2_CASES] +
+             [L2_CASES[i] + (f, True) for i in (1, 2, 3) for f in ("mxfp4", "nvfp4")])
 
 
-@pytest.mark.parametrize("T,K,E,H,I,align,fmt", L2_PARAMS)
-def test_l2_parity(M, T, K, E, H, I, align, fmt):
-    wl, rng, ids, stack = _gemm_case(T, K, E, H, I, align, seed=7 * T + I, fmt=fmt)
+@pytest.mark.parametrize("T,K,E,H,I,align,fmt,wide", L2_PARAMS)
+def test_l2_parity(M, T, K, E, H, I, align, fmt, wide):
+    wl, rng, ids, stack = _gemm_case(T, K, E, H, I, align, seed=7 * T + I, fmt=fmt, wide=wide)
     _, w2 = device_weights(M, stack, fmt)
     U = M.msum_upper(T, K, E, align)
-    hq = synth.e4m3_codes(rng, (U, I))
-    hsf = synth.act_scale_codes(rng, (U, I // 128))
+    hq = synth.e4m3_codes(rng, (U, I), wide)
+    hsf = synth.act_scale_codes(rng, (U, I // 128), wide)
     d_sorted = torch.empty(U, dtype=torch.int32, device="cuda")
     d_eids = torch.empty(U, dtype=torch.int32, device="cuda")
     d_inv = torch.empty(T, K, dtype=torch.int32, device="cuda")
@@ -252,7 +260,10 @@ def test_l2_parity(M, T, K, E, H, I, align, fmt):
         ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(exact), 1e-38))[1] - 8)
         bad = np.abs(y[rows] - exact) > ulp + 2.0 ** -16 * terms
         assert not bad.any(), f"expert {e}: {bad.sum()} outputs beyond tolerance"
-        assert (bf16_ulp_diff(host_bits(d_y)[rows], O.expert_l2(hq[rows], hsf[rows], W2)) <= 1).mean() > 0.999
+        # rounding identity on outputs in the fp32/bf16 normal range (below it the absolute bound applies)
+        normal = np.abs(exact) >= 2.0 ** -100
+        ud = bf16_ulp_diff(host_bits(d_y)[rows], O.expert_l2(hq[rows], hsf[rows], W2))
+        assert (ud[normal] <= 1).mean() > 0.999
 
 
 def test_unpermute_reduce_parity(M):
@@ -275,13 +286,14 @@ def _run_forward(M, w, inp, stack):
     w13, w2 = device_weights(M, stack, w.fmt)
     ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align)
     U = M.msum_upper(T, w.K, w.E, w.align)
-    o = dict(out=torch.empty(T, w.H, dtype=torch.bfloat16, device="cuda"),
-             topk_ids=torch.empty(T, w.K, dtype=torch.int32, device="cuda"),
-             topk_w=torch.empty(T, w.K, dtype=torch.float32, device="cuda"),
-             sorted_token_ids=torch.empty(U, dtype=torch.int32, device="cuda"),
-             expert_ids=torch.empty(U, dtype=torch.int32, device="cuda"),
-             inv_perm=torch.empty(T, w.K, dtype=torch.int32, device="cuda"),
-             m_sum=torch.empty(1, dtype=torch.int32, device="cuda"))
+    # outputs poisoned, so that anything left unwritten shows
+    o = dict(out=torch.full((T, w.H), float("nan"), dtype=torch.bfloat16, device="cuda"),
+             topk_ids=torch.full((T, w.K), -1, dtype=torch.int32, device="cuda"),
+             topk_w=torch.full((T, w.K), float("nan"), dtype=torch.float32, device="cuda"),
+             sorted_token_ids=torch.full((U,), -7, dtype=torch.int32, device="cuda"),
+             expert_ids=torch.full((U,), -7, dtype=torch.int32, device="cuda"),
+             inv_perm=torch.full((T, w.K), -7, dtype=torch.int32, device="cuda"),
+             m_sum=torch.full((1,), -7, dtype=torch.int32, device="cuda"))
     M.forward(dev_bf16(inp["hidden"]), dev(inp["w_gate"]),
               None if inp["gate_bias"] is None else dev(inp["gate_bias"]),
               None if inp["e_score_bias"] is None else dev(inp["e_score_bias"]), w.I, w.K, w.align, w.score_fn,
@@ -295,39 +307,35 @@ def _run_forward(M, w, inp, stack):
 def _check_perm_invariants(g, ids, E, align):
     """Properties of an expert-contiguous permute that hold for any routing."""
     T, K = ids.shape
-    inv = g["inv_perm"].numpy().reshape(-1)
-    ms = int(g["m_sum"].item())
-    srt, eid = g["sorted_token_ids"].numpy(), g["expert_ids"].numpy()
+    inv = g["inv_perm"].reshape(-1)
+    ms = int(g["m_sum"].reshape(-1)[0])
+    srt, eid = g["sorted_token_ids"], g["expert_ids"]
     assert len(set(inv.tolist())) == T * K and inv.max() < ms and ms % align == 0
     assert np.array_equal(srt[inv], np.arange(T * K)) and np.array_equal(eid[inv], ids.reshape(-1))
     real = eid[:ms][eid[:ms] >= 0]
     assert (np.diff(real) >= 0).all() and (eid >= 0).sum() == T * K
 
 
+ORACLE_THREADS = 16
+
+
 def _check_forward(M, w, T=None, tokens=None):
+    """The whole layer against the oracle: every token (or the given ones), every index output."""
     inp = synth.layer_inputs(w, T)
     T = inp["hidden"].shape[0]
     stack = synth.all_expert_weights(w)
-    g = _run_forward(M, w, inp, stack)
-    ref = O.forward(inp, _stack_provider(stack), w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=tokens)
-    r = ref["route"]
-    gids = g["topk_ids"].numpy()
-    # near-tie tokens (keys closer than the fp32 rounding of the kernel) must still be a valid top-K
-    assert check_topk(gids, g["topk_w"].numpy(), r, w.K) <= max(2, T // 100)
-    agree = (gids == r["topk_ids"]).all(axis=1)
-    p = ref["perm"]
-    if agree.all():
-        assert int(g["m_sum"].item()) == p["m_sum"]
-        assert np.array_equal(g["sorted_token_ids"].numpy(), p["sorted_token_ids"])
-        assert np.array_equal(g["expert_ids"].numpy(), p["expert_ids"])
-        assert np.array_equal(g["inv_perm"].numpy(), p["inv_perm"])
-    _check_perm_invariants(g, gids, w.E, w.align)
-    # the output of every checked token whose routing matches the oracle's
-    toks = ref["tokens"]
-    keep = agree[toks]
-    assert keep.sum() >= max(1, len(toks) - 1)
-    out = host_bits(g["out"])
-    rel = check_out(out[toks[keep]], ref["out"][keep])
+    g = {k: (v.view(torch.int16) if v.dtype == torch.bfloat16 else v).numpy()
+         for k, v in _run_forward(M, w, inp, stack).items()}
+    g["out"] = g["out"].view(np.uint16)
+    prov = _stack_provider(stack)
+
+    def oracle(toks, routing=None):
+        return O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize, tokens=toks, routing=routing,
+                         workers=ORACLE_THREADS)
+
+    ref = oracle(tokens)
+    rel, counts = check_layer(M, w, inp, g, ref, oracle, perm_fn=lambda ids: O.permute(ids, w.E, w.align))
+    _check_perm_invariants(g, g["topk_ids"], w.E, w.align)
     return rel, g, inp, stack
 
 
@@ -364,10 +372,11 @@ def test_forward_tiny_nvfp4(M):
 
 
 @pytest.mark.parametrize("name", ["batched", "prefill", "skewed"])
-def test_forward_sampled(M, name):
-    w = synth.WORKLOADS[name]
-    toks = np.random.default_rng(3).choice(w.T, 4, replace=False)
-    _check_forward(M, w, tokens=np.sort(toks))
+def test_forward_full_workload(M, name):
+    # every token of the workload against the oracle (every GEMM row block of every expert, and
+    # the last items of the dynamic work queue, hold some checked token's rows)
+    rel, g, _, _ = _check_forward(M, synth.WORKLOADS[name])
+    assert rel < OUT_TOL
 
 
 def test_forward_pad_only_row_blocks(M):

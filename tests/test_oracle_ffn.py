@@ -211,3 +211,45 @@ def test_l1_weight_general_differs_only_by_requant_rounding():
         ya = a["route"]["topk_w"][t, k] * F.bf16_to_f64(a["y_rows"][(t, e)])
         yb = F.bf16_to_f64(y_b)
         assert np.sqrt(np.mean((yb - ya) ** 2)) <= 0.1 * np.sqrt(np.mean(ya * ya))
+
+
+def test_routing_override_is_used_and_threads_change_nothing():
+    # a routing given from outside replaces the computed one: a hand-made routing that sends every
+    # token to one expert with weight 1 gives, per token, that expert's SwiGLU FFN alone (rows of
+    # the layer with E = 1 computed by loops above); and experts computed on worker threads give the
+    # same bits as one after another
+    w = synth.custom(T=6, H=256, I=128, E=4, K=2, align=4, score_fn="softmax", seed=31)
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    get = _weights_from_stack(stack)
+    ids = np.array([[2, 0]] * w.T, dtype=np.int32)
+    tw = np.array([[1.0, 0.0]] * w.T)
+    res = moe.forward(inp, get, "mxfp4", w.K, w.align, w.score_fn, routing=dict(topk_ids=ids, topk_w=tw))
+    assert np.array_equal(res["route"]["topk_ids"], ids)
+    W13 = moe.dequant_mxfp4(stack["w13_q"][2], stack["w13_sf"][2])
+    W2 = moe.dequant_mxfp4(stack["w2_q"][2], stack["w2_sf"][2])
+    xd = moe.dequant_fp8_groups(res["x_q"], res["x_sf"])
+    _, hq, hsf = moe.expert_l1_swiglu(xd, W13, w.I)
+    y2 = moe.expert_l2(hq, hsf, W2)
+    assert np.array_equal(res["out"], F.round_bf16_rne(F.bf16_to_f64(y2)))
+    # the permute follows the given routing: every token's two rows sit in the segments of 2 and 0
+    assert res["perm"]["expert_counts"].tolist() == [w.T, 0, w.T, 0]
+    a = moe.forward(inp, get, w.fmt, w.K, w.align, w.score_fn)
+    b = moe.forward(inp, get, w.fmt, w.K, w.align, w.score_fn, workers=4)
+    assert np.array_equal(a["out"], b["out"])
+    assert all(np.array_equal(a["y_rows"][k], b["y_rows"][k]) for k in a["y_rows"])
+
+
+def test_route_from_logits_matches_route_and_brute_force():
+    # routing from given logits: softmax / sqrt(softplus) of those logits, selection by full sort
+    rng = np.random.default_rng(32)
+    logits = rng.standard_normal((5, 12))
+    bias = rng.standard_normal(12) * 0.1
+    r = moe.route_from_logits(logits, bias, 3, "sqrt_softplus")
+    for t in range(5):
+        s = [math.sqrt(math.log1p(math.exp(l))) for l in logits[t]]
+        keys = [s[e] + float(np.float32(bias[e])) for e in range(12)]
+        order = sorted(range(12), key=lambda e: (-keys[e], e))[:3]
+        assert r["topk_ids"][t].tolist() == order
+        tot = sum(s[e] for e in order)
+        assert np.allclose(r["topk_w"][t], [s[e] / tot for e in order], rtol=1e-14)
