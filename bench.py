@@ -24,6 +24,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU baseline (the float64 oracle) runs its experts on ORACLE_THREADS worker threads with
+# single-threaded BLAS, so the thread count it reports is the one that ran.  Set before numpy loads.
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
@@ -49,6 +54,8 @@ def launches_per_forward(w, naive=False):
     permute = 1 if tk <= 128 else (2 if tk <= 1024 else 3)
     if naive:
         permute = 0                               # the routing launch writes the tiny-batch layout
+    elif w.fmt == "nvfp4":
+        permute = 1 if tk <= 1024 else 2          # token-order L1 input: no row or scale copy
     if w.fmt == "mxfp4":
         ffn = 1                                   # L1 and L2 in one launch
     else:
@@ -56,15 +63,30 @@ def launches_per_forward(w, naive=False):
     return route + permute + ffn + reduce
 
 
+HEADLINE = "decode"
+# timed steps per workload in the per-config part of the default run (at most --steps)
+PER_CONFIG_STEPS = {"tiny": 300, "decode": 300, "batched": 200, "prefill": 60, "skewed": 20}
+
+
+def oracle_threads():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except Exception:
+        return max(1, os.cpu_count() or 1)
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", default="decode", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--workload", default=None, choices=sorted(synth.WORKLOADS),
+                   help="measure this workload only; by default the headline (decode) line also carries "
+                        "per_config entries for the other workloads")
+    p.add_argument("--no-per-config", action="store_true", help="headline workload only")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="budget of the oracle CPU baseline (0 skips it, e.g. under a profiler)")
+                   help="budget of the oracle CPU baseline per workload (0 skips it, e.g. under a profiler)")
     p.add_argument("--ref-seconds", type=float, default=150.0,
                    help="time budget of the reference (oracle) arm's timed steps")
     p.add_argument("--experts", type=int, default=None,
@@ -77,6 +99,9 @@ def parse_args():
     p.add_argument("--weights", default="workload", choices=["workload", "int8"],
                    help="the workload's FP4 weight format, or the INT8 variant (int8 weights with per-channel "
                         "scales, int8 activations with per-token scales: moe_forward_i8) on the same shapes")
+    p.add_argument("--l1-input", default="token", choices=["token", "permuted"],
+                   help="stage-by-stage timing: the L1 GEMM reads the token-order activation through "
+                        "sorted_token_ids (as moe_forward does) or the permute's row copy x_perm")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
                         "BatchedExperts slots of max_tokens = max(16, the smallest power of two >= T) (moe_forward_batched) or "
@@ -194,7 +219,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------------ CPU oracle
 
-def oracle_forward(w):
+def oracle_forward(w, workers=1):
     """The oracle's whole-layer function for the workload's weight format, as f(inp, prov, tokens)."""
     if w.fmt == "int8":
         from oracle import int8 as QI
@@ -202,22 +227,29 @@ def oracle_forward(w):
                                                        tokens=tokens)
     from oracle import moe as O
     return lambda inp, prov, tokens: O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize,
-                                               tokens=tokens)
+                                               tokens=tokens, workers=workers)
 
 
-def oracle_tokens_per_s(w, inp, stack, budget_s, max_tokens=None):
-    """Times the float64 oracle on whole tokens of the workload until the budget is spent."""
-    fwd = oracle_forward(w)
+ORACLE_BATCH = 8     # tokens per oracle call of the CPU baseline (the decode batch)
+
+
+def oracle_tokens_per_s(w, inp, stack, budget_s):
+    """Times the float64 oracle on batches of whole tokens of the workload until the budget is spent.
+    Its experts run on oracle_threads() worker threads (BLAS single-threaded)."""
+    n_thr = 1 if w.fmt == "int8" else oracle_threads()
+    fwd = oracle_forward(w, n_thr)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
     done, t0 = 0, time.perf_counter()
-    order = list(range(w.T))
-    while done < len(order) and (max_tokens is None or done < max_tokens):
-        fwd(inp, prov, [order[done]])
-        done += 1
+    while done < w.T:
+        toks = list(range(done, min(w.T, done + ORACLE_BATCH)))
+        fwd(inp, prov, toks)
+        done += len(toks)
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    sample = (f"{done} token(s) of the {w.name} workload in batches of up to {ORACLE_BATCH} (routing of all {w.T} "
+              f"tokens each time), {dt:.1f} s, numpy float64, experts on {n_thr} thread(s), BLAS single-threaded")
+    return {"value": done / dt, "unit": "tokens/s", "cores": n_thr, "kind": "oracle", "sample": sample}
 
 
 def run_reference(args, w):
@@ -227,24 +259,26 @@ def run_reference(args, w):
         return
     inp = synth.layer_inputs(w)
     stack = synth.all_expert_weights(w)
-    fwd = oracle_forward(w)
+    cores = 1 if w.fmt == "int8" else oracle_threads()
+    fwd = oracle_forward(w, cores)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
+    nb = min(ORACLE_BATCH, w.T)
     # warm-up (at most one step: each oracle step is seconds long), then as many timed steps as fit
     # the time budget, at most --steps; the line reports the number actually run
     t0 = time.perf_counter()
     for i in range(min(args.warmup, 1)):
-        fwd(inp, prov, [i % w.T])
+        fwd(inp, prov, [(i * nb + j) % w.T for j in range(nb)])
     est = max(time.perf_counter() - t0, 1e-3)
     steps = max(1, min(args.steps, int(args.ref_seconds / est)))
     times = []
     for i in range(steps):
         t0 = time.perf_counter()
-        fwd(inp, prov, [i % w.T])
+        fwd(inp, prov, [(i * nb + j) % w.T for j in range(nb)])
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
-    value = 1e3 / ms
-    cores = os.cpu_count()
-    sample = f"1 token of the {w.name} workload per step (routing of all {w.T} tokens + that token's {w.K} experts)"
+    value = nb * 1e3 / ms
+    sample = (f"{nb} token(s) of the {w.name} workload per step (routing of all {w.T} tokens + those tokens' "
+              f"experts), experts on {cores} thread(s), BLAS single-threaded")
     line = {"impl": "reference", "metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": steps, "warmup": min(args.warmup, 1), "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
@@ -288,20 +322,13 @@ def kernel_name(stage, fmt):
     return f"{stage} grouped GEMM"
 
 
-def run_ours(args, w):
+def measure(args, w, steps, warmup, cpu_seconds, dev):
+    """One workload: device-timed forward steps, per-stage durations, end-to-end steps, CPU baseline.
+    Returns the pieces of a JSON line (rank 0 gets the CPU baseline)."""
     import torch
     import moe_expert_ffn_sqrt_gb300 as M
 
-    W, rank, local = world()
-    if W > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    M.lib()
-
+    W, rank, _ = world()
     inp = synth.layer_inputs(w)
     stack = synth.all_expert_weights(w)
 
@@ -355,14 +382,14 @@ def run_ours(args, w):
             torch.distributed.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     st = M.get_error(ws)
     if st != M.OK:
         raise RuntimeError(f"device status after warm-up: {M.status_str(st)}")
 
     # ---- timed region: one forward per step, L2 flushed between steps (outside the events)
-    K = args.steps
+    K = steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(dev.index)
     clocks.start()
@@ -411,6 +438,7 @@ def run_ours(args, w):
     # (INT8: the routing stage includes the per-token quantisation, L1 the row gather and the h requant,
     # L2 the conversion of h to fp16 rows)
     fused = w.fmt == "mxfp4" or batched
+    token_order = args.l1_input == "token" and not (batched or naive or i8)
     stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
     if naive:
         stages.remove("permute")
@@ -441,6 +469,8 @@ def run_ours(args, w):
         elif batched:
             M.permute_batched(ids, w.E, S, srt, eids, inv, msum, ws, expert_num_tokens=cnt, x_q=xq, x_sf=xsf,
                               x_perm=xp, x_perm_sf=xpsf)
+        elif token_order:
+            M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt)
         else:
             M.permute(ids, w.E, w.align, srt, eids, inv, msum, ws, expert_counts=cnt, x_q=xq, x_sf=xsf, x_perm=xp,
                       x_perm_sf=xpsf)
@@ -454,8 +484,14 @@ def run_ours(args, w):
             M.grouped_gemm_l2_i8(hq8, hs8, eids, msum, T, w.K, w.H, w.I, w.E, align, w2, y, ws)
         elif batched:
             M.grouped_ffn_batched(xp, xpsf, cnt, T, w.K, w.H, w.I, w.E, S, w13, w2, hq, hsf, y, ws)
+        elif fused and token_order:
+            M.grouped_ffn(xq, xsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, w2, hq, hsf, y, ws,
+                          sorted_token_ids=srt)
         elif fused:
             M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, w2, hq, hsf, y, ws)
+        elif token_order:
+            M.grouped_gemm_l1_swiglu(xq, xsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws,
+                                     sorted_token_ids=srt)
         else:
             M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws)
             j += 1
@@ -517,31 +553,67 @@ def run_ours(args, w):
     e2e = {"value": job_tokens_per_s(W, T, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": T * w.H * 2,
            "d2h_bytes_per_step": T * w.H * 2}
 
+    cpu = None
+    if rank == 0 and W == 1 and cpu_seconds > 0:
+        cpu = oracle_tokens_per_s(w, inp, stack, cpu_seconds)
+    cfg = workload_config(w)
+    cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
+    cfg["parallelism"] = f"replicas x{W}"
+    cfg["layout"] = (f"BatchedExperts, max_tokens={S}" if batched else
+                     "tiny-batch, one 16-row block per (token, expert) pair" if naive else
+                     "expert-contiguous, padded to align")
+    cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
+                              "stage calls)" if args.weights_in_l1 else "applied in the reduce")
+    cfg["l1_input"] = ("token-order rows read through sorted_token_ids" if not (batched or naive or i8) else
+                       "permuted row copy")
+    cfg["stage_l1_input"] = "token-order" if token_order else "permuted copy"
+    res = dict(value=value, ms=ms, steps=K, warmup=warmup, roofline=roofline, e2e=e2e, cpu=cpu, cfg=cfg,
+               clocks=clk, launches=launches_per_forward(w, naive) * K,
+               dtype={"mxfp4": "fp8xfp4 (fp32 accumulate)",
+                      "nvfp4": "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
+                      "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)"}[w.fmt])
+    del w13, w2, ws, flush, xp, hq, y, hidden, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, w, others):
+    import torch
+    import moe_expert_ffn_sqrt_gb300 as M
+
+    W, rank, local = world()
+    if W > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    M.lib()
+    head = measure(args, w, args.steps, args.warmup, args.cpu_seconds, dev)
+    per_config = {}
+    for wo in others:
+        r = measure(args, wo, min(args.steps, PER_CONFIG_STEPS.get(wo.name.split("-")[0], 50)),
+                    max(3, min(args.warmup, 5)), args.cpu_seconds, dev)
+        rf = r["roofline"]
+        per_config[wo.name] = {
+            "config": r["cfg"]["workload"], "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms"],
+            "steps": r["steps"], "warmup": r["warmup"], "dtype": r["dtype"],
+            "roofline": {k: rf[k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic", "kernel",
+                                            "algorithmic_bytes", "algorithmic_flops", "hbm_frac", "tensor_frac",
+                                            "layer_hbm_frac", "experts_touched", "peak_source")},
+            "stage_ms": rf["stage_ms"], "e2e": r["e2e"], "cpu_baseline": r["cpu"], "gpu_launches": r["launches"],
+            "clocks": r["clocks"]}
     line = None
     if rank == 0:
-        cpu = None
-        if W == 1 and args.cpu_seconds > 0:
-            v, n, dt = oracle_tokens_per_s(w, inp, stack, args.cpu_seconds)
-            cpu = {"value": v, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-                   "sample": f"{n} token(s) of the {w.name} workload (routing of all {w.T} tokens each time), "
-                             f"{dt:.1f} s, numpy float64"}
-        cfg = workload_config(w)
-        cfg["l2"] = "512 MiB buffer written between steps (outside the timed events); touched weights > L2"
-        cfg["parallelism"] = f"replicas x{W}"
-        cfg["layout"] = (f"BatchedExperts, max_tokens={S}" if batched else
-                         "tiny-batch, one 16-row block per (token, expert) pair" if naive else
-                         "expert-contiguous, padded to align")
-        cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
-                                  "stage calls)" if args.weights_in_l1 else "applied in the reduce")
-        line = {"metric": "MoE-layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": W, "steps": K,
-                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None,
-                "dtype": {"mxfp4": "fp8xfp4 (fp32 accumulate)",
-                          "nvfp4": "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
-                          "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)"}[w.fmt],
-                "data": "synthetic (seeded)",
-                "config": cfg, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_forward(w, naive) * K, "clocks": clk}
+        line = {"metric": "MoE-layer tokens/s", "value": head["value"], "unit": "tokens/s", "n_gpus": W,
+                "steps": head["steps"], "warmup": head["warmup"], "ms_per_step": head["ms"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic (seeded)",
+                "config": head["cfg"], "roofline": head["roofline"], "cpu_baseline": head["cpu"], "e2e": head["e2e"],
+                "gpu_launches": head["launches"], "clocks": head["clocks"]}
+        if per_config:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if W > 1:
         torch.distributed.destroy_process_group()
@@ -554,19 +626,26 @@ def main():
         raise SystemExit("--weights-in-l1 applies to the expert-contiguous layout")
     if args.weights == "int8" and (args.weights_in_l1 or args.layout != "contiguous"):
         raise SystemExit("--weights int8 runs the expert-contiguous layout with the weights applied in the reduce")
-    w = synth.WORKLOADS[args.workload]
-    if args.weights == "int8":
-        import dataclasses
-        w = dataclasses.replace(w, fmt="int8", name=f"{w.name}-int8")
-    if args.experts or args.tokens:
-        import dataclasses
-        E = args.experts or w.E
-        T = args.tokens or w.T
-        w = dataclasses.replace(w, E=E, T=T, name=f"{w.name}-T{T}-E{E}")
+    import dataclasses
+
+    def variant(w):
+        if args.weights == "int8":
+            w = dataclasses.replace(w, fmt="int8", name=f"{w.name}-int8")
+        if args.experts or args.tokens:
+            E = args.experts or w.E
+            T = args.tokens or w.T
+            w = dataclasses.replace(w, E=E, T=T, name=f"{w.name}-T{T}-E{E}")
+        return w
+
+    w = variant(synth.WORKLOADS[args.workload or HEADLINE])
+    # the default run (no --workload, no variant switch) also measures every other workload
+    plain = (args.workload is None and not args.no_per_config and args.weights == "workload" and
+             args.layout == "contiguous" and not args.weights_in_l1 and not args.experts and not args.tokens)
+    others = [synth.WORKLOADS[n] for n in ("tiny", "batched", "prefill", "skewed")] if plain else []
     if args.impl == "reference":
         run_reference(args, w)
     else:
-        run_ours(args, w)
+        run_ours(args, w, others)
 
 
 if __name__ == "__main__":

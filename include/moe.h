@@ -179,9 +179,11 @@ moe_status moe_route_noalloc(const uint16_t* hidden, const float* w_gate, const 
  *   expert_ids[row]        [U] out: expert of the row, -1 on padding rows and rows >= M_sum
  *   m_sum                  [1] out (device): sum_e round_up(cnt_e, align)
  *   expert_counts          [E] out or NULL: cnt_e
- *   x_q, x_sf, x_perm, x_perm_sf: optional (all NULL or all set): x_perm [U, H] gets row
- *   x_q[t] on row inv_perm[t,k]; x_perm_sf (tiled for `align`, rows = U, slabs = H/128) its scales.
- *   Rows of x_perm at padding positions are left unwritten.
+ *   x_q, x_sf, x_perm, x_perm_sf: optional (all NULL, all set, or only x_sf and x_perm_sf): x_perm
+ *   [U, H] gets row x_q[t] on row inv_perm[t,k]; x_perm_sf (tiled for `align`, rows = U, slabs =
+ *   H/128) its scales.  With x_sf and x_perm_sf alone only the scales move (the input of the
+ *   token-order L1, which reads the rows through sorted_token_ids).  Rows of x_perm at padding
+ *   positions are left unwritten.
  * An id outside [0, E) records MOE_ERR_DEVICE_INDEX and the outputs are unspecified. */
 moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align,
                        int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
@@ -190,17 +192,25 @@ moe_status moe_permute(const int32_t* topk_ids, int T, int K, int E, int align,
                        void* ws, size_t ws_bytes, void* stream);
 
 /* L1 grouped GEMM + SwiGLU + FP8 requant (MegaMoE page 二、阶段 2 and 阶段 3).
- * For every row r < M_sum with e = expert_ids[r] >= 0:
- *   gu = dequant(x_perm[r]) @ dequant(W13[e])^T   ([2I], fp32 accumulate)
+ * For every row r < M_sum with e = expert_ids[r] >= 0 and x_r the activation of that row:
+ *   gu = dequant(x_r) @ dequant(W13[e])^T   ([2I], fp32 accumulate)
  *   h  = silu(gu[0:I]) * gu[I:2I]
  *   h_q[r] / h_sf: h requantised per 128 along I by the rule of moe_route.
- *   x_perm [U, H] E4M3, x_perm_sf tiled (rows U, slabs H/128); h_q [U, I] E4M3 out,
- *   h_sf tiled (rows U, slabs I/128) out.  Rows with expert_ids = -1 are unspecified. */
-moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_perm_sf,
-                                      const int32_t* expert_ids, const int32_t* m_sum, int T,
-                                      int K, int H, int I, int E, int align, moe_weight w13,
-                                      uint8_t* h_q, uint8_t* h_sf, void* ws, size_t ws_bytes,
-                                      void* stream);
+ * The activation comes in one of two forms:
+ *   a_is_permuted != 0: a_q = x_perm [U, H] E4M3 (x_r = a_q[r]), a_sf = x_perm_sf tiled (rows U,
+ *     slabs H/128), both from moe_permute; sorted_token_ids may be NULL.
+ *   a_is_permuted == 0: a_q = x_q [T, H] E4M3 and a_sf = x_sf [T, H/128] UE8M0 in token order, as
+ *     moe_route writes them; x_r = a_q[sorted_token_ids[r] / K] (MegaMoE page, 什么时候需要
+ *     permute/unpermute, 路径 A: the rows are read through the index, never copied).
+ *     sorted_token_ids [U] from moe_permute is required.  The rows' scales are first gathered
+ *     into the workspace (tiled), the rows themselves are read by the GEMM with row-gather copies.
+ * h_q [U, I] E4M3 out, h_sf tiled (rows U, slabs I/128) out.  Rows with expert_ids = -1 are
+ * unspecified. */
+moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* a_q, const uint8_t* a_sf, int a_is_permuted,
+                                      const int32_t* sorted_token_ids, const int32_t* expert_ids,
+                                      const int32_t* m_sum, int T, int K, int H, int I, int E,
+                                      int align, moe_weight w13, uint8_t* h_q, uint8_t* h_sf,
+                                      void* ws, size_t ws_bytes, void* stream);
 
 /* moe_grouped_gemm_l1_swiglu with the routing weight applied in the L1 epilogue (MegaMoE page
  * 二、阶段 3: the SwiGLU output is silu(gate) * up * topk_weight, then amax -> UE8M0 -> E4M3):
@@ -228,11 +238,13 @@ moe_status moe_grouped_gemm_l2(const uint8_t* h_q, const uint8_t* h_sf, const in
  * With MXFP4 weights it is one launch in which an L2 tile starts once every L1 tile
  * of its row block is stored; it needs the full moe_workspace_size() workspace (per-row-block
  * counters that the launch leaves at zero).  With NVFP4 weights the two calls run in turn.
- * Arguments as for the two calls; h_q/h_sf/y_perm 16-byte aligned. */
-moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+ * Arguments as for the two calls (the L1 input permuted or token-order, as in
+ * moe_grouped_gemm_l1_swiglu); h_q/h_sf/y_perm 16-byte aligned. */
+moe_status moe_grouped_ffn(const uint8_t* a_q, const uint8_t* a_sf, int a_is_permuted,
+                           const int32_t* sorted_token_ids, const int32_t* expert_ids,
                            const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
-                           moe_weight w13, moe_weight w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm,
-                           void* ws, size_t ws_bytes, void* stream);
+                           moe_weight w13, moe_weight w2, uint8_t* h_q, uint8_t* h_sf,
+                           uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
 
 /* Weighted unpermute-reduce (note §9.6 "gather 再讲一遍"; MegaMoE page 阶段 5):
  *   out[t] = bf16_rne( sum_{k=0}^{K-1} topk_w[t,k] * y_perm[inv_perm[t,k]] ), summed in fp32

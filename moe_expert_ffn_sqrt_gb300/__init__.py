@@ -64,11 +64,11 @@ def lib():
         L.moe_permute.restype = S
         L.moe_permute.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, I, P, P, P, Z, P]
         L.moe_grouped_gemm_l1_swiglu.restype = S
-        L.moe_grouped_gemm_l1_swiglu.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
+        L.moe_grouped_gemm_l1_swiglu.argtypes = [P, P, I, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
         L.moe_grouped_gemm_l2.restype = S
         L.moe_grouped_gemm_l2.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, Z, P]
         L.moe_grouped_ffn.restype = S
-        L.moe_grouped_ffn.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, Z, P]
+        L.moe_grouped_ffn.argtypes = [P, P, I, P, P, P, I, I, I, I, I, I, _Weight, _Weight, P, P, P, P, Z, P]
         L.moe_unpermute_reduce.restype = S
         L.moe_unpermute_reduce.argtypes = [P, P, P, I, I, I, P, P]
         L.moe_forward.restype = S
@@ -269,8 +269,9 @@ def route_noalloc(hidden, w_gate, gate_bias, e_score_bias, K, score_fn, renormal
 
 def permute(topk_ids, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, ws, expert_counts=None,
             x_q=None, x_sf=None, x_perm=None, x_perm_sf=None):
+    """x_q/x_sf/x_perm/x_perm_sf: rows and scales copied; x_sf/x_perm_sf alone: the scales only."""
     T, K = topk_ids.shape
-    H = x_q.shape[1] if x_q is not None else 0
+    H = x_q.shape[1] if x_q is not None else (x_sf.shape[1] * 128 if x_sf is not None else 0)
     _check(lib().moe_permute(_ptr(topk_ids, torch.int32, "topk_ids"), T, K, E, align,
                              _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
                              _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
@@ -280,8 +281,13 @@ def permute(topk_ids, E, align, sorted_token_ids, expert_ids, inv_perm, m_sum, w
                              _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_permute")
 
 
-def grouped_gemm_l1_swiglu(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, ws):
-    _check(lib().moe_grouped_gemm_l1_swiglu(_ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+def grouped_gemm_l1_swiglu(a_q, a_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, ws,
+                           sorted_token_ids=None):
+    """sorted_token_ids None: a_q / a_sf are the permuted rows x_perm [U, H] with tiled scales.  Given:
+    a_q / a_sf are the token-order x_q [T, H] and x_sf [T, H/128], gathered through sorted_token_ids."""
+    _check(lib().moe_grouped_gemm_l1_swiglu(_ptr(a_q, torch.uint8, "a_q"), _ptr(a_sf, torch.uint8, "a_sf"),
+                                            int(sorted_token_ids is None),
+                                            _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
                                             _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
                                             T, K, H, I, E, align, w13.c(), _ptr(h_q, torch.uint8, "h_q"),
                                             _ptr(h_sf, torch.uint8, "h_sf"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
@@ -306,9 +312,12 @@ def grouped_gemm_l2(h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, y_pe
                                      _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()), "moe_grouped_gemm_l2")
 
 
-def grouped_ffn(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws):
-    """L1 + SwiGLU + requant and L2 in one call (one launch for MXFP4 weights)."""
-    _check(lib().moe_grouped_ffn(_ptr(x_perm, torch.uint8, "x_perm"), _ptr(x_perm_sf, torch.uint8, "x_perm_sf"),
+def grouped_ffn(a_q, a_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws,
+                sorted_token_ids=None):
+    """L1 + SwiGLU + requant and L2 in one call (one launch for MXFP4 weights); the L1 input as in
+    grouped_gemm_l1_swiglu (permuted rows, or token-order rows gathered through sorted_token_ids)."""
+    _check(lib().moe_grouped_ffn(_ptr(a_q, torch.uint8, "a_q"), _ptr(a_sf, torch.uint8, "a_sf"),
+                                 int(sorted_token_ids is None), _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
                                  _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(m_sum, torch.int32, "m_sum"),
                                  T, K, H, I, E, align, w13.c(), w2.c(), _ptr(h_q, torch.uint8, "h_q"),
                                  _ptr(h_sf, torch.uint8, "h_sf"), _ptr(y_perm, torch.bfloat16, "y_perm"),

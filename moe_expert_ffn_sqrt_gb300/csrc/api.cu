@@ -266,10 +266,11 @@ static moe_status permute_common(const int32_t* topk_ids, int T, int K, int E, i
     return MOE_ERR_INVALID_ARG;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   if (!topk_ids || !sorted_token_ids || !expert_ids || !inv_perm || !m_sum) return MOE_ERR_INVALID_ARG;
-  const bool copy = x_perm != nullptr;
-  if (copy != (x_q != nullptr) || copy != (x_sf != nullptr) || copy != (x_perm_sf != nullptr))
-    return MOE_ERR_INVALID_ARG;
-  if (copy && (H <= 0 || H % 128 || !aligned(x_q, 16) || !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
+  // rows and scales (x_q, x_sf, x_perm, x_perm_sf), the scales alone (x_sf, x_perm_sf), or neither
+  const bool copy = x_perm != nullptr, scales = x_perm_sf != nullptr;
+  if (copy != (x_q != nullptr) || scales != (x_sf != nullptr) || (copy && !scales)) return MOE_ERR_INVALID_ARG;
+  if (scales && (H <= 0 || H % 128)) return MOE_ERR_INVALID_ARG;
+  if (copy && (!aligned(x_q, 16) || !aligned(x_perm, 16))) return MOE_ERR_INVALID_ARG;
   if (!ws || ws_bytes < kAlign + permute_scratch_bytes(T, K, E)) return MOE_ERR_WORKSPACE;
   const size_t U = slot ? slot_rows(E, slot) : moe_msum_upper(T, K, E, align);
   int32_t* scratch = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kAlign);   // layout().perm
@@ -331,15 +332,20 @@ static GemmLaunch mx_launch(bool l1, const uint8_t* x, const uint8_t* x_sf, cons
   return L;
 }
 
+// gather_ids non-null (L1 only): x = token-order activation [T, H] and x_sf its plain scales
+// [T, H/128]; permuted row r reads token gather_ids[r] / K (the MXFP4 path first writes the
+// permuted rows' tiled scales into the workspace; the rows themselves are gathered by the GEMM).
 static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
                               size_t ws_bytes, void* stream, const FusedReduce* red = nullptr, size_t rows = 0,
-                              const int32_t* row_ids = nullptr, const float* row_w = nullptr) {
+                              const int32_t* row_ids = nullptr, const float* row_w = nullptr,
+                              const int32_t* gather_ids = nullptr) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
+  if (gather_ids && !l1) return MOE_ERR_INVALID_ARG;
   if (!(l1 ? weight_ok(w, E, 2 * I, H, 2) : weight_ok(w, E, H, I, 1))) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(x_sf, 16)) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (!gather_ids && !aligned(x_sf, 16))) return MOE_ERR_INVALID_ARG;
   if (l1 && (!h_q || !h_sf)) return MOE_ERR_INVALID_ARG;
   if (!l1 && (!y || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
   if ((row_ids == nullptr) != (row_w == nullptr) || (!l1 && row_w)) return MOE_ERR_INVALID_ARG;
@@ -352,7 +358,8 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
     uint16_t* xb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + Lw.xb);
     const int Kd = l1 ? H : I;
-    cudaError_t err = launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream));
+    cudaError_t err = launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream),
+                                         gather_ids, K, T);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     NvLaunch N;
     N.w = w.packed;
@@ -377,20 +384,36 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
   }
   const WsLayout Lw = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
-  GemmLaunch L = mx_launch(l1, x, x_sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
+  const uint8_t* sf = x_sf;
+  if (gather_ids) {
+    // the permuted rows' scales, tiled for the GEMM, into the workspace
+    uint8_t* psf = reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + Lw.x_perm_sf);
+    if (launch_permute_act_sf(gather_ids, K, expert_ids, m_sum, static_cast<int>(U), T, x_sf, H / 128, align, psf,
+                              S(stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    sf = psf;
+  }
+  GemmLaunch L = mx_launch(l1, x, sf, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
   if (red) L.red = *red;
   L.row_ids = row_ids;
   L.row_w = row_w;
+  if (gather_ids) {
+    L.gather_ids = gather_ids;
+    L.gather_k = K;
+    L.gather_rows = T;
+  }
   uint32_t* sched = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + Lw.sched);
   return cuda_status(launch_gemm(L, l1, sched, S(stream)));
 }
 
-moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
+moe_status moe_grouped_gemm_l1_swiglu(const uint8_t* a_q, const uint8_t* a_sf, int a_is_permuted,
+                                      const int32_t* sorted_token_ids, const int32_t* expert_ids,
                                       const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                                       moe_weight w13, uint8_t* h_q, uint8_t* h_sf, void* ws, size_t ws_bytes,
                                       void* stream) {
-  return gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, nullptr, ws,
-                     ws_bytes, stream);
+  if (!a_is_permuted && !sorted_token_ids) return MOE_ERR_INVALID_ARG;
+  return gemm_common(true, a_q, a_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf, nullptr, ws,
+                     ws_bytes, stream, nullptr, 0, nullptr, nullptr, a_is_permuted ? nullptr : sorted_token_ids);
 }
 
 moe_status moe_grouped_gemm_l1_swiglu_weighted(const uint8_t* x_perm, const uint8_t* x_perm_sf,
@@ -417,10 +440,11 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
                              const moe_weight& w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
                              size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0,
                              const int32_t* row_ids = nullptr, const float* row_w = nullptr,
-                             const int32_t* slot_counts = nullptr, int slot = 0) {
+                             const int32_t* slot_counts = nullptr, int slot = 0,
+                             const int32_t* gather_ids = nullptr) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
-                                nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w);
+                                nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w, gather_ids);
     if (st != MOE_OK) return st;
     return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws,
                        ws_bytes, stream, red, rows);
@@ -428,17 +452,34 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x_perm || !x_perm_sf || !expert_ids || !m_sum || !h_q || !h_sf || !y) return MOE_ERR_INVALID_ARG;
   if (!weight_ok(w13, E, 2 * I, H, 2) || !weight_ok(w2, E, H, I, 1)) return MOE_ERR_INVALID_ARG;
-  if (!aligned(x_perm, 16) || !aligned(x_perm_sf, 16) || !aligned(h_q, 16) || !aligned(h_sf, 16) || !aligned(y, 16))
+  if (!aligned(x_perm, 16) || !aligned(h_q, 16) || !aligned(h_sf, 16) || !aligned(y, 16))
     return MOE_ERR_INVALID_ARG;
+  if (!gather_ids && !aligned(x_perm_sf, 16)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const size_t U = rows ? rows : moe_msum_upper(T, K, E, align);
   const WsLayout L = layout_rows(T, H, I, E, K, align, U);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   if (U == 0) return MOE_OK;
   if ((row_ids == nullptr) != (row_w == nullptr)) return MOE_ERR_INVALID_ARG;
-  GemmLaunch l1 = mx_launch(true, x_perm, x_perm_sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
+  if (gather_ids && slot_counts) return MOE_ERR_INVALID_ARG;
+  const uint8_t* sf = x_perm_sf;
+  uint8_t* psf = reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + L.x_perm_sf);
+  if (gather_ids && x_perm_sf != psf) {
+    // token-order scales: the permuted rows' tiled scales into the workspace (moe_forward's permute
+    // writes them there itself)
+    if (launch_permute_act_sf(gather_ids, K, expert_ids, m_sum, static_cast<int>(U), T, x_perm_sf, H / 128, align,
+                              psf, S(stream)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    sf = psf;
+  }
+  GemmLaunch l1 = mx_launch(true, x_perm, sf, expert_ids, m_sum, H, I, E, align, U, w13, h_q, h_sf, nullptr, ws);
   l1.row_ids = row_ids;
   l1.row_w = row_w;
+  if (gather_ids) {
+    l1.gather_ids = gather_ids;
+    l1.gather_k = K;
+    l1.gather_rows = T;
+  }
   if (slot_counts && slot % gemm_block_n(align) == 0 && align % gemm_block_n(align) == 0) {
     // BatchedExperts with one expert per row block: only the blocks holding tokens are work
     l1.counts = slot_counts;
@@ -450,12 +491,13 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
   return cuda_status(launch_ffn(l1, l2, sched, S(stream)));
 }
 
-moe_status moe_grouped_ffn(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_ids,
-                           const int32_t* m_sum, int T, int K, int H, int I, int E, int align, moe_weight w13,
-                           moe_weight w2, uint8_t* h_q, uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes,
-                           void* stream) {
-  return ffn_common(x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws,
-                    ws_bytes, stream, nullptr);
+moe_status moe_grouped_ffn(const uint8_t* a_q, const uint8_t* a_sf, int a_is_permuted,
+                           const int32_t* sorted_token_ids, const int32_t* expert_ids, const int32_t* m_sum, int T,
+                           int K, int H, int I, int E, int align, moe_weight w13, moe_weight w2, uint8_t* h_q,
+                           uint8_t* h_sf, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  if (!a_is_permuted && !sorted_token_ids) return MOE_ERR_INVALID_ARG;
+  return ffn_common(a_q, a_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, w2, h_q, h_sf, y_perm, ws, ws_bytes,
+                    stream, nullptr, 0, nullptr, nullptr, nullptr, 0, a_is_permuted ? nullptr : sorted_token_ids);
 }
 
 moe_status moe_grouped_ffn_batched(const uint8_t* x_perm, const uint8_t* x_perm_sf, const int32_t* expert_num_tokens,
@@ -489,6 +531,14 @@ moe_status moe_unpermute_reduce(const uint16_t* y_perm, const int32_t* inv_perm,
 
 }  // extern "C"
 
+// moe_forward's L1 input: the token-order activation read through sorted_token_ids (MegaMoE page,
+// 路径 A), or the permuted copy x_perm.  The BatchedExperts and tiny-batch layouts keep their copies.
+static bool forward_reads_token_order(int T, int K) {
+  (void)T;
+  (void)K;
+  return true;
+}
+
 // slot 0: contiguous layout padded to align; slot > 0: BatchedExperts (align = slot_align(slot)).
 static moe_status forward_common(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                                  const float* e_score_bias, int T, int H, int I, int E, int K, int align, int slot,
@@ -521,6 +571,10 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   uint8_t* hq = reinterpret_cast<uint8_t*>(b + L.h_q);
   uint8_t* hsf = reinterpret_cast<uint8_t*>(b + L.h_sf);
   uint16_t* y = reinterpret_cast<uint16_t*>(b + L.y);
+  // token-order L1 input: the permute moves no rows (MXFP4: only the scales, tiled for the GEMM;
+  // NVFP4: nothing, its bf16 conversion reads the token-order scales)
+  const bool gather = !naive && slot == 0 && forward_reads_token_order(T, K);
+  const bool mx = w13.fmt == MOE_W_MXFP4;
   moe_status st;
   if (naive) {
     st = route_naive_common(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, ids, tw, sorted,
@@ -530,8 +584,12 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
     st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw, xq, xsf, ws,
                    ws_bytes, stream);
     if (st != MOE_OK) return st;
-    st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, slot ? cnt : expert_counts, xq, xsf, H, xp,
-                        xpsf, ws, ws_bytes, stream);
+    if (gather)
+      st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, expert_counts, nullptr,
+                          mx ? xsf : nullptr, H, nullptr, mx ? xpsf : nullptr, ws, ws_bytes, stream);
+    else
+      st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, slot ? cnt : expert_counts, xq, xsf, H,
+                          xp, xpsf, ws, ws_bytes, stream);
     if (st != MOE_OK) return st;
   }
   const bool fuse_reduce = T <= kFusedReduceMaxTokens;
@@ -544,9 +602,9 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
     red.tickets = reinterpret_cast<uint32_t*>(b + L.tickets);
     red.K = K;
   }
-  st = ffn_common(xp, xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y, ws, ws_bytes, stream,
-                  fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr, slot ? cnt : nullptr,
-                  slot);
+  st = ffn_common(gather ? xq : xp, gather && !mx ? xsf : xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y,
+                  ws, ws_bytes, stream, fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr,
+                  slot ? cnt : nullptr, slot, gather ? sorted : nullptr);
   if (st != MOE_OK || fuse_reduce) return st;
   return cuda_status(launch_unpermute_reduce(y, inv, l1w ? nullptr : tw, T, K, H, out, S(stream)));
 }

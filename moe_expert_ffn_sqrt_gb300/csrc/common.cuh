@@ -113,6 +113,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Four rows of a 2D tensor map with a one-row box, rows y0..y3 at column c0, landing as rows 0..3 of
+// a tile at dst (the tensor map's swizzle applies as for a four-row box at that address).  Rows
+// outside the tensor read as zeros.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int y0, int y1, int y2,
+                                            int y3, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),

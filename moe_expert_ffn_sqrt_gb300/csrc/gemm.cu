@@ -77,6 +77,13 @@ struct GemmPhase {
   int n_wt;                     // weight tiles per expert
   int out_cols;                 // L1: I, L2: H
   int n_tiles;                  // ceil(U/BN) * n_wt; 0 = phase not run by this launch
+  // Gather mode (L1): the activation tensor map covers the token-order rows [T, Kd], and permuted
+  // row r reads token gather_ids[r] / gather_k (gather_ids = sorted_token_ids [U]; padding rows
+  // name token T, past the tensor, and read zeros).  nullptr: the map covers the permuted rows.
+  const int32_t* gather_ids;
+  int gather_k;
+  int gather_rows;              // T
+  int gather_u;                 // entries of gather_ids
 };
 
 struct GemmArgs {
@@ -317,6 +324,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const CUtensorMap* mx = it.phase ? &tmap_x2 : &tmap_x1;
       const int r0 = it.rb * BN;
       const size_t chunk0 = (static_cast<size_t>(e) * P.n_wt + it.wt) * P.n_slabs;
+      // gather mode: lane j (< BN / 4) copies rows 4j .. 4j + 3 of the block, tokens looked up once
+      const bool gather = P.gather_ids != nullptr;
+      int g_tok[4] = {0, 0, 0, 0};
+      if (gather && lane < BN / 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = r0 + 4 * lane + i;
+          const int tk = r < P.gather_u ? __ldg(P.gather_ids + r) / P.gather_k : P.gather_rows;
+          g_tok[i] = (tk < 0 || tk > P.gather_rows) ? P.gather_rows : tk;
+        }
+      }
       if (it.phase == 1 && a.fused) {
         // h rows of this block come from other CTAs' L1 epilogues
         if (lane == 0) {
@@ -334,15 +352,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; ok && s < P.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
         if (!ok) break;
+        uint8_t* st = stages + stage * C::STAGE;
+        const uint32_t fb = smem_u32(full + stage);
+        bool good = true;
         if (lane == 0) {
-          uint8_t* st = stages + stage * C::STAGE;
-          const uint32_t fb = smem_u32(full + stage);
           const size_t wbase = (chunk0 + s) * C::W_CHUNK;
           const size_t sfa = (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
           // self-check: every copy inside its buffer and 16-byte aligned
-          const bool good = wbase + C::W_CHUNK <= P.w_bytes &&
-                            ((s & 3) != 0 || sfa + C::SFA_BYTES <= P.x_sf_bytes) &&
-                            ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0;
+          good = wbase + C::W_CHUNK <= P.w_bytes &&
+                 ((s & 3) != 0 || sfa + C::SFA_BYTES <= P.x_sf_bytes) &&
+                 ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0;
           if (!good) {
             record_error(a.status, kDevErrCheck);
             *abort_flag = 1;
@@ -352,10 +371,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_arrive_expect_tx(fb, bytes);
             tma_load_2d(smem_u32(st + C::W_OFF), mw, 0, static_cast<int>(wbase / 64), fb, pol_w);
             bulk_load(smem_u32(st + C::SFB_OFF), P.w + wbase + C::TX_W, 1024, fb);
-            tma_load_2d(smem_u32(st), mx, s * 128, r0, fb, pol_x);
+            if (!gather) tma_load_2d(smem_u32(st), mx, s * 128, r0, fb, pol_x);
             if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFA_OFF), P.x_sf + sfa, C::SFA_BYTES, fb);
           }
         }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (gather && good && lane < BN / 4)
+          tma_gather4(smem_u32(st + lane * 512), mx, s * 128, g_tok[0], g_tok[1], g_tok[2], g_tok[3], fb, pol_x);
         __syncwarp();
         if (++stage == C::STAGES) {
           stage = 0;
@@ -668,9 +690,22 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
   P.n_wt = weight_tiles(L.w_rows, pair);
   P.out_cols = l1 ? L.I : L.w_rows;
   P.n_tiles = (L.U + BN - 1) / BN * P.n_wt;
+  P.gather_ids = nullptr;
+  P.gather_k = 1;
+  P.gather_rows = 0;
+  P.gather_u = 0;
   // the packed stream viewed as rows of 128 FP4 codes (64 bytes); a box is 256 rows
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, L.w, 128, P.w_bytes / 64, 64, 128, kTileRows))
     return false;
+  if (l1 && L.gather_ids) {
+    // token-order rows [T, Kd], one-row box for the four-row gathers
+    if (L.gather_rows <= 0 || L.gather_k <= 0) return false;
+    P.gather_ids = L.gather_ids;
+    P.gather_k = L.gather_k;
+    P.gather_rows = L.gather_rows;
+    P.gather_u = L.U;
+    return make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.gather_rows, L.Kd, 128, 1);
+  }
   return make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.x, L.Kd, L.U, L.Kd, 128, BN);
 }
 

@@ -428,18 +428,27 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 
 // Activation rows (E4M3 codes + tiled UE8M0 scales) -> bf16 rows, exactly, for rows that hold a
 // (token, expert) pair.  One warp per row, 8 codes per lane step.
+// gather_ids non-null: x and sf are token-order ([T, Kd] codes, [T, Kd/128] plain scales) and row r
+// reads token gather_ids[r] / K.
 __global__ void __launch_bounds__(256) act_to_bf16_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ sf,
                                                           const int32_t* __restrict__ expert_ids,
                                                           const int32_t* __restrict__ m_sum, int U, int Kd, int bt,
-                                                          int nb, uint16_t* __restrict__ xb) {
+                                                          int nb, uint16_t* __restrict__ xb,
+                                                          const int32_t* __restrict__ gather_ids, int K, int T) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int msum = *m_sum;
   for (int r = blockIdx.x * 8 + warp; r < msum && r < U; r += gridDim.x * 8) {
     if (__ldg(expert_ids + r) < 0) continue;
+    int src = r;
+    if (gather_ids != nullptr) {
+      src = __ldg(gather_ids + r) / K;
+      if (src < 0 || src >= T) continue;
+    }
     for (int k0 = lane * 8; k0 < Kd; k0 += 256) {
-      const uint32_t b = sf[act_sf_offset(bt, nb, r, k0 / 128)];
+      const uint32_t b = gather_ids != nullptr ? sf[static_cast<size_t>(src) * (Kd / 128) + k0 / 128]
+                                               : sf[act_sf_offset(bt, nb, r, k0 / 128)];
       const float sc = b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);   // 2^(b-127)
-      const uint2 c = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(r) * Kd + k0);
+      const uint2 c = *reinterpret_cast<const uint2*>(x + static_cast<size_t>(src) * Kd + k0);
       const uint32_t cw[2] = {c.x, c.y};
       uint32_t o[4];
 #pragma unroll
@@ -554,11 +563,12 @@ cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, in
 }
 
 cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_t* expert_ids, const int32_t* m_sum,
-                               int U, int Kd, int align, uint16_t* xb, cudaStream_t stream) {
+                               int U, int Kd, int align, uint16_t* xb, cudaStream_t stream, const int32_t* gather_ids,
+                               int K, int T) {
   const int bt = act_sf_block_rows(align);
   const int blocks = (U + 7) / 8 < 4 * num_sms() ? (U + 7) / 8 : 4 * num_sms();
   act_to_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(x, sf, expert_ids, m_sum, U, Kd, bt,
-                                                                  act_sf_blocks(U, bt), xb);
+                                                                  act_sf_blocks(U, bt), xb, gather_ids, K, T);
   return cudaGetLastError();
 }
 

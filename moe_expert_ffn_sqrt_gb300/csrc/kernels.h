@@ -40,6 +40,12 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
                            const uint8_t* x_q, const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
                            uint32_t* status, int32_t* scratch, cudaStream_t stream, int slot = 0);
 
+// Tiled scales of the permuted rows gathered from token-order scales x_sf [T, slabs] through
+// sorted_ids (row r < M_sum with expert_ids[r] >= 0 takes token sorted_ids[r] / K).
+cudaError_t launch_permute_act_sf(const int32_t* sorted_ids, int K, const int32_t* expert_ids, const int32_t* m_sum,
+                                  int U, int T, const uint8_t* x_sf, int slabs, int align, uint8_t* out,
+                                  cudaStream_t stream);
+
 // gate.cu (T > 16: gate GEMM on the tensor cores, three exact bf16 parts of the fp32 gate weight)
 int gate_nsplit(int T, int H, int E);
 size_t gate_parts_bytes(int T, int H, int E);
@@ -66,6 +72,11 @@ struct GemmLaunch {
   const float* row_w = nullptr;       // row_w[row_ids[r]] (the routing weight of the row's pair)
   const int32_t* counts = nullptr;    // BatchedExperts: tokens per expert slot (masked work list)
   int slot = 0;                       // BatchedExperts slot rows (a multiple of the block height)
+  // L1 gather mode: x is the token-order [gather_rows, Kd] activation and permuted row r reads row
+  // gather_ids[r] / gather_k of it (x_sf stays the tiled permuted scales)
+  const int32_t* gather_ids = nullptr;
+  int gather_k = 1;
+  int gather_rows = 0;
 };
 int num_sms();
 int weight_tiles(int N, int pair);
@@ -98,8 +109,12 @@ struct NvLaunch {
 size_t packed_nv_weight_bytes(int E, int N, int Kd, int pair);
 cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
                            cudaStream_t stream);
+// bf16 rows of the activation for rows r < m_sum with expert_ids[r] >= 0.  gather_ids null: x is
+// [U, Kd] with tiled scales (block rows from align); else x is token-order [T, Kd] with plain scales
+// [T, Kd/128] and row r reads token gather_ids[r] / K.
 cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_t* expert_ids, const int32_t* m_sum,
-                               int U, int Kd, int align, uint16_t* xb, cudaStream_t stream);
+                               int U, int Kd, int align, uint16_t* xb, cudaStream_t stream,
+                               const int32_t* gather_ids = nullptr, int K = 1, int T = 0);
 cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
 
 // gemm_i8.cu (INT8 W8A8 variant: int8 codes as fp16 on the 16-bit MMA, row and channel scales in the

@@ -290,9 +290,11 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
     a.sorted_ids[r] = N;
     a.expert_ids[r] = -1;
   }
-  if (x_perm != nullptr && N <= kSmallCopyPairs) {
+  if ((x_perm != nullptr || x_perm_sf != nullptr) && N <= kSmallCopyPairs) {
     // one warp per (pair, 1 KB piece of its row); the piece-0 warp also copies the row's scales
-    const int chunks = H / 16, slabs = H / 128, pieces = (chunks + kCopyPiece - 1) / kCopyPiece;
+    // (x_perm null: the scales alone, one warp per pair)
+    const int chunks = x_perm != nullptr ? H / 16 : 0, slabs = H / 128;
+    const int pieces = x_perm != nullptr ? (chunks + kCopyPiece - 1) / kCopyPiece : 1;
     for (int u = blockIdx.x * kPermWarps + warp; u < N * pieces; u += gridDim.x * kPermWarps) {
       const int p = u / pieces, piece = u - p * pieces;
       const int e = s_ids[p];
@@ -319,7 +321,8 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const Pe
   }
 }
 
-// Row copy: x_perm[inv_perm[t,k]] = x_q[t], scales into the tiled layout.  One warp per pair.
+// Row copy: x_perm[inv_perm[t,k]] = x_q[t] (skipped when x_perm is null), scales into the tiled
+// layout.  One warp per pair.
 __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __restrict__ inv_perm,
                                                            const int32_t* __restrict__ topk_ids, int T, int K, int E,
                                                            int H, const uint8_t* __restrict__ x_q,
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(256) permute_rows_kernel(const int32_t* __rest
   if (dst < 0) return;                         // dropped by a full BatchedExperts slot
   const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
   uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
-  const int chunks = H / 16;
+  const int chunks = x_perm != nullptr ? H / 16 : 0;
   for (int j0 = 0; j0 < chunks; j0 += 8 * 32) {      // eight 16-byte loads per lane in flight, then stores
     uint4 v[8];
 #pragma unroll
@@ -394,12 +397,13 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     const size_t smem = 2 * static_cast<size_t>(E) * sizeof(int32_t);
     err = cudaFuncSetAttribute(permute_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    const bool copy = x_perm != nullptr && npairs <= kSmallCopyPairs;
-    const long long units = npairs * ((H / 16 + kCopyPiece - 1) / kCopyPiece);
+    const bool any = x_perm != nullptr || x_perm_sf != nullptr;     // rows and scales, or scales alone
+    const bool copy = any && npairs <= kSmallCopyPairs;
+    const long long units = npairs * (x_perm != nullptr ? (H / 16 + kCopyPiece - 1) / kCopyPiece : 1);
     const int grid = copy && npairs > 0 ? static_cast<int>((units + kPermWarps - 1) / kPermWarps) : 1;
     err = launch_pdl(permute_small_kernel, dim3(grid), dim3(kPermThreads), smem, stream, a, x_q, x_sf, H, x_perm,
                      x_perm_sf, bt, nb);
-    if (err != cudaSuccess || x_perm == nullptr || copy) return err;
+    if (err != cudaSuccess || !any || copy) return err;
   } else {
     if (scratch == nullptr) return cudaErrorInvalidValue;
     const int G = permute_ctas(npairs), W = permute_warp_chunk(npairs, G);
@@ -413,11 +417,41 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int K, int E, int ali
     if (err != cudaSuccess) return err;
     permute_place_kernel<<<G, kPermThreads, smem, stream>>>(a, W, scratch);
     err = cudaGetLastError();
-    if (err != cudaSuccess || x_perm == nullptr) return err;
+    if (err != cudaSuccess || (x_perm == nullptr && x_perm_sf == nullptr)) return err;
   }
   if (npairs == 0) return cudaSuccess;
   permute_rows_kernel<<<static_cast<int>((npairs + 7) / 8), 256, 0, stream>>>(inv_perm, topk_ids, T, K, E, H, x_q, x_sf,
                                                                                x_perm, x_perm_sf, bt, nb);
+  return cudaGetLastError();
+}
+
+// Scales of the permuted rows from token-order scales: row r < M_sum with expert_ids[r] >= 0 takes
+// the scales of token sorted_ids[r] / K into the tiled layout.  One thread per (row, slab).
+__global__ void __launch_bounds__(256) permute_act_sf_kernel(const int32_t* __restrict__ sorted_ids, int K,
+                                                             const int32_t* __restrict__ expert_ids,
+                                                             const int32_t* __restrict__ m_sum, int U, int T,
+                                                             const uint8_t* __restrict__ x_sf, int slabs, int bt,
+                                                             int nb, uint8_t* __restrict__ out) {
+  const int msum = min(*m_sum, U);
+  const long long n = static_cast<long long>(msum) * slabs;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / slabs), s = static_cast<int>(i - static_cast<long long>(r) * slabs);
+    if (__ldg(expert_ids + r) < 0) continue;
+    const int t = __ldg(sorted_ids + r) / K;
+    if (t < 0 || t >= T) continue;
+    out[act_sf_offset(bt, nb, r, s)] = __ldg(x_sf + static_cast<size_t>(t) * slabs + s);
+  }
+}
+
+cudaError_t launch_permute_act_sf(const int32_t* sorted_ids, int K, const int32_t* expert_ids, const int32_t* m_sum,
+                                  int U, int T, const uint8_t* x_sf, int slabs, int align, uint8_t* out,
+                                  cudaStream_t stream) {
+  const int bt = act_sf_block_rows(align);
+  const long long n = static_cast<long long>(U) * slabs;
+  const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 4 * 152));
+  permute_act_sf_kernel<<<grid < 1 ? 1 : grid, 256, 0, stream>>>(sorted_ids, K, expert_ids, m_sum, U, T, x_sf, slabs,
+                                                                  bt, act_sf_blocks(U, bt), out);
   return cudaGetLastError();
 }
 

@@ -103,12 +103,20 @@ def test_invalid_arguments_are_rejected(M):
     w = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 2)
     # misaligned weight pointer
     wbad = M._Weight(0x10010, None, M.W_MXFP4, 16, 512, 512, 2)
-    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wbad, fake, fake, ws, 4096,
-                                        None) == M.ERR_INVALID_ARG
+    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, 1, None, fake, fake, 8, 2, 512, 256, 16, 16, wbad, fake, fake, ws,
+                                        4096, None) == M.ERR_INVALID_ARG
     # W13 must be packed with pair = 2 and the matching shape
     wpair = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 1)
-    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wpair, fake, fake, ws, 4096,
-                                        None) == M.ERR_INVALID_ARG
+    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, 1, None, fake, fake, 8, 2, 512, 256, 16, 16, wpair, fake, fake, ws,
+                                        4096, None) == M.ERR_INVALID_ARG
+    # token-order input (a_is_permuted = 0) needs sorted_token_ids
+    assert L.moe_grouped_gemm_l1_swiglu(fake, fake, 0, None, fake, fake, 8, 2, 512, 256, 16, 16, w, fake, fake, ws,
+                                        4096, None) == M.ERR_INVALID_ARG
+    assert L.moe_grouped_ffn(fake, fake, 0, None, fake, fake, 8, 2, 512, 256, 16, 16, w, w, fake, fake, fake, ws,
+                             4096, None) == M.ERR_INVALID_ARG
+    # scales without rows is a valid permute mode; rows without scales is not
+    assert L.moe_permute(fake, 8, 2, 16, 16, fake, fake, fake, fake, None, fake, None, 128, fake, None, ws, 4096,
+                         None) == M.ERR_INVALID_ARG
     # NVFP4 needs a tensor scale pointer
     wnv = M._Weight(0x10000, None, M.W_NVFP4, 16, 512, 256, 1)
     assert L.moe_grouped_gemm_l2(fake, fake, fake, fake, 8, 2, 512, 256, 16, 16, wnv, fake, ws, 4096,
