@@ -55,7 +55,7 @@ def launches_per_forward(w, naive=False):
     if naive:
         permute = 0                               # the routing launch writes the tiny-batch layout
     elif w.fmt == "nvfp4":
-        permute = 1 if tk <= 1024 else 2          # token-order L1 input: no row or scale copy
+        permute = 1 if tk <= 1024 else 2          # NVFP4 reads the token-order rows: no row or scale copy
     if w.fmt == "mxfp4":
         ffn = 1                                   # L1 and L2 in one launch
     else:
@@ -99,9 +99,10 @@ def parse_args():
     p.add_argument("--weights", default="workload", choices=["workload", "int8"],
                    help="the workload's FP4 weight format, or the INT8 variant (int8 weights with per-channel "
                         "scales, int8 activations with per-token scales: moe_forward_i8) on the same shapes")
-    p.add_argument("--l1-input", default="token", choices=["token", "permuted"],
+    p.add_argument("--l1-input", default="auto", choices=["auto", "token", "permuted"],
                    help="stage-by-stage timing: the L1 GEMM reads the token-order activation through "
-                        "sorted_token_ids (as moe_forward does) or the permute's row copy x_perm")
+                        "sorted_token_ids or the permute's row copy x_perm; auto: as moe_forward does "
+                        "(token order with NVFP4 weights, the copy with MXFP4)")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
                         "BatchedExperts slots of max_tokens = max(16, the smallest power of two >= T) (moe_forward_batched) or "
@@ -438,7 +439,8 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     # (INT8: the routing stage includes the per-token quantisation, L1 the row gather and the h requant,
     # L2 the conversion of h to fp16 rows)
     fused = w.fmt == "mxfp4" or batched
-    token_order = args.l1_input == "token" and not (batched or naive or i8)
+    token_order = (args.l1_input == "token" or (args.l1_input == "auto" and w.fmt == "nvfp4")) and not (
+        batched or naive or i8)
     stages = ["route", "permute", "ffn", "reduce"] if fused else ["route", "permute", "l1", "l2", "reduce"]
     if naive:
         stages.remove("permute")
@@ -489,11 +491,12 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
                           sorted_token_ids=srt)
         elif fused:
             M.grouped_ffn(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, w2, hq, hsf, y, ws)
-        elif token_order:
-            M.grouped_gemm_l1_swiglu(xq, xsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws,
-                                     sorted_token_ids=srt)
         else:
-            M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws)
+            if token_order:
+                M.grouped_gemm_l1_swiglu(xq, xsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws,
+                                         sorted_token_ids=srt)
+            else:
+                M.grouped_gemm_l1_swiglu(xp, xpsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w13, hq, hsf, ws)
             j += 1
             e[j].record()
             M.grouped_gemm_l2(hq, hsf, eids, msum, T, w.K, w.H, w.I, w.E, align, w2, y, ws)
@@ -564,7 +567,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
                      "expert-contiguous, padded to align")
     cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
                               "stage calls)" if args.weights_in_l1 else "applied in the reduce")
-    cfg["l1_input"] = ("token-order rows read through sorted_token_ids" if not (batched or naive or i8) else
+    cfg["l1_input"] = ("token-order rows read through sorted_token_ids" if w.fmt == "nvfp4" and not batched else
                        "permuted row copy")
     cfg["stage_l1_input"] = "token-order" if token_order else "permuted copy"
     res = dict(value=value, ms=ms, steps=K, warmup=warmup, roofline=roofline, e2e=e2e, cpu=cpu, cfg=cfg,

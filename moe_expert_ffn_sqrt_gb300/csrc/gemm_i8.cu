@@ -70,6 +70,7 @@ struct I8Args {
   int out_cols;                 // I (L1) or H (L2)
   int n_tiles;
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
+  int split_pairs;              // items are halves of row-block pairs (small blocks) or whole pairs
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
@@ -543,7 +544,9 @@ cudaError_t launch_i8_t(const I8Launch& L, cudaStream_t stream) {
   a.out_cols = L1 ? L.I : L.w_rows;
   a.one_expert_blocks = L.align % BN == 0;
   const int nrb = (L.U + BN - 1) / BN;
-  a.n_tiles = (a.one_expert_blocks ? (nrb + 1) / 2 * 2 : nrb) * a.n_wt;   // items: halves of row-block pairs, or blocks
+  // items: halves of row-block pairs (blocks of up to 32 rows), whole pairs, or blocks
+  a.split_pairs = BN <= 32;
+  a.n_tiles = (a.one_expert_blocks ? (a.split_pairs ? (nrb + 1) / 2 * 2 : (nrb + 1) / 2) : nrb) * a.n_wt;
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;

@@ -66,6 +66,7 @@ struct NvArgs {
   int sf_nb;
   int n_tiles;
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
+  int split_pairs;              // items are halves of row-block pairs (small blocks) or whole pairs
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
   const int32_t* row_ids;       // L1: h of row r scaled by row_w[row_ids[r]] when row_w != nullptr
   const float* row_w;
@@ -539,7 +540,9 @@ cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
   a.sf_nb = act_sf_blocks(L.U, BN);
   a.one_expert_blocks = L.align % BN == 0;
   const int nrb = (L.U + BN - 1) / BN;
-  a.n_tiles = (a.one_expert_blocks ? (nrb + 1) / 2 * 2 : nrb) * a.n_wt;   // items: halves of row-block pairs, or blocks
+  // items: halves of row-block pairs (blocks of up to 32 rows), whole pairs, or blocks
+  a.split_pairs = BN <= 32;
+  a.n_tiles = (a.one_expert_blocks ? (a.split_pairs ? (nrb + 1) / 2 * 2 : (nrb + 1) / 2) : nrb) * a.n_wt;
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
