@@ -464,7 +464,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;                  // TMEM lane quarter this warp may access
     const int half = (warp - 2) >> 2;
     const int m = q * 32 + lane;
-    const bool warp_has_rows = q * 32 < BN;  // warp-uniform
+    // Every epilogue warp drains its lane quarter, also when the block has no rows there (BN < 128):
+    // those values are never stored (`mine` is false), and one code path for all warps keeps the
+    // epilogue within the 168 registers a thread has without spilling (a per-warp branch around the
+    // loads spilled 56 bytes at BN = 16, 32, 64).
+    const bool warp_has_rows = true;
     const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0;
     uint32_t islot = 0, iphase = 0;
