@@ -26,6 +26,18 @@ Readings where the page is silent:
 * the expert GEMMs are exact integer dot products of the codes, then scaled
   by the row scale and the channel scale (here in float64); L2 rounds to
   bfloat16 per row as in the FP8 path; topk_weight is applied in the gather.
+
+Block-quantised weights, the page's ``[256, 256]`` read the other way (§3.1
+relaxes the batched expert GEMM's checks "to support INT8 with
+block_shape [256, 256]"): ``fmt = "int8b"``.
+* weights: int8 codes, one float32 scale per block of 256 output rows x 256
+  reduction columns: w[n, k] = q[n, k] * s[n // 256, k // 256].
+* activations (the layer input and the SwiGLU output) are int8 with one
+  float32 scale per row and 256-column group, each group quantised by the
+  per-row rule above (a group's amax, its own scale).
+* the expert GEMMs: per 256-deep block kb of the reduction, the exact
+  integer dot product of the codes, times the row's group scale of kb and
+  the weight block's scale of kb; the blocks' terms summed (float64 here).
 """
 from typing import Callable, Dict
 
@@ -92,12 +104,80 @@ def expert_l2_i8(h_q: np.ndarray, h_s: np.ndarray, w2_q: np.ndarray, w2_s: np.nd
     return round_bf16_rne(acc * np.asarray(h_s, np.float64)[:, None] * np.asarray(w2_s, np.float64)[None, :])
 
 
+# ----------------------------------------------------------------------------
+# [256, 256] block-quantised weights ("int8b")
+
+I8_BLOCK = 256
+
+
+def quantize_i8_groups(x: np.ndarray, group: int = I8_BLOCK):
+    """x [R, C] (C a multiple of group) -> (q [R, C] int8, s [R, C/group] float32): every group of
+    ``group`` columns of a row quantised as its own row (quantize_i8_rows)."""
+    x = np.asarray(x)
+    R, C = x.shape
+    assert C % group == 0
+    q, s = quantize_i8_rows(x.reshape(R * (C // group), group))
+    return q.reshape(R, C), s.reshape(R, C // group)
+
+
+def act_quant_i8_groups(hidden_bits: np.ndarray, group: int = I8_BLOCK):
+    """hidden bf16 bits [T, H] -> x_q int8 [T, H], x_s float32 [T, H/group]."""
+    return quantize_i8_groups(bf16_to_f64(hidden_bits), group)
+
+
+def dequant_i8_groups(q: np.ndarray, s: np.ndarray, group: int = I8_BLOCK) -> np.ndarray:
+    """codes [R, C] with one scale per (row, group) [R, C/group] -> float64 [R, C]."""
+    q = np.asarray(q, dtype=np.float64)
+    R, C = q.shape
+    sc = np.asarray(s, dtype=np.float32).astype(np.float64)
+    return (q.reshape(R, C // group, group) * sc[:, :, None]).reshape(R, C)
+
+
+def dequant_i8_blocks(q: np.ndarray, s: np.ndarray, block: int = I8_BLOCK) -> np.ndarray:
+    """weight codes [N, Kd] with one scale per (block x block) [N/block, Kd/block] -> float64 [N, Kd]."""
+    q = np.asarray(q, dtype=np.float64)
+    sc = np.asarray(s, dtype=np.float32).astype(np.float64)
+    return q * np.repeat(np.repeat(sc, block, axis=0), block, axis=1)
+
+
+def i8_block_gemm(a_q: np.ndarray, a_s: np.ndarray, w_q: np.ndarray, w_s: np.ndarray,
+                  block: int = I8_BLOCK) -> np.ndarray:
+    """out[r, n] = sum_kb a_s[r, kb] * w_s[n // block, kb] * (sum_{k in kb} a_q[r, k] * w_q[n, k]), float64.
+
+    a_q [R, Kd] int8, a_s [R, Kd/block]; w_q [N, Kd] int8, w_s [N/block, Kd/block]."""
+    R, Kd = a_q.shape
+    N = w_q.shape[0]
+    out = np.zeros((R, N), dtype=np.float64)
+    ws_rows = np.repeat(np.asarray(w_s, dtype=np.float32).astype(np.float64), block, axis=0)   # [N, Kd/block]
+    for kb in range(Kd // block):
+        cols = slice(kb * block, (kb + 1) * block)
+        d = i8_dot(a_q[:, cols], w_q[:, cols]).astype(np.float64)        # exact integers
+        out += d * np.asarray(a_s, np.float32).astype(np.float64)[:, kb:kb + 1] * ws_rows[None, :, kb][0]
+    return out
+
+
+def expert_l1_swiglu_i8_block(x_q, x_s, w13_q, w13_s, I: int):
+    """L1 with [256, 256] weight blocks and per-256-group activation scales; h = bf16(silu(gate) * up)
+    quantised per (row, 256-group).  Returns (h float64 [R, I], h_q int8 [R, I], h_s float32 [R, I/256])."""
+    gu = i8_block_gemm(x_q, x_s, w13_q, w13_s)
+    g, u = gu[:, :I], gu[:, I:]
+    h = bf16_to_f64(round_bf16_rne(silu(g) * u))
+    h_q, h_s = quantize_i8_groups(h)
+    return h, h_q, h_s
+
+
+def expert_l2_i8_block(h_q, h_s, w2_q, w2_s) -> np.ndarray:
+    """y = bf16(block GEMM of h against W2) as bf16 bits [R, H]."""
+    return round_bf16_rne(i8_block_gemm(h_q, h_s, w2_q, w2_s))
+
+
 WeightProvider = Callable[[int], dict]
 """expert e -> dict(w13_q int8 [2I, H], w13_sf float32 [2I], w2_q int8 [H, I], w2_sf float32 [H])."""
 
 
 def forward_i8(inp: dict, weights: WeightProvider, K: int, align: int, score_fn: str,
-               renormalize: bool = True, tokens=None, topk_w_dtype=np.float64, routing=None) -> Dict[str, object]:
+               renormalize: bool = True, tokens=None, topk_w_dtype=np.float64, routing=None,
+               block: bool = False) -> Dict[str, object]:
     """Route -> per-token int8 quantisation -> permute -> per expert: integer L1, SwiGLU, bf16,
     per-row int8 requant, integer L2 -> bf16 rows -> weighted reduce (bf16).
 
@@ -105,6 +185,8 @@ def forward_i8(inp: dict, weights: WeightProvider, K: int, align: int, score_fn:
     ``out`` and ``x_q``/``x_s`` then hold only those tokens' rows, in the order given.
     ``topk_w_dtype``: precision of the routing weights in the final sum.
     ``routing``: optional dict with topk_ids [T,K] and topk_w [T,K] used in place of the computed routing.
+    ``block``: [256, 256] block-quantised weights (w*_sf [N/256, Kd/256]) and per-256-group activation
+    scales (``x_s`` then [len(tokens), H/256]).
     """
     hidden = inp["hidden"]
     T, H = hidden.shape
@@ -116,7 +198,7 @@ def forward_i8(inp: dict, weights: WeightProvider, K: int, align: int, score_fn:
                  topk_w=np.asarray(routing["topk_w"], dtype=np.float64))
     p = permute(r["topk_ids"], E, align)
     tok = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    q_rows, s_rows = act_quant_i8(hidden[tok])
+    q_rows, s_rows = act_quant_i8_groups(hidden[tok]) if block else act_quant_i8(hidden[tok])
     x_q = {int(t): q_rows[i] for i, t in enumerate(tok)}
     x_s = {int(t): s_rows[i] for i, t in enumerate(tok)}
     need = {}
@@ -128,9 +210,13 @@ def forward_i8(inp: dict, weights: WeightProvider, K: int, align: int, score_fn:
         w = weights(e)
         I = w["w13_q"].shape[0] // 2
         ts = sorted(set(ts))
-        _, hq, hs = expert_l1_swiglu_i8(np.stack([x_q[t] for t in ts]), np.array([x_s[t] for t in ts]),
-                                        w["w13_q"], w["w13_sf"], I)
-        y = expert_l2_i8(hq, hs, w["w2_q"], w["w2_sf"])
+        xq_e, xs_e = np.stack([x_q[t] for t in ts]), np.array([x_s[t] for t in ts])
+        if block:
+            _, hq, hs = expert_l1_swiglu_i8_block(xq_e, xs_e, w["w13_q"], w["w13_sf"], I)
+            y = expert_l2_i8_block(hq, hs, w["w2_q"], w["w2_sf"])
+        else:
+            _, hq, hs = expert_l1_swiglu_i8(xq_e, xs_e, w["w13_q"], w["w13_sf"], I)
+            y = expert_l2_i8(hq, hs, w["w2_q"], w["w2_sf"])
         for j, t in enumerate(ts):
             y_rows[(t, e)] = y[j]
             h_rows[(t, e)] = (hq[j], hs[j])

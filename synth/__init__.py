@@ -30,7 +30,8 @@ Distributions:
   with probabilities proportional to exp(-c**2 / (2 * 40**2)) (a discretised
   normal of spread 40, drawn through a 16-bit lookup table), and one float32
   scale per output channel uniform in [4.5e-4, 5.5e-4), again an RMS of
-  about 0.02.
+  about 0.02.  ``fmt="int8b"``: the same codes with one float32 scale per
+  256 x 256 block, uniform in the same range.
 Each expert's weights come from their own generator, seeded by
 (seed, matrix, expert), so any expert can be regenerated alone.
 """
@@ -131,6 +132,11 @@ def i8_channel_scales(rng: np.random.Generator, rows: int) -> np.ndarray:
     return rng.uniform(4.5e-4, 5.5e-4, size=rows).astype(np.float32)
 
 
+def i8_block_scales(rng: np.random.Generator, rows: int, cols: int) -> np.ndarray:
+    """[rows/256, cols/256] float32 scales of 256 x 256 weight blocks, uniform in [4.5e-4, 5.5e-4)."""
+    return rng.uniform(4.5e-4, 5.5e-4, size=(rows // 256, cols // 256)).astype(np.float32)
+
+
 def mx_scales(rng: np.random.Generator, rows: int, cols: int, wide: bool = False) -> np.ndarray:
     """[rows, cols/32] UE8M0 bytes, 120 or 121 (2**-7 or 2**-6); ``wide``: uniform over 97..131
     (2**-30 .. 2**4)."""
@@ -152,13 +158,14 @@ def expert_weights(w: Workload, e: int) -> dict:
 
     FP4 formats: ``*_q`` packed E2M1 [N, Kd/2], ``*_sf`` block scales, ``*_ts`` NVFP4 tensor scale.
     INT8: ``*_q`` int8 [N, Kd], ``*_sf`` float32 channel scales [N], ``*_ts`` None.
+    INT8 with [256, 256] blocks ("int8b"): ``*_sf`` float32 block scales [N/256, Kd/256].
     """
     out = {}
     for mat, (rows, cols) in (("w13", (2 * w.I, w.H)), ("w2", (w.H, w.I))):
         rng = _rng(w.seed, 1 if mat == "w13" else 2, e)
-        if w.fmt == "int8":
+        if w.fmt in ("int8", "int8b"):
             out[mat + "_q"] = i8_codes(rng, rows, cols)
-            out[mat + "_sf"] = i8_channel_scales(rng, rows)
+            out[mat + "_sf"] = i8_channel_scales(rng, rows) if w.fmt == "int8" else i8_block_scales(rng, rows, cols)
             out[mat + "_ts"] = None
             continue
         out[mat + "_q"] = fp4_codes(rng, rows, cols)

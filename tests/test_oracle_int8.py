@@ -172,3 +172,119 @@ def test_l2_linear_in_row_and_channel_scales():
     ws2[5] *= 2
     y3 = F.bf16_to_f64(Q.expert_l2_i8(hq, hs, w2, ws2))
     assert np.array_equal(y3[:, 5], 2 * y[:, 5]) and np.array_equal(np.delete(y3, 5, 1), np.delete(y, 5, 1))
+
+
+# ---------------------------------------------------------------------------- [256, 256] block-quantised weights
+
+
+def test_quantize_groups_by_hand():
+    # two groups of 256 with their own amax: each group is quantised as a row of its own
+    x = np.zeros((1, 512))
+    x[0, 0], x[0, 1], x[0, 2] = 2.0, -1.0, 0.5           # group 0: amax 2 -> inv = fp32(127/2) = 63.5
+    x[0, 256], x[0, 300] = 0.25, -0.125                   # group 1: amax 0.25 -> inv = 508
+    q, s = Q.quantize_i8_groups(x)
+    assert s.shape == (1, 2)
+    assert s[0, 0] == np.float32(2.0) / np.float32(127) and s[0, 1] == np.float32(0.25) / np.float32(127)
+    # 2 * 63.5 = 127; -1 * 63.5 = -63.5 -> -64 (ties to even); 0.5 * 63.5 = 31.75 -> 32
+    assert q[0, :3].tolist() == [127, -64, 32]
+    # 0.25 * 508 = 127; -0.125 * 508 = -63.5 -> -64
+    assert q[0, 256] == 127 and q[0, 300] == -64
+    assert (q[0, 3:256] == 0).all() and (np.delete(q[0, 256:], [0, 44]) == 0).all()
+    # an all-zero group: codes 0, scale 0
+    q0, s0 = Q.quantize_i8_groups(np.zeros((2, 256)))
+    assert (q0 == 0).all() and (s0 == 0).all()
+
+
+def test_dequant_blocks_by_hand():
+    rng = np.random.default_rng(41)
+    q = rng.integers(-127, 128, size=(512, 512)).astype(np.int8)
+    s = np.array([[0.5, 2.0], [0.25, 3.0]], np.float32)
+    w = Q.dequant_i8_blocks(q, s)
+    for n, k in [(0, 0), (255, 255), (0, 256), (256, 0), (511, 511), (300, 17), (17, 300)]:
+        assert w[n, k] == float(q[n, k]) * float(s[n // 256, k // 256])
+
+
+def test_block_gemm_brute_force():
+    rng = np.random.default_rng(42)
+    R, N, Kd = 2, 256, 512
+    a_q = rng.integers(-127, 128, size=(R, Kd)).astype(np.int8)
+    a_s = rng.uniform(1e-3, 1e-2, size=(R, 2)).astype(np.float32)
+    w_q = rng.integers(-127, 128, size=(N, Kd)).astype(np.int8)
+    w_s = rng.uniform(1e-4, 1e-3, size=(1, 2)).astype(np.float32)
+    out = Q.i8_block_gemm(a_q, a_s, w_q, w_s)
+    for r in range(R):
+        for n in (0, 77, 255):
+            terms = [int(a_q[r, k]) * int(w_q[n, k]) * float(a_s[r, k // 256]) * float(w_s[0, k // 256])
+                     for k in range(Kd)]
+            assert math.isclose(out[r, n], math.fsum(terms), rel_tol=1e-13, abs_tol=1e-18)
+
+
+def test_block_l1_against_dequantised_float_gemm():
+    # dequantise activations and weights first, then a float64 GEMM: the same values up to float64 rounding
+    rng = np.random.default_rng(43)
+    R, H, I = 7, 512, 256
+    x_q, x_s = Q.quantize_i8_groups(F.bf16_to_f64(synth.bf16_rows(rng, R, H)))
+    w13_q = synth.i8_codes(rng, 2 * I, H)
+    w13_s = synth.i8_block_scales(rng, 2 * I, H)
+    h, hq, hs = Q.expert_l1_swiglu_i8_block(x_q, x_s, w13_q, w13_s, I)
+    gu = Q.dequant_i8_groups(x_q, x_s) @ Q.dequant_i8_blocks(w13_q, w13_s).T
+    ref = F.bf16_to_f64(F.round_bf16_rne(moe.silu(gu[:, :I]) * gu[:, I:]))
+    assert np.abs(h - ref).max() <= np.abs(ref).max() * 2.0 ** -8
+    assert (h == ref).mean() > 0.999
+    assert hs.shape == (R, I // 256)
+    q2, s2 = Q.quantize_i8_groups(h)
+    assert np.array_equal(hq, q2) and np.array_equal(hs, s2)
+
+
+def test_block_variant_reduces_to_channel_wise_with_uniform_scales():
+    # one scale for every group of a row and one for every weight block: the block GEMM is the
+    # channel-wise one with that row scale and a constant channel scale
+    rng = np.random.default_rng(44)
+    R, H, I = 5, 512, 256
+    x_q = synth.i8_codes(rng, R, H)
+    row_s = rng.uniform(1e-3, 1e-2, size=R).astype(np.float32)
+    w13_q = synth.i8_codes(rng, 2 * I, H)
+    c = np.float32(5e-4)
+    hb, _, _ = Q.expert_l1_swiglu_i8_block(x_q, np.repeat(row_s[:, None], H // 256, 1), w13_q,
+                                           np.full((2 * I // 256, H // 256), c, np.float32), I)
+    hc, _, _ = Q.expert_l1_swiglu_i8(x_q, row_s, w13_q, np.full(2 * I, c, np.float32), I)
+    assert np.abs(hb - hc).max() <= np.abs(hc).max() * 2.0 ** -8 and (hb == hc).mean() > 0.999
+
+
+def test_block_l2_linear_in_block_scales():
+    rng = np.random.default_rng(45)
+    R, H, I = 4, 256, 512
+    h_q = synth.i8_codes(rng, R, I)
+    h_s = rng.uniform(1e-3, 1e-2, size=(R, I // 256)).astype(np.float32)
+    w2_q = synth.i8_codes(rng, H, I)
+    w2_s = synth.i8_block_scales(rng, H, I)
+    y1 = F.bf16_to_f64(Q.expert_l2_i8_block(h_q, h_s, w2_q, w2_s))
+    y2 = F.bf16_to_f64(Q.expert_l2_i8_block(h_q, h_s, w2_q, w2_s * np.float32(2)))
+    assert np.array_equal(y2, 2 * y1)
+    # a weight block's scale reaches only its own 256 reduction columns
+    w2_z = w2_s.copy()
+    w2_z[:, 1] = 0
+    yz = F.bf16_to_f64(Q.expert_l2_i8_block(h_q, h_s, w2_q, w2_z))
+    h0 = h_q.copy()
+    h0[:, 256:] = 0
+    assert np.array_equal(yz, F.bf16_to_f64(Q.expert_l2_i8_block(h0, h_s, w2_q, w2_s)))
+
+
+def test_block_forward_wiring_against_per_token_loop():
+    w = synth.custom(T=9, H=512, I=256, E=6, K=2, align=4, fmt="int8b", score_fn="sqrt_softplus", e_bias=True,
+                     seed=46)
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    get = lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()}
+    res = Q.forward_i8(inp, get, w.K, w.align, w.score_fn, w.renormalize, block=True)
+    r = res["route"]
+    xq, xs = Q.act_quant_i8_groups(inp["hidden"])
+    assert np.array_equal(res["x_q"], xq) and np.array_equal(res["x_s"], xs)
+    for t in range(w.T):
+        acc = np.zeros(w.H)
+        for k in range(w.K):
+            e = int(r["topk_ids"][t, k])
+            _, hq, hs = Q.expert_l1_swiglu_i8_block(xq[t:t + 1], xs[t:t + 1], stack["w13_q"][e], stack["w13_sf"][e], w.I)
+            y = F.bf16_to_f64(Q.expert_l2_i8_block(hq, hs, stack["w2_q"][e], stack["w2_sf"][e]))[0]
+            acc += r["topk_w"][t, k] * y
+        assert np.array_equal(res["out"][t], F.round_bf16_rne(acc))
