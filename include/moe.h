@@ -65,8 +65,10 @@ typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score_fn
  *   MXFP4: E2M1 codes + one UE8M0 scale per 32 along the reduction dim.
  *   NVFP4: E2M1 codes + one E4M3 scale per 16 along the reduction dim + one fp32 scale per
  *          expert matrix.
- *   INT8:  int8 codes + one fp32 scale per output channel (row); only the *_i8 calls take it. */
-typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1, MOE_W_INT8 = 2 } moe_wfmt;
+ *   INT8:  int8 codes + one fp32 scale per output channel (row); only the *_i8 calls take it.
+ *   INT8_B256: int8 codes + one fp32 scale per block of 256 output rows x 256 reduction columns
+ *          (§3.1 "INT8 with block_shape [256, 256]"); only the *_i8 calls take it. */
+typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1, MOE_W_INT8 = 2, MOE_W_INT8_B256 = 3 } moe_wfmt;
 
 /* One stacked expert weight tensor with logical shape [E, N, Kd] (N output rows, Kd the
  * reduction dim), in the packed stream written by moe_pack_weights.  W13: N = 2I, Kd = H,
@@ -75,7 +77,8 @@ typedef enum { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1, MOE_W_INT8 = 2 } moe_wfmt;
 typedef struct {
   const uint8_t* packed;  /* moe_pack_weights output (32-byte aligned)                        */
   const float* tscale;    /* NVFP4: [E] fp32 per-matrix scale; INT8: [E, N] fp32 per-output-  *
-                           * channel scales (logical row order, 16-byte aligned); MXFP4: NULL */
+                           * channel scales (logical row order, 16-byte aligned); INT8_B256:    *
+                           * [E, N/256, Kd/256] fp32 block scales; MXFP4: NULL                 */
   moe_wfmt fmt;
   int E, N, Kd;           /* logical shape                                                    */
   int pair;               /* 2 for W13 (gate/up row tiles interleaved), 1 for W2              */
@@ -385,6 +388,11 @@ moe_status moe_forward_naive(const uint16_t* hidden, const float* w_gate, const 
  * the 16-bit tensor cores with fp16 operands, summed in fp32) times the row scale times the channel
  * scale; L1 rounds silu(gate) * up to bf16 and then quantises each row of h.  Routing, the permute
  * and the reduce are those of the FP4 path; the index arrays have the same meaning.
+ * With MOE_W_INT8_B256 weights (both w13 and w2; H and I multiples of 256) every activation scale
+ * is per row and 256-column group instead ([rows, cols/256], each group quantised by the rule
+ * above), and the GEMMs sum, over the 256-deep blocks kb of the reduction, the integer dot product
+ * of the block times the row's group scale of kb times the weight block's scale (fp32 sums); the
+ * x_s / h_s arguments below are then [T, H/256] / [U, I/256].
  * ------------------------------------------------------------------------------------ */
 
 /* Workspace bytes of the INT8 calls (moe_workspace_size's layout plus the INT8 row scales and a
@@ -394,6 +402,10 @@ moe_status moe_workspace_size_i8(int T, int H, int I, int E, int K, int align, s
 /* Per-row int8 quantisation by the rule above: x [rows, cols] bf16 -> x_q [rows, cols] int8,
  * x_s [rows] fp32.  cols a multiple of 128; x and x_q 16-byte aligned.  No workspace. */
 moe_status moe_act_quant_i8(const uint16_t* x, int rows, int cols, int8_t* x_q, float* x_s, void* stream);
+
+/* The same rule per 256-column group (the activations of the MOE_W_INT8_B256 layer): x [rows, cols]
+ * bf16 -> x_q [rows, cols] int8, x_s [rows, cols/256] fp32.  cols a multiple of 256. */
+moe_status moe_act_quant_i8_b256(const uint16_t* x, int rows, int cols, int8_t* x_q, float* x_s, void* stream);
 
 /* L1 + SwiGLU + per-row int8 requant.  The activation rows are read in token order and gathered
  * through sorted_token_ids (row r of the permuted layout is token sorted_token_ids[r] / K):

@@ -102,8 +102,12 @@ bool weight_ok(const moe_weight& w, int E, int N, int Kd, int pair) {
 // An INT8 weight (the INT8 calls take no other format, and the FP4 calls no INT8 weight).
 bool weight_ok_i8(const moe_weight& w, int E, int N, int Kd, int pair) {
   if (!w.packed || !aligned(w.packed, 32) || !w.tscale || !aligned(w.tscale, 16)) return false;
-  return w.fmt == MOE_W_INT8 && w.E == E && w.N == N && w.Kd == Kd && w.pair == pair;
+  if (w.fmt == MOE_W_INT8_B256 && (N % 256 || Kd % 256)) return false;
+  return (w.fmt == MOE_W_INT8 || w.fmt == MOE_W_INT8_B256) && w.E == E && w.N == N && w.Kd == Kd && w.pair == pair;
 }
+
+// Scales per activation row of an INT8 operand with `cols` columns: one, or one per 256 columns.
+inline int i8_row_scales(bool block, int cols) { return block ? cols / 256 : 1; }
 
 // INT8 variant: the common layout (its x_q, h_q and xb regions hold the int8 token rows, the int8 h
 // and the fp16 operand rows) plus the per-row scales and the bf16 h between L1 and its quantisation.
@@ -118,9 +122,11 @@ I8Layout layout_i8(int T, int H, int I, int E, int K, int align, size_t U = 0) {
   I8Layout r;
   r.L = layout_rows(T, H, I, E, K, align, U);
   size_t off = r.L.total;
-  r.x_s = off;  off = up(off + static_cast<size_t>(T) * 4);   // token scales
-  r.a_s = off;  off = up(off + U * 4);                         // per-row scales of the GEMM operand rows
-  r.h_s = off;  off = up(off + U * 4);                         // h scales (forward)
+  // scale regions sized for the block format too (a scale per row and 256-column group)
+  const size_t nh = H >= 256 ? static_cast<size_t>(H) / 256 : 1, ni = I >= 256 ? static_cast<size_t>(I) / 256 : 1;
+  r.x_s = off;  off = up(off + static_cast<size_t>(T) * nh * 4);            // token scales
+  r.a_s = off;  off = up(off + U * (nh > ni ? nh : ni) * 4);                 // scales of the GEMM operand rows
+  r.h_s = off;  off = up(off + U * ni * 4);                                  // h scales (forward)
   r.hb = off;   off = up(off + U * I * 2);                     // bf16 h
   r.total = off;
   return r;
@@ -164,7 +170,7 @@ size_t moe_weight_packed_bytes(moe_wfmt fmt, int E, int N, int Kd, int pair) {
   if (pair == 2 ? N % 256 : N % 128) return 0;
   if (fmt == MOE_W_MXFP4) return packed_weight_bytes(E, N, Kd, pair);
   if (fmt == MOE_W_NVFP4) return packed_nv_weight_bytes(E, N, Kd, pair);
-  if (fmt == MOE_W_INT8) return packed_i8_weight_bytes(E, N, Kd, pair);
+  if (fmt == MOE_W_INT8 || fmt == MOE_W_INT8_B256) return packed_i8_weight_bytes(E, N, Kd, pair);
   return 0;
 }
 
@@ -172,7 +178,7 @@ moe_status moe_pack_weights(moe_wfmt fmt, const uint8_t* q, const uint8_t* sf, i
                             uint8_t* packed, void* stream) {
   if (!q || !packed || E <= 0 || N <= 0 || Kd <= 0 || Kd % 128) return MOE_ERR_INVALID_ARG;
   if ((pair != 1 && pair != 2) || (pair == 2 ? N % 256 : N % 128)) return MOE_ERR_INVALID_ARG;
-  if (fmt == MOE_W_INT8) {
+  if (fmt == MOE_W_INT8 || fmt == MOE_W_INT8_B256) {
     if (!aligned(q, 16) || !aligned(packed, 16)) return MOE_ERR_INVALID_ARG;
     return cuda_status(launch_pack_i8(reinterpret_cast<const int8_t*>(q), E, N, Kd, pair, packed, S(stream)));
   }
@@ -335,6 +341,29 @@ static GemmLaunch mx_launch(bool l1, const uint8_t* x, const uint8_t* x_sf, cons
 // gather_ids non-null (L1 only): x = token-order activation [T, H] and x_sf its plain scales
 // [T, H/128]; permuted row r reads token gather_ids[r] / K (the MXFP4 path first writes the
 // permuted rows' tiled scales into the workspace; the rows themselves are gathered by the GEMM).
+// Launch description of one NVFP4 GEMM (bf16 operand rows xb [U, Kd]).
+static NvLaunch nv_launch(bool l1, const uint16_t* xb, const int32_t* expert_ids, const int32_t* m_sum, int H, int I,
+                          int E, int align, size_t U, const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y,
+                          void* ws) {
+  NvLaunch N;
+  N.w = w.packed;
+  N.tscale = w.tscale;
+  N.xb = xb;
+  N.expert_ids = expert_ids;
+  N.m_sum = m_sum;
+  N.h_q = h_q;
+  N.h_sf = h_sf;
+  N.y = y;
+  N.status = status_of(ws);
+  N.E = E;
+  N.w_rows = l1 ? 2 * I : H;
+  N.Kd = l1 ? H : I;
+  N.I = I;
+  N.U = static_cast<int>(U);
+  N.align = align;
+  return N;
+}
+
 static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, const int32_t* expert_ids,
                               const int32_t* m_sum, int T, int K, int H, int I, int E, int align,
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
@@ -361,22 +390,7 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     cudaError_t err = launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream),
                                          gather_ids, K, T);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
-    NvLaunch N;
-    N.w = w.packed;
-    N.tscale = w.tscale;
-    N.xb = xb;
-    N.expert_ids = expert_ids;
-    N.m_sum = m_sum;
-    N.h_q = h_q;
-    N.h_sf = h_sf;
-    N.y = y;
-    N.status = status_of(ws);
-    N.E = E;
-    N.w_rows = l1 ? 2 * I : H;
-    N.Kd = Kd;
-    N.I = I;
-    N.U = static_cast<int>(U);
-    N.align = align;
+    NvLaunch N = nv_launch(l1, xb, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
     if (red) N.red = *red;
     N.row_ids = row_ids;
     N.row_w = row_w;
@@ -443,6 +457,9 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
                              const int32_t* slot_counts = nullptr, int slot = 0,
                              const int32_t* gather_ids = nullptr) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
+    // NVFP4: the two calls in turn.  (Both GEMMs in one cooperative launch, the L1 epilogue also
+    // writing the bf16 h rows L2 reads, measured 8.50 ms against 8.02 ms for the skewed workload:
+    // the heavier L1 epilogue holds both accumulators longer while the MMA waits.)
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
                                 nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w, gather_ids);
     if (st != MOE_OK) return st;
@@ -711,10 +728,12 @@ static moe_status l1_i8_common(const int8_t* x_q, const float* x_s, int x_rows, 
   uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
   float* as = reinterpret_cast<float*>(b + L.a_s);
   uint16_t* hb = reinterpret_cast<uint16_t*>(b + L.hb);
+  const bool block = w13.fmt == MOE_W_INT8_B256;
   if (launch_i8_rows_to_f16(x_q, x_s, x_rows, sorted_token_ids, K, expert_ids, m_sum, static_cast<int>(U), H, xf, as,
-                            status_of(ws), S(stream)) != cudaSuccess)
+                            status_of(ws), S(stream), i8_row_scales(block, H)) != cudaSuccess)
     return MOE_ERR_CUDA;
   I8Launch G;
+  G.block = block ? 1 : 0;
   G.w = w13.packed;
   G.col_scale = w13.tscale;
   G.xf = xf;
@@ -730,7 +749,8 @@ static moe_status l1_i8_common(const int8_t* x_q, const float* x_s, int x_rows, 
   G.U = static_cast<int>(U);
   G.align = align;
   if (launch_gemm_i8(G, true, S(stream)) != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_quant_rows_i8(hb, static_cast<int>(U), I, expert_ids, m_sum, h_q, h_s, h_f16, S(stream)));
+  return cuda_status(launch_quant_rows_i8(hb, static_cast<int>(U), I, expert_ids, m_sum, h_q, h_s, h_f16, S(stream),
+                                          block ? 256 : 0));
 }
 
 // L2 of the INT8 variant from fp16 h codes already in the workspace's operand rows.
@@ -752,6 +772,7 @@ static moe_status l2_i8_launch(const float* h_s, const int32_t* expert_ids, cons
   G.I = I;
   G.U = static_cast<int>(U);
   G.align = align;
+  G.block = w2.fmt == MOE_W_INT8_B256 ? 1 : 0;
   if (red) G.red = *red;
   return cuda_status(launch_gemm_i8(G, false, S(stream)));
 }
@@ -767,6 +788,7 @@ static moe_status forward_i8_common(const uint16_t* hidden, const float* w_gate,
   if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
   if (!hidden || !w_gate || !out || !weight_ok_i8(w13, E, 2 * I, H, 2) || !weight_ok_i8(w2, E, H, I, 1))
     return MOE_ERR_INVALID_ARG;
+  if (w13.fmt != w2.fmt) return MOE_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
   if (!ws) return MOE_ERR_WORKSPACE;
   const size_t U = slot ? slot_rows(E, slot) : moe_msum_upper(T, K, E, align);
@@ -791,7 +813,8 @@ static moe_status forward_i8_common(const uint16_t* hidden, const float* w_gate,
   moe_status st = moe_route(hidden, w_gate, gate_bias, e_score_bias, T, H, E, K, fn, renormalize, nullptr, ids, tw,
                             nullptr, nullptr, ws, ws_bytes, stream);
   if (st != MOE_OK) return st;
-  if (launch_quant_rows_i8(hidden, T, H, nullptr, nullptr, xq, xs, nullptr, S(stream)) != cudaSuccess)
+  if (launch_quant_rows_i8(hidden, T, H, nullptr, nullptr, xq, xs, nullptr, S(stream),
+                           w13.fmt == MOE_W_INT8_B256 ? 256 : 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   st = permute_common(ids, T, K, E, align, slot, sorted, eids, inv, ms, slot ? cnt : nullptr, nullptr, nullptr, H,
                       nullptr, nullptr, ws, ws_bytes, stream);
@@ -829,6 +852,13 @@ moe_status moe_act_quant_i8(const uint16_t* x, int rows, int cols, int8_t* x_q, 
   return cuda_status(launch_quant_rows_i8(x, rows, cols, nullptr, nullptr, x_q, x_s, nullptr, S(stream)));
 }
 
+moe_status moe_act_quant_i8_b256(const uint16_t* x, int rows, int cols, int8_t* x_q, float* x_s, void* stream) {
+  if (rows < 0 || cols <= 0 || cols % 256 || !x || !x_q || !x_s) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_q, 16)) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  return cuda_status(launch_quant_rows_i8(x, rows, cols, nullptr, nullptr, x_q, x_s, nullptr, S(stream), 256));
+}
+
 moe_status moe_grouped_gemm_l1_swiglu_i8(const int8_t* x_q, const float* x_s, const int32_t* sorted_token_ids,
                                          const int32_t* expert_ids, const int32_t* m_sum, int T, int K, int H, int I,
                                          int E, int align, moe_weight w13, int8_t* h_q, float* h_s, void* ws,
@@ -853,7 +883,7 @@ moe_status moe_grouped_gemm_l2_i8(const int8_t* h_q, const float* h_s, const int
   uint16_t* xf = reinterpret_cast<uint16_t*>(b + L.L.xb);
   float* as = reinterpret_cast<float*>(b + L.a_s);
   if (launch_i8_rows_to_f16(h_q, h_s, static_cast<int>(U), nullptr, 1, expert_ids, m_sum, static_cast<int>(U), I, xf,
-                            as, status_of(ws), S(stream)) != cudaSuccess)
+                            as, status_of(ws), S(stream), i8_row_scales(w2.fmt == MOE_W_INT8_B256, I)) != cudaSuccess)
     return MOE_ERR_CUDA;
   return l2_i8_launch(as, expert_ids, m_sum, H, I, E, align, U, w2, y_perm, nullptr, ws, L, stream);
 }

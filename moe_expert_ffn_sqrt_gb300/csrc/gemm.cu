@@ -194,7 +194,9 @@ constexpr int kItemSlots = 4;
 // (or has finished it), and that CTA's MMA and epilogue warps complete it whatever its producer
 // waits for: progress needs no co-residency of the CTAs, and the wait is bounded all the same.
 // The last CTA to exit sets all counters back to zero: no CTA can still be waiting or drawing then.
-template <int BN>
+// GATHER: the L1 phase reads its token rows with four-row gathers (GemmPhase::gather_ids); a
+// separate instance, so that the permuted-copy path carries none of that bookkeeping.
+template <int BN, bool GATHER>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
                     const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_x2,
@@ -325,7 +327,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int r0 = it.rb * BN;
       const size_t chunk0 = (static_cast<size_t>(e) * P.n_wt + it.wt) * P.n_slabs;
       // gather mode: lane j (< BN / 4) copies rows 4j .. 4j + 3 of the block, tokens looked up once
-      const bool gather = P.gather_ids != nullptr;
+      const bool gather = GATHER && P.gather_ids != nullptr;
       int g_tok[4] = {0, 0, 0, 0};
       if (gather && lane < BN / 4) {
 #pragma unroll
@@ -352,10 +354,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; ok && s < P.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
         if (!ok) break;
-        uint8_t* st = stages + stage * C::STAGE;
-        const uint32_t fb = smem_u32(full + stage);
         bool good = true;
         if (lane == 0) {
+          uint8_t* st = stages + stage * C::STAGE;
+          const uint32_t fb = smem_u32(full + stage);
           const size_t wbase = (chunk0 + s) * C::W_CHUNK;
           const size_t sfa = (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
           // self-check: every copy inside its buffer and 16-byte aligned
@@ -375,9 +377,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if ((s & 3) == 0) bulk_load(smem_u32(st + C::SFA_OFF), P.x_sf + sfa, C::SFA_BYTES, fb);
           }
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (gather && good && lane < BN / 4)
-          tma_gather4(smem_u32(st + lane * 512), mx, s * 128, g_tok[0], g_tok[1], g_tok[2], g_tok[3], fb, pol_x);
+        if (gather) {                          // warp-uniform: the other lanes copy the token rows
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (good && lane < BN / 4)
+            tma_gather4(smem_u32(stages + stage * C::STAGE + lane * 512), mx, s * 128, g_tok[0], g_tok[1], g_tok[2],
+                        g_tok[3], smem_u32(full + stage), pol_x);
+        }
         __syncwarp();
         if (++stage == C::STAGES) {
           stage = 0;
@@ -716,7 +721,7 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
 // l1 and/or l2 (non-null ones run).  `sched` holds gemm_sched_words(U, align) words that are zero
 // before the launch and zero again after it (work counter; with both phases also the per-row-block
 // counters that order them).
-template <int BN>
+template <int BN, bool GATHER>
 static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   GemmArgs a{};
@@ -764,7 +769,7 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   int grid = num_sms();
   if (grid > total) grid = total;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -784,25 +789,31 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
   if (err != cudaSuccess && pdl_ok) {
     (void)cudaGetLastError();
     pdl_ok = false;
     cfg.numAttrs = n - 1;
-    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN>, m[0], m[1], m[2], m[3], a);
+    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
   }
   return err;
 }
 
 int gemm_block_n(int align) { return act_sf_block_rows(align); }
 
-static cudaError_t launch_bn(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
+template <bool GATHER>
+static cudaError_t launch_bn_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
   switch (gemm_block_n((l1 ? l1 : l2)->align)) {
-    case 16: return launch_gemm_t<16>(l1, l2, sched, stream);
-    case 32: return launch_gemm_t<32>(l1, l2, sched, stream);
-    case 64: return launch_gemm_t<64>(l1, l2, sched, stream);
-    default: return launch_gemm_t<128>(l1, l2, sched, stream);
+    case 16: return launch_gemm_t<16, GATHER>(l1, l2, sched, stream);
+    case 32: return launch_gemm_t<32, GATHER>(l1, l2, sched, stream);
+    case 64: return launch_gemm_t<64, GATHER>(l1, l2, sched, stream);
+    default: return launch_gemm_t<128, GATHER>(l1, l2, sched, stream);
   }
+}
+
+static cudaError_t launch_bn(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
+  if (l1 && l1->gather_ids) return launch_bn_t<true>(l1, l2, sched, stream);
+  return launch_bn_t<false>(l1, l2, sched, stream);
 }
 
 cudaError_t launch_gemm(const GemmLaunch& L, bool l1, uint32_t* sched, cudaStream_t stream) {

@@ -18,6 +18,15 @@
 // The load ring keeps only the rows a row block holds (BN x 128 bytes per block and slab), so small
 // blocks leave room for a deeper ring; the MMA's 128-row operand window of a block stays inside its
 // ring slot (rows past BN are never stored).
+//
+// [256, 256] block-quantised weights (BLOCK): the scale of a product changes every 256 columns of
+// the reduction (one per activation row and group, one per weight block), so one fp32 accumulator
+// cannot take the whole reduction.  Each 256-deep K-block (four slabs) is accumulated alone in TMEM
+// columns [0, 256) -- exact, since 256 products of two int8 codes sum to less than 2^24 -- and the
+// epilogue folds it, times the row's group scale and the weight block's scale, into a running fp32
+// sum kept in TMEM columns [256, 512); the last K-block's fold feeds the SwiGLU (L1) or the bf16
+// output (L2) directly.  A pass then holds one row block (the second accumulator's columns hold the
+// sum), and the MMA waits for each fold.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -71,6 +80,8 @@ struct I8Args {
   int n_tiles;
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   int split_pairs;              // items are halves of row-block pairs (small blocks) or whole pairs
+  int pair_blocks;              // two blocks of one expert may share a pass (not with block scales)
+  int nkb;                      // BLOCK: 256-deep K-blocks (row_scale [U, nkb], col_scale [E, w_rows/256, nkb])
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
 };
 
@@ -135,7 +146,7 @@ __device__ __forceinline__ void convert_slab_i8(const uint8_t* __restrict__ code
 // MMAs, 2..11 convert codes into the fp16 ring, 12..15 drain the accumulators.  A pass with two row
 // blocks accumulates block j into TMEM columns [256j, 256j+256); the epilogue releases the
 // accumulators after the pass.
-template <int BN, bool L1>
+template <int BN, bool L1, bool BLOCK>
 __global__ void __launch_bounds__(kI8Threads, 1)
     moe_gemm_i8_kernel(const __grid_constant__ CUtensorMap tmap_x, const I8Args a) {
   using C = I8Cfg<BN>;
@@ -229,11 +240,15 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     int t = blockIdx.x, p = 0, ep = -1;
     RowPass P;
     const uint32_t id = idesc_f16(128, kI8Tile);
+    // BLOCK: one accumulator round per 256-deep K-block (4 slabs); otherwise one per pass
+    const int slabs_per_round = BLOCK ? 4 : a.n_slabs;
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
-      if (ok) {
+      bool ok = true;
+      for (int s0 = 0; ok && s0 < a.n_slabs; s0 += slabs_per_round) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+        if (!ok) break;
         tc_fence_after();
-        for (int s = 0; s < a.n_slabs; ++s) {
+        for (int s = s0; s < s0 + slabs_per_round; ++s) {
           ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
                                            mbar_wait(smem_u32(bready + bs), bph, a.status));
           if (!ok) break;
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_bf16(tmem + static_cast<uint32_t>(j * kI8Tile), desc_sw128(sa + j * C::kABytes + k * 32),
-                         desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
+                         desc_sw128(sb + k * 32), id, (s > s0 || k > 0) ? 1u : 0u);
             tc_commit(smem_u32(lempty + ls));
             tc_commit(smem_u32(bempty + bs));
           }
@@ -259,14 +274,15 @@ __global__ void __launch_bounds__(kI8Threads, 1)
             bph ^= 1;
           }
         }
+        if (!ok) break;
+        if (lane == 0) tc_commit(smem_u32(acc_full));
+        __syncwarp();
+        acc_phase ^= 1;
       }
       if (!ok) {
         *abort_flag = 1;
         break;
       }
-      if (lane == 0) tc_commit(smem_u32(acc_full));
-      __syncwarp();
-      acc_phase ^= 1;
     }
   } else if (warp < 2 + kI8ConvThreads / 32) {
     // ---------------- converters: int8 codes -> 128-byte-swizzled fp16 tile ----------------
@@ -308,6 +324,100 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     RowPass P;
     while (next_row_pass<BN>(a, msum, t, p, ep, P)) {
       const int wt = t % a.n_wt;
+      if (BLOCK) {
+        // one pass = one row block; fold each K-block into the running sum, finish on the last
+        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t sum = acc + static_cast<uint32_t>(kI8Tile);
+        const int row = P.rb * BN + m;
+        const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == P.e;
+        const int nbw = (a.w_rows + 255) / 256;     // weight row blocks
+        // weight blocks of the tile's columns: L1 gate rows 128 wt.. and up rows I + 128 wt..; L2 rows 256 wt..
+        const float* wsa = a.col_scale + (static_cast<size_t>(P.e) * nbw + (L1 ? (wt * 128) / 256 : wt)) * a.nkb;
+        const float* wsb = a.col_scale + (static_cast<size_t>(P.e) * nbw + (L1 ? (a.out_cols + wt * 128) / 256 : wt)) * a.nkb;
+        const float* rsp = a.row_scale + static_cast<size_t>(mine ? row : 0) * a.nkb;
+        bool okb = true;
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          okb = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+          okb = named_barrier_and(1, 128, okb);
+          if (!okb) break;
+          tc_fence_after();
+          const bool last = kb == a.nkb - 1;
+          const float rs = mine ? __ldg(rsp + kb) : 0.f;
+          const float fa = rs * __ldg(wsa + kb), fb = rs * __ldg(wsb + kb);
+          if (L1) {
+            // column c: gate channel wt*128 + c (scale fa) with its up channel in column 128 + c (fb)
+            uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * a.out_cols + wt * 128);
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+              uint32_t g[16], u[16], sg[16], su[16];
+              tc_ld_x16(acc + c0, g);
+              tc_ld_x16(acc + 128 + c0, u);
+              if (kb > 0) {
+                tc_ld_x16(sum + c0, sg);
+                tc_ld_x16(sum + 128 + c0, su);
+              }
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float pg = kb > 0 ? __uint_as_float(sg[i]) : 0.f;
+                const float pu = kb > 0 ? __uint_as_float(su[i]) : 0.f;
+                sg[i] = __float_as_uint(fmaf(__uint_as_float(g[i]), fa, pg));
+                su[i] = __float_as_uint(fmaf(__uint_as_float(u[i]), fb, pu));
+              }
+              if (!last) {
+                tc_st_x16(sum + c0, sg);
+                tc_st_x16(sum + 128 + c0, su);
+              } else if (mine) {
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float h0 = silu_mul_i8(__uint_as_float(sg[2 * i]), __uint_as_float(su[2 * i]));
+                  const float h1 = silu_mul_i8(__uint_as_float(sg[2 * i + 1]), __uint_as_float(su[2 * i + 1]));
+                  packed[i] = __bfloat16_as_ushort(__float2bfloat16_rn(h0)) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(h1))) << 16);
+                }
+                dst[c0 / 8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[c0 / 8 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
+            }
+          } else {
+            const int ncols = min(kI8Tile, a.out_cols - wt * kI8Tile);
+            uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * a.out_cols + wt * kI8Tile);
+#pragma unroll 1
+            for (int c0 = 0; c0 < kI8Tile; c0 += 16) {
+              uint32_t v[16], sv[16];
+              tc_ld_x16(acc + c0, v);
+              if (kb > 0) tc_ld_x16(sum + c0, sv);
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                sv[i] = __float_as_uint(fmaf(__uint_as_float(v[i]), fa, kb > 0 ? __uint_as_float(sv[i]) : 0.f));
+              if (!last) {
+                tc_st_x16(sum + c0, sv);
+              } else if (mine && c0 < ncols) {
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  packed[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(sv[2 * i]))) |
+                              (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(sv[2 * i + 1])))) << 16);
+                dst[c0 / 8] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[c0 / 8 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              }
+            }
+            if (last && a.red.out)
+              fused_reduce_tail(a.red, a.out, a.out_cols, mine, row, wt, a.n_wt, wt * kI8Tile, ncols);
+          }
+          if (!last) tc_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty));
+          acc_phase ^= 1;
+        }
+        if (!okb) {
+          *abort_flag = 1;
+          break;
+        }
+        continue;
+      }
       bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
       ok = named_barrier_and(1, 128, ok);
       if (!ok) {
@@ -421,7 +531,7 @@ __global__ void __launch_bounds__(256) i8_rows_to_f16_kernel(const int8_t* __res
                                                              const int32_t* __restrict__ expert_ids,
                                                              const int32_t* __restrict__ m_sum, int U, int C,
                                                              uint16_t* __restrict__ dst, float* __restrict__ dst_scale,
-                                                             uint32_t* status) {
+                                                             uint32_t* status, int nsc) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int msum = *m_sum;
   for (int r = blockIdx.x * 8 + warp; r < msum && r < U; r += gridDim.x * 8) {
@@ -431,7 +541,7 @@ __global__ void __launch_bounds__(256) i8_rows_to_f16_kernel(const int8_t* __res
       if (lane == 0) record_error(status, kDevErrCheck);
       continue;
     }
-    if (lane == 0) dst_scale[r] = __ldg(src_scale + s);
+    for (int j = lane; j < nsc; j += 32) dst_scale[static_cast<size_t>(r) * nsc + j] = __ldg(src_scale + static_cast<size_t>(s) * nsc + j);
     const int8_t* in = src + static_cast<size_t>(s) * C;
     uint16_t* out = dst + static_cast<size_t>(r) * C;
     for (int k0 = lane * 16; k0 < C; k0 += 512) {
@@ -443,24 +553,26 @@ __global__ void __launch_bounds__(256) i8_rows_to_f16_kernel(const int8_t* __res
   }
 }
 
-// Per-row symmetric int8 quantisation of bf16 rows: amax = max |x| over the row; inv = 127 / amax
-// and s = amax / 127, each one correctly rounded fp32 division; q = clamp(rint(x * inv), -127, 127)
-// with one fp32 multiply per value (rint: to nearest, ties to even).  A row with amax = 0 gives
-// q = 0, s = 0.  Rows: all of [0, R), or with expert_ids the rows r < min(R, m_sum) that hold a
-// pair.  With f16 non-null the codes are also written as fp16 values (the next GEMM's operand).
-// One warp per row, 8 values per lane step.
+// Symmetric int8 quantisation of bf16 rows, per group of G columns (G = C: per row): amax = max |x|
+// over the group; inv = 127 / amax and s = amax / 127, each one correctly rounded fp32 division;
+// q = clamp(rint(x * inv), -127, 127) with one fp32 multiply per value (rint: to nearest, ties to
+// even).  A group with amax = 0 gives q = 0, s = 0; s is [rows, C/G].  Rows: all of [0, R), or with
+// expert_ids the rows r < min(R, m_sum) that hold a pair.  With f16 non-null the codes are also
+// written as fp16 values (the next GEMM's operand).  One warp per row, 8 values per lane step.
 __global__ void __launch_bounds__(256) quant_rows_i8_kernel(const uint16_t* __restrict__ x, int R, int C,
                                                             const int32_t* __restrict__ expert_ids,
                                                             const int32_t* __restrict__ m_sum,
                                                             int8_t* __restrict__ q, float* __restrict__ s,
-                                                            uint16_t* __restrict__ f16) {
+                                                            uint16_t* __restrict__ f16, int G) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int rows = m_sum ? min(R, *m_sum) : R;
-  for (int r = blockIdx.x * 8 + warp; r < rows; r += gridDim.x * 8) {
+  const int ng = C / G;
+  for (int rg = blockIdx.x * 8 + warp; rg < rows * ng; rg += gridDim.x * 8) {
+    const int r = rg / ng, g = rg - r * ng;
     if (expert_ids && __ldg(expert_ids + r) < 0) continue;
-    const uint16_t* in = x + static_cast<size_t>(r) * C;
+    const uint16_t* in = x + static_cast<size_t>(r) * C + static_cast<size_t>(g) * G;
     float amax = 0.f;
-    for (int k0 = lane * 8; k0 < C; k0 += 256) {
+    for (int k0 = lane * 8; k0 < G; k0 += 256) {
       const uint4 v = *reinterpret_cast<const uint4*>(in + k0);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -469,9 +581,9 @@ __global__ void __launch_bounds__(256) quant_rows_i8_kernel(const uint16_t* __re
     }
     amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));   // amax >= 0: bits order
     const float inv = amax > 0.f ? __fdiv_rn(127.f, amax) : 0.f;
-    if (lane == 0) s[r] = __fdiv_rn(amax, 127.f);
-    int8_t* qo = q + static_cast<size_t>(r) * C;
-    for (int k0 = lane * 8; k0 < C; k0 += 256) {
+    if (lane == 0) s[static_cast<size_t>(r) * ng + g] = __fdiv_rn(amax, 127.f);
+    int8_t* qo = q + static_cast<size_t>(r) * C + static_cast<size_t>(g) * G;
+    for (int k0 = lane * 8; k0 < G; k0 += 256) {
       const uint4 v = *reinterpret_cast<const uint4*>(in + k0);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
       int c[8];
@@ -492,7 +604,8 @@ __global__ void __launch_bounds__(256) quant_rows_i8_kernel(const uint16_t* __re
         for (int j = 0; j < 4; ++j)
           o[j] = __half_as_ushort(__int2half_rn(c[2 * j])) |
                  (static_cast<uint32_t>(__half_as_ushort(__int2half_rn(c[2 * j + 1]))) << 16);
-        *reinterpret_cast<uint4*>(f16 + static_cast<size_t>(r) * C + k0) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(f16 + static_cast<size_t>(r) * C + static_cast<size_t>(g) * G + k0) =
+            make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
   }
@@ -521,7 +634,7 @@ __global__ void pack_i8_weights_kernel(const int8_t* __restrict__ q, int E, int 
   }
 }
 
-template <int BN, bool L1>
+template <int BN, bool L1, bool BLOCK>
 cudaError_t launch_i8_t(const I8Launch& L, cudaStream_t stream) {
   CUtensorMap mx;
   if (!make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.xf, static_cast<uint64_t>(L.Kd),
@@ -546,14 +659,17 @@ cudaError_t launch_i8_t(const I8Launch& L, cudaStream_t stream) {
   const int nrb = (L.U + BN - 1) / BN;
   // items: halves of row-block pairs (blocks of up to 32 rows), whole pairs, or blocks
   a.split_pairs = BN <= 32;
+  a.pair_blocks = BLOCK ? 0 : 1;
+  a.nkb = L.Kd / 256;
+  if (BLOCK && (L.Kd % 256 != 0 || L.w_rows % 256 != 0)) return cudaErrorInvalidValue;
   a.n_tiles = (a.one_expert_blocks ? (a.split_pairs ? (nrb + 1) / 2 * 2 : (nrb + 1) / 2) : nrb) * a.n_wt;
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
-  cudaError_t err =
-      cudaFuncSetAttribute(moe_gemm_i8_kernel<BN, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize, I8Cfg<BN>::kSmem);
+  cudaError_t err = cudaFuncSetAttribute(moe_gemm_i8_kernel<BN, L1, BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         I8Cfg<BN>::kSmem);
   if (err != cudaSuccess) return err;
-  moe_gemm_i8_kernel<BN, L1><<<grid, kI8Threads, I8Cfg<BN>::kSmem, stream>>>(mx, a);
+  moe_gemm_i8_kernel<BN, L1, BLOCK><<<grid, kI8Threads, I8Cfg<BN>::kSmem, stream>>>(mx, a);
   return cudaGetLastError();
 }
 
@@ -576,34 +692,42 @@ cudaError_t launch_pack_i8(const int8_t* q, int E, int N, int Kd, int pair, uint
 
 cudaError_t launch_i8_rows_to_f16(const int8_t* src, const float* src_scale, int src_rows, const int32_t* src_map,
                                   int K, const int32_t* expert_ids, const int32_t* m_sum, int U, int C, uint16_t* dst,
-                                  float* dst_scale, uint32_t* status, cudaStream_t stream) {
+                                  float* dst_scale, uint32_t* status, cudaStream_t stream, int nsc) {
   i8_rows_to_f16_kernel<<<rows_grid(U), 256, 0, stream>>>(src, src_scale, src_rows, src_map, K, expert_ids, m_sum, U,
-                                                           C, dst, dst_scale, status);
+                                                           C, dst, dst_scale, status, nsc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_rows_i8(const uint16_t* x, int R, int C, const int32_t* expert_ids, const int32_t* m_sum,
-                                 int8_t* q, float* s, uint16_t* f16, cudaStream_t stream) {
-  quant_rows_i8_kernel<<<rows_grid(R), 256, 0, stream>>>(x, R, C, expert_ids, m_sum, q, s, f16);
+                                 int8_t* q, float* s, uint16_t* f16, cudaStream_t stream, int group) {
+  const int G = group > 0 ? group : C;
+  const long long units = static_cast<long long>(R) * (C / G);
+  const int grid = static_cast<int>(units / 8 + 1 < 4LL * num_sms() ? units / 8 + 1 : 4LL * num_sms());
+  quant_rows_i8_kernel<<<grid, 256, 0, stream>>>(x, R, C, expert_ids, m_sum, q, s, f16, G);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_i8(const I8Launch& L, bool l1, cudaStream_t stream) {
+template <bool BLOCK>
+static cudaError_t launch_gemm_i8_b(const I8Launch& L, bool l1, cudaStream_t stream) {
   const int bn = act_sf_block_rows(L.align);
   if (l1) {
     switch (bn) {
-      case 16: return launch_i8_t<16, true>(L, stream);
-      case 32: return launch_i8_t<32, true>(L, stream);
-      case 64: return launch_i8_t<64, true>(L, stream);
-      default: return launch_i8_t<128, true>(L, stream);
+      case 16: return launch_i8_t<16, true, BLOCK>(L, stream);
+      case 32: return launch_i8_t<32, true, BLOCK>(L, stream);
+      case 64: return launch_i8_t<64, true, BLOCK>(L, stream);
+      default: return launch_i8_t<128, true, BLOCK>(L, stream);
     }
   }
   switch (bn) {
-    case 16: return launch_i8_t<16, false>(L, stream);
-    case 32: return launch_i8_t<32, false>(L, stream);
-    case 64: return launch_i8_t<64, false>(L, stream);
-    default: return launch_i8_t<128, false>(L, stream);
+    case 16: return launch_i8_t<16, false, BLOCK>(L, stream);
+    case 32: return launch_i8_t<32, false, BLOCK>(L, stream);
+    case 64: return launch_i8_t<64, false, BLOCK>(L, stream);
+    default: return launch_i8_t<128, false, BLOCK>(L, stream);
   }
+}
+
+cudaError_t launch_gemm_i8(const I8Launch& L, bool l1, cudaStream_t stream) {
+  return L.block ? launch_gemm_i8_b<true>(L, l1, stream) : launch_gemm_i8_b<false>(L, l1, stream);
 }
 
 }  // namespace moe

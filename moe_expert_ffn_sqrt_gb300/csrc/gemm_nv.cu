@@ -28,14 +28,16 @@ namespace moe {
 
 namespace {
 
-constexpr int kNvThreads = 512;          // warp 0 TMA, 1 MMA, 2..11 convert, 12..15 epilogue
-constexpr int kNvConvThreads = 320;
-constexpr int kNvConvBatch = 4;          // conversion tasks per thread with loads issued together
+constexpr int kNvThreads = 448;          // warp 0 TMA, 1 MMA, 2..9 convert, 10..13 epilogue
+constexpr int kNvConvThreads = 256;      // one weight row of the tile per converter thread
 constexpr int kNvBudget = 227 * 1024;
 constexpr uint32_t kNvTmemCols = 512;    // two 256-column accumulators
 constexpr int kNvTile = 256;             // weight rows per tile (MMA N)
 constexpr int kNvSlab = 64;              // K per pipeline stage (64 bf16 = one 128-byte row)
-constexpr int kNvChunk = kNvTile * 32 + kNvTile * 4;   // packed bytes per (tile, slab): codes + scales
+// Packed bytes per (tile, slab): the codes as two 4 KB halves (bytes 0..15, then 16..31, of each
+// row's 32 code bytes, rows consecutive: a converter thread's 16-byte loads are conflict-free),
+// then 256 rows x 4 E4M3 scales.
+constexpr int kNvChunk = kNvTile * 32 + kNvTile * 4;
 // Load ring slot: bf16 token rows of up to two row blocks (the MMA reads 128 rows = 16 KB each) +
 // one packed weight chunk.
 constexpr int kNvABytes = 16384;
@@ -50,21 +52,26 @@ constexpr int kNvSmem = 1024 + kNvLoadStages * kNvLoadStage + kNvBStages * kNvBS
 static_assert(kNvSmem <= kNvBudget, "shared memory budget");
 static_assert(kNvConvThreads % 32 == 0 && 2 + kNvConvThreads / 32 + 4 == kNvThreads / 32, "warp roles");
 
-struct NvArgs {
+// One GEMM of the layer as the kernel sees it (L1: W13 with SwiGLU + requant; L2: W2, bf16 out).
+struct NvPhase {
   const uint8_t* w;             // packed NVFP4 weight stream
   const float* tscale;          // [E]
+  size_t w_bytes;
+  int n_slabs;                  // K / 64
+  int n_wt;                     // weight tiles per expert
+  int out_cols;                 // L1: I, L2: H
+  int n_tiles;                  // items of this phase (0: not run by this launch)
+};
+
+struct NvArgs {
+  NvPhase ph[2];                // [0] L1, [1] L2
   const int32_t* expert_ids;
   const int32_t* m_sum;
   uint8_t* h_q;
   uint8_t* h_sf;
   uint16_t* y;
   uint32_t* status;
-  size_t w_bytes;
-  int n_slabs;                  // K / 64
-  int n_wt;
-  int out_cols;
   int sf_nb;
-  int n_tiles;
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
   int split_pairs;              // items are halves of row-block pairs (small blocks) or whole pairs
   FusedReduce red;              // L2: unpermute-reduce in the epilogue when red.out != nullptr
@@ -72,23 +79,26 @@ struct NvArgs {
   const float* row_w;
 };
 
+// The per-phase view next_row_pass walks.
+struct NvPassView {
+  int n_tiles, n_wt, one_expert_blocks, split_pairs, pair_blocks;
+  const int32_t* expert_ids;
+};
+
+__device__ __forceinline__ NvPassView pass_view(const NvArgs& a, int ph) {
+  return NvPassView{a.ph[ph].n_tiles, a.ph[ph].n_wt, a.one_expert_blocks, a.split_pairs, 1, a.expert_ids};
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
 
-// Four E2M1 codes (the low 16 bits of `w`, element i in nibble i) -> four bf16 values as two
-// bf16x2 words.  Magnitude codes 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6, whose bf16 patterns split
-// into the low-byte table {00,00,80,C0,00,40,80,C0} and the high-byte table {00,3F,3F,3F,40,40,
-// 40,40}; prmt looks up four bytes at once.  The code's sign bit becomes the bf16 sign bit.
-__device__ __forceinline__ void e2m1x4_to_bf16(uint32_t w, uint32_t& p0, uint32_t& p1) {
-  const uint32_t sel = w & 0x7777u;
-  const uint32_t lo = prmt(0xC0800000u, 0xC0804000u, sel);
-  const uint32_t hi = prmt(0x3F3F3F00u, 0x40404040u, sel);
-  p0 = prmt(lo, hi, 0x5140u) | ((w << 12) & 0x8000u) | ((w << 24) & 0x80000000u);
-  p1 = prmt(lo, hi, 0x7362u) | ((w << 4) & 0x8000u) | ((w << 16) & 0x80000000u);
-}
+// E2M1 magnitude codes 0..7 are 0, .5, 1, 1.5, 2, 3, 4, 6: their bf16 patterns split into the
+// low-byte table {00,00,80,C0,00,40,80,C0} and the high-byte table {00,3F,3F,3F,40,40,40,40}, which
+// prmt looks up four at a time.
+constexpr uint32_t kLoA = 0xC0800000u, kLoB = 0xC0804000u, kHiA = 0x3F3F3F00u, kHiB = 0x40404040u;
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162*>(&a), y = *reinterpret_cast<__nv_bfloat162*>(&b);
@@ -96,64 +106,64 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// E4M3 code -> bf16 bits (exact).
-__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t c) {
-  const __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
-  const float f = __half2float(*reinterpret_cast<const __half*>(&hr));
-  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+// Eight E2M1 codes (element i in nibble i of w) times one bf16 scale s2 (in both halves; positive)
+// -> eight bf16 values, exactly (a 2-bit E2M1 significand times a 4-bit E4M3 one fits bf16's 8):
+// magnitudes by table lookup, scaled, then each code's sign bit xor-ed into the bf16 sign bit.  The
+// signs come from a prmt in sign-replicate mode: byte k of w << 4 carries element 2k's sign in its
+// top bit and byte k of w element 2k+1's.
+__device__ __forceinline__ void e2m1x8_to_bf16(uint32_t w, uint32_t s2, uint32_t (&q)[4]) {
+  const uint32_t sel0 = w & 0x7777u, sel1 = (w >> 16) & 0x7777u;
+  const uint32_t lo0 = prmt(kLoA, kLoB, sel0), hi0 = prmt(kHiA, kHiB, sel0);
+  const uint32_t lo1 = prmt(kLoA, kLoB, sel1), hi1 = prmt(kHiA, kHiB, sel1);
+  const uint32_t w4 = w << 4;
+  q[0] = bf16x2_mul(prmt(lo0, hi0, 0x5140), s2) ^ (prmt(w4, w, 0xC080) & 0x80008000u);
+  q[1] = bf16x2_mul(prmt(lo0, hi0, 0x7362), s2) ^ (prmt(w4, w, 0xD090) & 0x80008000u);
+  q[2] = bf16x2_mul(prmt(lo1, hi1, 0x5140), s2) ^ (prmt(w4, w, 0xE0A0) & 0x80008000u);
+  q[3] = bf16x2_mul(prmt(lo1, hi1, 0x7362), s2) ^ (prmt(w4, w, 0xF0B0) & 0x80008000u);
+}
+
+// Two E4M3 codes (low 16 bits of v) -> their bf16 values, each in both halves of a word (exact).
+__device__ __forceinline__ void e4m3x2_to_bf16x2(uint32_t v, uint32_t& s0, uint32_t& s1) {
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+  const uint32_t u = *reinterpret_cast<const uint32_t*>(&b);
+  s0 = prmt(u, u, 0x1010);
+  s1 = prmt(u, u, 0x3232);
 }
 
 __device__ __forceinline__ float silu_mul_nv(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
-// Sixteen weights of the bf16 tile: codes 16p .. 16p+15 of weight row n (8 code bytes, one E4M3
-// scale) -> two 16-byte chunks at the row's 128-byte-swizzled positions.  Inputs come in already
-// loaded so that a thread can issue the loads of several pairs before it computes any.
-__device__ __forceinline__ void convert_pair(uint2 codes, uint32_t scale_code, uint8_t* btile, int n, int p) {
-  const uint32_t s = e4m3_to_bf16_bits(scale_code);
-  const uint32_t s2 = s | (s << 16);
-  const uint32_t cw[2] = {codes.x, codes.y};
+// Converts weight row n (one converter thread) of one slab: 64 codes (two conflict-free 16-byte
+// loads), four E4M3 scales, eight 16-byte stores into the row's 128-byte-swizzled chunks (chunk c
+// holds K positions 8c .. 8c+7 at byte ((c ^ (n & 7)) << 4) of the row).
+__device__ __forceinline__ void convert_row(const uint8_t* __restrict__ packed, uint8_t* __restrict__ btile, int n) {
+  const uint4 c0 = *reinterpret_cast<const uint4*>(packed + n * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(packed + kNvTile * 16 + n * 16);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(packed + kNvTile * 32 + n * 4);
+  uint32_t s2[4];
+  e4m3x2_to_bf16x2(sc, s2[0], s2[1]);
+  e4m3x2_to_bf16x2(sc >> 16, s2[2], s2[3]);
+  const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t row = smem_u32(btile) + static_cast<uint32_t>(n) * 128;
+  const uint32_t x = static_cast<uint32_t>(n & 7) << 4;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int c = 0; c < 8; ++c) {
     uint32_t q[4];
-    e2m1x4_to_bf16(cw[h], q[0], q[1]);
-    e2m1x4_to_bf16(cw[h] >> 16, q[2], q[3]);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) q[j] = bf16x2_mul(q[j], s2);
-    const int c = 2 * p + h;
-    *reinterpret_cast<uint4*>(btile + n * 128 + ((c ^ (n & 7)) << 4)) = make_uint4(q[0], q[1], q[2], q[3]);
-  }
-}
-
-// Converts one slab: 256 rows x 4 pairs of 16 weights = 1024 tasks over the converter threads,
-// kNvConvBatch tasks at a time with all their shared-memory loads issued first.
-__device__ __forceinline__ void convert_slab(const uint8_t* __restrict__ packed, uint8_t* __restrict__ btile,
-                                             int ctid) {
-  constexpr int kTasks = kNvTile * 4;
-  for (int t0 = ctid; t0 < kTasks; t0 += kNvConvThreads * kNvConvBatch) {
-    uint2 codes[kNvConvBatch];
-    uint32_t sc[kNvConvBatch];
-#pragma unroll
-    for (int j = 0; j < kNvConvBatch; ++j) {
-      const int task = t0 + j * kNvConvThreads;
-      if (task < kTasks) {
-        const int n = task >> 2, p = task & 3;
-        codes[j] = *reinterpret_cast<const uint2*>(packed + n * 32 + p * 8);
-        sc[j] = packed[kNvTile * 32 + n * 4 + p];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kNvConvBatch; ++j) {
-      const int task = t0 + j * kNvConvThreads;
-      if (task < kTasks) convert_pair(codes[j], sc[j], btile, task >> 2, task & 3);
-    }
+    e2m1x8_to_bf16(words[c], s2[c >> 1], q);
+    const uint32_t addr = row | ((static_cast<uint32_t>(c) << 4) ^ x);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                 : "memory");
   }
 }
 
 // Warp roles: 0 loads (TMA token rows + bulk copy of packed weights into the load ring), 1 issues
-// the MMAs, 2..11 convert packed weights into the bf16 ring, 12..15 drain the accumulators.
+// the MMAs, 2..9 convert packed weights into the bf16 ring, 10..13 drain the accumulators.
 // A pass with two row blocks accumulates block j into TMEM columns [256j, 256j+256); the
 // epilogue releases the accumulators after the pass.
-template <int BN, bool L1>
+// MODE 1: the L1 items (W13, SwiGLU + requant); 2: the L2 items (W2, bf16 out).  Items are assigned
+// statically, CTA c taking items c, c + gridDim, ...
+template <int BN, int MODE>
 __global__ void __launch_bounds__(kNvThreads, 1)
     moe_gemm_nv_kernel(const __grid_constant__ CUtensorMap tmap_x, const NvArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -169,6 +179,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   uint64_t* acc_empty = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  constexpr int kPh0 = (MODE & 1) ? 0 : 1, kPh1 = (MODE & 2) ? 1 : 0;   // phases run, in order
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -201,40 +212,43 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const uint64_t pol_x = policy_evict_last();
     int ls = 0;
     uint32_t lph = 0;
-    int t = blockIdx.x, p = 0, ep = -1;
-    RowPass P;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
-      const int wt = t % a.n_wt;
-      const size_t chunk0 = (static_cast<size_t>(P.e) * a.n_wt + wt) * a.n_slabs;
-      bool ok = true;
-      for (int s = 0; s < a.n_slabs; ++s) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status));
-        if (!ok) break;
-        if (lane == 0) {
-          uint8_t* st = lring + ls * kNvLoadStage;
-          const uint32_t fb = smem_u32(full + ls);
-          const size_t wbase = (chunk0 + s) * kNvChunk;
-          if (wbase + kNvChunk > a.w_bytes || (reinterpret_cast<uintptr_t>(a.w) & 15)) {
-            record_error(a.status, kDevErrCheck);
-            *abort_flag = 1;
-          } else {
-            mbar_arrive_expect_tx(fb, P.nb * BN * 128 + kNvChunk);
-            for (int j = 0; j < P.nb; ++j)
-              tma_load_2d(smem_u32(st + j * kNvABytes), &tmap_x, s * kNvSlab, (P.rb + j) * BN, fb, pol_x);
-            bulk_load(smem_u32(st + kNvPOff), a.w + wbase, kNvChunk, fb);
+    bool ok = true;
+    for (int ph = kPh0; ok && ph <= kPh1; ++ph) {
+      const NvPhase& F = a.ph[ph];
+      const NvPassView V = pass_view(a, ph);
+      const CUtensorMap* mx = &tmap_x;
+      int t = blockIdx.x, p = 0, ep = -1;
+      RowPass P;
+      while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(V, msum, t, p, ep, P)) {
+        const int wt = t % F.n_wt;
+        const size_t chunk0 = (static_cast<size_t>(P.e) * F.n_wt + wt) * F.n_slabs;
+        for (int s = 0; s < F.n_slabs; ++s) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status));
+          if (!ok) break;
+          if (lane == 0) {
+            uint8_t* st = lring + ls * kNvLoadStage;
+            const uint32_t fb = smem_u32(full + ls);
+            const size_t wbase = (chunk0 + s) * kNvChunk;
+            if (wbase + kNvChunk > F.w_bytes || (reinterpret_cast<uintptr_t>(F.w) & 15)) {
+              record_error(a.status, kDevErrCheck);
+              *abort_flag = 1;
+            } else {
+              mbar_arrive_expect_tx(fb, P.nb * BN * 128 + kNvChunk);
+              for (int j = 0; j < P.nb; ++j)
+                tma_load_2d(smem_u32(st + j * kNvABytes), mx, s * kNvSlab, (P.rb + j) * BN, fb, pol_x);
+              bulk_load(smem_u32(st + kNvPOff), F.w + wbase, kNvChunk, fb);
+            }
+          }
+          __syncwarp();
+          if (++ls == kNvLoadStages) {
+            ls = 0;
+            lph ^= 1;
           }
         }
-        __syncwarp();
-        if (++ls == kNvLoadStages) {
-          ls = 0;
-          lph ^= 1;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
+        if (!ok) break;
       }
     }
+    if (!ok) *abort_flag = 1;
     if (__any_sync(0xffffffffu, *abort_flag != 0)) {
       // let every copy issued into shared memory land before the CTA exits
       for (int s = 0; s < kNvLoadStages; ++s) mbar_wait(smem_u32(full + s), (s < ls) ? lph : (lph ^ 1), nullptr);
@@ -243,30 +257,70 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     // ---------------- MMA issuer: kind::f16, M=128, N=256, K=16 x 4 per slab and block ----------------
     int ls = 0, bs = 0;
     uint32_t lph = 0, bph = 0, acc_phase = 0;
-    int t = blockIdx.x, p = 0, ep = -1;
-    RowPass P;
     const uint32_t id = idesc_bf16(128, kNvTile);
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
-      if (ok) {
-        tc_fence_after();
-        for (int s = 0; s < a.n_slabs; ++s) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
-                                           mbar_wait(smem_u32(bready + bs), bph, a.status));
-          if (!ok) break;
+    bool ok = true;
+    for (int ph = kPh0; ok && ph <= kPh1; ++ph) {
+      const NvPhase& F = a.ph[ph];
+      const NvPassView V = pass_view(a, ph);
+      int t = blockIdx.x, p = 0, ep = -1;
+      RowPass P;
+      while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(V, msum, t, p, ep, P)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+        if (ok) {
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = smem_u32(lring + ls * kNvLoadStage);
-            const uint32_t sb = smem_u32(bring + bs * kNvBStage);
-            for (int j = 0; j < P.nb; ++j)
+          for (int s = 0; s < F.n_slabs; ++s) {
+            ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
+                                             mbar_wait(smem_u32(bready + bs), bph, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            if (lane == 0) {
+              const uint32_t sa = smem_u32(lring + ls * kNvLoadStage);
+              const uint32_t sb = smem_u32(bring + bs * kNvBStage);
+              for (int j = 0; j < P.nb; ++j)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + static_cast<uint32_t>(j * kNvTile), desc_sw128(sa + j * kNvABytes + k * 32),
-                         desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
-            tc_commit(smem_u32(lempty + ls));
-            tc_commit(smem_u32(bempty + bs));
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16(tmem + static_cast<uint32_t>(j * kNvTile), desc_sw128(sa + j * kNvABytes + k * 32),
+                           desc_sw128(sb + k * 32), id, (s > 0 || k > 0) ? 1u : 0u);
+              tc_commit(smem_u32(lempty + ls));
+              tc_commit(smem_u32(bempty + bs));
+            }
+            __syncwarp();
+            if (++ls == kNvLoadStages) {
+              ls = 0;
+              lph ^= 1;
+            }
+            if (++bs == kNvBStages) {
+              bs = 0;
+              bph ^= 1;
+            }
           }
-          __syncwarp();
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(smem_u32(acc_full));
+        __syncwarp();
+        acc_phase ^= 1;
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  } else if (warp < 2 + kNvConvThreads / 32) {
+    // ---------------- converters: packed NVFP4 slab -> 128-byte-swizzled bf16 tile, a row each ----------------
+    const int ctid = threadIdx.x - 64;
+    int ls = 0, bs = 0;
+    uint32_t lph = 0, bph = 0;
+    bool ok = true;
+    for (int ph = kPh0; ok && ph <= kPh1; ++ph) {
+      const NvPhase& F = a.ph[ph];
+      const NvPassView V = pass_view(a, ph);
+      int t = blockIdx.x, p = 0, ep = -1;
+      RowPass P;
+      while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(V, msum, t, p, ep, P)) {
+        for (int s = 0; s < F.n_slabs; ++s) {
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
+                                           mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
+          if (!ok) break;
+          convert_row(lring + ls * kNvLoadStage + kNvPOff, bring + bs * kNvBStage, ctid);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(smem_u32(bready + bs));
           if (++ls == kNvLoadStages) {
             ls = 0;
             lph ^= 1;
@@ -276,148 +330,125 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             bph ^= 1;
           }
         }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      if (lane == 0) tc_commit(smem_u32(acc_full));
-      __syncwarp();
-      acc_phase ^= 1;
-    }
-  } else if (warp < 2 + kNvConvThreads / 32) {
-    // ---------------- converters: packed NVFP4 slab -> 128-byte-swizzled bf16 tile ----------------
-    const int ctid = threadIdx.x - 64;
-    int ls = 0, bs = 0;
-    uint32_t lph = 0, bph = 0;
-    int t = blockIdx.x, p = 0, ep = -1;
-    RowPass P;
-    while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
-      bool ok = true;
-      for (int s = 0; s < a.n_slabs; ++s) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
-                                         mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
         if (!ok) break;
-        convert_slab(lring + ls * kNvLoadStage + kNvPOff, bring + bs * kNvBStage, ctid);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(smem_u32(bready + bs));
-        if (++ls == kNvLoadStages) {
-          ls = 0;
-          lph ^= 1;
-        }
-        if (++bs == kNvBStages) {
-          bs = 0;
-          bph ^= 1;
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
       }
     }
+    if (!ok) *abort_flag = 1;
   } else {
-    // ---------------- epilogue (warps 12..15): thread = token row m of each block ----------------
+    // ---------------- epilogue (warps 10..13): thread = token row m of each block ----------------
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const bool warp_has_rows = q * 32 < BN;   // warp-uniform
     uint32_t acc_phase = 0;
-    int t = blockIdx.x, p = 0, ep = -1;
-    RowPass P;
-    while (next_row_pass<BN>(a, msum, t, p, ep, P)) {
-      const int wt = t % a.n_wt;
-      bool ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
-      ok = named_barrier_and(1, 128, ok);
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const float ts = __ldg(a.tscale + P.e);
-      for (int j = 0; j < P.nb; ++j) {
-        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNvTile);
-        const int row = (P.rb + j) * BN + m;
-        const bool mine = m < BN && row < msum && __ldg(a.expert_ids + row) == P.e;
-        if (L1) {
-          const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
-          // pass 1: amax of h over the 128 columns; pass 2: recompute h, quantise, store
-          if (warp_has_rows) {
-            float amax = 0.f;
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-              uint32_t g[2][16], u[2][16];
-              tc_ld_x16(acc + c0, g[0]);
-              tc_ld_x16(acc + c0 + 16, g[1]);
-              tc_ld_x16(acc + 128 + c0, u[0]);
-              tc_ld_x16(acc + 128 + c0 + 16, u[1]);
-              tc_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                amax = fmaxf(amax, fabsf(silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
-                                                     __uint_as_float(u[i >> 4][i & 15]) * ts) * wr));
-            }
-            const int ex = ue8m0_exponent(amax);
-            const float sc = pow2_neg(ex);
-            uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * a.out_cols + wt * 128);
-#pragma unroll 1
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-              uint32_t g[2][16], u[2][16];
-              tc_ld_x16(acc + c0, g[0]);
-              tc_ld_x16(acc + c0 + 16, g[1]);
-              tc_ld_x16(acc + 128 + c0, u[0]);
-              tc_ld_x16(acc + 128 + c0 + 16, u[1]);
-              tc_wait_ld();
-              uint32_t packed[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float h[4];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const int c = 4 * i + v;
-                  h[v] = silu_mul_nv(__uint_as_float(g[c >> 4][c & 15]) * ts, __uint_as_float(u[c >> 4][c & 15]) * ts) * wr;
-                }
-                const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
-                const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
-                packed[i] = lo | (hi << 16);
-              }
-              if (mine) {
-                dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-              }
-            }
-            if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
-          }
-        } else {
-          const int ncols = min(kNvTile, a.out_cols - wt * kNvTile);
-          if (warp_has_rows) {
-            uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * a.out_cols + wt * kNvTile);
-#pragma unroll 1
-            for (int c0 = 0; c0 < kNvTile; c0 += 32) {
-              uint32_t v[2][16];
-              tc_ld_x16(acc + c0, v[0]);
-              tc_ld_x16(acc + c0 + 16, v[1]);
-              tc_wait_ld();
-              uint32_t packed[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
-                const uint32_t hi =
-                    __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
-                packed[i] = lo | (hi << 16);
-              }
-              if (mine && c0 < ncols) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-              }
-            }
-          }
-          if (a.red.out) fused_reduce_tail(a.red, a.y, a.out_cols, mine, row, wt, a.n_wt, wt * kNvTile, ncols);
+    bool ok = true;
+    for (int ph = kPh0; ok && ph <= kPh1; ++ph) {
+      const NvPhase& F = a.ph[ph];
+      const NvPassView V = pass_view(a, ph);
+      int t = blockIdx.x, p = 0, ep = -1;
+      RowPass P;
+      while (next_row_pass<BN>(V, msum, t, p, ep, P)) {
+        const int wt = t % F.n_wt;
+        ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+        ok = named_barrier_and(1, 128, ok);
+        if (!ok) {
+          *abort_flag = 1;
+          break;
         }
+        tc_fence_after();
+        const float ts = __ldg(F.tscale + P.e);
+        for (int j = 0; j < P.nb; ++j) {
+          const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNvTile);
+          const int row = (P.rb + j) * BN + m;
+          const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
+          const bool mine = row_e == P.e;
+          if (ph == 0) {
+            const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
+            // pass 1: h over the 128 columns, written back over the gate columns of the accumulator,
+            // and its amax; pass 2: read h back, quantise, store
+            if (warp_has_rows) {
+              float amax = 0.f;
+#pragma unroll 1
+              for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t g[2][16], u[2][16];
+                tc_ld_x16(acc + c0, g[0]);
+                tc_ld_x16(acc + c0 + 16, g[1]);
+                tc_ld_x16(acc + 128 + c0, u[0]);
+                tc_ld_x16(acc + 128 + c0 + 16, u[1]);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float h = silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
+                                              __uint_as_float(u[i >> 4][i & 15]) * ts) * wr;
+                  amax = fmaxf(amax, fabsf(h));
+                  g[i >> 4][i & 15] = __float_as_uint(h);
+                }
+                tc_st_x16(acc + c0, g[0]);
+                tc_st_x16(acc + c0 + 16, g[1]);
+              }
+              tc_wait_st();
+              const int ex = ue8m0_exponent(amax);
+              const float sc = pow2_neg(ex);
+              uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * F.out_cols + wt * 128);
+#pragma unroll 1
+              for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t g[2][16];
+                tc_ld_x16(acc + c0, g[0]);
+                tc_ld_x16(acc + c0 + 16, g[1]);
+                tc_wait_ld();
+                uint32_t packed[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  float h[4];
+#pragma unroll
+                  for (int v = 0; v < 4; ++v) {
+                    const int c = 4 * i + v;
+                    h[v] = __uint_as_float(g[c >> 4][c & 15]);
+                  }
+                  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
+                  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
+                  packed[i] = lo | (hi << 16);
+                }
+                if (mine) {
+                  dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                  dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                }
+              }
+              if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+            }
+          } else {
+            const int ncols = min(kNvTile, F.out_cols - wt * kNvTile);
+            if (warp_has_rows) {
+              uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * F.out_cols + wt * kNvTile);
+#pragma unroll 1
+              for (int c0 = 0; c0 < kNvTile; c0 += 32) {
+                uint32_t v[2][16];
+                tc_ld_x16(acc + c0, v[0]);
+                tc_ld_x16(acc + c0 + 16, v[1]);
+                tc_wait_ld();
+                uint32_t packed[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
+                  const uint32_t hi =
+                      __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
+                  packed[i] = lo | (hi << 16);
+                }
+                if (mine && c0 < ncols) {
+#pragma unroll
+                  for (int c = 0; c < 4; ++c)
+                    dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                }
+              }
+            }
+            if (a.red.out) fused_reduce_tail(a.red, a.y, F.out_cols, mine, row, wt, F.n_wt, wt * kNvTile, ncols);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(acc_empty));
+        acc_phase ^= 1;
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(acc_empty));
-      acc_phase ^= 1;
     }
+    if (!ok) *abort_flag = 1;
   }
   tc_fence_before();
   __syncthreads();
@@ -480,11 +511,13 @@ __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint
     const size_t ew = c / n_slabs;
     const int wt = static_cast<int>(ew % n_wt), e = static_cast<int>(ew / n_wt);
     const bool code = o < kNvTile * 32;
-    const int n = code ? o / 32 : (o - kNvTile * 32) / 4;
+    // codes: byte o = (half, row n, j) -> code byte 16 * half + j of row n's 32 (see kNvChunk)
+    const int n = code ? (o % (kNvTile * 16)) / 16 : (o - kNvTile * 32) / 4;
+    const int cb = code ? (o / (kNvTile * 16)) * 16 + o % 16 : 0;
     const int h = n / 128, mm = n % 128;
     const int r = pair == 2 ? h * (N / 2) + wt * 128 + mm : wt * 256 + n;
     if (code)
-      out[i] = r < N ? q[(static_cast<size_t>(e) * N + r) * (Kd / 2) + s * 32 + (o % 32)] : 0;
+      out[i] = r < N ? q[(static_cast<size_t>(e) * N + r) * (Kd / 2) + s * 32 + cb] : 0;
     else
       out[i] = r < N ? sf[(static_cast<size_t>(e) * N + r) * (Kd / 16) + s * 4 + (o - kNvTile * 32) % 4] : 0;
   }
@@ -507,49 +540,76 @@ EncodeTiledFnNv get_encode_nv() {
   return fn;
 }
 
-template <int BN, bool L1>
-cudaError_t launch_nv_t(const NvLaunch& L, cudaStream_t stream) {
+// Tensor map over bf16 activation rows [U, Kd] (box: 64 columns x BN rows, 128-byte swizzle).
+static bool make_rows_map(CUtensorMap* m, const uint16_t* rows, int Kd, int U, int BN) {
   EncodeTiledFnNv enc = get_encode_nv();
-  if (!enc) return cudaErrorInvalidValue;
-  CUtensorMap mx;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(L.Kd), static_cast<cuuint64_t>(L.U)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(L.Kd) * 2};
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(Kd), static_cast<cuuint64_t>(U)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(Kd) * 2};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(kNvSlab), static_cast<cuuint32_t>(BN)};
   cuuint32_t es[2] = {1, 1};
-  if (enc(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(L.xb), dims, strides, box, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
-  NvArgs a;
-  a.w = L.w;
-  a.tscale = L.tscale;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(rows), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static void fill_phase(const NvLaunch& L, bool l1, int nitems_per_wt, NvPhase& F) {
+  const int pair = l1 ? 2 : 1;
+  F.w = L.w;
+  F.tscale = L.tscale;
+  F.n_wt = pair == 2 ? L.w_rows / kNvTile : (L.w_rows + kNvTile - 1) / kNvTile;
+  F.n_slabs = L.Kd / kNvSlab;
+  F.w_bytes = static_cast<size_t>(L.E) * F.n_wt * F.n_slabs * kNvChunk;
+  F.out_cols = l1 ? L.I : L.w_rows;
+  F.n_tiles = nitems_per_wt * F.n_wt;
+}
+
+// L1 (l1 non-null) or L2 (l2 non-null).
+template <int BN>
+static cudaError_t launch_nv_t(const NvLaunch* l1, const NvLaunch* l2, cudaStream_t stream) {
+  const NvLaunch& L = l1 ? *l1 : *l2;
+  CUtensorMap mx = {};
+  if (!make_rows_map(&mx, L.xb, L.Kd, L.U, BN)) return cudaErrorInvalidValue;
+  NvArgs a{};
+  a.one_expert_blocks = L.align % BN == 0;
+  // items: halves of row-block pairs (blocks of up to 32 rows), whole pairs, or blocks
+  a.split_pairs = BN <= 32;
+  const int nrb = (L.U + BN - 1) / BN;
+  const int per_wt = a.one_expert_blocks ? (a.split_pairs ? (nrb + 1) / 2 * 2 : (nrb + 1) / 2) : nrb;
+  fill_phase(L, l1 != nullptr, per_wt, a.ph[l1 ? 0 : 1]);
   a.expert_ids = L.expert_ids;
   a.m_sum = L.m_sum;
   a.h_q = L.h_q;
   a.h_sf = L.h_sf;
   a.y = L.y;
+  a.status = L.status;
+  a.sf_nb = act_sf_blocks(L.U, BN);
   a.red = L.red;
   a.row_ids = L.row_ids;
   a.row_w = L.row_w;
-  a.status = L.status;
-  const int pair = L1 ? 2 : 1;
-  a.n_wt = pair == 2 ? L.w_rows / kNvTile : (L.w_rows + kNvTile - 1) / kNvTile;
-  a.n_slabs = L.Kd / kNvSlab;
-  a.w_bytes = static_cast<size_t>(L.E) * a.n_wt * a.n_slabs * kNvChunk;
-  a.out_cols = L1 ? L.I : L.w_rows;
-  a.sf_nb = act_sf_blocks(L.U, BN);
-  a.one_expert_blocks = L.align % BN == 0;
-  const int nrb = (L.U + BN - 1) / BN;
-  // items: halves of row-block pairs (blocks of up to 32 rows), whole pairs, or blocks
-  a.split_pairs = BN <= 32;
-  a.n_tiles = (a.one_expert_blocks ? (a.split_pairs ? (nrb + 1) / 2 * 2 : (nrb + 1) / 2) : nrb) * a.n_wt;
+  const int total = a.ph[l1 ? 0 : 1].n_tiles;
   int grid = num_sms();
-  if (grid > a.n_tiles) grid = a.n_tiles;
+  if (grid > total) grid = total;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(moe_gemm_nv_kernel<BN, L1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
-  if (err != cudaSuccess) return err;
-  moe_gemm_nv_kernel<BN, L1><<<grid, kNvThreads, kNvSmem, stream>>>(mx, a);
+  if (l1) {
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_nv_kernel<BN, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
+    if (err != cudaSuccess) return err;
+    moe_gemm_nv_kernel<BN, 1><<<grid, kNvThreads, kNvSmem, stream>>>(mx, a);
+  } else {
+    cudaError_t err = cudaFuncSetAttribute(moe_gemm_nv_kernel<BN, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kNvSmem);
+    if (err != cudaSuccess) return err;
+    moe_gemm_nv_kernel<BN, 2><<<grid, kNvThreads, kNvSmem, stream>>>(mx, a);
+  }
   return cudaGetLastError();
+}
+
+static cudaError_t launch_nv(const NvLaunch* l1, const NvLaunch* l2, cudaStream_t stream) {
+  switch (act_sf_block_rows((l1 ? l1 : l2)->align)) {
+    case 16: return launch_nv_t<16>(l1, l2, stream);
+    case 32: return launch_nv_t<32>(l1, l2, stream);
+    case 64: return launch_nv_t<64>(l1, l2, stream);
+    default: return launch_nv_t<128>(l1, l2, stream);
+  }
 }
 
 }  // namespace
@@ -576,21 +636,7 @@ cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_
 }
 
 cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream) {
-  const int bn = act_sf_block_rows(L.align);
-  if (l1) {
-    switch (bn) {
-      case 16: return launch_nv_t<16, true>(L, stream);
-      case 32: return launch_nv_t<32, true>(L, stream);
-      case 64: return launch_nv_t<64, true>(L, stream);
-      default: return launch_nv_t<128, true>(L, stream);
-    }
-  }
-  switch (bn) {
-    case 16: return launch_nv_t<16, false>(L, stream);
-    case 32: return launch_nv_t<32, false>(L, stream);
-    case 64: return launch_nv_t<64, false>(L, stream);
-    default: return launch_nv_t<128, false>(L, stream);
-  }
+  return l1 ? launch_nv(&L, nullptr, stream) : launch_nv(nullptr, &L, stream);
 }
 
 }  // namespace moe

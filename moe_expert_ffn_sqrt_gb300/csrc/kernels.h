@@ -121,27 +121,28 @@ cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
 // epilogue)
 struct I8Launch {
   const uint8_t* w;            // packed int8 weight stream
-  const float* col_scale;      // [E, w_rows] per-output-channel scales
+  const float* col_scale;      // [E, w_rows] per-output-channel scales (block: [E, w_rows/256, Kd/256])
   const uint16_t* xf;          // [U, Kd] fp16 activation codes
-  const float* row_scale;      // [U] per-row activation scales
+  const float* row_scale;      // [U] per-row activation scales (block: [U, Kd/256])
   const int32_t* expert_ids;
   const int32_t* m_sum;
   uint16_t* out;               // L1: h [U, I] bf16; L2: y [U, H] bf16
   uint32_t* status;
   int E, w_rows, Kd, I, U, align;
   FusedReduce red{};
+  int block = 0;               // [256, 256] block-quantised weights, per-256-group activation scales
 };
 size_t packed_i8_weight_bytes(int E, int N, int Kd, int pair);
 cudaError_t launch_pack_i8(const int8_t* q, int E, int N, int Kd, int pair, uint8_t* out, cudaStream_t stream);
-// fp16 rows of int8 codes (+ row scales) for rows r < m_sum with expert_ids[r] >= 0; source row
-// src_map[r] / K when src_map is given, else r.
+// fp16 rows of int8 codes (+ the row's nsc scales) for rows r < m_sum with expert_ids[r] >= 0;
+// source row src_map[r] / K when src_map is given, else r.
 cudaError_t launch_i8_rows_to_f16(const int8_t* src, const float* src_scale, int src_rows, const int32_t* src_map,
                                   int K, const int32_t* expert_ids, const int32_t* m_sum, int U, int C, uint16_t* dst,
-                                  float* dst_scale, uint32_t* status, cudaStream_t stream);
-// Per-row int8 quantisation of bf16 rows (all R rows, or with expert_ids the pair rows below m_sum);
-// f16 (nullable) receives the codes as fp16.
+                                  float* dst_scale, uint32_t* status, cudaStream_t stream, int nsc = 1);
+// Int8 quantisation of bf16 rows per group of `group` columns (0: the whole row; s is [rows, C/group])
+// (all R rows, or with expert_ids the pair rows below m_sum); f16 (nullable) receives the codes as fp16.
 cudaError_t launch_quant_rows_i8(const uint16_t* x, int R, int C, const int32_t* expert_ids, const int32_t* m_sum,
-                                 int8_t* q, float* s, uint16_t* f16, cudaStream_t stream);
+                                 int8_t* q, float* s, uint16_t* f16, cudaStream_t stream, int group = 0);
 cudaError_t launch_gemm_i8(const I8Launch& L, bool l1, cudaStream_t stream);
 
 // reduce.cu

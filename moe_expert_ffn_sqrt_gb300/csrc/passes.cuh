@@ -22,8 +22,10 @@ struct RowPass {
 // leave every other item empty and the passes unevenly spread over the CTAs), item t = k * n_wt + wt
 // is the whole pair: one pass over both blocks, or a pass per block.  Without one expert per block,
 // item t is block t / n_wt and each expert present in it is a pass (smallest expert id first).
+// With pair_blocks == 0 a pair's two blocks of one expert are two passes (one block each).
 // Called by whole warps; every role walks the same sequence.  Args needs n_tiles, n_wt,
-// one_expert_blocks, split_pairs and expert_ids; the item index modulo n_wt is the weight tile.
+// one_expert_blocks, split_pairs, pair_blocks and expert_ids; the item index modulo n_wt is the
+// weight tile.
 template <int BN, class Args>
 __device__ __forceinline__ bool next_row_pass(const Args& a, int msum, int& t, int& p, int& e_prev, RowPass& P) {
   const int lane = threadIdx.x & 31;
@@ -35,15 +37,16 @@ __device__ __forceinline__ bool next_row_pass(const Args& a, int msum, int& t, i
       if (rb0 * BN >= msum) return false;
       const int e0 = __ldg(a.expert_ids + rb0 * BN);
       const int e1 = rb1 * BN < msum ? __ldg(a.expert_ids + rb1 * BN) : -1;
+      const bool joint = a.pair_blocks && e1 == e0;   // one pass over both blocks
       if (a.split_pairs) {
         const int h = k & 1;
         if (p == 0) {
           p = 1;
           if (h == 0 && e0 >= 0) {
-            P = RowPass{e0, rb0, e1 == e0 ? 2 : 1};
+            P = RowPass{e0, rb0, joint ? 2 : 1};
             return true;
           }
-          if (h == 1 && e1 >= 0 && e1 != e0) {
+          if (h == 1 && e1 >= 0 && !joint) {
             P = RowPass{e1, rb1, 1};
             return true;
           }
@@ -52,13 +55,13 @@ __device__ __forceinline__ bool next_row_pass(const Args& a, int msum, int& t, i
         if (p == 0) {
           p = 1;
           if (e0 >= 0) {
-            P = RowPass{e0, rb0, e1 == e0 ? 2 : 1};
+            P = RowPass{e0, rb0, joint ? 2 : 1};
             return true;
           }
         }
         if (p == 1) {
           p = 2;
-          if (e1 >= 0 && e1 != e0) {
+          if (e1 >= 0 && !joint) {
             P = RowPass{e1, rb1, 1};
             return true;
           }

@@ -81,6 +81,6 @@ def test_launch_counts_match_the_measured_launch_lists():
     assert bench.launches_per_forward(W["prefill"]) == 8
     assert bench.launches_per_forward(dataclasses.replace(W["decode"], fmt="int8")) == 7
     assert bench.launches_per_forward(W["decode"], naive=True) == 2
-    # NVFP4: two launches (bf16 rows, GEMM) for each of L1 and L2; the permute copies nothing
-    # (the L1 conversion reads the token-order rows)
+    # NVFP4: two launches (bf16 rows, GEMM) for each of L1 and L2; the permute copies nothing (the
+    # L1 conversion reads the token-order rows)
     assert bench.launches_per_forward(W["skewed"]) == 3 + 2 + 4 + 1
