@@ -45,7 +45,7 @@ def launches_per_forward(w, naive=False):
     tk = w.T * w.K
     route = 1 if w.T <= 16 else 3                 # fused small-batch route, else gate split + gate GEMM + top-K
     reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue
-    if w.fmt == "int8":
+    if w.fmt in I8_FMTS:
         # route, per-token act quant, permute indices (one kernel up to 1024 pairs, else count + place),
         # then the row gather to fp16, L1, the per-row h requant and L2
         return route + 1 + (1 if tk <= 1024 else 2) + 4 + reduce
@@ -64,6 +64,7 @@ def launches_per_forward(w, naive=False):
 
 
 HEADLINE = "decode"
+I8_FMTS = ("int8", "int8b")
 # timed steps per workload in the per-config part of the default run (at most --steps)
 PER_CONFIG_STEPS = {"tiny": 300, "decode": 300, "batched": 200, "prefill": 60, "skewed": 20}
 
@@ -96,9 +97,10 @@ def parse_args():
     p.add_argument("--weights-in-l1", action="store_true",
                    help="apply the routing weights in the L1 epilogue and sum without weights "
                         "(moe_forward_l1_weighted) instead of weighting in the reduce")
-    p.add_argument("--weights", default="workload", choices=["workload", "int8"],
+    p.add_argument("--weights", default="workload", choices=["workload", "int8", "int8b"],
                    help="the workload's FP4 weight format, or the INT8 variant (int8 weights with per-channel "
-                        "scales, int8 activations with per-token scales: moe_forward_i8) on the same shapes")
+                        "scales, int8 activations with per-token scales: moe_forward_i8; int8b: [256, 256] weight blocks, "
+                        "per-256-group activation scales) on the same shapes")
     p.add_argument("--l1-input", default="auto", choices=["auto", "token", "permuted"],
                    help="stage-by-stage timing: the L1 GEMM reads the token-order activation through "
                         "sorted_token_ids or the permute's row copy x_perm; auto: as moe_forward does "
@@ -132,8 +134,11 @@ def job_tokens_per_s(world_size, tokens_per_rank, ms):
 
 
 def workload_config(w):
-    acts = ("INT8 activations (fp32 scale per token)" if w.fmt == "int8" else "FP8 E4M3 activations (UE8M0/128)")
-    wts = "INT8 weights (fp32 scale per channel)" if w.fmt == "int8" else f"{w.fmt.upper()} weights"
+    acts = {"int8": "INT8 activations (fp32 scale per token)",
+            "int8b": "INT8 activations (fp32 scale per token and 256-column group)"}.get(
+        w.fmt, "FP8 E4M3 activations (UE8M0/128)")
+    wts = {"int8": "INT8 weights (fp32 scale per channel)",
+           "int8b": "INT8 weights (fp32 scale per [256, 256] block)"}.get(w.fmt, f"{w.fmt.upper()} weights")
     return {"workload": f"{w.name}: T={w.T} H={w.H} I={w.I} E={w.E} K={w.K} align={w.align} "
                         f"{w.score_fn} {wts}, {acts}",
             "T": w.T, "H": w.H, "I": w.I, "E": w.E, "K": w.K, "align": w.align, "weights": w.fmt}
@@ -222,10 +227,10 @@ class ClockSampler:
 
 def oracle_forward(w, workers=1):
     """The oracle's whole-layer function for the workload's weight format, as f(inp, prov, tokens)."""
-    if w.fmt == "int8":
+    if w.fmt in I8_FMTS:
         from oracle import int8 as QI
         return lambda inp, prov, tokens: QI.forward_i8(inp, prov, w.K, w.align, w.score_fn, w.renormalize,
-                                                       tokens=tokens)
+                                                       tokens=tokens, block=w.fmt == "int8b")
     from oracle import moe as O
     return lambda inp, prov, tokens: O.forward(inp, prov, w.fmt, w.K, w.align, w.score_fn, w.renormalize,
                                                tokens=tokens, workers=workers)
@@ -237,7 +242,7 @@ ORACLE_BATCH = 8     # tokens per oracle call of the CPU baseline (the decode ba
 def oracle_tokens_per_s(w, inp, stack, budget_s):
     """Times the float64 oracle on batches of whole tokens of the workload until the budget is spent.
     Its experts run on oracle_threads() worker threads (BLAS single-threaded)."""
-    n_thr = 1 if w.fmt == "int8" else oracle_threads()
+    n_thr = 1 if w.fmt in I8_FMTS else oracle_threads()
     fwd = oracle_forward(w, n_thr)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
     done, t0 = 0, time.perf_counter()
@@ -260,7 +265,7 @@ def run_reference(args, w):
         return
     inp = synth.layer_inputs(w)
     stack = synth.all_expert_weights(w)
-    cores = 1 if w.fmt == "int8" else oracle_threads()
+    cores = 1 if w.fmt in I8_FMTS else oracle_threads()
     fwd = oracle_forward(w, cores)
     prov = (lambda e: {k: (v[e] if v is not None else None) for k, v in stack.items()})
     nb = min(ORACLE_BATCH, w.T)
@@ -294,13 +299,20 @@ def run_reference(args, w):
 def algorithmic_bytes(w, n_touched):
     """Bytes the method must move per launch of each stage (padding and untouched experts excluded)."""
     TK = w.T * w.K
-    if w.fmt == "int8":
+    if w.fmt in I8_FMTS:
         # int8 codes + fp32 channel scales; activations int8 + one fp32 scale per row
-        w13 = n_touched * (2 * w.I * w.H + 2 * w.I * 4)
-        w2 = n_touched * (w.H * w.I + w.H * 4)
-        l1 = w13 + TK * (w.H + 4) + TK * (w.I + 4)
-        l2 = w2 + TK * (w.I + 4) + TK * w.H * 2
-        return {"l1": l1, "l2": l2, "ffn": w13 + w2 + TK * (w.H + 4) + TK * w.H * 2,
+        # (int8b: one fp32 scale per [256, 256] weight block and per 256-column group of a row)
+        if w.fmt == "int8":
+            w13 = n_touched * (2 * w.I * w.H + 2 * w.I * 4)
+            w2 = n_touched * (w.H * w.I + w.H * 4)
+            sx, sh = 4, 4
+        else:
+            w13 = n_touched * (2 * w.I * w.H + (2 * w.I // 256) * (w.H // 256) * 4)
+            w2 = n_touched * (w.H * w.I + (w.H // 256) * (w.I // 256) * 4)
+            sx, sh = w.H // 256 * 4, w.I // 256 * 4
+        l1 = w13 + TK * (w.H + sx) + TK * (w.I + sh)
+        l2 = w2 + TK * (w.I + sh) + TK * w.H * 2
+        return {"l1": l1, "l2": l2, "ffn": w13 + w2 + TK * (w.H + sx) + TK * w.H * 2,
                 "layer": w13 + w2 + 4 * w.E * w.H + 2 * w.T * w.H * 2}
     if w.fmt == "mxfp4":
         w13 = n_touched * (2 * w.I * w.H // 2 + 2 * w.I * w.H // 32)
@@ -315,7 +327,7 @@ def algorithmic_bytes(w, n_touched):
 
 
 def kernel_name(stage, fmt):
-    if fmt == "int8":
+    if fmt in I8_FMTS:
         return {"ffn": "INT8 L1 (row gather, GEMM, h requant) then L2 (h to fp16, GEMM)",
                 "l1": "INT8 L1 (row gather, GEMM, h requant)", "l2": "INT8 L2 (h to fp16, GEMM)"}[stage]
     if stage == "ffn":
@@ -336,10 +348,10 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     def d(a):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    i8 = w.fmt == "int8"
-    if i8:      # int8 codes; the per-channel scales travel as the weight's tscale
-        w13 = M.Weight(d(stack["w13_q"]), None, d(stack["w13_sf"]), "int8", pair=2)
-        w2 = M.Weight(d(stack["w2_q"]), None, d(stack["w2_sf"]), "int8", pair=1)
+    i8 = w.fmt in I8_FMTS
+    if i8:      # int8 codes; the channel or block scales travel as the weight's tscale
+        w13 = M.Weight(d(stack["w13_q"]), None, d(stack["w13_sf"]), w.fmt, pair=2)
+        w2 = M.Weight(d(stack["w2_q"]), None, d(stack["w2_sf"]), w.fmt, pair=1)
     else:
         w13 = M.Weight(d(stack["w13_q"]), d(stack["w13_sf"]), None if stack["w13_ts"] is None else d(stack["w13_ts"]),
                        w.fmt, pair=2)
@@ -429,9 +441,10 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     y = torch.empty(U, w.H, dtype=torch.bfloat16, device=dev)
     if i8:
         xq8 = torch.empty(T, w.H, dtype=torch.int8, device=dev)
-        xs8 = torch.empty(T, dtype=torch.float32, device=dev)
+        blk = w.fmt == "int8b"      # one scale per 256-column group instead of one per row
+        xs8 = torch.empty((T, w.H // 256) if blk else (T,), dtype=torch.float32, device=dev)
         hq8 = torch.empty(U, w.I, dtype=torch.int8, device=dev)
-        hs8 = torch.empty(U, dtype=torch.float32, device=dev)
+        hs8 = torch.empty((U, w.I // 256) if blk else (U,), dtype=torch.float32, device=dev)
     # MXFP4: the expert FFN is one launch (moe_grouped_ffn), timed as one stage; NVFP4: L1 and L2 apart
     # (BatchedExperts: the whole FFN through moe_grouped_ffn_batched, whose row-map kernel from the
     # per-expert counts is counted in the stage; moe_forward_batched takes the row map from the permute)
@@ -516,7 +529,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     top = "ffn" if fused else max(("l1", "l2"), key=lambda s: stage_ms[s])
     top_key = f"{w.name}:{top}" + (":batched" if batched else "")
     kernel_file = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300", "csrc",
-                               {"mxfp4": "gemm.cu", "nvfp4": "gemm_nv.cu", "int8": "gemm_i8.cu"}[w.fmt])
+                               {"mxfp4": "gemm.cu", "nvfp4": "gemm_nv.cu", "int8": "gemm_i8.cu", "int8b": "gemm_i8.cu"}[w.fmt])
     tk = w.T * w.K
     flops = {"l1": 2.0 * tk * 2 * w.I * w.H, "l2": 2.0 * tk * w.I * w.H}
     flops["ffn"] = flops["l1"] + flops["l2"]
@@ -543,6 +556,17 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
 
     # ---- end to end through the public API with host buffers: H2D input, forward, D2H output
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # host cost of issuing one end-to-end step, measured while a GPU-side spin holds the device (so
+    # the launch queue never fills and the host never waits): steps outside the timed region
+    barrier()
+    n_probe = 16
+    torch.cuda._sleep(100 * SPIN_CYCLES)
+    h0 = time.perf_counter()
+    for i in range(n_probe):
+        hidden.copy_(hidden_host, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    host_us = (time.perf_counter() - h0) * 1e6 / n_probe
     barrier()
     for i in range(K):
         flush.fill_(i & 0xFF)
@@ -554,7 +578,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     barrier()
     e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_ev), dev)
     e2e = {"value": job_tokens_per_s(W, T, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": T * w.H * 2,
-           "d2h_bytes_per_step": T * w.H * 2}
+           "d2h_bytes_per_step": T * w.H * 2, "host_issue_us_per_step": host_us}
 
     cpu = None
     if rank == 0 and W == 1 and cpu_seconds > 0:
@@ -574,7 +598,8 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
                clocks=clk, launches=launches_per_forward(w, naive) * K,
                dtype={"mxfp4": "fp8xfp4 (fp32 accumulate)",
                       "nvfp4": "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
-                      "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)"}[w.fmt])
+                      "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)",
+                      "int8b": "int8xint8 as fp16 (exact codes, fp32 accumulate per 256-deep block)"}[w.fmt])
     del w13, w2, ws, flush, xp, hq, y, hidden, out
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -627,13 +652,13 @@ def main():
     args = parse_args()
     if args.weights_in_l1 and args.layout != "contiguous":
         raise SystemExit("--weights-in-l1 applies to the expert-contiguous layout")
-    if args.weights == "int8" and (args.weights_in_l1 or args.layout != "contiguous"):
-        raise SystemExit("--weights int8 runs the expert-contiguous layout with the weights applied in the reduce")
+    if args.weights in I8_FMTS and (args.weights_in_l1 or args.layout != "contiguous"):
+        raise SystemExit("--weights int8/int8b runs the expert-contiguous layout with the weights applied in the reduce")
     import dataclasses
 
     def variant(w):
-        if args.weights == "int8":
-            w = dataclasses.replace(w, fmt="int8", name=f"{w.name}-int8")
+        if args.weights in I8_FMTS:
+            w = dataclasses.replace(w, fmt=args.weights, name=f"{w.name}-{args.weights}")
         if args.experts or args.tokens:
             E = args.experts or w.E
             T = args.tokens or w.T

@@ -14,9 +14,10 @@ LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_DEVICE_INDEX, ERR_TIMEOUT, ERR_DEVICE_CHECK = range(8)
 SCORE_SOFTMAX, SCORE_SQRT_SOFTPLUS = 0, 1
-W_MXFP4, W_NVFP4, W_INT8 = 0, 1, 2
+W_MXFP4, W_NVFP4, W_INT8, W_INT8_B256 = 0, 1, 2, 3
 SCORE_FNS = {"softmax": SCORE_SOFTMAX, "sqrt_softplus": SCORE_SQRT_SOFTPLUS}
-WFMTS = {"mxfp4": W_MXFP4, "nvfp4": W_NVFP4, "int8": W_INT8}
+WFMTS = {"mxfp4": W_MXFP4, "nvfp4": W_NVFP4, "int8": W_INT8, "int8b": W_INT8_B256}
+I8_FMTS = (W_INT8, W_INT8_B256)
 
 
 class MoeError(RuntimeError):
@@ -98,6 +99,8 @@ def lib():
         L.moe_workspace_size_i8.restype = S
         L.moe_act_quant_i8.argtypes = [P, I, I, P, P, P]
         L.moe_act_quant_i8.restype = S
+        L.moe_act_quant_i8_b256.argtypes = [P, I, I, P, P, P]
+        L.moe_act_quant_i8_b256.restype = S
         L.moe_grouped_gemm_l1_swiglu_i8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
         L.moe_grouped_gemm_l1_swiglu_i8.restype = S
         L.moe_grouped_gemm_l2_i8.argtypes = [P, P, P, P, I, I, I, I, I, I, _Weight, P, P, Z, P]
@@ -200,10 +203,10 @@ def new_workspace(T, H, I, E, K, align, device="cuda"):
 def pack_weights(fmt, q, sf, pair, out=None):
     """Packs codes q and scales sf into the GEMMs' weight stream (moe_pack_weights).
 
-    FP4 formats: q [E, N, Kd/2] packed E2M1 (uint8), sf the block scales.  INT8: q [E, N, Kd] int8,
-    sf unused (the channel scales are passed to Weight as tscale).
+    FP4 formats: q [E, N, Kd/2] packed E2M1 (uint8), sf the block scales.  INT8 ("int8", "int8b"):
+    q [E, N, Kd] int8, sf unused (the channel or block scales are passed to Weight as tscale).
     """
-    if WFMTS.get(fmt, fmt) == W_INT8:
+    if WFMTS.get(fmt, fmt) in I8_FMTS:
         E, N, Kd = q.shape
         qp, sfp = _ptr(q, torch.int8, "q"), None
     else:
@@ -227,7 +230,8 @@ class Weight:
     def __init__(self, q, sf, tscale=None, fmt="mxfp4", pair=1):
         self.fmt = fmt
         self.E, self.N, kq = q.shape
-        self.Kd = kq if WFMTS.get(fmt, fmt) == W_INT8 else 2 * kq     # INT8: tscale = [E, N] channel scales
+        # INT8: tscale = [E, N] channel scales ("int8") or [E, N/256, Kd/256] block scales ("int8b")
+        self.Kd = kq if WFMTS.get(fmt, fmt) in I8_FMTS else 2 * kq
         self.pair = pair
         self.tscale = tscale
         self.packed = pack_weights(fmt, q, sf, pair)
@@ -460,10 +464,12 @@ def new_workspace_i8(T, H, I, E, K, align, device="cuda"):
 
 
 def act_quant_i8(x, x_q, x_s):
-    """Per-row int8 quantisation: x [R, C] bf16 -> x_q [R, C] int8, x_s [R] fp32."""
+    """Per-row int8 quantisation: x [R, C] bf16 -> x_q [R, C] int8, x_s [R] fp32; with x_s of shape
+    [R, C/256], per 256-column group (moe_act_quant_i8_b256)."""
     R, C = x.shape
-    _check(lib().moe_act_quant_i8(_ptr(x, torch.bfloat16, "x"), R, C, _ptr(x_q, torch.int8, "x_q"),
-                                  _ptr(x_s, torch.float32, "x_s"), _stream()), "moe_act_quant_i8")
+    fn = lib().moe_act_quant_i8_b256 if x_s.dim() == 2 else lib().moe_act_quant_i8
+    _check(fn(_ptr(x, torch.bfloat16, "x"), R, C, _ptr(x_q, torch.int8, "x_q"), _ptr(x_s, torch.float32, "x_s"),
+              _stream()), "moe_act_quant_i8")
 
 
 def grouped_gemm_l1_swiglu_i8(x_q, x_s, sorted_token_ids, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_s, ws):

@@ -44,7 +44,7 @@ def host_bits(t):
 
 
 def device_weights(M, stack, fmt):
-    if fmt == "int8":      # int8 codes; the per-channel scales travel as the weight's tscale
+    if fmt in ("int8", "int8b"):   # int8 codes; the channel or block scales travel as the weight's tscale
         return (M.Weight(dev(stack["w13_q"]), None, dev(stack["w13_sf"]), fmt, pair=2),
                 M.Weight(dev(stack["w2_q"]), None, dev(stack["w2_sf"]), fmt, pair=1))
     w13 = M.Weight(dev(stack["w13_q"]), dev(stack["w13_sf"]),
