@@ -157,6 +157,98 @@ __device__ __forceinline__ void convert_row(const uint8_t* __restrict__ packed, 
   }
 }
 
+// Drains one accumulator (this warp's lane quarter at TMEM address acc) for token row `row` (stored
+// when mine) of weight tile wt: L1 (ph 0) SwiGLU + FP8 requant into h_q / h_sf, L2 bf16 y (+ the
+// fused reduce).  Called by all four epilogue warps together.
+template <int BN>
+__device__ __forceinline__ void nv_drain(const NvArgs& a, const NvPhase& F, int ph, uint32_t acc, int row,
+                                         bool mine, int wt, float ts, bool warp_has_rows) {
+  if (ph == 0) {
+    const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
+    // pass 1: h over the 128 channels, written back over the gate columns of the accumulator,
+    // and its amax; pass 2: read h back, quantise, store.  Channel c's gate product is in column
+    // gcol(c) = (c & 63) + 128 * (c >> 6), its up product in gcol(c) + 64 (the W13 tile order).
+    if (warp_has_rows) {
+      float amax = 0.f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        const uint32_t gc = static_cast<uint32_t>((c0 & 63) + 128 * (c0 >> 6));
+        uint32_t g[2][16], u[2][16];
+        tc_ld_x16(acc + gc, g[0]);
+        tc_ld_x16(acc + gc + 16, g[1]);
+        tc_ld_x16(acc + gc + 64, u[0]);
+        tc_ld_x16(acc + gc + 80, u[1]);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float h = silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
+                                      __uint_as_float(u[i >> 4][i & 15]) * ts) * wr;
+          amax = fmaxf(amax, fabsf(h));
+          g[i >> 4][i & 15] = __float_as_uint(h);
+        }
+        tc_st_x16(acc + gc, g[0]);
+        tc_st_x16(acc + gc + 16, g[1]);
+      }
+      tc_wait_st();
+      const int ex = ue8m0_exponent(amax);
+      const float sc = pow2_neg(ex);
+      uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * F.out_cols + wt * 128);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        const uint32_t gc = static_cast<uint32_t>((c0 & 63) + 128 * (c0 >> 6));
+        uint32_t g[2][16];
+        tc_ld_x16(acc + gc, g[0]);
+        tc_ld_x16(acc + gc + 16, g[1]);
+        tc_wait_ld();
+        uint32_t packed[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float h[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int c = 4 * i + v;
+            h[v] = __uint_as_float(g[c >> 4][c & 15]);
+          }
+          const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
+          const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
+          packed[i] = lo | (hi << 16);
+        }
+        if (mine) {
+          dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+      }
+      if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+    }
+  } else {
+    const int ncols = min(kNvTile, F.out_cols - wt * kNvTile);
+    if (warp_has_rows) {
+      uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * F.out_cols + wt * kNvTile);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kNvTile; c0 += 32) {
+        uint32_t v[2][16];
+        tc_ld_x16(acc + c0, v[0]);
+        tc_ld_x16(acc + c0 + 16, v[1]);
+        tc_wait_ld();
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
+          const uint32_t hi =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
+          packed[i] = lo | (hi << 16);
+        }
+        if (mine && c0 < ncols) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        }
+      }
+    }
+    if (a.red.out) fused_reduce_tail(a.red, a.y, F.out_cols, mine, row, wt, F.n_wt, wt * kNvTile, ncols);
+  }
+}
+
 // Warp roles: 0 loads (TMA token rows + bulk copy of packed weights into the load ring), 1 issues
 // the MMAs, 2..9 convert packed weights into the bf16 ring, 10..13 drain the accumulators.
 // A pass with two row blocks accumulates block j into TMEM columns [256j, 256j+256); the
@@ -361,87 +453,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           const int row = (P.rb + j) * BN + m;
           const int row_e = (m < BN && row < msum) ? __ldg(a.expert_ids + row) : -1;
           const bool mine = row_e == P.e;
-          if (ph == 0) {
-            const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
-            // pass 1: h over the 128 columns, written back over the gate columns of the accumulator,
-            // and its amax; pass 2: read h back, quantise, store
-            if (warp_has_rows) {
-              float amax = 0.f;
-#pragma unroll 1
-              for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t g[2][16], u[2][16];
-                tc_ld_x16(acc + c0, g[0]);
-                tc_ld_x16(acc + c0 + 16, g[1]);
-                tc_ld_x16(acc + 128 + c0, u[0]);
-                tc_ld_x16(acc + 128 + c0 + 16, u[1]);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const float h = silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts,
-                                              __uint_as_float(u[i >> 4][i & 15]) * ts) * wr;
-                  amax = fmaxf(amax, fabsf(h));
-                  g[i >> 4][i & 15] = __float_as_uint(h);
-                }
-                tc_st_x16(acc + c0, g[0]);
-                tc_st_x16(acc + c0 + 16, g[1]);
-              }
-              tc_wait_st();
-              const int ex = ue8m0_exponent(amax);
-              const float sc = pow2_neg(ex);
-              uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * F.out_cols + wt * 128);
-#pragma unroll 1
-              for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t g[2][16];
-                tc_ld_x16(acc + c0, g[0]);
-                tc_ld_x16(acc + c0 + 16, g[1]);
-                tc_wait_ld();
-                uint32_t packed[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  float h[4];
-#pragma unroll
-                  for (int v = 0; v < 4; ++v) {
-                    const int c = 4 * i + v;
-                    h[v] = __uint_as_float(g[c >> 4][c & 15]);
-                  }
-                  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
-                  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
-                  packed[i] = lo | (hi << 16);
-                }
-                if (mine) {
-                  dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                  dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                }
-              }
-              if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
-            }
-          } else {
-            const int ncols = min(kNvTile, F.out_cols - wt * kNvTile);
-            if (warp_has_rows) {
-              uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * F.out_cols + wt * kNvTile);
-#pragma unroll 1
-              for (int c0 = 0; c0 < kNvTile; c0 += 32) {
-                uint32_t v[2][16];
-                tc_ld_x16(acc + c0, v[0]);
-                tc_ld_x16(acc + c0 + 16, v[1]);
-                tc_wait_ld();
-                uint32_t packed[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
-                  const uint32_t hi =
-                      __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
-                  packed[i] = lo | (hi << 16);
-                }
-                if (mine && c0 < ncols) {
-#pragma unroll
-                  for (int c = 0; c < 4; ++c)
-                    dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                }
-              }
-            }
-            if (a.red.out) fused_reduce_tail(a.red, a.y, F.out_cols, mine, row, wt, F.n_wt, wt * kNvTile, ncols);
-          }
+          nv_drain<BN>(a, F, ph, acc, row, mine, wt, ts, warp_has_rows);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(acc_empty));
@@ -455,6 +467,506 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kNvTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// CTA pairs for 128-row blocks (cta_group::2).  The two CTAs of a cluster run one MMA of M = 256
+// token rows (two row blocks, one per CTA) x N = 256 weight rows, each CTA holding half of the
+// weight tile: so each converts 128 weight rows per slab instead of 256, for the same tensor work
+// per SM.  With both TMEM accumulators a pass covers up to four row blocks of one expert (a
+// "quad": blocks 4q, 4q+1 in the even CTA, 4q+2, 4q+3 in the odd one).  The even CTA issues the
+// MMAs; each CTA loads its own token rows and its half of the packed chunk, converts its half, and
+// drains its own accumulator rows.  Cross-CTA signals: converter warps and epilogue warps of both
+// CTAs arrive on the even CTA's bf16-ready and accumulator-empty barriers; the MMA commits arrive
+// on both CTAs' slot-empty and accumulator-full barriers (multicast).
+
+constexpr int kNvHalfRows = kNvTile / 2;
+constexpr int kNvHalfChunk = kNvHalfRows * 36;   // 128 rows x (32 code bytes + 4 scales)
+constexpr int kNvPairLoadStage = (2 * kNvABytes + kNvHalfChunk + 1023) / 1024 * 1024;   // 37 KB
+constexpr int kNvPairLoadStages = 4;
+constexpr int kNvPairBStage = kNvHalfRows * 128;                                        // 16 KB
+constexpr int kNvPairBStages = 4;
+constexpr int kNvMaxRuns = 1024;                                        // experts with rows
+constexpr int kNvRunBytes = kNvMaxRuns * 2 * 2 + (kNvMaxRuns + 2) * 4;   // run table
+constexpr int kNvPairSmem =
+    1024 + kNvPairLoadStages * kNvPairLoadStage + kNvPairBStages * kNvPairBStage + kNvExtra + kNvRunBytes;
+static_assert(kNvPairSmem <= kNvBudget, "shared memory budget (pair)");
+// Row blocks whose first-row experts the prologue stages in the (then unused) load ring.
+constexpr int kNvPairMaxBlocks = kNvPairLoadStages * kNvPairLoadStage / 4;
+constexpr uint32_t kNvConvWarps = kNvConvThreads / 32;
+
+// Passes of a CTA pair.  An expert's row blocks are consecutive (a run); its passes take them four
+// at a time (c <= 4 blocks from b0).  Slot j of a pass is an accumulator: with 2j + 1 < c it holds two
+// blocks, b0 + 2j in the even CTA and b0 + 2j + 1 in the odd one (an M = 256 MMA); with 2j + 1 == c it
+// holds block b0 + 2j alone, split by rows: rows 0..63 in the even CTA, 64..127 in the odd one (an
+// M = 128 MMA, so a lone block costs no more tensor time than on one SM).  A run of n blocks makes
+// ceil(n / 4) passes and a pass never mixes experts.
+struct PairPass {
+  int e, b0, c;
+};
+
+// Run table in shared memory, built by every CTA at kernel start from expert_ids (one entry per
+// block: its first row's expert; blocks hold one expert each).
+struct RunTable {
+  uint16_t* start;   // [kNvMaxRuns] first block of run i
+  uint16_t* len;     // [kNvMaxRuns] blocks of run i
+  int* pfx;          // [kNvMaxRuns + 2] passes before run i; pfx[n] = all passes; last: n
+  int n;             // runs
+};
+
+// Pass `pi` of the table (pfx[i] <= pi < pfx[i + 1] for run i).
+__device__ __forceinline__ PairPass pair_pass(const RunTable& R, const int32_t* expert_ids, int pi) {
+  int lo = 0, hi = R.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (R.pfx[mid] <= pi) lo = mid;
+    else hi = mid - 1;
+  }
+  const int o = 4 * (pi - R.pfx[lo]);
+  PairPass P;
+  P.b0 = R.start[lo] + o;
+  P.c = min(4, static_cast<int>(R.len[lo]) - o);
+  P.e = __ldg(expert_ids + static_cast<size_t>(P.b0) * 128);
+  return P;
+}
+
+// Slot j of the pass: 2 = a block per CTA (M = 256), 1 = one block split by rows (M = 128), 0 = unused.
+__device__ __forceinline__ int pair_slot(const PairPass& P, int j) {
+  return 2 * j + 1 < P.c ? 2 : (2 * j + 1 == P.c ? 1 : 0);
+}
+
+// Converts part h (codes 32h .. 32h+31) of weight row n of this CTA's half tile.  The half chunk in
+// shared memory: code bytes 0..15 of its 128 rows (2 KB), then bytes 16..31 (2 KB), then 128 x 4
+// E4M3 scales.
+__device__ __forceinline__ void convert_half_row(const uint8_t* __restrict__ packed, uint8_t* __restrict__ btile,
+                                                 int n, int h) {
+  const uint4 c = *reinterpret_cast<const uint4*>(packed + h * (kNvHalfRows * 16) + n * 16);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(packed + kNvHalfRows * 32 + n * 4) >> (16 * h);
+  uint32_t s2[2];
+  e4m3x2_to_bf16x2(sc, s2[0], s2[1]);
+  const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+  const uint32_t row = smem_u32(btile) + static_cast<uint32_t>(n) * 128;
+  const uint32_t x = static_cast<uint32_t>(n & 7) << 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t q[4];
+    e2m1x8_to_bf16(words[i], s2[i >> 1], q);
+    const uint32_t addr = row | ((static_cast<uint32_t>(4 * h + i) << 4) ^ x);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                 : "memory");
+  }
+}
+
+// Drains a split slot (an M = 128 MMA over the pair): this CTA's 64 rows of the block, each row in
+// two lanes.  Lanes 0..63 (epilogue warps 0, 1) hold output columns 0..127 of row lane, lanes
+// 64..127 (warps 2, 3) columns 128..255 of row lane - 64; `half` is 0 or 1 accordingly and acc
+// already names this warp's lane quarter.  L1: a half holds 64 channels (gate products in columns
+// 0..63, up in 64..127), and the row's amax is combined through xa[64] in shared memory.  Called by
+// all four epilogue warps together.
+template <int BN>
+__device__ __forceinline__ void nv_drain_split(const NvArgs& a, const NvPhase& F, int ph, uint32_t acc, int row,
+                                               bool mine, int half, int rl, int wt, float ts, float* xa) {
+  if (ph == 0) {
+    const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
+    float amax = 0.f;
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t g[2][16], u[2][16];
+      tc_ld_x16(acc + c0, g[0]);
+      tc_ld_x16(acc + c0 + 16, g[1]);
+      tc_ld_x16(acc + 64 + c0, u[0]);
+      tc_ld_x16(acc + 64 + c0 + 16, u[1]);
+      tc_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float h = silu_mul_nv(__uint_as_float(g[i >> 4][i & 15]) * ts, __uint_as_float(u[i >> 4][i & 15]) * ts) * wr;
+        amax = fmaxf(amax, fabsf(h));
+        g[i >> 4][i & 15] = __float_as_uint(h);
+      }
+      tc_st_x16(acc + c0, g[0]);
+      tc_st_x16(acc + c0 + 16, g[1]);
+    }
+    tc_wait_st();
+    if (half) xa[rl] = amax;
+    named_barrier(1, 128);
+    if (!half) {
+      amax = fmaxf(amax, xa[rl]);
+      xa[rl] = amax;
+    }
+    named_barrier(1, 128);
+    if (half) amax = xa[rl];
+    const int ex = ue8m0_exponent(amax);
+    const float sc = pow2_neg(ex);
+    uint4* dst = reinterpret_cast<uint4*>(a.h_q + static_cast<size_t>(row) * F.out_cols + wt * 128 + 64 * half);
+#pragma unroll 1
+    for (int c0 = 0; c0 < 64; c0 += 32) {
+      uint32_t g[2][16];
+      tc_ld_x16(acc + c0, g[0]);
+      tc_ld_x16(acc + c0 + 16, g[1]);
+      tc_wait_ld();
+      uint32_t packed[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float h[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int c = 4 * i + v;
+          h[v] = __uint_as_float(g[c >> 4][c & 15]);
+        }
+        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(h[0] * sc, h[1] * sc), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(h[2] * sc, h[3] * sc), __NV_SATFINITE, __NV_E4M3);
+        packed[i] = lo | (hi << 16);
+      }
+      if (mine) {
+        dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+      }
+    }
+    if (mine && !half) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
+  } else {
+    const int tcols = min(kNvTile, F.out_cols - wt * kNvTile);
+    const int ncols = tcols - 128 * half;   // this half's columns (a last half tile may have none)
+    if (ncols > 0) {
+      uint4* dst = reinterpret_cast<uint4*>(a.y + static_cast<size_t>(row) * F.out_cols + wt * kNvTile + 128 * half);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[2][16];
+        tc_ld_x16(acc + c0, v[0]);
+        tc_ld_x16(acc + c0 + 16, v[1]);
+        tc_wait_ld();
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]) * ts));
+          const uint32_t hi =
+              __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15]) * ts));
+          packed[i] = lo | (hi << 16);
+        }
+        if (mine && c0 < ncols) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+        }
+      }
+    }
+    if (a.red.out) {
+      named_barrier(1, 128);   // both halves of each row stored before its row owner takes a ticket
+      fused_reduce_tail(a.red, a.y, F.out_cols, mine && !half, row, wt, F.n_wt, wt * kNvTile, tcols);
+    }
+  }
+}
+
+// Warp roles as in moe_gemm_nv_kernel; warp 1 of the odd CTA only takes part in the tensor-memory
+// allocation.  MODE 1: L1 items, 2: L2 items.  Launched in clusters of two CTAs; item t = pass
+// (t / n_wt) of the run table against weight tile t % n_wt, cluster c taking items c, c + clusters, ...
+template <int MODE>
+__global__ void __launch_bounds__(kNvThreads, 1)
+    moe_gemm_nv_pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_x64,
+                            const NvArgs a) {
+  constexpr int BN = 128;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* lring = smem;                                       // token rows of two blocks + half chunk
+  uint8_t* bring = smem + kNvPairLoadStages * kNvPairLoadStage;   // bf16 half tiles
+  uint8_t* extra = bring + kNvPairBStages * kNvPairBStage;
+  uint64_t* full = reinterpret_cast<uint64_t*>(extra);         // load slot filled (TMA + bulk copies)
+  uint64_t* lempty = full + kNvPairLoadStages;                 // load slot consumed (pair MMA commit)
+  uint64_t* bready = lempty + kNvPairLoadStages;               // even CTA: both halves written
+  uint64_t* bempty = bready + kNvPairBStages;                  // half tile consumed (pair MMA commit)
+  uint64_t* acc_full = bempty + kNvPairBStages;
+  uint64_t* acc_empty = acc_full + 1;                          // even CTA: both CTAs drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* xa = reinterpret_cast<float*>(extra + 256);          // [64] row amax of split slots (L1)
+  RunTable R;
+  R.start = reinterpret_cast<uint16_t*>(extra + kNvExtra);
+  R.len = R.start + kNvMaxRuns;
+  R.pfx = reinterpret_cast<int*>(R.len + kNvMaxRuns);
+  constexpr int kPh = (MODE & 1) ? 0 : 1;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = static_cast<int>(blockIdx.x >> 1), nclusters = static_cast<int>(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNvPairLoadStages; ++s) {
+      mbar_init(smem_u32(full + s), 1);
+      mbar_init(smem_u32(lempty + s), 1);
+    }
+    for (int s = 0; s < kNvPairBStages; ++s) {
+      mbar_init(smem_u32(bready + s), 2 * kNvConvWarps);
+      mbar_init(smem_u32(bempty + s), 1);
+    }
+    mbar_init(smem_u32(acc_full), 1);
+    mbar_init(smem_u32(acc_empty), 2 * 4);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmap_x);
+    prefetch_tmap(&tmap_x64);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), kNvTmemCols);
+    tmem_relinquish_pair();
+  }
+  // run table: each block's expert staged in the load ring, then runs and their pass counts
+  const int msum = *a.m_sum;
+  const int nrb = min((msum + BN - 1) / BN, kNvPairMaxBlocks);
+  int* eb = reinterpret_cast<int*>(lring);
+  for (int b = threadIdx.x; b < nrb; b += blockDim.x) eb[b] = __ldg(a.expert_ids + static_cast<size_t>(b) * BN);
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the ring's next writers are copies
+  __syncthreads();
+  if (warp == 0) {
+    int ns = 0, ne = 0;
+    for (int b0 = 0; b0 < nrb; b0 += 32) {
+      const int b = b0 + lane;
+      const int e = b < nrb ? eb[b] : -1;
+      const int ep = (b > 0 && b < nrb) ? eb[b - 1] : -1;
+      const int en = b + 1 < nrb ? eb[b + 1] : -1;
+      const uint32_t fs = __ballot_sync(0xffffffffu, e >= 0 && e != ep);
+      const uint32_t fe = __ballot_sync(0xffffffffu, e >= 0 && e != en);
+      const uint32_t lt = (1u << lane) - 1u;
+      if (e >= 0 && e != ep) {
+        const int i = ns + __popc(fs & lt);
+        if (i < kNvMaxRuns) R.start[i] = static_cast<uint16_t>(b);
+      }
+      if (e >= 0 && e != en) {
+        const int i = ne + __popc(fe & lt);
+        if (i < kNvMaxRuns) R.len[i] = static_cast<uint16_t>(b + 1);   // end, turned into a length below
+      }
+      ns += __popc(fs);
+      ne += __popc(fe);
+    }
+    if (ns > kNvMaxRuns) {
+      if (lane == 0) record_error(a.status, kDevErrCheck);
+      ns = 0;   // no passes: every role ends at once
+    }
+    int base = 0;
+    for (int i0 = 0; i0 < ns; i0 += 32) {
+      const int i = i0 + lane;
+      int np = 0;
+      if (i < ns) {
+        const int l = static_cast<int>(R.len[i]) - static_cast<int>(R.start[i]);
+        R.len[i] = static_cast<uint16_t>(l);
+        np = (l + 3) / 4;
+      }
+      int incl = np;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += v;
+      }
+      if (i < ns) R.pfx[i] = base + incl - np;
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      R.pfx[ns] = base;
+      R.pfx[kNvMaxRuns + 1] = ns;   // run count for the other roles
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any cross-CTA arrival
+  tc_fence_after();
+  R.n = R.pfx[kNvMaxRuns + 1];
+  const uint32_t tmem = *tmem_slot;
+  const NvPhase& F = a.ph[kPh];
+  const int n_items = R.pfx[R.n] * F.n_wt;
+
+  if (warp == 0) {
+    // ---------------- producer: own token rows by TMA, own half of the packed chunk ----------------
+    const uint64_t pol_x = policy_evict_last();
+    int ls = 0;
+    uint32_t lph = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); t += nclusters) {
+      const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
+      const int k0 = pair_slot(P, 0), k1 = pair_slot(P, 1);
+      const uint32_t tx = (k0 == 2 ? 128 : 64) * 128 + (k1 == 2 ? 128 * 128 : k1 == 1 ? 64 * 128 : 0);
+      const int wt = t % F.n_wt;
+      const size_t chunk0 = (static_cast<size_t>(P.e) * F.n_wt + wt) * F.n_slabs;
+      for (int s = 0; s < F.n_slabs; ++s) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status));
+        if (!ok) break;
+        if (lane == 0) {
+          uint8_t* st = lring + ls * kNvPairLoadStage;
+          const uint32_t fb = smem_u32(full + ls);
+          const size_t wbase = (chunk0 + s) * kNvChunk;
+          if (wbase + kNvChunk > F.w_bytes || (reinterpret_cast<uintptr_t>(F.w) & 15)) {
+            record_error(a.status, kDevErrCheck);
+            *abort_flag = 1;
+          } else {
+            mbar_arrive_expect_tx(fb, tx + kNvHalfChunk);
+            for (int j = 0; j < 2; ++j) {
+              const int k = j ? k1 : k0;
+              if (k == 2)
+                tma_load_2d(smem_u32(st + j * kNvABytes), &tmap_x, s * kNvSlab, (P.b0 + 2 * j + rank) * BN, fb,
+                            pol_x);
+              else if (k == 1)
+                tma_load_2d(smem_u32(st + j * kNvABytes), &tmap_x64, s * kNvSlab, (P.b0 + 2 * j) * BN + rank * 64,
+                            fb, pol_x);
+            }
+            uint8_t* hp = st + 2 * kNvABytes;
+            bulk_load(smem_u32(hp), F.w + wbase + rank * (kNvHalfRows * 16), kNvHalfRows * 16, fb);
+            bulk_load(smem_u32(hp + kNvHalfRows * 16), F.w + wbase + kNvTile * 16 + rank * (kNvHalfRows * 16),
+                      kNvHalfRows * 16, fb);
+            bulk_load(smem_u32(hp + kNvHalfRows * 32), F.w + wbase + kNvTile * 32 + rank * (kNvHalfRows * 4),
+                      kNvHalfRows * 4, fb);
+          }
+        }
+        __syncwarp();
+        if (++ls == kNvPairLoadStages) {
+          ls = 0;
+          lph ^= 1;
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+      // let every copy issued into shared memory land before the CTA exits
+      for (int s = 0; s < kNvPairLoadStages; ++s)
+        mbar_wait(smem_u32(full + s), (s < ls) ? lph : (lph ^ 1), nullptr);
+    } else {
+      // every slot released: the pair MMA's commits into this CTA's barriers have all landed
+      for (int s = 0; s < kNvPairLoadStages; ++s) {
+        mbar_wait(smem_u32(lempty + ls), lph ^ 1, a.status);
+        if (++ls == kNvPairLoadStages) {
+          ls = 0;
+          lph ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 0) {
+      // ---------------- MMA issuer: kind::f16 over the pair, M=256, N=256, K=16 x 4 per slab ----------------
+      int ls = 0, bs = 0;
+      uint32_t lph = 0, bph = 0, acc_phase = 0;
+      const uint32_t id2 = idesc_bf16(2 * BN, kNvTile), id1 = idesc_bf16(BN, kNvTile);
+      bool ok = true;
+      for (int t = cluster; ok && t < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); t += nclusters) {
+        const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
+        const int nacc = P.c > 2 ? 2 : 1;
+        const uint32_t ids[2] = {pair_slot(P, 0) == 2 ? id2 : id1, pair_slot(P, 1) == 2 ? id2 : id1};
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+        if (!ok) break;
+        tc_fence_after();
+        for (int s = 0; s < F.n_slabs; ++s) {
+          // the converters of both CTAs arrive only after their CTA's load slot is full
+          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bready + bs), bph, a.status));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t sa = smem_u32(lring + ls * kNvPairLoadStage);
+            const uint32_t sb = smem_u32(bring + bs * kNvPairBStage);
+            for (int j = 0; j < nacc; ++j)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_pair(tmem + static_cast<uint32_t>(j * kNvTile), desc_sw128(sa + j * kNvABytes + k * 32),
+                              desc_sw128(sb + k * 32), ids[j], (s > 0 || k > 0) ? 1u : 0u);
+            tc_commit_pair(smem_u32(lempty + ls), 0x3);
+            tc_commit_pair(smem_u32(bempty + bs), 0x3);
+          }
+          __syncwarp();
+          if (++ls == kNvPairLoadStages) {
+            ls = 0;
+            lph ^= 1;
+          }
+          if (++bs == kNvPairBStages) {
+            bs = 0;
+            bph ^= 1;
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit_pair(smem_u32(acc_full), 0x3);
+        __syncwarp();
+        acc_phase ^= 1;
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else if (warp < 2 + static_cast<int>(kNvConvWarps)) {
+    // ---------------- converters: half a weight row each (128 rows x 2 parts) ----------------
+    const int ctid = threadIdx.x - 64;
+    const int n = ctid & (kNvHalfRows - 1), h = ctid / kNvHalfRows;
+    const uint32_t peer_bready = mapa_shared(smem_u32(bready), 0);
+    int ls = 0, bs = 0;
+    uint32_t lph = 0, bph = 0;
+    bool ok = true;
+    for (int t = cluster; ok && t < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); t += nclusters) {
+      for (int s = 0; s < F.n_slabs; ++s) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
+                                         mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
+        if (!ok) break;
+        convert_half_row(lring + ls * kNvPairLoadStage + 2 * kNvABytes, bring + bs * kNvPairBStage, n, h);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(peer_bready + static_cast<uint32_t>(bs * 8));
+        if (++ls == kNvPairLoadStages) {
+          ls = 0;
+          lph ^= 1;
+        }
+        if (++bs == kNvPairBStages) {
+          bs = 0;
+          bph ^= 1;
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+    if (ok && *abort_flag == 0) {
+      // every bf16 slot released (the pair MMA's commits into this CTA have landed)
+      for (int s = 0; s < kNvPairBStages; ++s) {
+        mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status);
+        if (++bs == kNvPairBStages) {
+          bs = 0;
+          bph ^= 1;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 10..13): thread = token row m of this CTA's blocks ----------------
+    const int q = warp & 3;
+    const int m = q * 32 + lane;
+    const uint32_t peer_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int t = cluster; t < n_items; t += nclusters) {
+      const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
+      const int wt = t % F.n_wt;
+      ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+      ok = named_barrier_and(1, 128, ok);
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const float ts = __ldg(F.tscale + P.e);
+      for (int j = 0; j < 2; ++j) {
+        const int k = pair_slot(P, j);
+        if (k == 0) continue;
+        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNvTile);
+        if (k == 2) {
+          // M = 256: this CTA's block, row m in lane m
+          const int row = (P.b0 + 2 * j + static_cast<int>(rank)) * BN + m;
+          const int row_e = row < msum ? __ldg(a.expert_ids + row) : -1;
+          nv_drain<BN>(a, F, kPh, acc, row, row_e == P.e, wt, ts, true);
+        } else {
+          // M = 128: rows rank * 64 + (m & 63) of the block, output columns 128 * (m >> 6) + ...
+          const int rl = m & 63;
+          const int row = (P.b0 + 2 * j) * BN + static_cast<int>(rank) * 64 + rl;
+          const int row_e = row < msum ? __ldg(a.expert_ids + row) : -1;
+          nv_drain_split<BN>(a, F, kPh, acc, row, row_e == P.e, m >> 6, rl, wt, ts, xa);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(peer_acc_empty);
+      acc_phase ^= 1;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  tc_fence_before();
+  cluster_sync();   // no CTA leaves while the pair MMA or the other CTA's arrivals may touch it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, kNvTmemCols);
   }
 }
 
@@ -498,7 +1010,8 @@ __global__ void __launch_bounds__(256) act_to_bf16_kernel(const uint8_t* __restr
 }
 
 // NVFP4 packing: per (expert, 256-row tile, 64-deep slab) 256 rows x 32 bytes of codes followed by
-// 256 rows x 4 E4M3 scales (one per 16 codes); tiles formed as in pack_mx_weights_kernel.
+// 256 rows x 4 E4M3 scales (one per 16 codes).  A W2 tile is 256 consecutive rows; a W13 tile is
+// 128 gate channels and their up rows, in the order gate 0..63, up 0..63, gate 64..127, up 64..127.
 __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int E, int N,
                                        int Kd, int pair, uint8_t* __restrict__ out) {
   const int n_slabs = Kd / kNvSlab, n_wt = pair == 2 ? N / kNvTile : (N + kNvTile - 1) / kNvTile;
@@ -514,8 +1027,10 @@ __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint
     // codes: byte o = (half, row n, j) -> code byte 16 * half + j of row n's 32 (see kNvChunk)
     const int n = code ? (o % (kNvTile * 16)) / 16 : (o - kNvTile * 32) / 4;
     const int cb = code ? (o / (kNvTile * 16)) * 16 + o % 16 : 0;
-    const int h = n / 128, mm = n % 128;
-    const int r = pair == 2 ? h * (N / 2) + wt * 128 + mm : wt * 256 + n;
+    // W13 tile rows in quarters of 64: gate channels 128wt + 0..63, their up rows, gate 128wt + 64..127,
+    // their up rows (a channel's gate and up products sit 64 accumulator columns apart)
+    const int qd = n / 64;
+    const int r = pair == 2 ? (qd & 1) * (N / 2) + wt * 128 + 64 * (qd >> 1) + (n & 63) : wt * 256 + n;
     if (code)
       out[i] = r < N ? q[(static_cast<size_t>(e) * N + r) * (Kd / 2) + s * 32 + cb] : 0;
     else
@@ -564,6 +1079,54 @@ static void fill_phase(const NvLaunch& L, bool l1, int nitems_per_wt, NvPhase& F
   F.n_tiles = nitems_per_wt * F.n_wt;
 }
 
+// The CTA-pair kernel in clusters of two: as many clusters as can be resident at once (0 when
+// the device cannot host one, then the caller runs the single-CTA kernel).
+template <int MODE>
+static int nv_pair_clusters() {
+  static int n = -1;
+  if (n < 0) {
+    int c = 0;
+    if (cudaFuncSetAttribute(moe_gemm_nv_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kNvPairSmem) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (num_sms() / 2));
+      cfg.blockDim = dim3(kNvThreads);
+      cfg.dynamicSmemBytes = kNvPairSmem;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&c, moe_gemm_nv_pair_kernel<MODE>, &cfg) != cudaSuccess) c = 0;
+    }
+    (void)cudaGetLastError();
+    n = c;
+  }
+  return n;
+}
+
+template <int MODE>
+static cudaError_t launch_nv_pair(const CUtensorMap& mx, const CUtensorMap& mx64, const NvArgs& a, int items,
+                                  int clusters, cudaStream_t stream) {
+  if (clusters > items) clusters = items;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(kNvThreads);
+  cfg.dynamicSmemBytes = kNvPairSmem;
+  cfg.stream = stream;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, moe_gemm_nv_pair_kernel<MODE>, mx, mx64, a);
+}
+
 // L1 (l1 non-null) or L2 (l2 non-null).
 template <int BN>
 static cudaError_t launch_nv_t(const NvLaunch* l1, const NvLaunch* l2, cudaStream_t stream) {
@@ -587,6 +1150,20 @@ static cudaError_t launch_nv_t(const NvLaunch* l1, const NvLaunch* l2, cudaStrea
   a.red = L.red;
   a.row_ids = L.row_ids;
   a.row_w = L.row_w;
+  if (BN == 128 && a.one_expert_blocks && L.E <= kNvMaxRuns && nrb <= kNvPairMaxBlocks) {
+    // 128-row blocks: CTA pairs over each expert's blocks, four at a time (the kernel counts the
+    // passes; nrb bounds them for the grid)
+    const int clusters = l1 ? nv_pair_clusters<1>() : nv_pair_clusters<2>();
+    if (clusters > 0) {
+      CUtensorMap mx64 = {};
+      if (!make_rows_map(&mx64, L.xb, L.Kd, L.U, 64)) return cudaErrorInvalidValue;
+      NvArgs b = a;
+      fill_phase(L, l1 != nullptr, nrb, b.ph[l1 ? 0 : 1]);
+      const int items = b.ph[l1 ? 0 : 1].n_tiles;
+      return l1 ? launch_nv_pair<1>(mx, mx64, b, items, clusters, stream)
+                : launch_nv_pair<2>(mx, mx64, b, items, clusters, stream);
+    }
+  }
   const int total = a.ph[l1 ? 0 : 1].n_tiles;
   int grid = num_sms();
   if (grid > total) grid = total;

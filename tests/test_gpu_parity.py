@@ -174,8 +174,13 @@ L1_CASES = [(8, 4, 16, 512, 256, 16), (37, 4, 16, 512, 256, 16), (200, 6, 32, 10
             (300, 2, 4, 256, 256, 128), (41, 3, 8, 640, 256, 32)]
 # "wide": every E4M3 activation code (zeros, subnormals, the top binade), activation scales 2^-120 .. 2^10,
 # MXFP4 block scales 2^-30 .. 2^4, NVFP4 scale codes 0x01 .. 0x7E
+# NVFP4 with 128-row blocks runs on CTA pairs over quads of blocks: experts with one, two and more
+# than four blocks (quads holding several experts, whole quads of one expert), padding-only blocks
+# (align 256) and a single partial quad
+PAIR_CASES = [(1200, 4, 8, 512, 256, 128), (600, 6, 16, 1024, 512, 256), (130, 1, 1, 256, 256, 128)]
 L1_PARAMS = ([c + ("mxfp4", False) for c in L1_CASES] + [c + ("nvfp4", False) for c in L1_CASES[:5]] +
-             [L1_CASES[i] + (f, True) for i in (1, 2, 4) for f in ("mxfp4", "nvfp4")])
+             [L1_CASES[i] + (f, True) for i in (1, 2, 4) for f in ("mxfp4", "nvfp4")] +
+             [c + ("nvfp4", False) for c in PAIR_CASES] + [PAIR_CASES[0] + ("nvfp4", True)])
 
 
 @pytest.mark.parametrize("T,K,E,H,I,align,fmt,wide", L1_PARAMS)
@@ -226,7 +231,8 @@ def test_l1_swiglu_parity(M, T, K, E, H, I, align, fmt, wide):
 L2_CASES = [(8, 4, 16, 512, 256, 16), (37, 4, 16, 512, 256, 16), (200, 6, 32, 1024, 512, 64), (64, 4, 8, 384, 512, 1),
             (300, 2, 4, 256, 256, 128)]
 L2_PARAMS = ([c + ("mxfp4", False) for c in L2_CASES] + [c + ("nvfp4", False) for c in L2_CASES] +
-             [L2_CASES[i] + (f, True) for i in (1, 2, 3) for f in ("mxfp4", "nvfp4")])
+             [L2_CASES[i] + (f, True) for i in (1, 2, 3) for f in ("mxfp4", "nvfp4")] +
+             [c + ("nvfp4", False) for c in PAIR_CASES] + [PAIR_CASES[1] + ("nvfp4", True)])
 
 
 @pytest.mark.parametrize("T,K,E,H,I,align,fmt,wide", L2_PARAMS)
@@ -548,7 +554,8 @@ def test_grouped_ffn_matches_separate_gemms(M, case):
 GATHER_CASES = [(8, 6, 32, 7168, 2048, 16, "mxfp4"), (37, 4, 16, 512, 256, 16, "mxfp4"),
                 (300, 2, 4, 256, 256, 128, "mxfp4"), (64, 4, 8, 512, 384, 1, "mxfp4"), (41, 3, 8, 640, 256, 32, "mxfp4"),
                 (600, 6, 16, 1024, 512, 256, "mxfp4"), (200, 6, 32, 1024, 512, 64, "nvfp4"),
-                (37, 4, 16, 512, 256, 16, "nvfp4"), (1, 1, 4, 256, 256, 16, "mxfp4")]
+                (37, 4, 16, 512, 256, 16, "nvfp4"), (1, 1, 4, 256, 256, 16, "mxfp4"),
+                (1200, 4, 8, 512, 256, 128, "nvfp4")]
 
 
 @pytest.mark.parametrize("T,K,E,H,I,align,fmt", GATHER_CASES)
