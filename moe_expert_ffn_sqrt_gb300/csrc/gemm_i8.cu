@@ -51,15 +51,21 @@ constexpr int kI8Extra = 1024;
 static_assert(kI8ConvThreads % 32 == 0 && 2 + kI8ConvThreads / 32 + 4 == kI8Threads / 32, "warp roles");
 
 // Shared-memory plan for row blocks of BN rows: load slots of [block 0 rows][block 1 rows][codes].
-template <int BN>
+// Block-quantised weights with blocks of up to 32 rows keep the running K-block sum in shared
+// memory ([BN rows][257 floats], conflict-free column walks), so that the two TMEM accumulators take
+// alternate K-blocks and each fold overlaps the next K-block's MMAs.
+template <int BN, bool BLOCK = false>
 struct I8Cfg {
   static constexpr int kABytes = BN * 128;
   static constexpr int kPOff = 2 * kABytes;
   static constexpr int kStage = (kPOff + kI8Chunk + 1023) / 1024 * 1024;
   static constexpr int kBStages = 2;
-  static constexpr int kFit = (kI8Budget - 1024 - kBStages * kI8BStage - kI8Extra) / kStage;
+  static constexpr bool kSumSmem = BLOCK && BN <= 32;
+  static constexpr int kSumStride = 257;
+  static constexpr int kSumBytes = kSumSmem ? (BN * kSumStride * 4 + 1023) / 1024 * 1024 : 0;
+  static constexpr int kFit = (kI8Budget - 1024 - kBStages * kI8BStage - kSumBytes - kI8Extra) / kStage;
   static constexpr int kStages = kFit > 8 ? 8 : kFit;
-  static constexpr int kSmem = 1024 + kStages * kStage + kBStages * kI8BStage + kI8Extra;
+  static constexpr int kSmem = 1024 + kStages * kStage + kBStages * kI8BStage + kSumBytes + kI8Extra;
   static_assert(kStages >= 2 && kSmem <= kI8Budget, "shared memory budget");
   static_assert(kABytes + 128 * 128 <= kStage, "the MMA's 128-row window of block 1 stays in its slot");
 };
@@ -149,19 +155,20 @@ __device__ __forceinline__ void convert_slab_i8(const uint8_t* __restrict__ code
 template <int BN, bool L1, bool BLOCK>
 __global__ void __launch_bounds__(kI8Threads, 1)
     moe_gemm_i8_kernel(const __grid_constant__ CUtensorMap tmap_x, const I8Args a) {
-  using C = I8Cfg<BN>;
+  using C = I8Cfg<BN, BLOCK>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* lring = smem;                                   // [kStages] token rows + int8 codes
   uint8_t* bring = smem + C::kStages * C::kStage;          // [kBStages] fp16 weight tiles
-  uint8_t* extra = bring + C::kBStages * kI8BStage;
+  float* ssum = reinterpret_cast<float*>(bring + C::kBStages * kI8BStage);   // running K-block sums
+  uint8_t* extra = bring + C::kBStages * kI8BStage + C::kSumBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(extra);     // load slot filled (TMA)
   uint64_t* lempty = full + C::kStages;                    // load slot consumed (MMA commit)
   uint64_t* bready = lempty + C::kStages;                  // fp16 tile written (converters)
   uint64_t* bempty = bready + C::kBStages;                 // fp16 tile consumed (MMA commit)
-  uint64_t* acc_full = bempty + C::kBStages;
-  uint64_t* acc_empty = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_full = bempty + C::kBStages;               // [2]: accumulator 0 / 1 written
+  uint64_t* acc_empty = acc_full + 2;                      // [2]: accumulator 0 / 1 drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -174,8 +181,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
       mbar_init(smem_u32(bready + s), kI8ConvThreads);
       mbar_init(smem_u32(bempty + s), 1);
     }
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), 128);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_x);
@@ -236,7 +245,9 @@ __global__ void __launch_bounds__(kI8Threads, 1)
   } else if (warp == 1) {
     // ---------------- MMA issuer: kind::f16 (fp16 operands), M=128, N=256, K=16 x 4 per slab ----------------
     int ls = 0, bs = 0;
-    uint32_t lph = 0, bph = 0, acc_phase = 0;
+    uint32_t lph = 0, bph = 0;
+    uint32_t aph = 0;   // bit b: phase of accumulator b
+    int rnd = 0;   // accumulator rounds so far (alternating accumulators with kSumSmem)
     int t = blockIdx.x, p = 0, ep = -1;
     RowPass P;
     const uint32_t id = idesc_f16(128, kI8Tile);
@@ -245,7 +256,8 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     while (!__any_sync(0xffffffffu, *abort_flag != 0) && next_row_pass<BN>(a, msum, t, p, ep, P)) {
       bool ok = true;
       for (int s0 = 0; ok && s0 < a.n_slabs; s0 += slabs_per_round) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
+        const int buf = C::kSumSmem ? (rnd & 1) : 0;
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty + buf), ((aph >> buf) & 1u) ^ 1u, a.status));
         if (!ok) break;
         tc_fence_after();
         for (int s = s0; s < s0 + slabs_per_round; ++s) {
@@ -259,7 +271,7 @@ __global__ void __launch_bounds__(kI8Threads, 1)
             for (int j = 0; j < P.nb; ++j)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16(tmem + static_cast<uint32_t>(j * kI8Tile), desc_sw128(sa + j * C::kABytes + k * 32),
+                mma_bf16(tmem + static_cast<uint32_t>((buf + j) * kI8Tile), desc_sw128(sa + j * C::kABytes + k * 32),
                          desc_sw128(sb + k * 32), id, (s > s0 || k > 0) ? 1u : 0u);
             tc_commit(smem_u32(lempty + ls));
             tc_commit(smem_u32(bempty + bs));
@@ -275,9 +287,10 @@ __global__ void __launch_bounds__(kI8Threads, 1)
           }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit(smem_u32(acc_full));
+        if (lane == 0) tc_commit(smem_u32(acc_full + buf));
         __syncwarp();
-        acc_phase ^= 1;
+        aph ^= 1u << buf;
+        ++rnd;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -320,10 +333,117 @@ __global__ void __launch_bounds__(kI8Threads, 1)
     const int m = q * 32 + lane;
     const bool warp_has_rows = q * 32 < BN;   // warp-uniform
     uint32_t acc_phase = 0;
+    uint32_t aph = 0;   // bit b: phase of accumulator b
+    int rnd = 0;
     int t = blockIdx.x, p = 0, ep = -1;
     RowPass P;
     while (next_row_pass<BN>(a, msum, t, p, ep, P)) {
       const int wt = t % a.n_wt;
+      if (C::kSumSmem) {
+        // K-blocks alternate between the two accumulators; thread m folds its row into its row of the
+        // shared-memory sum (same fma order as the tensor-memory sum), the last K-block's fold feeding
+        // the SwiGLU or the bf16 output.  Each accumulator is released once read.
+        const uint32_t lq = static_cast<uint32_t>(q * 32) << 16;
+        const int row = P.rb * BN + m;
+        const bool act = m < BN;
+        const bool mine = act && row < msum && __ldg(a.expert_ids + row) == P.e;
+        const int nbw = (a.w_rows + 255) / 256;
+        const float* wsa = a.col_scale + (static_cast<size_t>(P.e) * nbw + (L1 ? (wt * 128) / 256 : wt)) * a.nkb;
+        const float* wsb = a.col_scale + (static_cast<size_t>(P.e) * nbw + (L1 ? (a.out_cols + wt * 128) / 256 : wt)) * a.nkb;
+        const float* rsp = a.row_scale + static_cast<size_t>(mine ? row : 0) * a.nkb;
+        float* srow = ssum + (act ? m : 0) * C::kSumStride;
+        const int ncols = L1 ? 128 : min(kI8Tile, a.out_cols - wt * kI8Tile);
+        bool okb = true;
+        for (int kb = 0; kb < a.nkb; ++kb) {
+          const int buf = rnd & 1;
+          okb = mbar_wait(smem_u32(acc_full + buf), (aph >> buf) & 1u, a.status) && *abort_flag == 0;
+          okb = named_barrier_and(1, 128, okb);
+          if (!okb) break;
+          tc_fence_after();
+          const uint32_t acc = tmem + lq + static_cast<uint32_t>(buf * kI8Tile);
+          const bool last = kb == a.nkb - 1;
+          const float rs = mine ? __ldg(rsp + kb) : 0.f;
+          const float fa = rs * __ldg(wsa + kb), fb = rs * __ldg(wsb + kb);
+          if (warp_has_rows) {
+            // four tensor-memory loads in flight per wait (one warp holds all the rows of a small block)
+            if (L1) {
+              uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * a.out_cols + wt * 128);
+#pragma unroll 1
+              for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t g[2][16], u[2][16];
+                tc_ld_x16(acc + c0, g[0]);
+                tc_ld_x16(acc + c0 + 16, g[1]);
+                tc_ld_x16(acc + 128 + c0, u[0]);
+                tc_ld_x16(acc + 128 + c0 + 16, u[1]);
+                tc_wait_ld();
+                if (act) {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) {
+                    const float sg = fmaf(__uint_as_float(g[i >> 4][i & 15]), fa, kb > 0 ? srow[c0 + i] : 0.f);
+                    const float su = fmaf(__uint_as_float(u[i >> 4][i & 15]), fb, kb > 0 ? srow[128 + c0 + i] : 0.f);
+                    if (!last) {
+                      srow[c0 + i] = sg;
+                      srow[128 + c0 + i] = su;
+                    } else {
+                      g[i >> 4][i & 15] = __float_as_uint(silu_mul_i8(sg, su));
+                    }
+                  }
+                  if (last && mine) {
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                      packed[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(g[i >> 3][(2 * i) & 15]))) |
+                                  (static_cast<uint32_t>(__bfloat16_as_ushort(
+                                       __float2bfloat16_rn(__uint_as_float(g[i >> 3][(2 * i + 1) & 15])))) << 16);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                      dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                  }
+                }
+              }
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(a.out + static_cast<size_t>(row) * a.out_cols + wt * kI8Tile);
+#pragma unroll 1
+              for (int c0 = 0; c0 < kI8Tile; c0 += 64) {
+                uint32_t v[4][16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tc_ld_x16(acc + c0 + 16 * k, v[k]);
+                tc_wait_ld();
+                if (act) {
+#pragma unroll
+                  for (int i = 0; i < 64; ++i) {
+                    const float sv = fmaf(__uint_as_float(v[i >> 4][i & 15]), fa, kb > 0 ? srow[c0 + i] : 0.f);
+                    if (!last) srow[c0 + i] = sv;
+                    else v[i >> 4][i & 15] = __float_as_uint(sv);
+                  }
+                  if (last && mine && c0 < ncols) {
+                    uint32_t packed[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                      packed[i] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i) & 15]))) |
+                                  (static_cast<uint32_t>(__bfloat16_as_ushort(
+                                       __float2bfloat16_rn(__uint_as_float(v[i >> 3][(2 * i + 1) & 15])))) << 16);
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                      dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                  }
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(acc_empty + buf));
+          aph ^= 1u << buf;
+          ++rnd;
+          if (!L1 && last && a.red.out)
+            fused_reduce_tail(a.red, a.out, a.out_cols, mine, row, wt, a.n_wt, wt * kI8Tile, ncols);
+        }
+        if (!okb) {
+          *abort_flag = 1;
+          break;
+        }
+        continue;
+      }
       if (BLOCK) {
         // one pass = one row block; fold each K-block into the running sum, finish on the last
         const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16);
@@ -666,10 +786,11 @@ cudaError_t launch_i8_t(const I8Launch& L, cudaStream_t stream) {
   int grid = num_sms();
   if (grid > a.n_tiles) grid = a.n_tiles;
   if (grid < 1) grid = 1;
+  constexpr int kSmem = I8Cfg<BN, BLOCK>::kSmem;
   cudaError_t err = cudaFuncSetAttribute(moe_gemm_i8_kernel<BN, L1, BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         I8Cfg<BN>::kSmem);
+                                         kSmem);
   if (err != cudaSuccess) return err;
-  moe_gemm_i8_kernel<BN, L1, BLOCK><<<grid, kI8Threads, I8Cfg<BN>::kSmem, stream>>>(mx, a);
+  moe_gemm_i8_kernel<BN, L1, BLOCK><<<grid, kI8Threads, kSmem, stream>>>(mx, a);
   return cudaGetLastError();
 }
 
