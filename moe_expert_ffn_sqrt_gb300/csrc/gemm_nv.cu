@@ -487,6 +487,9 @@ constexpr int kNvPairLoadStage = (2 * kNvABytes + kNvHalfChunk + 1023) / 1024 * 
 constexpr int kNvPairLoadStages = 4;
 constexpr int kNvPairBStage = kNvHalfRows * 128;                                        // 16 KB
 constexpr int kNvPairBStages = 4;
+// The load slot and the bf16 slot of a slab advance together, so one barrier (the load slot's
+// "empty") releases both: one MMA commit per slab.
+static_assert(kNvPairBStages == kNvPairLoadStages, "load and bf16 slots advance together");
 constexpr int kNvMaxRuns = 1024;                                        // experts with rows
 constexpr int kNvRunBytes = kNvMaxRuns * 2 * 2 + (kNvMaxRuns + 2) * 4;   // run table
 constexpr int kNvPairSmem =
@@ -671,9 +674,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   uint8_t* bring = smem + kNvPairLoadStages * kNvPairLoadStage;   // bf16 half tiles
   uint8_t* extra = bring + kNvPairBStages * kNvPairBStage;
   uint64_t* full = reinterpret_cast<uint64_t*>(extra);         // load slot filled (TMA + bulk copies)
-  uint64_t* lempty = full + kNvPairLoadStages;                 // load slot consumed (pair MMA commit)
+  uint64_t* lempty = full + kNvPairLoadStages;                 // load + bf16 slot consumed (pair MMA commit)
   uint64_t* bready = lempty + kNvPairLoadStages;               // even CTA: both halves written
-  uint64_t* bempty = bready + kNvPairBStages;                  // half tile consumed (pair MMA commit)
+  uint64_t* bempty = bready + kNvPairBStages;                  // unused (lempty releases both slots)
   uint64_t* acc_full = bempty + kNvPairBStages;
   uint64_t* acc_empty = acc_full + 1;                          // even CTA: both CTAs drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
@@ -838,49 +841,48 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   } else if (warp == 1) {
     if (rank == 0) {
       // ---------------- MMA issuer: kind::f16 over the pair, M=256, N=256, K=16 x 4 per slab ----------------
-      int ls = 0, bs = 0;
-      uint32_t lph = 0, bph = 0, acc_phase = 0;
-      const uint32_t id2 = idesc_bf16(2 * BN, kNvTile), id1 = idesc_bf16(BN, kNvTile);
-      bool ok = true;
-      for (int t = cluster; ok && t < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); t += nclusters) {
-        const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
-        const int nacc = P.c > 2 ? 2 : 1;
-        const uint32_t ids[2] = {pair_slot(P, 0) == 2 ? id2 : id1, pair_slot(P, 1) == 2 ? id2 : id1};
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
-        if (!ok) break;
-        tc_fence_after();
-        for (int s = 0; s < F.n_slabs; ++s) {
-          // the converters of both CTAs arrive only after their CTA's load slot is full
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bready + bs), bph, a.status));
+      // One thread: the issue of a pair MMA takes ~100 cycles of its 128 cycles of tensor work, so
+      // the loop between slabs is kept short (no warp votes, descriptors advanced by adding).
+      if (lane == 0) {
+        int ls = 0;
+        uint32_t lph = 0, acc_phase = 0;
+        const uint32_t id2 = idesc_bf16(2 * BN, kNvTile), id1 = idesc_bf16(BN, kNvTile);
+        const uint64_t da0 = desc_sw128(smem_u32(lring)), db0 = desc_sw128(smem_u32(bring));
+        bool ok = true;
+        for (int t = cluster; ok && t < n_items && *abort_flag == 0; t += nclusters) {
+          const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
+          const int nacc = P.c > 2 ? 2 : 1;
+          const uint32_t ids[2] = {pair_slot(P, 0) == 2 ? id2 : id1, pair_slot(P, 1) == 2 ? id2 : id1};
+          ok = mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status);
           if (!ok) break;
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t sa = smem_u32(lring + ls * kNvPairLoadStage);
-            const uint32_t sb = smem_u32(bring + bs * kNvPairBStage);
+          for (int s = 0; s < F.n_slabs; ++s) {
+            // the converters of both CTAs arrive only after their CTA's load slot is full
+            ok = mbar_wait(smem_u32(bready + ls), lph, a.status);
+            if (!ok) break;
+            tc_fence_after();
+            // descriptor start addresses count 16-byte units: + 2 per 32-byte K step
+            const uint64_t da = da0 + static_cast<uint64_t>(ls * (kNvPairLoadStage >> 4));
+            const uint64_t db = db0 + static_cast<uint64_t>(ls * (kNvPairBStage >> 4));
             for (int j = 0; j < nacc; ++j)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16_pair(tmem + static_cast<uint32_t>(j * kNvTile), desc_sw128(sa + j * kNvABytes + k * 32),
-                              desc_sw128(sb + k * 32), ids[j], (s > 0 || k > 0) ? 1u : 0u);
+                mma_bf16_pair(tmem + static_cast<uint32_t>(j * kNvTile),
+                              da + static_cast<uint64_t>(j * (kNvABytes >> 4) + 2 * k), db + static_cast<uint64_t>(2 * k),
+                              ids[j], (s > 0 || k > 0) ? 1u : 0u);
             tc_commit_pair(smem_u32(lempty + ls), 0x3);
-            tc_commit_pair(smem_u32(bempty + bs), 0x3);
+            if (++ls == kNvPairLoadStages) {
+              ls = 0;
+              lph ^= 1;
+            }
           }
-          __syncwarp();
-          if (++ls == kNvPairLoadStages) {
-            ls = 0;
-            lph ^= 1;
-          }
-          if (++bs == kNvPairBStages) {
-            bs = 0;
-            bph ^= 1;
-          }
+          if (!ok) break;
+          tc_commit_pair(smem_u32(acc_full), 0x3);
+          acc_phase ^= 1;
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit_pair(smem_u32(acc_full), 0x3);
-        __syncwarp();
-        acc_phase ^= 1;
+        if (!ok) *abort_flag = 1;
       }
-      if (!ok) *abort_flag = 1;
+      __syncwarp();
     }
   } else if (warp < 2 + static_cast<int>(kNvConvWarps)) {
     // ---------------- converters: half a weight row each (128 rows x 2 parts) ----------------
@@ -892,8 +894,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     bool ok = true;
     for (int t = cluster; ok && t < n_items && !__any_sync(0xffffffffu, *abort_flag != 0); t += nclusters) {
       for (int s = 0; s < F.n_slabs; ++s) {
+        // the bf16 slot bs == ls is free once the slab that last used it was consumed (lempty)
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + ls), lph, a.status) &&
-                                         mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status));
+                                         mbar_wait(smem_u32(lempty + bs), bph ^ 1, a.status));
         if (!ok) break;
         convert_half_row(lring + ls * kNvPairLoadStage + 2 * kNvABytes, bring + bs * kNvPairBStage, n, h);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -911,9 +914,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     }
     if (!ok) *abort_flag = 1;
     if (ok && *abort_flag == 0) {
-      // every bf16 slot released (the pair MMA's commits into this CTA have landed)
+      // every slot released (the pair MMA's commits into this CTA have landed)
       for (int s = 0; s < kNvPairBStages; ++s) {
-        mbar_wait(smem_u32(bempty + bs), bph ^ 1, a.status);
+        mbar_wait(smem_u32(lempty + bs), bph ^ 1, a.status);
         if (++bs == kNvPairBStages) {
           bs = 0;
           bph ^= 1;
