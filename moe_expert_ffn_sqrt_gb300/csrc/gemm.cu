@@ -404,63 +404,67 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < C::STAGES; ++s) mbar_wait(smem_u32(full + s), (s < stage) ? phase : (phase ^ 1), nullptr);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (whole warp iterates, lane 0 issues) ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t acc_phase = 0;
-    uint32_t islot = 0, iphase = 0;
-    while (true) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(item_full + islot), iphase, a.status));
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      const int4 item = items[islot];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(item_empty + islot));
-      if (++islot == kItemSlots) {
-        islot = 0;
-        iphase ^= 1;
-      }
-      if (item.x < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int n_slabs = a.ph[item.w >> 16].n_slabs;
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status));
-      if (ok) {
-        tc_fence_after();
-        for (int s = 0; s < n_slabs; ++s) {
-          ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(full + stage), phase, a.status));
-          if (!ok) break;
+    // ---------------- MMA issuer (one thread) ----------------
+    // The loop between slabs is kept short (no warp votes; descriptors advanced by addition): the
+    // MMA thread's time per slab must stay below the slab's arrival interval.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_phase = 0;
+      uint32_t islot = 0, iphase = 0;
+      const uint64_t dst0 = desc_sw128(smem_u32(stages));
+      const uint32_t id0 = idesc_mxf8f6f4(0, 5, 128, kTileRows, 0, 0);
+      while (true) {
+        bool ok = mbar_wait(smem_u32(item_full + islot), iphase, a.status);
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        const int4 item = items[islot];
+        mbar_arrive(smem_u32(item_empty + islot));
+        if (++islot == kItemSlots) {
+          islot = 0;
+          iphase ^= 1;
+        }
+        if (item.x < 0 || *abort_flag != 0) break;
+        const int n_slabs = a.ph[item.w >> 16].n_slabs;
+        ok = mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status);
+        if (ok) {
           tc_fence_after();
-          if (lane == 0) {
+          for (int s = 0; s < n_slabs; ++s) {
+            ok = mbar_wait(smem_u32(full + stage), phase, a.status);
+            if (!ok) break;
+            tc_fence_after();
             const uint32_t st = smem_u32(stages + stage * C::STAGE);
             const uint32_t sfa = tmem + kSfaCol + ((s >> 2) & 1) * 16;
             const uint32_t sfb = tmem + kSfbCol + (s & 1) * 16;
             if ((s & 3) == 0) tc_cp_32x128b_x4(sfa, smem_desc(st + C::SFA_OFF, 0, 128, 0));
             tc_cp_32x128b_x4(sfb, smem_desc(st + C::SFB_OFF, 0, 128, 0));
             tc_cp_32x128b_x4(sfb + 4, smem_desc(st + C::SFB_OFF + 512, 0, 128, 0));
+            // descriptor start addresses count 16-byte units: + 2 per 32-byte K step
+            const uint64_t da = dst0 + static_cast<uint64_t>(stage * (C::STAGE >> 4));
+            const uint64_t dw = da + static_cast<uint64_t>(C::W_OFF >> 4);
+            const uint32_t ids = id0 | (static_cast<uint32_t>(s & 3) << 29);   // scale-factor id of A
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t id = idesc_mxf8f6f4(0, 5, 128, kTileRows, s & 3, k);
-              mma_mxf8f6f4(tmem, desc_sw128(st + k * 32), desc_sw128(st + C::W_OFF + k * 32), id, sfa, sfb,
+            for (int k = 0; k < 4; ++k)
+              mma_mxf8f6f4(tmem, da + 2 * k, dw + 2 * k, ids | (static_cast<uint32_t>(k) << 4), sfa, sfb,
                            (s > 0 || k > 0) ? 1u : 0u);
-            }
             tc_commit(smem_u32(empty + stage));
-          }
-          __syncwarp();
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1;
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
+        if (!ok) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_commit(smem_u32(acc_full));
+        acc_phase ^= 1;
       }
-      if (!ok) {
-        *abort_flag = 1;
-        break;
-      }
-      if (lane == 0) tc_commit(smem_u32(acc_full));
-      __syncwarp();
-      acc_phase ^= 1;
     }
+    __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..9): thread = token row m of the block, one column half --------
     // Warps 2..5 take the first half of the accumulator's columns and warps 6..9 the second, so each
