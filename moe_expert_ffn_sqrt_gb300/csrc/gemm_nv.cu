@@ -163,6 +163,9 @@ __device__ __forceinline__ void convert_row(const uint8_t* __restrict__ packed, 
 template <int BN>
 __device__ __forceinline__ void nv_drain(const NvArgs& a, const NvPhase& F, int ph, uint32_t acc, int row,
                                          bool mine, int wt, float ts, bool warp_has_rows) {
+  // 32-byte stores when the output base allows (row strides are multiples of 32 bytes)
+  const bool v8 = ((reinterpret_cast<uintptr_t>(ph == 0 ? static_cast<const void*>(a.h_q) : static_cast<const void*>(a.y)) &
+                    31) == 0);
   if (ph == 0) {
     const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
     // pass 1: h over the 128 channels, written back over the gate columns of the accumulator,
@@ -214,8 +217,13 @@ __device__ __forceinline__ void nv_drain(const NvArgs& a, const NvPhase& F, int 
           packed[i] = lo | (hi << 16);
         }
         if (mine) {
-          dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          if (v8)   // 32 codes as one whole-sector store
+            st_global_v8(dst + c0 / 16, packed[0], packed[1], packed[2], packed[3], packed[4], packed[5], packed[6],
+                         packed[7]);
+          else {
+            dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          }
         }
       }
       if (mine) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
@@ -239,9 +247,16 @@ __device__ __forceinline__ void nv_drain(const NvArgs& a, const NvPhase& F, int 
           packed[i] = lo | (hi << 16);
         }
         if (mine && c0 < ncols) {
+          if (v8) {   // whole-sector stores
+            st_global_v8(dst + c0 / 8, packed[0], packed[1], packed[2], packed[3], packed[4], packed[5], packed[6],
+                         packed[7]);
+            st_global_v8(dst + c0 / 8 + 2, packed[8], packed[9], packed[10], packed[11], packed[12], packed[13],
+                         packed[14], packed[15]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            for (int c = 0; c < 4; ++c)
+              dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          }
         }
       }
     }
@@ -570,6 +585,8 @@ __device__ __forceinline__ void convert_half_row(const uint8_t* __restrict__ pac
 template <int BN>
 __device__ __forceinline__ void nv_drain_split(const NvArgs& a, const NvPhase& F, int ph, uint32_t acc, int row,
                                                bool mine, int half, int rl, int wt, float ts, float* xa) {
+  const bool v8 = ((reinterpret_cast<uintptr_t>(ph == 0 ? static_cast<const void*>(a.h_q) : static_cast<const void*>(a.y)) &
+                    31) == 0);
   if (ph == 0) {
     const float wr = (a.row_w != nullptr && mine) ? __ldg(a.row_w + __ldg(a.row_ids + row)) : 1.f;
     float amax = 0.f;
@@ -622,8 +639,13 @@ __device__ __forceinline__ void nv_drain_split(const NvArgs& a, const NvPhase& F
         packed[i] = lo | (hi << 16);
       }
       if (mine) {
-        dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        if (v8)
+          st_global_v8(dst + c0 / 16, packed[0], packed[1], packed[2], packed[3], packed[4], packed[5], packed[6],
+                       packed[7]);
+        else {
+          dst[c0 / 16] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          dst[c0 / 16 + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
       }
     }
     if (mine && !half) a.h_sf[act_sf_offset(BN, a.sf_nb, row, wt)] = static_cast<uint8_t>(ex + 127);
@@ -647,9 +669,16 @@ __device__ __forceinline__ void nv_drain_split(const NvArgs& a, const NvPhase& F
           packed[i] = lo | (hi << 16);
         }
         if (mine && c0 < ncols) {
+          if (v8) {   // whole-sector stores
+            st_global_v8(dst + c0 / 8, packed[0], packed[1], packed[2], packed[3], packed[4], packed[5], packed[6],
+                         packed[7]);
+            st_global_v8(dst + c0 / 8 + 2, packed[8], packed[9], packed[10], packed[11], packed[12], packed[13],
+                         packed[14], packed[15]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            for (int c = 0; c < 4; ++c)
+              dst[c0 / 8 + c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+          }
         }
       }
     }
