@@ -429,6 +429,21 @@ def test_forward_decode_full(M):
     assert rel < OUT_TOL
 
 
+@pytest.mark.parametrize("T,E,K", [(20, 8, 4), (32, 4, 4), (9, 2, 1)])
+def test_forward_nvfp4_pair_fused_reduce(M, T, E, K):
+    # NVFP4 with 128-row blocks runs on CTA pairs; up to 32 tokens every expert holds one block (a
+    # lone block, split by rows over the pair as an M = 128 MMA) and the weighted reduce runs in
+    # the L2 epilogue, after both halves of each row are stored
+    w = synth.custom(T=T, H=512, I=256, E=E, K=K, align=128, score_fn="sqrt_softplus", e_bias=True, fmt="nvfp4",
+                     seed=60 + T)
+    _check_forward(M, w)
+    inp = synth.layer_inputs(w)
+    stack = synth.all_expert_weights(w)
+    a = _run_forward(M, w, inp, stack)["out"]
+    b = _run_stages(M, w, inp, stack)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 def test_forward_tiny_nvfp4(M):
     w = synth.custom(T=40, H=512, I=256, E=16, K=4, align=16, score_fn="sqrt_softplus", e_bias=True, fmt="nvfp4",
                      gate_offset="zipf", seed=9)
