@@ -351,6 +351,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
+      if (!gather) {
+        // one thread issues the item's slabs; the self-check of the copy ranges is done per item
+        // (the slab loop is the producer's critical path at small batches: the copies' issue cost)
+        if (lane == 0 && ok) {
+          const size_t wend = (chunk0 + P.n_slabs) * C::W_CHUNK;
+          const size_t sfa_last = (static_cast<size_t>((P.n_slabs - 1) >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
+          const bool good = wend <= P.w_bytes && sfa_last + C::SFA_BYTES <= P.x_sf_bytes &&
+                            ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0;
+          if (!good) {
+            record_error(a.status, kDevErrCheck);
+            *abort_flag = 1;
+            ok = false;
+          }
+          const uint32_t stages0 = smem_u32(stages);
+          const uint8_t* wsrc = P.w + chunk0 * C::W_CHUNK;
+          int wrow = static_cast<int>(chunk0 * C::W_CHUNK / 64);
+          for (int s = 0; ok && s < P.n_slabs; ++s) {
+            ok = mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status);
+            if (!ok) break;
+            const uint32_t st = stages0 + static_cast<uint32_t>(stage * C::STAGE);
+            const uint32_t fb = smem_u32(full + stage);
+            const bool sf4 = (s & 3) == 0;
+            mbar_arrive_expect_tx(fb, C::TX_W + 1024 + C::X_BYTES + (sf4 ? C::SFA_BYTES : 0));
+            tma_load_2d(st + C::W_OFF, mw, 0, wrow, fb, pol_w);
+            bulk_load(st + C::SFB_OFF, wsrc + C::TX_W, 1024, fb);
+            tma_load_2d(st, mx, s * 128, r0, fb, pol_x);
+            if (sf4)
+              bulk_load(st + C::SFA_OFF, P.x_sf + (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN),
+                        C::SFA_BYTES, fb);
+            wsrc += C::W_CHUNK;
+            wrow += static_cast<int>(C::W_CHUNK / 64);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
+        // lane 0's ring position and status for the whole warp
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        stage = __shfl_sync(0xffffffffu, stage, 0);
+        phase = __shfl_sync(0xffffffffu, phase, 0);
+        continue;
+      }
       for (int s = 0; ok && s < P.n_slabs; ++s) {
         ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status));
         if (!ok) break;
