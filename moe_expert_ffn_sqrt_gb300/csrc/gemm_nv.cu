@@ -706,9 +706,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
   uint64_t* lempty = full + kNvPairLoadStages;                 // load + bf16 slot consumed (pair MMA commit)
   uint64_t* bready = lempty + kNvPairLoadStages;               // even CTA: both halves written
   uint64_t* bempty = bready + kNvPairBStages;                  // unused (lempty releases both slots)
-  uint64_t* acc_full = bempty + kNvPairBStages;
-  uint64_t* acc_empty = acc_full + 1;                          // even CTA: both CTAs drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_full = bempty + kNvPairBStages;                // [2] accumulator b written
+  uint64_t* acc_empty = acc_full + 2;                          // [2] even CTA: both CTAs drained b
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* xa = reinterpret_cast<float*>(extra + 256);          // [64] row amax of split slots (L1)
   RunTable R;
@@ -729,8 +729,10 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       mbar_init(smem_u32(bready + s), 2 * kNvConvWarps);
       mbar_init(smem_u32(bempty + s), 1);
     }
-    mbar_init(smem_u32(acc_full), 1);
-    mbar_init(smem_u32(acc_empty), 2 * 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(acc_full + b), 1);
+      mbar_init(smem_u32(acc_empty + b), 2 * 4);
+    }
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmap_x);
@@ -874,7 +876,11 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       // the loop between slabs is kept short (no warp votes, descriptors advanced by adding).
       if (lane == 0) {
         int ls = 0;
-        uint32_t lph = 0, acc_phase = 0;
+        uint32_t lph = 0;
+        // accumulators: a two-slot pass takes both; one-slot passes alternate between them, so that
+        // one pass's drain overlaps the next one's MMAs (bit b of aph: accumulator b's phase)
+        uint32_t aph = 0;
+        int nb = 0;
         const uint32_t id2 = idesc_bf16(2 * BN, kNvTile), id1 = idesc_bf16(BN, kNvTile);
         const uint64_t da0 = desc_sw128(smem_u32(lring)), db0 = desc_sw128(smem_u32(bring));
         bool ok = true;
@@ -882,7 +888,9 @@ __global__ void __launch_bounds__(kNvThreads, 1)
           const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
           const int nacc = P.c > 2 ? 2 : 1;
           const uint32_t ids[2] = {pair_slot(P, 0) == 2 ? id2 : id1, pair_slot(P, 1) == 2 ? id2 : id1};
-          ok = mbar_wait(smem_u32(acc_empty), acc_phase ^ 1, a.status);
+          const int b0 = nacc == 2 ? 0 : nb;   // accumulator of slot j: b0 + j
+          for (int j = 0; ok && j < nacc; ++j)
+            ok = mbar_wait(smem_u32(acc_empty + b0 + j), ((aph >> (b0 + j)) & 1u) ^ 1u, a.status);
           if (!ok) break;
           tc_fence_after();
           for (int s = 0; s < F.n_slabs; ++s) {
@@ -896,7 +904,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             for (int j = 0; j < nacc; ++j)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16_pair(tmem + static_cast<uint32_t>(j * kNvTile),
+                mma_bf16_pair(tmem + static_cast<uint32_t>((b0 + j) * kNvTile),
                               da + static_cast<uint64_t>(j * (kNvABytes >> 4) + 2 * k), db + static_cast<uint64_t>(2 * k),
                               ids[j], (s > 0 || k > 0) ? 1u : 0u);
             tc_commit_pair(smem_u32(lempty + ls), 0x3);
@@ -906,8 +914,11 @@ __global__ void __launch_bounds__(kNvThreads, 1)
             }
           }
           if (!ok) break;
-          tc_commit_pair(smem_u32(acc_full), 0x3);
-          acc_phase ^= 1;
+          for (int j = 0; j < nacc; ++j) {
+            tc_commit_pair(smem_u32(acc_full + b0 + j), 0x3);
+            aph ^= 1u << (b0 + j);
+          }
+          if (nacc == 1) nb ^= 1;
         }
         if (!ok) *abort_flag = 1;
       }
@@ -957,12 +968,16 @@ __global__ void __launch_bounds__(kNvThreads, 1)
     const int q = warp & 3;
     const int m = q * 32 + lane;
     const uint32_t peer_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
-    uint32_t acc_phase = 0;
+    uint32_t aph = 0;   // the MMA thread's accumulator choice, repeated
+    int nb = 0;
     bool ok = true;
     for (int t = cluster; t < n_items; t += nclusters) {
       const PairPass P = pair_pass(R, a.expert_ids, t / F.n_wt);
       const int wt = t % F.n_wt;
-      ok = mbar_wait(smem_u32(acc_full), acc_phase, a.status) && *abort_flag == 0;
+      const int nacc = P.c > 2 ? 2 : 1;
+      const int b0 = nacc == 2 ? 0 : nb;
+      ok = *abort_flag == 0;
+      for (int j = 0; ok && j < nacc; ++j) ok = mbar_wait(smem_u32(acc_full + b0 + j), (aph >> (b0 + j)) & 1u, a.status);
       ok = named_barrier_and(1, 128, ok);
       if (!ok) {
         *abort_flag = 1;
@@ -973,7 +988,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       for (int j = 0; j < 2; ++j) {
         const int k = pair_slot(P, j);
         if (k == 0) continue;
-        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(j * kNvTile);
+        const uint32_t acc = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>((b0 + j) * kNvTile);
         if (k == 2) {
           // M = 256: this CTA's block, row m in lane m
           const int row = (P.b0 + 2 * j + static_cast<int>(rank)) * BN + m;
@@ -989,8 +1004,11 @@ __global__ void __launch_bounds__(kNvThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(peer_acc_empty);
-      acc_phase ^= 1;
+      for (int j = 0; j < nacc; ++j) {
+        if (lane == 0) mbar_arrive_cluster(peer_acc_empty + static_cast<uint32_t>((b0 + j) * 8));
+        aph ^= 1u << (b0 + j);
+      }
+      if (nacc == 1) nb ^= 1;
     }
     if (!ok) *abort_flag = 1;
   }
