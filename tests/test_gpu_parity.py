@@ -177,7 +177,8 @@ L1_CASES = [(8, 4, 16, 512, 256, 16), (37, 4, 16, 512, 256, 16), (200, 6, 32, 10
 # NVFP4 with 128-row blocks runs on CTA pairs over quads of blocks: experts with one, two and more
 # than four blocks (quads holding several experts, whole quads of one expert), padding-only blocks
 # (align 256) and a single partial quad
-PAIR_CASES = [(1200, 4, 8, 512, 256, 128), (600, 6, 16, 1024, 512, 256), (130, 1, 1, 256, 256, 128)]
+PAIR_CASES = [(1200, 4, 8, 512, 256, 128), (600, 6, 16, 1024, 512, 256), (130, 1, 1, 256, 256, 128),
+              (700, 4, 8, 384, 256, 128)]   # H = 384: W2's last tile is half a tile (the odd CTA's rows zero)
 L1_PARAMS = ([c + ("mxfp4", False) for c in L1_CASES] + [c + ("nvfp4", False) for c in L1_CASES[:5]] +
              [L1_CASES[i] + (f, True) for i in (1, 2, 4) for f in ("mxfp4", "nvfp4")] +
              [c + ("nvfp4", False) for c in PAIR_CASES] + [PAIR_CASES[0] + ("nvfp4", True)])
@@ -429,12 +430,12 @@ def test_forward_decode_full(M):
     assert rel < OUT_TOL
 
 
-@pytest.mark.parametrize("T,E,K", [(20, 8, 4), (32, 4, 4), (9, 2, 1)])
-def test_forward_nvfp4_pair_fused_reduce(M, T, E, K):
+@pytest.mark.parametrize("T,E,K,H", [(20, 8, 4, 512), (32, 4, 4, 512), (9, 2, 1, 512), (24, 8, 4, 384)])
+def test_forward_nvfp4_pair_fused_reduce(M, T, E, K, H):
     # NVFP4 with 128-row blocks runs on CTA pairs; up to 32 tokens every expert holds one block (a
     # lone block, split by rows over the pair as an M = 128 MMA) and the weighted reduce runs in
     # the L2 epilogue, after both halves of each row are stored
-    w = synth.custom(T=T, H=512, I=256, E=E, K=K, align=128, score_fn="sqrt_softplus", e_bias=True, fmt="nvfp4",
+    w = synth.custom(T=T, H=H, I=256, E=E, K=K, align=128, score_fn="sqrt_softplus", e_bias=True, fmt="nvfp4",
                      seed=60 + T)
     _check_forward(M, w)
     inp = synth.layer_inputs(w)
