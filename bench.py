@@ -410,6 +410,9 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     barrier()
     for i in range(K):
         flush.fill_(i & 0xFF)
+        # a GPU-side spin (outside the events) keeps the host ahead, so that a slow or contended host
+        # cannot stretch the device time between the events; the end-to-end loop below has none
+        torch.cuda._sleep(2 * SPIN_CYCLES)
         ev[i][0].record()
         step()
         ev[i][1].record()
@@ -463,7 +466,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
         flush.fill_(i & 0xFF)
         # a GPU-side spin keeps the host ahead: every stage is enqueued before the GPU reaches it, so
         # the events around a stage measure its kernels, not the host's launch latency
-        torch.cuda._sleep(SPIN_CYCLES)
+        torch.cuda._sleep(4 * SPIN_CYCLES)
         e = sev[i]
         j = 0
         e[j].record()
