@@ -41,6 +41,7 @@ constexpr int kGemmThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2..9 e
 constexpr int kEpiThreads = 256;         // two warps per TMEM lane quarter, one per column half
 constexpr int kEpiThread0 = 64;          // first epilogue thread
 constexpr int kSmemBudget = 227 * 1024;
+constexpr int kGemmStaticSmem = 6 * 1024;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: accumulator [0, 256); token scales 2 slots x 16 at 256; weight scales 2 x 16 at 288.
 constexpr uint32_t kSfaCol = 256;
@@ -58,7 +59,8 @@ struct GemmCfg {
   static constexpr int SFA_BYTES = 512;
   static constexpr int STAGE = (SFA_OFF + SFA_BYTES + 1023) / 1024 * 1024;
   static constexpr int EXTRA = 1024;                             // barriers and flags
-  static constexpr int S_FIT = (kSmemBudget - EXTRA - 1024) / STAGE;
+  // dynamic + static shared memory (6 KB: the row-block prefix and the amax exchange) within the budget
+  static constexpr int S_FIT = (kSmemBudget - kGemmStaticSmem - EXTRA - 1024) / STAGE;
   static constexpr int STAGES = S_FIT > 8 ? 8 : S_FIT;
   static constexpr int SMEM = 1024 + STAGES * STAGE + EXTRA;
   static constexpr uint32_t TX_W = kTileRows * 64;               // global bytes of the FP4 box
@@ -839,10 +841,11 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
   if (err != cudaSuccess && pdl_ok) {
     (void)cudaGetLastError();
-    pdl_ok = false;
     cfg.numAttrs = n - 1;
     err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
+    if (err == cudaSuccess) pdl_ok = false;   // only the attribute was refused
   }
+  if (err != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for later calls
   return err;
 }
 
