@@ -37,7 +37,8 @@
 
 namespace moe {
 
-constexpr int kGemmThreads = 320;        // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kGemmThreads = 352;        // warps 0 and 10 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kProducer2Warp = 10;       // second copy-issuing warp (odd slabs)
 constexpr int kEpiThreads = 256;         // two warps per TMEM lane quarter, one per column half
 constexpr int kEpiThread0 = 64;          // first epilogue thread
 constexpr int kSmemBudget = 227 * 1024;
@@ -188,6 +189,52 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return __fdividef(
 
 constexpr int kItemSlots = 4;
 
+// One thread issues the copies of an item's slabs whose running slab index gslab has parity
+// `mine`: the two producer warps take alternate slabs, since a thread issues a bulk copy only
+// every ~300 cycles and one thread could not keep the ring full.  stage / phase / gslab advance
+// over every slab of the item (both producers see every item); a failed wait or range check stops
+// the loop and returns false.  The copy ranges are checked once per item.
+template <int BN>
+__device__ __forceinline__ bool issue_mx_slabs(const GemmArgs& a, const GemmPhase& P, const CUtensorMap* mw,
+                                               const CUtensorMap* mx, int r0, size_t chunk0, uint32_t mine,
+                                               uint8_t* stages, uint64_t* full, uint64_t* empty, int& stage,
+                                               uint32_t& phase, uint32_t& gslab, uint64_t pol_w, uint64_t pol_x) {
+  using C = GemmCfg<BN>;
+  const size_t wend = (chunk0 + P.n_slabs) * C::W_CHUNK;
+  const size_t sfa_last = (static_cast<size_t>((P.n_slabs - 1) >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
+  if (!(wend <= P.w_bytes && sfa_last + C::SFA_BYTES <= P.x_sf_bytes &&
+        ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0)) {
+    record_error(a.status, kDevErrCheck);
+    return false;
+  }
+  const uint32_t stages0 = smem_u32(stages);
+  const uint8_t* wsrc = P.w + chunk0 * C::W_CHUNK;
+  int wrow = static_cast<int>(chunk0 * C::W_CHUNK / 64);
+  for (int s = 0; s < P.n_slabs; ++s) {
+    if ((gslab & 1u) == mine) {
+      if (!mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status)) return false;
+      const uint32_t st = stages0 + static_cast<uint32_t>(stage * C::STAGE);
+      const uint32_t fb = smem_u32(full + stage);
+      const bool sf4 = (s & 3) == 0;
+      mbar_arrive_expect_tx(fb, C::TX_W + 1024 + C::X_BYTES + (sf4 ? C::SFA_BYTES : 0));
+      tma_load_2d(st + C::W_OFF, mw, 0, wrow, fb, pol_w);
+      bulk_load(st + C::SFB_OFF, wsrc + C::TX_W, 1024, fb);
+      tma_load_2d(st, mx, s * 128, r0, fb, pol_x);
+      if (sf4)
+        bulk_load(st + C::SFA_OFF, P.x_sf + (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN),
+                  C::SFA_BYTES, fb);
+    }
+    wsrc += C::W_CHUNK;
+    wrow += static_cast<int>(C::W_CHUNK / 64);
+    ++gslab;
+    if (++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  return true;
+}
+
 // Runs the L1 items, the L2 items, or both.  With both, an L2 item of row block rb reads h rows
 // written by other CTAs: its producer first waits until sched[rb] counts all n_wt L1 tiles of the
 // block (each L1 item's epilogue adds one after its stores).  Items are drawn in index order, all
@@ -213,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* item_full = acc_empty + 1;             // [kItemSlots], producer arrives
-  uint64_t* item_empty = item_full + kItemSlots;   // [kItemSlots], MMA warp + epilogue arrive
+  uint64_t* item_empty = item_full + kItemSlots;   // [kItemSlots], MMA warp, epilogue, producer 2 arrive
   // (t, e, row block, weight tile | phase << 16), decoded once by the producer; t < 0 ends the work
   int4* items = reinterpret_cast<int4*>(item_empty + kItemSlots);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(items + kItemSlots);
@@ -229,7 +276,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(smem_u32(acc_empty), kEpiThreads);
     for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(smem_u32(item_full + s), 1);
-      mbar_init(smem_u32(item_empty + s), 2);
+      mbar_init(smem_u32(item_empty + s), 3);   // MMA thread, epilogue, second producer
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -290,7 +337,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
     int stage = 0;
-    uint32_t phase = 0;
+    uint32_t phase = 0, gslab = 0;
     uint32_t islot = 0, iphase = 0;
     int t = -1, e = -1;
     Item it{0, 0, 0};
@@ -354,46 +401,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ok = __shfl_sync(0xffffffffu, ok, 0);
       }
       if (!gather) {
-        // one thread issues the item's slabs; the self-check of the copy ranges is done per item
-        // (the slab loop is the producer's critical path at small batches: the copies' issue cost)
+        // lane 0 issues the item's even slabs (warp 10 the odd ones)
         if (lane == 0 && ok) {
-          const size_t wend = (chunk0 + P.n_slabs) * C::W_CHUNK;
-          const size_t sfa_last = (static_cast<size_t>((P.n_slabs - 1) >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN);
-          const bool good = wend <= P.w_bytes && sfa_last + C::SFA_BYTES <= P.x_sf_bytes &&
-                            ((reinterpret_cast<uintptr_t>(P.w) | reinterpret_cast<uintptr_t>(P.x_sf)) & 15) == 0;
-          if (!good) {
-            record_error(a.status, kDevErrCheck);
-            *abort_flag = 1;
-            ok = false;
-          }
-          const uint32_t stages0 = smem_u32(stages);
-          const uint8_t* wsrc = P.w + chunk0 * C::W_CHUNK;
-          int wrow = static_cast<int>(chunk0 * C::W_CHUNK / 64);
-          for (int s = 0; ok && s < P.n_slabs; ++s) {
-            ok = mbar_wait(smem_u32(empty + stage), phase ^ 1, a.status);
-            if (!ok) break;
-            const uint32_t st = stages0 + static_cast<uint32_t>(stage * C::STAGE);
-            const uint32_t fb = smem_u32(full + stage);
-            const bool sf4 = (s & 3) == 0;
-            mbar_arrive_expect_tx(fb, C::TX_W + 1024 + C::X_BYTES + (sf4 ? C::SFA_BYTES : 0));
-            tma_load_2d(st + C::W_OFF, mw, 0, wrow, fb, pol_w);
-            bulk_load(st + C::SFB_OFF, wsrc + C::TX_W, 1024, fb);
-            tma_load_2d(st, mx, s * 128, r0, fb, pol_x);
-            if (sf4)
-              bulk_load(st + C::SFA_OFF, P.x_sf + (static_cast<size_t>(s >> 2) * a.sf_nb + r0 / BN) * act_sf_chunk_bytes(BN),
-                        C::SFA_BYTES, fb);
-            wsrc += C::W_CHUNK;
-            wrow += static_cast<int>(C::W_CHUNK / 64);
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
+          ok = issue_mx_slabs<BN>(a, P, mw, mx, r0, chunk0, 0u, stages, full, empty, stage, phase, gslab, pol_w, pol_x);
+          if (!ok) *abort_flag = 1;
         }
         // lane 0's ring position and status for the whole warp
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         stage = __shfl_sync(0xffffffffu, stage, 0);
         phase = __shfl_sync(0xffffffffu, phase, 0);
+        gslab = __shfl_sync(0xffffffffu, gslab, 0);
         continue;
       }
       for (int s = 0; ok && s < P.n_slabs; ++s) {
@@ -429,6 +446,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         g_tok[3], smem_u32(full + stage), pol_x);
         }
         __syncwarp();
+        ++gslab;
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
@@ -510,6 +528,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
     __syncwarp();
+  } else if (warp == kProducer2Warp) {
+    // ---------------- second producer (one thread): the odd slabs of every copy-path item ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();
+      const uint64_t pol_x = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, gslab = 0;
+      uint32_t islot = 0, iphase = 0;
+      while (true) {
+        bool ok = mbar_wait(smem_u32(item_full + islot), iphase, a.status);
+        const int4 item = items[islot];
+        if (ok) mbar_arrive(smem_u32(item_empty + islot));
+        if (++islot == kItemSlots) {
+          islot = 0;
+          iphase ^= 1;
+        }
+        if (!ok) *abort_flag = 1;
+        if (!ok || item.x < 0 || *abort_flag != 0) break;
+        const int ph = item.w >> 16;
+        const GemmPhase& P = a.ph[ph];
+        if (GATHER && P.gather_ids != nullptr) {
+          // the first producer's whole warp issues gathered items; keep the ring position
+          gslab += static_cast<uint32_t>(P.n_slabs);
+          stage += P.n_slabs;
+          phase ^= static_cast<uint32_t>((stage / C::STAGES) & 1);
+          stage %= C::STAGES;
+          continue;
+        }
+        if (ph == 1 && a.fused) {
+          // the item's h rows come from other CTAs' L1 epilogues (the first producer waits too)
+          const uint32_t need = static_cast<uint32_t>(a.ph[0].n_wt);
+          if (ld_acquire_gpu(a.sched + item.z) < need) ok = wait_counter(a.sched + item.z, need, a.status);
+          fence_proxy_async_global();
+          if (!ok) {
+            *abort_flag = 1;
+            break;
+          }
+        }
+        const size_t chunk0 = (static_cast<size_t>(item.y) * P.n_wt + (item.w & 0xFFFF)) * P.n_slabs;
+        if (!issue_mx_slabs<BN>(a, P, ph ? &tmap_w2 : &tmap_w1, ph ? &tmap_x2 : &tmap_x1, item.z * BN, chunk0, 1u, stages,
+                                full, empty, stage, phase, gslab, pol_w, pol_x)) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+      if (*abort_flag != 0) {
+        // let every copy issued into shared memory land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s) mbar_wait(smem_u32(full + s), (s < stage) ? phase : (phase ^ 1), nullptr);
+      }
+    }
   } else {
     // ---------------- epilogue (warps 2..9): thread = token row m of the block, one column half --------
     // Warps 2..5 take the first half of the accumulator's columns and warps 6..9 the second, so each
