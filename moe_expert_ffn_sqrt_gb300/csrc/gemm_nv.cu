@@ -34,10 +34,12 @@ constexpr int kNvBudget = 227 * 1024;
 constexpr uint32_t kNvTmemCols = 512;    // two 256-column accumulators
 constexpr int kNvTile = 256;             // weight rows per tile (MMA N)
 constexpr int kNvSlab = 64;              // K per pipeline stage (64 bf16 = one 128-byte row)
-// Packed bytes per (tile, slab): the codes as two 4 KB halves (bytes 0..15, then 16..31, of each
-// row's 32 code bytes, rows consecutive: a converter thread's 16-byte loads are conflict-free),
-// then 256 rows x 4 E4M3 scales.
-constexpr int kNvChunk = kNvTile * 32 + kNvTile * 4;
+// Packed bytes per (tile, slab): two 4608-byte halves, one per 128 rows of the tile (the CTA of a
+// pair that converts those rows loads its half with one copy).  A half holds code bytes 0..15 of
+// its 128 rows (2 KB, rows consecutive: a converter thread's 16-byte loads are conflict-free), then
+// code bytes 16..31 (2 KB), then the rows' 4 E4M3 scales (512 B).
+constexpr int kNvHalfChunk = 128 * 36;
+constexpr int kNvChunk = 2 * kNvHalfChunk;
 // Load ring slot: bf16 token rows of up to two row blocks (the MMA reads 128 rows = 16 KB each) +
 // one packed weight chunk.
 constexpr int kNvABytes = 16384;
@@ -138,9 +140,11 @@ __device__ __forceinline__ float silu_mul_nv(float g, float u) { return __fdivid
 // loads), four E4M3 scales, eight 16-byte stores into the row's 128-byte-swizzled chunks (chunk c
 // holds K positions 8c .. 8c+7 at byte ((c ^ (n & 7)) << 4) of the row).
 __device__ __forceinline__ void convert_row(const uint8_t* __restrict__ packed, uint8_t* __restrict__ btile, int n) {
-  const uint4 c0 = *reinterpret_cast<const uint4*>(packed + n * 16);
-  const uint4 c1 = *reinterpret_cast<const uint4*>(packed + kNvTile * 16 + n * 16);
-  const uint32_t sc = *reinterpret_cast<const uint32_t*>(packed + kNvTile * 32 + n * 4);
+  const uint8_t* hp = packed + (n >> 7) * kNvHalfChunk;
+  const int m = n & 127;
+  const uint4 c0 = *reinterpret_cast<const uint4*>(hp + m * 16);
+  const uint4 c1 = *reinterpret_cast<const uint4*>(hp + 2048 + m * 16);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(hp + 4096 + m * 4);
   uint32_t s2[4];
   e4m3x2_to_bf16x2(sc, s2[0], s2[1]);
   e4m3x2_to_bf16x2(sc >> 16, s2[2], s2[3]);
@@ -497,7 +501,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
 // on both CTAs' slot-empty and accumulator-full barriers (multicast).
 
 constexpr int kNvHalfRows = kNvTile / 2;
-constexpr int kNvHalfChunk = kNvHalfRows * 36;   // 128 rows x (32 code bytes + 4 scales)
+static_assert(kNvHalfChunk == kNvHalfRows * 36, "a half chunk is 128 rows x (32 code bytes + 4 scales)");
 constexpr int kNvPairLoadStage = (2 * kNvABytes + kNvHalfChunk + 1023) / 1024 * 1024;   // 37 KB
 constexpr int kNvPairLoadStages = 4;
 constexpr int kNvPairBStage = kNvHalfRows * 128;                                        // 16 KB
@@ -840,11 +844,7 @@ __global__ void __launch_bounds__(kNvThreads, 1)
                             fb, pol_x);
             }
             uint8_t* hp = st + 2 * kNvABytes;
-            bulk_load(smem_u32(hp), F.w + wbase + rank * (kNvHalfRows * 16), kNvHalfRows * 16, fb);
-            bulk_load(smem_u32(hp + kNvHalfRows * 16), F.w + wbase + kNvTile * 16 + rank * (kNvHalfRows * 16),
-                      kNvHalfRows * 16, fb);
-            bulk_load(smem_u32(hp + kNvHalfRows * 32), F.w + wbase + kNvTile * 32 + rank * (kNvHalfRows * 4),
-                      kNvHalfRows * 4, fb);
+            bulk_load(smem_u32(hp), F.w + wbase + rank * kNvHalfChunk, kNvHalfChunk, fb);
           }
         }
         __syncwarp();
@@ -1059,8 +1059,8 @@ __global__ void __launch_bounds__(256) act_to_bf16_kernel(const uint8_t* __restr
   }
 }
 
-// NVFP4 packing: per (expert, 256-row tile, 64-deep slab) 256 rows x 32 bytes of codes followed by
-// 256 rows x 4 E4M3 scales (one per 16 codes).  A W2 tile is 256 consecutive rows; a W13 tile is
+// NVFP4 packing: per (expert, 256-row tile, 64-deep slab) 256 rows x 32 bytes of codes and 4 E4M3
+// scales (one per 16 codes), in two halves of 128 rows (layout at kNvChunk).  A W2 tile is 256 consecutive rows; a W13 tile is
 // 128 gate channels and their up rows, in the order gate 0..63, up 0..63, gate 64..127, up 64..127.
 __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint8_t* __restrict__ sf, int E, int N,
                                        int Kd, int pair, uint8_t* __restrict__ out) {
@@ -1073,10 +1073,12 @@ __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint
     const int s = static_cast<int>(c % n_slabs);
     const size_t ew = c / n_slabs;
     const int wt = static_cast<int>(ew % n_wt), e = static_cast<int>(ew / n_wt);
-    const bool code = o < kNvTile * 32;
-    // codes: byte o = (half, row n, j) -> code byte 16 * half + j of row n's 32 (see kNvChunk)
-    const int n = code ? (o % (kNvTile * 16)) / 16 : (o - kNvTile * 32) / 4;
-    const int cb = code ? (o / (kNvTile * 16)) * 16 + o % 16 : 0;
+    // byte o: half hh of the tile (rows 128hh ..), then within the half p: codes (part, row m, j) ->
+    // code byte 16 * part + j of row m's 32, then row m's 4 scales (see kNvChunk)
+    const int hh = o / kNvHalfChunk, p = o % kNvHalfChunk;
+    const bool code = p < 4096;
+    const int n = 128 * hh + (code ? (p % 2048) / 16 : (p - 4096) / 4);
+    const int cb = code ? (p / 2048) * 16 + p % 16 : 0;
     // W13 tile rows in quarters of 64: gate channels 128wt + 0..63, their up rows, gate 128wt + 64..127,
     // their up rows (a channel's gate and up products sit 64 accumulator columns apart)
     const int qd = n / 64;
@@ -1084,7 +1086,7 @@ __global__ void pack_nv_weights_kernel(const uint8_t* __restrict__ q, const uint
     if (code)
       out[i] = r < N ? q[(static_cast<size_t>(e) * N + r) * (Kd / 2) + s * 32 + cb] : 0;
     else
-      out[i] = r < N ? sf[(static_cast<size_t>(e) * N + r) * (Kd / 16) + s * 4 + (o - kNvTile * 32) % 4] : 0;
+      out[i] = r < N ? sf[(static_cast<size_t>(e) * N + r) * (Kd / 16) + s * 4 + (p - 4096) % 4] : 0;
   }
 }
 
