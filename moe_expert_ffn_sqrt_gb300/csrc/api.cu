@@ -369,7 +369,7 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
                               const moe_weight& w, uint8_t* h_q, uint8_t* h_sf, uint16_t* y, void* ws,
                               size_t ws_bytes, void* stream, const FusedReduce* red = nullptr, size_t rows = 0,
                               const int32_t* row_ids = nullptr, const float* row_w = nullptr,
-                              const int32_t* gather_ids = nullptr) {
+                              const int32_t* gather_ids = nullptr, const int32_t* gather_inv = nullptr) {
   if (!dims_ok(T, H, I, E, K, align)) return MOE_ERR_INVALID_ARG;
   if (!x || !x_sf || !expert_ids || !m_sum) return MOE_ERR_INVALID_ARG;
   if (gather_ids && !l1) return MOE_ERR_INVALID_ARG;
@@ -387,8 +387,12 @@ static moe_status gemm_common(bool l1, const uint8_t* x, const uint8_t* x_sf, co
     if (ws_bytes < Lw.total) return MOE_ERR_WORKSPACE;
     uint16_t* xb = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + Lw.xb);
     const int Kd = l1 ? H : I;
-    cudaError_t err = launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream),
-                                         gather_ids, K, T);
+    // token-order rows with the pairs' row positions at hand: one pass per token
+    cudaError_t err =
+        (gather_ids && gather_inv)
+            ? launch_act_to_bf16_tokens(x, x_sf, gather_inv, T, K, static_cast<int>(U), Kd, xb, S(stream))
+            : launch_act_to_bf16(x, x_sf, expert_ids, m_sum, static_cast<int>(U), Kd, align, xb, S(stream), gather_ids,
+                                 K, T);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
     NvLaunch N = nv_launch(l1, xb, expert_ids, m_sum, H, I, E, align, U, w, h_q, h_sf, y, ws);
     if (red) N.red = *red;
@@ -455,13 +459,13 @@ static moe_status ffn_common(const uint8_t* x_perm, const uint8_t* x_perm_sf, co
                              size_t ws_bytes, void* stream, const FusedReduce* red, size_t rows = 0,
                              const int32_t* row_ids = nullptr, const float* row_w = nullptr,
                              const int32_t* slot_counts = nullptr, int slot = 0,
-                             const int32_t* gather_ids = nullptr) {
+                             const int32_t* gather_ids = nullptr, const int32_t* gather_inv = nullptr) {
   if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4) {
     // NVFP4: the two calls in turn.  (Both GEMMs in one cooperative launch, the L1 epilogue also
     // writing the bf16 h rows L2 reads, measured 8.50 ms against 8.02 ms for the skewed workload:
     // the heavier L1 epilogue holds both accumulators longer while the MMA waits.)
     moe_status st = gemm_common(true, x_perm, x_perm_sf, expert_ids, m_sum, T, K, H, I, E, align, w13, h_q, h_sf,
-                                nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w, gather_ids);
+                                nullptr, ws, ws_bytes, stream, nullptr, rows, row_ids, row_w, gather_ids, gather_inv);
     if (st != MOE_OK) return st;
     return gemm_common(false, h_q, h_sf, expert_ids, m_sum, T, K, H, I, E, align, w2, nullptr, nullptr, y, ws,
                        ws_bytes, stream, red, rows);
@@ -622,7 +626,7 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   }
   st = ffn_common(gather ? xq : xp, gather && !mx ? xsf : xpsf, eids, ms, T, K, H, I, E, align, w13, w2, hq, hsf, y,
                   ws, ws_bytes, stream, fuse_reduce ? &red : nullptr, U, l1w ? sorted : nullptr, l1w ? tw : nullptr,
-                  slot ? cnt : nullptr, slot, gather ? sorted : nullptr);
+                  slot ? cnt : nullptr, slot, gather ? sorted : nullptr, gather ? inv : nullptr);
   if (st != MOE_OK || fuse_reduce) return st;
   return cuda_status(launch_unpermute_reduce(y, inv, l1w ? nullptr : tw, T, K, H, out, S(stream)));
 }

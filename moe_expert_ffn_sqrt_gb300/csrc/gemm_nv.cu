@@ -1059,6 +1059,46 @@ __global__ void __launch_bounds__(256) act_to_bf16_kernel(const uint8_t* __restr
   }
 }
 
+// Token-order activation rows -> bf16, one warp per token: the token's row (E4M3 codes x its plain
+// UE8M0 scales) is read and converted once and stored to each of its K permuted rows inv_perm[t*K+k]
+// (the by-row kernel above reads it once per row).  The same conversion, so the same bits.
+__global__ void __launch_bounds__(256) act_to_bf16_tokens_kernel(const uint8_t* __restrict__ x,
+                                                                 const uint8_t* __restrict__ sf,
+                                                                 const int32_t* __restrict__ inv_perm, int T, int K,
+                                                                 int U, int Kd, uint16_t* __restrict__ xb) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8) {
+    int rv = -1;
+    if (lane < K) {
+      rv = __ldg(inv_perm + static_cast<size_t>(t) * K + lane);
+      if (rv < 0 || rv >= U) rv = -1;
+    }
+    const uint8_t* xr = x + static_cast<size_t>(t) * Kd;
+    const uint8_t* sr = sf + static_cast<size_t>(t) * (Kd / 128);
+    for (int k0 = lane * 8; k0 < Kd; k0 += 256) {
+      const uint32_t b = sr[k0 / 128];
+      const float sc = b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);   // 2^(b-127)
+      const uint2 c = *reinterpret_cast<const uint2*>(xr + k0);
+      const uint32_t cw[2] = {c.x, c.y};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t two = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f.x * sc));
+        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f.y * sc));
+        o[j] = lo | (hi << 16);
+      }
+      const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int k = 0; k < K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, rv, k);
+        if (r >= 0) *reinterpret_cast<uint4*>(xb + static_cast<size_t>(r) * Kd + k0) = v;
+      }
+    }
+  }
+}
+
 // NVFP4 packing: per (expert, 256-row tile, 64-deep slab) 256 rows x 32 bytes of codes and 4 E4M3
 // scales (one per 16 codes), in two halves of 128 rows (layout at kNvChunk).  A W2 tile is 256 consecutive rows; a W13 tile is
 // 128 gate channels and their up rows, in the order gate 0..63, up 0..63, gate 64..127, up 64..127.
@@ -1261,6 +1301,14 @@ cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_
   const int blocks = (U + 7) / 8 < 4 * num_sms() ? (U + 7) / 8 : 4 * num_sms();
   act_to_bf16_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(x, sf, expert_ids, m_sum, U, Kd, bt,
                                                                   act_sf_blocks(U, bt), xb, gather_ids, K, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_to_bf16_tokens(const uint8_t* x, const uint8_t* sf, const int32_t* inv_perm, int T, int K, int U,
+                                      int Kd, uint16_t* xb, cudaStream_t stream) {
+  if (K < 1 || K > 32) return cudaErrorInvalidValue;
+  const int blocks = (T + 7) / 8 < 8 * num_sms() ? (T + 7) / 8 : 8 * num_sms();
+  act_to_bf16_tokens_kernel<<<blocks > 0 ? blocks : 1, 256, 0, stream>>>(x, sf, inv_perm, T, K, U, Kd, xb);
   return cudaGetLastError();
 }
 

@@ -115,6 +115,10 @@ cudaError_t launch_pack_nv(const uint8_t* q, const uint8_t* sf, int E, int N, in
 cudaError_t launch_act_to_bf16(const uint8_t* x, const uint8_t* sf, const int32_t* expert_ids, const int32_t* m_sum,
                                int U, int Kd, int align, uint16_t* xb, cudaStream_t stream,
                                const int32_t* gather_ids = nullptr, int K = 1, int T = 0);
+// The same rows from token-order x [T, Kd] with plain scales [T, Kd/128], one pass per token: row
+// inv_perm[t*K + k] (entries outside [0, U) skipped) gets token t's converted row.  K <= 32.
+cudaError_t launch_act_to_bf16_tokens(const uint8_t* x, const uint8_t* sf, const int32_t* inv_perm, int T, int K, int U,
+                                      int Kd, uint16_t* xb, cudaStream_t stream);
 cudaError_t launch_gemm_nv(const NvLaunch& L, bool l1, cudaStream_t stream);
 
 // gemm_i8.cu (INT8 W8A8 variant: int8 codes as fp16 on the 16-bit MMA, row and channel scales in the
