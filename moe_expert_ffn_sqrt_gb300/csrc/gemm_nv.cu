@@ -1066,6 +1066,7 @@ __global__ void __launch_bounds__(256) act_to_bf16_tokens_kernel(const uint8_t* 
                                                                  const uint8_t* __restrict__ sf,
                                                                  const int32_t* __restrict__ inv_perm, int T, int K,
                                                                  int U, int Kd, uint16_t* __restrict__ xb) {
+  __shared__ int s_rows[8][32];   // the warp's token's K row positions (read by lanes that diverge at the row's end)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   for (int t = blockIdx.x * 8 + warp; t < T; t += gridDim.x * 8) {
     int rv = -1;
@@ -1073,29 +1074,44 @@ __global__ void __launch_bounds__(256) act_to_bf16_tokens_kernel(const uint8_t* 
       rv = __ldg(inv_perm + static_cast<size_t>(t) * K + lane);
       if (rv < 0 || rv >= U) rv = -1;
     }
+    s_rows[warp][lane] = rv;
+    __syncwarp();
     const uint8_t* xr = x + static_cast<size_t>(t) * Kd;
     const uint8_t* sr = sf + static_cast<size_t>(t) * (Kd / 128);
-    for (int k0 = lane * 8; k0 < Kd; k0 += 256) {
-      const uint32_t b = sr[k0 / 128];
-      const float sc = b ? __uint_as_float(b << 23) : __uint_as_float(0x00400000u);   // 2^(b-127)
-      const uint2 c = *reinterpret_cast<const uint2*>(xr + k0);
-      const uint32_t cw[2] = {c.x, c.y};
-      uint32_t o[4];
+    // four lane steps (1024 codes of the row) loaded before any is converted and stored
+    for (int kb = 0; kb < Kd; kb += 1024) {
+      uint2 c[4];
+      uint32_t b[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t two = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
-        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-        const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f.x * sc));
-        const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f.y * sc));
-        o[j] = lo | (hi << 16);
+      for (int u = 0; u < 4; ++u) {
+        const int k0 = kb + u * 256 + lane * 8;
+        c[u] = k0 < Kd ? __ldg(reinterpret_cast<const uint2*>(xr + k0)) : make_uint2(0, 0);
+        b[u] = k0 < Kd ? __ldg(sr + k0 / 128) : 0u;
       }
-      const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
-      for (int k = 0; k < K; ++k) {
-        const int r = __shfl_sync(0xffffffffu, rv, k);
-        if (r >= 0) *reinterpret_cast<uint4*>(xb + static_cast<size_t>(r) * Kd + k0) = v;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k0 = kb + u * 256 + lane * 8;
+        if (k0 >= Kd) break;
+        const float sc = b[u] ? __uint_as_float(b[u] << 23) : __uint_as_float(0x00400000u);   // 2^(b-127)
+        const uint32_t cw[2] = {c[u].x, c[u].y};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t two = (cw[j >> 1] >> (16 * (j & 1))) & 0xFFFF;
+          const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(f.x * sc));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(f.y * sc));
+          o[j] = lo | (hi << 16);
+        }
+        const uint4 v = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int k = 0; k < K; ++k) {
+          const int r = s_rows[warp][k];
+          if (r >= 0) *reinterpret_cast<uint4*>(xb + static_cast<size_t>(r) * Kd + k0) = v;
+        }
       }
     }
+    __syncwarp();   // every lane has read s_rows before the next token's rows replace them
   }
 }
 
