@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kGateThreads, 1)
 int gate_nsplit(int T, int H, int E) {
   const int tiles = ((E + kGateM - 1) / kGateM) * ((T + kGateN - 1) / kGateN);
   const int nkb = H / kGateKB;
-  int ns = 148 / tiles;
+  int ns = num_sms() / tiles;                // about one CTA per SM
   if (ns > kGateMaxSplit) ns = kGateMaxSplit;
   if (ns > nkb) ns = nkb;
   if (ns < 1) ns = 1;
