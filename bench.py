@@ -40,8 +40,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 SPIN_CYCLES = 1_000_000      # ~0.5 ms at 2 GHz, outside the timed events
 
 
-def launches_per_forward(w, naive=False):
+def launches_per_forward(w, naive=False, single=False):
     """Kernel launches of one forward call, mirroring the library's dispatch."""
+    if single:
+        return 1                                  # moe_forward_single_launch: the whole layer
     tk = w.T * w.K
     route = 1 if w.T <= 16 else 3                 # fused small-batch route, else gate split + gate GEMM + top-K
     reduce = 0 if w.T <= 32 else 1                # small batches reduce inside the L2 epilogue
@@ -105,10 +107,12 @@ def parse_args():
                    help="stage-by-stage timing: the L1 GEMM reads the token-order activation through "
                         "sorted_token_ids or the permute's row copy x_perm; auto: as moe_forward does "
                         "(token order with NVFP4 weights, the copy with MXFP4)")
-    p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive"],
+    p.add_argument("--layout", default="contiguous", choices=["contiguous", "batched", "naive", "single"],
                    help="permuted-row layout: expert-contiguous segments padded to align (moe_forward) or "
                         "BatchedExperts slots of max_tokens = max(16, the smallest power of two >= T) (moe_forward_batched) or "
-                        "the tiny-batch layout, one 16-row block per (token, expert) pair, no sort (moe_forward_naive)")
+                        "the tiny-batch layout, one 16-row block per (token, expert) pair, no sort (moe_forward_naive); "
+                        "single: moe_forward's layout with the whole layer in one launch (moe_forward_single_launch, "
+                        "up to 16 tokens, MXFP4)")
     return p.parse_args()
 
 
@@ -365,6 +369,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     e_bias = None if inp["e_score_bias"] is None else d(inp["e_score_bias"])
     batched = args.layout == "batched"
     naive = args.layout == "naive"
+    single = args.layout == "single"
     # BatchedExperts slot: the smallest power of two >= T, at least 16 (one expert per GEMM row block)
     S = max(16, 1 << max(0, (T - 1).bit_length()))
     if batched:
@@ -388,7 +393,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
                               ws)
         else:
             M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13, w2, out,
-                      ws, weights_in_l1=args.weights_in_l1)
+                      ws, weights_in_l1=args.weights_in_l1, single_launch=single)
 
     def barrier():
         if W > 1:
@@ -591,6 +596,8 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
     cfg["parallelism"] = f"replicas x{W}"
     cfg["layout"] = (f"BatchedExperts, max_tokens={S}" if batched else
                      "tiny-batch, one 16-row block per (token, expert) pair" if naive else
+                     "expert-contiguous, padded to align; the whole layer in one cooperative launch (stage_ms "
+                     "from the separate stage calls)" if single else
                      "expert-contiguous, padded to align")
     cfg["routing_weights"] = ("applied in the L1 epilogue, unweighted reduce (stage_ms from the reduce-weighted "
                               "stage calls)" if args.weights_in_l1 else "applied in the reduce")
@@ -598,7 +605,7 @@ def measure(args, w, steps, warmup, cpu_seconds, dev):
                        "permuted row copy")
     cfg["stage_l1_input"] = "token-order" if token_order else "permuted copy"
     res = dict(value=value, ms=ms, steps=K, warmup=warmup, roofline=roofline, e2e=e2e, cpu=cpu, cfg=cfg,
-               clocks=clk, launches=launches_per_forward(w, naive) * K,
+               clocks=clk, launches=launches_per_forward(w, naive, single) * K,
                dtype={"mxfp4": "fp8xfp4 (fp32 accumulate)",
                       "nvfp4": "bf16 (exact fp8/nvfp4 values, fp32 accumulate)",
                       "int8": "int8xint8 as fp16 (exact codes, fp32 accumulate)",

@@ -269,6 +269,24 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
                        int32_t* sorted_token_ids, int32_t* expert_ids, int32_t* inv_perm,
                        int32_t* m_sum, void* ws, size_t ws_bytes, void* stream);
 
+/* moe_forward as one launch: the single persistent kernel of page "DeepSeek V4 MegaMoE Kernel
+ * 深度解析", 一、架构概览 整体思路 (one launch for the whole layer) and 二、Fused 了什么 (stages 1-5),
+ * for small batches: the routing (gate, scores, top-K, FP8 activations), the permute, L1 with
+ * SwiGLU and requant, L2 and the weighted reduce run as phases of one cooperative kernel, with two
+ * grid-wide barriers between routing, permute and the expert GEMMs.  Same arguments, workspace
+ * (moe_workspace_size) and results as moe_forward, bit for bit.  Supported: MXFP4 weights,
+ * 1 <= T <= 16, E <= 256, T*K <= 128, align <= 16; other problems return MOE_ERR_UNSUPPORTED
+ * (moe_forward covers them).  A barrier wait that runs out is reported as MOE_ERR_TIMEOUT by
+ * moe_get_error, with out unspecified.  The calls of one stream must not overlap: the launch
+ * starts after the previous one and reuses the workspace's routing scratch. */
+moe_status moe_forward_single_launch(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                     const float* e_score_bias, int T, int H, int I, int E, int K,
+                                     int align, moe_score_fn fn, int renormalize, moe_weight w13,
+                                     moe_weight w2, uint16_t* out, int32_t* topk_ids, float* topk_w,
+                                     int32_t* sorted_token_ids, int32_t* expert_ids,
+                                     int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes,
+                                     void* stream);
+
 /* --------------------------------------------------------------------------------------
  * BatchedExperts layout (MegaMoE page, vLLM 的两种 Activation Format and 路径 B: each expert
  * owns a fixed slot of max_tokens rows filled through a boolean mask over the tokens; note

@@ -89,6 +89,8 @@ def lib():
         L.moe_grouped_gemm_l1_swiglu_weighted.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, _Weight, P, P, P, Z, P]
         L.moe_forward_l1_weighted.restype = S
         L.moe_forward_l1_weighted.argtypes = L.moe_forward.argtypes
+        L.moe_forward_single_launch.restype = S
+        L.moe_forward_single_launch.argtypes = L.moe_forward.argtypes
         L.moe_route_naive.restype = S
         L.moe_route_naive.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, Z, P]
         L.moe_forward_naive.restype = S
@@ -339,11 +341,15 @@ def unpermute_reduce(y_perm, inv_perm, topk_w, out):
 
 def forward(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, renormalize, w13, w2, out, ws,
             topk_ids=None, topk_w=None, sorted_token_ids=None, expert_ids=None, inv_perm=None, m_sum=None,
-            weights_in_l1=False):
-    """moe_forward, or moe_forward_l1_weighted when weights_in_l1 (routing weights applied in L1)."""
+            weights_in_l1=False, single_launch=False):
+    """moe_forward; moe_forward_l1_weighted when weights_in_l1 (routing weights applied in L1);
+    moe_forward_single_launch when single_launch (the whole layer in one launch, small batches)."""
     T, H = hidden.shape
     E = w_gate.shape[0]
-    fn = lib().moe_forward_l1_weighted if weights_in_l1 else lib().moe_forward
+    if weights_in_l1 and single_launch:
+        raise MoeError(ERR_INVALID_ARG, "forward")
+    fn = (lib().moe_forward_l1_weighted if weights_in_l1 else
+          lib().moe_forward_single_launch if single_launch else lib().moe_forward)
     _check(fn(_ptr(hidden, torch.bfloat16, "hidden"), _ptr(w_gate, torch.float32, "w_gate"),
                              _ptr(gate_bias, torch.float32, "gate_bias"), _ptr(e_score_bias, torch.float32, "e_score_bias"),
                              T, H, I, E, K, align, SCORE_FNS.get(score_fn, score_fn), int(renormalize), w13.c(), w2.c(),
@@ -351,7 +357,7 @@ def forward(hidden, w_gate, gate_bias, e_score_bias, I, K, align, score_fn, reno
                              _ptr(topk_w, torch.float32, "topk_w"), _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"),
                              _ptr(expert_ids, torch.int32, "expert_ids"), _ptr(inv_perm, torch.int32, "inv_perm"),
                              _ptr(m_sum, torch.int32, "m_sum"), _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream()),
-           "moe_forward")
+           "moe_forward_single_launch" if single_launch else "moe_forward")
 
 
 # ------------------------------------------------------------------ BatchedExperts layout

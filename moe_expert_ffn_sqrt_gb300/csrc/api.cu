@@ -631,7 +631,95 @@ static moe_status forward_common(const uint16_t* hidden, const float* w_gate, co
   return cuda_status(launch_unpermute_reduce(y, inv, l1w ? nullptr : tw, T, K, H, out, S(stream)));
 }
 
+// moe_forward in one launch (small batches, MXFP4): the same workspace layout, the same routing,
+// permute and GEMM code, run as phases of one cooperative kernel.
+static moe_status forward_single_launch(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                        const float* e_score_bias, int T, int H, int I, int E, int K, int align,
+                                        moe_score_fn fn, int renormalize, const moe_weight& w13, const moe_weight& w2,
+                                        uint16_t* out, int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids,
+                                        int32_t* expert_ids, int32_t* inv_perm, int32_t* m_sum, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!dims_ok(T, H, I, E, K, align) || E > 1024) return MOE_ERR_INVALID_ARG;
+  if (!hidden || !w_gate || !out || !weight_ok(w13, E, 2 * I, H, 2) || !weight_ok(w2, E, H, I, 1))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(out, 16)) return MOE_ERR_INVALID_ARG;
+  if (!ws) return MOE_ERR_WORKSPACE;
+  const size_t U = moe_msum_upper(T, K, E, align);
+  const WsLayout L = layout_rows(T, H, I, E, K, align, U);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  if (w13.fmt != MOE_W_MXFP4 || w2.fmt != MOE_W_MXFP4 || !prelude_supported(T, E, K, align) ||
+      T > kFusedReduceMaxTokens)
+    return MOE_ERR_UNSUPPORTED;
+  char* b = static_cast<char*>(ws);
+  int32_t* ids = topk_ids ? topk_ids : reinterpret_cast<int32_t*>(b + L.topk_ids);
+  float* tw = topk_w ? topk_w : reinterpret_cast<float*>(b + L.topk_w);
+  int32_t* sorted = sorted_token_ids ? sorted_token_ids : reinterpret_cast<int32_t*>(b + L.sorted);
+  int32_t* eids = expert_ids ? expert_ids : reinterpret_cast<int32_t*>(b + L.expert_ids);
+  int32_t* inv = inv_perm ? inv_perm : reinterpret_cast<int32_t*>(b + L.inv_perm);
+  int32_t* ms = m_sum ? m_sum : reinterpret_cast<int32_t*>(b + L.m_sum);
+  uint8_t* xq = reinterpret_cast<uint8_t*>(b + L.x_q);
+  uint8_t* xsf = reinterpret_cast<uint8_t*>(b + L.x_sf);
+  uint8_t* xp = reinterpret_cast<uint8_t*>(b + L.x_perm);
+  uint8_t* xpsf = reinterpret_cast<uint8_t*>(b + L.x_perm_sf);
+  uint8_t* hq = reinterpret_cast<uint8_t*>(b + L.h_q);
+  uint8_t* hsf = reinterpret_cast<uint8_t*>(b + L.h_sf);
+  uint16_t* y = reinterpret_cast<uint16_t*>(b + L.y);
+  // the routing scratch where moe_route keeps it
+  const size_t poff = up(kAlign + permute_scratch_bytes(T, K, E));
+  if (poff + route_scratch_bytes(T, H, E) > ws_bytes) return MOE_ERR_WORKSPACE;
+  FusedReduce red{};
+  red.out = out;
+  red.inv_perm = inv;
+  red.topk_w = tw;
+  red.sorted_ids = sorted;
+  red.tickets = reinterpret_cast<uint32_t*>(b + L.tickets);
+  red.K = K;
+  GemmLaunch l1 = mx_launch(true, xp, xpsf, eids, ms, H, I, E, align, U, w13, hq, hsf, nullptr, ws);
+  GemmLaunch l2 = mx_launch(false, hq, hsf, eids, ms, H, I, E, align, U, w2, nullptr, nullptr, y, ws);
+  l2.red = red;
+  PreludeLaunch p{};
+  p.hidden = hidden;
+  p.w_gate = w_gate;
+  p.gate_bias = gate_bias;
+  p.e_bias = e_score_bias;
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.K = K;
+  p.score_fn = static_cast<int>(fn);
+  p.renormalize = renormalize;
+  p.logits_out = nullptr;
+  p.topk_ids = ids;
+  p.topk_w = tw;
+  p.x_q = xq;
+  p.x_sf = xsf;
+  p.partial = route_partials(b + poff);
+  p.align = align;
+  p.U = static_cast<int>(U);
+  p.sorted_ids = sorted;
+  p.expert_ids = eids;
+  p.inv_perm = inv;
+  p.m_sum = ms;
+  p.counts = nullptr;
+  p.x_perm = xp;
+  p.x_perm_sf = xpsf;
+  p.status = status_of(ws);
+  uint32_t* sched = reinterpret_cast<uint32_t*>(b + L.sched);
+  return cuda_status(launch_ffn_prelude(l1, l2, p, sched, S(stream)));
+}
+
 extern "C" {
+
+moe_status moe_forward_single_launch(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
+                                     const float* e_score_bias, int T, int H, int I, int E, int K, int align,
+                                     moe_score_fn fn, int renormalize, moe_weight w13, moe_weight w2, uint16_t* out,
+                                     int32_t* topk_ids, float* topk_w, int32_t* sorted_token_ids, int32_t* expert_ids,
+                                     int32_t* inv_perm, int32_t* m_sum, void* ws, size_t ws_bytes, void* stream) {
+  return forward_single_launch(hidden, w_gate, gate_bias, e_score_bias, T, H, I, E, K, align, fn, renormalize, w13, w2,
+                               out, topk_ids, topk_w, sorted_token_ids, expert_ids, inv_perm, m_sum, ws, ws_bytes,
+                               stream);
+}
 
 moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                        const float* e_score_bias, int T, int H, int I, int E, int K, int align, moe_score_fn fn,

@@ -34,6 +34,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "permute_small.cuh"
+#include "route_small.cuh"
 
 namespace moe {
 
@@ -70,6 +72,19 @@ struct GemmCfg {
   static_assert(X_SLOT + 16384 <= STAGE, "MMA A reads must stay inside the stage");
 };
 
+// Single-launch forward: the small-batch routing and permute run inside the GEMM launch first.
+struct PreludeArgs {
+  RouteFinishArgs r;            // routing (its topk_ids, topk_w, logits, x_q, x_sf are stored by CTA 0 / all)
+  const float* w_gate;          // [E, H]
+  float* partial;               // [kGemvSplit, T, E] gate partial sums
+  PermuteArgs p;                // the small permute over the routing's ids
+  const uint8_t* x_q;           // [T, H] E4M3 (written by the routing phase)
+  const uint8_t* x_sf;          // [T, H/128]
+  uint8_t* x_perm;              // [U, H]
+  uint8_t* x_perm_sf;           // tiled
+  int H, bt, nb;
+};
+
 // One GEMM of the layer as the kernel sees it.
 struct GemmPhase {
   const uint8_t* w;             // packed weight stream
@@ -98,9 +113,10 @@ struct GemmArgs {
   uint16_t* y;                  // L2 out [U, H] bf16
   uint32_t* status;
   int sf_nb;                    // blocks of the tiled token-scale layouts
-  uint32_t* sched;              // [n_ready + 2] words, zero at launch and left at zero by the last CTA
+  uint32_t* sched;              // [n_ready + 4] words, zero at launch and left at zero by the last CTA
                                 // to exit: [0, n_ready) finished L1 tiles per row block (fused
-                                // launches), [n_ready] next work item, [n_ready + 1] exited CTAs
+                                // launches), [n_ready] next work item, [n_ready + 1] exited CTAs,
+                                // [n_ready + 2, + 3] the single-launch forward's grid barriers
   int n_ready;                  // ceil(U/BN)
   int fused;                    // both phases in one launch: L2 items wait for their block's L1 tiles
   int one_expert_blocks;        // permute alignment is a multiple of BN: one expert per row block
@@ -112,6 +128,7 @@ struct GemmArgs {
   const int32_t* counts;        // nullptr: every row block below m_sum is an item
   int slot_blocks;
   int E;
+  PreludeArgs pre;              // single-launch forward only
 };
 
 constexpr int kMaxMaskedExperts = 1024;   // masked mode: experts in the shared prefix table
@@ -235,6 +252,22 @@ __device__ __forceinline__ bool issue_mx_slabs(const GemmArgs& a, const GemmPhas
   return true;
 }
 
+// Every CTA of a cooperative launch arrives on the counter and waits until all have (bounded:
+// false, with the status recorded, if the wait runs out).  Thread 0 arrives and waits, with fences
+// on both sides as a grid-wide barrier needs; the CTA's barriers spread the result.
+__device__ __forceinline__ bool grid_barrier(uint32_t* ctr, uint32_t* status, volatile int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const bool ok = wait_counter(ctr, gridDim.x, status);
+    __threadfence();
+    *flag = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
 // Runs the L1 items, the L2 items, or both.  With both, an L2 item of row block rb reads h rows
 // written by other CTAs: its producer first waits until sched[rb] counts all n_wt L1 tiles of the
 // block (each L1 item's epilogue adds one after its stores).  Items are drawn in index order, all
@@ -245,7 +278,14 @@ __device__ __forceinline__ bool issue_mx_slabs(const GemmArgs& a, const GemmPhas
 // The last CTA to exit sets all counters back to zero: no CTA can still be waiting or drawing then.
 // GATHER: the L1 phase reads its token rows with four-row gathers (GemmPhase::gather_ids); a
 // separate instance, so that the permuted-copy path carries none of that bookkeeping.
-template <int BN, bool GATHER>
+// PRELUDE (the single-launch forward, small batches; the launch is cooperative, so every CTA is
+// resident): before the FFN work the CTAs run the small-batch routing (the blocks of its grid
+// spread over the CTAs, threads 0..255 of each), meet at a grid barrier, then each CTA computes
+// the top-K of every token into shared memory (CTA 0 stores the routing outputs) and runs the
+// small permute on it (CTA 0 stores the indices; padding, tail and row copies are split over the
+// CTAs), and they meet again.  The same device functions as the routing and permute launches,
+// so the results are the same bits.
+template <int BN, bool GATHER, bool PRELUDE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
                     const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_x2,
@@ -292,6 +332,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
+  }
+  if constexpr (PRELUDE) {
+    // scratch in the ring (not yet in use): partial-sum exchange [8][4 * 16] floats, the top-K ids
+    // (<= 128), the permute's counts, segment starts, ids and ranks (256 each), total and a flag
+    float(*red)[kGemvE * kGemvT] = reinterpret_cast<float(*)[kGemvE * kGemvT]>(stages);
+    int32_t* s_topk = reinterpret_cast<int32_t*>(stages + 8 * kGemvE * kGemvT * sizeof(float));
+    int32_t* p_cnt = s_topk + 128;
+    int32_t* p_seg = p_cnt + 256;
+    int32_t* p_ids = p_seg + 256;
+    int32_t* p_rank = p_ids + 256;
+    int32_t* p_total = p_rank + 256;
+    volatile int* p_flag = reinterpret_cast<volatile int*>(p_total + 1);
+    const PreludeArgs& q = a.pre;
+    const int gx = (q.r.E + kGemvE - 1) / kGemvE;
+    const auto sync256 = [] { named_barrier(2, 256); };
+    for (int vb = blockIdx.x; vb < gx * kGemvSplit; vb += gridDim.x) {
+      if (threadIdx.x < 256) {
+        route_small_gemv<kGemvT>(q.r, q.w_gate, q.partial, vb % gx, vb / gx, gx, threadIdx.x, red, sync256);
+        named_barrier(2, 256);   // red is reused by the next block
+      }
+    }
+    bool pre_ok = grid_barrier(a.sched + a.n_ready + 2, a.status, p_flag);
+    if (pre_ok) {
+      if (threadIdx.x < 256) {
+        route_small_topk<kGemvT, 8>(q.r, q.partial, threadIdx.x / 32, threadIdx.x % 32, 8, s_topk, blockIdx.x == 0);
+        named_barrier(2, 256);   // every token's ids in s_topk
+        permute_small_body<256>(q.p, s_topk, q.x_q, q.x_sf, q.H, q.x_perm, q.x_perm_sf, q.bt, q.nb, p_cnt, p_seg, p_ids,
+                                p_rank, p_total, threadIdx.x, blockIdx.x, gridDim.x, sync256);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the ring's next writers are copies
+      fence_proxy_async_global();   // x_perm and its scales are read next by TMA and bulk copies
+      pre_ok = grid_barrier(a.sched + a.n_ready + 3, a.status, p_flag);
+      fence_proxy_async_global();
+    }
+    if (!pre_ok && threadIdx.x == 0) *abort_flag = 1;   // every role then stops before its first item
   }
   // masked mode: each expert's row blocks that hold tokens, loaded by all threads at once; the
   // prefix over experts is formed after the barrier below
@@ -749,7 +824,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   if (s_last_cta) {
     __threadfence();
-    for (int i = threadIdx.x; i < a.n_ready + 2; i += blockDim.x) a.sched[i] = 0;
+    for (int i = threadIdx.x; i < a.n_ready + 4; i += blockDim.x) a.sched[i] = 0;
   }
 }
 
@@ -838,8 +913,9 @@ static bool make_phase(const GemmLaunch& L, bool l1, GemmPhase& P, CUtensorMap& 
 // l1 and/or l2 (non-null ones run).  `sched` holds gemm_sched_words(U, align) words that are zero
 // before the launch and zero again after it (work counter; with both phases also the per-row-block
 // counters that order them).
-template <int BN, bool GATHER>
-static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream) {
+template <int BN, bool GATHER, bool PRELUDE = false>
+static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uint32_t* sched, cudaStream_t stream,
+                                 const PreludeArgs* pre = nullptr) {
   using C = GemmCfg<BN>;
   GemmArgs a{};
   CUtensorMap m[4] = {};
@@ -886,7 +962,13 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   int grid = num_sms();
   if (grid > total) grid = total;
   if (grid < 1) grid = 1;
-  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN, GATHER>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if constexpr (PRELUDE) {
+    if (!pre) return cudaErrorInvalidValue;
+    a.pre = *pre;
+    grid = num_sms();   // one CTA per SM, all resident (cooperative launch): the routing blocks need them all
+  }
+  cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN, GATHER, PRELUDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -896,21 +978,27 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   // Programmatic stream serialization lets the CTAs start their prologue (barriers, TMEM, tensor
   // maps) while the permute finishes; they wait for it before reading its results.  Should the
   // runtime refuse it, the launch is repeated without it.
+  // The single-launch forward is cooperative instead (its grid barriers need every CTA resident)
+  // and starts only after the previous launch, whose outputs its routing phase overwrites.
   static bool pdl_ok = true;
   cudaLaunchAttribute attr[1];
   int n = 0;
-  if (pdl_ok) {
+  if (PRELUDE) {
+    attr[n].id = cudaLaunchAttributeCooperative;
+    attr[n].val.cooperative = 1;
+    ++n;
+  } else if (pdl_ok) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
-  if (err != cudaSuccess && pdl_ok) {
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a);
+  if (err != cudaSuccess && !PRELUDE && pdl_ok) {
     (void)cudaGetLastError();
     cfg.numAttrs = n - 1;
-    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER>, m[0], m[1], m[2], m[3], a);
+    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a);
     if (err == cudaSuccess) pdl_ok = false;   // only the attribute was refused
   }
   if (err != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for later calls
@@ -942,9 +1030,53 @@ cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* sch
   return launch_bn(&l1, &l2, sched, stream);
 }
 
+cudaError_t launch_ffn_prelude(const GemmLaunch& l1, const GemmLaunch& l2, const PreludeLaunch& p, uint32_t* sched,
+                               cudaStream_t stream) {
+  if (!prelude_supported(p.T, p.E, p.K, p.align) || gemm_block_n(l1.align) != 16 || l1.gather_ids || l1.counts)
+    return cudaErrorInvalidValue;
+  PreludeArgs q{};
+  q.r.partial = p.partial;
+  q.r.nsplit = kGemvSplit;
+  q.r.gate_bias = p.gate_bias;
+  q.r.e_bias = p.e_bias;
+  q.r.T = p.T;
+  q.r.H = p.H;
+  q.r.E = p.E;
+  q.r.K = p.K;
+  q.r.score_fn = p.score_fn;
+  q.r.renormalize = p.renormalize;
+  q.r.logits_out = p.logits_out;
+  q.r.topk_ids = p.topk_ids;
+  q.r.topk_w = p.topk_w;
+  q.r.hidden = p.hidden;
+  q.r.x_q = p.x_q;
+  q.r.x_sf = p.x_sf;
+  q.r.topk_blocks = p.T;
+  q.r.nv = NaiveLayout{};
+  q.r.gate_failed = nullptr;
+  q.w_gate = p.w_gate;
+  q.partial = p.partial;
+  q.p = PermuteArgs{p.topk_ids, p.T, p.K, p.E, p.align, p.U, p.sorted_ids, p.expert_ids, p.inv_perm, p.m_sum,
+                    p.counts, p.status, 0};
+  q.x_q = p.x_q;
+  q.x_sf = p.x_sf;
+  q.x_perm = p.x_perm;
+  q.x_perm_sf = p.x_perm_sf;
+  q.H = p.H;
+  q.bt = act_sf_block_rows(p.align);
+  q.nb = act_sf_blocks(p.U, q.bt);
+  return launch_gemm_t<16, false, true>(&l1, &l2, sched, stream, &q);
+}
+
+bool prelude_supported(int T, int E, int K, int align) {
+  // the routing's 16-token and 256-expert register tiles, one thread per (token, slot) pair in a
+  // 256-thread permute that also copies the rows (up to 128 pairs), 16-row GEMM blocks
+  return T >= 1 && T <= kGemvT && E >= 1 && E <= 256 && T * K <= 128 && gemm_block_n(align) == 16;
+}
+
 size_t gemm_sched_words(int U, int align) {
   const int bn = gemm_block_n(align);
-  return static_cast<size_t>((U + bn - 1) / bn) + 2;   // row-block counters, work counter, exit counter
+  return static_cast<size_t>((U + bn - 1) / bn) + 4;   // row-block counters, work, exit, two grid barriers
 }
 
 // ------------------------------------------------------------------------------------------

@@ -24,6 +24,8 @@ struct NaiveLayout {
   uint8_t* xp_sf = nullptr;    // tiled (block rows kNaiveRows, rows U, slabs H/128)
   int U = 0, sf_nb = 0;
 };
+// The gate partial sums inside a routing scratch buffer (route_scratch_bytes of it).
+float* route_partials(void* scratch);
 cudaError_t launch_route(const uint16_t* hidden, const float* w_gate, const float* gate_bias, const float* e_bias,
                          int T, int H, int E, int K, int score_fn, int renormalize, float* logits_out,
                          int32_t* topk_ids, float* topk_w, uint8_t* x_q, uint8_t* x_sf, void* scratch,
@@ -87,6 +89,35 @@ cudaError_t launch_gemm(const GemmLaunch& L, bool l1, uint32_t* sched, cudaStrea
 // L1 and L2 in one launch (L2 tiles wait for their row block's L1 tiles).
 cudaError_t launch_ffn(const GemmLaunch& l1, const GemmLaunch& l2, uint32_t* sched, cudaStream_t stream);
 size_t gemm_sched_words(int U, int align);
+// Single-launch forward (small batches, MXFP4, 16-row GEMM blocks): the small-batch routing and
+// permute run inside the FFN launch before its GEMM work (cooperative launch, two grid barriers).
+// The fields are those of launch_route and launch_permute; partial = the routing scratch's partial
+// sums (route_partials).
+struct PreludeLaunch {
+  const uint16_t* hidden;
+  const float* w_gate;
+  const float* gate_bias;
+  const float* e_bias;
+  int T, H, E, K, score_fn, renormalize;
+  float* logits_out;
+  int32_t* topk_ids;
+  float* topk_w;
+  uint8_t* x_q;
+  uint8_t* x_sf;
+  float* partial;
+  int align, U;
+  int32_t* sorted_ids;
+  int32_t* expert_ids;
+  int32_t* inv_perm;
+  int32_t* m_sum;
+  int32_t* counts;
+  uint8_t* x_perm;
+  uint8_t* x_perm_sf;
+  uint32_t* status;
+};
+bool prelude_supported(int T, int E, int K, int align);
+cudaError_t launch_ffn_prelude(const GemmLaunch& l1, const GemmLaunch& l2, const PreludeLaunch& p, uint32_t* sched,
+                               cudaStream_t stream);
 cudaError_t launch_pack_mx(const uint8_t* q, const uint8_t* sf, int E, int N, int Kd, int pair, uint8_t* out,
                            cudaStream_t stream);
 
