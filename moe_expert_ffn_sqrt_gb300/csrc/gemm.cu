@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "permute_small.cuh"
@@ -128,8 +130,13 @@ struct GemmArgs {
   const int32_t* counts;        // nullptr: every row block below m_sum is an item
   int slot_blocks;
   int E;
-  PreludeArgs pre;              // single-launch forward only
 };
+
+// The kernel's last parameter: the prelude's arguments in the single-launch instance, nothing
+// (an empty struct) in the others, so that their parameter block stays as small as before.
+struct NoPrelude {};
+template <bool PRELUDE>
+using PreludeParam = typename std::conditional<PRELUDE, PreludeArgs, NoPrelude>::type;
 
 constexpr int kMaxMaskedExperts = 1024;   // masked mode: experts in the shared prefix table
 
@@ -289,7 +296,7 @@ template <int BN, bool GATHER, bool PRELUDE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     moe_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w1, const __grid_constant__ CUtensorMap tmap_x1,
                     const __grid_constant__ CUtensorMap tmap_w2, const __grid_constant__ CUtensorMap tmap_x2,
-                    const GemmArgs a) {
+                    const GemmArgs a, const PreludeParam<PRELUDE> pre) {
   using C = GemmCfg<BN>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -344,7 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int32_t* p_rank = p_ids + 256;
     int32_t* p_total = p_rank + 256;
     volatile int* p_flag = reinterpret_cast<volatile int*>(p_total + 1);
-    const PreludeArgs& q = a.pre;
+    const PreludeArgs& q = pre;
     const int gx = (q.r.E + kGemvE - 1) / kGemvE;
     const auto sync256 = [] { named_barrier(2, 256); };
     for (int vb = blockIdx.x; vb < gx * kGemvSplit; vb += gridDim.x) {
@@ -356,9 +363,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     bool pre_ok = grid_barrier(a.sched + a.n_ready + 2, a.status, p_flag);
     if (pre_ok) {
       if (threadIdx.x < 256) {
-        route_small_topk<kGemvT, 8>(q.r, q.partial, threadIdx.x / 32, threadIdx.x % 32, 8, s_topk, blockIdx.x == 0);
+        if (blockIdx.x == 0)   // CTA 0 also stores the routing outputs
+          route_small_topk<kGemvT, 8, true, true>(q.r, q.partial, threadIdx.x / 32, threadIdx.x % 32, s_topk);
+        else
+          route_small_topk<kGemvT, 8, true, false>(q.r, q.partial, threadIdx.x / 32, threadIdx.x % 32, s_topk);
         named_barrier(2, 256);   // every token's ids in s_topk
-        permute_small_body<256>(q.p, s_topk, q.x_q, q.x_sf, q.H, q.x_perm, q.x_perm_sf, q.bt, q.nb, p_cnt, p_seg, p_ids,
+        permute_small_body<256, true>(q.p, s_topk, q.x_q, q.x_sf, q.H, q.x_perm, q.x_perm_sf, q.bt, q.nb, p_cnt, p_seg, p_ids,
                                 p_rank, p_total, threadIdx.x, blockIdx.x, gridDim.x, sync256);
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the ring's next writers are copies
@@ -962,9 +972,10 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   int grid = num_sms();
   if (grid > total) grid = total;
   if (grid < 1) grid = 1;
+  PreludeParam<PRELUDE> pp{};
   if constexpr (PRELUDE) {
     if (!pre) return cudaErrorInvalidValue;
-    a.pre = *pre;
+    pp = *pre;
     grid = num_sms();   // one CTA per SM, all resident (cooperative launch): the routing blocks need them all
   }
   cudaError_t err = cudaFuncSetAttribute(moe_gemm_kernel<BN, GATHER, PRELUDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -994,11 +1005,11 @@ static cudaError_t launch_gemm_t(const GemmLaunch* l1, const GemmLaunch* l2, uin
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a);
+  err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a, pp);
   if (err != cudaSuccess && !PRELUDE && pdl_ok) {
     (void)cudaGetLastError();
     cfg.numAttrs = n - 1;
-    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a);
+    err = cudaLaunchKernelEx(&cfg, moe_gemm_kernel<BN, GATHER, PRELUDE>, m[0], m[1], m[2], m[3], a, pp);
     if (err == cudaSuccess) pdl_ok = false;   // only the attribute was refused
   }
   if (err != cudaSuccess) (void)cudaGetLastError();   // a refused launch leaves no error for later calls

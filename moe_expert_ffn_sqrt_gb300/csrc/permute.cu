@@ -175,17 +175,126 @@ __global__ void __launch_bounds__(kPermThreads, 1) permute_place_kernel(const Pe
   }
 }
 
+// The small permute (method in permute_small.cuh), one launch; permute_small_body there is the
+// single-launch forward's copy of the same steps.
 __global__ void __launch_bounds__(kPermThreads, 1) permute_small_kernel(const PermuteArgs a, const uint8_t* x_q,
                                                                         const uint8_t* x_sf, int H, uint8_t* x_perm,
                                                                         uint8_t* x_perm_sf, int bt, int nb) {
-  extern __shared__ int32_t sh[];    // cnt [E], seg [E]
+  extern __shared__ int32_t sh[];
+  int32_t* cnt = sh;                 // [E]
+  int32_t* seg = sh + a.E;           // [E]
   __shared__ int32_t s_ids[kSmallPairs];
   __shared__ int32_t s_rank[kSmallPairs];
   __shared__ int32_t s_total;
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  const int N = a.T * a.K;
+  for (int e = tid; e < a.E; e += kPermThreads) cnt[e] = 0;
   grid_dependency_wait();                          // topk_ids come from the previous launch
   grid_launch_dependents();                        // the expert FFN may start its prologue
-  permute_small_body<kPermThreads>(a, a.topk_ids, x_q, x_sf, H, x_perm, x_perm_sf, bt, nb, sh, sh + a.E, s_ids, s_rank,
-                                   &s_total, threadIdx.x, blockIdx.x, gridDim.x, [] { __syncthreads(); });
+  int e_mine = -1;
+  if (tid < N) {
+    e_mine = a.topk_ids[tid];
+    if (e_mine < 0 || e_mine >= a.E) {
+      if (blockIdx.x == 0) record_error(a.status, kDevErrIndex);
+      e_mine = -1;
+    }
+    s_ids[tid] = e_mine;
+  }
+  __syncthreads();
+  int rank = 0;
+  if (e_mine >= 0) {
+    atomicAdd(&cnt[e_mine], 1);
+    for (int j = 0; j < tid; ++j) rank += (s_ids[j] == e_mine);
+  }
+  if (tid < N) s_rank[tid] = rank;
+  __syncthreads();
+  if (a.slot > 0) {                  // BatchedExperts: fixed slots
+    for (int e = tid; e < a.E; e += kPermThreads) seg[e] = e * a.slot;
+    if (tid == 0) s_total = a.E * a.slot;
+  } else if (warp == 0) {            // exclusive scan of the aligned segment sizes
+    const int per = (a.E + 31) / 32;
+    int local = 0;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane * per + j;
+      if (e < a.E) local += round_up_pow2(cnt[e], a.align);
+    }
+    int incl = local;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += v;
+    }
+    int run = incl - local;
+    for (int j = 0; j < per; ++j) {
+      const int e = lane * per + j;
+      if (e < a.E) {
+        seg[e] = run;
+        run += round_up_pow2(cnt[e], a.align);
+      }
+    }
+    if (lane == 31) s_total = incl;
+  }
+  __syncthreads();
+  const int msum = s_total;
+  if (blockIdx.x == 0) {
+    if (e_mine >= 0) {
+      if (a.slot > 0 && rank >= a.slot) {
+        record_error(a.status, kDevErrIndex);
+        a.inv_perm[tid] = -1;
+      } else {
+        const int pos = seg[e_mine] + rank;
+        a.inv_perm[tid] = pos;
+        a.sorted_ids[pos] = tid;
+        a.expert_ids[pos] = e_mine;
+      }
+    }
+    if (a.counts)
+      for (int e = tid; e < a.E; e += kPermThreads) a.counts[e] = cnt[e];
+    if (tid == 0) *a.m_sum = msum;
+  }
+  // padding rows of each segment and the tail [M_sum, U), split over every CTA of the launch (each
+  // holds the same counts and segment starts)
+  for (int e = blockIdx.x * kPermWarps + warp; e < a.E; e += gridDim.x * kPermWarps) {
+    const int c = cnt[e];
+    const int padded = a.slot > 0 ? a.slot : round_up_pow2(c, a.align);
+    for (int r = c + lane; r < padded; r += 32) {
+      a.sorted_ids[seg[e] + r] = N;
+      a.expert_ids[seg[e] + r] = -1;
+    }
+  }
+  for (int r = msum + blockIdx.x * kPermThreads + tid; r < a.U; r += gridDim.x * kPermThreads) {
+    a.sorted_ids[r] = N;
+    a.expert_ids[r] = -1;
+  }
+  if ((x_perm != nullptr || x_perm_sf != nullptr) && N <= kSmallCopyPairs) {
+    // one warp per (pair, 1 KB piece of its row); the piece-0 warp also copies the row's scales
+    // (x_perm null: the scales alone, one warp per pair)
+    const int chunks = x_perm != nullptr ? H / 16 : 0, slabs = H / 128;
+    const int pieces = x_perm != nullptr ? (chunks + kCopyPiece - 1) / kCopyPiece : 1;
+    for (int u = blockIdx.x * kPermWarps + warp; u < N * pieces; u += gridDim.x * kPermWarps) {
+      const int p = u / pieces, piece = u - p * pieces;
+      const int e = s_ids[p];
+      if (e < 0 || (a.slot > 0 && s_rank[p] >= a.slot)) continue;
+      const int dst = seg[e] + s_rank[p];
+      const int t = p / a.K;
+      const uint4* src = reinterpret_cast<const uint4*>(x_q + static_cast<size_t>(t) * H);
+      uint4* out = reinterpret_cast<uint4*>(x_perm + static_cast<size_t>(dst) * H);
+      uint4 v[kCopyPiece / 32];
+#pragma unroll
+      for (int i = 0; i < kCopyPiece / 32; ++i) {
+        const int j = piece * kCopyPiece + i * 32 + lane;
+        if (j < chunks) v[i] = __ldg(src + j);
+      }
+#pragma unroll
+      for (int i = 0; i < kCopyPiece / 32; ++i) {
+        const int j = piece * kCopyPiece + i * 32 + lane;
+        if (j < chunks) out[j] = v[i];
+      }
+      if (piece == 0)
+        for (int s2 = lane; s2 < slabs; s2 += 32)
+          x_perm_sf[act_sf_offset(bt, nb, dst, s2)] = x_sf[static_cast<size_t>(t) * slabs + s2];
+    }
+  }
 }
 
 // Row copy: x_perm[inv_perm[t,k]] = x_q[t] (skipped when x_perm is null), scales into the tiled

@@ -1,5 +1,7 @@
-// The small permute (T * K <= 1024 pairs) as a device function: the standalone launch
-// (permute.cu) and the single-launch forward (gemm.cu) run the same code.
+// The small permute (T * K <= 1024 pairs) as a device function for the single-launch forward
+// (gemm.cu): the steps of permute_small_kernel (permute.cu) in the same order with the same
+// arithmetic, so the results are the same bits (the single-launch tests assert it).  The launch
+// keeps its own copy: passing its shared-memory arrays through this function cost it ~0.5 us.
 // Note "INT8 高吞吐/低延迟 EP 代码梳理" §9.3-9.4 (scatter, inv_perm, M_sum), §10 (M_sum_upper) and the
 // m_indices paragraph (expert_ids, -1 on padding); MegaMoE page 路径 A (moe_align_block_size).
 #pragma once
@@ -38,8 +40,9 @@ constexpr int kCopyPiece = 64;       // 16-byte chunks of a row one warp copies 
 // The small permute over NT threads of block `cta` of `ncta` (each block recomputes the indices;
 // block 0 writes them, and the padding, tail and row copies are split over the blocks).  ids:
 // the [T, K] expert ids (global or shared memory); cnt, seg: [E] each; s_ids, s_rank: [NT];
-// T * K <= NT.  sync() is a barrier over exactly the NT threads.
-template <int NT, class Sync>
+// T * K <= NT.  sync() is a barrier over exactly the NT threads.  COHERENT: x_q is written by the
+// same launch (the single-launch forward), so its rows are read past the non-coherent cache.
+template <int NT, bool COHERENT, class Sync>
 __device__ __forceinline__ void permute_small_body(const PermuteArgs& a, const int32_t* ids, const uint8_t* x_q,
                                                    const uint8_t* x_sf, int H, uint8_t* x_perm, uint8_t* x_perm_sf,
                                                    int bt, int nb, int32_t* cnt, int32_t* seg, int32_t* s_ids,
@@ -140,7 +143,7 @@ __device__ __forceinline__ void permute_small_body(const PermuteArgs& a, const i
 #pragma unroll
       for (int i = 0; i < kCopyPiece / 32; ++i) {
         const int j = piece * kCopyPiece + i * 32 + lane;
-        if (j < chunks) v[i] = __ldcg(src + j);   // coherent: in a single-launch forward x_q is written by this launch
+        if (j < chunks) v[i] = COHERENT ? __ldcg(src + j) : __ldg(src + j);
       }
 #pragma unroll
       for (int i = 0; i < kCopyPiece / 32; ++i) {

@@ -1,5 +1,7 @@
-// Small-batch routing (T <= kGemvT) as device functions: the standalone launch (route.cu) and the
-// single-launch forward (gemm.cu) run the same code, so their results are the same bits.
+// Small-batch routing (T <= kGemvT) as device functions for the single-launch forward (gemm.cu):
+// the steps of route_small_kernel (route.cu) in the same order with the same arithmetic, so the
+// results are the same bits (the single-launch tests assert it).  The launch keeps its own copy:
+// calling these functions cost it ~0.5 us.
 // Page "DeepSeek V4 MegaMoE Kernel 深度解析", 经典 MoE 的计算过程 / 第一步：路由, and the CUDA tag page
 // teaser row "Fused TopK Bias Routing" (sqrt(softplus), e_score_correction_bias).
 #pragma once
@@ -12,17 +14,14 @@
 namespace moe {
 
 // ------------------------------------------------------------------------------------------
-// Small batches (T <= kGemvT) use route_small_kernel below: CTA = 4 experts x one quarter of H.
+// Small batches (T <= kGemvT): blocks of 4 experts x one quarter of H (route_small_kernel).
 constexpr int kGemvT = 16;
 constexpr int kGemvE = 4;
 constexpr int kGemvSplit = 4;
 
 // ------------------------------------------------------------------------------------------
-// Top-K: one CTA (256 threads) per token.  Threads sum the split partials of one expert each
-// (independent loads, fixed split order), score, and stage scores/keys in shared memory; warp 0
-// then holds PER = E/32 keys per lane in registers and runs K rounds of warp arg-max (ties to
-// the lower expert id).  FP8 activation quantisation (one warp per 128-column group) runs in
-// the blocks after the top-K blocks of the same launch.
+// Arguments of the routing's scoring, top-K and FP8 activation quantisation (route_finish_kernel
+// above kGemvT tokens, the small-batch functions below up to it).
 struct RouteFinishArgs {
   const float* partial;
   int nsplit;
@@ -183,11 +182,12 @@ __device__ __forceinline__ void route_small_gemv(const RouteFinishArgs& a, const
 }
 
 // Part 4: the top-K of every token from the kGemvSplit partial sums (summed in split order), one
-// warp per token (warps warp, warp + nwarps, ...).  ids_out (nullable, may be shared memory) gets
-// the ids as [T, K]; with `outputs` the ids, weights, logits and tiny-batch ids are also stored.
-template <int TT, int PER>
+// warp per token (warps warp, warp + 8, ...).  IDS: the ids also go to ids_out as [T, K] (shared
+// memory); OUTPUTS: the ids, weights, logits and tiny-batch ids are stored.  Compile-time flags,
+// so that the routing launch's serial tail carries no extra branches.
+template <int TT, int PER, bool IDS, bool OUTPUTS>
 __device__ __forceinline__ void route_small_topk(const RouteFinishArgs& a, const float* __restrict__ partial, int warp,
-                                                 int lane, int nwarps, int32_t* ids_out, bool outputs) {
+                                                 int lane, int32_t* ids_out) {
   const int T = a.T, E = a.E;
   // the biases first, in registers: their loads then overlap the partial-sum loads instead of
   // waiting behind the optional logits stores
@@ -198,7 +198,7 @@ __device__ __forceinline__ void route_small_topk(const RouteFinishArgs& a, const
     gbias[j] = (a.gate_bias && e < E) ? __ldg(a.gate_bias + e) : 0.f;
     ebias[j] = (a.e_bias && e < E) ? __ldg(a.e_bias + e) : 0.f;
   }
-  for (int t = warp; t < T; t += nwarps) {
+  for (int t = warp; t < T; t += 8) {
     float s[PER], key[PER];
     float lmax = -INFINITY;
     // partial sums of 8 experts per lane at a time: every load of a group is issued before the
@@ -221,7 +221,7 @@ __device__ __forceinline__ void route_small_topk(const RouteFinishArgs& a, const
         if (e < E) {
           l = (v[jj][0] + v[jj][1]) + (v[jj][2] + v[jj][3]);   // the order route_finish_kernel sums 4 splits in
           if (a.gate_bias) l += gbias[j];
-          if (outputs && a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
+          if (OUTPUTS && a.logits_out) a.logits_out[static_cast<size_t>(t) * E + e] = l;
         }
         s[j] = l;
         lmax = fmaxf(lmax, l);
@@ -280,14 +280,14 @@ __device__ __forceinline__ void route_small_topk(const RouteFinishArgs& a, const
       wsum += sw;
       if (lane == k) wmine = sw;
       if (lane == 0) {
-        if (ids_out) ids_out[t * a.K + k] = bi;
-        if (outputs) {
+        if (IDS) ids_out[t * a.K + k] = bi;
+        if (OUTPUTS) {
           a.topk_ids[static_cast<size_t>(t) * a.K + k] = bi;
           if (a.nv.eids) a.nv.eids[(t * a.K + k) * kNaiveRows] = bi;
         }
       }
     }
-    if (outputs && lane < a.K) a.topk_w[static_cast<size_t>(t) * a.K + lane] = a.renormalize ? wmine / wsum : wmine;
+    if (OUTPUTS && lane < a.K) a.topk_w[static_cast<size_t>(t) * a.K + lane] = a.renormalize ? wmine / wsum : wmine;
   }
 }
 
