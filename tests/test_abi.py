@@ -130,6 +130,31 @@ def test_invalid_arguments_are_rejected(M):
     assert M.status_str(M.ERR_TIMEOUT) == "device wait timed out"
 
 
+def test_single_launch_refusals_on_the_host(M):
+    # moe_forward_single_launch validates as moe_forward does, then refuses what its one launch does
+    # not cover (more than 16 tokens, more than 128 (token, slot) pairs, GEMM blocks above 16 rows,
+    # NVFP4) before any device work
+    L = M.lib()
+    fake = ctypes.c_void_p(0x10000)     # never dereferenced
+    ws = ctypes.c_void_p(0x20000)
+    big = 1 << 40
+
+    def call(T, K, align, w13, w2, ws_bytes):
+        return L.moe_forward_single_launch(fake, fake, None, None, T, 512, 256, 16, K, align, 0, 1, w13, w2, fake,
+                                           None, None, None, None, None, None, ws, ws_bytes, None)
+
+    w13 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 512, 2)
+    w2 = M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 256, 1)
+    assert call(8, 4, 16, w13, w2, 1024) == M.ERR_WORKSPACE
+    assert call(17, 4, 16, w13, w2, big) == M.ERR_UNSUPPORTED
+    assert call(16, 9, 16, w13, w2, big) == M.ERR_UNSUPPORTED
+    assert call(8, 4, 32, w13, w2, big) == M.ERR_UNSUPPORTED
+    n13 = M._Weight(0x10000, 0x30000, M.W_NVFP4, 16, 512, 512, 2)
+    n2 = M._Weight(0x10000, 0x30000, M.W_NVFP4, 16, 512, 256, 1)
+    assert call(8, 4, 16, n13, n2, big) == M.ERR_UNSUPPORTED
+    assert call(8, 4, 16, w13, M._Weight(0x10000, None, M.W_MXFP4, 16, 512, 256, 2), big) == M.ERR_INVALID_ARG
+
+
 def test_product_path_does_not_touch_the_oracle():
     # the library and its binding never import, load or call the oracle
     pkg = os.path.join(ROOT, "moe_expert_ffn_sqrt_gb300")
