@@ -278,7 +278,8 @@ moe_status moe_forward(const uint16_t* hidden, const float* w_gate, const float*
  * 1 <= T <= 16, E <= 256, T*K <= 128, align <= 16; other problems return MOE_ERR_UNSUPPORTED
  * (moe_forward covers them).  A barrier wait that runs out is reported as MOE_ERR_TIMEOUT by
  * moe_get_error, with out unspecified.  The calls of one stream must not overlap: the launch
- * starts after the previous one and reuses the workspace's routing scratch. */
+ * starts after the previous one and reuses the workspace's routing scratch.  Like moe_forward it
+ * can be captured into a CUDA graph (a cooperative kernel node). */
 moe_status moe_forward_single_launch(const uint16_t* hidden, const float* w_gate, const float* gate_bias,
                                      const float* e_score_bias, int T, int H, int I, int E, int K,
                                      int align, moe_score_fn fn, int renormalize, moe_weight w13,

@@ -22,7 +22,7 @@ def M():
     return ensure_lib()
 
 
-@pytest.mark.parametrize("case", ["decode", "tiny77", "nvfp4", "naive", "batched_layout"])
+@pytest.mark.parametrize("case", ["decode", "tiny77", "nvfp4", "naive", "batched_layout", "single_launch"])
 def test_forward_graph_replay_matches_eager(M, case):
     if case == "nvfp4":
         w = synth.custom(T=40, H=512, I=256, E=16, K=4, align=16, score_fn="sqrt_softplus", e_bias=True,
@@ -53,8 +53,9 @@ def test_forward_graph_replay_matches_eager(M, case):
                                          w13, w2, out, ws)
     else:
         ws = M.new_workspace(T, w.H, w.I, w.E, w.K, w.align)
+        single = case == "single_launch"     # the whole layer as one cooperative launch
         call = lambda: M.forward(hidden, w_gate, gate_bias, e_bias, w.I, w.K, w.align, w.score_fn, w.renormalize, w13,
-                                 w2, out, ws)
+                                 w2, out, ws, single_launch=single)
     # eager reference outputs, one per input
     eager = []
     for inp in inps:
