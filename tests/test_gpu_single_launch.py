@@ -68,6 +68,10 @@ CASES = {
     "align_1": (synth.custom(T=11, H=512, I=384, E=16, K=4, align=1, score_fn="sqrt_softplus", e_bias=True,
                              seed=23), None),
     "h_384": (synth.custom(T=9, H=384, I=256, E=48, K=3, align=8, score_fn="softmax", seed=24), None),
+    "gate_bias": (synth.custom(T=12, H=1024, I=256, E=128, K=6, align=16, score_fn="sqrt_softplus", e_bias=True,
+                               gate_offset="normal", seed=25), None),
+    "zipf_gate": (synth.custom(T=16, H=512, I=256, E=256, K=8, align=16, score_fn="sqrt_softplus", e_bias=True,
+                               gate_offset="zipf", seed=26), None),
 }
 
 
